@@ -1,0 +1,196 @@
+"""fp64 CPU oracle for the HSTU fused attention forward.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``; the product package never imports
+it. The arithmetic lives in ``hstu_oracle.c`` (plain C, fp64 loops, in the
+operation order of "RecOps Running Case Documentation", Introduction to the
+HSTU_V1 Forward Operator: QK matmul, SiLU, scaling, mask, matmul with V). This
+module only builds that file with gcc and marshals arrays to it.
+
+Inputs are upcast to float64 exactly (every bf16/fp16/fp32 value is a double).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hstu_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+MASK_CAUSAL = 0  # Inputs and Outputs table: "0: built-in lower triangular mask"
+MASK_NONE = 2  # "2: do not use a mask"
+
+
+def build(force: bool = False) -> str:
+    """Compile hstu_oracle.c into liboracle.so beside it (gcc, -O2, pthreads)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
+        )
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+class use_library:
+    """Context manager that points this module at another build of the oracle
+    source (the mutation tests compile deliberately broken copies)."""
+
+    def __init__(self, path):
+        self._path = path
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self._saved = _lib
+        _lib = _bind(ctypes.CDLL(self._path))
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self._saved
+        return False
+
+
+def _bind(lib):
+    d = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.POINTER(ctypes.c_int64)
+    c64 = ctypes.c_int64
+    lib.hstu_oracle_valid.restype = ctypes.c_int
+    lib.hstu_oracle_valid.argtypes = [c64, c64, c64, ctypes.c_int, c64, c64, c64]
+    lib.hstu_oracle_fwd.restype = ctypes.c_int
+    lib.hstu_oracle_fwd.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, i64, i64,
+                                    ctypes.c_int, c64, ctypes.c_double, ctypes.c_double,
+                                    d, ctypes.c_int]
+    lib.hstu_oracle_fwd_rows.restype = ctypes.c_int
+    lib.hstu_oracle_fwd_rows.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, i64,
+                                         i64, ctypes.c_int, c64, ctypes.c_double,
+                                         ctypes.c_double, i64, c64, d, ctypes.c_int]
+    lib.hstu_oracle_count_valid.restype = ctypes.c_int64
+    lib.hstu_oracle_count_valid.argtypes = [i64, c64, c64, i64, i64, ctypes.c_int, c64]
+    return lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: exact upcast on the CPU
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i64(x):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int64))
+
+
+def _p(a, ty):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(ty))
+
+
+def _common(q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    so = _i64(seq_offsets)
+    if q.ndim != 3 or k.ndim != 3 or v.shape != k.shape or q.shape[2] != k.shape[2]:
+        raise ValueError("q [T, Nq, D], k/v [T, Nk, D] expected")
+    B = so.shape[0] - 1
+    nc, nt = _i64(num_context), _i64(num_targets)
+    rab = _f64(rab)
+    if rab is not None:
+        if max_seqlen is None:
+            raise ValueError("max_seqlen is required with rab")
+        if rab.shape != (B, q.shape[1], max_seqlen, max_seqlen):
+            raise ValueError(f"rab must be [B, Nq, S, S], got {rab.shape}")
+    return q, k, v, so, B, rab, nc, nt
+
+
+def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=None,
+             mask_type=MASK_CAUSAL, target_group_size=0, alpha=1.0, silu_scale=None,
+             max_seqlen=None, nthreads=1):
+    """Whole forward in fp64. Returns out [T, Nq, D] as float64 (rows outside
+    every sequence are 0). silu_scale defaults to 1/max_seqlen (Inputs and
+    Outputs table, silu_scale)."""
+    q, k, v, so, B, rab, nc, nt = _common(q, k, v, seq_offsets, rab, num_context,
+                                          num_targets, max_seqlen)
+    if max_seqlen is None:
+        max_seqlen = int(np.max(np.diff(so))) if B > 0 else 1
+    if silu_scale is None:
+        silu_scale = 1.0 / max_seqlen
+    out = np.zeros(q.shape, dtype=np.float64)
+    rc = _load().hstu_oracle_fwd(_p(q, ctypes.c_double), _p(k, ctypes.c_double),
+                                 _p(v, ctypes.c_double), _p(so, ctypes.c_int64), B, q.shape[1],
+                                 k.shape[1], q.shape[2], _p(rab, ctypes.c_double), max_seqlen,
+                                 _p(nc, ctypes.c_int64), _p(nt, ctypes.c_int64), mask_type,
+                                 target_group_size, float(alpha), float(silu_scale),
+                                 _p(out, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
+
+
+def hstu_fwd_rows(q, k, v, seq_offsets, rows, *, rab=None, num_context=None, num_targets=None,
+                  mask_type=MASK_CAUSAL, target_group_size=0, alpha=1.0, silu_scale=None,
+                  max_seqlen=None, nthreads=1):
+    """Selected output rows: rows is an int array [n, 3] of (b, h, i) (i local to
+    sequence b). Returns [n, D] float64, row r = out[seq_offsets[b] + i, h, :]."""
+    q, k, v, so, B, rab, nc, nt = _common(q, k, v, seq_offsets, rab, num_context,
+                                          num_targets, max_seqlen)
+    if max_seqlen is None:
+        max_seqlen = int(np.max(np.diff(so))) if B > 0 else 1
+    if silu_scale is None:
+        silu_scale = 1.0 / max_seqlen
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    out = np.zeros((rows.shape[0], q.shape[2]), dtype=np.float64)
+    rc = _load().hstu_oracle_fwd_rows(_p(q, ctypes.c_double), _p(k, ctypes.c_double),
+                                      _p(v, ctypes.c_double), _p(so, ctypes.c_int64), B,
+                                      q.shape[1], k.shape[1], q.shape[2],
+                                      _p(rab, ctypes.c_double), max_seqlen,
+                                      _p(nc, ctypes.c_int64), _p(nt, ctypes.c_int64), mask_type,
+                                      target_group_size, float(alpha), float(silu_scale),
+                                      _p(rows, ctypes.c_int64), rows.shape[0],
+                                      _p(out, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out
+
+
+def valid(i, j, L, mask_type=MASK_CAUSAL, num_context=0, num_targets=0, target_group_size=0):
+    """The oracle's mask predicate for one pair (0 or 1)."""
+    return _load().hstu_oracle_valid(i, j, L, mask_type, num_context, num_targets,
+                                     target_group_size)
+
+
+def mask_matrix(L, mask_type=MASK_CAUSAL, num_context=0, num_targets=0, target_group_size=0):
+    """[L, L] 0/1 matrix of the oracle's predicate (small L only)."""
+    return np.array([[valid(i, j, L, mask_type, num_context, num_targets, target_group_size)
+                      for j in range(L)] for i in range(L)], dtype=np.int64)
+
+
+def count_valid(seq_offsets, num_heads_q, *, num_context=None, num_targets=None,
+                mask_type=MASK_CAUSAL, target_group_size=0):
+    """Sum over sequences of Nq * #valid(i, j): the mask-aware pair count."""
+    so = _i64(seq_offsets)
+    nc, nt = _i64(num_context), _i64(num_targets)
+    return int(_load().hstu_oracle_count_valid(_p(so, ctypes.c_int64), so.shape[0] - 1,
+                                               num_heads_q, _p(nc, ctypes.c_int64),
+                                               _p(nt, ctypes.c_int64), mask_type,
+                                               target_group_size))

@@ -1,0 +1,232 @@
+/*
+ * HSTU fused attention forward: plain fp64 CPU oracle.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the checker, not the product: only the
+ * tests, the smoke check and the benchmark's CPU-baseline leg load it. It shares
+ * no code, header or constant with the CUDA library.
+ *
+ * Source: "RecOps Running Case Documentation" (gitcode.com/Ascend/RecSDK,
+ * docs/en/rec_ops/hstu_v1_forward.md).
+ *   - Introduction to the HSTU_V1 Forward Operator: the operator chains, in this
+ *     order, the QK matrix multiplication, the SiLU activation, the scaling, the
+ *     mask application and the multiplication with V.
+ *   - Feature table, "Attention mechanism": S = Q*K^T, P = silu(S), O = P*V.
+ *   - Feature table, "GQA": several query heads share one key/value head.
+ *   - Feature table, "Relative attention bias": optional rab [b, n, s, s].
+ *   - Feature table, "Support causal mask": built from num_context, num_targets
+ *     and target_group_size, any of which may be absent.
+ *   - Inputs and Outputs table: jagged [s_b, N, D] layout with seq_offsets [B+1];
+ *     mask_type 0 = built-in lower-triangular (causal) mask, 2 = no mask;
+ *     silu_scale defaults to 1/max_seq_len; target_group_size 0 = no target
+ *     mask; alpha = "alpha scaling parameter".
+ *
+ * Readings taken where the page is silent (each also listed in the design notes):
+ *   - alpha multiplies Q*K^T only; rab is added after it, before SiLU.
+ *   - rab is indexed by local positions: rab[b, h, i, j], row stride max_seqlen.
+ *   - GQA head map: kv head = h / (Nq / Nk) (contiguous groups).
+ *   - Causal mask with H = (g > 0) ? max(L - nt, 0) : L (history length):
+ *       valid(i, j) = (j <= i && j < H)                       causal over history
+ *                  || (i < nc && j < H)                       context rows see all history
+ *                  || (g > 0 && i >= H && j >= H && j <= i
+ *                      && (i - H) / g == (j - H) / g)         targets: own group, causal
+ *                  || (g == 0 && j <= i)                      no target mask: plain causal
+ *   - A masked entry of P is exactly 0 (select, not multiply).
+ *
+ * Pinned by tests/test_oracle_pins.py: closed forms (L = 1, silu(ln 3) = 0.75 ln 3,
+ * silu(x) - silu(-x) = x), the dense equal-length case against torch.matmul and
+ * torch.nn.functional.silu in fp64, hand-written 0/1 mask matrices, and the
+ * invariants (Q = 0 gives 0, causal locality, GQA = replicated MHA, batch
+ * permutation, V = ones). The alpha/rab positions and the mask semantics are
+ * readings of a silent page: parity of those readings is unpinned by the page.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_MASK_CAUSAL 0 /* "0: built-in lower triangular mask" */
+#define ORACLE_MASK_NONE 2   /* "2: do not use a mask" */
+
+/* The mask predicate (reading above). Returns 1 when query row i may attend key j. */
+int hstu_oracle_valid(int64_t i, int64_t j, int64_t L, int mask_type, int64_t nc,
+                      int64_t nt, int64_t g) {
+  if (i < 0 || j < 0 || i >= L || j >= L) return 0;
+  if (mask_type == ORACLE_MASK_NONE) return 1;
+  int64_t H = L;
+  if (g > 0) {
+    H = L - nt;
+    if (H < 0) H = 0;
+  }
+  if (j <= i && j < H) return 1;
+  if (i < nc && j < H) return 1;
+  if (g > 0 && i >= H && j >= H && j <= i && (i - H) / g == (j - H) / g) return 1;
+  if (g == 0 && j <= i) return 1;
+  return 0;
+}
+
+/* silu(x) = x * sigmoid(x) = x / (1 + exp(-x)). */
+static double silu(double x) { return x / (1.0 + exp(-x)); }
+
+typedef struct {
+  const double *q, *k, *v, *rab;
+  const int64_t *seq_offsets, *num_context, *num_targets;
+  int64_t B, Nq, Nk, D, max_seqlen;
+  int mask_type;
+  int64_t g;
+  double alpha, silu_scale;
+  double *out;
+  /* row mode: rows[3*r + {0,1,2}] = (b, h, i); out_rows is [nrows, D] */
+  const int64_t *rows;
+  int64_t nrows;
+  double *out_rows;
+  int64_t next; /* work counter, taken with an atomic add */
+} job_t;
+
+/* One output row: out[t0 + i, h, :] for sequence b, query head h, local row i. */
+static void one_row(const job_t *J, int64_t b, int64_t h, int64_t i, double *o) {
+  const int64_t t0 = J->seq_offsets[b];
+  const int64_t L = J->seq_offsets[b + 1] - t0;
+  const int64_t D = J->D;
+  const int64_t G = J->Nq / J->Nk;
+  const int64_t hk = h / G;
+  const int64_t nc = J->num_context ? J->num_context[b] : 0;
+  const int64_t nt = J->num_targets ? J->num_targets[b] : 0;
+  const double *qi = J->q + ((t0 + i) * J->Nq + h) * D;
+  for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+  for (int64_t j = 0; j < L; ++j) {
+    const double *kj = J->k + ((t0 + j) * J->Nk + hk) * D;
+    const double *vj = J->v + ((t0 + j) * J->Nk + hk) * D;
+    /* 1. QK matrix multiplication */
+    double s = 0.0;
+    for (int64_t d = 0; d < D; ++d) s += qi[d] * kj[d];
+    /* alpha on Q*K^T, then the relative attention bias */
+    double x = J->alpha * s;
+    if (J->rab) x += J->rab[((b * J->Nq + h) * J->max_seqlen + i) * J->max_seqlen + j];
+    /* 2. SiLU activation */
+    double p = silu(x);
+    /* 3. scaling */
+    p *= J->silu_scale;
+    /* 4. mask application */
+    if (!hstu_oracle_valid(i, j, L, J->mask_type, nc, nt, J->g)) p = 0.0;
+    /* 5. matrix multiplication with V */
+    for (int64_t d = 0; d < D; ++d) o[d] += p * vj[d];
+  }
+}
+
+static void *worker_units(void *arg) {
+  job_t *J = (job_t *)arg;
+  const int64_t units = J->B * J->Nq;
+  for (;;) {
+    int64_t u = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+    if (u >= units) break;
+    const int64_t b = u / J->Nq, h = u % J->Nq;
+    const int64_t t0 = J->seq_offsets[b];
+    const int64_t L = J->seq_offsets[b + 1] - t0;
+    for (int64_t i = 0; i < L; ++i) one_row(J, b, h, i, J->out + ((t0 + i) * J->Nq + h) * J->D);
+  }
+  return NULL;
+}
+
+static void *worker_rows(void *arg) {
+  job_t *J = (job_t *)arg;
+  for (;;) {
+    int64_t r = __atomic_fetch_add(&J->next, 1, __ATOMIC_RELAXED);
+    if (r >= J->nrows) break;
+    one_row(J, J->rows[3 * r], J->rows[3 * r + 1], J->rows[3 * r + 2], J->out_rows + r * J->D);
+  }
+  return NULL;
+}
+
+static int run_pool(job_t *J, void *(*fn)(void *), int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads == 1) {
+    fn(J);
+    return 0;
+  }
+  pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!th) return -1;
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    if (pthread_create(&th[t], NULL, fn, J) != 0) break;
+    ++started;
+  }
+  if (started == 0) fn(J);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  free(th);
+  return 0;
+}
+
+static int check_args(int64_t B, int64_t Nq, int64_t Nk, int64_t D, int mask_type) {
+  if (B < 0 || Nq <= 0 || Nk <= 0 || D <= 0) return -1;
+  if (Nq % Nk != 0) return -1;
+  if (mask_type != ORACLE_MASK_CAUSAL && mask_type != ORACLE_MASK_NONE) return -1;
+  return 0;
+}
+
+/*
+ * Whole forward. q [T, Nq, D], k/v [T, Nk, D], rab [B, Nq, S, S] or NULL,
+ * seq_offsets [B+1], num_context/num_targets [B] or NULL; out [T, Nq, D].
+ * Rows of out outside every sequence are left untouched. Returns 0 or -1.
+ */
+int hstu_oracle_fwd(const double *q, const double *k, const double *v,
+                    const int64_t *seq_offsets, int64_t B, int64_t Nq, int64_t Nk,
+                    int64_t D, const double *rab, int64_t max_seqlen,
+                    const int64_t *num_context, const int64_t *num_targets,
+                    int mask_type, int64_t target_group_size, double alpha,
+                    double silu_scale, double *out, int nthreads) {
+  if (check_args(B, Nq, Nk, D, mask_type)) return -1;
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.q = q; J.k = k; J.v = v; J.rab = rab;
+  J.seq_offsets = seq_offsets; J.num_context = num_context; J.num_targets = num_targets;
+  J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen;
+  J.mask_type = mask_type; J.g = target_group_size;
+  J.alpha = alpha; J.silu_scale = silu_scale; J.out = out;
+  return run_pool(&J, worker_units, nthreads);
+}
+
+/* Selected rows only: rows[3r..3r+2] = (b, h, i); out_rows [nrows, D]. */
+int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
+                         const int64_t *seq_offsets, int64_t B, int64_t Nq, int64_t Nk,
+                         int64_t D, const double *rab, int64_t max_seqlen,
+                         const int64_t *num_context, const int64_t *num_targets,
+                         int mask_type, int64_t target_group_size, double alpha,
+                         double silu_scale, const int64_t *rows, int64_t nrows,
+                         double *out_rows, int nthreads) {
+  if (check_args(B, Nq, Nk, D, mask_type)) return -1;
+  for (int64_t r = 0; r < nrows; ++r) {
+    const int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+    if (b < 0 || b >= B || h < 0 || h >= Nq || i < 0 ||
+        i >= seq_offsets[b + 1] - seq_offsets[b])
+      return -1;
+  }
+  job_t J;
+  memset(&J, 0, sizeof(J));
+  J.q = q; J.k = k; J.v = v; J.rab = rab;
+  J.seq_offsets = seq_offsets; J.num_context = num_context; J.num_targets = num_targets;
+  J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen;
+  J.mask_type = mask_type; J.g = target_group_size;
+  J.alpha = alpha; J.silu_scale = silu_scale;
+  J.rows = rows; J.nrows = nrows; J.out_rows = out_rows;
+  return run_pool(&J, worker_rows, nthreads);
+}
+
+/* Number of (query head, i, j) triples with valid(i, j): sum over b of Nq * #valid. */
+int64_t hstu_oracle_count_valid(const int64_t *seq_offsets, int64_t B, int64_t Nq,
+                                const int64_t *num_context, const int64_t *num_targets,
+                                int mask_type, int64_t target_group_size) {
+  int64_t total = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t L = seq_offsets[b + 1] - seq_offsets[b];
+    const int64_t nc = num_context ? num_context[b] : 0;
+    const int64_t nt = num_targets ? num_targets[b] : 0;
+    int64_t c = 0;
+    for (int64_t i = 0; i < L; ++i)
+      for (int64_t j = 0; j < L; ++j)
+        c += hstu_oracle_valid(i, j, L, mask_type, nc, nt, target_group_size);
+    total += c * Nq;
+  }
+  return total;
+}

@@ -1,0 +1,304 @@
+"""Pins for the fp64 CPU oracle: closed forms, library special cases, hand-written
+mask matrices and invariants of the definition. CPU only.
+
+Source for every pin: "RecOps Running Case Documentation"
+(gitcode.com/Ascend/RecSDK, docs/en/rec_ops/hstu_v1_forward.md), feature table
+(attention mechanism S = Q*K^T, P = silu(S), O = P*V; MHA/GQA; jagged layout;
+rab; causal mask from num_context / num_targets / target_group_size) and the
+Inputs and Outputs table (mask_type codes, silu_scale default, alpha).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _jagged(rng, lengths, nq, nk, d, scale=1.0):
+    so = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    t = int(so[-1])
+    q = rng.standard_normal((t, nq, d)) * scale
+    k = rng.standard_normal((t, nk, d)) * scale
+    v = rng.standard_normal((t, nk, d))
+    return q, k, v, so
+
+
+# --------------------------------------------------------------------------- closed forms
+def test_single_token_closed_forms():
+    """L = 1: out = silu_scale * silu(alpha * q.k + rab) * v, at x = +-ln 3 and 0."""
+    with open(os.path.join(GOLDEN, "closed_forms.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        d = len(c["q"])
+        q = np.array(c["q"]).reshape(1, 1, d)
+        k = np.array(c["k"]).reshape(1, 1, d)
+        v = np.array(c["v"]).reshape(1, 1, d)
+        so = np.array([0, 1])
+        rab = None if c["rab"] is None else np.full((1, 1, 1, 1), c["rab"])
+        out = oracle.hstu_fwd(q, k, v, so, rab=rab, mask_type=oracle.MASK_CAUSAL,
+                              alpha=c["alpha"], silu_scale=c["silu_scale"], max_seqlen=1)
+        np.testing.assert_allclose(out.reshape(-1), c["expected"], rtol=0, atol=1e-12,
+                                   err_msg=c["name"])
+
+
+def test_silu_odd_part_identity():
+    """silu(x) - silu(-x) = x for every x: with Q = 0 and a random rab, the outputs
+    for +rab and -rab differ by silu_scale * sum_j valid * rab_ij * v_j."""
+    rng = _rng(11)
+    lengths = [5, 3]
+    q, k, v, so = _jagged(rng, lengths, 2, 1, 3)
+    q[:] = 0.0
+    S = max(lengths)
+    rab = rng.standard_normal((2, 2, S, S)) * 3.0
+    kw = dict(mask_type=oracle.MASK_CAUSAL, num_context=[1, 0], num_targets=[2, 1],
+              target_group_size=1, alpha=0.7, silu_scale=0.25, max_seqlen=S)
+    a = oracle.hstu_fwd(q, k, v, so, rab=rab, **kw)
+    b = oracle.hstu_fwd(q, k, v, so, rab=-rab, **kw)
+    expect = np.zeros_like(a)
+    for bi, L in enumerate(lengths):
+        t0 = so[bi]
+        m = oracle.mask_matrix(L, oracle.MASK_CAUSAL, [1, 0][bi], [2, 1][bi], 1)
+        for h in range(2):
+            expect[t0:t0 + L, h] = 0.25 * (m * rab[bi, h, :L, :L]) @ v[t0:t0 + L, 0]
+    np.testing.assert_allclose(a - b, expect, rtol=0, atol=1e-12)
+
+
+def test_q_zero_with_rab_closed_form():
+    """Q = 0: x_ij = rab_ij, so out_i = silu_scale * sum_j valid * silu(rab_ij) * v_j,
+    with silu from torch (library)."""
+    rng = _rng(12)
+    lengths = [4, 6]
+    q, k, v, so = _jagged(rng, lengths, 1, 1, 2)
+    q[:] = 0.0
+    S = 6
+    rab = rng.standard_normal((2, 1, S, S))
+    out = oracle.hstu_fwd(q, k, v, so, rab=rab, mask_type=oracle.MASK_NONE, alpha=3.0,
+                          silu_scale=0.5, max_seqlen=S)
+    for bi, L in enumerate(lengths):
+        t0 = so[bi]
+        p = F.silu(torch.from_numpy(rab[bi, 0, :L, :L])).numpy()
+        np.testing.assert_allclose(out[t0:t0 + L, 0], 0.5 * p @ v[t0:t0 + L, 0], rtol=0,
+                                   atol=1e-12)
+
+
+# --------------------------------------------------------------------------- library cases
+def _torch_dense(q, k, v, rab, alpha, scale, causal):
+    """Equal-length, no-context/no-target case with torch fp64 library ops.
+    q [B, L, Nq, D]; k, v [B, L, Nk, D]; rab [B, Nq, L, L] or None."""
+    G = q.shape[2] // k.shape[2]
+    qt = torch.from_numpy(q).permute(0, 2, 1, 3)
+    kt = torch.from_numpy(k).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    vt = torch.from_numpy(v).repeat_interleave(G, dim=2).permute(0, 2, 1, 3)
+    x = alpha * torch.matmul(qt, kt.transpose(-1, -2))
+    if rab is not None:
+        x = x + torch.from_numpy(rab)
+    p = F.silu(x) * scale
+    if causal:
+        p = p * torch.tril(torch.ones(x.shape[-2:], dtype=torch.float64))
+    return torch.matmul(p, vt).permute(0, 2, 1, 3).numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nk", [(4, 4), (4, 2), (6, 1)])
+def test_equal_lengths_match_torch_matmul(causal, nq, nk):
+    rng = _rng(13 + nq + nk + int(causal))
+    B, L, D = 3, 7, 5
+    q = rng.standard_normal((B, L, nq, D))
+    k = rng.standard_normal((B, L, nk, D))
+    v = rng.standard_normal((B, L, nk, D))
+    rab = rng.standard_normal((B, nq, L, L))
+    so = np.arange(B + 1) * L
+    out = oracle.hstu_fwd(q.reshape(B * L, nq, D), k.reshape(B * L, nk, D),
+                          v.reshape(B * L, nk, D), so, rab=rab,
+                          mask_type=oracle.MASK_CAUSAL if causal else oracle.MASK_NONE,
+                          alpha=0.37, silu_scale=1.0 / L, max_seqlen=L)
+    ref = _torch_dense(q, k, v, rab, 0.37, 1.0 / L, causal)
+    np.testing.assert_allclose(out.reshape(B, L, nq, D), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_jagged_lengths_match_torch_per_sequence():
+    """Ragged lengths, rab with max_seqlen > L: each sequence reads the top-left
+    [L, L] block of its rab slice."""
+    rng = _rng(14)
+    lengths = [3, 9, 1, 6]
+    S = 10
+    q, k, v, so = _jagged(rng, lengths, 2, 2, 4)
+    rab = rng.standard_normal((4, 2, S, S))
+    out = oracle.hstu_fwd(q, k, v, so, rab=rab, mask_type=oracle.MASK_CAUSAL, alpha=0.5,
+                          silu_scale=1.0 / S, max_seqlen=S)
+    for bi, L in enumerate(lengths):
+        t0 = so[bi]
+        ref = _torch_dense(q[None, t0:t0 + L], k[None, t0:t0 + L], v[None, t0:t0 + L],
+                           rab[bi:bi + 1, :, :L, :L], 0.5, 1.0 / S, True)
+        np.testing.assert_allclose(out[t0:t0 + L], ref[0], rtol=1e-12, atol=1e-12)
+
+
+def test_silu_scale_default_is_one_over_max_seqlen():
+    rng = _rng(15)
+    q, k, v, so = _jagged(rng, [4, 2], 1, 1, 3)
+    a = oracle.hstu_fwd(q, k, v, so, max_seqlen=8)
+    b = oracle.hstu_fwd(q, k, v, so, max_seqlen=8, silu_scale=0.125)
+    np.testing.assert_array_equal(a, b)
+
+
+# --------------------------------------------------------------------------- mask matrices
+def _cases():
+    with open(os.path.join(GOLDEN, "mask_cases.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: c["name"])
+def test_mask_matrices_through_forward(case):
+    """Q = 0, rab = ln 3, V = identity (D = L): out[i, j] = scale * 0.75 ln3 * valid(i, j),
+    so the forward itself must reproduce the hand-written 0/1 matrix."""
+    L = case["L"]
+    want = np.array([[int(ch) for ch in row] for row in case["matrix"]])
+    q = np.zeros((L, 1, L))
+    k = _rng(16).standard_normal((L, 1, L))
+    v = np.eye(L).reshape(L, 1, L)
+    rab = np.full((1, 1, L, L), math.log(3.0))
+    out = oracle.hstu_fwd(q, k, v, [0, L], rab=rab, num_context=[case["nc"]],
+                          num_targets=[case["nt"]], mask_type=case["mask_type"],
+                          target_group_size=case["g"], alpha=1.0, silu_scale=0.5, max_seqlen=L)
+    got = out[:, 0, :] / (0.5 * 0.75 * math.log(3.0))
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+    m = oracle.mask_matrix(L, case["mask_type"], case["nc"], case["nt"], case["g"])
+    np.testing.assert_array_equal(m, want)
+
+
+def test_count_valid_closed_forms():
+    so = [0, 5, 12, 13]
+    assert oracle.count_valid(so, 3, mask_type=oracle.MASK_NONE) == 3 * (25 + 49 + 1)
+    assert oracle.count_valid(so, 3) == 3 * (15 + 28 + 1)
+    nc, nt = [1, 2, 0], [2, 3, 1]
+    want = sum(3 * int(oracle.mask_matrix(L, 0, c, t, 2).sum())
+               for L, c, t in zip([5, 7, 1], nc, nt))
+    assert oracle.count_valid(so, 3, num_context=nc, num_targets=nt, target_group_size=2) == want
+
+
+# --------------------------------------------------------------------------- invariants
+def test_q_zero_without_rab_gives_zero():
+    """silu(0) = 0, so Q = 0 and no rab give O = 0 for every mask."""
+    rng = _rng(17)
+    q, k, v, so = _jagged(rng, [6, 3], 4, 2, 8)
+    q[:] = 0.0
+    for mt in (oracle.MASK_CAUSAL, oracle.MASK_NONE):
+        out = oracle.hstu_fwd(q, k, v, so, mask_type=mt, num_context=[2, 1],
+                              num_targets=[2, 1], target_group_size=1, alpha=1.0,
+                              silu_scale=1.0)
+        assert np.all(out == 0.0)
+
+
+def test_causal_rows_ignore_later_keys():
+    """For rows i >= num_context, perturbing K/V rows j > i leaves row i unchanged."""
+    rng = _rng(18)
+    lengths = [9, 7]
+    q, k, v, so = _jagged(rng, lengths, 2, 1, 4)
+    kw = dict(mask_type=oracle.MASK_CAUSAL, num_context=[2, 1], num_targets=[3, 2],
+              target_group_size=2, alpha=0.6, silu_scale=0.2)
+    base = oracle.hstu_fwd(q, k, v, so, **kw)
+    for bi, L in enumerate(lengths):
+        nc = kw["num_context"][bi]
+        for i in range(nc, L):
+            k2, v2 = k.copy(), v.copy()
+            t0 = so[bi]
+            k2[t0 + i + 1:t0 + L] += 5.0
+            v2[t0 + i + 1:t0 + L] -= 3.0
+            pert = oracle.hstu_fwd(q, k2, v2, so, **kw)
+            np.testing.assert_array_equal(pert[t0 + i], base[t0 + i])
+
+
+def test_gqa_equals_replicated_mha():
+    rng = _rng(19)
+    q, k, v, so = _jagged(rng, [5, 8], 6, 2, 4)
+    kw = dict(mask_type=oracle.MASK_CAUSAL, num_context=[1, 3], num_targets=[2, 2],
+              target_group_size=1, alpha=0.3, silu_scale=0.1)
+    gqa = oracle.hstu_fwd(q, k, v, so, **kw)
+    mha = oracle.hstu_fwd(q, np.repeat(k, 3, axis=1), np.repeat(v, 3, axis=1), so, **kw)
+    np.testing.assert_array_equal(gqa, mha)
+
+
+def test_batch_permutation_permutes_outputs():
+    rng = _rng(20)
+    lengths = [4, 7, 2]
+    q, k, v, so = _jagged(rng, lengths, 2, 2, 3)
+    S = 8
+    rab = rng.standard_normal((3, 2, S, S))
+    nc, nt = np.array([1, 2, 0]), np.array([1, 3, 1])
+    kw = dict(mask_type=oracle.MASK_CAUSAL, target_group_size=2, alpha=0.4, silu_scale=0.3,
+              max_seqlen=S)
+    out = oracle.hstu_fwd(q, k, v, so, rab=rab, num_context=nc, num_targets=nt, **kw)
+    perm = [2, 0, 1]
+    seg = lambda a, b: a[so[b]:so[b + 1]]
+    q2 = np.concatenate([seg(q, b) for b in perm])
+    k2 = np.concatenate([seg(k, b) for b in perm])
+    v2 = np.concatenate([seg(v, b) for b in perm])
+    so2 = np.concatenate([[0], np.cumsum([lengths[b] for b in perm])])
+    out2 = oracle.hstu_fwd(q2, k2, v2, so2, rab=rab[perm], num_context=nc[perm],
+                           num_targets=nt[perm], **kw)
+    np.testing.assert_array_equal(out2, np.concatenate([seg(out, b) for b in perm]))
+
+
+def test_v_ones_gives_equal_columns():
+    """V = ones: every output column equals the masked row sum of scale*silu(x)."""
+    rng = _rng(21)
+    q, k, v, so = _jagged(rng, [6, 5], 2, 1, 4)
+    kw = dict(mask_type=oracle.MASK_CAUSAL, num_context=[1, 0], num_targets=[2, 2],
+              target_group_size=1, alpha=0.9, silu_scale=0.5)
+    out = oracle.hstu_fwd(q, k, np.ones_like(v), so, **kw)
+    np.testing.assert_array_equal(out, np.repeat(out[:, :, :1], 4, axis=2))
+    # V = e_0 (first column ones, others zero) gives that row sum in column 0 only
+    e0 = np.zeros_like(v)
+    e0[:, :, 0] = 1.0
+    one = oracle.hstu_fwd(q, k, e0, so, **kw)
+    np.testing.assert_array_equal(one[:, :, 0], out[:, :, 0])
+    assert np.all(one[:, :, 1:] == 0.0)
+
+
+def test_linear_in_silu_scale_and_v():
+    rng = _rng(22)
+    q, k, v, so = _jagged(rng, [7], 1, 1, 3)
+    a = oracle.hstu_fwd(q, k, v, so, alpha=0.5, silu_scale=0.25)
+    b = oracle.hstu_fwd(q, k, v, so, alpha=0.5, silu_scale=0.5)
+    np.testing.assert_array_equal(2.0 * a, b)
+    c = oracle.hstu_fwd(q, k, 4.0 * v, so, alpha=0.5, silu_scale=0.25)
+    np.testing.assert_array_equal(4.0 * a, c)
+
+
+def test_rows_api_matches_full_forward():
+    rng = _rng(23)
+    lengths = [5, 9]
+    q, k, v, so = _jagged(rng, lengths, 4, 2, 6)
+    kw = dict(mask_type=oracle.MASK_CAUSAL, num_context=[2, 0], num_targets=[1, 4],
+              target_group_size=2, alpha=0.2, silu_scale=0.1, max_seqlen=9)
+    full = oracle.hstu_fwd(q, k, v, so, **kw)
+    rows = [(0, 0, 0), (0, 3, 4), (1, 1, 8), (1, 2, 3)]
+    got = oracle.hstu_fwd_rows(q, k, v, so, rows, nthreads=2, **kw)
+    for r, (b, h, i) in enumerate(rows):
+        np.testing.assert_array_equal(got[r], full[so[b] + i, h])
+
+
+def test_threads_do_not_change_results():
+    rng = _rng(24)
+    q, k, v, so = _jagged(rng, [9, 4, 6], 4, 4, 5)
+    a = oracle.hstu_fwd(q, k, v, so, alpha=0.3, silu_scale=0.2, nthreads=1)
+    b = oracle.hstu_fwd(q, k, v, so, alpha=0.3, silu_scale=0.2, nthreads=4)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_rejects_bad_head_ratio():
+    rng = _rng(25)
+    q, k, v, so = _jagged(rng, [3], 3, 2, 2)
+    with pytest.raises(ValueError):
+        oracle.hstu_fwd(q, k, v, so)
