@@ -1,0 +1,367 @@
+"""Benchmark of the HSTU fused attention forward on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one forward (work-list build + tensor-core kernel) over one batch of
+the workload: by default bf16, causal, batch 32, jagged lengths U[256, 2048]
+(max_seqlen 2048), 4 heads, head_dim 128, no rab. The metric is mask-aware useful
+TFLOP/s = 4 * D * (valid (head, i, j) pairs) / time. Inputs are resident in HBM;
+the timed steps rotate through input sets whose total exceeds L2 so no step
+reads its inputs from the previous step's L2. Prints one JSON line (rank 0).
+
+With N > 1 (torchrun) every rank runs its own full replica of the workload (the
+forward has no exchange step); value = all ranks' work / max time over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores over a bounded
+sample of the same workload (the only reference this operator has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            m = json.load(f)
+        return dict(bf16=float(m.get("bf16_tflops")), hbm=float(m.get("hbm_gbs")),
+                    bf16_sustained=float(m.get("bf16_tflops_sustained", m.get("bf16_tflops"))),
+                    source="measured")
+    return dict(bf16=1900.0, hbm=6800.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or self.tmp is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.tmp.flush()
+        with open(self.tmp.name) as f:
+            rows = [r.strip().split(", ") for r in f if r.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _workload(name):
+    from hstu_dense_forward_gb300 import workloads as W
+    return W.WORKLOADS[name]
+
+
+def _algorithmic_bytes(w, inp, pairs_per_head):
+    """Q, K, V read once, O written once, rab entries at valid pairs (2 bytes each)."""
+    el = torch.finfo(w.torch_dtype).bits // 8
+    T = int(inp["seq_offsets"][-1])
+    qo = 2 * T * w.num_heads_q * w.head_dim * el
+    kv = 2 * T * w.num_heads_kv * w.head_dim * el
+    rab = pairs_per_head * el if w.rab else 0
+    return qo + kv + rab
+
+
+def run_ours(args):
+    import numpy as np  # noqa: F401
+
+    from hstu_dense_forward_gb300 import build as B
+    from hstu_dense_forward_gb300 import count_pairs, hstu_fwd, useful_flops
+    from hstu_dense_forward_gb300 import workloads as W
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        B.build()
+    if ws > 1:
+        dist.barrier()
+    w = _workload(args.workload)
+    inp = W.generate(w)
+    pairs = count_pairs(inp["seq_offsets"], w.num_heads_q, max_seqlen=w.max_seqlen,
+                        num_context=inp["num_context"], num_targets=inp["num_targets"],
+                        causal=w.causal, target_group_size=w.target_group_size)
+    flops = useful_flops(pairs, w.head_dim)
+    set_bytes = sum(t.numel() * t.element_size() for t in
+                    (inp["q"], inp["k"], inp["v"], inp["rab"]) if t is not None) * 2  # + out
+    nsets = max(3, -(-3 * L2_BYTES // max(set_bytes, 1)))
+    nsets = min(nsets, 8)
+    sets = []
+    for s in range(nsets):
+        d = W.to_device(inp, dev)
+        d["out"] = torch.empty_like(d["q"])
+        sets.append(d)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(d):
+        hstu_fwd(d["q"], d["k"], d["v"], d["seq_offsets"], max_seqlen=d["max_seqlen"],
+                 rab=d["rab"], num_context=d["num_context"], num_targets=d["num_targets"],
+                 causal=d["causal"], target_group_size=d["target_group_size"], alpha=d["alpha"],
+                 silu_scale=d["silu_scale"], out=d["out"])
+
+    for i in range(args.warmup):
+        step(sets[i % nsets])
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(sets[i % nsets])
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    ms_per_step = ms / args.steps
+    value = flops * args.steps * ws / (ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device -> forward -> host
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out_h = torch.empty_like(inp["q"]).pin_memory()
+    dq = W.to_device(inp, dev)
+    dq["out"] = torch.empty_like(dq["q"])
+    in_keys = [k for k in ("q", "k", "v", "seq_offsets", "num_context", "num_targets", "rab")
+               if host[k] is not None]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in in_keys)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for k in in_keys:
+            dq[k].copy_(host[k], non_blocking=True)
+        step(dq)
+        out_h.copy_(dq["out"], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_value = flops * ws / (e2e_ms * 1e-3) / 1e12
+
+    peaks = _peaks()
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
+                "traffic": args.traffic, "peak_source": peaks["source"]}
+    if w.rab:
+        gbs = _algorithmic_bytes(w, inp, pairs // w.num_heads_q * w.num_heads_q) / (
+            ms_per_step * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
+                    "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4), "traffic": args.traffic,
+                    "peak_source": peaks["source"]}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp, args.cpu_seconds)
+    if rank == 0:
+        line = {
+            "metric": "HSTU fwd mask-aware useful TFLOP/s (bf16, causal jagged); ms/call",
+            "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": w.name, "batch": w.batch, "max_seqlen": w.max_seqlen,
+                       "heads_q": w.num_heads_q, "heads_kv": w.num_heads_kv,
+                       "head_dim": w.head_dim, "mask": "causal" if w.causal else "none",
+                       "rab": w.rab, "tokens": int(inp["seq_offsets"][-1]),
+                       "valid_pairs": pairs, "useful_gflop_per_step": round(flops / 1e9, 3),
+                       "l2": f"rotating {nsets} input sets of {set_bytes / 2**20:.0f} MiB (> L2)",
+                       "parallelism": f"replicas x{ws}"},
+            "gpu_launches": 2 * args.steps,
+            "roofline": roofline,
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(w, inp, seconds):
+    """The fp64 oracle on the host cores over the first sequences of the workload
+    (all heads, whole rows), grown until it takes about `seconds`."""
+    import oracle
+
+    nthreads = os.cpu_count() or 1
+    so = inp["seq_offsets"].to(torch.int64)
+    nb = 1
+    best = None
+    while True:
+        sub = so[: nb + 1]
+        T = int(sub[-1])
+        args = dict(rab=None if inp["rab"] is None else inp["rab"][:nb],
+                    num_context=None if inp["num_context"] is None else inp["num_context"][:nb],
+                    num_targets=None if inp["num_targets"] is None else inp["num_targets"][:nb],
+                    mask_type=oracle.MASK_CAUSAL if w.causal else oracle.MASK_NONE,
+                    target_group_size=w.target_group_size, alpha=w.alpha_value,
+                    silu_scale=w.silu_scale_value, max_seqlen=w.max_seqlen)
+        q, k, v = inp["q"][:T], inp["k"][:T], inp["v"][:T]
+        t0 = time.perf_counter()
+        oracle.hstu_fwd(q, k, v, sub, nthreads=nthreads, **args)
+        dt = time.perf_counter() - t0
+        pairs = oracle.count_valid(sub, w.num_heads_q, num_context=args["num_context"],
+                                   num_targets=args["num_targets"], mask_type=args["mask_type"],
+                                   target_group_size=w.target_group_size)
+        best = (nb, dt, pairs)
+        if dt >= seconds / 4 or nb >= w.batch:
+            break
+        nb = min(w.batch, max(nb + 1, int(nb * min(8.0, (seconds / 4) / max(dt, 1e-3)))))
+    nb, dt, pairs = best
+    tflops = 4 * w.head_dim * pairs / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"sequences 0..{nb - 1} of {w.batch} (all {w.num_heads_q} heads, whole "
+                      f"rows), fp64, {dt:.2f} s"}
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as the reference arm: each step is one bounded sample."""
+    import oracle
+    from hstu_dense_forward_gb300 import workloads as W
+
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    oracle.build()
+    w = _workload(args.workload)
+    inp = W.generate(w)
+    nthreads = os.cpu_count() or 1
+    so = inp["seq_offsets"].to(torch.int64)
+    nb = 1  # one sequence, all heads, whole rows: a bounded sample per step
+    sub = so[: nb + 1]
+    T = int(sub[-1])
+    kw = dict(rab=None if inp["rab"] is None else inp["rab"][:nb],
+              num_context=None if inp["num_context"] is None else inp["num_context"][:nb],
+              num_targets=None if inp["num_targets"] is None else inp["num_targets"][:nb],
+              mask_type=oracle.MASK_CAUSAL if w.causal else oracle.MASK_NONE,
+              target_group_size=w.target_group_size, alpha=w.alpha_value,
+              silu_scale=w.silu_scale_value, max_seqlen=w.max_seqlen)
+    q, k, v = inp["q"][:T], inp["k"][:T], inp["v"][:T]
+    pairs = oracle.count_valid(sub, w.num_heads_q, num_context=kw["num_context"],
+                               num_targets=kw["num_targets"], mask_type=kw["mask_type"],
+                               target_group_size=w.target_group_size)
+    for _ in range(args.warmup):
+        oracle.hstu_fwd(q, k, v, sub, nthreads=nthreads, **kw)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.hstu_fwd(q, k, v, sub, nthreads=nthreads, **kw)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 4 * w.head_dim * pairs / dt / 1e12
+    sample = f"sequence 0 of {w.batch} (L={T}, all {w.num_heads_q} heads, whole rows), fp64"
+    line = {"impl": "reference",
+            "metric": "HSTU fwd mask-aware useful TFLOP/s (bf16, causal jagged); ms/call",
+            "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; shapes and distributions of the workload)",
+            "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bf16_causal_b32_s2048_h4_d128")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the forward kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+"""GB300 (sm_103a) HSTU fused attention forward.
+
+    out = hstu_fwd(q, k, v, seq_offsets, max_seqlen=S, causal=True, ...)
+
+computes, per jagged sequence and query head ("RecOps Running Case
+Documentation", Introduction to the HSTU_V1 Forward Operator and the feature
+table): S = Q K^T scaled by alpha, plus the optional relative attention bias
+rab, SiLU, the scaling silu_scale, the causal context/history/target mask or no
+mask, and the product with V. MHA and GQA (Nq a multiple of Nk), fp32, fp16 and
+bf16. The work runs in libhstu_fwd.so (tcgen05/TMA kernels for fp16/bf16, CUDA-core
+FFMA for fp32); this module marshals torch tensors to its C ABI and uses torch
+only for device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import HstuError
+
+__all__ = ["hstu_fwd", "HstuFwdPlan", "HstuError", "count_pairs", "useful_flops"]
+
+_DTYPES = {torch.float32: _abi.HSTU_F32, torch.float16: _abi.HSTU_F16,
+           torch.bfloat16: _abi.HSTU_BF16}
+
+
+def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, index_is_int64,
+          causal, target_group_size, has_rab, has_num_context, has_num_targets, watchdog_ms=0):
+    d = _abi.Desc()
+    d.dtype = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    d.batch = int(batch)
+    d.num_heads_q = int(num_heads_q)
+    d.num_heads_kv = int(num_heads_kv)
+    d.head_dim = int(head_dim)
+    d.max_seqlen = int(max_seqlen)
+    d.index_is_int64 = int(bool(index_is_int64))
+    d.mask_type = _abi.HSTU_MASK_CAUSAL if causal else _abi.HSTU_MASK_NONE
+    d.target_group_size = int(target_group_size)
+    d.has_rab = int(bool(has_rab))
+    d.has_num_context = int(bool(has_num_context))
+    d.has_num_targets = int(bool(has_num_targets))
+    d.watchdog_ms = int(watchdog_ms)
+    return d
+
+
+class HstuFwdPlan:
+    """One hstu_fwd_plan (validated descriptor + device workspace). Runs on one plan
+    must not execute concurrently: keep one plan per stream."""
+
+    def __init__(self, **desc_fields):
+        self.desc = _desc(**desc_fields)
+        self._keep = _abi.lib()
+        h = ctypes.c_void_p()
+        _abi.check(self._keep.hstu_fwd_create(ctypes.byref(self.desc), ctypes.byref(h)),
+                   "hstu_fwd_create")
+        self._h = h
+
+    def run_ptr(self, q, k, v, seq_offsets, rab, num_context, num_targets, total_tokens,
+                alpha, silu_scale, out, stream):
+        """Raw entry: integer device addresses (0 for absent) and a cudaStream_t value."""
+        _abi.check(self._keep.hstu_fwd_run(self._h, q, k, v, seq_offsets, rab or None,
+                                           num_context or None, num_targets or None,
+                                           int(total_tokens), float(alpha), float(silu_scale),
+                                           out, stream or None), "hstu_fwd_run")
+
+    def run(self, q, k, v, seq_offsets, out, *, rab=None, num_context=None, num_targets=None,
+            alpha=1.0, silu_scale=None, stream=None):
+        if silu_scale is None:
+            silu_scale = 1.0 / self.desc.max_seqlen
+        if stream is None:
+            stream = torch.cuda.current_stream(q.device)
+        ptr = lambda t: 0 if t is None else t.data_ptr()
+        self.run_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_offsets.data_ptr(), ptr(rab),
+                     ptr(num_context), ptr(num_targets), q.shape[0], alpha, silu_scale,
+                     out.data_ptr(), stream.cuda_stream)
+        return out
+
+    def get_error(self) -> int:
+        """Synchronise; return and clear the device error word (0 = none)."""
+        w = ctypes.c_int(0)
+        self._keep.hstu_fwd_get_error(self._h, ctypes.byref(w))
+        return w.value
+
+    def launches_per_run(self) -> int:
+        n = ctypes.c_int(0)
+        _abi.check(self._keep.hstu_fwd_launches_per_run(self._h, ctypes.byref(n)),
+                   "hstu_fwd_launches_per_run")
+        return n.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._keep.hstu_fwd_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_plans: dict = {}
+
+
+def _check_tensor(t, name, dtype, device, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def hstu_fwd(q, k, v, seq_offsets, *, max_seqlen, rab=None, num_context=None, num_targets=None,
+             causal=True, target_group_size=0, alpha=1.0, silu_scale=None, out=None,
+             watchdog_ms=0):
+    """HSTU forward on jagged tensors.
+
+    q [T, Nq, D], k/v [T, Nk, D] (same dtype: fp32, fp16 or bf16), seq_offsets [B+1]
+    int32/int64 (num_context / num_targets [B] of the same integer dtype), rab
+    [B, Nq, max_seqlen, max_seqlen] of q's dtype or None. causal=False is mask_type
+    2 (no mask). silu_scale defaults to 1/max_seqlen (Inputs and Outputs table).
+    Returns out [T, Nq, D]; rows that belong to no sequence are left as allocated.
+    """
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("hstu_fwd runs on CUDA tensors only")
+    _check_tensor(q, "q", None, dev, 3)
+    if q.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    _check_tensor(k, "k", q.dtype, dev, 3)
+    _check_tensor(v, "v", q.dtype, dev, 3)
+    _check_tensor(seq_offsets, "seq_offsets", None, dev, 1)
+    if seq_offsets.dtype not in (torch.int32, torch.int64):
+        raise TypeError("seq_offsets must be int32 or int64")
+    if k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
+        raise ValueError("k and v must be [T, Nk, D] with q's T and D")
+    for name, t in (("num_context", num_context), ("num_targets", num_targets)):
+        if t is not None:
+            _check_tensor(t, name, seq_offsets.dtype, dev, 1)
+    if rab is not None:
+        _check_tensor(rab, "rab", q.dtype, dev, 4)
+    T, Nq, D = q.shape
+    B = seq_offsets.shape[0] - 1
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_tensor(out, "out", q.dtype, dev, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    stream = torch.cuda.current_stream(dev)
+    key = (dev.index, stream.cuda_stream, q.dtype, B, Nq, k.shape[1], D, int(max_seqlen),
+           seq_offsets.dtype, bool(causal), int(target_group_size), rab is not None,
+           num_context is not None, num_targets is not None, int(watchdog_ms))
+    plan = _plans.get(key)
+    if plan is None:
+        with torch.cuda.device(dev):
+            plan = HstuFwdPlan(dtype=q.dtype, batch=B, num_heads_q=Nq, num_heads_kv=k.shape[1],
+                               head_dim=D, max_seqlen=max_seqlen,
+                               index_is_int64=seq_offsets.dtype == torch.int64, causal=causal,
+                               target_group_size=target_group_size, has_rab=rab is not None,
+                               has_num_context=num_context is not None,
+                               has_num_targets=num_targets is not None, watchdog_ms=watchdog_ms)
+        _plans[key] = plan
+    with torch.cuda.device(dev):
+        plan.run(q, k, v, seq_offsets, out, rab=rab, num_context=num_context,
+                 num_targets=num_targets, alpha=alpha, silu_scale=silu_scale, stream=stream)
+    return out
+
+
+def plan_for(**kw) -> HstuFwdPlan:
+    """A fresh plan (see HstuFwdPlan); keyword arguments as the descriptor fields."""
+    return HstuFwdPlan(**kw)
+
+
+def count_pairs(seq_offsets, num_heads_q, *, max_seqlen, num_context=None, num_targets=None,
+                causal=True, target_group_size=0) -> int:
+    """Mask-aware (query head, i, j) pair count, computed by the library on the host
+    from CPU integer tensors or sequences."""
+    so = torch.as_tensor(seq_offsets, dtype=torch.int64).contiguous().cpu()
+    nc = None if num_context is None else torch.as_tensor(num_context, dtype=torch.int64).contiguous().cpu()
+    nt = None if num_targets is None else torch.as_tensor(num_targets, dtype=torch.int64).contiguous().cpu()
+    d = _desc(dtype=_abi.HSTU_BF16, batch=so.numel() - 1, num_heads_q=num_heads_q,
+              num_heads_kv=1, head_dim=64, max_seqlen=max_seqlen, index_is_int64=True,
+              causal=causal, target_group_size=target_group_size, has_rab=False,
+              has_num_context=nc is not None, has_num_targets=nt is not None)
+    out = ctypes.c_longlong(0)
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    _abi.check(_abi.lib().hstu_fwd_count_pairs(ctypes.byref(d), ptr(so), ptr(nc), ptr(nt),
+                                               ctypes.byref(out)), "hstu_fwd_count_pairs")
+    return int(out.value)
+
+
+def useful_flops(pairs: int, head_dim: int) -> int:
+    """Mask-aware useful flops: 2*D for Q.K and 2*D for P.V per valid pair."""
+    return 4 * int(head_dim) * int(pairs)

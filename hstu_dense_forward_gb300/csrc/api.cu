@@ -1,0 +1,309 @@
+// C ABI and host planner of the HSTU forward: descriptor validation, workspace,
+// TMA tensor maps, kernel selection and launch. See include/hstu_fwd.h for the
+// contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/hstu_fwd.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using hstu::FwdParams;
+using hstu::TcMaps;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct hstu_fwd_plan {
+  hstu_fwd_desc desc;
+  int device;
+  int num_sms;
+  int grid;            // CTAs of the forward kernel
+  bool tensor_cores;   // bf16/fp16 tcgen05 path (else the fp32 CUDA-core path)
+  uint32_t* d_work;    // work list [B * ceil(S / 128)]
+  int* d_count;        // entries in the work list
+  int* d_err;          // device error word
+  long long timeout_ns;
+  // tensor maps of the last run, re-encoded when a pointer or T changes
+  TcMaps maps;
+  const void* map_ptrs[4];
+  long long map_T;
+  bool maps_valid;
+};
+
+extern "C" {
+
+const char* hstu_status_string(hstu_status s) {
+  switch (s) {
+    case HSTU_OK: return "ok";
+    case HSTU_ERR_INVALID_ARG: return "invalid argument";
+    case HSTU_ERR_UNSUPPORTED: return "unsupported configuration";
+    case HSTU_ERR_CUDA: return "CUDA runtime error";
+    case HSTU_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case HSTU_ERR_DEVICE_CHECK: return "device rejected the inputs";
+  }
+  return "unknown status";
+}
+
+static hstu_status validate_desc(const hstu_fwd_desc* d) {
+  if (!d) return HSTU_ERR_INVALID_ARG;
+  if (d->reserved[0] || d->reserved[1] || d->reserved[2]) return HSTU_ERR_INVALID_ARG;
+  if (d->dtype != HSTU_F32 && d->dtype != HSTU_F16 && d->dtype != HSTU_BF16)
+    return HSTU_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->batch > (1 << 20)) return HSTU_ERR_INVALID_ARG;
+  if (d->num_heads_q < 0 || d->num_heads_kv < 1) return HSTU_ERR_INVALID_ARG;
+  if (d->num_heads_q % d->num_heads_kv != 0) return HSTU_ERR_INVALID_ARG;
+  if (d->head_dim < 1) return HSTU_ERR_INVALID_ARG;
+  if (d->max_seqlen < 1 || d->max_seqlen > hstu::kMaxMTiles * hstu::kTileM)
+    return HSTU_ERR_INVALID_ARG;
+  if (d->target_group_size < 0 || d->watchdog_ms < 0) return HSTU_ERR_INVALID_ARG;
+  if (d->mask_type == HSTU_MASK_UPPER || d->mask_type == HSTU_MASK_CUSTOM)
+    return HSTU_ERR_UNSUPPORTED;
+  if (d->mask_type != HSTU_MASK_CAUSAL && d->mask_type != HSTU_MASK_NONE)
+    return HSTU_ERR_INVALID_ARG;
+  if (d->dtype == HSTU_F32) {
+    if (d->head_dim > 256) return HSTU_ERR_UNSUPPORTED;
+  } else {
+    if (!hstu::tc_supported_dim(d->head_dim)) return HSTU_ERR_UNSUPPORTED;
+    if (d->has_rab && d->max_seqlen % 8 != 0) return HSTU_ERR_UNSUPPORTED;
+  }
+  return HSTU_OK;
+}
+
+hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
+  if (!plan) return HSTU_ERR_INVALID_ARG;
+  *plan = nullptr;
+  hstu_status st = validate_desc(desc);
+  if (st != HSTU_OK) return st;
+  hstu_fwd_plan* P = new hstu_fwd_plan();
+  memset(P, 0, sizeof(*P));
+  P->desc = *desc;
+  P->timeout_ns = (long long)(desc->watchdog_ms > 0 ? desc->watchdog_ms : 1000) * 1000000ll;
+  P->tensor_cores = desc->dtype != HSTU_F32;
+  cudaError_t e = cudaGetDevice(&P->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&P->num_sms, cudaDevAttrMultiProcessorCount, P->device);
+  if (e == cudaSuccess) {
+    if (P->tensor_cores) {
+      int major = 0, minor = 0;
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, P->device);
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, P->device);
+      if (major != 10 || minor != 3 || !encode_fn()) {
+        delete P;
+        return HSTU_ERR_UNSUPPORTED;
+      }
+      e = hstu::tc_prepare(desc->head_dim, desc->dtype == HSTU_BF16, desc->has_rab);
+      P->grid = P->num_sms;
+    } else {
+      e = hstu::simt_prepare();
+      P->grid = P->num_sms * (desc->head_dim <= 64 ? 4 : (desc->head_dim <= 128 ? 2 : 1));
+    }
+  }
+  const size_t mtiles = (size_t)hstu::ceil_div(desc->max_seqlen, hstu::kTileM);
+  const size_t entries = (size_t)(desc->batch > 0 ? desc->batch : 1) * mtiles;
+  if (e == cudaSuccess) e = cudaMalloc(&P->d_work, entries * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&P->d_count, 2 * sizeof(int));
+  if (e == cudaSuccess) {
+    P->d_err = P->d_count + 1;
+    e = cudaMemset(P->d_count, 0, 2 * sizeof(int));
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(P->d_work);
+    cudaFree(P->d_count);
+    delete P;
+    return HSTU_ERR_CUDA;
+  }
+  *plan = P;
+  return HSTU_OK;
+}
+
+static bool encode3d(CUtensorMap* m, CUtensorMapDataType ty, const void* base, uint64_t d0,
+                     uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1,
+                     uint32_t b2, CUtensorMapSwizzle swz) {
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, ty, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
+                             const void* rab, long long T) {
+  const void* ptrs[4] = {q, k, v, rab};
+  if (P->maps_valid && P->map_T == T && memcmp(ptrs, P->map_ptrs, sizeof(ptrs)) == 0)
+    return HSTU_OK;
+  const hstu_fwd_desc& d = P->desc;
+  const CUtensorMapDataType ty =
+      d.dtype == HSTU_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int swb = hstu::tc_swizzle_bytes(d.head_dim);
+  const CUtensorMapSwizzle swz = swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                 : swb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                             : CU_TENSOR_MAP_SWIZZLE_32B;
+  const uint32_t epc = (uint32_t)(swb / 2);
+  const uint64_t D = (uint64_t)d.head_dim, Nq = (uint64_t)d.num_heads_q,
+                 Nk = (uint64_t)d.num_heads_kv;
+  bool ok = encode3d(&P->maps.q, ty, q, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, epc, 1,
+                     hstu::kTileM, swz) &&
+            encode3d(&P->maps.k, ty, k, D, Nk, (uint64_t)T, D * 2, Nk * D * 2, epc, 1,
+                     hstu::kTileN, swz) &&
+            encode3d(&P->maps.v, ty, v, D, Nk, (uint64_t)T, D * 2, Nk * D * 2, epc, 1,
+                     hstu::kTileN, swz);
+  if (ok && rab) {
+    const uint64_t S = (uint64_t)d.max_seqlen;
+    ok = encode3d(&P->maps.rab, ty, rab, S, S, (uint64_t)d.batch * Nq, S * 2, S * S * 2, 64,
+                  hstu::kTileM, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else if (ok) {
+    P->maps.rab = P->maps.q;  // unused by the kernel
+  }
+  if (!ok) {
+    P->maps_valid = false;
+    return HSTU_ERR_INVALID_ARG;
+  }
+  memcpy(P->map_ptrs, ptrs, sizeof(ptrs));
+  P->map_T = T;
+  P->maps_valid = true;
+  return HSTU_OK;
+}
+
+hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
+                         const void* seq_offsets, const void* rab, const void* num_context,
+                         const void* num_targets, long long total_tokens, float alpha,
+                         float silu_scale, void* out, void* stream) {
+  if (!P) return HSTU_ERR_INVALID_ARG;
+  const hstu_fwd_desc& d = P->desc;
+  if (total_tokens < 0 || total_tokens > 0x7fffffffll) return HSTU_ERR_INVALID_ARG;
+  if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
+  if (!q || !k || !v || !seq_offsets || !out) return HSTU_ERR_INVALID_ARG;
+  if ((rab != nullptr) != (d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
+  if ((num_context != nullptr) != (d.has_num_context != 0)) return HSTU_ERR_INVALID_ARG;
+  if ((num_targets != nullptr) != (d.has_num_targets != 0)) return HSTU_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (rab && !aligned16(rab)))
+    return HSTU_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != P->device) return HSTU_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  FwdParams p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.rab = rab;
+  p.out = out;
+  p.seq_offsets = seq_offsets;
+  p.num_context = num_context;
+  p.num_targets = num_targets;
+  p.work = P->d_work;
+  p.work_count = P->d_count;
+  p.err = P->d_err;
+  p.total_tokens = total_tokens;
+  p.timeout_ns = P->timeout_ns;
+  p.index64 = d.index_is_int64 ? 1 : 0;
+  p.B = d.batch;
+  p.Nq = d.num_heads_q;
+  p.Nk = d.num_heads_kv;
+  p.D = d.head_dim;
+  p.S = d.max_seqlen;
+  p.mask_type = d.mask_type;
+  p.g = d.mask_type == HSTU_MASK_CAUSAL ? d.target_group_size : 0;
+  p.alpha = alpha;
+  p.silu_scale = silu_scale;
+
+  if (P->tensor_cores) {
+    hstu_status ms = make_maps(P, q, k, v, rab, total_tokens);
+    if (ms != HSTU_OK) return ms;
+  }
+  if (hstu::launch_build_worklist(p, P->d_work, P->d_count, hstu::kTileM, st) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  cudaError_t e = P->tensor_cores
+                      ? hstu::launch_fwd_tc(p, P->maps, d.dtype == HSTU_BF16, P->grid, st, true)
+                      : hstu::launch_fwd_simt(p, P->grid, st, true);
+  return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+hstu_status hstu_fwd_destroy(hstu_fwd_plan* P) {
+  if (!P) return HSTU_OK;
+  cudaDeviceSynchronize();
+  cudaFree(P->d_work);
+  cudaFree(P->d_count);
+  delete P;
+  return HSTU_OK;
+}
+
+hstu_status hstu_fwd_get_error(hstu_fwd_plan* P, int* device_error) {
+  if (!P || !device_error) return HSTU_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return HSTU_ERR_CUDA;
+  int w = 0;
+  if (cudaMemcpy(&w, P->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  if (cudaMemset(P->d_err, 0, sizeof(int)) != cudaSuccess) return HSTU_ERR_CUDA;
+  *device_error = w;
+  if (w == HSTU_DEVERR_TIMEOUT) return HSTU_ERR_TIMEOUT;
+  if (w != HSTU_DEVERR_NONE) return HSTU_ERR_DEVICE_CHECK;
+  return HSTU_OK;
+}
+
+hstu_status hstu_fwd_launches_per_run(const hstu_fwd_plan* P, int* launches) {
+  if (!P || !launches) return HSTU_ERR_INVALID_ARG;
+  *launches = 2;  // work-list builder + forward kernel
+  return HSTU_OK;
+}
+
+hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* d, const void* seq_offsets_host,
+                                 const void* num_context_host, const void* num_targets_host,
+                                 long long* pairs) {
+  if (!d || !pairs || (d->batch > 0 && !seq_offsets_host)) return HSTU_ERR_INVALID_ARG;
+  if (d->mask_type != HSTU_MASK_CAUSAL && d->mask_type != HSTU_MASK_NONE)
+    return HSTU_ERR_UNSUPPORTED;
+  const int is64 = d->index_is_int64 ? 1 : 0;
+  const int g = d->mask_type == HSTU_MASK_CAUSAL ? d->target_group_size : 0;
+  long long total = 0;
+  for (int b = 0; b < d->batch; ++b) {
+    const long long t0 = hstu::load_index(seq_offsets_host, b, is64);
+    const long long L = hstu::load_index(seq_offsets_host, b + 1, is64) - t0;
+    if (L < 0 || L > d->max_seqlen) return HSTU_ERR_INVALID_ARG;
+    const long long nc = num_context_host ? hstu::load_index(num_context_host, b, is64) : 0;
+    const long long nt = num_targets_host ? hstu::load_index(num_targets_host, b, is64) : 0;
+    const hstu::SeqGeom s = hstu::make_geom((int)L, nc, nt, g, d->mask_type);
+    long long c = 0;
+    for (int i = 0; i < (int)L; ++i) {
+      const hstu::RowRange r = hstu::row_range(s, i, d->mask_type);
+      c += r.hist_end;
+      if (r.grp_hi >= r.grp_lo) c += r.grp_hi - r.grp_lo + 1;
+    }
+    total += c * d->num_heads_q;
+  }
+  *pairs = total;
+  return HSTU_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Launch interface between the host planner (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hstu {
+
+// Everything a forward kernel reads besides the tensor maps. Device pointers.
+struct FwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* rab;          // [B, Nq, S, S] or nullptr
+  void* out;
+  const void* seq_offsets;  // [B+1]
+  const void* num_context;  // [B] or nullptr
+  const void* num_targets;  // [B] or nullptr
+  const uint32_t* work;     // work list: packed (b, m-tile), heaviest first
+  const int* work_count;    // number of list entries
+  int* err;                 // device error word (HSTU_DEVERR_*)
+  long long total_tokens;   // T
+  long long timeout_ns;     // limit of one pipeline wait
+  int index64;              // index tensors are int64
+  int B, Nq, Nk, D, S;      // batch, heads, head dim, max_seqlen
+  int mask_type, g;         // mask code, target group size
+  float alpha, silu_scale;
+};
+
+__host__ __device__ inline long long load_index(const void* p, long long i, int is64) {
+  return is64 ? static_cast<const long long*>(p)[i] : static_cast<const int*>(p)[i];
+}
+
+// Scheduler: validates seq_offsets and writes the work list (one CTA).
+cudaError_t launch_build_worklist(const FwdParams& p, uint32_t* work, int* work_count,
+                                  int tile_m, cudaStream_t stream);
+
+// fp32 path on CUDA cores.
+size_t simt_smem_bytes(int D);
+cudaError_t simt_prepare();
+cudaError_t launch_fwd_simt(const FwdParams& p, int grid, cudaStream_t stream, bool pdl);
+
+// bf16 / fp16 tensor-core path (tcgen05, TMA, TMEM).
+struct TcMaps {
+  CUtensorMap q, k, v, rab;
+};
+bool tc_supported_dim(int D);
+int tc_swizzle_bytes(int D);  // row width of one TMA box / UMMA swizzle atom
+cudaError_t tc_prepare(int D, int bf16, int rab);
+cudaError_t launch_fwd_tc(const FwdParams& p, const TcMaps& maps, int bf16, int grid,
+                          cudaStream_t stream, bool pdl);
+
+}  // namespace hstu

@@ -1,0 +1,109 @@
+// Work-list builder for the persistent forward kernels.
+//
+// One work item is (sequence b, query tile of tile_m rows, query head h). The
+// list holds (b, m-tile) pairs sorted by the number of key/value tiles the item
+// visits, largest first (counting sort), so that the persistent kernel deals the
+// longest items out first. Heads are expanded arithmetically by the kernel
+// (item index = pair * Nq + h), which keeps the query heads of one GQA group
+// adjacent in time and lets them share K/V tiles through L2.
+//
+// The builder also checks the caller's seq_offsets ("increasing from 0; the user
+// must ensure validity", Inputs and Outputs table) and, if they are unusable,
+// records HSTU_DEVERR_OFFSETS and publishes an empty list so that no kernel
+// reads or writes outside the tensors.
+#include "../../include/hstu_fwd.h"
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace hstu {
+
+namespace {
+
+constexpr int kThreads = 1024;
+
+__global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, uint32_t* work,
+                                                                  int* work_count, int tile_m,
+                                                                  int nbins) {
+  // Let the dependent forward kernel start its prologue now; it waits for this
+  // grid's completion (griddepcontrol.wait) before it reads the list.
+  ptx::grid_dependents_launch();
+  extern __shared__ int hist[];  // [nbins] counts, then [nbins] cursors
+  int* cursor = hist + nbins;
+  __shared__ int bad;
+  for (int i = threadIdx.x; i < 2 * nbins; i += blockDim.x) hist[i] = 0;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+
+  const long long T = p.total_tokens;
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    long long a = load_index(p.seq_offsets, b, p.index64);
+    long long e = load_index(p.seq_offsets, b + 1, p.index64);
+    if (a < 0 || e < a || e > T || e - a > p.S) bad = 1;
+  }
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) {
+      *work_count = 0;
+      atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_OFFSETS);
+    }
+    return;
+  }
+
+  const int tile_n = kTileN;
+  // pass 1: histogram of key-tile counts
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    const long long t0 = load_index(p.seq_offsets, b, p.index64);
+    const int L = (int)(load_index(p.seq_offsets, b + 1, p.index64) - t0);
+    const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
+    const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
+    const SeqGeom s = make_geom(L, nc, nt, p.g, p.mask_type);
+    const int mtiles = ceil_div(L, tile_m);
+    for (int mt = 0; mt < mtiles; ++mt) {
+      const int nkv = ceil_div(kv_end_for_rows(s, mt * tile_m, tile_m, p.mask_type), tile_n);
+      atomicAdd(&hist[nkv], 1);
+    }
+  }
+  __syncthreads();
+  // exclusive scan, largest key-tile count first
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int n = nbins - 1; n >= 0; --n) {
+      cursor[n] = run;
+      run += hist[n];
+    }
+    *work_count = run;
+  }
+  __syncthreads();
+  // pass 2: scatter
+  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    const long long t0 = load_index(p.seq_offsets, b, p.index64);
+    const int L = (int)(load_index(p.seq_offsets, b + 1, p.index64) - t0);
+    const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
+    const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
+    const SeqGeom s = make_geom(L, nc, nt, p.g, p.mask_type);
+    const int mtiles = ceil_div(L, tile_m);
+    for (int mt = 0; mt < mtiles; ++mt) {
+      const int nkv = ceil_div(kv_end_for_rows(s, mt * tile_m, tile_m, p.mask_type), tile_n);
+      const int pos = atomicAdd(&cursor[nkv], 1);
+      work[pos] = pack_item(b, mt);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_worklist(const FwdParams& p, uint32_t* work, int* work_count,
+                                  int tile_m, cudaStream_t stream) {
+  const int nbins = ceil_div(p.S, kTileN) + 1;
+  const size_t smem = sizeof(int) * 2 * (size_t)nbins;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(build_worklist_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  build_worklist_kernel<<<1, kThreads, smem, stream>>>(p, work, work_count, tile_m, nbins);
+  return cudaGetLastError();
+}
+
+}  // namespace hstu

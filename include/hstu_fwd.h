@@ -1,0 +1,153 @@
+/*
+ * hstu_fwd.h — C ABI of the GB300 (sm_103a) HSTU fused attention forward.
+ *
+ * The operation ("RecOps Running Case Documentation", gitcode.com/Ascend/RecSDK,
+ * docs/en/rec_ops/hstu_v1_forward.md):
+ *   - Introduction to the HSTU_V1 Forward Operator: one fused operator chains the
+ *     QK matrix multiplication, the SiLU activation, the scaling, the mask and the
+ *     multiplication with V.
+ *   - Feature table: S = Q*K^T, P = silu(S), O = P*V; MHA and GQA (query heads
+ *     map many-to-one onto key/value heads); jagged sequences; fp32/fp16/bf16;
+ *     optional relative attention bias rab [b, n, s, s]; no mask or a causal mask
+ *     built from num_context, num_targets and target_group_size.
+ *   - Inputs and Outputs table: argument layouts, mask_type codes, the silu_scale
+ *     default 1/max_seq_len, alpha, and "empty input: the operator does not run".
+ *
+ * For every sequence b (L = seq_offsets[b+1] - seq_offsets[b], t0 = seq_offsets[b]),
+ * query head h (kv head hk = h / (Nq / Nk)), row i < L and column d < D:
+ *
+ *   x_ij = alpha * sum_d q[t0+i, h, d] * k[t0+j, hk, d]  (+ rab[b, h, i, j])
+ *   out[t0+i, h, d] = silu_scale * sum_{j < L, valid(i,j)} silu(x_ij) * v[t0+j, hk, d]
+ *
+ * with silu(x) = x / (1 + exp(-x)). The page does not place alpha or rab in the
+ * formula; this library multiplies Q*K^T by alpha and adds rab after it. The
+ * causal predicate valid(i, j) (the page names its inputs but does not spell it
+ * out) is, with H = (g > 0) ? max(L - nt, 0) : L:
+ *   (j <= i && j < H) || (i < nc && j < H)
+ *   || (g > 0 && i >= H && j >= H && j <= i && (i - H) / g == (j - H) / g)
+ *   || (g == 0 && j <= i)
+ * nc = num_context[b] (0 when absent), nt = num_targets[b] (0 when absent),
+ * g = target_group_size. mask_type NONE makes every (i, j) with i, j < L valid.
+ *
+ * Ownership: the caller owns every tensor. All tensor arguments of
+ * hstu_fwd_run are DEVICE pointers to contiguous, 16-byte aligned memory on the
+ * plan's device. The plan owns a small device workspace (work list, error word),
+ * allocated by hstu_fwd_create and freed by hstu_fwd_destroy.
+ *
+ * Errors are returned as hstu_status codes; nothing aborts, throws or traps.
+ * Asynchronous errors found on the device (invalid seq_offsets, a pipeline wait
+ * that ran past its time limit) are recorded in the plan's error word and read
+ * with hstu_fwd_get_error.
+ */
+#ifndef HSTU_FWD_H_
+#define HSTU_FWD_H_
+
+#if defined(__GNUC__)
+#define HSTU_API __attribute__((visibility("default")))
+#else
+#define HSTU_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  HSTU_OK = 0,
+  HSTU_ERR_INVALID_ARG = 1,  /* null pointer, bad size or alignment, bad descriptor */
+  HSTU_ERR_UNSUPPORTED = 2,  /* valid on the page but not built here (see each field) */
+  HSTU_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  HSTU_ERR_TIMEOUT = 4,      /* a device pipeline wait ran past its limit (error word) */
+  HSTU_ERR_DEVICE_CHECK = 5  /* the device rejected the inputs (error word) */
+} hstu_status;
+
+/* Element type of q, k, v, rab and out (Inputs and Outputs table: "the type must
+ * match q"; the output "same as q"). */
+typedef enum { HSTU_F32 = 0, HSTU_F16 = 1, HSTU_BF16 = 2 } hstu_dtype;
+
+/* mask_type codes of the Inputs and Outputs table. UPPER ("currently not
+ * supported" on the page) and CUSTOM are rejected with HSTU_ERR_UNSUPPORTED. */
+typedef enum {
+  HSTU_MASK_CAUSAL = 0, /* built-in lower-triangular mask with context/targets */
+  HSTU_MASK_UPPER = 1,
+  HSTU_MASK_NONE = 2,   /* bidirectional: no mask */
+  HSTU_MASK_CUSTOM = 3
+} hstu_mask_type;
+
+/* Device error word values (hstu_fwd_get_error). */
+enum {
+  HSTU_DEVERR_NONE = 0,
+  HSTU_DEVERR_OFFSETS = 1,  /* seq_offsets not increasing from >= 0, last > total_tokens,
+                               or a length above max_seqlen: nothing was written */
+  HSTU_DEVERR_TIMEOUT = 2   /* a pipeline wait gave up; out is incomplete */
+};
+
+typedef struct {
+  int dtype;             /* hstu_dtype */
+  int batch;             /* B in [0, 2^20]; 0 = empty input, run does nothing */
+  int num_heads_q;       /* Nq >= 0; 0 = empty input */
+  int num_heads_kv;      /* Nk >= 1, Nq % Nk == 0 (Inputs and Outputs table, k) */
+  int head_dim;          /* D: f16/bf16 need D in {32, 64, 128, 256}; f32 needs 1 <= D <= 256 */
+  int max_seqlen;        /* S in [1, 131072]: bound on every L; rab is [B, Nq, S, S];
+                            for rab with f16/bf16, S must be a multiple of 8 */
+  int index_is_int64;    /* 1: seq_offsets/num_context/num_targets are int64, 0: int32 */
+  int mask_type;         /* hstu_mask_type: CAUSAL or NONE */
+  int target_group_size; /* g >= 0; 0 = no target mask (causal only) */
+  int has_rab;           /* 1: rab is passed to every run */
+  int has_num_context;   /* 1: num_context [B] is passed to every run */
+  int has_num_targets;   /* 1: num_targets [B] is passed to every run */
+  int watchdog_ms;       /* limit of one device pipeline wait; 0 = 1000 ms */
+  int reserved[3];       /* must be 0 */
+} hstu_fwd_desc;
+
+typedef struct hstu_fwd_plan hstu_fwd_plan; /* opaque */
+
+/* Validate desc for the current CUDA device, allocate the plan's workspace.
+ * *plan is set on HSTU_OK only. */
+HSTU_API hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan);
+
+/*
+ * Enqueue one forward on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   q    [T, Nq, D]        k, v [T, Nk, D]       out [T, Nq, D]   (dtype of the plan)
+ *   seq_offsets [B+1]      increasing from 0, seq_offsets[B] <= T
+ *   rab  [B, Nq, S, S] or NULL (must be non-NULL iff desc.has_rab)
+ *   num_context, num_targets [B] or NULL (non-NULL iff the desc flags say so)
+ *   total_tokens = T, the row count of q, k, v and out.
+ * Rows of out that belong to no sequence are not written. silu_scale is used as
+ * given (the Python layer supplies 1/max_seqlen when the caller passes none).
+ * Asynchronous: no allocation, no synchronisation. One plan must not be used by
+ * two runs that may execute at the same time (it holds one work list).
+ * Returns HSTU_OK with nothing enqueued when B, Nq or T is 0.
+ */
+HSTU_API hstu_status hstu_fwd_run(hstu_fwd_plan* plan, const void* q, const void* k, const void* v,
+                         const void* seq_offsets, const void* rab, const void* num_context,
+                         const void* num_targets, long long total_tokens, float alpha,
+                         float silu_scale, void* out, void* stream);
+
+/* Free the workspace. NULL is accepted. Synchronises the device first. */
+HSTU_API hstu_status hstu_fwd_destroy(hstu_fwd_plan* plan);
+
+/* Synchronise the device, read the plan's device error word into *device_error
+ * (HSTU_DEVERR_*), and clear it. Returns HSTU_ERR_DEVICE_CHECK or
+ * HSTU_ERR_TIMEOUT when the word was set, else HSTU_OK. */
+HSTU_API hstu_status hstu_fwd_get_error(hstu_fwd_plan* plan, int* device_error);
+
+/* Kernel launches one hstu_fwd_run enqueues for this plan (for launch accounting). */
+HSTU_API hstu_status hstu_fwd_launches_per_run(const hstu_fwd_plan* plan, int* launches);
+
+/* Host-side count of the mask-aware work: sum over sequences of Nq * #valid(i, j),
+ * from HOST arrays seq_offsets [B+1] and optional num_context / num_targets [B]
+ * (int32 or int64 per desc.index_is_int64). 4 * D * pairs is the useful flop
+ * count of one run. */
+HSTU_API hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* desc, const void* seq_offsets_host,
+                                 const void* num_context_host, const void* num_targets_host,
+                                 long long* pairs);
+
+/* Static description of a status code. */
+HSTU_API const char* hstu_status_string(hstu_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HSTU_FWD_H_ */

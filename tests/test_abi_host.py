@@ -1,0 +1,94 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for sm_103a,
+loads, exports every entry point the header declares, validates descriptors
+before touching the device, and counts mask-aware work like the oracle."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from hstu_dense_forward_gb300 import _abi, count_pairs, useful_flops
+
+
+def test_library_exports_every_declared_symbol(built_lib):
+    L = ctypes.CDLL(built_lib)
+    names = _abi.declared_symbols()
+    assert {"hstu_fwd_create", "hstu_fwd_run", "hstu_fwd_destroy", "hstu_fwd_get_error",
+            "hstu_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/hstu_fwd.h but not exported"
+
+
+def _desc(**kw):
+    d = _abi.Desc()
+    base = dict(dtype=_abi.HSTU_BF16, batch=2, num_heads_q=4, num_heads_kv=2, head_dim=128,
+                max_seqlen=256, index_is_int64=1, mask_type=_abi.HSTU_MASK_CAUSAL,
+                target_group_size=0, has_rab=0, has_num_context=0, has_num_targets=0,
+                watchdog_ms=0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_heads_q=3, num_heads_kv=2), _abi.HSTU_ERR_INVALID_ARG),   # Nq % Nk != 0
+    (dict(mask_type=_abi.HSTU_MASK_UPPER), _abi.HSTU_ERR_UNSUPPORTED),  # "currently not supported"
+    (dict(mask_type=_abi.HSTU_MASK_CUSTOM), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(mask_type=7), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(head_dim=48), _abi.HSTU_ERR_UNSUPPORTED),                      # no tensor-core tile
+    (dict(dtype=_abi.HSTU_F32, head_dim=300), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(head_dim=0), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(max_seqlen=0), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(max_seqlen=200000), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(has_rab=1, max_seqlen=100), _abi.HSTU_ERR_UNSUPPORTED),        # TMA row stride
+    (dict(dtype=9), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(batch=-1), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(target_group_size=-2), _abi.HSTU_ERR_INVALID_ARG),
+])
+def test_create_rejects_bad_descriptors(built_lib, kw, status):
+    lib = _abi.lib()
+    h = ctypes.c_void_p()
+    d = _desc(**kw)
+    assert lib.hstu_fwd_create(ctypes.byref(d), ctypes.byref(h)) == status
+    assert not h.value
+
+
+def test_null_arguments(built_lib):
+    lib = _abi.lib()
+    assert lib.hstu_fwd_destroy(None) == _abi.HSTU_OK
+    assert lib.hstu_fwd_create(None, None) == _abi.HSTU_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    assert lib.hstu_fwd_create(None, ctypes.byref(h)) == _abi.HSTU_ERR_INVALID_ARG
+    assert lib.hstu_fwd_run(None, None, None, None, None, None, None, None, 0, 1.0, 1.0,
+                            None, None) == _abi.HSTU_ERR_INVALID_ARG
+    n = ctypes.c_int()
+    assert lib.hstu_fwd_get_error(None, ctypes.byref(n)) == _abi.HSTU_ERR_INVALID_ARG
+    for s in range(6):
+        assert lib.hstu_status_string(s)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_count_pairs_matches_oracle(built_lib, seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 6))
+    S = 64
+    lengths = rng.integers(0, S + 1, B)
+    so = np.concatenate([[0], np.cumsum(lengths)])
+    causal = seed % 3 != 0
+    nc = rng.integers(0, 10, B) if seed % 2 else None
+    nt = rng.integers(0, 20, B) if seed >= 2 else None
+    g = int(rng.integers(0, 5)) if causal else 0
+    want = oracle.count_valid(so, 3, num_context=nc, num_targets=nt,
+                              mask_type=oracle.MASK_CAUSAL if causal else oracle.MASK_NONE,
+                              target_group_size=g)
+    got = count_pairs(so, 3, max_seqlen=S, num_context=nc, num_targets=nt, causal=causal,
+                      target_group_size=g)
+    assert got == want
+    assert useful_flops(got, 128) == 4 * 128 * want
+
+
+def test_count_pairs_closed_forms(built_lib):
+    so = [0, 100, 250]
+    assert count_pairs(so, 2, max_seqlen=150) == 2 * (100 * 101 // 2 + 150 * 151 // 2)
+    assert count_pairs(so, 2, max_seqlen=150, causal=False) == 2 * (100 ** 2 + 150 ** 2)
