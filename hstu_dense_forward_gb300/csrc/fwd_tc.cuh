@@ -6,18 +6,21 @@
 // HSTU has no softmax, so there is no running max or rescaling: O is a plain sum
 // over key tiles and key tiles the mask removes entirely are never visited.
 //
-// CTA layout (persistent, one CTA per SM, 320 threads):
-//   warps 0-7  epilogue: two warpgroups; each thread owns one query row (TMEM lane)
-//              and half of the 128 key columns of every S tile. It reads S from
+// CTA layout (persistent, one CTA per SM, 672 threads):
+//   warps 0-15 epilogue: four warpgroups; each thread owns one query row (TMEM lane)
+//              and a quarter of the 128 key columns of every S tile. It reads S from
 //              TMEM, applies alpha, rab, SiLU (as h + h*tanh(h), h = x/2, one MUFU
 //              op per element) and the mask, and writes P (bf16/fp16) back to TMEM.
 //              At the end of a work item it reads O, scales, converts and stores.
-//   warp 8     producer: TMA loads of the Q tile, the K/V ring and the rab ring.
-//   warp 9     MMA issuer (one thread) and TMEM owner:
-//                S(t)  = Q K(t)^T   tcgen05.mma  A = Q (smem), B = K (smem, K-major)
-//                O    += P(t) V(t)  tcgen05.mma  A = P (TMEM),  B = V (smem, MN-major)
-//              S(t+1) is issued before O += P(t) V(t), so the tensor cores compute the
-//              next scores while the epilogue works on the current ones.
+//   warps 16, 18, 19  producers: TMA loads of the K (+ rab) ring, the V ring and the
+//              Q tiles, one thread each.
+//   warp 17    TMEM owner; one thread issues S(t) = Q K(t)^T (tcgen05.mma, A = Q and
+//              B = K from smem, K-major)
+//   warp 20    one thread issues O += P(t) V(t) (tcgen05.mma, A = P from TMEM, B = V
+//              from smem, MN-major)
+//              The score issuer runs ahead: S(t+2) goes out as soon as the epilogue has
+//              read S(t), so the tensor cores compute the next scores while the epilogue
+//              works on the current ones.
 // TMEM (512 columns): S double buffer at columns 0 and 128, O at 256 (D columns),
 // P double buffer after O (D <= 128) or written over the S buffer it came from
 // (D = 256, where O takes all remaining columns).
@@ -39,11 +42,15 @@
 namespace hstu {
 namespace tc {
 
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kEpiWG = 4;                   // epilogue warpgroups
+constexpr int kEpiWarps = 4 * kEpiWG;
+constexpr int kProducerWarp = kEpiWarps;      // K and rab loads
+constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr int kVProducerWarp = kEpiWarps + 2;  // V loads
+constexpr int kQProducerWarp = kEpiWarps + 3;  // Q loads
+constexpr int kPvWarp = kEpiWarps + 4;         // issues O += P V
+constexpr int kThreads = (kEpiWarps + 5) * 32;
+constexpr int kColsPerWG = kTileN / kEpiWG;  // S columns each warpgroup owns per tile
 constexpr uint32_t kTmemCols = 512;
 
 template <int D, bool RAB>
@@ -57,7 +64,8 @@ struct Cfg {
   static constexpr int TILE_BYTES = 128 * D * 2;
   static constexpr int RAB_BYTES = 128 * 128 * 2;
   static constexpr int NQ = (D <= 64) ? 2 : ((D == 128 && !RAB) ? 2 : 1);
-  static constexpr int NS = (D <= 64) ? 4 : (D == 128 ? 2 : 1);
+  static constexpr int NK = (D <= 64) ? 4 : (D == 128 ? (RAB ? 2 : 3) : 1);  // K ring depth
+  static constexpr int NV = (D <= 64) ? 4 : (D == 128 ? 2 : 1);              // V ring depth
   static constexpr int NR = RAB ? ((D == 256) ? 1 : 2) : 0;
   static constexpr bool P_ALIAS = (D == 256);
   // TMEM columns
@@ -66,8 +74,8 @@ struct Cfg {
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
-  static constexpr int OFF_R = OFF_V + NS * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
+  static constexpr int OFF_R = OFF_V + NV * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_R + NR * RAB_BYTES;
   static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES;
@@ -78,24 +86,29 @@ struct Cfg {
   static_assert(P_ALIAS || P_COL0 + 128 <= kTmemCols, "TMEM map");
 };
 
-// Barrier block layout (uint64 each).
+// One work item, decoded once (by the Q producer) and read by every role.
+struct Item {
+  int b, h, hk, L, m0, n_kv;
+  long long t0;
+  SeqGeom geom;
+};
+
+constexpr int kInfoDepth = 4;                   // decoded items kept in shared memory
+constexpr int kInfoReaders = kEpiWarps + 4;     // epilogue warps, two MMA issuers, K and V producers
+
+// Barrier block layout.
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t r_full[2], r_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t o_full, o_empty, drain;
+  uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
+  Item info[kInfoDepth];
   uint32_t tmem_base;
   volatile int abort;
 };
 static_assert(sizeof(Bars) <= 1024, "barrier block");
-
-// One work item, decoded identically by every role.
-struct Item {
-  int b, h, hk, L, m0, n_kv;
-  long long t0;
-  SeqGeom geom;
-};
 
 __device__ __forceinline__ bool decode_item(const FwdParams& p, long long idx, Item& it) {
   const uint32_t e = p.work[idx / p.Nq];
@@ -126,15 +139,14 @@ __device__ __forceinline__ bool wait_bar(Bars* bars, uint64_t* bar, uint32_t par
   const uint32_t a = ptx::smem_u32(bar);
   if (ptx::mbar_try_wait(a, parity)) return true;
   const uint64_t start = ptx::globaltimer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (ptx::mbar_try_wait(a, parity)) return true;
-    if ((n & 31u) == 0) {
-      if (bars->abort) return false;
-      if ((long long)(ptx::globaltimer_ns() - start) > p.timeout_ns) {
-        bars->abort = 1;
-        atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_TIMEOUT);
-        return false;
-      }
+  for (;;) {
+    // sleep until the phase flips (or 20 us pass), then check the abort flag and clock
+    if (ptx::mbar_try_wait_sleep(a, parity, 20000u)) return true;
+    if (bars->abort) return false;
+    if ((long long)(ptx::globaltimer_ns() - start) > p.timeout_ns) {
+      bars->abort = 1;
+      atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_TIMEOUT);
+      return false;
     }
   }
 }
@@ -145,6 +157,37 @@ __device__ __forceinline__ bool warp_wait(Bars* bars, uint64_t* bar, uint32_t pa
                                           const FwdParams& p) {
   const bool ok = wait_bar(bars, bar, parity, p);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Item ring: the Q producer decodes item k (global loads of the work list and the
+// sequence metadata) and publishes it in slot k % kInfoDepth; every other role
+// reads it from shared memory, so no role waits on those loads at an item start.
+__device__ __forceinline__ bool put_item(Bars* bars, int k, const Item& it, const FwdParams& p) {
+  const int s = k % kInfoDepth;
+  if (!wait_bar(bars, &bars->info_empty[s], ((k / kInfoDepth) & 1) ^ 1, p)) return false;
+  bars->info[s] = it;
+  ptx::mbar_arrive(ptx::smem_u32(&bars->info_full[s]));
+  return true;
+}
+
+// Single-thread reader.
+__device__ __forceinline__ bool get_item(Bars* bars, int k, Item& it, const FwdParams& p) {
+  const int s = k % kInfoDepth;
+  if (!wait_bar(bars, &bars->info_full[s], (k / kInfoDepth) & 1, p)) return false;
+  it = bars->info[s];
+  ptx::mbar_arrive(ptx::smem_u32(&bars->info_empty[s]));
+  return true;
+}
+
+// Whole-warp reader (one arrival per warp).
+__device__ __forceinline__ bool get_item_warp(Bars* bars, int k, Item& it, const FwdParams& p,
+                                              int lane) {
+  const int s = k % kInfoDepth;
+  if (!warp_wait(bars, &bars->info_full[s], (k / kInfoDepth) & 1, p)) return false;
+  it = bars->info[s];
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->info_empty[s]));
+  return true;
 }
 
 template <bool BF16>
@@ -169,37 +212,57 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
   }
 }
 
-// ------------------------------------------------------------------ producer
+// ------------------------------------------------------------------ producers
+// Three producer threads in separate warps stream Q, K (+ rab) and V, so that no
+// load waits behind the release of another ring's slot. With two Q buffers the Q
+// producer runs up to two work items ahead; with one, it prefetches the next
+// item's Q tile into L2 so that the load after the slot frees hits in L2.
 template <int D, bool RAB>
-__device__ void producer(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tq,
-                         const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tr,
-                         long long total) {
+__device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tq,
+                           long long total) {
   using C = Cfg<D, RAB>;
-  uint32_t q_it = 0, kv_it = 0, r_it = 0;
+  uint32_t q_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   for (int k = 0;; ++k) {
     const long long idx = item_index(k);
     if (idx >= total) break;
     Item it;
     decode_item(p, idx, it);
-    // Q tile
-    {
-      const int s = q_it % C::NQ;
-      if (!wait_bar(bars, &bars->q_empty[s], ((q_it / C::NQ) & 1) ^ 1, p)) return;
-      const uint32_t full = ptx::smem_u32(&bars->q_full[s]);
-      ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
-      const uint32_t dst = sbase + C::OFF_Q + s * C::TILE_BYTES;
+    if (!put_item(bars, k, it, p)) return;
+    if (C::NQ == 1 && item_index(k + 1) < total) {
+      Item nx;
+      decode_item(p, item_index(k + 1), nx);
 #pragma unroll
       for (int cb = 0; cb < C::NCB; ++cb)
-        ptx::tma_load_3d(dst + cb * C::CB_BYTES, tq, full, cb * C::EPC, it.h,
-                         (int)(it.t0 + it.m0));
-      ++q_it;
+        ptx::tma_prefetch_3d(tq, cb * C::EPC, nx.h, (int)(nx.t0 + nx.m0));
     }
+    const int s = q_it % C::NQ;
+    if (!wait_bar(bars, &bars->q_empty[s], ((q_it / C::NQ) & 1) ^ 1, p)) return;
+    const uint32_t full = ptx::smem_u32(&bars->q_full[s]);
+    ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
+    const uint32_t dst = sbase + C::OFF_Q + s * C::TILE_BYTES;
+#pragma unroll
+    for (int cb = 0; cb < C::NCB; ++cb)
+      ptx::tma_load_3d(dst + cb * C::CB_BYTES, tq, full, cb * C::EPC, it.h, (int)(it.t0 + it.m0));
+    ++q_it;
+  }
+}
+
+template <int D, bool RAB>
+__device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tk,
+                           const CUtensorMap* tr, long long total) {
+  using C = Cfg<D, RAB>;
+  uint32_t k_it = 0, r_it = 0;
+  const uint32_t sbase = ptx::smem_u32(smem);
+  for (int k = 0;; ++k) {
+    const long long idx = item_index(k);
+    if (idx >= total) break;
+    Item it;
+    if (!get_item(bars, k, it, p)) return;
     for (int j = 0; j < it.n_kv; ++j) {
-      const int s = kv_it % C::NS;
-      const uint32_t ph = ((kv_it / C::NS) & 1) ^ 1;
+      const int s = k_it % C::NK;
       const int row = (int)(it.t0 + j * kTileN);
-      if (!wait_bar(bars, &bars->k_empty[s], ph, p)) return;
+      if (!wait_bar(bars, &bars->k_empty[s], ((k_it / C::NK) & 1) ^ 1, p)) return;
       {
         const uint32_t full = ptx::smem_u32(&bars->k_full[s]);
         ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
@@ -208,6 +271,7 @@ __device__ void producer(const FwdParams& p, Bars* bars, uint8_t* smem, const CU
         for (int cb = 0; cb < C::NCB; ++cb)
           ptx::tma_load_3d(dst + cb * C::CB_BYTES, tk, full, cb * C::EPC, it.hk, row);
       }
+      ++k_it;
       if constexpr (RAB) {
         const int rs = r_it % C::NR;
         if (!wait_bar(bars, &bars->r_empty[rs], ((r_it / C::NR) & 1) ^ 1, p)) return;
@@ -219,85 +283,127 @@ __device__ void producer(const FwdParams& p, Bars* bars, uint8_t* smem, const CU
         ptx::tma_load_3d(dst + C::RAB_BYTES / 2, tr, full, j * kTileN + 64, it.m0, plane);
         ++r_it;
       }
-      if (!wait_bar(bars, &bars->v_empty[s], ph, p)) return;
-      {
-        const uint32_t full = ptx::smem_u32(&bars->v_full[s]);
-        ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
-        const uint32_t dst = sbase + C::OFF_V + s * C::TILE_BYTES;
-#pragma unroll
-        for (int cb = 0; cb < C::NCB; ++cb)
-          ptx::tma_load_3d(dst + cb * C::CB_BYTES, tv, full, cb * C::EPC, it.hk, row);
-      }
-      ++kv_it;
     }
   }
 }
 
-// ------------------------------------------------------------------ MMA issuer
-template <int D, bool BF16, bool RAB>
-__device__ void mma_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
+template <int D, bool RAB>
+__device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tv,
                            long long total) {
   using C = Cfg<D, RAB>;
-  constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16 ? 1u : 0u, 128, kTileN, 0);
-  constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16 ? 1u : 0u, 128, D, 1);
+  uint32_t v_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
-  uint32_t q_it = 0, k_it = 0, v_it = 0, t = 0, u = 0;
-
-  // S(t) = Q K^T into S buffer t % 2
-  auto issue_s = [&](int qs) -> bool {
-    const uint32_t sb = t & 1;
-    if (C::P_ALIAS && t >= 2) {  // P(t-2) lives in this S buffer until PV(t-2) is done
-      if (!wait_bar(bars, &bars->pv_done[sb], ((t >> 1) & 1) ^ 1, p)) return false;
-    }
-    const int ks = k_it % C::NS;
-    if (!wait_bar(bars, &bars->k_full[ks], (k_it / C::NS) & 1, p)) return false;
-    ptx::tc_fence_after();
-    const uint32_t qa = sbase + C::OFF_Q + qs * C::TILE_BYTES;
-    const uint32_t ka = sbase + C::OFF_K + ks * C::TILE_BYTES;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk * 16 / C::EPC) * C::CB_BYTES + ((kk * 16) % C::EPC) * 2;
-      const uint64_t ad = ptx::smem_desc(qa + off, 16, 8 * C::SWB, C::SWZ);
-      const uint64_t bd = ptx::smem_desc(ka + off, 16, 8 * C::SWB, C::SWZ);
-      ptx::mma_ss(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
-    }
-    ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
-    ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
-    ++k_it;
-    return true;
-  };
-
   for (int k = 0;; ++k) {
     const long long idx = item_index(k);
     if (idx >= total) break;
     Item it;
-    decode_item(p, idx, it);
-    const int qs = q_it % C::NQ;
-    if (!wait_bar(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) goto done;
-    const uint32_t t_first = t;
-    if (!issue_s(qs)) goto done;
+    if (!get_item(bars, k, it, p)) return;
     for (int j = 0; j < it.n_kv; ++j) {
-      const uint32_t tj = t_first + j;  // tile whose P is consumed now
-      t = tj + 1;                       // next S to issue
-      if (j + 1 < it.n_kv) {
-        if (!issue_s(qs)) goto done;
+      const int s = v_it % C::NV;
+      if (!wait_bar(bars, &bars->v_empty[s], ((v_it / C::NV) & 1) ^ 1, p)) return;
+      const uint32_t full = ptx::smem_u32(&bars->v_full[s]);
+      ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
+      const uint32_t dst = sbase + C::OFF_V + s * C::TILE_BYTES;
+#pragma unroll
+      for (int cb = 0; cb < C::NCB; ++cb)
+        ptx::tma_load_3d(dst + cb * C::CB_BYTES, tv, full, cb * C::EPC, it.hk,
+                         (int)(it.t0 + j * kTileN));
+      ++v_it;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuers
+// Two threads issue tcgen05.mma: one the score products S(t) = Q K(t)^T, the other
+// the accumulations O += P(t) V(t). An issuing thread stalls while the tensor pipe is
+// busy; with one issuer per product neither waits behind the other, and the next
+// scores are issued the moment their S buffer is free.
+
+// Both issuers end by waiting until their own MMAs have completed (TMEM is freed after).
+__device__ __forceinline__ void mma_drain(Bars* bars, const FwdParams& p) {
+  ptx::mma_commit(ptx::smem_u32(&bars->drain));
+  const uint32_t a = ptx::smem_u32(&bars->drain);
+  const uint64_t start = ptx::globaltimer_ns();
+  while (!ptx::mbar_try_wait_sleep(a, 0, 20000u)) {
+    if ((long long)(ptx::globaltimer_ns() - start) > p.timeout_ns) {
+      bars->abort = 1;
+      atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_TIMEOUT);
+      break;
+    }
+  }
+}
+
+template <int D, bool BF16, bool RAB>
+__device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
+                             long long total) {
+  using C = Cfg<D, RAB>;
+  constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16 ? 1u : 0u, 128, kTileN, 0);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint32_t q_it = 0, k_it = 0, t = 0;
+  for (int k = 0;; ++k) {
+    if (item_index(k) >= total) break;
+    Item it;
+    if (!get_item(bars, k, it, p)) break;
+    const int qs = q_it % C::NQ;
+    if (!wait_bar(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) break;
+    const uint32_t qa = sbase + C::OFF_Q + qs * C::TILE_BYTES;
+    bool ok = true;
+    for (int j = 0; j < it.n_kv && ok; ++j, ++t) {
+      const uint32_t sb = t & 1;
+      if (t >= 2) {
+        // S buffer sb is free once the epilogue has read S(t-2) (P in its own buffer)
+        // or, when P(t-2) was written over it, once PV(t-2) has read P(t-2).
+        uint64_t* bar = C::P_ALIAS ? &bars->pv_done[sb] : &bars->p_full[sb];
+        if (!wait_bar(bars, bar, ((t >> 1) & 1) ^ 1, p)) { ok = false; break; }
       }
+      const int ks = k_it % C::NK;
+      if (!wait_bar(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) { ok = false; break; }
+      ptx::tc_fence_after();
+      const uint32_t ka = sbase + C::OFF_K + ks * C::TILE_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk * 16 / C::EPC) * C::CB_BYTES + ((kk * 16) % C::EPC) * 2;
+        const uint64_t ad = ptx::smem_desc(qa + off, 16, 8 * C::SWB, C::SWZ);
+        const uint64_t bd = ptx::smem_desc(ka + off, 16, 8 * C::SWB, C::SWZ);
+        ptx::mma_ss(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+      }
+      ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
+      ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
       if (j + 1 == it.n_kv) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
-      // O += P(tj) V(tj)
-      const uint32_t sb = tj & 1;
-      if (!wait_bar(bars, &bars->p_full[sb], (tj >> 1) & 1, p)) goto done;
-      const int vs = v_it % C::NS;
-      if (!wait_bar(bars, &bars->v_full[vs], (v_it / C::NS) & 1, p)) goto done;
-      if (j == 0) {
-        if (!wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) goto done;
-      }
+      ++k_it;
+    }
+    if (!ok) break;
+    ++q_it;
+  }
+  mma_drain(bars, p);
+}
+
+template <int D, bool BF16, bool RAB>
+__device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
+                              long long total) {
+  using C = Cfg<D, RAB>;
+  constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16 ? 1u : 0u, 128, D, 1);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint32_t v_it = 0, t = 0, u = 0;
+  for (int k = 0;; ++k) {
+    if (item_index(k) >= total) break;
+    Item it;
+    if (!get_item(bars, k, it, p)) break;
+    bool ok = true;
+    for (int j = 0; j < it.n_kv; ++j, ++t) {
+      const uint32_t sb = t & 1;
+      if (!wait_bar(bars, &bars->p_full[sb], (t >> 1) & 1, p)) { ok = false; break; }
+      const int vs = v_it % C::NV;
+      if (!wait_bar(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) { ok = false; break; }
+      if (j == 0 && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk) {
         uint32_t pcol;
+        // keys [16kk, 16kk + 16) were written by warpgroup kk / 2 (32 keys each)
         if constexpr (C::P_ALIAS)
-          pcol = C::S_COL0 + sb * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+          pcol = C::S_COL0 + sb * 128 + (kk >> 1) * kColsPerWG + (kk & 1) * 8;
         else
           pcol = C::P_COL0 + sb * 64 + kk * 8;
         const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
@@ -307,37 +413,50 @@ __device__ void mma_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32
       ptx::mma_commit(ptx::smem_u32(&bars->pv_done[sb]));
       ++v_it;
     }
-    t = t_first + it.n_kv;
+    if (!ok) break;
     ptx::mma_commit(ptx::smem_u32(&bars->o_full));
-    ++q_it;
     ++u;
   }
-done:
-  // Drain: every MMA issued above has finished before TMEM can be released.
-  ptx::mma_commit(ptx::smem_u32(&bars->drain));
-  {
-    const uint32_t a = ptx::smem_u32(&bars->drain);
-    const uint64_t start = ptx::globaltimer_ns();
-    while (!ptx::mbar_try_wait(a, 0)) {
-      if ((long long)(ptx::globaltimer_ns() - start) > p.timeout_ns) {
-        bars->abort = 1;
-        atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_TIMEOUT);
-        break;
-      }
-    }
-  }
+  mma_drain(bars, p);
 }
 
 // ------------------------------------------------------------------ epilogue
+// Warp w of warpgroup wg = w / 4 reads TMEM lanes 32*(w % 4) .. +31 (one query row per
+// thread) and S columns [32*wg, 32*wg + 32) of every tile; it writes the 16 packed P
+// columns of those keys and, at the end of an item, O columns [wg*D/4, (wg+1)*D/4).
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&r)[8]) {
+  ptx::tmem_ld8(taddr, r);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&r)[16]) {
+  ptx::tmem_ld16(taddr, r);
+}
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
+  ptx::tmem_ld32(taddr, r);
+}
+
+// Per-warp arrive: every lane has finished its part (and fenced its tcgen05 ops).
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
+}
+
 template <int D, bool BF16, bool RAB>
 __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                          long long total, int warp, int lane) {
   using C = Cfg<D, RAB>;
   using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
-  const int wg = warp >> 2;                // column half of S, column half of O
-  const int quarter = warp & 3;            // TMEM lane quarter
-  const int r = quarter * 32 + lane;       // query row within the tile
+  constexpr int OC = D / kEpiWG;             // O columns per warpgroup
+  constexpr int OCH = OC < 32 ? OC : 32;     // O columns per TMEM load
+  const int wg = warp >> 2;
+  const int quarter = warp & 3;              // TMEM lane quarter
+  const int r = quarter * 32 + lane;         // query row within the tile
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+  const int col = wg * kColsPerWG;           // first S column of this warpgroup
   const float half_alpha = 0.5f * p.alpha;
   uint32_t t = 0, u = 0, r_it = 0;
   T16* out = static_cast<T16*>(p.out);
@@ -346,111 +465,98 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     const long long idx = item_index(k);
     if (idx >= total) break;
     Item it;
-    decode_item(p, idx, it);
+    if (!get_item_warp(bars, k, it, p, lane)) return;
     const int i = it.m0 + r;
     const RowRange rr = row_range(it.geom, i, p.mask_type);
     for (int j = 0; j < it.n_kv; ++j, ++t) {
       const uint32_t sb = t & 1;
       if (!warp_wait(bars, &bars->s_full[sb], (t >> 1) & 1, p)) return;
       ptx::tc_fence_after();
-      const uint8_t* rab_row = nullptr;
-      int rs = 0;
+      uint32_t sv[kColsPerWG];
+      ptx::tmem_ld32(tmem + lane_off + C::S_COL0 + sb * 128 + col, sv);
+      const int n0 = j * kTileN;
+      const bool full = tile_all_valid(it.geom, it.m0, kTileM, n0, kTileN, p.mask_type);
+      float x[kColsPerWG];
       if constexpr (RAB) {
-        rs = r_it % C::NR;
+        const int rs = r_it % C::NR;
         if (!warp_wait(bars, &bars->r_full[rs], (r_it / C::NR) & 1, p)) return;
-        rab_row = smem + C::OFF_R + rs * C::RAB_BYTES + wg * (C::RAB_BYTES / 2) + r * 128;
+        // rab tile: two 64-column TMA boxes of 128 rows x 128 bytes, 128-byte swizzle
+        const uint8_t* rab_row =
+            smem + C::OFF_R + rs * C::RAB_BYTES + (wg >> 1) * (C::RAB_BYTES / 2) + r * 128;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int chunk = ((wg & 1) * 4 + q4) ^ (r & 7);
+          const uint4 w = *reinterpret_cast<const uint4*>(rab_row + chunk * 16);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 rb = unpack2<BF16>(ww[e]);
+            x[q4 * 8 + 2 * e] = fmaf(__uint_as_float(sv[q4 * 8 + 2 * e]), half_alpha, 0.5f * rb.x);
+            x[q4 * 8 + 2 * e + 1] =
+                fmaf(__uint_as_float(sv[q4 * 8 + 2 * e + 1]), half_alpha, 0.5f * rb.y);
+          }
+        }
+        warp_arrive(&bars->r_empty[rs], lane);
+        ++r_it;
+      } else {
+#pragma unroll
+        for (int e = 0; e < kColsPerWG; ++e) x[e] = __uint_as_float(sv[e]) * half_alpha;
+      }
+      // x holds h = (alpha*s + rab)/2. silu(2h) = 2h*sigmoid(2h) = h*(1 + tanh(h)):
+      // a masked entry gets h = 0, so its P is silu(0) = 0. h is rounded to the
+      // 16-bit type, tanh runs packed (one MUFU op per two entries) and
+      // p = h*t + h is one packed fused multiply-add that yields P directly.
+      if (!full) {
+#pragma unroll
+        for (int e = 0; e < kColsPerWG; ++e)
+          if (!valid_in_range(rr, n0 + col + e)) x[e] = 0.f;
+      }
+      uint32_t pk[kColsPerWG / 2];
+#pragma unroll
+      for (int e = 0; e < kColsPerWG / 2; ++e) {
+        const uint32_t h2 = pack2<BF16>(x[2 * e], x[2 * e + 1]);
+        if constexpr (BF16)
+          pk[e] = ptx::fma_bf16x2(h2, ptx::tanh_bf16x2(h2), h2);
+        else
+          pk[e] = ptx::fma_f16x2(h2, ptx::tanh_f16x2(h2), h2);
       }
       if constexpr (!C::P_ALIAS) {  // P buffer sb is free once PV(t-2) is done
         if (t >= 2 && !warp_wait(bars, &bars->pv_done[sb], ((t >> 1) & 1) ^ 1, p)) return;
       }
-      const int n0 = j * kTileN;
-      const bool full = tile_all_valid(it.geom, it.m0, kTileM, n0, kTileN, p.mask_type);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int col = wg * 64 + c * 32;  // first S column of this chunk
-        uint32_t sv[32];
-        ptx::tmem_ld32(tmem + lane_off + C::S_COL0 + sb * 128 + col, sv);
-        float x[32];
-        if constexpr (RAB) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int chunk = (c * 4 + q4) ^ (r & 7);  // 128-byte TMA swizzle
-            const uint4 w = *reinterpret_cast<const uint4*>(rab_row + chunk * 16);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 rb = unpack2<BF16>(ww[e]);
-              x[q4 * 8 + 2 * e] = fmaf(__uint_as_float(sv[q4 * 8 + 2 * e]), half_alpha, 0.5f * rb.x);
-              x[q4 * 8 + 2 * e + 1] =
-                  fmaf(__uint_as_float(sv[q4 * 8 + 2 * e + 1]), half_alpha, 0.5f * rb.y);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(sv[e]) * half_alpha;
-        }
-        // silu(2h) = 2h * sigmoid(2h) = h * (1 + tanh(h)), h = x/2
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = fmaf(x[e], ptx::tanh_approx(x[e]), x[e]);
-        if (!full) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!valid_in_range(rr, n0 + col + e)) x[e] = 0.f;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(x[2 * e], x[2 * e + 1]);
-        uint32_t pcol;
-        if constexpr (C::P_ALIAS)
-          pcol = C::S_COL0 + sb * 128 + wg * 64 + c * 16;
-        else
-          pcol = C::P_COL0 + sb * 64 + wg * 32 + c * 16;
-        ptx::tmem_st16(tmem + lane_off + pcol, pk);
-      }
+      const uint32_t pcol = C::P_ALIAS ? C::S_COL0 + sb * 128 + col
+                                       : C::P_COL0 + sb * 64 + wg * (kColsPerWG / 2);
+      ptx::tmem_st16(tmem + lane_off + pcol, pk);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_u32(&bars->p_full[sb]));
-      if constexpr (RAB) {
-        ptx::mbar_arrive(ptx::smem_u32(&bars->r_empty[rs]));
-        ++r_it;
-      }
+      warp_arrive(&bars->p_full[sb], lane);
     }
-    // output tile
+    // output tile: read this warpgroup's O columns, release O, then scale and store
     if (!warp_wait(bars, &bars->o_full, u & 1, p)) return;
     ptx::tc_fence_after();
-    constexpr int HALF = D / 2;
-    constexpr int CH = HALF < 32 ? HALF : 32;
-    const bool row_ok = i < it.L;
-    T16* orow = out + ((it.t0 + i) * p.Nq + it.h) * (long long)D + wg * HALF;
+    uint32_t ov[OC];
 #pragma unroll
-    for (int c0 = 0; c0 < HALF; c0 += CH) {
-      const uint32_t taddr = tmem + lane_off + C::O_COL + wg * HALF + c0;
-      uint32_t pk[CH / 2];
-      if constexpr (CH == 32) {
-        uint32_t ov[32];
-        ptx::tmem_ld32(taddr, ov);
+    for (int c0 = 0; c0 < OC; c0 += OCH) {
+      uint32_t part[OCH];
+      tmem_ld<OCH>(tmem + lane_off + C::O_COL + wg * OC + c0, part);
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack2<BF16>(__uint_as_float(ov[2 * e]) * p.silu_scale,
-                              __uint_as_float(ov[2 * e + 1]) * p.silu_scale);
-      } else {
-        uint32_t ov[16];
-        ptx::tmem_ld16(taddr, ov);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          pk[e] = pack2<BF16>(__uint_as_float(ov[2 * e]) * p.silu_scale,
-                              __uint_as_float(ov[2 * e + 1]) * p.silu_scale);
-      }
-      if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-        for (int v4 = 0; v4 < CH / 8; ++v4)
-          dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-      }
+      for (int e = 0; e < OCH; ++e) ov[c0 + e] = part[e];
     }
     ptx::tc_fence_before();
-    ptx::mbar_arrive(ptx::smem_u32(&bars->o_empty));
+    warp_arrive(&bars->o_empty, lane);
     ++u;
+    if (i < it.L) {
+      T16* orow = out + ((it.t0 + i) * p.Nq + it.h) * (long long)D + wg * OC;
+      uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+      for (int v4 = 0; v4 < OC / 8; ++v4) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = pack2<BF16>(__uint_as_float(ov[v4 * 8 + 2 * e]) * p.silu_scale,
+                             __uint_as_float(ov[v4 * 8 + 2 * e + 1]) * p.silu_scale);
+        dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
   }
 }
 
@@ -472,9 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&bars->q_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->q_empty[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->r_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->r_empty[s]), kEpiThreads);
+      ptx::mbar_init(ptx::smem_u32(&bars->r_empty[s]), kEpiWarps);
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->p_full[s]), kEpiThreads);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_full[s]), kEpiWarps);
       ptx::mbar_init(ptx::smem_u32(&bars->pv_done[s]), 1);
     }
     for (int s = 0; s < 4; ++s) {
@@ -484,8 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&bars->v_empty[s]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&bars->o_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->o_empty), kEpiThreads);
-    ptx::mbar_init(ptx::smem_u32(&bars->drain), 1);
+    ptx::mbar_init(ptx::smem_u32(&bars->o_empty), kEpiWarps);
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), 2);  // one commit from each MMA issuer
+    for (int s = 0; s < kInfoDepth; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->info_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), kInfoReaders);
+    }
     bars->abort = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
@@ -510,9 +620,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kEpiWarps) {
     epilogue<D, BF16, RAB>(p, bars, smem, tmem, total, warp, lane);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer<D, RAB>(p, bars, smem, &tm_q, &tm_k, &tm_v, &tm_r, total);
+    if (lane == 0) producer_k<D, RAB>(p, bars, smem, &tm_k, &tm_r, total);
+  } else if (warp == kQProducerWarp) {
+    if (lane == 0) producer_q<D, RAB>(p, bars, smem, &tm_q, total);
+  } else if (warp == kVProducerWarp) {
+    if (lane == 0) producer_v<D, RAB>(p, bars, smem, &tm_v, total);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+    if (lane == 0) mma_s_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+  } else if (warp == kPvWarp) {
+    if (lane == 0) mma_pv_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
   }
   __syncwarp();
   ptx::tc_fence_before();

@@ -198,3 +198,13 @@ def test_full_size_sampled_rows(cuda_device, name):
     err = float(np.max(np.abs(g - ref)) / np.max(np.abs(ref)))
     assert np.isfinite(err) and err <= TOL[w.dtype], f"{name}: rel err {err:.3e}"
     assert torch.isfinite(got[: int(so[-1])].float()).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_wide_score_range(cuda_device, dtype):
+    """alpha = 1 with unit-variance inputs puts x = q.k over roughly [-40, 40], so
+    SiLU is exercised deep in both tails (the packed 16-bit tanh near -1 and +1)."""
+    w = W.Workload(name="wide", dtype=dtype, batch=2, num_heads_q=2, num_heads_kv=2, head_dim=64,
+                   max_seqlen=300, len_lo=200, len_hi=300, causal=True, sigma=1.0, alpha=1.0,
+                   seed=71)
+    _check(w, cuda_device)
