@@ -94,7 +94,9 @@ struct Item {
 };
 
 constexpr int kInfoDepth = 4;                   // decoded items kept in shared memory
-constexpr int kInfoReaders = kEpiWarps + 4;     // epilogue warps, two MMA issuers, K and V producers
+// item readers: epilogue warps, the MMA issuer(s), K and V producers
+template <bool P_ALIAS>
+constexpr int info_readers() { return kEpiWarps + (P_ALIAS ? 3 : 4); }
 
 // Barrier block layout.
 struct Bars {
@@ -333,6 +335,82 @@ __device__ __forceinline__ void mma_drain(Bars* bars, const FwdParams& p) {
   }
 }
 
+// Single issuer, used when P is written over its S buffer (D = 256): there S(t+2)
+// can only start after PV(t) has read P(t), so the two products form one chain and
+// are issued in that order: S(t0), S(t0+1), then per tile PV(t), S(t+2).
+template <int D, bool BF16, bool RAB>
+__device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
+                                  long long total) {
+  using C = Cfg<D, RAB>;
+  constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16 ? 1u : 0u, 128, kTileN, 0);
+  constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16 ? 1u : 0u, 128, D, 1);
+  const uint32_t sbase = ptx::smem_u32(smem);
+  uint32_t q_it = 0, k_it = 0, v_it = 0, u = 0, t_base = 0;
+  auto issue_s = [&](uint32_t t, int qs) -> bool {
+    const uint32_t sb = t & 1;
+    if (t >= 2 && !wait_bar(bars, &bars->pv_done[sb], ((t >> 1) & 1) ^ 1, p)) return false;
+    const int ks = k_it % C::NK;
+    if (!wait_bar(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) return false;
+    ptx::tc_fence_after();
+    const uint32_t qa = sbase + C::OFF_Q + qs * C::TILE_BYTES;
+    const uint32_t ka = sbase + C::OFF_K + ks * C::TILE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk * 16 / C::EPC) * C::CB_BYTES + ((kk * 16) % C::EPC) * 2;
+      const uint64_t ad = ptx::smem_desc(qa + off, 16, 8 * C::SWB, C::SWZ);
+      const uint64_t bd = ptx::smem_desc(ka + off, 16, 8 * C::SWB, C::SWZ);
+      ptx::mma_ss(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+    }
+    ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
+    ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
+    ++k_it;
+    return true;
+  };
+  auto issue_pv = [&](uint32_t t, bool first) -> bool {
+    const uint32_t sb = t & 1;
+    const int vs = v_it % C::NV;
+    if (!wait_bar(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) return false;
+    if (first && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) return false;
+    ptx::tc_fence_after();
+    const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < kTileN / 16; ++kk) {
+      const uint32_t pcol = C::S_COL0 + sb * 128 + (16 * kk / kColsPerWG) * kColsPerWG +
+                            ((16 * kk) % kColsPerWG) / 2;
+      const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
+      ptx::mma_ts(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (!first || kk > 0) ? 1u : 0u);
+    }
+    ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
+    ptx::mma_commit(ptx::smem_u32(&bars->pv_done[sb]));
+    ++v_it;
+    return true;
+  };
+  for (int k = 0;; ++k) {
+    if (item_index(k) >= total) break;
+    Item it;
+    if (!get_item(bars, k, it, p)) break;
+    const int qs = q_it % C::NQ;
+    if (!wait_bar(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) break;
+    const int n = it.n_kv;
+    bool ok = issue_s(t_base, qs) && (n < 2 || issue_s(t_base + 1, qs));
+    if (ok && n <= 2) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
+    for (int j = 0; j < n && ok; ++j) {
+      const uint32_t t = t_base + j;
+      ok = wait_bar(bars, &bars->p_full[t & 1], (t >> 1) & 1, p) && issue_pv(t, j == 0);
+      if (ok && j + 2 < n) {
+        ok = issue_s(t + 2, qs);
+        if (ok && j + 3 == n) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
+      }
+    }
+    if (!ok) break;
+    t_base += n;
+    ptx::mma_commit(ptx::smem_u32(&bars->o_full));
+    ++q_it;
+    ++u;
+  }
+  mma_drain(bars, p);
+}
+
 template <int D, bool BF16, bool RAB>
 __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                              long long total) {
@@ -401,9 +479,11 @@ __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uin
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk) {
         uint32_t pcol;
-        // keys [16kk, 16kk + 16) were written by warpgroup kk / 2 (32 keys each)
+        // keys [16kk, 16kk + 16): with P over S, warpgroup 16kk / kColsPerWG wrote them
+        // packed at the start of its own S columns
         if constexpr (C::P_ALIAS)
-          pcol = C::S_COL0 + sb * 128 + (kk >> 1) * kColsPerWG + (kk & 1) * 8;
+          pcol = C::S_COL0 + sb * 128 + (16 * kk / kColsPerWG) * kColsPerWG +
+                 ((16 * kk) % kColsPerWG) / 2;
         else
           pcol = C::P_COL0 + sb * 64 + kk * 8;
         const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
@@ -472,60 +552,70 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       const uint32_t sb = t & 1;
       if (!warp_wait(bars, &bars->s_full[sb], (t >> 1) & 1, p)) return;
       ptx::tc_fence_after();
-      uint32_t sv[kColsPerWG];
-      ptx::tmem_ld32(tmem + lane_off + C::S_COL0 + sb * 128 + col, sv);
       const int n0 = j * kTileN;
       const bool full = tile_all_valid(it.geom, it.m0, kTileM, n0, kTileN, p.mask_type);
-      float x[kColsPerWG];
+      const uint8_t* rab_row = nullptr;
+      int rs = 0;
       if constexpr (RAB) {
-        const int rs = r_it % C::NR;
+        rs = r_it % C::NR;
         if (!warp_wait(bars, &bars->r_full[rs], (r_it / C::NR) & 1, p)) return;
-        // rab tile: two 64-column TMA boxes of 128 rows x 128 bytes, 128-byte swizzle
-        const uint8_t* rab_row =
-            smem + C::OFF_R + rs * C::RAB_BYTES + (wg >> 1) * (C::RAB_BYTES / 2) + r * 128;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int chunk = ((wg & 1) * 4 + q4) ^ (r & 7);
-          const uint4 w = *reinterpret_cast<const uint4*>(rab_row + chunk * 16);
-          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 rb = unpack2<BF16>(ww[e]);
-            x[q4 * 8 + 2 * e] = fmaf(__uint_as_float(sv[q4 * 8 + 2 * e]), half_alpha, 0.5f * rb.x);
-            x[q4 * 8 + 2 * e + 1] =
-                fmaf(__uint_as_float(sv[q4 * 8 + 2 * e + 1]), half_alpha, 0.5f * rb.y);
-          }
-        }
-        warp_arrive(&bars->r_empty[rs], lane);
-        ++r_it;
-      } else {
-#pragma unroll
-        for (int e = 0; e < kColsPerWG; ++e) x[e] = __uint_as_float(sv[e]) * half_alpha;
-      }
-      // x holds h = (alpha*s + rab)/2. silu(2h) = 2h*sigmoid(2h) = h*(1 + tanh(h)):
-      // a masked entry gets h = 0, so its P is silu(0) = 0. h is rounded to the
-      // 16-bit type, tanh runs packed (one MUFU op per two entries) and
-      // p = h*t + h is one packed fused multiply-add that yields P directly.
-      if (!full) {
-#pragma unroll
-        for (int e = 0; e < kColsPerWG; ++e)
-          if (!valid_in_range(rr, n0 + col + e)) x[e] = 0.f;
-      }
-      uint32_t pk[kColsPerWG / 2];
-#pragma unroll
-      for (int e = 0; e < kColsPerWG / 2; ++e) {
-        const uint32_t h2 = pack2<BF16>(x[2 * e], x[2 * e + 1]);
-        if constexpr (BF16)
-          pk[e] = ptx::fma_bf16x2(h2, ptx::tanh_bf16x2(h2), h2);
-        else
-          pk[e] = ptx::fma_f16x2(h2, ptx::tanh_f16x2(h2), h2);
+        rab_row = smem + C::OFF_R + rs * C::RAB_BYTES + r * 128;
       }
       if constexpr (!C::P_ALIAS) {  // P buffer sb is free once PV(t-2) is done
         if (t >= 2 && !warp_wait(bars, &bars->pv_done[sb], ((t >> 1) & 1) ^ 1, p)) return;
       }
-      const uint32_t pcol = C::P_ALIAS ? C::S_COL0 + sb * 128 + col
-                                       : C::P_COL0 + sb * 64 + wg * (kColsPerWG / 2);
-      ptx::tmem_st16(tmem + lane_off + pcol, pk);
+#pragma unroll
+      for (int c = 0; c < kColsPerWG / 32; ++c) {
+        const int cc = col + c * 32;  // first S column of this 32-column chunk
+        uint32_t sv[32];
+        ptx::tmem_ld32(tmem + lane_off + C::S_COL0 + sb * 128 + cc, sv);
+        float x[32];
+        if constexpr (RAB) {
+          // rab tile: two 64-column TMA boxes of 128 rows x 128 bytes, 128-byte swizzle
+          const uint8_t* box = rab_row + (cc >> 6) * (C::RAB_BYTES / 2);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int chunk = (((cc & 63) >> 3) + q4) ^ (r & 7);
+            const uint4 w = *reinterpret_cast<const uint4*>(box + chunk * 16);
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 rb = unpack2<BF16>(ww[e]);
+              x[q4 * 8 + 2 * e] = fmaf(__uint_as_float(sv[q4 * 8 + 2 * e]), half_alpha, 0.5f * rb.x);
+              x[q4 * 8 + 2 * e + 1] =
+                  fmaf(__uint_as_float(sv[q4 * 8 + 2 * e + 1]), half_alpha, 0.5f * rb.y);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(sv[e]) * half_alpha;
+        }
+        // x holds h = (alpha*s + rab)/2. silu(2h) = 2h*sigmoid(2h) = h*(1 + tanh(h)):
+        // a masked entry gets h = 0, so its P is silu(0) = 0. h is rounded to the
+        // 16-bit type, tanh runs on packed pairs and p = h*t + h is one packed fused
+        // multiply-add that yields P directly.
+        if (!full) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (!valid_in_range(rr, n0 + cc + e)) x[e] = 0.f;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t h2 = pack2<BF16>(x[2 * e], x[2 * e + 1]);
+          if constexpr (BF16)
+            pk[e] = ptx::fma_bf16x2(h2, ptx::tanh_bf16x2(h2), h2);
+          else
+            pk[e] = ptx::fma_f16x2(h2, ptx::tanh_f16x2(h2), h2);
+        }
+        const uint32_t pcol = C::P_ALIAS ? C::S_COL0 + sb * 128 + col + c * 16
+                                         : C::P_COL0 + sb * 64 + cc / 2;
+        ptx::tmem_st16(tmem + lane_off + pcol, pk);
+      }
+      if constexpr (RAB) {
+        warp_arrive(&bars->r_empty[rs], lane);
+        ++r_it;
+      }
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       warp_arrive(&bars->p_full[sb], lane);
@@ -591,10 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(ptx::smem_u32(&bars->o_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->o_empty), kEpiWarps);
-    ptx::mbar_init(ptx::smem_u32(&bars->drain), 2);  // one commit from each MMA issuer
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), C::P_ALIAS ? 1 : 2);  // one commit per issuer
     for (int s = 0; s < kInfoDepth; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->info_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), kInfoReaders);
+      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), info_readers<C::P_ALIAS>());
     }
     bars->abort = 0;
     ptx::fence_barrier_init();
@@ -626,9 +716,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kVProducerWarp) {
     if (lane == 0) producer_v<D, RAB>(p, bars, smem, &tm_v, total);
   } else if (warp == kMmaWarp) {
-    if (lane == 0) mma_s_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+    if (lane == 0) {
+      if constexpr (C::P_ALIAS)
+        mma_serial_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+      else
+        mma_s_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+    }
   } else if (warp == kPvWarp) {
-    if (lane == 0) mma_pv_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+    if (lane == 0 && !C::P_ALIAS) mma_pv_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
   }
   __syncwarp();
   ptx::tc_fence_before();
