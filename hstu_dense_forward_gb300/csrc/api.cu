@@ -52,7 +52,7 @@ struct hstu_fwd_plan {
   long long timeout_ns;
   // tensor maps of the last run, re-encoded when a pointer or T changes
   TcMaps maps;
-  const void* map_ptrs[4];
+  const void* map_ptrs[5];
   long long map_T;
   bool maps_valid;
 };
@@ -157,8 +157,8 @@ static bool encode3d(CUtensorMap* m, CUtensorMapDataType ty, const void* base, u
 }
 
 static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
-                             const void* rab, long long T) {
-  const void* ptrs[4] = {q, k, v, rab};
+                             const void* rab, const void* out, long long T) {
+  const void* ptrs[5] = {q, k, v, rab, out};
   if (P->maps_valid && P->map_T == T && memcmp(ptrs, P->map_ptrs, sizeof(ptrs)) == 0)
     return HSTU_OK;
   const hstu_fwd_desc& d = P->desc;
@@ -176,7 +176,9 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
             encode3d(&P->maps.k, ty, k, D, Nk, (uint64_t)T, D * 2, Nk * D * 2, epc, 1,
                      hstu::kTileN, swz) &&
             encode3d(&P->maps.v, ty, v, D, Nk, (uint64_t)T, D * 2, Nk * D * 2, epc, 1,
-                     hstu::kTileN, swz);
+                     hstu::kTileN, swz) &&
+            encode3d(&P->maps.out, ty, out, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, epc, 1,
+                     hstu::kTileM, swz);
   if (ok && rab) {
     const uint64_t S = (uint64_t)d.max_seqlen;
     ok = encode3d(&P->maps.rab, ty, rab, S, S, (uint64_t)d.batch * Nq, S * 2, S * S * 2, 64,
@@ -239,7 +241,7 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
   p.silu_scale = silu_scale;
 
   if (P->tensor_cores) {
-    hstu_status ms = make_maps(P, q, k, v, rab, total_tokens);
+    hstu_status ms = make_maps(P, q, k, v, rab, out, total_tokens);
     if (ms != HSTU_OK) return ms;
   }
   if (hstu::launch_build_worklist(p, P->d_work, P->d_count, hstu::kTileM, st) != cudaSuccess)

@@ -25,7 +25,7 @@ cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::fwd_tc_kernel<D, BF16, RAB>, m.q, m.k, m.v, m.rab, p);
+  return cudaLaunchKernelEx(&cfg, tc::fwd_tc_kernel<D, BF16, RAB>, m.q, m.k, m.v, m.rab, m.out, p);
 }
 
 template <bool BF16, bool RAB>

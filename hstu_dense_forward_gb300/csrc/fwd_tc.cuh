@@ -50,6 +50,7 @@ constexpr int kVProducerWarp = kEpiWarps + 2;  // V loads
 constexpr int kQProducerWarp = kEpiWarps + 3;  // Q loads
 constexpr int kPvWarp = kEpiWarps + 4;         // issues O += P V
 constexpr int kThreads = (kEpiWarps + 5) * 32;
+constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kColsPerWG = kTileN / kEpiWG;  // S columns each warpgroup owns per tile
 constexpr uint32_t kTmemCols = 512;
 
@@ -64,9 +65,11 @@ struct Cfg {
   static constexpr int TILE_BYTES = 128 * D * 2;
   static constexpr int RAB_BYTES = 128 * 128 * 2;
   static constexpr int NQ = (D <= 64) ? 2 : ((D == 128 && !RAB) ? 2 : 1);
-  static constexpr int NK = (D <= 64) ? 4 : (D == 128 ? (RAB ? 2 : 3) : 1);  // K ring depth
-  static constexpr int NV = (D <= 64) ? 4 : (D == 128 ? 2 : 1);              // V ring depth
+  static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 3 : 4) : (D == 128 ? 2 : 1));
+  static constexpr int NV = NK;                                  // K and V ring depths
   static constexpr int NR = RAB ? ((D == 256) ? 1 : 2) : 0;
+  // O is staged in shared memory and written by TMA when there is room for a tile
+  static constexpr bool STAGE = D <= 64 || (D == 128 && !RAB);
   static constexpr bool P_ALIAS = (D == 256);
   // TMEM columns
   static constexpr uint32_t S_COL0 = 0, O_COL = 256;
@@ -76,7 +79,8 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
   static constexpr int OFF_R = OFF_V + NV * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_R + NR * RAB_BYTES;
+  static constexpr int OFF_O = OFF_R + NR * RAB_BYTES;
+  static constexpr int OFF_BAR = OFF_O + (STAGE ? TILE_BYTES : 0);
   static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES;
   // keep one CTA per SM (TMEM is allocated whole)
@@ -104,7 +108,7 @@ struct Bars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t r_full[2], r_empty[2];
   uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t o_full, o_empty, drain;
+  uint64_t o_full, o_empty, drain, epi_sync;
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   Item info[kInfoDepth];
   uint32_t tmem_base;
@@ -525,9 +529,26 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
   if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
 }
 
+// Byte offset of a 16-byte chunk inside a TMA box written with SWB-byte swizzling
+// (the 16-byte chunk index is XORed with the row index within each swizzle atom).
+template <int SWB>
+__device__ __forceinline__ uint32_t swizzle(uint32_t o) {
+  constexpr uint32_t mask = SWB == 128 ? 0x70u : (SWB == 64 ? 0x30u : 0x10u);
+  return o ^ ((o >> 3) & mask);
+}
+
+// Barrier among the epilogue warps (bounded: an mbarrier rather than bar.sync).
+__device__ __forceinline__ bool epi_barrier(Bars* bars, uint32_t& phase, const FwdParams& p,
+                                            int lane) {
+  warp_arrive(&bars->epi_sync, lane);
+  const bool ok = warp_wait(bars, &bars->epi_sync, phase & 1, p);
+  ++phase;
+  return ok;
+}
+
 template <int D, bool BF16, bool RAB>
 __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
-                         long long total, int warp, int lane) {
+                         const CUtensorMap* tm_o, long long total, int warp, int lane) {
   using C = Cfg<D, RAB>;
   using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr int OC = D / kEpiWG;             // O columns per warpgroup
@@ -538,7 +559,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
   const int col = wg * kColsPerWG;           // first S column of this warpgroup
   const float half_alpha = 0.5f * p.alpha;
-  uint32_t t = 0, u = 0, r_it = 0;
+  uint32_t t = 0, u = 0, r_it = 0, epi_phase = 0;
   T16* out = static_cast<T16*>(p.out);
 
   for (int k = 0;; ++k) {
@@ -560,9 +581,6 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         rs = r_it % C::NR;
         if (!warp_wait(bars, &bars->r_full[rs], (r_it / C::NR) & 1, p)) return;
         rab_row = smem + C::OFF_R + rs * C::RAB_BYTES + r * 128;
-      }
-      if constexpr (!C::P_ALIAS) {  // P buffer sb is free once PV(t-2) is done
-        if (t >= 2 && !warp_wait(bars, &bars->pv_done[sb], ((t >> 1) & 1) ^ 1, p)) return;
       }
 #pragma unroll
       for (int c = 0; c < kColsPerWG / 32; ++c) {
@@ -610,6 +628,10 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         }
         const uint32_t pcol = C::P_ALIAS ? C::S_COL0 + sb * 128 + col + c * 16
                                          : C::P_COL0 + sb * 64 + cc / 2;
+        if constexpr (!C::P_ALIAS) {  // P buffer sb is free once PV(t-2) has read it
+          if (c == 0 && t >= 2 && !warp_wait(bars, &bars->pv_done[sb], ((t >> 1) & 1) ^ 1, p))
+            return;
+        }
         ptx::tmem_st16(tmem + lane_off + pcol, pk);
       }
       if constexpr (RAB) {
@@ -634,7 +656,46 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     ptx::tc_fence_before();
     warp_arrive(&bars->o_empty, lane);
     ++u;
-    if (i < it.L) {
+    if constexpr (C::STAGE) {
+      // Stage the scaled tile in shared memory in the TMA box layout (swizzled 16-byte
+      // chunks, conflict-free for one row per lane), then write it with TMA when the
+      // whole tile lies inside the sequence, else with coalesced predicated stores.
+      uint8_t* stage = smem + C::OFF_O;
+      if (threadIdx.x == 0) ptx::bulk_wait_read0();  // previous tile's store has read it
+      if (!epi_barrier(bars, epi_phase, p, lane)) return;
+#pragma unroll
+      for (int v4 = 0; v4 < OC / 8; ++v4) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = pack2<BF16>(__uint_as_float(ov[v4 * 8 + 2 * e]) * p.silu_scale,
+                             __uint_as_float(ov[v4 * 8 + 2 * e + 1]) * p.silu_scale);
+        const int cidx = wg * OC + v4 * 8;
+        const uint32_t o = (cidx / C::EPC) * C::CB_BYTES + r * C::SWB + (cidx % C::EPC) * 2;
+        *reinterpret_cast<uint4*>(stage + swizzle<C::SWB>(o)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      ptx::fence_proxy_async_smem();
+      if (!epi_barrier(bars, epi_phase, p, lane)) return;
+      if (it.m0 + kTileM <= it.L) {
+        if (threadIdx.x == 0) {
+#pragma unroll
+          for (int cb = 0; cb < C::NCB; ++cb)
+            ptx::tma_store_3d(tm_o, ptx::smem_u32(stage + cb * C::CB_BYTES), cb * C::EPC, it.h,
+                              (int)(it.t0 + it.m0));
+          ptx::bulk_commit();
+        }
+      } else {
+        constexpr int CHUNKS = kTileM * D / 8;  // 16-byte chunks in the tile
+        for (int x = threadIdx.x; x < CHUNKS; x += kEpiThreads) {
+          const int row = x / (D / 8), cidx = (x % (D / 8)) * 8;
+          if (it.m0 + row >= it.L) continue;
+          const uint32_t o = (cidx / C::EPC) * C::CB_BYTES + row * C::SWB + (cidx % C::EPC) * 2;
+          const uint4 w = *reinterpret_cast<const uint4*>(stage + swizzle<C::SWB>(o));
+          *reinterpret_cast<uint4*>(out + ((it.t0 + it.m0 + row) * p.Nq + it.h) * (long long)D +
+                                    cidx) = w;
+        }
+      }
+    } else if (i < it.L) {
       T16* orow = out + ((it.t0 + i) * p.Nq + it.h) * (long long)D + wg * OC;
       uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
@@ -648,6 +709,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       }
     }
   }
+  if (C::STAGE && threadIdx.x == 0) ptx::bulk_wait0();  // the last TMA store is complete
 }
 
 // ------------------------------------------------------------------ kernel
@@ -655,7 +717,7 @@ template <int D, bool BF16, bool RAB>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
-                  const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using C = Cfg<D, RAB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -681,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(ptx::smem_u32(&bars->o_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->o_empty), kEpiWarps);
+    ptx::mbar_init(ptx::smem_u32(&bars->epi_sync), kEpiWarps);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), C::P_ALIAS ? 1 : 2);  // one commit per issuer
     for (int s = 0; s < kInfoDepth; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->info_full[s]), 1);
@@ -693,6 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
     if (RAB) ptx::prefetch_tmap(&tm_r);
+    if (C::STAGE) ptx::prefetch_tmap(&tm_o);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
@@ -708,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long total = (long long)(*p.work_count) * p.Nq;
 
   if (warp < kEpiWarps) {
-    epilogue<D, BF16, RAB>(p, bars, smem, tmem, total, warp, lane);
+    epilogue<D, BF16, RAB>(p, bars, smem, tmem, &tm_o, total, warp, lane);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_k<D, RAB>(p, bars, smem, &tm_k, &tm_r, total);
   } else if (warp == kQProducerWarp) {

@@ -42,7 +42,7 @@ cudaError_t launch_fwd_simt(const FwdParams& p, int grid, cudaStream_t stream, b
 
 // bf16 / fp16 tensor-core path (tcgen05, TMA, TMEM).
 struct TcMaps {
-  CUtensorMap q, k, v, rab;
+  CUtensorMap q, k, v, rab, out;
 };
 bool tc_supported_dim(int D);
 int tc_swizzle_bytes(int D);  // row width of one TMA box / UMMA swizzle atom
