@@ -169,6 +169,7 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
                                  : swb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                              : CU_TENSOR_MAP_SWIZZLE_32B;
   const uint32_t epc = (uint32_t)(swb / 2);
+  const uint32_t oc = (uint32_t)hstu::tc_out_box_cols(d.head_dim);
   const uint64_t D = (uint64_t)d.head_dim, Nq = (uint64_t)d.num_heads_q,
                  Nk = (uint64_t)d.num_heads_kv;
   bool ok = encode3d(&P->maps.q, ty, q, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, epc, 1,
@@ -177,8 +178,11 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
                      hstu::kTileN, swz) &&
             encode3d(&P->maps.v, ty, v, D, Nk, (uint64_t)T, D * 2, Nk * D * 2, epc, 1,
                      hstu::kTileN, swz) &&
-            encode3d(&P->maps.out, ty, out, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, epc, 1,
-                     hstu::kTileM, swz);
+            encode3d(&P->maps.out, ty, out, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, oc, 1, 32,
+                     oc * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                     : oc * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                     : oc * 2 == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                    : CU_TENSOR_MAP_SWIZZLE_NONE);
   if (ok && rab) {
     const uint64_t S = (uint64_t)d.max_seqlen;
     ok = encode3d(&P->maps.rab, ty, rab, S, S, (uint64_t)d.batch * Nq, S * 2, S * S * 2, 64,

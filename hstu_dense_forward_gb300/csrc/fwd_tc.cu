@@ -55,6 +55,8 @@ bool tc_supported_dim(int D) { return D == 32 || D == 64 || D == 128 || D == 256
 
 int tc_swizzle_bytes(int D) { return D * 2 >= 128 ? 128 : D * 2; }
 
+int tc_out_box_cols(int D) { return D / tc::kEpiWG; }
+
 cudaError_t tc_prepare(int D, int bf16, int rab) {
   FwdParams p = {};
   p.D = D;

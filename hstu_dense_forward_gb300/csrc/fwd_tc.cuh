@@ -70,6 +70,9 @@ struct Cfg {
   static constexpr int NR = RAB ? ((D == 256) ? 1 : 2) : 0;
   // O is staged in shared memory and written by TMA when there is room for a tile
   static constexpr bool STAGE = D <= 64 || (D == 128 && !RAB);
+  static constexpr int OC = D / kEpiWG;              // O columns per epilogue warpgroup
+  static constexpr int OSWB = OC * 2;                // O staging row bytes (swizzle span)
+  static constexpr int WARP_STAGE = 32 * OC * 2;     // one warp's O block in shared memory
   static constexpr bool P_ALIAS = (D == 256);
   // TMEM columns
   static constexpr uint32_t S_COL0 = 0, O_COL = 256;
@@ -113,6 +116,8 @@ struct Bars {
   Item info[kInfoDepth];
   uint32_t tmem_base;
   volatile int abort;
+  volatile uint32_t s_issued;  // score tiles issued so far by the S issuer
+  volatile int s_done;         // the S issuer has issued its last tile
 };
 static_assert(sizeof(Bars) <= 1024, "barrier block");
 
@@ -453,11 +458,29 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
       ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
       if (j + 1 == it.n_kv) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
       ++k_it;
+      bars->s_issued = t + 1;
     }
     if (!ok) break;
     ++q_it;
   }
+  bars->s_done = 1;
   mma_drain(bars, p);
+}
+
+// Wait (bounded) until the S issuer has issued `n` score tiles or has no more to issue.
+__device__ __forceinline__ bool wait_issued(Bars* bars, uint32_t n, const FwdParams& p) {
+  if (bars->s_issued >= n || bars->s_done) return true;
+  const uint64_t start = ptx::globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (bars->s_issued >= n || bars->s_done) return true;
+    if (bars->abort) return false;
+    if ((long long)(ptx::globaltimer_ns() - start) > p.timeout_ns) {
+      bars->abort = 1;
+      atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 template <int D, bool BF16, bool RAB>
@@ -478,6 +501,10 @@ __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uin
       const int vs = v_it % C::NV;
       if (!wait_bar(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) { ok = false; break; }
       if (j == 0 && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) { ok = false; break; }
+      // Within an item, queue PV(t) behind S(t+2): the tensor pipe then finishes the scores
+      // the epilogue needs next before this accumulation (ordering only; correctness never
+      // depends on it).
+      if (j + 2 < it.n_kv && !wait_issued(bars, t + 3, p)) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
 #pragma unroll
@@ -533,8 +560,12 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 // (the 16-byte chunk index is XORed with the row index within each swizzle atom).
 template <int SWB>
 __device__ __forceinline__ uint32_t swizzle(uint32_t o) {
-  constexpr uint32_t mask = SWB == 128 ? 0x70u : (SWB == 64 ? 0x30u : 0x10u);
-  return o ^ ((o >> 3) & mask);
+  if constexpr (SWB <= 16) {
+    return o;  // one chunk per row: no swizzle
+  } else {
+    constexpr uint32_t mask = SWB == 128 ? 0x70u : (SWB == 64 ? 0x30u : 0x10u);
+    return o ^ ((o >> 3) & mask);
+  }
 }
 
 // Barrier among the epilogue warps (bounded: an mbarrier rather than bar.sync).
@@ -657,12 +688,13 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     warp_arrive(&bars->o_empty, lane);
     ++u;
     if constexpr (C::STAGE) {
-      // Stage the scaled tile in shared memory in the TMA box layout (swizzled 16-byte
-      // chunks, conflict-free for one row per lane), then write it with TMA when the
-      // whole tile lies inside the sequence, else with coalesced predicated stores.
-      uint8_t* stage = smem + C::OFF_O;
-      if (threadIdx.x == 0) ptx::bulk_wait_read0();  // previous tile's store has read it
-      if (!epi_barrier(bars, epi_phase, p, lane)) return;
+      // Each warp stages its own 32-row x (D/4)-column block of the scaled tile in
+      // shared memory (TMA box layout, swizzled 16-byte chunks, conflict-free for one
+      // row per lane) and writes it with one TMA store when all 32 rows lie inside the
+      // sequence; a block that crosses the end of the sequence is stored row by row.
+      uint8_t* stage = smem + C::OFF_O + warp * C::WARP_STAGE;
+      if (lane == 0) ptx::bulk_wait_read0();  // this warp's previous store has read it
+      __syncwarp();
 #pragma unroll
       for (int v4 = 0; v4 < OC / 8; ++v4) {
         uint32_t w[4];
@@ -670,30 +702,23 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         for (int e = 0; e < 4; ++e)
           w[e] = pack2<BF16>(__uint_as_float(ov[v4 * 8 + 2 * e]) * p.silu_scale,
                              __uint_as_float(ov[v4 * 8 + 2 * e + 1]) * p.silu_scale);
-        const int cidx = wg * OC + v4 * 8;
-        const uint32_t o = (cidx / C::EPC) * C::CB_BYTES + r * C::SWB + (cidx % C::EPC) * 2;
-        *reinterpret_cast<uint4*>(stage + swizzle<C::SWB>(o)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + v4 * 16)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
-      ptx::fence_proxy_async_smem();
-      if (!epi_barrier(bars, epi_phase, p, lane)) return;
-      if (it.m0 + kTileM <= it.L) {
-        if (threadIdx.x == 0) {
-#pragma unroll
-          for (int cb = 0; cb < C::NCB; ++cb)
-            ptx::tma_store_3d(tm_o, ptx::smem_u32(stage + cb * C::CB_BYTES), cb * C::EPC, it.h,
-                              (int)(it.t0 + it.m0));
+      const int row0 = it.m0 + quarter * 32;  // first row of this warp's block
+      if (row0 + 32 <= it.L) {
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_3d(tm_o, ptx::smem_u32(stage), wg * OC, it.h, (int)(it.t0 + row0));
           ptx::bulk_commit();
         }
-      } else {
-        constexpr int CHUNKS = kTileM * D / 8;  // 16-byte chunks in the tile
-        for (int x = threadIdx.x; x < CHUNKS; x += kEpiThreads) {
-          const int row = x / (D / 8), cidx = (x % (D / 8)) * 8;
-          if (it.m0 + row >= it.L) continue;
-          const uint32_t o = (cidx / C::EPC) * C::CB_BYTES + row * C::SWB + (cidx % C::EPC) * 2;
-          const uint4 w = *reinterpret_cast<const uint4*>(stage + swizzle<C::SWB>(o));
-          *reinterpret_cast<uint4*>(out + ((it.t0 + it.m0 + row) * p.Nq + it.h) * (long long)D +
-                                    cidx) = w;
-        }
+      } else if (i < it.L) {
+        uint4* dst = reinterpret_cast<uint4*>(out + ((it.t0 + i) * p.Nq + it.h) * (long long)D +
+                                              wg * OC);
+#pragma unroll
+        for (int v4 = 0; v4 < OC / 8; ++v4)
+          dst[v4] = *reinterpret_cast<const uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + v4 * 16));
       }
     } else if (i < it.L) {
       T16* orow = out + ((it.t0 + i) * p.Nq + it.h) * (long long)D + wg * OC;
@@ -709,7 +734,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       }
     }
   }
-  if (C::STAGE && threadIdx.x == 0) ptx::bulk_wait0();  // the last TMA store is complete
+  if (C::STAGE && lane == 0) ptx::bulk_wait0();  // this warp's last TMA store is complete
 }
 
 // ------------------------------------------------------------------ kernel
@@ -750,6 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), info_readers<C::P_ALIAS>());
     }
     bars->abort = 0;
+    bars->s_issued = 0;
+    bars->s_done = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
     ptx::prefetch_tmap(&tm_q);

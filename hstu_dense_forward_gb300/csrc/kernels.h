@@ -46,6 +46,7 @@ struct TcMaps {
 };
 bool tc_supported_dim(int D);
 int tc_swizzle_bytes(int D);  // row width of one TMA box / UMMA swizzle atom
+int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
 cudaError_t tc_prepare(int D, int bf16, int rab);
 cudaError_t launch_fwd_tc(const FwdParams& p, const TcMaps& maps, int bf16, int grid,
                           cudaStream_t stream, bool pdl);
