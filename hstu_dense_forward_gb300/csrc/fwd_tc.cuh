@@ -18,12 +18,12 @@
 //              B = K from smem, K-major)
 //   warp 20    one thread issues O += P(t) V(t) (tcgen05.mma, A = P from TMEM, B = V
 //              from smem, MN-major)
-//              The score issuer runs ahead: S(t+2) goes out as soon as the epilogue has
-//              read S(t), so the tensor cores compute the next scores while the epilogue
-//              works on the current ones.
-// TMEM (512 columns): S double buffer at columns 0 and 128, O at 256 (D columns),
-// P double buffer after O (D <= 128) or written over the S buffer it came from
-// (D = 256, where O takes all remaining columns).
+//              With three S buffers each issuer goes as soon as its inputs are ready:
+//              PV(t) once P(t) is written, then S(t+3) once PV(t) has read P(t); the
+//              epilogue meanwhile works on S(t+1) and S(t+2), already computed.
+// TMEM (512 columns): S buffers of 128 columns from column 0 (three for D <= 128, two
+// for D = 256), O after them (D columns). P(t) is written over the columns of S(t) the
+// writing warpgroup has already read, so S(t + NSB) waits for PV(t) to have read P(t).
 //
 // Every mbarrier wait is bounded (FwdParams::timeout_ns): on expiry the CTA
 // records HSTU_DEVERR_TIMEOUT, all roles leave their loops, the MMA queue is
@@ -73,10 +73,12 @@ struct Cfg {
   static constexpr int OC = D / kEpiWG;              // O columns per epilogue warpgroup
   static constexpr int OSWB = OC * 2;                // O staging row bytes (swizzle span)
   static constexpr int WARP_STAGE = 32 * OC * 2;     // one warp's O block in shared memory
-  static constexpr bool P_ALIAS = (D == 256);
+  // S buffers in TMEM; P is written over the S buffer it was computed from. D = 256
+  // leaves room for two (O takes 256 columns) and uses one MMA issuer; smaller D use three.
+  static constexpr int NSB = (D == 256) ? 2 : 3;
+  static constexpr bool SERIAL = (NSB == 2);
   // TMEM columns
-  static constexpr uint32_t S_COL0 = 0, O_COL = 256;
-  static constexpr uint32_t P_COL0 = O_COL + D;  // used when !P_ALIAS
+  static constexpr uint32_t S_COL0 = 0, O_COL = NSB * 128;
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
@@ -89,8 +91,7 @@ struct Cfg {
   // keep one CTA per SM (TMEM is allocated whole)
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 < 120 * 1024) ? 120 * 1024 : SMEM_USED + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(!P_ALIAS || D == 256, "alias only when O fills the spare TMEM");
-  static_assert(P_ALIAS || P_COL0 + 128 <= kTmemCols, "TMEM map");
+  static_assert(O_COL + D <= kTmemCols, "TMEM map");
 };
 
 // One work item, decoded once (by the Q producer) and read by every role.
@@ -102,22 +103,20 @@ struct Item {
 
 constexpr int kInfoDepth = 4;                   // decoded items kept in shared memory
 // item readers: epilogue warps, the MMA issuer(s), K and V producers
-template <bool P_ALIAS>
-constexpr int info_readers() { return kEpiWarps + (P_ALIAS ? 3 : 4); }
+template <bool SERIAL>
+constexpr int info_readers() { return kEpiWarps + (SERIAL ? 3 : 4); }
 
 // Barrier block layout.
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t r_full[2], r_empty[2];
-  uint64_t s_full[2], p_full[2], pv_done[2];
+  uint64_t s_full[3], p_full[3], pv_done[3];
   uint64_t o_full, o_empty, drain, epi_sync;
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   Item info[kInfoDepth];
   uint32_t tmem_base;
   volatile int abort;
-  volatile uint32_t s_issued;  // score tiles issued so far by the S issuer
-  volatile int s_done;         // the S issuer has issued its last tile
 };
 static_assert(sizeof(Bars) <= 1024, "barrier block");
 
@@ -356,8 +355,9 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
   const uint32_t sbase = ptx::smem_u32(smem);
   uint32_t q_it = 0, k_it = 0, v_it = 0, u = 0, t_base = 0;
   auto issue_s = [&](uint32_t t, int qs) -> bool {
-    const uint32_t sb = t & 1;
-    if (t >= 2 && !wait_bar(bars, &bars->pv_done[sb], ((t >> 1) & 1) ^ 1, p)) return false;
+    const uint32_t sb = t % C::NSB;
+    if (t >= C::NSB && !wait_bar(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p))
+      return false;
     const int ks = k_it % C::NK;
     if (!wait_bar(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) return false;
     ptx::tc_fence_after();
@@ -376,7 +376,7 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
     return true;
   };
   auto issue_pv = [&](uint32_t t, bool first) -> bool {
-    const uint32_t sb = t & 1;
+    const uint32_t sb = t % C::NSB;
     const int vs = v_it % C::NV;
     if (!wait_bar(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) return false;
     if (first && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) return false;
@@ -405,7 +405,7 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
     if (ok && n <= 2) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
     for (int j = 0; j < n && ok; ++j) {
       const uint32_t t = t_base + j;
-      ok = wait_bar(bars, &bars->p_full[t & 1], (t >> 1) & 1, p) && issue_pv(t, j == 0);
+      ok = wait_bar(bars, &bars->p_full[t % C::NSB], (t / C::NSB) & 1, p) && issue_pv(t, j == 0);
       if (ok && j + 2 < n) {
         ok = issue_s(t + 2, qs);
         if (ok && j + 3 == n) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
@@ -436,12 +436,11 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
     const uint32_t qa = sbase + C::OFF_Q + qs * C::TILE_BYTES;
     bool ok = true;
     for (int j = 0; j < it.n_kv && ok; ++j, ++t) {
-      const uint32_t sb = t & 1;
-      if (t >= 2) {
-        // S buffer sb is free once the epilogue has read S(t-2) (P in its own buffer)
-        // or, when P(t-2) was written over it, once PV(t-2) has read P(t-2).
-        uint64_t* bar = C::P_ALIAS ? &bars->pv_done[sb] : &bars->p_full[sb];
-        if (!wait_bar(bars, bar, ((t >> 1) & 1) ^ 1, p)) { ok = false; break; }
+      const uint32_t sb = t % C::NSB;
+      // S buffer sb holds P(t - NSB) until PV(t - NSB) has read it
+      if (t >= C::NSB && !wait_bar(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p)) {
+        ok = false;
+        break;
       }
       const int ks = k_it % C::NK;
       if (!wait_bar(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) { ok = false; break; }
@@ -458,29 +457,11 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
       ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
       if (j + 1 == it.n_kv) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
       ++k_it;
-      bars->s_issued = t + 1;
     }
     if (!ok) break;
     ++q_it;
   }
-  bars->s_done = 1;
   mma_drain(bars, p);
-}
-
-// Wait (bounded) until the S issuer has issued `n` score tiles or has no more to issue.
-__device__ __forceinline__ bool wait_issued(Bars* bars, uint32_t n, const FwdParams& p) {
-  if (bars->s_issued >= n || bars->s_done) return true;
-  const uint64_t start = ptx::globaltimer_ns();
-  for (;;) {
-    __nanosleep(64);
-    if (bars->s_issued >= n || bars->s_done) return true;
-    if (bars->abort) return false;
-    if ((long long)(ptx::globaltimer_ns() - start) > p.timeout_ns) {
-      bars->abort = 1;
-      atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_TIMEOUT);
-      return false;
-    }
-  }
 }
 
 template <int D, bool BF16, bool RAB>
@@ -496,27 +477,19 @@ __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uin
     if (!get_item(bars, k, it, p)) break;
     bool ok = true;
     for (int j = 0; j < it.n_kv; ++j, ++t) {
-      const uint32_t sb = t & 1;
-      if (!wait_bar(bars, &bars->p_full[sb], (t >> 1) & 1, p)) { ok = false; break; }
+      const uint32_t sb = t % C::NSB;
+      if (!wait_bar(bars, &bars->p_full[sb], (t / C::NSB) & 1, p)) { ok = false; break; }
       const int vs = v_it % C::NV;
       if (!wait_bar(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) { ok = false; break; }
       if (j == 0 && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) { ok = false; break; }
-      // Within an item, queue PV(t) behind S(t+2): the tensor pipe then finishes the scores
-      // the epilogue needs next before this accumulation (ordering only; correctness never
-      // depends on it).
-      if (j + 2 < it.n_kv && !wait_issued(bars, t + 3, p)) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk) {
-        uint32_t pcol;
-        // keys [16kk, 16kk + 16): with P over S, warpgroup 16kk / kColsPerWG wrote them
-        // packed at the start of its own S columns
-        if constexpr (C::P_ALIAS)
-          pcol = C::S_COL0 + sb * 128 + (16 * kk / kColsPerWG) * kColsPerWG +
-                 ((16 * kk) % kColsPerWG) / 2;
-        else
-          pcol = C::P_COL0 + sb * 64 + kk * 8;
+        // keys [16kk, 16kk + 16): warpgroup 16kk / kColsPerWG wrote them packed at the
+        // start of its own S columns
+        const uint32_t pcol = C::S_COL0 + sb * 128 + (16 * kk / kColsPerWG) * kColsPerWG +
+                              ((16 * kk) % kColsPerWG) / 2;
         const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
         ptx::mma_ts(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
       }
@@ -601,8 +574,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     const int i = it.m0 + r;
     const RowRange rr = row_range(it.geom, i, p.mask_type);
     for (int j = 0; j < it.n_kv; ++j, ++t) {
-      const uint32_t sb = t & 1;
-      if (!warp_wait(bars, &bars->s_full[sb], (t >> 1) & 1, p)) return;
+      const uint32_t sb = t % C::NSB;
+      if (!warp_wait(bars, &bars->s_full[sb], (t / C::NSB) & 1, p)) return;
       ptx::tc_fence_after();
       const int n0 = j * kTileN;
       const bool full = tile_all_valid(it.geom, it.m0, kTileM, n0, kTileN, p.mask_type);
@@ -657,13 +630,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           else
             pk[e] = ptx::fma_f16x2(h2, ptx::tanh_f16x2(h2), h2);
         }
-        const uint32_t pcol = C::P_ALIAS ? C::S_COL0 + sb * 128 + col + c * 16
-                                         : C::P_COL0 + sb * 64 + cc / 2;
-        if constexpr (!C::P_ALIAS) {  // P buffer sb is free once PV(t-2) has read it
-          if (c == 0 && t >= 2 && !warp_wait(bars, &bars->pv_done[sb], ((t >> 1) & 1) ^ 1, p))
-            return;
-        }
-        ptx::tmem_st16(tmem + lane_off + pcol, pk);
+        // P over the S columns this warpgroup has already read
+        ptx::tmem_st16(tmem + lane_off + C::S_COL0 + sb * 128 + col + c * 16, pk);
       }
       if constexpr (RAB) {
         warp_arrive(&bars->r_empty[rs], lane);
@@ -751,14 +719,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == kProducerWarp && lane == 0) {
+    for (int s = 0; s < 3; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&bars->s_full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars->p_full[s]), kEpiWarps);
+      ptx::mbar_init(ptx::smem_u32(&bars->pv_done[s]), 1);
+    }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->q_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->q_empty[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->r_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->r_empty[s]), kEpiWarps);
-      ptx::mbar_init(ptx::smem_u32(&bars->s_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->p_full[s]), kEpiWarps);
-      ptx::mbar_init(ptx::smem_u32(&bars->pv_done[s]), 1);
     }
     for (int s = 0; s < 4; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->k_full[s]), 1);
@@ -769,14 +739,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(ptx::smem_u32(&bars->o_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->o_empty), kEpiWarps);
     ptx::mbar_init(ptx::smem_u32(&bars->epi_sync), kEpiWarps);
-    ptx::mbar_init(ptx::smem_u32(&bars->drain), C::P_ALIAS ? 1 : 2);  // one commit per issuer
+    ptx::mbar_init(ptx::smem_u32(&bars->drain), C::SERIAL ? 1 : 2);  // one commit per issuer
     for (int s = 0; s < kInfoDepth; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->info_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), info_readers<C::P_ALIAS>());
+      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), info_readers<C::SERIAL>());
     }
     bars->abort = 0;
-    bars->s_issued = 0;
-    bars->s_done = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
     ptx::prefetch_tmap(&tm_q);
@@ -808,13 +776,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) producer_v<D, RAB>(p, bars, smem, &tm_v, total);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      if constexpr (C::P_ALIAS)
+      if constexpr (C::SERIAL)
         mma_serial_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
       else
         mma_s_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
     }
   } else if (warp == kPvWarp) {
-    if (lane == 0 && !C::P_ALIAS) mma_pv_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+    if (lane == 0 && !C::SERIAL) mma_pv_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
   }
   __syncwarp();
   ptx::tc_fence_before();
