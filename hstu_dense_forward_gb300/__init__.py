@@ -20,7 +20,8 @@ import torch
 from . import _abi
 from ._abi import HstuError
 
-__all__ = ["hstu_fwd", "HstuFwdPlan", "HstuError", "count_pairs", "useful_flops"]
+__all__ = ["hstu_fwd", "hstu_fwd_noalloc", "HstuFwdPlan", "HstuError", "count_pairs",
+           "useful_flops"]
 
 _DTYPES = {torch.float32: _abi.HSTU_F32, torch.float16: _abi.HSTU_F16,
            torch.bfloat16: _abi.HSTU_BF16}
@@ -171,6 +172,34 @@ def hstu_fwd(q, k, v, seq_offsets, *, max_seqlen, rab=None, num_context=None, nu
     with torch.cuda.device(dev):
         plan.run(q, k, v, seq_offsets, out, rab=rab, num_context=num_context,
                  num_targets=num_targets, alpha=alpha, silu_scale=silu_scale, stream=stream)
+    return out
+
+
+def hstu_fwd_noalloc(q, k, v, seq_offsets, out, *, max_seqlen, rab=None, num_context=None,
+                     num_targets=None, causal=True, target_group_size=0, alpha=1.0,
+                     silu_scale=None):
+    """hstu_fwd through the library's allocation-free entry point (hstu_fwd_run_noalloc):
+    no plan, the work list lives in a fixed device array of the library. `out` must be
+    given (this call allocates nothing, torch included). Calls that may overlap on the GPU
+    share that array and must be serialised by the caller."""
+    dev = q.device
+    for name, t in (("k", k), ("v", v), ("out", out)):
+        _check_tensor(t, name, q.dtype, dev, 3)
+    _check_tensor(q, "q", None, dev, 3)
+    d = _desc(dtype=q.dtype, batch=seq_offsets.shape[0] - 1, num_heads_q=q.shape[1],
+              num_heads_kv=k.shape[1], head_dim=q.shape[2], max_seqlen=max_seqlen,
+              index_is_int64=seq_offsets.dtype == torch.int64, causal=causal,
+              target_group_size=target_group_size, has_rab=rab is not None,
+              has_num_context=num_context is not None, has_num_targets=num_targets is not None)
+    if silu_scale is None:
+        silu_scale = 1.0 / max_seqlen
+    ptr = lambda t: None if t is None else t.data_ptr()
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev)
+        _abi.check(_abi.lib().hstu_fwd_run_noalloc(
+            ctypes.byref(d), q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_offsets.data_ptr(),
+            ptr(rab), ptr(num_context), ptr(num_targets), q.shape[0], float(alpha),
+            float(silu_scale), out.data_ptr(), stream.cuda_stream), "hstu_fwd_run_noalloc")
     return out
 
 

@@ -78,6 +78,9 @@ def lib():
         L.hstu_fwd_count_pairs.restype = ctypes.c_int
         L.hstu_fwd_count_pairs.argtypes = [ctypes.POINTER(Desc), vp, vp, vp,
                                            ctypes.POINTER(ctypes.c_longlong)]
+        L.hstu_fwd_run_noalloc.restype = ctypes.c_int
+        L.hstu_fwd_run_noalloc.argtypes = [ctypes.POINTER(Desc), vp, vp, vp, vp, vp, vp, vp, ll, f,
+                                           f, vp, vp]
         L.hstu_status_string.restype = ctypes.c_char_p
         L.hstu_status_string.argtypes = [ctypes.c_int]
         _lib = L

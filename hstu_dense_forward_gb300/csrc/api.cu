@@ -312,4 +312,148 @@ hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* d, const void* seq_offsets
   return HSTU_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Entry point that allocates nothing: the work list lives in this file-scope device
+// array instead of a plan's cudaMalloc'ed workspace. Layout (32-bit words):
+// [0] entry count, [1] device error word, [64 ..] work-list entries.
+// ---------------------------------------------------------------------------
+#define HSTU_NOALLOC_MAX_ENTRIES 16384  // (sequence, 128-row query tile) pairs
+static __device__ __align__(256) uint32_t g_noalloc_scratch[64 + HSTU_NOALLOC_MAX_ENTRIES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+uint32_t* g_noalloc_ptr[kMaxDevices];   // device address of the array, per device
+int g_noalloc_sms[kMaxDevices];
+uint32_t g_noalloc_prepared[kMaxDevices];  // kernel variants configured (bit per variant)
+
+// Per-device set-up, run by the first call on each device with that device current.
+cudaError_t noalloc_setup(int dev, const hstu_fwd_desc& d, uint32_t** scratch, int* sms) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&g_noalloc_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = static_cast<uint32_t*>(ptr);
+  }
+  // shared-memory opt-in of the kernel variant this descriptor uses
+  int bit = 0;
+  if (d.dtype != HSTU_F32) {
+    const int di = d.head_dim == 32 ? 0 : d.head_dim == 64 ? 1 : d.head_dim == 128 ? 2 : 3;
+    bit = 1 + di * 4 + (d.dtype == HSTU_BF16 ? 2 : 0) + (d.has_rab ? 1 : 0);
+  }
+  if (!(g_noalloc_prepared[dev] & (1u << bit))) {
+    cudaError_t e = d.dtype == HSTU_F32
+                        ? hstu::simt_prepare()
+                        : hstu::tc_prepare(d.head_dim, d.dtype == HSTU_BF16, d.has_rab);
+    if (e != cudaSuccess) return e;
+    g_noalloc_prepared[dev] |= 1u << bit;
+  }
+  *scratch = g_noalloc_ptr[dev];
+  *sms = g_noalloc_sms[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const void* k,
+                                 const void* v, const void* seq_offsets, const void* rab,
+                                 const void* num_context, const void* num_targets,
+                                 long long total_tokens, float alpha, float silu_scale, void* out,
+                                 void* stream) {
+  hstu_status st = validate_desc(desc);
+  if (st != HSTU_OK) return st;
+  const hstu_fwd_desc& d = *desc;
+  if (total_tokens < 0 || total_tokens > 0x7fffffffll) return HSTU_ERR_INVALID_ARG;
+  if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
+  if ((long long)d.batch * hstu::ceil_div(d.max_seqlen, hstu::kTileM) > HSTU_NOALLOC_MAX_ENTRIES)
+    return HSTU_ERR_UNSUPPORTED;  // work list larger than the static scratch array
+  if (!q || !k || !v || !seq_offsets || !out) return HSTU_ERR_INVALID_ARG;
+  if ((rab != nullptr) != (d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
+  if ((num_context != nullptr) != (d.has_num_context != 0)) return HSTU_ERR_INVALID_ARG;
+  if ((num_targets != nullptr) != (d.has_num_targets != 0)) return HSTU_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (rab && !aligned16(rab)))
+    return HSTU_ERR_INVALID_ARG;
+  const bool tc = d.dtype != HSTU_F32;
+  if (tc && !encode_fn()) return HSTU_ERR_UNSUPPORTED;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HSTU_ERR_CUDA;
+  if (tc) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) return HSTU_ERR_UNSUPPORTED;
+  }
+  uint32_t* scratch = nullptr;
+  int sms = 0;
+  if (noalloc_setup(dev, d, &scratch, &sms) != cudaSuccess) return HSTU_ERR_CUDA;
+  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+
+  FwdParams p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.rab = rab;
+  p.out = out;
+  p.seq_offsets = seq_offsets;
+  p.num_context = num_context;
+  p.num_targets = num_targets;
+  p.work = scratch + 64;
+  p.work_count = reinterpret_cast<int*>(scratch);
+  p.err = reinterpret_cast<int*>(scratch) + 1;
+  p.total_tokens = total_tokens;
+  p.timeout_ns = (long long)(d.watchdog_ms > 0 ? d.watchdog_ms : 1000) * 1000000ll;
+  p.index64 = d.index_is_int64 ? 1 : 0;
+  p.B = d.batch;
+  p.Nq = d.num_heads_q;
+  p.Nk = d.num_heads_kv;
+  p.D = d.head_dim;
+  p.S = d.max_seqlen;
+  p.mask_type = d.mask_type;
+  p.g = d.mask_type == HSTU_MASK_CAUSAL ? d.target_group_size : 0;
+  p.alpha = alpha;
+  p.silu_scale = silu_scale;
+
+  TcMaps maps;
+  if (tc) {
+    const CUtensorMapDataType ty =
+        d.dtype == HSTU_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int swb = hstu::tc_swizzle_bytes(d.head_dim);
+    const CUtensorMapSwizzle swz = swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : swb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+    const uint32_t epc = (uint32_t)(swb / 2);
+    const uint32_t oc = (uint32_t)hstu::tc_out_box_cols(d.head_dim);
+    const uint64_t D = (uint64_t)d.head_dim, Nq = (uint64_t)d.num_heads_q,
+                   Nk = (uint64_t)d.num_heads_kv, T = (uint64_t)total_tokens;
+    bool ok = encode3d(&maps.q, ty, q, D, Nq, T, D * 2, Nq * D * 2, epc, 1, hstu::kTileM, swz) &&
+              encode3d(&maps.k, ty, k, D, Nk, T, D * 2, Nk * D * 2, epc, 1, hstu::kTileN, swz) &&
+              encode3d(&maps.v, ty, v, D, Nk, T, D * 2, Nk * D * 2, epc, 1, hstu::kTileN, swz) &&
+              encode3d(&maps.out, ty, out, D, Nq, T, D * 2, Nq * D * 2, oc, 1, 32,
+                       oc * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                       : oc * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                       : oc * 2 == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                      : CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (ok && rab) {
+      const uint64_t S = (uint64_t)d.max_seqlen;
+      ok = encode3d(&maps.rab, ty, rab, S, S, (uint64_t)d.batch * Nq, S * 2, S * S * 2, 64,
+                    hstu::kTileM, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+    } else if (ok) {
+      maps.rab = maps.q;  // unused by the kernel
+    }
+    if (!ok) return HSTU_ERR_INVALID_ARG;
+  }
+  // the error word keeps the previous call's value: clear it (the count is rewritten)
+  if (cudaMemsetAsync(p.err, 0, sizeof(int), st_) != cudaSuccess) return HSTU_ERR_CUDA;
+  if (hstu::launch_build_worklist(p, scratch + 64, reinterpret_cast<int*>(scratch),
+                                  hstu::kTileM, st_) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+  const int grid = tc ? sms : sms * (d.head_dim <= 64 ? 4 : (d.head_dim <= 128 ? 2 : 1));
+  cudaError_t e = tc ? hstu::launch_fwd_tc(p, maps, d.dtype == HSTU_BF16, grid, st_, true)
+                     : hstu::launch_fwd_simt(p, grid, st_, true);
+  return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
 }  // extern "C"

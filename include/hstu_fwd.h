@@ -143,6 +143,34 @@ HSTU_API hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* desc, const void*
                                  const void* num_context_host, const void* num_targets_host,
                                  long long* pairs);
 
+/*
+ * Same forward as hstu_fwd_run, without a plan and without allocating anything.
+ * The source pages have no counterpart to this entry point: it exists for callers
+ * that cannot call cudaMalloc, such as a plugin that its host framework only hands
+ * input and output buffers, a runtime whose memory pool has already reserved all
+ * device memory, or a latency-critical path that must not pay for cudaMalloc's
+ * implicit device synchronisation.
+ *   - The work list lives in a fixed device array inside the library (about 64 KB,
+ *     held by every GPU that loads the library until the process exits). It has room
+ *     for batch * ceil(max_seqlen / 128) <= 16384 entries; larger descriptors return
+ *     HSTU_ERR_UNSUPPORTED without launching anything.
+ *   - Arguments, layouts and ownership are those of hstu_fwd_run; desc is validated
+ *     like hstu_fwd_create validates it, on every call.
+ *   - The first call on a device (with that device current) looks up the array's
+ *     device address and configures the kernels for that device; make that first
+ *     call before any stream capture.
+ *   - All calls share the one array: calls whose kernels may overlap on the GPU
+ *     (different streams without ordering, several host threads) race and produce
+ *     wrong results. Serialise them.
+ *   - Device-detected input errors (invalid seq_offsets) leave out unwritten but are
+ *     not reported back; use a plan and hstu_fwd_get_error when they must be.
+ */
+HSTU_API hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const void* k,
+                                          const void* v, const void* seq_offsets, const void* rab,
+                                          const void* num_context, const void* num_targets,
+                                          long long total_tokens, float alpha, float silu_scale,
+                                          void* out, void* stream);
+
 /* Static description of a status code. */
 HSTU_API const char* hstu_status_string(hstu_status status);
 
