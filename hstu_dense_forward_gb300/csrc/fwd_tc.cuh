@@ -101,7 +101,7 @@ struct Item {
   SeqGeom geom;
 };
 
-constexpr int kInfoDepth = 4;                   // decoded items kept in shared memory
+constexpr int kInfoDepth = 8;                   // decoded items kept in shared memory
 // item readers: epilogue warps, the MMA issuer(s), K and V producers
 template <bool SERIAL>
 constexpr int info_readers() { return kEpiWarps + (SERIAL ? 3 : 4); }
@@ -186,17 +186,6 @@ __device__ __forceinline__ bool get_item(Bars* bars, int k, Item& it, const FwdP
   if (!wait_bar(bars, &bars->info_full[s], (k / kInfoDepth) & 1, p)) return false;
   it = bars->info[s];
   ptx::mbar_arrive(ptx::smem_u32(&bars->info_empty[s]));
-  return true;
-}
-
-// Whole-warp reader (one arrival per warp).
-__device__ __forceinline__ bool get_item_warp(Bars* bars, int k, Item& it, const FwdParams& p,
-                                              int lane) {
-  const int s = k % kInfoDepth;
-  if (!warp_wait(bars, &bars->info_full[s], (k / kInfoDepth) & 1, p)) return false;
-  it = bars->info[s];
-  __syncwarp();
-  if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->info_empty[s]));
   return true;
 }
 
@@ -565,12 +554,76 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   const float half_alpha = 0.5f * p.alpha;
   uint32_t t = 0, u = 0, r_it = 0, epi_phase = 0;
   T16* out = static_cast<T16*>(p.out);
+  int prev_slot = -1;  // item ring slot of the item whose O is still in TMEM
+  // Output of a finished item: read this warpgroup's O columns chunk by chunk, scale,
+  // stage (or store), release O, then write the staged block. Called after P of the next
+  // item's first tile has been written, so that the epilogue is not idle while the item's
+  // last accumulation completes. The item stays in its ring slot until this returns.
+  auto drain = [&](int slot) -> bool {
+    const Item& pit = bars->info[slot];
+    const int pi = pit.m0 + r;
+    if (!warp_wait(bars, &bars->o_full, u & 1, p)) return false;
+    ptx::tc_fence_after();
+    uint8_t* stage = smem + C::OFF_O + warp * C::WARP_STAGE;
+    if constexpr (C::STAGE) {
+      if (lane == 0) ptx::bulk_wait_read0();  // this warp's previous store has read it
+      __syncwarp();
+    }
+    T16* orow = out + ((pit.t0 + pi) * p.Nq + pit.h) * (long long)D + wg * OC;
+#pragma unroll
+    for (int c0 = 0; c0 < OC; c0 += OCH) {
+      uint32_t part[OCH];
+      tmem_ld<OCH>(tmem + lane_off + C::O_COL + wg * OC + c0, part);
+#pragma unroll
+      for (int v4 = 0; v4 < OCH / 8; ++v4) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          w[e] = pack2<BF16>(__uint_as_float(part[v4 * 8 + 2 * e]) * p.silu_scale,
+                             __uint_as_float(part[v4 * 8 + 2 * e + 1]) * p.silu_scale);
+        if constexpr (C::STAGE) {
+          // this warp's 32-row x (D/4)-column block in the TMA box layout: swizzled 16-byte
+          // chunks, conflict-free for one row per lane
+          *reinterpret_cast<uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + c0 * 2 + v4 * 16)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        } else if (pi < pit.L) {
+          reinterpret_cast<uint4*>(orow + c0)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    ptx::tc_fence_before();
+    warp_arrive(&bars->o_empty, lane);
+    ++u;
+    if constexpr (C::STAGE) {
+      // one TMA store when all 32 rows of the block lie inside the sequence; a block that
+      // crosses the end of the sequence is stored row by row
+      const int row0 = pit.m0 + quarter * 32;
+      if (row0 + 32 <= pit.L) {
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_3d(tm_o, ptx::smem_u32(stage), wg * OC, pit.h, (int)(pit.t0 + row0));
+          ptx::bulk_commit();
+        }
+      } else if (pi < pit.L) {
+#pragma unroll
+        for (int v4 = 0; v4 < OC / 8; ++v4)
+          reinterpret_cast<uint4*>(orow)[v4] =
+              *reinterpret_cast<const uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + v4 * 16));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->info_empty[slot]));
+    return true;
+  };
 
   for (int k = 0;; ++k) {
     const long long idx = item_index(k);
     if (idx >= total) break;
-    Item it;
-    if (!get_item_warp(bars, k, it, p, lane)) return;
+    // the item is released by drain() once its O has been written
+    const int slot = k % kInfoDepth;
+    if (!warp_wait(bars, &bars->info_full[slot], (k / kInfoDepth) & 1, p)) return;
+    const Item it = bars->info[slot];
     const int i = it.m0 + r;
     const RowRange rr = row_range(it.geom, i, p.mask_type);
     for (int j = 0; j < it.n_kv; ++j, ++t) {
@@ -640,68 +693,14 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       warp_arrive(&bars->p_full[sb], lane);
-    }
-    // output tile: read this warpgroup's O columns, release O, then scale and store
-    if (!warp_wait(bars, &bars->o_full, u & 1, p)) return;
-    ptx::tc_fence_after();
-    uint32_t ov[OC];
-#pragma unroll
-    for (int c0 = 0; c0 < OC; c0 += OCH) {
-      uint32_t part[OCH];
-      tmem_ld<OCH>(tmem + lane_off + C::O_COL + wg * OC + c0, part);
-#pragma unroll
-      for (int e = 0; e < OCH; ++e) ov[c0 + e] = part[e];
-    }
-    ptx::tc_fence_before();
-    warp_arrive(&bars->o_empty, lane);
-    ++u;
-    if constexpr (C::STAGE) {
-      // Each warp stages its own 32-row x (D/4)-column block of the scaled tile in
-      // shared memory (TMA box layout, swizzled 16-byte chunks, conflict-free for one
-      // row per lane) and writes it with one TMA store when all 32 rows lie inside the
-      // sequence; a block that crosses the end of the sequence is stored row by row.
-      uint8_t* stage = smem + C::OFF_O + warp * C::WARP_STAGE;
-      if (lane == 0) ptx::bulk_wait_read0();  // this warp's previous store has read it
-      __syncwarp();
-#pragma unroll
-      for (int v4 = 0; v4 < OC / 8; ++v4) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = pack2<BF16>(__uint_as_float(ov[v4 * 8 + 2 * e]) * p.silu_scale,
-                             __uint_as_float(ov[v4 * 8 + 2 * e + 1]) * p.silu_scale);
-        *reinterpret_cast<uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + v4 * 16)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      const int row0 = it.m0 + quarter * 32;  // first row of this warp's block
-      if (row0 + 32 <= it.L) {
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          ptx::tma_store_3d(tm_o, ptx::smem_u32(stage), wg * OC, it.h, (int)(it.t0 + row0));
-          ptx::bulk_commit();
-        }
-      } else if (i < it.L) {
-        uint4* dst = reinterpret_cast<uint4*>(out + ((it.t0 + i) * p.Nq + it.h) * (long long)D +
-                                              wg * OC);
-#pragma unroll
-        for (int v4 = 0; v4 < OC / 8; ++v4)
-          dst[v4] = *reinterpret_cast<const uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + v4 * 16));
-      }
-    } else if (i < it.L) {
-      T16* orow = out + ((it.t0 + i) * p.Nq + it.h) * (long long)D + wg * OC;
-      uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-      for (int v4 = 0; v4 < OC / 8; ++v4) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = pack2<BF16>(__uint_as_float(ov[v4 * 8 + 2 * e]) * p.silu_scale,
-                             __uint_as_float(ov[v4 * 8 + 2 * e + 1]) * p.silu_scale);
-        dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+      if (j == 0 && prev_slot >= 0) {  // the previous item's O, now that this P is queued
+        if (!drain(prev_slot)) return;
+        prev_slot = -1;
       }
     }
+    prev_slot = slot;
   }
+  if (prev_slot >= 0 && !drain(prev_slot)) return;
   if (C::STAGE && lane == 0) ptx::bulk_wait0();  // this warp's last TMA store is complete
 }
 
