@@ -189,6 +189,16 @@ __device__ __forceinline__ bool get_item(Bars* bars, int k, Item& it, const FwdP
   return true;
 }
 
+// Bits e (0..31) set where column base + e is valid for the row (RowRange intervals).
+__device__ __forceinline__ uint32_t low_bits(int n) {  // n lowest bits, n clamped to [0, 32]
+  return n <= 0 ? 0u : (n >= 32 ? 0xffffffffu : ((1u << n) - 1u));
+}
+__device__ __forceinline__ uint32_t chunk_mask(const RowRange& r, int base) {
+  const uint32_t hist = low_bits(r.hist_end - base);
+  const uint32_t grp = low_bits(r.grp_hi - base + 1) & ~low_bits(r.grp_lo - base);
+  return r.grp_lo <= r.grp_hi ? (hist | grp) : hist;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if constexpr (BF16) {
@@ -670,9 +680,12 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         // 16-bit type, tanh runs on packed pairs and p = h*t + h is one packed fused
         // multiply-add that yields P directly.
         if (!full) {
+          // valid columns of this row form [0, hist_end) U [grp_lo, grp_hi]: as a bit mask
+          // over the 32 columns of the chunk
+          const uint32_t m = chunk_mask(rr, n0 + cc);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (!valid_in_range(rr, n0 + cc + e)) x[e] = 0.f;
+            if (!(m & (1u << e))) x[e] = 0.f;
         }
         uint32_t pk[16];
 #pragma unroll
@@ -693,7 +706,9 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       warp_arrive(&bars->p_full[sb], lane);
-      if (j == 0 && prev_slot >= 0) {  // the previous item's O, now that this P is queued
+      // the previous item's O, once two more P tiles are queued behind its last one (by
+      // then its last accumulation has finished), or at the last tile of this item
+      if (prev_slot >= 0 && (j == 1 || j + 1 == it.n_kv)) {
         if (!drain(prev_slot)) return;
         prev_slot = -1;
       }
