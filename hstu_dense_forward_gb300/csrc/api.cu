@@ -128,10 +128,10 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
   const size_t mtiles = (size_t)hstu::ceil_div(desc->max_seqlen, hstu::kTileM);
   const size_t entries = (size_t)(desc->batch > 0 ? desc->batch : 1) * mtiles;
   if (e == cudaSuccess) e = cudaMalloc(&P->d_work, entries * sizeof(uint32_t));
-  if (e == cudaSuccess) e = cudaMalloc(&P->d_count, 2 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMalloc(&P->d_count, 3 * sizeof(int));
   if (e == cudaSuccess) {
-    P->d_err = P->d_count + 1;
-    e = cudaMemset(P->d_count, 0, 2 * sizeof(int));
+    P->d_err = P->d_count + 1;  // [0] count, [1] error word, [2] scheduling counter
+    e = cudaMemset(P->d_count, 0, 3 * sizeof(int));
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -230,6 +230,7 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
   p.num_targets = num_targets;
   p.work = P->d_work;
   p.work_count = P->d_count;
+  p.next_item = P->d_count + 2;
   p.err = P->d_err;
   p.total_tokens = total_tokens;
   p.timeout_ns = P->timeout_ns;
@@ -315,7 +316,7 @@ hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* d, const void* seq_offsets
 // ---------------------------------------------------------------------------
 // Entry point that allocates nothing: the work list lives in this file-scope device
 // array instead of a plan's cudaMalloc'ed workspace. Layout (32-bit words):
-// [0] entry count, [1] device error word, [64 ..] work-list entries.
+// [0] entry count, [1] device error word, [2] scheduling counter, [64 ..] work-list entries.
 // ---------------------------------------------------------------------------
 #define HSTU_NOALLOC_MAX_ENTRIES 16384  // (sequence, 128-row query tile) pairs
 static __device__ __align__(256) uint32_t g_noalloc_scratch[64 + HSTU_NOALLOC_MAX_ENTRIES];
@@ -403,6 +404,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   p.work = scratch + 64;
   p.work_count = reinterpret_cast<int*>(scratch);
   p.err = reinterpret_cast<int*>(scratch) + 1;
+  p.next_item = reinterpret_cast<int*>(scratch) + 2;
   p.total_tokens = total_tokens;
   p.timeout_ns = (long long)(d.watchdog_ms > 0 ? d.watchdog_ms : 1000) * 1000000ll;
   p.index64 = d.index_is_int64 ? 1 : 0;

@@ -135,13 +135,6 @@ __device__ __forceinline__ bool decode_item(const FwdParams& p, long long idx, I
   return true;
 }
 
-// k-th item of this CTA: snake order over the (heaviest-first) list, so that
-// every CTA gets a mix of long and short items.
-__device__ __forceinline__ long long item_index(int k) {
-  const long long G = gridDim.x;
-  const long long c = (k & 1) ? (G - 1 - blockIdx.x) : blockIdx.x;
-  return (long long)k * G + c;
-}
 
 // Bounded wait. Returns false when this CTA is aborting (own timeout or another role's).
 __device__ __forceinline__ bool wait_bar(Bars* bars, uint64_t* bar, uint32_t parity,
@@ -232,18 +225,29 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   using C = Cfg<D, RAB>;
   uint32_t q_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
+  // Items are claimed dynamically from the heaviest-first list (one atomic per item);
+  // with a single Q buffer the next item is claimed one early so that its Q tile can be
+  // prefetched into L2.
+  long long idx = atomicAdd(p.next_item, 1);
   for (int k = 0;; ++k) {
-    const long long idx = item_index(k);
-    if (idx >= total) break;
     Item it;
+    if (idx >= total) {  // no work left: publish the end marker
+      it.n_kv = -1;
+      put_item(bars, k, it, p);
+      return;
+    }
     decode_item(p, idx, it);
     if (!put_item(bars, k, it, p)) return;
-    if (C::NQ == 1 && item_index(k + 1) < total) {
-      Item nx;
-      decode_item(p, item_index(k + 1), nx);
+    long long nidx = -1;
+    if (C::NQ == 1) {
+      nidx = atomicAdd(p.next_item, 1);
+      if (nidx < total) {
+        Item nx;
+        decode_item(p, nidx, nx);
 #pragma unroll
-      for (int cb = 0; cb < C::NCB; ++cb)
-        ptx::tma_prefetch_3d(tq, cb * C::EPC, nx.h, (int)(nx.t0 + nx.m0));
+        for (int cb = 0; cb < C::NCB; ++cb)
+          ptx::tma_prefetch_3d(tq, cb * C::EPC, nx.h, (int)(nx.t0 + nx.m0));
+      }
     }
     const int s = q_it % C::NQ;
     if (!wait_bar(bars, &bars->q_empty[s], ((q_it / C::NQ) & 1) ^ 1, p)) return;
@@ -254,6 +258,7 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
     for (int cb = 0; cb < C::NCB; ++cb)
       ptx::tma_load_3d(dst + cb * C::CB_BYTES, tq, full, cb * C::EPC, it.h, (int)(it.t0 + it.m0));
     ++q_it;
+    idx = C::NQ == 1 ? nidx : atomicAdd(p.next_item, 1);
   }
 }
 
@@ -264,10 +269,8 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   uint32_t k_it = 0, r_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   for (int k = 0;; ++k) {
-    const long long idx = item_index(k);
-    if (idx >= total) break;
     Item it;
-    if (!get_item(bars, k, it, p)) return;
+    if (!get_item(bars, k, it, p) || it.n_kv < 0) return;
     for (int j = 0; j < it.n_kv; ++j) {
       const int s = k_it % C::NK;
       const int row = (int)(it.t0 + j * kTileN);
@@ -303,10 +306,8 @@ __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   uint32_t v_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   for (int k = 0;; ++k) {
-    const long long idx = item_index(k);
-    if (idx >= total) break;
     Item it;
-    if (!get_item(bars, k, it, p)) return;
+    if (!get_item(bars, k, it, p) || it.n_kv < 0) return;
     for (int j = 0; j < it.n_kv; ++j) {
       const int s = v_it % C::NV;
       if (!wait_bar(bars, &bars->v_empty[s], ((v_it / C::NV) & 1) ^ 1, p)) return;
@@ -394,9 +395,8 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
     return true;
   };
   for (int k = 0;; ++k) {
-    if (item_index(k) >= total) break;
     Item it;
-    if (!get_item(bars, k, it, p)) break;
+    if (!get_item(bars, k, it, p) || it.n_kv < 0) break;
     const int qs = q_it % C::NQ;
     if (!wait_bar(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) break;
     const int n = it.n_kv;
@@ -427,9 +427,8 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
   const uint32_t sbase = ptx::smem_u32(smem);
   uint32_t q_it = 0, k_it = 0, t = 0;
   for (int k = 0;; ++k) {
-    if (item_index(k) >= total) break;
     Item it;
-    if (!get_item(bars, k, it, p)) break;
+    if (!get_item(bars, k, it, p) || it.n_kv < 0) break;
     const int qs = q_it % C::NQ;
     if (!wait_bar(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) break;
     const uint32_t qa = sbase + C::OFF_Q + qs * C::TILE_BYTES;
@@ -471,9 +470,8 @@ __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uin
   const uint32_t sbase = ptx::smem_u32(smem);
   uint32_t v_it = 0, t = 0, u = 0;
   for (int k = 0;; ++k) {
-    if (item_index(k) >= total) break;
     Item it;
-    if (!get_item(bars, k, it, p)) break;
+    if (!get_item(bars, k, it, p) || it.n_kv < 0) break;
     bool ok = true;
     for (int j = 0; j < it.n_kv; ++j, ++t) {
       const uint32_t sb = t % C::NSB;
@@ -628,12 +626,11 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   };
 
   for (int k = 0;; ++k) {
-    const long long idx = item_index(k);
-    if (idx >= total) break;
     // the item is released by drain() once its O has been written
     const int slot = k % kInfoDepth;
     if (!warp_wait(bars, &bars->info_full[slot], (k / kInfoDepth) & 1, p)) return;
     const Item it = bars->info[slot];
+    if (it.n_kv < 0) break;  // end marker
     const int i = it.m0 + r;
     const RowRange rr = row_range(it.geom, i, p.mask_type);
     for (int j = 0; j < it.n_kv; ++j, ++t) {

@@ -18,6 +18,7 @@ struct FwdParams {
   const void* num_targets;  // [B] or nullptr
   const uint32_t* work;     // work list: packed (b, m-tile), heaviest first
   const int* work_count;    // number of list entries
+  int* next_item;           // dynamic scheduling counter (reset by the work-list builder)
   int* err;                 // device error word (HSTU_DEVERR_*)
   long long total_tokens;   // T
   long long timeout_ns;     // limit of one pipeline wait

@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
     if (a < 0 || e < a || e > T || e - a > p.S) bad = 1;
   }
   __syncthreads();
+  if (threadIdx.x == 0) *p.next_item = 0;  // the forward kernel claims items from 0
   if (bad) {
     if (threadIdx.x == 0) {
       *work_count = 0;
