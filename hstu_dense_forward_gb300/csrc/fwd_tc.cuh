@@ -204,14 +204,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 template <bool BF16>
-__device__ __forceinline__ float2 unpack2(uint32_t w) {
-  if constexpr (BF16) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w);
-    return __bfloat1622float2(v);
-  } else {
-    __half2 v = *reinterpret_cast<__half2*>(&w);
-    return __half22float2(v);
-  }
+__device__ __forceinline__ uint32_t tanh2(uint32_t x) {
+  if constexpr (BF16)
+    return ptx::tanh_bf16x2(x);
+  else
+    return ptx::tanh_f16x2(x);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
+  if constexpr (BF16)
+    return ptx::fma_bf16x2(a, b, c);
+  else
+    return ptx::fma_f16x2(a, b, c);
 }
 
 // ------------------------------------------------------------------ producers
@@ -651,10 +656,14 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         const int cc = col + c * 32;  // first S column of this 32-column chunk
         uint32_t sv[32];
         ptx::tmem_ld32(tmem + lane_off + C::S_COL0 + sb * 128 + cc, sv);
-        float x[32];
+        uint32_t pk[16];
         if constexpr (RAB) {
-          // rab tile: two 64-column TMA boxes of 128 rows x 128 bytes, 128-byte swizzle
+          // rab tile: two 64-column TMA boxes of 128 rows x 128 bytes, 128-byte swizzle.
+          // h = alpha*s/2 is rounded to the 16-bit type and rab/2 is added in packed
+          // form (one fused multiply-add per pair); a masked pair half becomes 0.
           const uint8_t* box = rab_row + (cc >> 6) * (C::RAB_BYTES / 2);
+          const uint32_t m = full ? 0xffffffffu : chunk_mask(rr, n0 + cc);
+          const uint32_t half2 = BF16 ? 0x3f003f00u : 0x38003800u;  // (0.5, 0.5)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int chunk = (((cc & 63) >> 3) + q4) ^ (r & 7);
@@ -662,36 +671,38 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
             const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 rb = unpack2<BF16>(ww[e]);
-              x[q4 * 8 + 2 * e] = fmaf(__uint_as_float(sv[q4 * 8 + 2 * e]), half_alpha, 0.5f * rb.x);
-              x[q4 * 8 + 2 * e + 1] =
-                  fmaf(__uint_as_float(sv[q4 * 8 + 2 * e + 1]), half_alpha, 0.5f * rb.y);
+              const int c2 = q4 * 4 + e;  // pair index: columns 2*c2, 2*c2 + 1
+              uint32_t h2 = pack2<BF16>(__uint_as_float(sv[2 * c2]) * half_alpha,
+                                        __uint_as_float(sv[2 * c2 + 1]) * half_alpha);
+              h2 = fma2<BF16>(ww[e], half2, h2);
+              if (!full) {
+                const uint32_t lo = (m >> (2 * c2)) & 1u, hi = (m >> (2 * c2 + 1)) & 1u;
+                h2 &= (lo * 0x0000ffffu) | (hi * 0xffff0000u);
+              }
+              pk[c2] = fma2<BF16>(h2, tanh2<BF16>(h2), h2);
             }
           }
         } else {
+          float x[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(sv[e]) * half_alpha;
-        }
-        // x holds h = (alpha*s + rab)/2. silu(2h) = 2h*sigmoid(2h) = h*(1 + tanh(h)):
-        // a masked entry gets h = 0, so its P is silu(0) = 0. h is rounded to the
-        // 16-bit type, tanh runs on packed pairs and p = h*t + h is one packed fused
-        // multiply-add that yields P directly.
-        if (!full) {
-          // valid columns of this row form [0, hist_end) U [grp_lo, grp_hi]: as a bit mask
-          // over the 32 columns of the chunk
-          const uint32_t m = chunk_mask(rr, n0 + cc);
+          // x holds h = alpha*s/2. silu(2h) = 2h*sigmoid(2h) = h*(1 + tanh(h)): a masked
+          // entry gets h = 0, so its P is silu(0) = 0. h is rounded to the 16-bit type,
+          // tanh runs on packed pairs and p = h*t + h is one packed fused multiply-add
+          // that yields P directly.
+          if (!full) {
+            // valid columns of this row form [0, hist_end) U [grp_lo, grp_hi]: as a bit
+            // mask over the 32 columns of the chunk
+            const uint32_t m = chunk_mask(rr, n0 + cc);
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (!(m & (1u << e))) x[e] = 0.f;
-        }
-        uint32_t pk[16];
+            for (int e = 0; e < 32; ++e)
+              if (!(m & (1u << e))) x[e] = 0.f;
+          }
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const uint32_t h2 = pack2<BF16>(x[2 * e], x[2 * e + 1]);
-          if constexpr (BF16)
-            pk[e] = ptx::fma_bf16x2(h2, ptx::tanh_bf16x2(h2), h2);
-          else
-            pk[e] = ptx::fma_f16x2(h2, ptx::tanh_f16x2(h2), h2);
+          for (int e = 0; e < 16; ++e) {
+            const uint32_t h2 = pack2<BF16>(x[2 * e], x[2 * e + 1]);
+            pk[e] = fma2<BF16>(h2, tanh2<BF16>(h2), h2);
+          }
         }
         // P over the S columns this warpgroup has already read
         ptx::tmem_st16(tmem + lane_off + C::S_COL0 + sb * 128 + col + c * 16, pk);
