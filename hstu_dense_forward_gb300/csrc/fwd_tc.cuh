@@ -15,15 +15,16 @@
 //   warps 16, 18, 19  producers: TMA loads of the K (+ rab) ring, the V ring and the
 //              Q tiles, one thread each.
 //   warp 17    TMEM owner; one thread issues S(t) = Q K(t)^T (tcgen05.mma, A = Q and
-//              B = K from smem, K-major)
+//              B = K from smem, K-major) as soon as its S buffer is free.
 //   warp 20    one thread issues O += P(t) V(t) (tcgen05.mma, A = P from TMEM, B = V
-//              from smem, MN-major)
-//              With three S buffers each issuer goes as soon as its inputs are ready:
-//              PV(t) once P(t) is written, then S(t+3) once PV(t) has read P(t); the
-//              epilogue meanwhile works on S(t+1) and S(t+2), already computed.
-// TMEM (512 columns): S buffers of 128 columns from column 0 (three for D <= 128, two
-// for D = 256), O after them (D columns). P(t) is written over the columns of S(t) the
-// writing warpgroup has already read, so S(t + NSB) waits for PV(t) to have read P(t).
+//              from smem, MN-major) as soon as P(t) is written. Two issuers keep a
+//              thread stalled on tensor-pipe back-pressure from delaying the other
+//              product. D = 256 uses one issuer (see mma_serial_issuer).
+// TMEM (512 columns): two S buffers of 128 columns from column 0, O after them (D columns)
+// and, for D <= 128, two P buffers of 64 columns after O. An S buffer is handed back as
+// soon as the epilogue has loaded it, so S(t + 2) is computed while the epilogue works on
+// tile t. For D = 256 P(t) is written over the columns of S(t) already read, and
+// S(t + 2) waits for PV(t) to have read P(t).
 //
 // Every mbarrier wait is bounded (FwdParams::timeout_ns): on expiry the CTA
 // records HSTU_DEVERR_TIMEOUT, all roles leave their loops, the MMA queue is
@@ -75,10 +76,15 @@ struct Cfg {
   static constexpr int WARP_STAGE = 32 * OC * 2;     // one warp's O block in shared memory
   // S buffers in TMEM; P is written over the S buffer it was computed from. D = 256
   // leaves room for two (O takes 256 columns) and uses one MMA issuer; smaller D use three.
-  static constexpr int NSB = (D == 256) ? 2 : 3;
-  static constexpr bool SERIAL = (NSB == 2);
+  // Two S buffers. For D <= 128, P has its own two 64-column buffers after O and an S
+  // buffer is released as soon as the epilogue has loaded it; for D = 256 (O takes 256
+  // columns) P is written over the S buffer it came from and one thread issues all MMAs.
+  static constexpr int NSB = 2;
+  static constexpr bool P_SEP = (D <= 128);
+  static constexpr bool SERIAL = !P_SEP;
   // TMEM columns
   static constexpr uint32_t S_COL0 = 0, O_COL = NSB * 128;
+  static constexpr uint32_t P_COL0 = O_COL + D;  // P buffers (P_SEP only)
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
@@ -91,7 +97,7 @@ struct Cfg {
   // keep one CTA per SM (TMEM is allocated whole)
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 < 120 * 1024) ? 120 * 1024 : SMEM_USED + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(O_COL + D <= kTmemCols, "TMEM map");
+  static_assert(O_COL + D + (P_SEP ? 128 : 0) <= kTmemCols, "TMEM map");
 };
 
 // One work item, decoded once (by the Q producer) and read by every role.
@@ -111,7 +117,7 @@ struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t r_full[2], r_empty[2];
-  uint64_t s_full[3], p_full[3], pv_done[3];
+  uint64_t s_full[3], p_full[3], pv_done[3], s_free[2];
   uint64_t o_full, o_empty, drain, epi_sync;
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   Item info[kInfoDepth];
@@ -440,13 +446,19 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
     bool ok = true;
     for (int j = 0; j < it.n_kv && ok; ++j, ++t) {
       const uint32_t sb = t % C::NSB;
-      // S buffer sb holds P(t - NSB) until PV(t - NSB) has read it
-      if (t >= C::NSB && !wait_bar(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p)) {
+      const int ks = k_it % C::NK;
+      // S buffer sb is free once the epilogue has loaded S(t - NSB) into registers; both
+      // conditions are tested at once, and only one found unmet is waited for
+      uint64_t* sfree = &bars->s_free[sb];
+      uint64_t* kfull = &bars->k_full[ks];
+      const uint32_t sf_par = ((t / C::NSB) & 1) ^ 1, kf_par = (k_it / C::NK) & 1;
+      const uint32_t ready = ptx::mbar_test2(ptx::smem_u32(sfree), sf_par, ptx::smem_u32(kfull),
+                                             kf_par);
+      if (!(ready & 1u) && t >= C::NSB && !wait_bar(bars, sfree, sf_par, p)) {
         ok = false;
         break;
       }
-      const int ks = k_it % C::NK;
-      if (!wait_bar(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) { ok = false; break; }
+      if (!(ready & 2u) && !wait_bar(bars, kfull, kf_par, p)) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t ka = sbase + C::OFF_K + ks * C::TILE_BYTES;
 #pragma unroll
@@ -480,18 +492,21 @@ __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uin
     bool ok = true;
     for (int j = 0; j < it.n_kv; ++j, ++t) {
       const uint32_t sb = t % C::NSB;
-      if (!wait_bar(bars, &bars->p_full[sb], (t / C::NSB) & 1, p)) { ok = false; break; }
       const int vs = v_it % C::NV;
-      if (!wait_bar(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) { ok = false; break; }
+      uint64_t* pfull = &bars->p_full[sb];
+      uint64_t* vfull = &bars->v_full[vs];
+      const uint32_t pf_par = (t / C::NSB) & 1, vf_par = (v_it / C::NV) & 1;
+      const uint32_t ready = ptx::mbar_test2(ptx::smem_u32(pfull), pf_par, ptx::smem_u32(vfull),
+                                             vf_par);
+      if (!(ready & 1u) && !wait_bar(bars, pfull, pf_par, p)) { ok = false; break; }
+      if (!(ready & 2u) && !wait_bar(bars, vfull, vf_par, p)) { ok = false; break; }
       if (j == 0 && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) { ok = false; break; }
       ptx::tc_fence_after();
       const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
 #pragma unroll
       for (int kk = 0; kk < kTileN / 16; ++kk) {
-        // keys [16kk, 16kk + 16): warpgroup 16kk / kColsPerWG wrote them packed at the
-        // start of its own S columns
-        const uint32_t pcol = C::S_COL0 + sb * 128 + (16 * kk / kColsPerWG) * kColsPerWG +
-                              ((16 * kk) % kColsPerWG) / 2;
+        // keys [16kk, 16kk + 16) are packed in P columns [8kk, 8kk + 8)
+        const uint32_t pcol = C::P_COL0 + sb * 64 + kk * 8;
         const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
         ptx::mma_ts(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
       }
@@ -656,6 +671,10 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         const int cc = col + c * 32;  // first S column of this 32-column chunk
         uint32_t sv[32];
         ptx::tmem_ld32(tmem + lane_off + C::S_COL0 + sb * 128 + cc, sv);
+        if (C::P_SEP && c + 1 == kColsPerWG / 32) {  // all of this warp's S columns loaded
+          ptx::tc_fence_before();
+          warp_arrive(&bars->s_free[sb], lane);
+        }
         uint32_t pk[16];
         if constexpr (RAB) {
           // rab tile: two 64-column TMA boxes of 128 rows x 128 bytes, 128-byte swizzle.
@@ -704,8 +723,17 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
             pk[e] = fma2<BF16>(h2, tanh2<BF16>(h2), h2);
           }
         }
-        // P over the S columns this warpgroup has already read
-        ptx::tmem_st16(tmem + lane_off + C::S_COL0 + sb * 128 + col + c * 16, pk);
+        uint32_t pcol;
+        if constexpr (C::P_SEP) {
+          // P buffer sb is free once PV(t - NSB) has read it
+          if (c == 0 && t >= C::NSB &&
+              !warp_wait(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p))
+            return;
+          pcol = C::P_COL0 + sb * 64 + cc / 2;
+        } else {
+          pcol = C::S_COL0 + sb * 128 + col + c * 16;  // over S columns already read
+        }
+        ptx::tmem_st16(tmem + lane_off + pcol, pk);
       }
       if constexpr (RAB) {
         warp_arrive(&bars->r_empty[rs], lane);
@@ -741,6 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == kProducerWarp && lane == 0) {
+    for (int s = 0; s < 2; ++s) ptx::mbar_init(ptx::smem_u32(&bars->s_free[s]), kEpiWarps);
     for (int s = 0; s < 3; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->s_full[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&bars->p_full[s]), kEpiWarps);

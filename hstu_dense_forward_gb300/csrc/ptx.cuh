@@ -52,6 +52,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking tests of two barrier phases issued back to back, so that their latencies
+// overlap. Bit 0 / bit 1 of the result: phase parity par_a of bar_a / par_b of bar_b has
+// completed.
+__device__ __forceinline__ uint32_t mbar_test2(uint32_t bar_a, uint32_t par_a, uint32_t bar_b,
+                                               uint32_t par_b) {
+  uint32_t ra, rb;
+  asm volatile(
+      "{\n\t.reg .pred pa, pb;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 pa, [%2], %3;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 pb, [%4], %5;\n\t"
+      "selp.u32 %0, 1, 0, pa;\n\t"
+      "selp.u32 %1, 1, 0, pb;\n\t}"
+      : "=r"(ra), "=r"(rb)
+      : "r"(bar_a), "r"(par_a), "r"(bar_b), "r"(par_b)
+      : "memory");
+  return ra | (rb << 1);
+}
+
 // Blocking form: the thread is suspended until the phase completes or `ns`
 // nanoseconds pass, instead of spinning on the shared-memory pipe.
 __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
