@@ -46,9 +46,14 @@ struct hstu_fwd_plan {
   int num_sms;
   int grid;            // CTAs of the forward kernel
   bool tensor_cores;   // bf16/fp16 tcgen05 path (else the fp32 CUDA-core path)
-  uint32_t* d_work;    // work list [B * ceil(S / 128)]
-  int* d_count;        // entries in the work list
-  int* d_err;          // device error word
+  // Two work lists used by alternate runs, so that a run's work-list build can overlap the
+  // end of the previous run's forward kernel: list b at d_work + b * work_cap, its entry
+  // count at d_count[4 * b] and its claim counter at d_count[4 * b + 2].
+  uint32_t* d_work;    // 2 x work_cap entries
+  size_t work_cap;     // B * ceil(S / 128)
+  int* d_count;
+  int* d_err;          // device error word (d_count[1])
+  int parity;          // work list of the next run
   long long timeout_ns;
   // tensor maps of the last run, re-encoded when a pointer or T changes
   TcMaps maps;
@@ -127,11 +132,12 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
   }
   const size_t mtiles = (size_t)hstu::ceil_div(desc->max_seqlen, hstu::kTileM);
   const size_t entries = (size_t)(desc->batch > 0 ? desc->batch : 1) * mtiles;
-  if (e == cudaSuccess) e = cudaMalloc(&P->d_work, entries * sizeof(uint32_t));
-  if (e == cudaSuccess) e = cudaMalloc(&P->d_count, 3 * sizeof(int));
+  P->work_cap = entries;
+  if (e == cudaSuccess) e = cudaMalloc(&P->d_work, 2 * entries * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMalloc(&P->d_count, 8 * sizeof(int));
   if (e == cudaSuccess) {
-    P->d_err = P->d_count + 1;  // [0] count, [1] error word, [2] scheduling counter
-    e = cudaMemset(P->d_count, 0, 3 * sizeof(int));
+    P->d_err = P->d_count + 1;
+    e = cudaMemset(P->d_count, 0, 8 * sizeof(int));
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -228,9 +234,11 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
   p.seq_offsets = seq_offsets;
   p.num_context = num_context;
   p.num_targets = num_targets;
-  p.work = P->d_work;
-  p.work_count = P->d_count;
-  p.next_item = P->d_count + 2;
+  const int b = P->parity;
+  P->parity ^= 1;
+  p.work = P->d_work + b * P->work_cap;
+  p.work_count = P->d_count + 4 * b;
+  p.next_item = P->d_count + 4 * b + 2;
   p.err = P->d_err;
   p.total_tokens = total_tokens;
   p.timeout_ns = P->timeout_ns;
@@ -249,7 +257,8 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
     hstu_status ms = make_maps(P, q, k, v, rab, out, total_tokens);
     if (ms != HSTU_OK) return ms;
   }
-  if (hstu::launch_build_worklist(p, P->d_work, P->d_count, hstu::kTileM, st) != cudaSuccess)
+  if (hstu::launch_build_worklist(p, P->d_work + b * P->work_cap, P->d_count + 4 * b,
+                                  hstu::kTileM, st, true) != cudaSuccess)
     return HSTU_ERR_CUDA;
   cudaError_t e = P->tensor_cores
                       ? hstu::launch_fwd_tc(p, P->maps, d.dtype == HSTU_BF16, P->grid, st, true)
@@ -449,8 +458,9 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   }
   // the error word keeps the previous call's value: clear it (the count is rewritten)
   if (cudaMemsetAsync(p.err, 0, sizeof(int), st_) != cudaSuccess) return HSTU_ERR_CUDA;
+  // one work list: the build must not overlap a previous call (no programmatic launch)
   if (hstu::launch_build_worklist(p, scratch + 64, reinterpret_cast<int*>(scratch),
-                                  hstu::kTileM, st_) != cudaSuccess)
+                                  hstu::kTileM, st_, false) != cudaSuccess)
     return HSTU_ERR_CUDA;
   const int grid = tc ? sms : sms * (d.head_dim <= 64 ? 4 : (d.head_dim <= 128 ? 2 : 1));
   cudaError_t e = tc ? hstu::launch_fwd_tc(p, maps, d.dtype == HSTU_BF16, grid, st_, true)

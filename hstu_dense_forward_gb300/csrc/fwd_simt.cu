@@ -28,6 +28,7 @@ constexpr int kMaxU = kMaxD / 16;  // output columns per thread / 16
 
 __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams p) {
   ptx::grid_dependency_wait();  // the work list comes from the previous launch
+  ptx::grid_dependents_launch();  // after the wait: see the work-list builder
   extern __shared__ float sm[];
   const int D = p.D;
   const int ldk = D + 1;  // padded rows: threads of one warp read different K rows

@@ -52,7 +52,12 @@ constexpr int kQProducerWarp = kEpiWarps + 3;  // Q loads
 constexpr int kPvWarp = kEpiWarps + 4;         // issues O += P V
 constexpr int kThreads = (kEpiWarps + 5) * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
-constexpr int kColsPerWG = kTileN / kEpiWG;  // S columns each warpgroup owns per tile
+// The epilogue warps form two groups of two warpgroups; group g takes the S tiles t with
+// t % 2 == g (S and P buffer g), so that one group computes while the other waits for
+// its next tile.
+constexpr int kEpiGroups = 2;
+constexpr int kGroupWarps = kEpiWarps / kEpiGroups;
+constexpr int kColsPerWG = kTileN / (kEpiWG / kEpiGroups);  // S columns of a warpgroup per tile
 constexpr uint32_t kTmemCols = 512;
 
 template <int D, bool RAB>
@@ -236,10 +241,11 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   using C = Cfg<D, RAB>;
   uint32_t q_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
-  // Items are claimed dynamically from the heaviest-first list (one atomic per item);
-  // with a single Q buffer the next item is claimed one early so that its Q tile can be
-  // prefetched into L2.
-  long long idx = atomicAdd(p.next_item, 1);
+  // Items are claimed dynamically from the heaviest-first list: CTA i starts with item i,
+  // later items take one atomic each. With a single Q buffer the next item is claimed one
+  // early so that its Q tile can be prefetched into L2.
+  auto claim = [&]() -> long long { return (long long)gridDim.x + atomicAdd(p.next_item, 1); };
+  long long idx = blockIdx.x;
   for (int k = 0;; ++k) {
     Item it;
     if (idx >= total) {  // no work left: publish the end marker
@@ -251,7 +257,7 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
     if (!put_item(bars, k, it, p)) return;
     long long nidx = -1;
     if (C::NQ == 1) {
-      nidx = atomicAdd(p.next_item, 1);
+      nidx = claim();
       if (nidx < total) {
         Item nx;
         decode_item(p, nidx, nx);
@@ -269,7 +275,7 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
     for (int cb = 0; cb < C::NCB; ++cb)
       ptx::tma_load_3d(dst + cb * C::CB_BYTES, tq, full, cb * C::EPC, it.h, (int)(it.t0 + it.m0));
     ++q_it;
-    idx = C::NQ == 1 ? nidx : atomicAdd(p.next_item, 1);
+    idx = C::NQ == 1 ? nidx : claim();
   }
 }
 
@@ -578,9 +584,10 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   const int quarter = warp & 3;              // TMEM lane quarter
   const int r = quarter * 32 + lane;         // query row within the tile
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-  const int col = wg * kColsPerWG;           // first S column of this warpgroup
+  const int group = wg / (kEpiWG / kEpiGroups);  // takes the S tiles t with t % 2 == group
+  const int col = (wg % (kEpiWG / kEpiGroups)) * kColsPerWG;  // first S column of this warpgroup
   const float half_alpha = 0.5f * p.alpha;
-  uint32_t t = 0, u = 0, r_it = 0, epi_phase = 0;
+  uint32_t t = 0, u = 0;
   T16* out = static_cast<T16*>(p.out);
   int prev_slot = -1;  // item ring slot of the item whose O is still in TMEM
   // Output of a finished item: read this warpgroup's O columns chunk by chunk, scale,
@@ -654,7 +661,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     const int i = it.m0 + r;
     const RowRange rr = row_range(it.geom, i, p.mask_type);
     for (int j = 0; j < it.n_kv; ++j, ++t) {
-      const uint32_t sb = t % C::NSB;
+      if ((int)(t % kEpiGroups) != group) continue;  // the other group's tile
+      const uint32_t sb = t % C::NSB;                 // == group
       if (!warp_wait(bars, &bars->s_full[sb], (t / C::NSB) & 1, p)) return;
       ptx::tc_fence_after();
       const int n0 = j * kTileN;
@@ -662,12 +670,12 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       const uint8_t* rab_row = nullptr;
       int rs = 0;
       if constexpr (RAB) {
-        rs = r_it % C::NR;
-        if (!warp_wait(bars, &bars->r_full[rs], (r_it / C::NR) & 1, p)) return;
+        rs = t % C::NR;  // one rab tile per S tile, in tile order
+        if (!warp_wait(bars, &bars->r_full[rs], (t / C::NR) & 1, p)) return;
         rab_row = smem + C::OFF_R + rs * C::RAB_BYTES + r * 128;
       }
-#pragma unroll
-      for (int c = 0; c < kColsPerWG / 32; ++c) {
+#pragma unroll 1
+      for (int c = 0; c < kColsPerWG / 32; ++c) {  // 32-column chunks, one after the other
         const int cc = col + c * 32;  // first S column of this 32-column chunk
         uint32_t sv[32];
         ptx::tmem_ld32(tmem + lane_off + C::S_COL0 + sb * 128 + cc, sv);
@@ -735,20 +743,19 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         }
         ptx::tmem_st16(tmem + lane_off + pcol, pk);
       }
-      if constexpr (RAB) {
-        warp_arrive(&bars->r_empty[rs], lane);
-        ++r_it;
-      }
+      if constexpr (RAB) warp_arrive(&bars->r_empty[rs], lane);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       warp_arrive(&bars->p_full[sb], lane);
-      // the previous item's O, once two more P tiles are queued behind its last one (by
-      // then its last accumulation has finished), or at the last tile of this item
-      if (prev_slot >= 0 && (j == 1 || j + 1 == it.n_kv)) {
+      // this group's part of the previous item's O, after its first P tile of this item
+      // (the other group writes the previous item's last P meanwhile)
+      if (prev_slot >= 0) {
         if (!drain(prev_slot)) return;
         prev_slot = -1;
       }
     }
+    // a group with no tile in this item drains the previous one here
+    if (prev_slot >= 0 && !drain(prev_slot)) return;
     prev_slot = slot;
   }
   if (prev_slot >= 0 && !drain(prev_slot)) return;
@@ -762,6 +769,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                   const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   using C = Cfg<D, RAB>;
+  static_assert(C::NQ <= (int)(sizeof(Bars::q_full) / sizeof(uint64_t)) &&
+                    C::NK <= (int)(sizeof(Bars::k_full) / sizeof(uint64_t)) &&
+                    C::NV <= (int)(sizeof(Bars::v_full) / sizeof(uint64_t)) &&
+                    C::NR <= (int)(sizeof(Bars::r_full) / sizeof(uint64_t)),
+                "ring depths exceed the barrier arrays");
+  static_assert(C::NSB == kEpiGroups, "one S buffer per epilogue group");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -769,24 +782,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (warp == kProducerWarp && lane == 0) {
-    for (int s = 0; s < 2; ++s) ptx::mbar_init(ptx::smem_u32(&bars->s_free[s]), kEpiWarps);
-    for (int s = 0; s < 3; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars->s_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->p_full[s]), kEpiWarps);
-      ptx::mbar_init(ptx::smem_u32(&bars->pv_done[s]), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars->q_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->q_empty[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->r_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->r_empty[s]), kEpiWarps);
-    }
-    for (int s = 0; s < 4; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars->k_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->k_empty[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->v_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->v_empty[s]), 1);
-    }
+#define HSTU_INIT_ALL(arr, count)                                       \
+  for (int s = 0; s < (int)(sizeof(bars->arr) / sizeof(uint64_t)); ++s) \
+    ptx::mbar_init(ptx::smem_u32(&bars->arr[s]), (count));
+    // S / P buffer g belongs to epilogue group g: its warps arrive on s_free, p_full, r_empty
+    HSTU_INIT_ALL(s_free, kGroupWarps)
+    HSTU_INIT_ALL(s_full, 1)
+    HSTU_INIT_ALL(p_full, kGroupWarps)
+    HSTU_INIT_ALL(pv_done, 1)
+    HSTU_INIT_ALL(q_full, 1)
+    HSTU_INIT_ALL(q_empty, 1)
+    HSTU_INIT_ALL(r_full, 1)
+    HSTU_INIT_ALL(r_empty, kGroupWarps)
+    HSTU_INIT_ALL(k_full, 1)
+    HSTU_INIT_ALL(k_empty, 1)
+    HSTU_INIT_ALL(v_full, 1)
+    HSTU_INIT_ALL(v_empty, 1)
+#undef HSTU_INIT_ALL
     ptx::mbar_init(ptx::smem_u32(&bars->o_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->o_empty), kEpiWarps);
     ptx::mbar_init(ptx::smem_u32(&bars->epi_sync), kEpiWarps);
@@ -813,8 +825,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // The work list is written by the launch before this one.
+  // The work list is written by the launch before this one. Dependents (the next call's
+  // work-list build) are released only after this wait: by then the call before this one,
+  // which used the other work list, has completed.
   ptx::grid_dependency_wait();
+  ptx::grid_dependents_launch();
   const long long total = (long long)(*p.work_count) * p.Nq;
 
   if (warp < kEpiWarps) {

@@ -34,7 +34,8 @@ __host__ __device__ inline long long load_index(const void* p, long long i, int 
 
 // Scheduler: validates seq_offsets and writes the work list (one CTA).
 cudaError_t launch_build_worklist(const FwdParams& p, uint32_t* work, int* work_count,
-                                  int tile_m, cudaStream_t stream);
+                                  int tile_m, cudaStream_t stream,
+                                  bool pdl);
 
 // fp32 path on CUDA cores.
 size_t simt_smem_bytes(int D);

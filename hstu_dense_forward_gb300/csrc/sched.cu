@@ -7,6 +7,14 @@
 // (item index = pair * Nq + h), which keeps the query heads of one GQA group
 // adjacent in time and lets them share K/V tiles through L2.
 //
+// Launched with programmatic dependent launch after the previous forward kernel, the
+// builder may start while that kernel's last CTAs still run (that kernel releases its
+// dependents only after its own wait, so the forward call before it, which used the other
+// of the plan's two work lists, has completed). It reads only the call's inputs and writes
+// this call's work list, then waits for the previous kernel before it completes: the forward
+// kernel behind it, which waits for the builder, therefore starts its work only after the
+// previous call has finished.
+//
 // The builder also checks the caller's seq_offsets ("increasing from 0; the user
 // must ensure validity", Inputs and Outputs table) and, if they are unusable,
 // records HSTU_DEVERR_OFFSETS and publishes an empty list so that no kernel
@@ -20,7 +28,7 @@ namespace hstu {
 
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 256;  // small enough to share an SM with a forward CTA
 
 __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, uint32_t* work,
                                                                   int* work_count, int tile_m,
@@ -48,6 +56,7 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
       *work_count = 0;
       atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_OFFSETS);
     }
+    ptx::grid_dependency_wait();
     return;
   }
 
@@ -90,12 +99,14 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
       work[pos] = pack_item(b, mt);
     }
   }
+  // complete only after the kernel before this one in the stream
+  ptx::grid_dependency_wait();
 }
 
 }  // namespace
 
 cudaError_t launch_build_worklist(const FwdParams& p, uint32_t* work, int* work_count,
-                                  int tile_m, cudaStream_t stream) {
+                                  int tile_m, cudaStream_t stream, bool pdl) {
   const int nbins = ceil_div(p.S, kTileN) + 1;
   const size_t smem = sizeof(int) * 2 * (size_t)nbins;
   if (smem > 48 * 1024) {
@@ -103,8 +114,17 @@ cudaError_t launch_build_worklist(const FwdParams& p, uint32_t* work, int* work_
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  build_worklist_kernel<<<1, kThreads, smem, stream>>>(p, work, work_count, tile_m, nbins);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, build_worklist_kernel, p, work, work_count, tile_m, nbins);
 }
 
 }  // namespace hstu
