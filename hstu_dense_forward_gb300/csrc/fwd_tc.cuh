@@ -52,12 +52,6 @@ constexpr int kQProducerWarp = kEpiWarps + 3;  // Q loads
 constexpr int kPvWarp = kEpiWarps + 4;         // issues O += P V
 constexpr int kThreads = (kEpiWarps + 5) * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
-// The epilogue warps form two groups of two warpgroups; group g takes the S tiles t with
-// t % 2 == g (S and P buffer g), so that one group computes while the other waits for
-// its next tile.
-constexpr int kEpiGroups = 2;
-constexpr int kGroupWarps = kEpiWarps / kEpiGroups;
-constexpr int kColsPerWG = kTileN / (kEpiWG / kEpiGroups);  // S columns of a warpgroup per tile
 constexpr uint32_t kTmemCols = 512;
 
 template <int D, bool RAB>
@@ -79,6 +73,13 @@ struct Cfg {
   static constexpr int OC = D / kEpiWG;              // O columns per epilogue warpgroup
   static constexpr int OSWB = OC * 2;                // O staging row bytes (swizzle span)
   static constexpr int WARP_STAGE = 32 * OC * 2;     // one warp's O block in shared memory
+  // Epilogue groups. With two, the epilogue warps form two groups of two warpgroups and
+  // group g takes the S tiles t with t % 2 == g (S and P buffer g), so that one group
+  // computes while the other waits for its next tile; that pays for D = 256, whose longer
+  // products leave the epilogue waiting. With one, all four warpgroups work on every tile.
+  static constexpr int EPI_GROUPS = D == 256 ? 2 : 1;
+  static constexpr int GROUP_WARPS = kEpiWarps / EPI_GROUPS;
+  static constexpr int COLS_PER_WG = kTileN / (kEpiWG / EPI_GROUPS);  // S columns per tile
   // S buffers in TMEM; P is written over the S buffer it was computed from. D = 256
   // leaves room for two (O takes 256 columns) and uses one MMA issuer; smaller D use three.
   // Two S buffers. For D <= 128, P has its own two 64-column buffers after O and an S
@@ -401,8 +402,8 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
     const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
-      const uint32_t pcol = C::S_COL0 + sb * 128 + (16 * kk / kColsPerWG) * kColsPerWG +
-                            ((16 * kk) % kColsPerWG) / 2;
+      const uint32_t pcol = C::S_COL0 + sb * 128 + (16 * kk / C::COLS_PER_WG) * C::COLS_PER_WG +
+                            ((16 * kk) % C::COLS_PER_WG) / 2;
       const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
       ptx::mma_ts(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (!first || kk > 0) ? 1u : 0u);
     }
@@ -584,8 +585,9 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   const int quarter = warp & 3;              // TMEM lane quarter
   const int r = quarter * 32 + lane;         // query row within the tile
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-  const int group = wg / (kEpiWG / kEpiGroups);  // takes the S tiles t with t % 2 == group
-  const int col = (wg % (kEpiWG / kEpiGroups)) * kColsPerWG;  // first S column of this warpgroup
+  constexpr int WG_PER_GROUP = kEpiWG / C::EPI_GROUPS;
+  const int group = wg / WG_PER_GROUP;  // takes the S tiles t with t % EPI_GROUPS == group
+  const int col = (wg % WG_PER_GROUP) * C::COLS_PER_WG;  // first S column of this warpgroup
   const float half_alpha = 0.5f * p.alpha;
   uint32_t t = 0, u = 0;
   T16* out = static_cast<T16*>(p.out);
@@ -660,8 +662,9 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     if (it.n_kv < 0) break;  // end marker
     const int i = it.m0 + r;
     const RowRange rr = row_range(it.geom, i, p.mask_type);
+    int gtile = 0;  // tiles of this item processed by this group
     for (int j = 0; j < it.n_kv; ++j, ++t) {
-      if ((int)(t % kEpiGroups) != group) continue;  // the other group's tile
+      if ((int)(t % C::EPI_GROUPS) != group) continue;  // the other group's tile
       const uint32_t sb = t % C::NSB;                 // == group
       if (!warp_wait(bars, &bars->s_full[sb], (t / C::NSB) & 1, p)) return;
       ptx::tc_fence_after();
@@ -675,11 +678,11 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         rab_row = smem + C::OFF_R + rs * C::RAB_BYTES + r * 128;
       }
 #pragma unroll 1
-      for (int c = 0; c < kColsPerWG / 32; ++c) {  // 32-column chunks, one after the other
+      for (int c = 0; c < C::COLS_PER_WG / 32; ++c) {  // 32-column chunks, one after the other
         const int cc = col + c * 32;  // first S column of this 32-column chunk
         uint32_t sv[32];
         ptx::tmem_ld32(tmem + lane_off + C::S_COL0 + sb * 128 + cc, sv);
-        if (C::P_SEP && c + 1 == kColsPerWG / 32) {  // all of this warp's S columns loaded
+        if (C::P_SEP && c + 1 == C::COLS_PER_WG / 32) {  // all of this warp's S columns loaded
           ptx::tc_fence_before();
           warp_arrive(&bars->s_free[sb], lane);
         }
@@ -747,9 +750,11 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       warp_arrive(&bars->p_full[sb], lane);
-      // this group's part of the previous item's O, after its first P tile of this item
-      // (the other group writes the previous item's last P meanwhile)
-      if (prev_slot >= 0) {
+      // this group's part of the previous item's O, once the item's last P is queued and,
+      // with one group, one more P tile behind it (by then the item's last accumulation
+      // has finished), or at this group's last tile of the item
+      ++gtile;
+      if (prev_slot >= 0 && (gtile == (C::EPI_GROUPS == 1 ? 2 : 1) || j + C::EPI_GROUPS >= it.n_kv)) {
         if (!drain(prev_slot)) return;
         prev_slot = -1;
       }
@@ -774,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     C::NV <= (int)(sizeof(Bars::v_full) / sizeof(uint64_t)) &&
                     C::NR <= (int)(sizeof(Bars::r_full) / sizeof(uint64_t)),
                 "ring depths exceed the barrier arrays");
-  static_assert(C::NSB == kEpiGroups, "one S buffer per epilogue group");
+  static_assert(C::NSB % C::EPI_GROUPS == 0, "S buffers per epilogue group");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -785,15 +790,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define HSTU_INIT_ALL(arr, count)                                       \
   for (int s = 0; s < (int)(sizeof(bars->arr) / sizeof(uint64_t)); ++s) \
     ptx::mbar_init(ptx::smem_u32(&bars->arr[s]), (count));
-    // S / P buffer g belongs to epilogue group g: its warps arrive on s_free, p_full, r_empty
-    HSTU_INIT_ALL(s_free, kGroupWarps)
+    // the warps of the epilogue group that owns an S / P buffer arrive on s_free, p_full
+    // and r_empty
+    HSTU_INIT_ALL(s_free, C::GROUP_WARPS)
     HSTU_INIT_ALL(s_full, 1)
-    HSTU_INIT_ALL(p_full, kGroupWarps)
+    HSTU_INIT_ALL(p_full, C::GROUP_WARPS)
     HSTU_INIT_ALL(pv_done, 1)
     HSTU_INIT_ALL(q_full, 1)
     HSTU_INIT_ALL(q_empty, 1)
     HSTU_INIT_ALL(r_full, 1)
-    HSTU_INIT_ALL(r_empty, kGroupWarps)
+    HSTU_INIT_ALL(r_empty, C::GROUP_WARPS)
     HSTU_INIT_ALL(k_full, 1)
     HSTU_INIT_ALL(k_empty, 1)
     HSTU_INIT_ALL(v_full, 1)
