@@ -8,12 +8,15 @@
 //
 // CTA layout (persistent, one CTA per SM, 672 threads):
 //   warps 0-15 epilogue: four warpgroups; each thread owns one query row (TMEM lane)
-//              and a quarter of the 128 key columns of every S tile. It reads S from
-//              TMEM, applies alpha, rab, SiLU (as h + h*tanh(h), h = x/2, one MUFU
-//              op per element) and the mask, and writes P (bf16/fp16) back to TMEM.
-//              At the end of a work item it reads O, scales, converts and stores.
+//              and a quarter of the 128 key columns of every S tile (for D = 256: two
+//              groups of two warpgroups take alternate tiles, half the columns each). It
+//              reads S from TMEM, applies alpha, rab, SiLU (as h + h*tanh(h), h = x/2,
+//              one MUFU op per element) and the mask, and writes P (bf16/fp16) back to
+//              TMEM. An item's O is read, scaled, converted and stored by TMA after P of
+//              the next item's second tile.
 //   warps 16, 18, 19  producers: TMA loads of the K (+ rab) ring, the V ring and the
-//              Q tiles, one thread each.
+//              Q tiles, one thread each; the Q producer also claims and decodes the
+//              work items (heaviest first; CTA i starts with item i).
 //   warp 17    TMEM owner; one thread issues S(t) = Q K(t)^T (tcgen05.mma, A = Q and
 //              B = K from smem, K-major) as soon as its S buffer is free.
 //   warp 20    one thread issues O += P(t) V(t) (tcgen05.mma, A = P from TMEM, B = V
