@@ -6,7 +6,7 @@
 // HSTU has no softmax, so there is no running max or rescaling: O is a plain sum
 // over key tiles and key tiles the mask removes entirely are never visited.
 //
-// CTA layout (persistent, one CTA per SM, 672 threads):
+// CTA layout (persistent, one CTA per SM, 704 threads):
 //   warps 0-15 epilogue: four warpgroups; each thread owns one query row (TMEM lane)
 //              and a quarter of the 128 key columns of every S tile (for D = 256: two
 //              groups of two warpgroups take alternate tiles, half the columns each). It
@@ -14,9 +14,9 @@
 //              one MUFU op per element) and the mask, and writes P (bf16/fp16) back to
 //              TMEM. An item's O is read, scaled, converted and stored by TMA after P of
 //              the next item's second tile.
-//   warps 16, 18, 19  producers: TMA loads of the K (+ rab) ring, the V ring and the
-//              Q tiles, one thread each; the Q producer also claims and decodes the
-//              work items (heaviest first; CTA i starts with item i).
+//   warps 16, 18, 19, 21  producers: TMA loads of the K ring, the V ring, the Q tiles
+//              and the rab ring, one thread each; the Q producer also claims and decodes
+//              the work items (heaviest first; CTA i starts with item i).
 //   warp 17    TMEM owner; one thread issues S(t) = Q K(t)^T (tcgen05.mma, A = Q and
 //              B = K from smem, K-major) as soon as its S buffer is free.
 //   warp 20    one thread issues O += P(t) V(t) (tcgen05.mma, A = P from TMEM, B = V
@@ -53,7 +53,8 @@ constexpr int kMmaWarp = kEpiWarps + 1;
 constexpr int kVProducerWarp = kEpiWarps + 2;  // V loads
 constexpr int kQProducerWarp = kEpiWarps + 3;  // Q loads
 constexpr int kPvWarp = kEpiWarps + 4;         // issues O += P V
-constexpr int kThreads = (kEpiWarps + 5) * 32;
+constexpr int kRabWarp = kEpiWarps + 5;        // rab loads
+constexpr int kThreads = (kEpiWarps + 6) * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 
@@ -68,9 +69,10 @@ struct Cfg {
   static constexpr int TILE_BYTES = 128 * D * 2;
   static constexpr int RAB_BYTES = 128 * 128 * 2;
   static constexpr int NQ = (D <= 64) ? 2 : ((D == 128 && !RAB) ? 2 : 1);
-  static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 3 : 4) : (D == 128 ? 2 : 1));
+  static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 2 : 4) : (D == 128 ? 2 : 1));
   static constexpr int NV = NK;                                  // K and V ring depths
-  static constexpr int NR = RAB ? ((D == 256) ? 1 : 2) : 0;
+  // rab tiles stream from HBM once each: the deeper the ring, the more bytes in flight
+  static constexpr int NR = RAB ? (D == 32 ? 4 : (D == 64 ? 3 : (D == 128 ? 2 : 1))) : 0;
   // O is staged in shared memory and written by TMA when there is room for a tile
   static constexpr bool STAGE = D <= 64 || (D == 128 && !RAB);
   static constexpr int OC = D / kEpiWG;              // O columns per epilogue warpgroup
@@ -117,15 +119,15 @@ struct Item {
 };
 
 constexpr int kInfoDepth = 8;                   // decoded items kept in shared memory
-// item readers: epilogue warps, the MMA issuer(s), K and V producers
-template <bool SERIAL>
-constexpr int info_readers() { return kEpiWarps + (SERIAL ? 3 : 4); }
+// item readers: epilogue warps, the MMA issuer(s), K and V producers, the rab producer
+template <bool SERIAL, bool RAB>
+constexpr int info_readers() { return kEpiWarps + (SERIAL ? 3 : 4) + (RAB ? 1 : 0); }
 
 // Barrier block layout.
 struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
-  uint64_t r_full[2], r_empty[2];
+  uint64_t r_full[4], r_empty[4];
   uint64_t s_full[3], p_full[3], pv_done[3], s_free[2];
   uint64_t o_full, o_empty, drain, epi_sync;
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
@@ -285,9 +287,9 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 
 template <int D, bool RAB>
 __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tk,
-                           const CUtensorMap* tr, long long total) {
+                           long long total) {
   using C = Cfg<D, RAB>;
-  uint32_t k_it = 0, r_it = 0;
+  uint32_t k_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   for (int k = 0;; ++k) {
     Item it;
@@ -296,26 +298,38 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       const int s = k_it % C::NK;
       const int row = (int)(it.t0 + j * kTileN);
       if (!wait_bar(bars, &bars->k_empty[s], ((k_it / C::NK) & 1) ^ 1, p)) return;
-      {
-        const uint32_t full = ptx::smem_u32(&bars->k_full[s]);
-        ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
-        const uint32_t dst = sbase + C::OFF_K + s * C::TILE_BYTES;
+      const uint32_t full = ptx::smem_u32(&bars->k_full[s]);
+      ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
+      const uint32_t dst = sbase + C::OFF_K + s * C::TILE_BYTES;
 #pragma unroll
-        for (int cb = 0; cb < C::NCB; ++cb)
-          ptx::tma_load_3d(dst + cb * C::CB_BYTES, tk, full, cb * C::EPC, it.hk, row);
-      }
+      for (int cb = 0; cb < C::NCB; ++cb)
+        ptx::tma_load_3d(dst + cb * C::CB_BYTES, tk, full, cb * C::EPC, it.hk, row);
       ++k_it;
-      if constexpr (RAB) {
-        const int rs = r_it % C::NR;
-        if (!wait_bar(bars, &bars->r_empty[rs], ((r_it / C::NR) & 1) ^ 1, p)) return;
-        const uint32_t full = ptx::smem_u32(&bars->r_full[rs]);
-        ptx::mbar_arrive_expect_tx(full, C::RAB_BYTES);
-        const uint32_t dst = sbase + C::OFF_R + rs * C::RAB_BYTES;
-        const int plane = it.b * p.Nq + it.h;
-        ptx::tma_load_3d(dst, tr, full, j * kTileN, it.m0, plane);
-        ptx::tma_load_3d(dst + C::RAB_BYTES / 2, tr, full, j * kTileN + 64, it.m0, plane);
-        ++r_it;
-      }
+    }
+  }
+}
+
+// rab tiles of every S tile, in tile order, on their own thread: the rab ring is released
+// by the epilogue (late in a tile), and waiting for it must not hold back the K loads.
+template <int D, bool RAB>
+__device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tr,
+                           long long total) {
+  using C = Cfg<D, RAB>;
+  uint32_t r_it = 0;
+  const uint32_t sbase = ptx::smem_u32(smem);
+  for (int k = 0;; ++k) {
+    Item it;
+    if (!get_item(bars, k, it, p) || it.n_kv < 0) return;
+    const int plane = it.b * p.Nq + it.h;
+    for (int j = 0; j < it.n_kv; ++j) {
+      const int rs = r_it % C::NR;
+      if (!wait_bar(bars, &bars->r_empty[rs], ((r_it / C::NR) & 1) ^ 1, p)) return;
+      const uint32_t full = ptx::smem_u32(&bars->r_full[rs]);
+      ptx::mbar_arrive_expect_tx(full, C::RAB_BYTES);
+      const uint32_t dst = sbase + C::OFF_R + rs * C::RAB_BYTES;
+      ptx::tma_load_3d(dst, tr, full, j * kTileN, it.m0, plane);
+      ptx::tma_load_3d(dst + C::RAB_BYTES / 2, tr, full, j * kTileN + 64, it.m0, plane);
+      ++r_it;
     }
   }
 }
@@ -814,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(ptx::smem_u32(&bars->drain), C::SERIAL ? 1 : 2);  // one commit per issuer
     for (int s = 0; s < kInfoDepth; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->info_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), info_readers<C::SERIAL>());
+      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), info_readers<C::SERIAL, RAB>());
     }
     bars->abort = 0;
     ptx::fence_barrier_init();
@@ -844,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kEpiWarps) {
     epilogue<D, BF16, RAB>(p, bars, smem, tmem, &tm_o, total, warp, lane);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_k<D, RAB>(p, bars, smem, &tm_k, &tm_r, total);
+    if (lane == 0) producer_k<D, RAB>(p, bars, smem, &tm_k, total);
   } else if (warp == kQProducerWarp) {
     if (lane == 0) producer_q<D, RAB>(p, bars, smem, &tm_q, total);
   } else if (warp == kVProducerWarp) {
@@ -856,6 +870,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       else
         mma_s_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
     }
+  } else if (warp == kRabWarp) {
+    if (RAB && lane == 0) producer_r<D, RAB>(p, bars, smem, &tm_r, total);
   } else if (warp == kPvWarp) {
     if (lane == 0 && !C::SERIAL) mma_pv_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
   }
