@@ -75,11 +75,11 @@ def _bind(lib):
     lib.hstu_oracle_valid.restype = ctypes.c_int
     lib.hstu_oracle_valid.argtypes = [c64, c64, c64, ctypes.c_int, c64, c64, c64]
     lib.hstu_oracle_fwd.restype = ctypes.c_int
-    lib.hstu_oracle_fwd.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, i64, i64,
+    lib.hstu_oracle_fwd.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, c64, i64, i64,
                                     ctypes.c_int, c64, ctypes.c_double, ctypes.c_double,
                                     d, ctypes.c_int]
     lib.hstu_oracle_fwd_rows.restype = ctypes.c_int
-    lib.hstu_oracle_fwd_rows.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, i64,
+    lib.hstu_oracle_fwd_rows.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, c64, i64,
                                          i64, ctypes.c_int, c64, ctypes.c_double,
                                          ctypes.c_double, i64, c64, d, ctypes.c_int]
     lib.hstu_oracle_count_valid.restype = ctypes.c_int64
@@ -115,12 +115,15 @@ def _common(q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen):
     B = so.shape[0] - 1
     nc, nt = _i64(num_context), _i64(num_targets)
     rab = _f64(rab)
+    rab_heads = 0
     if rab is not None:
         if max_seqlen is None:
             raise ValueError("max_seqlen is required with rab")
-        if rab.shape != (B, q.shape[1], max_seqlen, max_seqlen):
-            raise ValueError(f"rab must be [B, Nq, S, S], got {rab.shape}")
-    return q, k, v, so, B, rab, nc, nt
+        if rab.ndim != 4 or rab.shape[1] not in (1, q.shape[1]) or \
+                rab.shape != (B, rab.shape[1], max_seqlen, max_seqlen):
+            raise ValueError(f"rab must be [B, Nq, S, S] or [B, 1, S, S], got {rab.shape}")
+        rab_heads = rab.shape[1]
+    return q, k, v, so, B, rab, rab_heads, nc, nt
 
 
 def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=None,
@@ -129,8 +132,8 @@ def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=No
     """Whole forward in fp64. Returns out [T, Nq, D] as float64 (rows outside
     every sequence are 0). silu_scale defaults to 1/max_seqlen (Inputs and
     Outputs table, silu_scale)."""
-    q, k, v, so, B, rab, nc, nt = _common(q, k, v, seq_offsets, rab, num_context,
-                                          num_targets, max_seqlen)
+    q, k, v, so, B, rab, rab_heads, nc, nt = _common(q, k, v, seq_offsets, rab, num_context,
+                                                     num_targets, max_seqlen)
     if max_seqlen is None:
         max_seqlen = int(np.max(np.diff(so))) if B > 0 else 1
     if silu_scale is None:
@@ -138,7 +141,8 @@ def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=No
     out = np.zeros(q.shape, dtype=np.float64)
     rc = _load().hstu_oracle_fwd(_p(q, ctypes.c_double), _p(k, ctypes.c_double),
                                  _p(v, ctypes.c_double), _p(so, ctypes.c_int64), B, q.shape[1],
-                                 k.shape[1], q.shape[2], _p(rab, ctypes.c_double), max_seqlen,
+                                 k.shape[1], q.shape[2], _p(rab, ctypes.c_double), rab_heads,
+                                 max_seqlen,
                                  _p(nc, ctypes.c_int64), _p(nt, ctypes.c_int64), mask_type,
                                  target_group_size, float(alpha), float(silu_scale),
                                  _p(out, ctypes.c_double), int(nthreads))
@@ -152,8 +156,8 @@ def hstu_fwd_rows(q, k, v, seq_offsets, rows, *, rab=None, num_context=None, num
                   max_seqlen=None, nthreads=1):
     """Selected output rows: rows is an int array [n, 3] of (b, h, i) (i local to
     sequence b). Returns [n, D] float64, row r = out[seq_offsets[b] + i, h, :]."""
-    q, k, v, so, B, rab, nc, nt = _common(q, k, v, seq_offsets, rab, num_context,
-                                          num_targets, max_seqlen)
+    q, k, v, so, B, rab, rab_heads, nc, nt = _common(q, k, v, seq_offsets, rab, num_context,
+                                                     num_targets, max_seqlen)
     if max_seqlen is None:
         max_seqlen = int(np.max(np.diff(so))) if B > 0 else 1
     if silu_scale is None:
@@ -163,7 +167,7 @@ def hstu_fwd_rows(q, k, v, seq_offsets, rows, *, rab=None, num_context=None, num
     rc = _load().hstu_oracle_fwd_rows(_p(q, ctypes.c_double), _p(k, ctypes.c_double),
                                       _p(v, ctypes.c_double), _p(so, ctypes.c_int64), B,
                                       q.shape[1], k.shape[1], q.shape[2],
-                                      _p(rab, ctypes.c_double), max_seqlen,
+                                      _p(rab, ctypes.c_double), rab_heads, max_seqlen,
                                       _p(nc, ctypes.c_int64), _p(nt, ctypes.c_int64), mask_type,
                                       target_group_size, float(alpha), float(silu_scale),
                                       _p(rows, ctypes.c_int64), rows.shape[0],

@@ -23,6 +23,8 @@
  * Readings taken where the page is silent (each also listed in the design notes):
  *   - alpha multiplies Q*K^T only; rab is added after it, before SiLU.
  *   - rab is indexed by local positions: rab[b, h, i, j], row stride max_seqlen.
+ *   - Feature table, "Support for rab broadcasting": rab may be [b, 1, s, s]; its one
+ *     plane per sequence is then added for every query head.
  *   - GQA head map: kv head = h / (Nq / Nk) (contiguous groups).
  *   - Causal mask with H = (g > 0) ? max(L - nt, 0) : L (history length):
  *       valid(i, j) = (j <= i && j < H)                       causal over history
@@ -73,6 +75,7 @@ typedef struct {
   const double *q, *k, *v, *rab;
   const int64_t *seq_offsets, *num_context, *num_targets;
   int64_t B, Nq, Nk, D, max_seqlen;
+  int64_t rab_heads; /* rab planes per sequence: Nq, or 1 (broadcast to every head) */
   int mask_type;
   int64_t g;
   double alpha, silu_scale;
@@ -103,7 +106,10 @@ static void one_row(const job_t *J, int64_t b, int64_t h, int64_t i, double *o) 
     for (int64_t d = 0; d < D; ++d) s += qi[d] * kj[d];
     /* alpha on Q*K^T, then the relative attention bias */
     double x = J->alpha * s;
-    if (J->rab) x += J->rab[((b * J->Nq + h) * J->max_seqlen + i) * J->max_seqlen + j];
+    if (J->rab) {
+      const int64_t plane = b * J->rab_heads + (J->rab_heads == 1 ? 0 : h);
+      x += J->rab[(plane * J->max_seqlen + i) * J->max_seqlen + j];
+    }
     /* 2. SiLU activation */
     double p = silu(x);
     /* 3. scaling */
@@ -166,22 +172,24 @@ static int check_args(int64_t B, int64_t Nq, int64_t Nk, int64_t D, int mask_typ
 }
 
 /*
- * Whole forward. q [T, Nq, D], k/v [T, Nk, D], rab [B, Nq, S, S] or NULL,
+ * Whole forward. q [T, Nq, D], k/v [T, Nk, D], rab [B, rab_heads, S, S] or NULL
+ * (rab_heads = Nq, or 1 for a plane shared by all heads),
  * seq_offsets [B+1], num_context/num_targets [B] or NULL; out [T, Nq, D].
  * Rows of out outside every sequence are left untouched. Returns 0 or -1.
  */
 int hstu_oracle_fwd(const double *q, const double *k, const double *v,
                     const int64_t *seq_offsets, int64_t B, int64_t Nq, int64_t Nk,
-                    int64_t D, const double *rab, int64_t max_seqlen,
+                    int64_t D, const double *rab, int64_t rab_heads, int64_t max_seqlen,
                     const int64_t *num_context, const int64_t *num_targets,
                     int mask_type, int64_t target_group_size, double alpha,
                     double silu_scale, double *out, int nthreads) {
   if (check_args(B, Nq, Nk, D, mask_type)) return -1;
+  if (rab && rab_heads != 1 && rab_heads != Nq) return -1;
   job_t J;
   memset(&J, 0, sizeof(J));
   J.q = q; J.k = k; J.v = v; J.rab = rab;
   J.seq_offsets = seq_offsets; J.num_context = num_context; J.num_targets = num_targets;
-  J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen;
+  J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen; J.rab_heads = rab_heads;
   J.mask_type = mask_type; J.g = target_group_size;
   J.alpha = alpha; J.silu_scale = silu_scale; J.out = out;
   return run_pool(&J, worker_units, nthreads);
@@ -190,12 +198,13 @@ int hstu_oracle_fwd(const double *q, const double *k, const double *v,
 /* Selected rows only: rows[3r..3r+2] = (b, h, i); out_rows [nrows, D]. */
 int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
                          const int64_t *seq_offsets, int64_t B, int64_t Nq, int64_t Nk,
-                         int64_t D, const double *rab, int64_t max_seqlen,
+                         int64_t D, const double *rab, int64_t rab_heads, int64_t max_seqlen,
                          const int64_t *num_context, const int64_t *num_targets,
                          int mask_type, int64_t target_group_size, double alpha,
                          double silu_scale, const int64_t *rows, int64_t nrows,
                          double *out_rows, int nthreads) {
   if (check_args(B, Nq, Nk, D, mask_type)) return -1;
+  if (rab && rab_heads != 1 && rab_heads != Nq) return -1;
   for (int64_t r = 0; r < nrows; ++r) {
     const int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
     if (b < 0 || b >= B || h < 0 || h >= Nq || i < 0 ||
@@ -206,7 +215,7 @@ int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
   memset(&J, 0, sizeof(J));
   J.q = q; J.k = k; J.v = v; J.rab = rab;
   J.seq_offsets = seq_offsets; J.num_context = num_context; J.num_targets = num_targets;
-  J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen;
+  J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen; J.rab_heads = rab_heads;
   J.mask_type = mask_type; J.g = target_group_size;
   J.alpha = alpha; J.silu_scale = silu_scale;
   J.rows = rows; J.nrows = nrows; J.out_rows = out_rows;

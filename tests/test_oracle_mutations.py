@@ -16,10 +16,10 @@ MUTATIONS = [
     ("transposed_scores", "const double *qi = J->q + ((t0 + i) * J->Nq + h) * D;",
      "const double *qi = J->q + ((t0 + i) * J->Nq + h) * D; (void)0;\n"
      "    const double *qq = qi; (void)qq;"),  # placeholder replaced below
-    ("dropped_rab", "if (J->rab) x +=", "if (0) x +="),
-    ("alpha_scales_rab", "if (J->rab) x += J->rab[((b * J->Nq + h) * J->max_seqlen + i) * J->max_seqlen + j];",
-     "if (J->rab) x += J->alpha * J->rab[((b * J->Nq + h) * J->max_seqlen + i) * J->max_seqlen + j];"),
-    ("rab_transposed", "* J->max_seqlen + i) * J->max_seqlen + j]", "* J->max_seqlen + j) * J->max_seqlen + i]"),
+    ("dropped_rab", "x += J->rab[(plane", "x += 0.0 * J->rab[(plane"),
+    ("alpha_scales_rab", "x += J->rab[(plane", "x += J->alpha * J->rab[(plane"),
+    ("rab_transposed", "(plane * J->max_seqlen + i) * J->max_seqlen + j]", "(plane * J->max_seqlen + j) * J->max_seqlen + i]"),
+    ("rab_head_ignored", "(J->rab_heads == 1 ? 0 : h)", "(J->rab_heads == 1 ? 0 : 0)"),
     ("silu_sign", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
     ("sigmoid_not_silu", "return x / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(-x));"),
     ("gqa_modulo", "const int64_t hk = h / G;", "const int64_t hk = h % J->Nk;"),
@@ -44,7 +44,9 @@ def _pin_checks():
     checks = [pins.test_single_token_closed_forms, pins.test_silu_odd_part_identity,
               pins.test_q_zero_with_rab_closed_form, pins.test_jagged_lengths_match_torch_per_sequence,
               pins.test_count_valid_closed_forms, pins.test_q_zero_without_rab_gives_zero,
-              pins.test_causal_rows_ignore_later_keys, pins.test_gqa_equals_replicated_mha]
+              pins.test_causal_rows_ignore_later_keys, pins.test_gqa_equals_replicated_mha,
+              lambda: pins.test_q_zero_rab_per_head_and_broadcast_closed_form(1),
+              lambda: pins.test_q_zero_rab_per_head_and_broadcast_closed_form(3)]
     for causal in (False, True):
         for nq, nk in ((4, 4), (4, 2), (6, 1)):
             checks.append(lambda c=causal, a=nq, b=nk: pins.test_equal_lengths_match_torch_matmul(c, a, b))

@@ -92,6 +92,28 @@ def test_q_zero_with_rab_closed_form():
                                    atol=1e-12)
 
 
+@pytest.mark.parametrize("rab_heads", [1, 3])
+def test_q_zero_rab_per_head_and_broadcast_closed_form(rab_heads):
+    """Q = 0 with three query heads: out[t0+i, h] = silu_scale * sum_j silu(rab[b, r, i, j])
+    * v[t0+j, h] with r = h for rab [B, Nq, S, S] and r = 0 for the broadcast form
+    [B, 1, S, S] (feature table, "Support for rab broadcasting"); silu from torch."""
+    rng = _rng(13)
+    lengths = [3, 5]
+    q, k, v, so = _jagged(rng, lengths, 3, 3, 2)
+    q[:] = 0.0
+    S = 5
+    rab = rng.standard_normal((2, rab_heads, S, S))
+    out = oracle.hstu_fwd(q, k, v, so, rab=rab, mask_type=oracle.MASK_NONE, alpha=2.0,
+                          silu_scale=0.25, max_seqlen=S)
+    for bi, L in enumerate(lengths):
+        t0 = so[bi]
+        for h in range(3):
+            r = 0 if rab_heads == 1 else h
+            p = F.silu(torch.from_numpy(rab[bi, r, :L, :L])).numpy()
+            np.testing.assert_allclose(out[t0:t0 + L, h], 0.25 * p @ v[t0:t0 + L, h], rtol=0,
+                                       atol=1e-12)
+
+
 # --------------------------------------------------------------------------- library cases
 def _torch_dense(q, k, v, rab, alpha, scale, causal):
     """Equal-length, no-context/no-target case with torch fp64 library ops.
