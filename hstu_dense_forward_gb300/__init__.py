@@ -28,7 +28,8 @@ _DTYPES = {torch.float32: _abi.HSTU_F32, torch.float16: _abi.HSTU_F16,
 
 
 def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, index_is_int64,
-          causal, target_group_size, has_rab, has_num_context, has_num_targets, watchdog_ms=0):
+          causal, target_group_size, has_rab, has_num_context, has_num_targets, watchdog_ms=0,
+          layout="jagged", rab_heads=0):
     d = _abi.Desc()
     d.dtype = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     d.batch = int(batch)
@@ -43,6 +44,10 @@ def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, inde
     d.has_num_context = int(bool(has_num_context))
     d.has_num_targets = int(bool(has_num_targets))
     d.watchdog_ms = int(watchdog_ms)
+    if layout not in ("jagged", "normal"):
+        raise ValueError(f"layout must be 'jagged' or 'normal', got {layout!r}")
+    d.layout = _abi.HSTU_LAYOUT_NORMAL if layout == "normal" else _abi.HSTU_LAYOUT_JAGGED
+    d.rab_heads = int(rab_heads)
     return d
 
 
@@ -61,7 +66,7 @@ class HstuFwdPlan:
     def run_ptr(self, q, k, v, seq_offsets, rab, num_context, num_targets, total_tokens,
                 alpha, silu_scale, out, stream):
         """Raw entry: integer device addresses (0 for absent) and a cudaStream_t value."""
-        _abi.check(self._keep.hstu_fwd_run(self._h, q, k, v, seq_offsets, rab or None,
+        _abi.check(self._keep.hstu_fwd_run(self._h, q, k, v, seq_offsets or None, rab or None,
                                            num_context or None, num_targets or None,
                                            int(total_tokens), float(alpha), float(silu_scale),
                                            out, stream or None), "hstu_fwd_run")
@@ -73,7 +78,7 @@ class HstuFwdPlan:
         if stream is None:
             stream = torch.cuda.current_stream(q.device)
         ptr = lambda t: 0 if t is None else t.data_ptr()
-        self.run_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_offsets.data_ptr(), ptr(rab),
+        self.run_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), ptr(seq_offsets), ptr(rab),
                      ptr(num_context), ptr(num_targets), q.shape[0], alpha, silu_scale,
                      out.data_ptr(), stream.cuda_stream)
         return out
@@ -118,61 +123,108 @@ def _check_tensor(t, name, dtype, device, ndim=None):
         raise ValueError(f"{name} must be contiguous")
 
 
-def hstu_fwd(q, k, v, seq_offsets, *, max_seqlen, rab=None, num_context=None, num_targets=None,
-             causal=True, target_group_size=0, alpha=1.0, silu_scale=None, out=None,
-             watchdog_ms=0):
-    """HSTU forward on jagged tensors.
+def _rab_heads(rab, B, Nq, S):
+    """0 for rab [B, Nq, S, S]; 1 for the broadcast form [B, 1, S, S] (feature table,
+    "Support for rab broadcasting")."""
+    if rab is None:
+        return 0
+    if rab.shape not in ((B, Nq, S, S), (B, 1, S, S)):
+        raise ValueError(f"rab must be [B, Nq, S, S] or [B, 1, S, S] = [{B}, {Nq} or 1, {S}, "
+                         f"{S}], got {list(rab.shape)}")
+    return 1 if rab.shape[1] == 1 and Nq > 1 else 0
 
-    q [T, Nq, D], k/v [T, Nk, D] (same dtype: fp32, fp16 or bf16), seq_offsets [B+1]
-    int32/int64 (num_context / num_targets [B] of the same integer dtype), rab
-    [B, Nq, max_seqlen, max_seqlen] of q's dtype or None. causal=False is mask_type
-    2 (no mask). silu_scale defaults to 1/max_seqlen (Inputs and Outputs table).
-    Returns out [T, Nq, D]; rows that belong to no sequence are left as allocated.
+
+def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_context=None,
+             num_targets=None, causal=True, target_group_size=0, alpha=1.0, silu_scale=None,
+             out=None, watchdog_ms=0, layout="jagged"):
+    """HSTU forward.
+
+    layout "jagged" (default): q [T, Nq, D], k/v [T, Nk, D], seq_offsets [B+1] int32/int64,
+    max_seqlen required. layout "normal" (Inputs and Outputs table, layout): q [B, S, Nq, D],
+    k/v [B, S, Nk, D], every sequence of S tokens, no seq_offsets, max_seqlen = S.
+    Same dtype for q, k, v: fp32, fp16 or bf16. num_context / num_targets [B] of the index
+    dtype (int32/int64). rab [B, Nq, S, S] or [B, 1, S, S] (one plane for all heads) of q's
+    dtype, or None. causal=False is mask_type 2 (no mask). silu_scale defaults to
+    1/max_seqlen. Returns out with q's shape; rows that belong to no sequence are left as
+    allocated.
     """
     dev = q.device
     if dev.type != "cuda":
         raise ValueError("hstu_fwd runs on CUDA tensors only")
-    _check_tensor(q, "q", None, dev, 3)
     if q.dtype not in _DTYPES:
         raise TypeError(f"unsupported dtype {q.dtype}")
-    _check_tensor(k, "k", q.dtype, dev, 3)
-    _check_tensor(v, "v", q.dtype, dev, 3)
-    _check_tensor(seq_offsets, "seq_offsets", None, dev, 1)
-    if seq_offsets.dtype not in (torch.int32, torch.int64):
-        raise TypeError("seq_offsets must be int32 or int64")
-    if k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
-        raise ValueError("k and v must be [T, Nk, D] with q's T and D")
+    if layout == "normal":
+        _check_tensor(q, "q", None, dev, 4)
+        _check_tensor(k, "k", q.dtype, dev, 4)
+        _check_tensor(v, "v", q.dtype, dev, 4)
+        if seq_offsets is not None:
+            raise ValueError("the normal layout takes no seq_offsets")
+        B, S = q.shape[0], q.shape[1]
+        if max_seqlen is None:
+            max_seqlen = S
+        elif int(max_seqlen) != S:
+            raise ValueError(f"the normal layout needs max_seqlen == S = {S}")
+        if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+            raise ValueError("k and v must be [B, S, Nk, D] with q's B, S and D")
+        idx = [t for t in (num_context, num_targets) if t is not None]
+        idx_dtype = idx[0].dtype if idx else torch.int64
+        res = out
+        if res is None:
+            res = torch.empty_like(q)
+        else:
+            _check_tensor(res, "out", q.dtype, dev, 4)
+            if res.shape != q.shape:
+                raise ValueError("out must have q's shape")
+        q3, k3, v3 = q.view(B * S, *q.shape[2:]), k.view(B * S, *k.shape[2:]), v.view(B * S, *v.shape[2:])
+        out3 = res.view(B * S, *q.shape[2:])
+    elif layout == "jagged":
+        _check_tensor(q, "q", None, dev, 3)
+        _check_tensor(k, "k", q.dtype, dev, 3)
+        _check_tensor(v, "v", q.dtype, dev, 3)
+        if seq_offsets is None or max_seqlen is None:
+            raise ValueError("the jagged layout needs seq_offsets and max_seqlen")
+        _check_tensor(seq_offsets, "seq_offsets", None, dev, 1)
+        idx_dtype = seq_offsets.dtype
+        if k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
+            raise ValueError("k and v must be [T, Nk, D] with q's T and D")
+        B = seq_offsets.shape[0] - 1
+        if out is None:
+            out = torch.empty_like(q)
+        else:
+            _check_tensor(out, "out", q.dtype, dev, 3)
+            if out.shape != q.shape:
+                raise ValueError("out must have q's shape")
+        q3, k3, v3, out3, res = q, k, v, out, out
+    else:
+        raise ValueError(f"layout must be 'jagged' or 'normal', got {layout!r}")
+    if idx_dtype not in (torch.int32, torch.int64):
+        raise TypeError("index tensors must be int32 or int64")
     for name, t in (("num_context", num_context), ("num_targets", num_targets)):
         if t is not None:
-            _check_tensor(t, name, seq_offsets.dtype, dev, 1)
+            _check_tensor(t, name, idx_dtype, dev, 1)
+    T, Nq, D = q3.shape
     if rab is not None:
         _check_tensor(rab, "rab", q.dtype, dev, 4)
-    T, Nq, D = q.shape
-    B = seq_offsets.shape[0] - 1
-    if out is None:
-        out = torch.empty_like(q)
-    else:
-        _check_tensor(out, "out", q.dtype, dev, 3)
-        if out.shape != q.shape:
-            raise ValueError("out must have q's shape")
+    rab_heads = _rab_heads(rab, B, Nq, int(max_seqlen))
     stream = torch.cuda.current_stream(dev)
-    key = (dev.index, stream.cuda_stream, q.dtype, B, Nq, k.shape[1], D, int(max_seqlen),
-           seq_offsets.dtype, bool(causal), int(target_group_size), rab is not None,
-           num_context is not None, num_targets is not None, int(watchdog_ms))
+    key = (dev.index, stream.cuda_stream, q.dtype, B, Nq, k3.shape[1], D, int(max_seqlen),
+           idx_dtype, bool(causal), int(target_group_size), rab is not None,
+           num_context is not None, num_targets is not None, int(watchdog_ms), layout, rab_heads)
     plan = _plans.get(key)
     if plan is None:
         with torch.cuda.device(dev):
-            plan = HstuFwdPlan(dtype=q.dtype, batch=B, num_heads_q=Nq, num_heads_kv=k.shape[1],
+            plan = HstuFwdPlan(dtype=q.dtype, batch=B, num_heads_q=Nq, num_heads_kv=k3.shape[1],
                                head_dim=D, max_seqlen=max_seqlen,
-                               index_is_int64=seq_offsets.dtype == torch.int64, causal=causal,
+                               index_is_int64=idx_dtype == torch.int64, causal=causal,
                                target_group_size=target_group_size, has_rab=rab is not None,
                                has_num_context=num_context is not None,
-                               has_num_targets=num_targets is not None, watchdog_ms=watchdog_ms)
+                               has_num_targets=num_targets is not None, watchdog_ms=watchdog_ms,
+                               layout=layout, rab_heads=rab_heads)
         _plans[key] = plan
     with torch.cuda.device(dev):
-        plan.run(q, k, v, seq_offsets, out, rab=rab, num_context=num_context,
+        plan.run(q3, k3, v3, seq_offsets, out3, rab=rab, num_context=num_context,
                  num_targets=num_targets, alpha=alpha, silu_scale=silu_scale, stream=stream)
-    return out
+    return res
 
 
 def hstu_fwd_noalloc(q, k, v, seq_offsets, out, *, max_seqlen, rab=None, num_context=None,
@@ -186,11 +238,13 @@ def hstu_fwd_noalloc(q, k, v, seq_offsets, out, *, max_seqlen, rab=None, num_con
     for name, t in (("k", k), ("v", v), ("out", out)):
         _check_tensor(t, name, q.dtype, dev, 3)
     _check_tensor(q, "q", None, dev, 3)
-    d = _desc(dtype=q.dtype, batch=seq_offsets.shape[0] - 1, num_heads_q=q.shape[1],
+    B = seq_offsets.shape[0] - 1
+    d = _desc(dtype=q.dtype, batch=B, num_heads_q=q.shape[1],
               num_heads_kv=k.shape[1], head_dim=q.shape[2], max_seqlen=max_seqlen,
               index_is_int64=seq_offsets.dtype == torch.int64, causal=causal,
               target_group_size=target_group_size, has_rab=rab is not None,
-              has_num_context=num_context is not None, has_num_targets=num_targets is not None)
+              has_num_context=num_context is not None, has_num_targets=num_targets is not None,
+              rab_heads=_rab_heads(rab, B, q.shape[1], int(max_seqlen)))
     if silu_scale is None:
         silu_scale = 1.0 / max_seqlen
     ptr = lambda t: None if t is None else t.data_ptr()
@@ -209,16 +263,18 @@ def plan_for(**kw) -> HstuFwdPlan:
 
 
 def count_pairs(seq_offsets, num_heads_q, *, max_seqlen, num_context=None, num_targets=None,
-                causal=True, target_group_size=0) -> int:
+                causal=True, target_group_size=0, layout="jagged", batch=None) -> int:
     """Mask-aware (query head, i, j) pair count, computed by the library on the host
-    from CPU integer tensors or sequences."""
-    so = torch.as_tensor(seq_offsets, dtype=torch.int64).contiguous().cpu()
+    from CPU integer tensors or sequences. For layout "normal" pass seq_offsets=None and
+    batch=B (every sequence has max_seqlen tokens)."""
+    so = None if seq_offsets is None else torch.as_tensor(seq_offsets, dtype=torch.int64).contiguous().cpu()
     nc = None if num_context is None else torch.as_tensor(num_context, dtype=torch.int64).contiguous().cpu()
     nt = None if num_targets is None else torch.as_tensor(num_targets, dtype=torch.int64).contiguous().cpu()
-    d = _desc(dtype=_abi.HSTU_BF16, batch=so.numel() - 1, num_heads_q=num_heads_q,
+    B = int(batch) if so is None else so.numel() - 1
+    d = _desc(dtype=_abi.HSTU_BF16, batch=B, num_heads_q=num_heads_q,
               num_heads_kv=1, head_dim=64, max_seqlen=max_seqlen, index_is_int64=True,
               causal=causal, target_group_size=target_group_size, has_rab=False,
-              has_num_context=nc is not None, has_num_targets=nt is not None)
+              has_num_context=nc is not None, has_num_targets=nt is not None, layout=layout)
     out = ctypes.c_longlong(0)
     ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     _abi.check(_abi.lib().hstu_fwd_count_pairs(ctypes.byref(d), ptr(so), ptr(nc), ptr(nt),

@@ -16,6 +16,7 @@ HSTU_OK, HSTU_ERR_INVALID_ARG, HSTU_ERR_UNSUPPORTED, HSTU_ERR_CUDA, HSTU_ERR_TIM
 HSTU_F32, HSTU_F16, HSTU_BF16 = 0, 1, 2
 HSTU_MASK_CAUSAL, HSTU_MASK_UPPER, HSTU_MASK_NONE, HSTU_MASK_CUSTOM = 0, 1, 2, 3
 HSTU_DEVERR_NONE, HSTU_DEVERR_OFFSETS, HSTU_DEVERR_TIMEOUT = 0, 1, 2
+HSTU_LAYOUT_JAGGED, HSTU_LAYOUT_NORMAL = 0, 1
 
 
 class Desc(ctypes.Structure):
@@ -33,7 +34,9 @@ class Desc(ctypes.Structure):
         ("has_num_context", ctypes.c_int),
         ("has_num_targets", ctypes.c_int),
         ("watchdog_ms", ctypes.c_int),
-        ("reserved", ctypes.c_int * 3),
+        ("layout", ctypes.c_int),
+        ("rab_heads", ctypes.c_int),
+        ("reserved", ctypes.c_int),
     ]
 
 

@@ -76,9 +76,22 @@ const char* hstu_status_string(hstu_status s) {
   return "unknown status";
 }
 
+// seq_offsets for the jagged layout; none for the normal layout, whose token count is
+// fixed (B sequences of S tokens).
+static bool layout_args_ok(const hstu_fwd_desc& d, const void* seq_offsets,
+                           long long total_tokens) {
+  if (d.layout == HSTU_LAYOUT_NORMAL)
+    return seq_offsets == nullptr && total_tokens == (long long)d.batch * d.max_seqlen;
+  return seq_offsets != nullptr;
+}
+
 static hstu_status validate_desc(const hstu_fwd_desc* d) {
   if (!d) return HSTU_ERR_INVALID_ARG;
-  if (d->reserved[0] || d->reserved[1] || d->reserved[2]) return HSTU_ERR_INVALID_ARG;
+  if (d->reserved) return HSTU_ERR_INVALID_ARG;
+  if (d->layout != HSTU_LAYOUT_JAGGED && d->layout != HSTU_LAYOUT_NORMAL)
+    return HSTU_ERR_INVALID_ARG;
+  if (d->rab_heads != 0 && d->rab_heads != 1 && d->rab_heads != d->num_heads_q)
+    return HSTU_ERR_INVALID_ARG;
   if (d->dtype != HSTU_F32 && d->dtype != HSTU_F16 && d->dtype != HSTU_BF16)
     return HSTU_ERR_INVALID_ARG;
   if (d->batch < 0 || d->batch > (1 << 20)) return HSTU_ERR_INVALID_ARG;
@@ -191,7 +204,8 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
                                     : CU_TENSOR_MAP_SWIZZLE_NONE);
   if (ok && rab) {
     const uint64_t S = (uint64_t)d.max_seqlen;
-    ok = encode3d(&P->maps.rab, ty, rab, S, S, (uint64_t)d.batch * Nq, S * 2, S * S * 2, 64,
+    ok = encode3d(&P->maps.rab, ty, rab, S, S, (uint64_t)d.batch * (d.rab_heads == 1 ? 1 : Nq),
+                  S * 2, S * S * 2, 64,
                   hstu::kTileM, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   } else if (ok) {
     P->maps.rab = P->maps.q;  // unused by the kernel
@@ -214,7 +228,8 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
   const hstu_fwd_desc& d = P->desc;
   if (total_tokens < 0 || total_tokens > 0x7fffffffll) return HSTU_ERR_INVALID_ARG;
   if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
-  if (!q || !k || !v || !seq_offsets || !out) return HSTU_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !layout_args_ok(d, seq_offsets, total_tokens))
+    return HSTU_ERR_INVALID_ARG;
   if ((rab != nullptr) != (d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
   if ((num_context != nullptr) != (d.has_num_context != 0)) return HSTU_ERR_INVALID_ARG;
   if ((num_targets != nullptr) != (d.has_num_targets != 0)) return HSTU_ERR_INVALID_ARG;
@@ -250,6 +265,8 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
   p.S = d.max_seqlen;
   p.mask_type = d.mask_type;
   p.g = d.mask_type == HSTU_MASK_CAUSAL ? d.target_group_size : 0;
+  p.dense = d.layout == HSTU_LAYOUT_NORMAL ? 1 : 0;
+  p.rab_bcast = d.rab_heads == 1 ? 1 : 0;
   p.alpha = alpha;
   p.silu_scale = silu_scale;
 
@@ -297,15 +314,20 @@ hstu_status hstu_fwd_launches_per_run(const hstu_fwd_plan* P, int* launches) {
 hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* d, const void* seq_offsets_host,
                                  const void* num_context_host, const void* num_targets_host,
                                  long long* pairs) {
-  if (!d || !pairs || (d->batch > 0 && !seq_offsets_host)) return HSTU_ERR_INVALID_ARG;
+  if (!d || !pairs) return HSTU_ERR_INVALID_ARG;
+  const bool normal = d->layout == HSTU_LAYOUT_NORMAL;
+  if (normal ? seq_offsets_host != nullptr : (d->batch > 0 && !seq_offsets_host))
+    return HSTU_ERR_INVALID_ARG;
   if (d->mask_type != HSTU_MASK_CAUSAL && d->mask_type != HSTU_MASK_NONE)
     return HSTU_ERR_UNSUPPORTED;
   const int is64 = d->index_is_int64 ? 1 : 0;
   const int g = d->mask_type == HSTU_MASK_CAUSAL ? d->target_group_size : 0;
   long long total = 0;
   for (int b = 0; b < d->batch; ++b) {
-    const long long t0 = hstu::load_index(seq_offsets_host, b, is64);
-    const long long L = hstu::load_index(seq_offsets_host, b + 1, is64) - t0;
+    const long long t0 = normal ? (long long)b * d->max_seqlen
+                                : hstu::load_index(seq_offsets_host, b, is64);
+    const long long L =
+        (normal ? (long long)(b + 1) * d->max_seqlen : hstu::load_index(seq_offsets_host, b + 1, is64)) - t0;
     if (L < 0 || L > d->max_seqlen) return HSTU_ERR_INVALID_ARG;
     const long long nc = num_context_host ? hstu::load_index(num_context_host, b, is64) : 0;
     const long long nt = num_targets_host ? hstu::load_index(num_targets_host, b, is64) : 0;
@@ -379,7 +401,8 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
   if ((long long)d.batch * hstu::ceil_div(d.max_seqlen, hstu::kTileM) > HSTU_NOALLOC_MAX_ENTRIES)
     return HSTU_ERR_UNSUPPORTED;  // work list larger than the static scratch array
-  if (!q || !k || !v || !seq_offsets || !out) return HSTU_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !layout_args_ok(d, seq_offsets, total_tokens))
+    return HSTU_ERR_INVALID_ARG;
   if ((rab != nullptr) != (d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
   if ((num_context != nullptr) != (d.has_num_context != 0)) return HSTU_ERR_INVALID_ARG;
   if ((num_targets != nullptr) != (d.has_num_targets != 0)) return HSTU_ERR_INVALID_ARG;
@@ -424,6 +447,8 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   p.S = d.max_seqlen;
   p.mask_type = d.mask_type;
   p.g = d.mask_type == HSTU_MASK_CAUSAL ? d.target_group_size : 0;
+  p.dense = d.layout == HSTU_LAYOUT_NORMAL ? 1 : 0;
+  p.rab_bcast = d.rab_heads == 1 ? 1 : 0;
   p.alpha = alpha;
   p.silu_scale = silu_scale;
 
@@ -449,7 +474,8 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
                                       : CU_TENSOR_MAP_SWIZZLE_NONE);
     if (ok && rab) {
       const uint64_t S = (uint64_t)d.max_seqlen;
-      ok = encode3d(&maps.rab, ty, rab, S, S, (uint64_t)d.batch * Nq, S * 2, S * S * 2, 64,
+      ok = encode3d(&maps.rab, ty, rab, S, S, (uint64_t)d.batch * (d.rab_heads == 1 ? 1 : Nq),
+                    S * 2, S * S * 2, 64,
                     hstu::kTileM, 1, CU_TENSOR_MAP_SWIZZLE_128B);
     } else if (ok) {
       maps.rab = maps.q;  // unused by the kernel

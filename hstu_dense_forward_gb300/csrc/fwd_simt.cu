@@ -52,8 +52,8 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams 
     const int h = (int)(it % p.Nq);
     const uint32_t e = p.work[it / p.Nq];
     const int b = item_b(e);
-    const long long t0 = load_index(p.seq_offsets, b, p.index64);
-    const int L = (int)(load_index(p.seq_offsets, b + 1, p.index64) - t0);
+    const long long t0 = seq_start(p, b);
+    const int L = (int)(seq_start(p, b + 1) - t0);
     const int m0 = item_mt(e) * kTileM + half * BM;
     if (m0 >= L) continue;
     const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams 
           float x = p.alpha * sc[a][c];
           const bool ok = (i < L) && (j < L) && valid_in_range(rr, j);
           if (rab != nullptr && ok)
-            x += rab[(((long long)b * p.Nq + h) * p.S + i) * p.S + j];
+            x += rab[(rab_plane(p, b, h) * p.S + i) * p.S + j];
           const float pv = x / (1.0f + expf(-x));
           Ps[r * (BN + 1) + tx + 16 * c] = ok ? pv : 0.f;
         }

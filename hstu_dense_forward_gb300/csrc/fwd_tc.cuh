@@ -143,8 +143,8 @@ __device__ __forceinline__ bool decode_item(const FwdParams& p, long long idx, I
   it.hk = it.h / (p.Nq / p.Nk);
   it.b = item_b(e);
   it.m0 = item_mt(e) * kTileM;
-  it.t0 = load_index(p.seq_offsets, it.b, p.index64);
-  it.L = (int)(load_index(p.seq_offsets, it.b + 1, p.index64) - it.t0);
+  it.t0 = seq_start(p, it.b);
+  it.L = (int)(seq_start(p, it.b + 1) - it.t0);
   const long long nc = p.num_context ? load_index(p.num_context, it.b, p.index64) : 0;
   const long long nt = p.num_targets ? load_index(p.num_targets, it.b, p.index64) : 0;
   it.geom = make_geom(it.L, nc, nt, p.g, p.mask_type);
@@ -320,7 +320,7 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   for (int k = 0;; ++k) {
     Item it;
     if (!get_item(bars, k, it, p) || it.n_kv < 0) return;
-    const int plane = it.b * p.Nq + it.h;
+    const int plane = (int)rab_plane(p, it.b, it.h);
     for (int j = 0; j < it.n_kv; ++j) {
       const int rs = r_it % C::NR;
       if (!wait_bar(bars, &bars->r_empty[rs], ((r_it / C::NR) & 1) ^ 1, p)) return;

@@ -25,11 +25,23 @@ struct FwdParams {
   int index64;              // index tensors are int64
   int B, Nq, Nk, D, S;      // batch, heads, head dim, max_seqlen
   int mask_type, g;         // mask code, target group size
+  int dense;                // normal layout: sequence b is tokens [b * S, (b + 1) * S)
+  int rab_bcast;            // rab [B, 1, S, S]: one bias plane for every query head
   float alpha, silu_scale;
 };
 
 __host__ __device__ inline long long load_index(const void* p, long long i, int is64) {
   return is64 ? static_cast<const long long*>(p)[i] : static_cast<const int*>(p)[i];
+}
+
+// First token of sequence b: from seq_offsets (jagged layout) or b * S (normal layout).
+__host__ __device__ inline long long seq_start(const FwdParams& p, long long b) {
+  return p.dense ? b * p.S : load_index(p.seq_offsets, b, p.index64);
+}
+
+// rab plane of (sequence b, query head h): [B, Nq, S, S], or [B, 1, S, S] broadcast.
+__host__ __device__ inline long long rab_plane(const FwdParams& p, long long b, int h) {
+  return p.rab_bcast ? b : b * p.Nq + h;
 }
 
 // Scheduler: validates seq_offsets and writes the work list (one CTA).

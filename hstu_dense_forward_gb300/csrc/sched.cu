@@ -45,8 +45,8 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
 
   const long long T = p.total_tokens;
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    long long a = load_index(p.seq_offsets, b, p.index64);
-    long long e = load_index(p.seq_offsets, b + 1, p.index64);
+    long long a = seq_start(p, b);
+    long long e = seq_start(p, b + 1);
     if (a < 0 || e < a || e > T || e - a > p.S) bad = 1;
   }
   __syncthreads();
@@ -63,8 +63,8 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
   const int tile_n = kTileN;
   // pass 1: histogram of key-tile counts
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const long long t0 = load_index(p.seq_offsets, b, p.index64);
-    const int L = (int)(load_index(p.seq_offsets, b + 1, p.index64) - t0);
+    const long long t0 = seq_start(p, b);
+    const int L = (int)(seq_start(p, b + 1) - t0);
     const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
     const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
     const SeqGeom s = make_geom(L, nc, nt, p.g, p.mask_type);
@@ -87,8 +87,8 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
   __syncthreads();
   // pass 2: scatter
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const long long t0 = load_index(p.seq_offsets, b, p.index64);
-    const int L = (int)(load_index(p.seq_offsets, b + 1, p.index64) - t0);
+    const long long t0 = seq_start(p, b);
+    const int L = (int)(seq_start(p, b + 1) - t0);
     const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
     const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
     const SeqGeom s = make_geom(L, nc, nt, p.g, p.mask_type);

@@ -65,6 +65,11 @@ typedef enum {
  * match q"; the output "same as q"). */
 typedef enum { HSTU_F32 = 0, HSTU_F16 = 1, HSTU_BF16 = 2 } hstu_dtype;
 
+/* Tensor layout (Inputs and Outputs table, layout): "jagged" q [T, Nq, D] with
+ * seq_offsets, or "normal" q [B, S, Nq, D] where every sequence has S = max_seqlen
+ * tokens (the same memory as jagged with seq_offsets[b] = b * S, T = B * S). */
+typedef enum { HSTU_LAYOUT_JAGGED = 0, HSTU_LAYOUT_NORMAL = 1 } hstu_layout;
+
 /* mask_type codes of the Inputs and Outputs table. UPPER ("currently not
  * supported" on the page) and CUSTOM are rejected with HSTU_ERR_UNSUPPORTED. */
 typedef enum {
@@ -97,7 +102,11 @@ typedef struct {
   int has_num_context;   /* 1: num_context [B] is passed to every run */
   int has_num_targets;   /* 1: num_targets [B] is passed to every run */
   int watchdog_ms;       /* limit of one device pipeline wait; 0 = 1000 ms */
-  int reserved[3];       /* must be 0 */
+  int layout;            /* hstu_layout; 0 = jagged */
+  int rab_heads;         /* bias planes per sequence: 0 or Nq for rab [B, Nq, S, S]; 1 for
+                            rab [B, 1, S, S], one plane added for every query head (feature
+                            table, "Support for rab broadcasting") */
+  int reserved;          /* must be 0 */
 } hstu_fwd_desc;
 
 typedef struct hstu_fwd_plan hstu_fwd_plan; /* opaque */
@@ -109,8 +118,10 @@ HSTU_API hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** 
 /*
  * Enqueue one forward on `stream` (a cudaStream_t; NULL = legacy default stream).
  *   q    [T, Nq, D]        k, v [T, Nk, D]       out [T, Nq, D]   (dtype of the plan)
- *   seq_offsets [B+1]      increasing from 0, seq_offsets[B] <= T
- *   rab  [B, Nq, S, S] or NULL (must be non-NULL iff desc.has_rab)
+ *   seq_offsets [B+1]      increasing from 0, seq_offsets[B] <= T; for the normal layout
+ *                          NULL, and T must be B * S (q is [B, S, Nq, D])
+ *   rab  [B, Nq, S, S] (or [B, 1, S, S] with desc.rab_heads = 1) or NULL (must be
+ *        non-NULL iff desc.has_rab)
  *   num_context, num_targets [B] or NULL (non-NULL iff the desc flags say so)
  *   total_tokens = T, the row count of q, k, v and out.
  * Rows of out that belong to no sequence are not written. silu_scale is used as
@@ -136,7 +147,8 @@ HSTU_API hstu_status hstu_fwd_get_error(hstu_fwd_plan* plan, int* device_error);
 HSTU_API hstu_status hstu_fwd_launches_per_run(const hstu_fwd_plan* plan, int* launches);
 
 /* Host-side count of the mask-aware work: sum over sequences of Nq * #valid(i, j),
- * from HOST arrays seq_offsets [B+1] and optional num_context / num_targets [B]
+ * from HOST arrays seq_offsets [B+1] (NULL for the normal layout: every length is S)
+ * and optional num_context / num_targets [B]
  * (int32 or int64 per desc.index_is_int64). 4 * D * pairs is the useful flop
  * count of one run. */
 HSTU_API hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* desc, const void* seq_offsets_host,

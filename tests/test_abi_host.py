@@ -45,6 +45,9 @@ def _desc(**kw):
     (dict(dtype=9), _abi.HSTU_ERR_INVALID_ARG),
     (dict(batch=-1), _abi.HSTU_ERR_INVALID_ARG),
     (dict(target_group_size=-2), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(layout=2), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(has_rab=1, rab_heads=2), _abi.HSTU_ERR_INVALID_ARG),          # neither 1 nor Nq
+    (dict(reserved=1), _abi.HSTU_ERR_INVALID_ARG),
 ])
 def test_create_rejects_bad_descriptors(built_lib, kw, status):
     lib = _abi.lib()
@@ -92,3 +95,33 @@ def test_count_pairs_closed_forms(built_lib):
     so = [0, 100, 250]
     assert count_pairs(so, 2, max_seqlen=150) == 2 * (100 * 101 // 2 + 150 * 151 // 2)
     assert count_pairs(so, 2, max_seqlen=150, causal=False) == 2 * (100 ** 2 + 150 ** 2)
+
+
+def test_count_pairs_normal_layout(built_lib):
+    """The normal layout is B sequences of max_seqlen tokens: the count equals the jagged
+    count with offsets b * S, and no offsets may be passed."""
+    S, B = 96, 3
+    nc, nt = [5, 0, 20], [10, 30, 0]
+    want = count_pairs([b * S for b in range(B + 1)], 4, max_seqlen=S, num_context=nc,
+                       num_targets=nt, target_group_size=3)
+    got = count_pairs(None, 4, max_seqlen=S, num_context=nc, num_targets=nt,
+                      target_group_size=3, layout="normal", batch=B)
+    assert got == want
+    lib = _abi.lib()
+    d = _desc(batch=B, max_seqlen=S, layout=_abi.HSTU_LAYOUT_NORMAL)
+    so = (ctypes.c_longlong * (B + 1))(*[b * S for b in range(B + 1)])
+    out = ctypes.c_longlong(0)
+    assert lib.hstu_fwd_count_pairs(ctypes.byref(d), so, None, None,
+                                    ctypes.byref(out)) == _abi.HSTU_ERR_INVALID_ARG
+
+
+def test_rab_broadcast_descriptor_accepted(built_lib):
+    lib = _abi.lib()
+    for rab_heads in (0, 1, 4):
+        h = ctypes.c_void_p()
+        d = _desc(has_rab=1, rab_heads=rab_heads)
+        st = lib.hstu_fwd_create(ctypes.byref(d), ctypes.byref(h))
+        # a plan needs a GB300; without one creation stops at the device check
+        assert st in (_abi.HSTU_OK, _abi.HSTU_ERR_UNSUPPORTED, _abi.HSTU_ERR_CUDA)
+        if h.value:
+            lib.hstu_fwd_destroy(h)

@@ -1,0 +1,118 @@
+"""The normal layout (Inputs and Outputs table, layout: q [B, S, N, D]) and the rab
+broadcast form [B, 1, S, S] (feature table, "Support for rab broadcasting"), through the
+C ABI: against the fp64 oracle, and bit for bit against the equivalent jagged call / the
+rab replicated to every head (same arithmetic, so the results must be identical)."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hstu_dense_forward_gb300 import hstu_fwd, hstu_fwd_noalloc
+from hstu_dense_forward_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp32": 1e-5, "bf16": 2e-2, "fp16": 1e-2}
+BASE = W.WORKLOADS["bf16_causal_b32_s2048_h4_d128"]
+
+
+def _uniform(dtype, d, B, S, heads, **kw):
+    w = W.scaled(BASE, batch=B, max_seqlen=S, dtype=dtype, head_dim=d, num_heads_q=heads[0],
+                 num_heads_kv=heads[1], **kw)
+    return replace(w, fixed_offsets=tuple(b * S for b in range(B + 1)))
+
+
+def _jagged_call(d, **kw):
+    return hstu_fwd(d["q"], d["k"], d["v"], d["seq_offsets"], max_seqlen=d["max_seqlen"],
+                    num_context=d["num_context"], num_targets=d["num_targets"],
+                    causal=d["causal"], target_group_size=d["target_group_size"],
+                    alpha=d["alpha"], silu_scale=d["silu_scale"], **kw)
+
+
+def _rel_err(got, ref):
+    g = got.double().cpu().numpy().reshape(ref.shape)
+    return float(np.max(np.abs(g - ref)) / np.max(np.abs(ref)))
+
+
+@pytest.mark.parametrize("dtype,d,heads,extra", [
+    ("bf16", 128, (4, 4), {}),
+    ("fp16", 64, (4, 2), dict(context_range=(0, 20), target_range=(10, 60),
+                              target_group_size=3)),
+    ("fp32", 64, (2, 2), {}),
+])
+def test_normal_layout_matches_jagged(cuda_device, dtype, d, heads, extra):
+    B, S = 3, 320
+    w = _uniform(dtype, d, B, S, heads, **extra)
+    dv = W.to_device(W.generate(w), cuda_device)
+    ref = _jagged_call(dv)
+    q4 = dv["q"].view(B, S, *dv["q"].shape[1:])
+    k4 = dv["k"].view(B, S, *dv["k"].shape[1:])
+    v4 = dv["v"].view(B, S, *dv["v"].shape[1:])
+    got = hstu_fwd(q4, k4, v4, None, num_context=dv["num_context"],
+                   num_targets=dv["num_targets"], causal=dv["causal"],
+                   target_group_size=dv["target_group_size"], alpha=dv["alpha"],
+                   silu_scale=dv["silu_scale"], layout="normal")
+    torch.cuda.synchronize()
+    assert got.shape == q4.shape
+    assert torch.equal(got.view_as(ref), ref)
+
+
+def test_normal_layout_against_oracle(cuda_device):
+    B, S = 2, 200
+    w = _uniform("bf16", 64, B, S, (2, 2), target_range=(20, 50), target_group_size=2)
+    inp = W.generate(w)
+    dv = W.to_device(inp, cuda_device)
+    q4 = dv["q"].view(B, S, *dv["q"].shape[1:])
+    got = hstu_fwd(q4, dv["k"].view(B, S, *dv["k"].shape[1:]), dv["v"].view(B, S, *dv["v"].shape[1:]),
+                   num_targets=dv["num_targets"], target_group_size=2, alpha=inp["alpha"],
+                   silu_scale=inp["silu_scale"], layout="normal")
+    torch.cuda.synchronize()
+    ref = oracle.hstu_fwd(inp["q"], inp["k"], inp["v"], inp["seq_offsets"],
+                          num_targets=inp["num_targets"], mask_type=oracle.MASK_CAUSAL,
+                          target_group_size=2, alpha=inp["alpha"], silu_scale=inp["silu_scale"],
+                          max_seqlen=S, nthreads=8)
+    assert _rel_err(got, ref) <= TOL["bf16"]
+
+
+def _bcast_case(dtype, d, heads, causal=True):
+    w = W.scaled(BASE, batch=3, max_seqlen=264, len_lo=1, len_hi=264, dtype=dtype, head_dim=d,
+                 num_heads_q=heads[0], num_heads_kv=heads[1], causal=causal)
+    inp = W.generate(w)
+    g = torch.Generator().manual_seed(21)
+    rab = (torch.randn(3, 1, 264, 264, generator=g) * 0.5).to(W.DTYPES[dtype])
+    return w, inp, rab
+
+
+@pytest.mark.parametrize("dtype,d,heads,causal", [("bf16", 128, (4, 4), True),
+                                                  ("fp16", 64, (8, 2), False),
+                                                  ("bf16", 256, (2, 1), True),
+                                                  ("fp32", 32, (4, 4), True)])
+def test_rab_broadcast_against_oracle_and_replicated(cuda_device, dtype, d, heads, causal):
+    w, inp, rab = _bcast_case(dtype, d, heads, causal)
+    dv = W.to_device(inp, cuda_device)
+    rab_d = rab.to(cuda_device)
+    got = _jagged_call(dv, rab=rab_d)
+    rep = _jagged_call(dv, rab=rab_d.expand(-1, heads[0], -1, -1).contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(got, rep)
+    ref = oracle.hstu_fwd(inp["q"], inp["k"], inp["v"], inp["seq_offsets"], rab=rab,
+                          mask_type=oracle.MASK_CAUSAL if causal else oracle.MASK_NONE,
+                          alpha=inp["alpha"], silu_scale=inp["silu_scale"], max_seqlen=264,
+                          nthreads=8)
+    T = int(inp["seq_offsets"][-1])
+    assert _rel_err(got[:T], ref[:T]) <= TOL[dtype]
+
+
+def test_rab_broadcast_allocation_free_entry(cuda_device):
+    w, inp, rab = _bcast_case("bf16", 64, (4, 4))
+    dv = W.to_device(inp, cuda_device)
+    rab_d = rab.to(cuda_device)
+    ref = _jagged_call(dv, rab=rab_d)
+    out = torch.empty_like(dv["q"])
+    hstu_fwd_noalloc(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], out, max_seqlen=264,
+                     rab=rab_d, causal=True, alpha=dv["alpha"], silu_scale=dv["silu_scale"])
+    torch.cuda.synchronize()
+    T = int(inp["seq_offsets"][-1])
+    assert torch.equal(out[:T], ref[:T])
