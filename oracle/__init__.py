@@ -26,6 +26,7 @@ _lib = None
 
 MASK_CAUSAL = 0  # Inputs and Outputs table: "0: built-in lower triangular mask"
 MASK_NONE = 2  # "2: do not use a mask"
+MASK_CUSTOM = 3  # "3: use a custom mask ... the user must define and pass in the mask"
 
 
 def build(force: bool = False) -> str:
@@ -75,12 +76,12 @@ def _bind(lib):
     lib.hstu_oracle_valid.restype = ctypes.c_int
     lib.hstu_oracle_valid.argtypes = [c64, c64, c64, ctypes.c_int, c64, c64, c64]
     lib.hstu_oracle_fwd.restype = ctypes.c_int
-    lib.hstu_oracle_fwd.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, c64, i64, i64,
-                                    ctypes.c_int, c64, ctypes.c_double, ctypes.c_double,
+    lib.hstu_oracle_fwd.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, d, c64, i64,
+                                    i64, ctypes.c_int, c64, ctypes.c_double, ctypes.c_double,
                                     d, ctypes.c_int]
     lib.hstu_oracle_fwd_rows.restype = ctypes.c_int
-    lib.hstu_oracle_fwd_rows.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, c64, i64,
-                                         i64, ctypes.c_int, c64, ctypes.c_double,
+    lib.hstu_oracle_fwd_rows.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, d, c64,
+                                         i64, i64, ctypes.c_int, c64, ctypes.c_double,
                                          ctypes.c_double, i64, c64, d, ctypes.c_int]
     lib.hstu_oracle_count_valid.restype = ctypes.c_int64
     lib.hstu_oracle_count_valid.argtypes = [i64, c64, c64, i64, i64, ctypes.c_int, c64]
@@ -107,7 +108,8 @@ def _p(a, ty):
     return None if a is None else a.ctypes.data_as(ctypes.POINTER(ty))
 
 
-def _common(q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen):
+def _common(q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen, mask=None,
+            mask_type=MASK_CAUSAL):
     q, k, v = _f64(q), _f64(k), _f64(v)
     so = _i64(seq_offsets)
     if q.ndim != 3 or k.ndim != 3 or v.shape != k.shape or q.shape[2] != k.shape[2]:
@@ -123,17 +125,23 @@ def _common(q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen):
                 rab.shape != (B, rab.shape[1], max_seqlen, max_seqlen):
             raise ValueError(f"rab must be [B, Nq, S, S] or [B, 1, S, S], got {rab.shape}")
         rab_heads = rab.shape[1]
-    return q, k, v, so, B, rab, rab_heads, nc, nt
+    mask = _f64(mask)
+    if (mask is not None) != (mask_type == MASK_CUSTOM):
+        raise ValueError("a mask tensor is passed exactly with mask_type MASK_CUSTOM")
+    if mask is not None and (max_seqlen is None or
+                             mask.shape != (B, q.shape[1], max_seqlen, max_seqlen)):
+        raise ValueError("mask must be [B, Nq, S, S] with S = max_seqlen")
+    return q, k, v, so, B, rab, rab_heads, nc, nt, mask
 
 
 def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=None,
              mask_type=MASK_CAUSAL, target_group_size=0, alpha=1.0, silu_scale=None,
-             max_seqlen=None, nthreads=1):
+             max_seqlen=None, nthreads=1, mask=None):
     """Whole forward in fp64. Returns out [T, Nq, D] as float64 (rows outside
     every sequence are 0). silu_scale defaults to 1/max_seqlen (Inputs and
     Outputs table, silu_scale)."""
-    q, k, v, so, B, rab, rab_heads, nc, nt = _common(q, k, v, seq_offsets, rab, num_context,
-                                                     num_targets, max_seqlen)
+    q, k, v, so, B, rab, rab_heads, nc, nt, mask = _common(
+        q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen, mask, mask_type)
     if max_seqlen is None:
         max_seqlen = int(np.max(np.diff(so))) if B > 0 else 1
     if silu_scale is None:
@@ -142,7 +150,7 @@ def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=No
     rc = _load().hstu_oracle_fwd(_p(q, ctypes.c_double), _p(k, ctypes.c_double),
                                  _p(v, ctypes.c_double), _p(so, ctypes.c_int64), B, q.shape[1],
                                  k.shape[1], q.shape[2], _p(rab, ctypes.c_double), rab_heads,
-                                 max_seqlen,
+                                 _p(mask, ctypes.c_double), max_seqlen,
                                  _p(nc, ctypes.c_int64), _p(nt, ctypes.c_int64), mask_type,
                                  target_group_size, float(alpha), float(silu_scale),
                                  _p(out, ctypes.c_double), int(nthreads))
@@ -153,11 +161,11 @@ def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=No
 
 def hstu_fwd_rows(q, k, v, seq_offsets, rows, *, rab=None, num_context=None, num_targets=None,
                   mask_type=MASK_CAUSAL, target_group_size=0, alpha=1.0, silu_scale=None,
-                  max_seqlen=None, nthreads=1):
+                  max_seqlen=None, nthreads=1, mask=None):
     """Selected output rows: rows is an int array [n, 3] of (b, h, i) (i local to
     sequence b). Returns [n, D] float64, row r = out[seq_offsets[b] + i, h, :]."""
-    q, k, v, so, B, rab, rab_heads, nc, nt = _common(q, k, v, seq_offsets, rab, num_context,
-                                                     num_targets, max_seqlen)
+    q, k, v, so, B, rab, rab_heads, nc, nt, mask = _common(
+        q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen, mask, mask_type)
     if max_seqlen is None:
         max_seqlen = int(np.max(np.diff(so))) if B > 0 else 1
     if silu_scale is None:
@@ -167,7 +175,8 @@ def hstu_fwd_rows(q, k, v, seq_offsets, rows, *, rab=None, num_context=None, num
     rc = _load().hstu_oracle_fwd_rows(_p(q, ctypes.c_double), _p(k, ctypes.c_double),
                                       _p(v, ctypes.c_double), _p(so, ctypes.c_int64), B,
                                       q.shape[1], k.shape[1], q.shape[2],
-                                      _p(rab, ctypes.c_double), rab_heads, max_seqlen,
+                                      _p(rab, ctypes.c_double), rab_heads,
+                                      _p(mask, ctypes.c_double), max_seqlen,
                                       _p(nc, ctypes.c_int64), _p(nt, ctypes.c_int64), mask_type,
                                       target_group_size, float(alpha), float(silu_scale),
                                       _p(rows, ctypes.c_int64), rows.shape[0],

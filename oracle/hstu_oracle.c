@@ -16,7 +16,8 @@
  *   - Feature table, "Support causal mask": built from num_context, num_targets
  *     and target_group_size, any of which may be absent.
  *   - Inputs and Outputs table: jagged [s_b, N, D] layout with seq_offsets [B+1];
- *     mask_type 0 = built-in lower-triangular (causal) mask, 2 = no mask;
+ *     mask_type 0 = built-in lower-triangular (causal) mask, 2 = no mask, 3 = custom
+ *     mask passed in as mask [B, N, S, S] of q's type;
  *     silu_scale defaults to 1/max_seq_len; target_group_size 0 = no target
  *     mask; alpha = "alpha scaling parameter".
  *
@@ -33,6 +34,9 @@
  *                      && (i - H) / g == (j - H) / g)         targets: own group, causal
  *                  || (g == 0 && j <= i)                      no target mask: plain causal
  *   - A masked entry of P is exactly 0 (select, not multiply).
+ *   - Custom mask (mask_type 3): every key of the sequence is a candidate and P is
+ *     multiplied by mask[b, h, i, j] after the SiLU and the scaling (the chain's order);
+ *     a 0/1 mask selects exactly like the built-in one.
  *
  * Pinned by tests/test_oracle_pins.py: closed forms (L = 1, silu(ln 3) = 0.75 ln 3,
  * silu(x) - silu(-x) = x), the dense equal-length case against torch.matmul and
@@ -50,12 +54,15 @@
 
 #define ORACLE_MASK_CAUSAL 0 /* "0: built-in lower triangular mask" */
 #define ORACLE_MASK_NONE 2   /* "2: do not use a mask" */
+#define ORACLE_MASK_CUSTOM 3 /* "3: use a custom mask ... the user must pass in the mask" */
 
 /* The mask predicate (reading above). Returns 1 when query row i may attend key j. */
 int hstu_oracle_valid(int64_t i, int64_t j, int64_t L, int mask_type, int64_t nc,
                       int64_t nt, int64_t g) {
   if (i < 0 || j < 0 || i >= L || j >= L) return 0;
-  if (mask_type == ORACLE_MASK_NONE) return 1;
+  /* no mask, or a custom mask: every key of the sequence is a candidate (a custom mask
+     acts through its values, step 4 of the forward) */
+  if (mask_type == ORACLE_MASK_NONE || mask_type == ORACLE_MASK_CUSTOM) return 1;
   int64_t H = L;
   if (g > 0) {
     H = L - nt;
@@ -73,6 +80,7 @@ static double silu(double x) { return x / (1.0 + exp(-x)); }
 
 typedef struct {
   const double *q, *k, *v, *rab;
+  const double *mask; /* custom mask [B, Nq, S, S] (mask_type 3) */
   const int64_t *seq_offsets, *num_context, *num_targets;
   int64_t B, Nq, Nk, D, max_seqlen;
   int64_t rab_heads; /* rab planes per sequence: Nq, or 1 (broadcast to every head) */
@@ -114,8 +122,11 @@ static void one_row(const job_t *J, int64_t b, int64_t h, int64_t i, double *o) 
     double p = silu(x);
     /* 3. scaling */
     p *= J->silu_scale;
-    /* 4. mask application */
+    /* 4. mask application: the built-in mask selects; a custom mask multiplies P by
+       mask[b, h, i, j] (a 0/1 mask selects the same way) */
     if (!hstu_oracle_valid(i, j, L, J->mask_type, nc, nt, J->g)) p = 0.0;
+    if (J->mask_type == ORACLE_MASK_CUSTOM)
+      p *= J->mask[((b * J->Nq + h) * J->max_seqlen + i) * J->max_seqlen + j];
     /* 5. matrix multiplication with V */
     for (int64_t d = 0; d < D; ++d) o[d] += p * vj[d];
   }
@@ -167,27 +178,31 @@ static int run_pool(job_t *J, void *(*fn)(void *), int nthreads) {
 static int check_args(int64_t B, int64_t Nq, int64_t Nk, int64_t D, int mask_type) {
   if (B < 0 || Nq <= 0 || Nk <= 0 || D <= 0) return -1;
   if (Nq % Nk != 0) return -1;
-  if (mask_type != ORACLE_MASK_CAUSAL && mask_type != ORACLE_MASK_NONE) return -1;
+  if (mask_type != ORACLE_MASK_CAUSAL && mask_type != ORACLE_MASK_NONE &&
+      mask_type != ORACLE_MASK_CUSTOM)
+    return -1;
   return 0;
 }
 
 /*
  * Whole forward. q [T, Nq, D], k/v [T, Nk, D], rab [B, rab_heads, S, S] or NULL
- * (rab_heads = Nq, or 1 for a plane shared by all heads),
+ * (rab_heads = Nq, or 1 for a plane shared by all heads), mask [B, Nq, S, S] (custom
+ * mask, mask_type 3 only) or NULL,
  * seq_offsets [B+1], num_context/num_targets [B] or NULL; out [T, Nq, D].
  * Rows of out outside every sequence are left untouched. Returns 0 or -1.
  */
 int hstu_oracle_fwd(const double *q, const double *k, const double *v,
                     const int64_t *seq_offsets, int64_t B, int64_t Nq, int64_t Nk,
-                    int64_t D, const double *rab, int64_t rab_heads, int64_t max_seqlen,
-                    const int64_t *num_context, const int64_t *num_targets,
-                    int mask_type, int64_t target_group_size, double alpha,
-                    double silu_scale, double *out, int nthreads) {
+                    int64_t D, const double *rab, int64_t rab_heads, const double *mask,
+                    int64_t max_seqlen, const int64_t *num_context,
+                    const int64_t *num_targets, int mask_type, int64_t target_group_size,
+                    double alpha, double silu_scale, double *out, int nthreads) {
   if (check_args(B, Nq, Nk, D, mask_type)) return -1;
   if (rab && rab_heads != 1 && rab_heads != Nq) return -1;
+  if ((mask_type == ORACLE_MASK_CUSTOM) != (mask != NULL)) return -1;
   job_t J;
   memset(&J, 0, sizeof(J));
-  J.q = q; J.k = k; J.v = v; J.rab = rab;
+  J.q = q; J.k = k; J.v = v; J.rab = rab; J.mask = mask;
   J.seq_offsets = seq_offsets; J.num_context = num_context; J.num_targets = num_targets;
   J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen; J.rab_heads = rab_heads;
   J.mask_type = mask_type; J.g = target_group_size;
@@ -198,13 +213,15 @@ int hstu_oracle_fwd(const double *q, const double *k, const double *v,
 /* Selected rows only: rows[3r..3r+2] = (b, h, i); out_rows [nrows, D]. */
 int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
                          const int64_t *seq_offsets, int64_t B, int64_t Nq, int64_t Nk,
-                         int64_t D, const double *rab, int64_t rab_heads, int64_t max_seqlen,
+                         int64_t D, const double *rab, int64_t rab_heads,
+                         const double *mask, int64_t max_seqlen,
                          const int64_t *num_context, const int64_t *num_targets,
                          int mask_type, int64_t target_group_size, double alpha,
                          double silu_scale, const int64_t *rows, int64_t nrows,
                          double *out_rows, int nthreads) {
   if (check_args(B, Nq, Nk, D, mask_type)) return -1;
   if (rab && rab_heads != 1 && rab_heads != Nq) return -1;
+  if ((mask_type == ORACLE_MASK_CUSTOM) != (mask != NULL)) return -1;
   for (int64_t r = 0; r < nrows; ++r) {
     const int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
     if (b < 0 || b >= B || h < 0 || h >= Nq || i < 0 ||
@@ -213,7 +230,7 @@ int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
   }
   job_t J;
   memset(&J, 0, sizeof(J));
-  J.q = q; J.k = k; J.v = v; J.rab = rab;
+  J.q = q; J.k = k; J.v = v; J.rab = rab; J.mask = mask;
   J.seq_offsets = seq_offsets; J.num_context = num_context; J.num_targets = num_targets;
   J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen; J.rab_heads = rab_heads;
   J.mask_type = mask_type; J.g = target_group_size;

@@ -31,7 +31,12 @@ MUTATIONS = [
     ("dropped_scale", "p *= J->silu_scale;", "p *= 1.0;"),
     ("v_row_of_query", "const double *vj = J->v + ((t0 + j) * J->Nk + hk) * D;",
      "const double *vj = J->v + ((t0 + i) * J->Nk + hk) * D;"),
-    ("mask_none_causal", "if (mask_type == ORACLE_MASK_NONE) return 1;", ""),
+    ("mask_none_causal", "if (mask_type == ORACLE_MASK_NONE || mask_type == ORACLE_MASK_CUSTOM) return 1;",
+     "if (mask_type == ORACLE_MASK_CUSTOM) return 1;"),
+    ("custom_mask_ignored", "p *= J->mask[", "p *= 1.0 + 0.0 * J->mask["),
+    ("custom_mask_before_silu", "    double p = silu(x);", "    if (J->mask_type == ORACLE_MASK_CUSTOM)\n"
+     "      x *= J->mask[((b * J->Nq + h) * J->max_seqlen + i) * J->max_seqlen + j];\n"
+     "    double p = silu(x);"),
 ]
 # a real transposition: Q row j against K row i
 MUTATIONS[0] = ("transposed_scores",
@@ -46,7 +51,8 @@ def _pin_checks():
               pins.test_count_valid_closed_forms, pins.test_q_zero_without_rab_gives_zero,
               pins.test_causal_rows_ignore_later_keys, pins.test_gqa_equals_replicated_mha,
               lambda: pins.test_q_zero_rab_per_head_and_broadcast_closed_form(1),
-              lambda: pins.test_q_zero_rab_per_head_and_broadcast_closed_form(3)]
+              lambda: pins.test_q_zero_rab_per_head_and_broadcast_closed_form(3),
+              pins.test_custom_mask_closed_forms]
     for causal in (False, True):
         for nq, nk in ((4, 4), (4, 2), (6, 1)):
             checks.append(lambda c=causal, a=nq, b=nk: pins.test_equal_lengths_match_torch_matmul(c, a, b))

@@ -114,6 +114,41 @@ def test_q_zero_rab_per_head_and_broadcast_closed_form(rab_heads):
                                        atol=1e-12)
 
 
+def test_custom_mask_closed_forms():
+    """Custom mask (mask_type 3, Inputs and Outputs table): an all-ones mask gives the
+    unmasked forward; the built-in causal 0/1 matrix as a custom mask gives the causal
+    forward; Q = 0 with a general mask M gives out_i = silu_scale * sum_j silu(0) ... = 0,
+    so a rab R is used instead: out_i = silu_scale * sum_j silu(R_ij) * M_ij * v_j
+    (mask applied after SiLU and scaling; silu from torch)."""
+    rng = _rng(14)
+    lengths = [5, 7]
+    q, k, v, so = _jagged(rng, lengths, 2, 1, 3)
+    S = 7
+    ones = np.ones((2, 2, S, S))
+    a = oracle.hstu_fwd(q, k, v, so, mask=ones, mask_type=oracle.MASK_CUSTOM, max_seqlen=S,
+                        alpha=0.7, silu_scale=0.3)
+    b = oracle.hstu_fwd(q, k, v, so, mask_type=oracle.MASK_NONE, max_seqlen=S, alpha=0.7,
+                        silu_scale=0.3)
+    np.testing.assert_array_equal(a, b)
+    causal = np.tril(np.ones((S, S)))[None, None].repeat(2, 0).repeat(2, 1)
+    a = oracle.hstu_fwd(q, k, v, so, mask=causal, mask_type=oracle.MASK_CUSTOM, max_seqlen=S,
+                        alpha=0.7, silu_scale=0.3)
+    b = oracle.hstu_fwd(q, k, v, so, mask_type=oracle.MASK_CAUSAL, max_seqlen=S, alpha=0.7,
+                        silu_scale=0.3)
+    np.testing.assert_array_equal(a, b)
+    q[:] = 0.0
+    R = rng.standard_normal((2, 2, S, S))
+    M = rng.uniform(-1.0, 2.0, (2, 2, S, S))
+    out = oracle.hstu_fwd(q, k, v, so, rab=R, mask=M, mask_type=oracle.MASK_CUSTOM,
+                          max_seqlen=S, alpha=1.5, silu_scale=0.25)
+    for bi, L in enumerate(lengths):
+        t0 = so[bi]
+        for h in range(2):
+            p = F.silu(torch.from_numpy(R[bi, h, :L, :L])).numpy() * M[bi, h, :L, :L]
+            np.testing.assert_allclose(out[t0:t0 + L, h], 0.25 * p @ v[t0:t0 + L, 0], rtol=0,
+                                       atol=1e-12)
+
+
 # --------------------------------------------------------------------------- library cases
 def _torch_dense(q, k, v, rab, alpha, scale, causal):
     """Equal-length, no-context/no-target case with torch fp64 library ops.
