@@ -29,7 +29,7 @@ _DTYPES = {torch.float32: _abi.HSTU_F32, torch.float16: _abi.HSTU_F16,
 
 def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, index_is_int64,
           causal, target_group_size, has_rab, has_num_context, has_num_targets, watchdog_ms=0,
-          layout="jagged", rab_heads=0):
+          layout="jagged", rab_heads=0, custom_mask=False):
     d = _abi.Desc()
     d.dtype = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     d.batch = int(batch)
@@ -38,7 +38,8 @@ def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, inde
     d.head_dim = int(head_dim)
     d.max_seqlen = int(max_seqlen)
     d.index_is_int64 = int(bool(index_is_int64))
-    d.mask_type = _abi.HSTU_MASK_CAUSAL if causal else _abi.HSTU_MASK_NONE
+    d.mask_type = (_abi.HSTU_MASK_CUSTOM if custom_mask else
+                   _abi.HSTU_MASK_CAUSAL if causal else _abi.HSTU_MASK_NONE)
     d.target_group_size = int(target_group_size)
     d.has_rab = int(bool(has_rab))
     d.has_num_context = int(bool(has_num_context))
@@ -72,12 +73,18 @@ class HstuFwdPlan:
                                            out, stream or None), "hstu_fwd_run")
 
     def run(self, q, k, v, seq_offsets, out, *, rab=None, num_context=None, num_targets=None,
-            alpha=1.0, silu_scale=None, stream=None):
+            alpha=1.0, silu_scale=None, stream=None, mask=None):
         if silu_scale is None:
             silu_scale = 1.0 / self.desc.max_seqlen
         if stream is None:
             stream = torch.cuda.current_stream(q.device)
         ptr = lambda t: 0 if t is None else t.data_ptr()
+        if self.desc.mask_type == _abi.HSTU_MASK_CUSTOM:
+            _abi.check(self._keep.hstu_fwd_run_masked(
+                self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), ptr(seq_offsets) or None,
+                ptr(mask) or None, q.shape[0], float(alpha), float(silu_scale), out.data_ptr(),
+                stream.cuda_stream or None), "hstu_fwd_run_masked")
+            return out
         self.run_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), ptr(seq_offsets), ptr(rab),
                      ptr(num_context), ptr(num_targets), q.shape[0], alpha, silu_scale,
                      out.data_ptr(), stream.cuda_stream)
@@ -136,7 +143,7 @@ def _rab_heads(rab, B, Nq, S):
 
 def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_context=None,
              num_targets=None, causal=True, target_group_size=0, alpha=1.0, silu_scale=None,
-             out=None, watchdog_ms=0, layout="jagged"):
+             out=None, watchdog_ms=0, layout="jagged", mask=None):
     """HSTU forward.
 
     layout "jagged" (default): q [T, Nq, D], k/v [T, Nk, D], seq_offsets [B+1] int32/int64,
@@ -144,9 +151,10 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     k/v [B, S, Nk, D], every sequence of S tokens, no seq_offsets, max_seqlen = S.
     Same dtype for q, k, v: fp32, fp16 or bf16. num_context / num_targets [B] of the index
     dtype (int32/int64). rab [B, Nq, S, S] or [B, 1, S, S] (one plane for all heads) of q's
-    dtype, or None. causal=False is mask_type 2 (no mask). silu_scale defaults to
-    1/max_seqlen. Returns out with q's shape; rows that belong to no sequence are left as
-    allocated.
+    dtype, or None. causal=False is mask_type 2 (no mask). mask [B, Nq, S, S] of q's dtype
+    selects mask_type 3 (custom mask: P is multiplied by it after the SiLU; no rab, context
+    or target counts with it). silu_scale defaults to 1/max_seqlen. Returns out with q's
+    shape; rows that belong to no sequence are left as allocated.
     """
     dev = q.device
     if dev.type != "cuda":
@@ -206,10 +214,18 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     if rab is not None:
         _check_tensor(rab, "rab", q.dtype, dev, 4)
     rab_heads = _rab_heads(rab, B, Nq, int(max_seqlen))
+    custom = mask is not None
+    if custom:
+        if rab is not None or num_context is not None or num_targets is not None:
+            raise ValueError("a custom mask takes no rab, num_context or num_targets")
+        _check_tensor(mask, "mask", q.dtype, dev, 4)
+        if tuple(mask.shape) != (B, Nq, int(max_seqlen), int(max_seqlen)):
+            raise ValueError(f"mask must be [B, Nq, S, S], got {list(mask.shape)}")
     stream = torch.cuda.current_stream(dev)
     key = (dev.index, stream.cuda_stream, q.dtype, B, Nq, k3.shape[1], D, int(max_seqlen),
            idx_dtype, bool(causal), int(target_group_size), rab is not None,
-           num_context is not None, num_targets is not None, int(watchdog_ms), layout, rab_heads)
+           num_context is not None, num_targets is not None, int(watchdog_ms), layout, rab_heads,
+           custom)
     plan = _plans.get(key)
     if plan is None:
         with torch.cuda.device(dev):
@@ -219,11 +235,12 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
                                target_group_size=target_group_size, has_rab=rab is not None,
                                has_num_context=num_context is not None,
                                has_num_targets=num_targets is not None, watchdog_ms=watchdog_ms,
-                               layout=layout, rab_heads=rab_heads)
+                               layout=layout, rab_heads=rab_heads, custom_mask=custom)
         _plans[key] = plan
     with torch.cuda.device(dev):
         plan.run(q3, k3, v3, seq_offsets, out3, rab=rab, num_context=num_context,
-                 num_targets=num_targets, alpha=alpha, silu_scale=silu_scale, stream=stream)
+                 num_targets=num_targets, alpha=alpha, silu_scale=silu_scale, stream=stream,
+                 mask=mask)
     return res
 
 

@@ -81,6 +81,8 @@ def lib():
         L.hstu_fwd_count_pairs.restype = ctypes.c_int
         L.hstu_fwd_count_pairs.argtypes = [ctypes.POINTER(Desc), vp, vp, vp,
                                            ctypes.POINTER(ctypes.c_longlong)]
+        L.hstu_fwd_run_masked.restype = ctypes.c_int
+        L.hstu_fwd_run_masked.argtypes = [vp, vp, vp, vp, vp, vp, ll, f, f, vp, vp]
         L.hstu_fwd_run_noalloc.restype = ctypes.c_int
         L.hstu_fwd_run_noalloc.argtypes = [ctypes.POINTER(Desc), vp, vp, vp, vp, vp, vp, vp, ll, f,
                                            f, vp, vp]

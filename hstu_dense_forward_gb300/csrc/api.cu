@@ -101,10 +101,17 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
   if (d->max_seqlen < 1 || d->max_seqlen > hstu::kMaxMTiles * hstu::kTileM)
     return HSTU_ERR_INVALID_ARG;
   if (d->target_group_size < 0 || d->watchdog_ms < 0) return HSTU_ERR_INVALID_ARG;
-  if (d->mask_type == HSTU_MASK_UPPER || d->mask_type == HSTU_MASK_CUSTOM)
-    return HSTU_ERR_UNSUPPORTED;
-  if (d->mask_type != HSTU_MASK_CAUSAL && d->mask_type != HSTU_MASK_NONE)
+  if (d->mask_type == HSTU_MASK_UPPER) return HSTU_ERR_UNSUPPORTED;  // "currently not supported"
+  if (d->mask_type != HSTU_MASK_CAUSAL && d->mask_type != HSTU_MASK_NONE &&
+      d->mask_type != HSTU_MASK_CUSTOM)
     return HSTU_ERR_INVALID_ARG;
+  if (d->mask_type == HSTU_MASK_CUSTOM) {
+    // the mask replaces the built-in one (no context / target counts); it streams through
+    // the rab path, so rab and a custom mask together are not built
+    if (d->has_num_context || d->has_num_targets || d->rab_heads) return HSTU_ERR_INVALID_ARG;
+    if (d->has_rab) return HSTU_ERR_UNSUPPORTED;
+    if (d->dtype != HSTU_F32 && d->max_seqlen % 8 != 0) return HSTU_ERR_UNSUPPORTED;
+  }
   if (d->dtype == HSTU_F32) {
     if (d->head_dim > 256) return HSTU_ERR_UNSUPPORTED;
   } else {
@@ -136,7 +143,9 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
         delete P;
         return HSTU_ERR_UNSUPPORTED;
       }
-      e = hstu::tc_prepare(desc->head_dim, desc->dtype == HSTU_BF16, desc->has_rab);
+      // kernel variant: 0 no rab, 1 rab, 2 custom mask (streamed like rab)
+      e = hstu::tc_prepare(desc->head_dim, desc->dtype == HSTU_BF16,
+                           desc->mask_type == HSTU_MASK_CUSTOM ? 2 : (desc->has_rab ? 1 : 0));
       P->grid = P->num_sms;
     } else {
       e = hstu::simt_prepare();
@@ -220,17 +229,19 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
   return HSTU_OK;
 }
 
-hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
-                         const void* seq_offsets, const void* rab, const void* num_context,
-                         const void* num_targets, long long total_tokens, float alpha,
-                         float silu_scale, void* out, void* stream) {
-  if (!P) return HSTU_ERR_INVALID_ARG;
+// One forward. `rab` carries the relative attention bias, or the custom mask when
+// is_mask (plans of mask_type CUSTOM, through hstu_fwd_run_masked).
+static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
+                            const void* seq_offsets, const void* rab, bool is_mask,
+                            const void* num_context, const void* num_targets,
+                            long long total_tokens, float alpha, float silu_scale, void* out,
+                            void* stream) {
   const hstu_fwd_desc& d = P->desc;
   if (total_tokens < 0 || total_tokens > 0x7fffffffll) return HSTU_ERR_INVALID_ARG;
   if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
   if (!q || !k || !v || !out || !layout_args_ok(d, seq_offsets, total_tokens))
     return HSTU_ERR_INVALID_ARG;
-  if ((rab != nullptr) != (d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
+  if ((rab != nullptr) != (is_mask || d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
   if ((num_context != nullptr) != (d.has_num_context != 0)) return HSTU_ERR_INVALID_ARG;
   if ((num_targets != nullptr) != (d.has_num_targets != 0)) return HSTU_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
@@ -263,10 +274,11 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
   p.Nk = d.num_heads_kv;
   p.D = d.head_dim;
   p.S = d.max_seqlen;
-  p.mask_type = d.mask_type;
+  p.mask_type = is_mask ? hstu::kMaskNone : d.mask_type;  // a custom mask: every key a candidate
   p.g = d.mask_type == HSTU_MASK_CAUSAL ? d.target_group_size : 0;
   p.dense = d.layout == HSTU_LAYOUT_NORMAL ? 1 : 0;
   p.rab_bcast = d.rab_heads == 1 ? 1 : 0;
+  p.rab_is_mask = is_mask ? 1 : 0;
   p.alpha = alpha;
   p.silu_scale = silu_scale;
 
@@ -281,6 +293,26 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
                       ? hstu::launch_fwd_tc(p, P->maps, d.dtype == HSTU_BF16, P->grid, st, true)
                       : hstu::launch_fwd_simt(p, P->grid, st, true);
   return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
+}
+
+hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
+                         const void* seq_offsets, const void* rab, const void* num_context,
+                         const void* num_targets, long long total_tokens, float alpha,
+                         float silu_scale, void* out, void* stream) {
+  if (!P || P->desc.mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_INVALID_ARG;
+  return run_impl(P, q, k, v, seq_offsets, rab, false, num_context, num_targets, total_tokens,
+                  alpha, silu_scale, out, stream);
+}
+
+hstu_status hstu_fwd_run_masked(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
+                                const void* seq_offsets, const void* mask,
+                                long long total_tokens, float alpha, float silu_scale,
+                                void* out, void* stream) {
+  if (!P || P->desc.mask_type != HSTU_MASK_CUSTOM) return HSTU_ERR_INVALID_ARG;
+  if (!mask && P->desc.batch > 0 && P->desc.num_heads_q > 0 && total_tokens > 0)
+    return HSTU_ERR_INVALID_ARG;
+  return run_impl(P, q, k, v, seq_offsets, mask, true, nullptr, nullptr, total_tokens, alpha,
+                  silu_scale, out, stream);
 }
 
 hstu_status hstu_fwd_destroy(hstu_fwd_plan* P) {
@@ -318,10 +350,13 @@ hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* d, const void* seq_offsets
   const bool normal = d->layout == HSTU_LAYOUT_NORMAL;
   if (normal ? seq_offsets_host != nullptr : (d->batch > 0 && !seq_offsets_host))
     return HSTU_ERR_INVALID_ARG;
-  if (d->mask_type != HSTU_MASK_CAUSAL && d->mask_type != HSTU_MASK_NONE)
+  if (d->mask_type != HSTU_MASK_CAUSAL && d->mask_type != HSTU_MASK_NONE &&
+      d->mask_type != HSTU_MASK_CUSTOM)
     return HSTU_ERR_UNSUPPORTED;
   const int is64 = d->index_is_int64 ? 1 : 0;
   const int g = d->mask_type == HSTU_MASK_CAUSAL ? d->target_group_size : 0;
+  // a custom mask makes every (i, j) of the sequence a computed pair
+  const int mt = d->mask_type == HSTU_MASK_CUSTOM ? HSTU_MASK_NONE : d->mask_type;
   long long total = 0;
   for (int b = 0; b < d->batch; ++b) {
     const long long t0 = normal ? (long long)b * d->max_seqlen
@@ -331,10 +366,10 @@ hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* d, const void* seq_offsets
     if (L < 0 || L > d->max_seqlen) return HSTU_ERR_INVALID_ARG;
     const long long nc = num_context_host ? hstu::load_index(num_context_host, b, is64) : 0;
     const long long nt = num_targets_host ? hstu::load_index(num_targets_host, b, is64) : 0;
-    const hstu::SeqGeom s = hstu::make_geom((int)L, nc, nt, g, d->mask_type);
+    const hstu::SeqGeom s = hstu::make_geom((int)L, nc, nt, g, mt);
     long long c = 0;
     for (int i = 0; i < (int)L; ++i) {
-      const hstu::RowRange r = hstu::row_range(s, i, d->mask_type);
+      const hstu::RowRange r = hstu::row_range(s, i, mt);
       c += r.hist_end;
       if (r.grp_hi >= r.grp_lo) c += r.grp_hi - r.grp_lo + 1;
     }
@@ -401,6 +436,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
   if ((long long)d.batch * hstu::ceil_div(d.max_seqlen, hstu::kTileM) > HSTU_NOALLOC_MAX_ENTRIES)
     return HSTU_ERR_UNSUPPORTED;  // work list larger than the static scratch array
+  if (d.mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_UNSUPPORTED;  // hstu_fwd_run_masked only
   if (!q || !k || !v || !out || !layout_args_ok(d, seq_offsets, total_tokens))
     return HSTU_ERR_INVALID_ARG;
   if ((rab != nullptr) != (d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;

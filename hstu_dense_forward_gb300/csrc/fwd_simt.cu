@@ -110,9 +110,11 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams 
           const int j = n0 + tx + 16 * c;
           float x = p.alpha * sc[a][c];
           const bool ok = (i < L) && (j < L) && valid_in_range(rr, j);
-          if (rab != nullptr && ok)
-            x += rab[(rab_plane(p, b, h) * p.S + i) * p.S + j];
-          const float pv = x / (1.0f + expf(-x));
+          const float t = (rab != nullptr && ok) ? rab[(rab_plane(p, b, h) * p.S + i) * p.S + j]
+                                                 : 0.f;
+          if (!p.rab_is_mask) x += t;  // relative attention bias before the SiLU
+          float pv = x / (1.0f + expf(-x));
+          if (p.rab_is_mask) pv *= t;  // custom mask after it
           Ps[r * (BN + 1) + tx + 16 * c] = ok ? pv : 0.f;
         }
       }

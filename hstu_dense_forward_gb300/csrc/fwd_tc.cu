@@ -1,5 +1,6 @@
-// Instantiations and launch of the tensor-core forward kernel.
-#include "fwd_tc.cuh"
+// Instantiations and launch of the tensor-core forward kernel (the custom-mask variants
+// are instantiated in fwd_tc_mask.cu, a translation unit of their own).
+#include "fwd_tc_launch.cuh"
 
 namespace hstu {
 
@@ -7,25 +8,13 @@ namespace {
 
 template <int D, bool BF16, bool RAB>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(tc::fwd_tc_kernel<D, BF16, RAB>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              tc::Cfg<D, RAB>::SMEM_BYTES);
+  return tc::prepare_one<D, BF16, RAB, false>();
 }
 
 template <int D, bool BF16, bool RAB>
 cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t stream,
                        bool pdl) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(tc::kThreads);
-  cfg.dynamicSmemBytes = tc::Cfg<D, RAB>::SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc::fwd_tc_kernel<D, BF16, RAB>, m.q, m.k, m.v, m.rab, m.out, p);
+  return tc::launch_one<D, BF16, RAB, false>(p, m, grid, stream, pdl);
 }
 
 template <bool BF16, bool RAB>
@@ -42,6 +31,7 @@ cudaError_t dispatch_d(const FwdParams& p, const TcMaps& m, int grid, cudaStream
 
 cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cudaStream_t st,
                      bool pdl, bool prepare) {
+  if (p.rab_is_mask) return tc::dispatch_mask(p, m, bf16, grid, st, pdl, prepare);
   const bool rab = p.rab != nullptr;
   if (bf16) return rab ? dispatch_d<true, true>(p, m, grid, st, pdl, prepare)
                        : dispatch_d<true, false>(p, m, grid, st, pdl, prepare);
@@ -61,6 +51,7 @@ cudaError_t tc_prepare(int D, int bf16, int rab) {
   FwdParams p = {};
   p.D = D;
   p.rab = rab ? reinterpret_cast<const void*>(1) : nullptr;
+  p.rab_is_mask = rab == 2 ? 1 : 0;
   TcMaps m = {};
   return dispatch(p, m, bf16, 0, nullptr, false, true);
 }

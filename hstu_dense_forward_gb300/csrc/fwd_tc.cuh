@@ -591,7 +591,7 @@ __device__ __forceinline__ bool epi_barrier(Bars* bars, uint32_t& phase, const F
   return ok;
 }
 
-template <int D, bool BF16, bool RAB>
+template <int D, bool BF16, bool RAB, bool MASK>
 __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                          const CUtensorMap* tm_o, long long total, int warp, int lane) {
   using C = Cfg<D, RAB>;
@@ -707,7 +707,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         if constexpr (RAB) {
           // rab tile: two 64-column TMA boxes of 128 rows x 128 bytes, 128-byte swizzle.
           // h = alpha*s/2 is rounded to the 16-bit type and rab/2 is added in packed
-          // form (one fused multiply-add per pair); a masked pair half becomes 0.
+          // form (one fused multiply-add per pair); a masked pair half becomes 0. When the
+          // stream carries a custom mask instead, P is multiplied by it after the SiLU.
           const uint8_t* box = rab_row + (cc >> 6) * (C::RAB_BYTES / 2);
           const uint32_t m = full ? 0xffffffffu : chunk_mask(rr, n0 + cc);
           const uint32_t half2 = BF16 ? 0x3f003f00u : 0x38003800u;  // (0.5, 0.5)
@@ -721,12 +722,14 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
               const int c2 = q4 * 4 + e;  // pair index: columns 2*c2, 2*c2 + 1
               uint32_t h2 = pack2<BF16>(__uint_as_float(sv[2 * c2]) * half_alpha,
                                         __uint_as_float(sv[2 * c2 + 1]) * half_alpha);
-              h2 = fma2<BF16>(ww[e], half2, h2);
+              if constexpr (!MASK) h2 = fma2<BF16>(ww[e], half2, h2);
               if (!full) {
                 const uint32_t lo = (m >> (2 * c2)) & 1u, hi = (m >> (2 * c2 + 1)) & 1u;
                 h2 &= (lo * 0x0000ffffu) | (hi * 0xffff0000u);
               }
               pk[c2] = fma2<BF16>(h2, tanh2<BF16>(h2), h2);
+              // custom mask: P times the mask pair (adding -0 keeps the product exact)
+              if constexpr (MASK) pk[c2] = fma2<BF16>(pk[c2], ww[e], 0x80008000u);
             }
           }
         } else {
@@ -785,7 +788,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool BF16, bool RAB>
+// MASK: the rab stream carries a custom mask (multiplied into P after the SiLU).
+template <int D, bool BF16, bool RAB, bool MASK = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
@@ -856,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long total = (long long)(*p.work_count) * p.Nq;
 
   if (warp < kEpiWarps) {
-    epilogue<D, BF16, RAB>(p, bars, smem, tmem, &tm_o, total, warp, lane);
+    epilogue<D, BF16, RAB, MASK>(p, bars, smem, tmem, &tm_o, total, warp, lane);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_k<D, RAB>(p, bars, smem, &tm_k, total);
   } else if (warp == kQProducerWarp) {

@@ -27,6 +27,9 @@ struct FwdParams {
   int mask_type, g;         // mask code, target group size
   int dense;                // normal layout: sequence b is tokens [b * S, (b + 1) * S)
   int rab_bcast;            // rab [B, 1, S, S]: one bias plane for every query head
+  int rab_is_mask;          // the rab stream carries a custom mask [B, Nq, S, S]: P is
+                            // multiplied by it after the SiLU instead of rab being added
+                            // before (mask_type is then NONE for the tile geometry)
   float alpha, silu_scale;
 };
 
@@ -61,7 +64,7 @@ struct TcMaps {
 bool tc_supported_dim(int D);
 int tc_swizzle_bytes(int D);  // row width of one TMA box / UMMA swizzle atom
 int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
-cudaError_t tc_prepare(int D, int bf16, int rab);
+cudaError_t tc_prepare(int D, int bf16, int rab);  // rab: 0 none, 1 rab, 2 custom mask
 cudaError_t launch_fwd_tc(const FwdParams& p, const TcMaps& maps, int bf16, int grid,
                           cudaStream_t stream, bool pdl);
 

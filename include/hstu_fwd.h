@@ -71,12 +71,14 @@ typedef enum { HSTU_F32 = 0, HSTU_F16 = 1, HSTU_BF16 = 2 } hstu_dtype;
 typedef enum { HSTU_LAYOUT_JAGGED = 0, HSTU_LAYOUT_NORMAL = 1 } hstu_layout;
 
 /* mask_type codes of the Inputs and Outputs table. UPPER ("currently not
- * supported" on the page) and CUSTOM are rejected with HSTU_ERR_UNSUPPORTED. */
+ * supported" on the page) is rejected with HSTU_ERR_UNSUPPORTED. */
 typedef enum {
   HSTU_MASK_CAUSAL = 0, /* built-in lower-triangular mask with context/targets */
   HSTU_MASK_UPPER = 1,
   HSTU_MASK_NONE = 2,   /* bidirectional: no mask */
-  HSTU_MASK_CUSTOM = 3
+  HSTU_MASK_CUSTOM = 3  /* mask [B, Nq, S, S] passed to hstu_fwd_run_masked: P is multiplied
+                           by mask[b, h, i, j] after the SiLU and the scaling; no context or
+                           target counts, no rab with it (HSTU_ERR_UNSUPPORTED) */
 } hstu_mask_type;
 
 /* Device error word values (hstu_fwd_get_error). */
@@ -134,6 +136,20 @@ HSTU_API hstu_status hstu_fwd_run(hstu_fwd_plan* plan, const void* q, const void
                          const void* seq_offsets, const void* rab, const void* num_context,
                          const void* num_targets, long long total_tokens, float alpha,
                          float silu_scale, void* out, void* stream);
+
+/*
+ * Enqueue one forward of a plan created with mask_type HSTU_MASK_CUSTOM ("3: use a
+ * custom mask; the user must define and pass in the mask", Inputs and Outputs table).
+ *   mask [B, Nq, S, S] of the plan's dtype, 16-byte aligned; every other argument as
+ *   for hstu_fwd_run (no rab, num_context or num_targets). Every key j < L of a
+ *   sequence is a candidate and P(i, j) is multiplied by mask[b, h, i, j]; a 0/1 mask
+ *   selects. Returns HSTU_ERR_INVALID_ARG for a plan of another mask type (and
+ *   hstu_fwd_run does for a CUSTOM plan).
+ */
+HSTU_API hstu_status hstu_fwd_run_masked(hstu_fwd_plan* plan, const void* q, const void* k,
+                                         const void* v, const void* seq_offsets,
+                                         const void* mask, long long total_tokens, float alpha,
+                                         float silu_scale, void* out, void* stream);
 
 /* Free the workspace. NULL is accepted. Synchronises the device first. */
 HSTU_API hstu_status hstu_fwd_destroy(hstu_fwd_plan* plan);

@@ -34,7 +34,10 @@ def _desc(**kw):
 @pytest.mark.parametrize("kw,status", [
     (dict(num_heads_q=3, num_heads_kv=2), _abi.HSTU_ERR_INVALID_ARG),   # Nq % Nk != 0
     (dict(mask_type=_abi.HSTU_MASK_UPPER), _abi.HSTU_ERR_UNSUPPORTED),  # "currently not supported"
-    (dict(mask_type=_abi.HSTU_MASK_CUSTOM), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(mask_type=_abi.HSTU_MASK_CUSTOM, has_rab=1), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(mask_type=_abi.HSTU_MASK_CUSTOM, has_num_targets=1), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(mask_type=_abi.HSTU_MASK_CUSTOM, rab_heads=1), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(mask_type=_abi.HSTU_MASK_CUSTOM, max_seqlen=100), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(mask_type=7), _abi.HSTU_ERR_INVALID_ARG),
     (dict(head_dim=48), _abi.HSTU_ERR_UNSUPPORTED),                      # no tensor-core tile
     (dict(dtype=_abi.HSTU_F32, head_dim=300), _abi.HSTU_ERR_UNSUPPORTED),
@@ -125,3 +128,15 @@ def test_rab_broadcast_descriptor_accepted(built_lib):
         assert st in (_abi.HSTU_OK, _abi.HSTU_ERR_UNSUPPORTED, _abi.HSTU_ERR_CUDA)
         if h.value:
             lib.hstu_fwd_destroy(h)
+
+
+def test_count_pairs_custom_mask_counts_every_pair(built_lib):
+    """With a custom mask every (i, j) of a sequence is computed (its values act as
+    weights), so the work count is that of no mask."""
+    lib = _abi.lib()
+    so = (ctypes.c_longlong * 3)(0, 100, 250)
+    out = ctypes.c_longlong(0)
+    d = _desc(mask_type=_abi.HSTU_MASK_CUSTOM, max_seqlen=256)
+    assert lib.hstu_fwd_count_pairs(ctypes.byref(d), so, None, None,
+                                    ctypes.byref(out)) == _abi.HSTU_OK
+    assert out.value == 4 * (100 ** 2 + 150 ** 2)

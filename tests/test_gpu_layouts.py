@@ -1,7 +1,7 @@
-"""The normal layout (Inputs and Outputs table, layout: q [B, S, N, D]) and the rab
-broadcast form [B, 1, S, S] (feature table, "Support for rab broadcasting"), through the
-C ABI: against the fp64 oracle, and bit for bit against the equivalent jagged call / the
-rab replicated to every head (same arithmetic, so the results must be identical)."""
+"""The normal layout (Inputs and Outputs table, layout: q [B, S, N, D]), the rab
+broadcast form [B, 1, S, S] (feature table, "Support for rab broadcasting") and the custom
+mask (mask_type 3), through the C ABI: against the fp64 oracle, and against the equivalent
+jagged call / the rab replicated to every head / the built-in causal mask."""
 from dataclasses import replace
 
 import numpy as np
@@ -116,3 +116,51 @@ def test_rab_broadcast_allocation_free_entry(cuda_device):
     torch.cuda.synchronize()
     T = int(inp["seq_offsets"][-1])
     assert torch.equal(out[:T], ref[:T])
+
+
+def _mask_case(dtype, d, heads, S=264, binary=False, seed=31):
+    w = W.scaled(BASE, batch=3, max_seqlen=S, len_lo=1, len_hi=S, dtype=dtype, head_dim=d,
+                 num_heads_q=heads[0], num_heads_kv=heads[1], causal=False)
+    inp = W.generate(w)
+    g = torch.Generator().manual_seed(seed)
+    if binary:
+        m = (torch.rand(3, heads[0], S, S, generator=g) < 0.6).float()
+    else:
+        m = torch.rand(3, heads[0], S, S, generator=g) * 3.0 - 1.0  # weights in [-1, 2)
+    return inp, m.to(W.DTYPES[dtype])
+
+
+@pytest.mark.parametrize("dtype,d,heads,binary", [("bf16", 128, (4, 4), False),
+                                                  ("fp16", 64, (8, 2), True),
+                                                  ("bf16", 256, (2, 2), False),
+                                                  ("fp32", 64, (2, 1), False)])
+def test_custom_mask_against_oracle(cuda_device, dtype, d, heads, binary):
+    """mask_type 3: P multiplied by mask[b, h, i, j] after the SiLU and the scaling."""
+    inp, m = _mask_case(dtype, d, heads, binary=binary)
+    dv = W.to_device(inp, cuda_device)
+    got = hstu_fwd(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], max_seqlen=264,
+                   alpha=inp["alpha"], silu_scale=inp["silu_scale"], mask=m.to(cuda_device))
+    torch.cuda.synchronize()
+    ref = oracle.hstu_fwd(inp["q"], inp["k"], inp["v"], inp["seq_offsets"], mask=m,
+                          mask_type=oracle.MASK_CUSTOM, alpha=inp["alpha"],
+                          silu_scale=inp["silu_scale"], max_seqlen=264, nthreads=8)
+    T = int(inp["seq_offsets"][-1])
+    assert _rel_err(got[:T], ref[:T]) <= TOL[dtype]
+
+
+def test_custom_causal_mask_matches_builtin(cuda_device):
+    """The built-in causal mask written out as a 0/1 custom mask gives the same output
+    (the custom path computes the tiles above the diagonal and multiplies them by 0)."""
+    inp, _ = _mask_case("bf16", 128, (4, 4))
+    dv = W.to_device(inp, cuda_device)
+    S = 264
+    causal = torch.tril(torch.ones(S, S)).to(torch.bfloat16)
+    m = causal[None, None].expand(3, 4, S, S).contiguous().to(cuda_device)
+    got = hstu_fwd(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], max_seqlen=S,
+                   alpha=inp["alpha"], silu_scale=inp["silu_scale"], mask=m)
+    ref = hstu_fwd(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], max_seqlen=S,
+                   alpha=inp["alpha"], silu_scale=inp["silu_scale"], causal=True)
+    torch.cuda.synchronize()
+    T = int(inp["seq_offsets"][-1])
+    g, r = got[:T].float(), ref[:T].float()
+    assert float((g - r).abs().max()) <= 1e-3 * float(r.abs().max())
