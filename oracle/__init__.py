@@ -75,16 +75,19 @@ def _bind(lib):
     c64 = ctypes.c_int64
     lib.hstu_oracle_valid.restype = ctypes.c_int
     lib.hstu_oracle_valid.argtypes = [c64, c64, c64, ctypes.c_int, c64, c64, c64]
+    kv = [i64, d, c64, i64, i64, i64, c64]  # seq_offsets_k, kv_cache, num_pages, page table
     lib.hstu_oracle_fwd.restype = ctypes.c_int
-    lib.hstu_oracle_fwd.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, d, c64, i64,
-                                    i64, ctypes.c_int, c64, ctypes.c_double, ctypes.c_double,
-                                    d, ctypes.c_int]
+    lib.hstu_oracle_fwd.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, d, c64] + kv + [
+        i64, i64, ctypes.c_int, c64, ctypes.c_double, ctypes.c_double, d, ctypes.c_int]
     lib.hstu_oracle_fwd_rows.restype = ctypes.c_int
-    lib.hstu_oracle_fwd_rows.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, d, c64,
-                                         i64, i64, ctypes.c_int, c64, ctypes.c_double,
-                                         ctypes.c_double, i64, c64, d, ctypes.c_int]
+    lib.hstu_oracle_fwd_rows.argtypes = [d, d, d, i64, c64, c64, c64, c64, d, c64, d,
+                                         c64] + kv + [i64, i64, ctypes.c_int, c64,
+                                                      ctypes.c_double, ctypes.c_double, i64,
+                                                      c64, d, ctypes.c_int]
     lib.hstu_oracle_count_valid.restype = ctypes.c_int64
     lib.hstu_oracle_count_valid.argtypes = [i64, c64, c64, i64, i64, ctypes.c_int, c64]
+    lib.hstu_oracle_count_valid_kv.restype = ctypes.c_int64
+    lib.hstu_oracle_count_valid_kv.argtypes = [i64, i64, c64, c64, i64, i64, ctypes.c_int, c64]
     return lib
 
 
@@ -108,12 +111,50 @@ def _p(a, ty):
     return None if a is None else a.ctypes.data_as(ctypes.POINTER(ty))
 
 
+class _KV:
+    """Key side of a call: offsets of the new k/v rows and the paged history."""
+
+    def __init__(self, B, nk, d, seq_offsets_k, kv_cache, page_offsets, page_ids,
+                 last_page_len):
+        self.so_k = _i64(seq_offsets_k)
+        if self.so_k is not None and self.so_k.shape != (B + 1,):
+            raise ValueError("seq_offsets_k must be [B+1]")
+        self.cache = _f64(kv_cache)
+        self.num_pages, self.page_size = 0, 0
+        self.po = self.ids = self.last = None
+        if self.cache is not None:
+            if self.cache.ndim != 5 or self.cache.shape[1] != 2 or \
+                    self.cache.shape[3:] != (nk, d):
+                raise ValueError("kv_cache must be [num_pages, 2, page_size, Nk, D]")
+            self.num_pages, self.page_size = self.cache.shape[0], self.cache.shape[2]
+            self.po, self.ids = _i64(page_offsets), _i64(page_ids)
+            self.last = _i64(last_page_len)
+            if self.po is None or self.ids is None or self.last is None or \
+                    self.po.shape != (B + 1,) or self.last.shape != (B,):
+                raise ValueError("page_offsets [B+1], page_ids and last_page_len [B] "
+                                 "go with kv_cache")
+            if self.ids.size < int(self.po[-1]):
+                raise ValueError("page_ids shorter than page_offsets[B]")
+
+    def args(self):
+        return [_p(self.so_k, ctypes.c_int64), _p(self.cache, ctypes.c_double),
+                self.num_pages, _p(self.po, ctypes.c_int64), _p(self.ids, ctypes.c_int64),
+                _p(self.last, ctypes.c_int64), self.page_size]
+
+
+def history_lengths(page_offsets, last_page_len, page_size):
+    """Cached rows per sequence: (pages - 1) * page_size + last_page_len, 0 without pages."""
+    po, last = _i64(page_offsets), _i64(last_page_len)
+    pages = np.diff(po)
+    return np.where(pages > 0, (pages - 1) * page_size + last, 0)
+
+
 def _common(q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen, mask=None,
             mask_type=MASK_CAUSAL):
     q, k, v = _f64(q), _f64(k), _f64(v)
     so = _i64(seq_offsets)
     if q.ndim != 3 or k.ndim != 3 or v.shape != k.shape or q.shape[2] != k.shape[2]:
-        raise ValueError("q [T, Nq, D], k/v [T, Nk, D] expected")
+        raise ValueError("q [T, Nq, D], k/v [Tk, Nk, D] expected")
     B = so.shape[0] - 1
     nc, nt = _i64(num_context), _i64(num_targets)
     rab = _f64(rab)
@@ -134,23 +175,36 @@ def _common(q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen, mas
     return q, k, v, so, B, rab, rab_heads, nc, nt, mask
 
 
+def _key_lengths(so, kv):
+    so_k = kv.so_k if kv.so_k is not None else so
+    lk = np.diff(so_k)
+    if kv.cache is not None:
+        lk = lk + history_lengths(kv.po, kv.last, kv.page_size)
+    return lk
+
+
 def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=None,
              mask_type=MASK_CAUSAL, target_group_size=0, alpha=1.0, silu_scale=None,
-             max_seqlen=None, nthreads=1, mask=None):
+             max_seqlen=None, nthreads=1, mask=None, seq_offsets_k=None, kv_cache=None,
+             page_offsets=None, page_ids=None, last_page_len=None):
     """Whole forward in fp64. Returns out [T, Nq, D] as float64 (rows outside
     every sequence are 0). silu_scale defaults to 1/max_seqlen (Inputs and
-    Outputs table, silu_scale)."""
+    Outputs table, silu_scale). max_seqlen is the key-side bound (the S of rab and
+    mask); with seq_offsets_k and/or a kv_cache the keys of a sequence are its cached
+    history followed by its new k/v rows, and its queries are the last ones."""
     q, k, v, so, B, rab, rab_heads, nc, nt, mask = _common(
         q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen, mask, mask_type)
+    kv = _KV(B, k.shape[1], k.shape[2], seq_offsets_k, kv_cache, page_offsets, page_ids,
+             last_page_len)
     if max_seqlen is None:
-        max_seqlen = int(np.max(np.diff(so))) if B > 0 else 1
+        max_seqlen = int(np.max(_key_lengths(so, kv))) if B > 0 else 1
     if silu_scale is None:
         silu_scale = 1.0 / max_seqlen
     out = np.zeros(q.shape, dtype=np.float64)
     rc = _load().hstu_oracle_fwd(_p(q, ctypes.c_double), _p(k, ctypes.c_double),
                                  _p(v, ctypes.c_double), _p(so, ctypes.c_int64), B, q.shape[1],
                                  k.shape[1], q.shape[2], _p(rab, ctypes.c_double), rab_heads,
-                                 _p(mask, ctypes.c_double), max_seqlen,
+                                 _p(mask, ctypes.c_double), max_seqlen, *kv.args(),
                                  _p(nc, ctypes.c_int64), _p(nt, ctypes.c_int64), mask_type,
                                  target_group_size, float(alpha), float(silu_scale),
                                  _p(out, ctypes.c_double), int(nthreads))
@@ -161,13 +215,16 @@ def hstu_fwd(q, k, v, seq_offsets, *, rab=None, num_context=None, num_targets=No
 
 def hstu_fwd_rows(q, k, v, seq_offsets, rows, *, rab=None, num_context=None, num_targets=None,
                   mask_type=MASK_CAUSAL, target_group_size=0, alpha=1.0, silu_scale=None,
-                  max_seqlen=None, nthreads=1, mask=None):
+                  max_seqlen=None, nthreads=1, mask=None, seq_offsets_k=None, kv_cache=None,
+                  page_offsets=None, page_ids=None, last_page_len=None):
     """Selected output rows: rows is an int array [n, 3] of (b, h, i) (i local to
     sequence b). Returns [n, D] float64, row r = out[seq_offsets[b] + i, h, :]."""
     q, k, v, so, B, rab, rab_heads, nc, nt, mask = _common(
         q, k, v, seq_offsets, rab, num_context, num_targets, max_seqlen, mask, mask_type)
+    kv = _KV(B, k.shape[1], k.shape[2], seq_offsets_k, kv_cache, page_offsets, page_ids,
+             last_page_len)
     if max_seqlen is None:
-        max_seqlen = int(np.max(np.diff(so))) if B > 0 else 1
+        max_seqlen = int(np.max(_key_lengths(so, kv))) if B > 0 else 1
     if silu_scale is None:
         silu_scale = 1.0 / max_seqlen
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
@@ -176,7 +233,7 @@ def hstu_fwd_rows(q, k, v, seq_offsets, rows, *, rab=None, num_context=None, num
                                       _p(v, ctypes.c_double), _p(so, ctypes.c_int64), B,
                                       q.shape[1], k.shape[1], q.shape[2],
                                       _p(rab, ctypes.c_double), rab_heads,
-                                      _p(mask, ctypes.c_double), max_seqlen,
+                                      _p(mask, ctypes.c_double), max_seqlen, *kv.args(),
                                       _p(nc, ctypes.c_int64), _p(nt, ctypes.c_int64), mask_type,
                                       target_group_size, float(alpha), float(silu_scale),
                                       _p(rows, ctypes.c_int64), rows.shape[0],
@@ -207,3 +264,15 @@ def count_valid(seq_offsets, num_heads_q, *, num_context=None, num_targets=None,
                                                num_heads_q, _p(nc, ctypes.c_int64),
                                                _p(nt, ctypes.c_int64), mask_type,
                                                target_group_size))
+
+
+def count_valid_kv(query_lengths, key_lengths, num_heads_q, *, num_context=None,
+                   num_targets=None, mask_type=MASK_CAUSAL, target_group_size=0):
+    """Pair count with per-sequence query and key lengths, queries at the end of the keys."""
+    lq, lk = _i64(query_lengths), _i64(key_lengths)
+    nc, nt = _i64(num_context), _i64(num_targets)
+    return int(_load().hstu_oracle_count_valid_kv(_p(lq, ctypes.c_int64),
+                                                  _p(lk, ctypes.c_int64), lq.shape[0],
+                                                  num_heads_q, _p(nc, ctypes.c_int64),
+                                                  _p(nt, ctypes.c_int64), mask_type,
+                                                  target_group_size))

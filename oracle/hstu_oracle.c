@@ -37,13 +37,31 @@
  *   - Custom mask (mask_type 3): every key of the sequence is a candidate and P is
  *     multiplied by mask[b, h, i, j] after the SiLU and the scaling (the chain's order);
  *     a 0/1 mask selects exactly like the built-in one.
+ *   - Different query and key lengths (Inputs and Outputs table: seq_offsets_q,
+ *     seq_offsets_k, max_seq_len_q, max_seq_len_k, is_delta_qk): sequence b has Lq query
+ *     rows and Lk >= Lq keys, and the queries are the last Lq tokens of the sequence:
+ *     query row i sits at position p = Lk - Lq + i. The mask, the rab row and the custom
+ *     mask row are taken at p (with L = Lk); rab and mask are [B, N, Sk, Sk],
+ *     Sk = max_seq_len_k. So a call with fewer queries computes exactly the last Lq rows
+ *     of the call with all Lk queries.
+ *   - KV cache (Inputs and Outputs table: kv_cache [num_pages, 2, page_size, N, D],
+ *     page_offsets [B+1], page_ids, last_page_len [B]; feature table "Page"): the cache
+ *     holds the history of each sequence. Its keys are the rows of pages
+ *     page_ids[page_offsets[b]], ..., page_ids[page_offsets[b+1] - 1] in that order
+ *     (plane 0 of a page holds K, plane 1 holds V), every page full except the last, which
+ *     holds last_page_len[b] rows; the new k/v rows of the call follow the history. So
+ *     Lk = (pages - 1) * page_size + last_page_len[b] + (new k rows), or just the new rows
+ *     when the sequence has no pages.
  *
  * Pinned by tests/test_oracle_pins.py: closed forms (L = 1, silu(ln 3) = 0.75 ln 3,
  * silu(x) - silu(-x) = x), the dense equal-length case against torch.matmul and
  * torch.nn.functional.silu in fp64, hand-written 0/1 mask matrices, and the
  * invariants (Q = 0 gives 0, causal locality, GQA = replicated MHA, batch
- * permutation, V = ones). The alpha/rab positions and the mask semantics are
- * readings of a silent page: parity of those readings is unpinned by the page.
+ * permutation, V = ones); the key side by the identities "fewer queries = the last rows
+ * of the call with all queries" and "paged keys = the same keys passed contiguously"
+ * (bit for bit), and a Q = 0 closed form through a cache. The alpha/rab positions, the
+ * mask semantics and the query alignment are readings of a silent page: parity of those
+ * readings is unpinned by the page.
  */
 #include <math.h>
 #include <pthread.h>
@@ -80,9 +98,13 @@ static double silu(double x) { return x / (1.0 + exp(-x)); }
 
 typedef struct {
   const double *q, *k, *v, *rab;
-  const double *mask; /* custom mask [B, Nq, S, S] (mask_type 3) */
+  const double *mask; /* custom mask [B, Nq, Sk, Sk] (mask_type 3) */
   const int64_t *seq_offsets, *num_context, *num_targets;
-  int64_t B, Nq, Nk, D, max_seqlen;
+  const int64_t *seq_offsets_k; /* offsets of the k/v rows, or NULL: those of q */
+  const double *kv_cache;       /* [num_pages, 2, page_size, Nk, D] or NULL */
+  const int64_t *page_offsets, *page_ids, *last_page_len;
+  int64_t page_size;
+  int64_t B, Nq, Nk, D, max_seqlen; /* max_seqlen: Sk, the row length of rab and mask */
   int64_t rab_heads; /* rab planes per sequence: Nq, or 1 (broadcast to every head) */
   int mask_type;
   int64_t g;
@@ -95,10 +117,37 @@ typedef struct {
   int64_t next; /* work counter, taken with an atomic add */
 } job_t;
 
-/* One output row: out[t0 + i, h, :] for sequence b, query head h, local row i. */
+/* Cached history length of sequence b (0 without a cache). */
+static int64_t history_len(const job_t *J, int64_t b) {
+  if (!J->kv_cache) return 0;
+  const int64_t pages = J->page_offsets[b + 1] - J->page_offsets[b];
+  return pages > 0 ? (pages - 1) * J->page_size + J->last_page_len[b] : 0;
+}
+
+/* Number of new k/v rows of sequence b. */
+static int64_t new_kv_len(const job_t *J, int64_t b) {
+  const int64_t *so = J->seq_offsets_k ? J->seq_offsets_k : J->seq_offsets;
+  return so[b + 1] - so[b];
+}
+
+/* Key (plane 0) or value (plane 1) row of key position j of sequence b, head hk. */
+static const double *kv_row(const job_t *J, int64_t b, int64_t hk, int64_t j, int plane) {
+  const int64_t hist = history_len(J, b);
+  if (j < hist) {
+    const int64_t page = J->page_ids[J->page_offsets[b] + j / J->page_size];
+    const int64_t row = j % J->page_size;
+    return J->kv_cache + (((page * 2 + plane) * J->page_size + row) * J->Nk + hk) * J->D;
+  }
+  const int64_t *so = J->seq_offsets_k ? J->seq_offsets_k : J->seq_offsets;
+  return (plane ? J->v : J->k) + ((so[b] + (j - hist)) * J->Nk + hk) * J->D;
+}
+
+/* One output row: out[t0 + i, h, :] for sequence b, query head h, local query row i. */
 static void one_row(const job_t *J, int64_t b, int64_t h, int64_t i, double *o) {
   const int64_t t0 = J->seq_offsets[b];
-  const int64_t L = J->seq_offsets[b + 1] - t0;
+  const int64_t Lq = J->seq_offsets[b + 1] - t0;
+  const int64_t L = history_len(J, b) + new_kv_len(J, b); /* keys of the sequence */
+  const int64_t pos = L - Lq + i; /* position of the query in the sequence */
   const int64_t D = J->D;
   const int64_t G = J->Nq / J->Nk;
   const int64_t hk = h / G;
@@ -107,8 +156,8 @@ static void one_row(const job_t *J, int64_t b, int64_t h, int64_t i, double *o) 
   const double *qi = J->q + ((t0 + i) * J->Nq + h) * D;
   for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
   for (int64_t j = 0; j < L; ++j) {
-    const double *kj = J->k + ((t0 + j) * J->Nk + hk) * D;
-    const double *vj = J->v + ((t0 + j) * J->Nk + hk) * D;
+    const double *kj = kv_row(J, b, hk, j, 0);
+    const double *vj = kv_row(J, b, hk, j, 1);
     /* 1. QK matrix multiplication */
     double s = 0.0;
     for (int64_t d = 0; d < D; ++d) s += qi[d] * kj[d];
@@ -116,7 +165,7 @@ static void one_row(const job_t *J, int64_t b, int64_t h, int64_t i, double *o) 
     double x = J->alpha * s;
     if (J->rab) {
       const int64_t plane = b * J->rab_heads + (J->rab_heads == 1 ? 0 : h);
-      x += J->rab[(plane * J->max_seqlen + i) * J->max_seqlen + j];
+      x += J->rab[(plane * J->max_seqlen + pos) * J->max_seqlen + j];
     }
     /* 2. SiLU activation */
     double p = silu(x);
@@ -124,9 +173,9 @@ static void one_row(const job_t *J, int64_t b, int64_t h, int64_t i, double *o) 
     p *= J->silu_scale;
     /* 4. mask application: the built-in mask selects; a custom mask multiplies P by
        mask[b, h, i, j] (a 0/1 mask selects the same way) */
-    if (!hstu_oracle_valid(i, j, L, J->mask_type, nc, nt, J->g)) p = 0.0;
+    if (!hstu_oracle_valid(pos, j, L, J->mask_type, nc, nt, J->g)) p = 0.0;
     if (J->mask_type == ORACLE_MASK_CUSTOM)
-      p *= J->mask[((b * J->Nq + h) * J->max_seqlen + i) * J->max_seqlen + j];
+      p *= J->mask[((b * J->Nq + h) * J->max_seqlen + pos) * J->max_seqlen + j];
     /* 5. matrix multiplication with V */
     for (int64_t d = 0; d < D; ++d) o[d] += p * vj[d];
   }
@@ -140,8 +189,8 @@ static void *worker_units(void *arg) {
     if (u >= units) break;
     const int64_t b = u / J->Nq, h = u % J->Nq;
     const int64_t t0 = J->seq_offsets[b];
-    const int64_t L = J->seq_offsets[b + 1] - t0;
-    for (int64_t i = 0; i < L; ++i) one_row(J, b, h, i, J->out + ((t0 + i) * J->Nq + h) * J->D);
+    const int64_t Lq = J->seq_offsets[b + 1] - t0;
+    for (int64_t i = 0; i < Lq; ++i) one_row(J, b, h, i, J->out + ((t0 + i) * J->Nq + h) * J->D);
   }
   return NULL;
 }
@@ -184,17 +233,55 @@ static int check_args(int64_t B, int64_t Nq, int64_t Nk, int64_t D, int mask_typ
   return 0;
 }
 
+/* The key side: a page table that names pages outside the cache or a last page length
+ * outside [1, page_size], or a sequence with more queries than keys, is rejected. */
+static int check_kv(const job_t *J, int64_t num_pages) {
+  if (J->kv_cache && J->page_size <= 0) return -1;
+  for (int64_t b = 0; b < J->B; ++b) {
+    if (J->kv_cache) {
+      const int64_t pages = J->page_offsets[b + 1] - J->page_offsets[b];
+      if (pages < 0) return -1;
+      if (pages > 0 && (J->last_page_len[b] < 1 || J->last_page_len[b] > J->page_size))
+        return -1;
+      for (int64_t x = 0; x < pages; ++x) {
+        const int64_t id = J->page_ids[J->page_offsets[b] + x];
+        if (id < 0 || id >= num_pages) return -1;
+      }
+    }
+    const int64_t Lq = J->seq_offsets[b + 1] - J->seq_offsets[b];
+    if (Lq < 0 || new_kv_len(J, b) < 0 || Lq > history_len(J, b) + new_kv_len(J, b)) return -1;
+  }
+  return 0;
+}
+
+static void set_kv(job_t *J, const int64_t *seq_offsets_k, const double *kv_cache,
+                   const int64_t *page_offsets, const int64_t *page_ids,
+                   const int64_t *last_page_len, int64_t page_size) {
+  J->seq_offsets_k = seq_offsets_k;
+  J->kv_cache = kv_cache;
+  J->page_offsets = page_offsets;
+  J->page_ids = page_ids;
+  J->last_page_len = last_page_len;
+  J->page_size = page_size;
+}
+
 /*
- * Whole forward. q [T, Nq, D], k/v [T, Nk, D], rab [B, rab_heads, S, S] or NULL
+ * Whole forward. q [T, Nq, D], k/v [Tk, Nk, D], rab [B, rab_heads, S, S] or NULL
  * (rab_heads = Nq, or 1 for a plane shared by all heads), mask [B, Nq, S, S] (custom
- * mask, mask_type 3 only) or NULL,
- * seq_offsets [B+1], num_context/num_targets [B] or NULL; out [T, Nq, D].
+ * mask, mask_type 3 only) or NULL, S = max_seqlen (the key-side bound Sk),
+ * seq_offsets [B+1] (queries), num_context/num_targets [B] or NULL; out [T, Nq, D].
+ * Key side: seq_offsets_k [B+1] (new k/v rows; NULL = seq_offsets), and kv_cache
+ * [num_pages, 2, page_size, Nk, D] with page_offsets [B+1], page_ids, last_page_len [B]
+ * (kv_cache NULL = no history).
  * Rows of out outside every sequence are left untouched. Returns 0 or -1.
  */
 int hstu_oracle_fwd(const double *q, const double *k, const double *v,
                     const int64_t *seq_offsets, int64_t B, int64_t Nq, int64_t Nk,
                     int64_t D, const double *rab, int64_t rab_heads, const double *mask,
-                    int64_t max_seqlen, const int64_t *num_context,
+                    int64_t max_seqlen, const int64_t *seq_offsets_k, const double *kv_cache,
+                    int64_t num_pages, const int64_t *page_offsets, const int64_t *page_ids,
+                    const int64_t *last_page_len, int64_t page_size,
+                    const int64_t *num_context,
                     const int64_t *num_targets, int mask_type, int64_t target_group_size,
                     double alpha, double silu_scale, double *out, int nthreads) {
   if (check_args(B, Nq, Nk, D, mask_type)) return -1;
@@ -202,6 +289,9 @@ int hstu_oracle_fwd(const double *q, const double *k, const double *v,
   if ((mask_type == ORACLE_MASK_CUSTOM) != (mask != NULL)) return -1;
   job_t J;
   memset(&J, 0, sizeof(J));
+  J.seq_offsets = seq_offsets; J.B = B;
+  set_kv(&J, seq_offsets_k, kv_cache, page_offsets, page_ids, last_page_len, page_size);
+  if (check_kv(&J, num_pages)) return -1;
   J.q = q; J.k = k; J.v = v; J.rab = rab; J.mask = mask;
   J.seq_offsets = seq_offsets; J.num_context = num_context; J.num_targets = num_targets;
   J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen; J.rab_heads = rab_heads;
@@ -215,6 +305,10 @@ int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
                          const int64_t *seq_offsets, int64_t B, int64_t Nq, int64_t Nk,
                          int64_t D, const double *rab, int64_t rab_heads,
                          const double *mask, int64_t max_seqlen,
+                         const int64_t *seq_offsets_k, const double *kv_cache,
+                         int64_t num_pages, const int64_t *page_offsets,
+                         const int64_t *page_ids, const int64_t *last_page_len,
+                         int64_t page_size,
                          const int64_t *num_context, const int64_t *num_targets,
                          int mask_type, int64_t target_group_size, double alpha,
                          double silu_scale, const int64_t *rows, int64_t nrows,
@@ -230,6 +324,9 @@ int hstu_oracle_fwd_rows(const double *q, const double *k, const double *v,
   }
   job_t J;
   memset(&J, 0, sizeof(J));
+  J.seq_offsets = seq_offsets; J.B = B;
+  set_kv(&J, seq_offsets_k, kv_cache, page_offsets, page_ids, last_page_len, page_size);
+  if (check_kv(&J, num_pages)) return -1;
   J.q = q; J.k = k; J.v = v; J.rab = rab; J.mask = mask;
   J.seq_offsets = seq_offsets; J.num_context = num_context; J.num_targets = num_targets;
   J.B = B; J.Nq = Nq; J.Nk = Nk; J.D = D; J.max_seqlen = max_seqlen; J.rab_heads = rab_heads;
@@ -252,6 +349,25 @@ int64_t hstu_oracle_count_valid(const int64_t *seq_offsets, int64_t B, int64_t N
     for (int64_t i = 0; i < L; ++i)
       for (int64_t j = 0; j < L; ++j)
         c += hstu_oracle_valid(i, j, L, mask_type, nc, nt, target_group_size);
+    total += c * Nq;
+  }
+  return total;
+}
+
+/* Mask-aware pair count with per-sequence query and key lengths: sum over b of
+ * Nq * #{(i, j) : i < lq[b], j < lk[b], valid(lk[b] - lq[b] + i, j, lk[b])}. */
+int64_t hstu_oracle_count_valid_kv(const int64_t *lq, const int64_t *lk, int64_t B, int64_t Nq,
+                                   const int64_t *num_context, const int64_t *num_targets,
+                                   int mask_type, int64_t target_group_size) {
+  int64_t total = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    const int64_t nc = num_context ? num_context[b] : 0;
+    const int64_t nt = num_targets ? num_targets[b] : 0;
+    int64_t c = 0;
+    for (int64_t i = 0; i < lq[b]; ++i)
+      for (int64_t j = 0; j < lk[b]; ++j)
+        c += hstu_oracle_valid(lk[b] - lq[b] + i, j, lk[b], mask_type, nc, nt,
+                               target_group_size);
     total += c * Nq;
   }
   return total;

@@ -18,7 +18,7 @@ MUTATIONS = [
      "    const double *qq = qi; (void)qq;"),  # placeholder replaced below
     ("dropped_rab", "x += J->rab[(plane", "x += 0.0 * J->rab[(plane"),
     ("alpha_scales_rab", "x += J->rab[(plane", "x += J->alpha * J->rab[(plane"),
-    ("rab_transposed", "(plane * J->max_seqlen + i) * J->max_seqlen + j]", "(plane * J->max_seqlen + j) * J->max_seqlen + i]"),
+    ("rab_transposed", "(plane * J->max_seqlen + pos) * J->max_seqlen + j]", "(plane * J->max_seqlen + j) * J->max_seqlen + pos]"),
     ("rab_head_ignored", "(J->rab_heads == 1 ? 0 : h)", "(J->rab_heads == 1 ? 0 : 0)"),
     ("silu_sign", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
     ("sigmoid_not_silu", "return x / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(-x));"),
@@ -29,20 +29,35 @@ MUTATIONS = [
     ("history_off_by_one", "H = L - nt;", "H = L - nt + 1;"),
     ("targets_see_future_in_group", "j >= H && j <= i && (i - H)", "j >= H && (i - H)"),
     ("dropped_scale", "p *= J->silu_scale;", "p *= 1.0;"),
-    ("v_row_of_query", "const double *vj = J->v + ((t0 + j) * J->Nk + hk) * D;",
-     "const double *vj = J->v + ((t0 + i) * J->Nk + hk) * D;"),
+    ("v_row_of_query", "const double *vj = kv_row(J, b, hk, j, 1);",
+     "const double *vj = kv_row(J, b, hk, i, 1);"),
     ("mask_none_causal", "if (mask_type == ORACLE_MASK_NONE || mask_type == ORACLE_MASK_CUSTOM) return 1;",
      "if (mask_type == ORACLE_MASK_CUSTOM) return 1;"),
     ("custom_mask_ignored", "p *= J->mask[", "p *= 1.0 + 0.0 * J->mask["),
     ("custom_mask_before_silu", "    double p = silu(x);", "    if (J->mask_type == ORACLE_MASK_CUSTOM)\n"
-     "      x *= J->mask[((b * J->Nq + h) * J->max_seqlen + i) * J->max_seqlen + j];\n"
+     "      x *= J->mask[((b * J->Nq + h) * J->max_seqlen + pos) * J->max_seqlen + j];\n"
      "    double p = silu(x);"),
+    # queries with fewer rows than keys (Inputs and Outputs table: seq_offsets_q/k)
+    ("delta_position_is_row", "const int64_t pos = L - Lq + i;", "const int64_t pos = i;"),
+    ("delta_rab_row_local", "x += J->rab[(plane * J->max_seqlen + pos)",
+     "x += J->rab[(plane * J->max_seqlen + i)"),
+    ("delta_mask_row_local", "* J->max_seqlen + pos) * J->max_seqlen + j];\n    /* 5.",
+     "* J->max_seqlen + i) * J->max_seqlen + j];\n    /* 5."),
+    # KV cache pages (Inputs and Outputs table: kv_cache, page_offsets, page_ids, last_page_len)
+    ("page_rows_reversed", "const int64_t row = j % J->page_size;",
+     "const int64_t row = J->page_size - 1 - j % J->page_size;"),
+    ("pages_reversed", "J->page_ids[J->page_offsets[b] + j / J->page_size]",
+     "J->page_ids[J->page_offsets[b + 1] - 1 - j / J->page_size]"),
+    ("kv_planes_swapped", "(((page * 2 + plane)", "(((page * 2 + 1 - plane)"),
+    ("last_page_counted_full", "(pages - 1) * J->page_size + J->last_page_len[b]",
+     "pages * J->page_size"),
+    ("history_ignored", "  if (!J->kv_cache) return 0;\n  const int64_t pages", "  return 0;\n  const int64_t pages"),
 ]
-# a real transposition: Q row j against K row i
+# a real transposition: Q row j against K row i (query rows past Lq stay at i: in bounds)
 MUTATIONS[0] = ("transposed_scores",
-                "const double *kj = J->k + ((t0 + j) * J->Nk + hk) * D;",
-                "const double *kj = J->k + ((t0 + i) * J->Nk + hk) * D;\n"
-                "    qi = J->q + ((t0 + j) * J->Nq + h) * D;")
+                "const double *kj = kv_row(J, b, hk, j, 0);",
+                "const double *kj = kv_row(J, b, hk, i, 0);\n"
+                "    qi = J->q + ((t0 + (j < Lq ? j : i)) * J->Nq + h) * D;")
 
 
 def _pin_checks():
@@ -52,7 +67,13 @@ def _pin_checks():
               pins.test_causal_rows_ignore_later_keys, pins.test_gqa_equals_replicated_mha,
               lambda: pins.test_q_zero_rab_per_head_and_broadcast_closed_form(1),
               lambda: pins.test_q_zero_rab_per_head_and_broadcast_closed_form(3),
-              pins.test_custom_mask_closed_forms]
+              pins.test_custom_mask_closed_forms,
+              pins.test_delta_queries_are_the_last_rows_of_the_full_forward,
+              pins.test_delta_custom_mask_rows_follow_positions,
+              pins.test_delta_paged_q_zero_closed_form,
+              pins.test_count_valid_kv_closed_forms]
+    for ps in (4, 8):
+        checks.append(lambda a=ps: pins.test_paged_history_equals_contiguous_keys(a))
     for causal in (False, True):
         for nq, nk in ((4, 4), (4, 2), (6, 1)):
             checks.append(lambda c=causal, a=nq, b=nk: pins.test_equal_lengths_match_torch_matmul(c, a, b))

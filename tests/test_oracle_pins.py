@@ -149,6 +149,145 @@ def test_custom_mask_closed_forms():
                                        atol=1e-12)
 
 
+# ------------------------------------------------------ fewer queries than keys; KV cache
+# Inputs and Outputs table: seq_offsets_q / seq_offsets_k / max_seq_len_k / is_delta_qk
+# (query and key lengths may differ) and kv_cache [num_pages, 2, page_size, N, D] with
+# page_offsets, page_ids, last_page_len (feature table "Page": the KV cache of the history).
+# Reading: the queries are the last Lq tokens of the Lk keys (row i at position Lk - Lq + i).
+def _delta_case(rng, lk, lq, nq, nk, d):
+    """Full sequences of lk keys; the queries of the delta call are the last lq rows."""
+    so_k = np.concatenate([[0], np.cumsum(lk)]).astype(np.int64)
+    so_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int64)
+    tk = int(so_k[-1])
+    q_full = rng.standard_normal((tk, nq, d))
+    k = rng.standard_normal((tk, nk, d))
+    v = rng.standard_normal((tk, nk, d))
+    rows = np.concatenate([np.arange(so_k[b + 1] - lq[b], so_k[b + 1]) for b in range(len(lk))])
+    return q_full, k, v, so_k, so_q, rows.astype(np.int64)
+
+
+def test_delta_queries_are_the_last_rows_of_the_full_forward():
+    """With Lq < Lk queries (the last ones), every output row equals the row of the call
+    with all Lk queries, bit for bit: mask, rab and targets are taken at the position."""
+    rng = _rng(41)
+    lk = [9, 6, 12, 1, 7]
+    lq = [4, 6, 1, 1, 0]
+    q_full, k, v, so_k, so_q, rows = _delta_case(rng, lk, lq, 4, 2, 3)
+    S = 13
+    rab = rng.standard_normal((5, 4, S, S))
+    for kw in (dict(mask_type=oracle.MASK_CAUSAL, num_context=[2, 0, 3, 0, 1],
+                    num_targets=[3, 2, 4, 0, 2], target_group_size=2, rab=rab),
+               dict(mask_type=oracle.MASK_CAUSAL),
+               dict(mask_type=oracle.MASK_NONE, rab=rab[:, :1].copy())):
+        full = oracle.hstu_fwd(q_full, k, v, so_k, alpha=0.8, silu_scale=0.2, max_seqlen=S, **kw)
+        delta = oracle.hstu_fwd(q_full[rows], k, v, so_q, seq_offsets_k=so_k, alpha=0.8,
+                                silu_scale=0.2, max_seqlen=S, **kw)
+        np.testing.assert_array_equal(delta, full[rows])
+    with pytest.raises(ValueError):  # more queries than keys
+        oracle.hstu_fwd(q_full[:3], k[:2], v[:2], [0, 3], seq_offsets_k=[0, 2], max_seqlen=S)
+
+
+def test_delta_custom_mask_rows_follow_positions():
+    """A custom mask is read at the query's position too: the delta rows equal the full
+    call's last rows."""
+    rng = _rng(42)
+    lk, lq = [8, 5], [3, 5]
+    q_full, k, v, so_k, so_q, rows = _delta_case(rng, lk, lq, 2, 2, 2)
+    S = 8
+    m = rng.uniform(-1.0, 2.0, (2, 2, S, S))
+    kw = dict(mask=m, mask_type=oracle.MASK_CUSTOM, alpha=1.1, silu_scale=0.3, max_seqlen=S)
+    full = oracle.hstu_fwd(q_full, k, v, so_k, **kw)
+    delta = oracle.hstu_fwd(q_full[rows], k, v, so_q, seq_offsets_k=so_k, **kw)
+    np.testing.assert_array_equal(delta, full[rows])
+
+
+def _paged(rng, k_full, v_full, so_k, hist, page_size, spare=3):
+    """Move the first hist[b] keys of every sequence into randomly placed pages of a cache
+    whose unused rows hold large finite values; return the new rows and the page table."""
+    B = len(hist)
+    npages = [0 if h == 0 else -(-h // page_size) for h in hist]
+    num_pages = sum(npages) + spare
+    nk, d = k_full.shape[1:]
+    cache = rng.uniform(1e5, 2e5, (num_pages, 2, page_size, nk, d))
+    ids = rng.permutation(num_pages)[:sum(npages)].astype(np.int64)
+    po = np.concatenate([[0], np.cumsum(npages)]).astype(np.int64)
+    last = np.zeros(B, dtype=np.int64)
+    new_k, new_v, lnew = [], [], []
+    for b in range(B):
+        t0 = so_k[b]
+        for x in range(npages[b]):
+            n = min(page_size, hist[b] - x * page_size)
+            pg = ids[po[b] + x]
+            cache[pg, 0, :n] = k_full[t0 + x * page_size:t0 + x * page_size + n]
+            cache[pg, 1, :n] = v_full[t0 + x * page_size:t0 + x * page_size + n]
+            last[b] = n
+        new_k.append(k_full[t0 + hist[b]:so_k[b + 1]])
+        new_v.append(v_full[t0 + hist[b]:so_k[b + 1]])
+        lnew.append(int(so_k[b + 1] - t0 - hist[b]))
+    so_new = np.concatenate([[0], np.cumsum(lnew)]).astype(np.int64)
+    return np.concatenate(new_k), np.concatenate(new_v), so_new, cache, po, ids, last
+
+
+@pytest.mark.parametrize("page_size", [4, 8])
+def test_paged_history_equals_contiguous_keys(page_size):
+    """Keys split into cache pages (shuffled page ids, partly filled last pages, sequences
+    without history and without new rows) give the same output as the same keys passed
+    contiguously, bit for bit."""
+    rng = _rng(43 + page_size)
+    lk = [11, 6, 9, 16, 5]
+    lq = [3, 6, 9, 2, 1]
+    hist = [7, 0, 9, 8, 5]  # partial last page, no history, all keys cached, full pages
+    q_full, k, v, so_k, so_q, rows = _delta_case(rng, lk, lq, 2, 1, 3)
+    nk_, nv_, so_new, cache, po, ids, last = _paged(rng, k, v, so_k, hist, page_size)
+    np.testing.assert_array_equal(oracle.history_lengths(po, last, page_size), hist)
+    S = 16 + page_size
+    rab = rng.standard_normal((5, 2, S, S))
+    kw = dict(mask_type=oracle.MASK_CAUSAL, num_context=[1, 2, 0, 3, 0],
+              num_targets=[2, 1, 3, 4, 0], target_group_size=1, rab=rab, alpha=0.6,
+              silu_scale=0.4, max_seqlen=S)
+    ref = oracle.hstu_fwd(q_full[rows], k, v, so_q, seq_offsets_k=so_k, **kw)
+    got = oracle.hstu_fwd(q_full[rows], nk_, nv_, so_q, seq_offsets_k=so_new, kv_cache=cache,
+                          page_offsets=po, page_ids=ids, last_page_len=last, **kw)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_delta_paged_q_zero_closed_form():
+    """Q = 0 with a rab R, plain causal mask, keys from a cache plus new rows: query i of a
+    sequence with Lk keys sits at p = Lk - Lq + i and
+    out_i = silu_scale * sum_{j <= p} silu(R[p, j]) * v_j (silu from torch)."""
+    rng = _rng(45)
+    lk, lq, hist, ps = [10, 7], [4, 7], [6, 4], 4
+    q_full, k, v, so_k, so_q, rows = _delta_case(rng, lk, lq, 1, 1, 2)
+    nk_, nv_, so_new, cache, po, ids, last = _paged(rng, k, v, so_k, hist, ps)
+    S = 10 + ps
+    R = rng.standard_normal((2, 1, S, S))
+    out = oracle.hstu_fwd(np.zeros((sum(lq), 1, 2)), nk_, nv_, so_q, seq_offsets_k=so_new,
+                          kv_cache=cache, page_offsets=po, page_ids=ids, last_page_len=last,
+                          rab=R, mask_type=oracle.MASK_CAUSAL, alpha=3.0, silu_scale=0.5,
+                          max_seqlen=S)
+    for b in range(2):
+        vb = v[so_k[b]:so_k[b + 1], 0]
+        for i in range(lq[b]):
+            p = lk[b] - lq[b] + i
+            w = F.silu(torch.from_numpy(R[b, 0, p, :p + 1])).numpy()
+            np.testing.assert_allclose(out[so_q[b] + i, 0], 0.5 * w @ vb[:p + 1], rtol=0,
+                                       atol=1e-12)
+
+
+def test_count_valid_kv_closed_forms():
+    """Pairs with the queries at the end of the keys: no mask Lq * Lk; plain causal
+    sum_i (Lk - Lq + i + 1) = Lq * (Lk - Lq) + Lq * (Lq + 1) / 2; Lq = Lk is the
+    ordinary count."""
+    lq, lk = [3, 5, 0, 4], [7, 5, 2, 9]
+    assert oracle.count_valid_kv(lq, lk, 2, mask_type=oracle.MASK_NONE) == \
+        2 * sum(a * b for a, b in zip(lq, lk))
+    assert oracle.count_valid_kv(lq, lk, 3, mask_type=oracle.MASK_CAUSAL) == \
+        3 * sum(a * (b - a) + a * (a + 1) // 2 for a, b in zip(lq, lk))
+    so = np.concatenate([[0], np.cumsum(lk)])
+    kw = dict(num_context=[1, 2, 0, 3], num_targets=[2, 1, 0, 5], target_group_size=2)
+    assert oracle.count_valid_kv(lk, lk, 2, **kw) == oracle.count_valid(so, 2, **kw)
+
+
 # --------------------------------------------------------------------------- library cases
 def _torch_dense(q, k, v, rab, alpha, scale, causal):
     """Equal-length, no-context/no-target case with torch fp64 library ops.
