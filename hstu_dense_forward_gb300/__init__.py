@@ -7,7 +7,9 @@ Documentation", Introduction to the HSTU_V1 Forward Operator and the feature
 table): S = Q K^T scaled by alpha, plus the optional relative attention bias
 rab, SiLU, the scaling silu_scale, the causal context/history/target mask or no
 mask, and the product with V. MHA and GQA (Nq a multiple of Nk), fp32, fp16 and
-bf16. The work runs in libhstu_fwd.so (tcgen05/TMA kernels for fp16/bf16, CUDA-core
+bf16. Queries may be fewer than keys (seq_offsets_k: the queries are the last tokens of
+their sequences), and the keys may start with a history held in a paged KV cache
+(kv_cache, page_offsets, page_ids, last_page_len). The work runs in libhstu_fwd.so (tcgen05/TMA kernels for fp16/bf16, CUDA-core
 FFMA for fp32); this module marshals torch tensors to its C ABI and uses torch
 only for device memory and the current stream.
 """
@@ -21,7 +23,7 @@ from . import _abi
 from ._abi import HstuError
 
 __all__ = ["hstu_fwd", "hstu_fwd_noalloc", "HstuFwdPlan", "HstuError", "count_pairs",
-           "useful_flops"]
+           "count_pairs_kv", "useful_flops"]
 
 _DTYPES = {torch.float32: _abi.HSTU_F32, torch.float16: _abi.HSTU_F16,
            torch.bfloat16: _abi.HSTU_BF16}
@@ -29,7 +31,8 @@ _DTYPES = {torch.float32: _abi.HSTU_F32, torch.float16: _abi.HSTU_F16,
 
 def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, index_is_int64,
           causal, target_group_size, has_rab, has_num_context, has_num_targets, watchdog_ms=0,
-          layout="jagged", rab_heads=0, custom_mask=False):
+          layout="jagged", rab_heads=0, custom_mask=False, is_delta_qk=False, max_seqlen_k=0,
+          page_size=0):
     d = _abi.Desc()
     d.dtype = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     d.batch = int(batch)
@@ -49,7 +52,19 @@ def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, inde
         raise ValueError(f"layout must be 'jagged' or 'normal', got {layout!r}")
     d.layout = _abi.HSTU_LAYOUT_NORMAL if layout == "normal" else _abi.HSTU_LAYOUT_JAGGED
     d.rab_heads = int(rab_heads)
+    d.is_delta_qk = int(bool(is_delta_qk))
+    d.max_seqlen_k = int(max_seqlen_k)
+    d.page_size = int(page_size)
     return d
+
+
+def _key_side(d) -> bool:
+    return bool(d.is_delta_qk or d.page_size)
+
+
+def _key_bound(d) -> int:
+    """Bound on the keys of a sequence and the S of rab / mask."""
+    return d.max_seqlen_k if _key_side(d) and d.max_seqlen_k > 0 else d.max_seqlen
 
 
 class HstuFwdPlan:
@@ -73,12 +88,29 @@ class HstuFwdPlan:
                                            out, stream or None), "hstu_fwd_run")
 
     def run(self, q, k, v, seq_offsets, out, *, rab=None, num_context=None, num_targets=None,
-            alpha=1.0, silu_scale=None, stream=None, mask=None):
+            alpha=1.0, silu_scale=None, stream=None, mask=None, seq_offsets_k=None,
+            kv_cache=None, page_offsets=None, page_ids=None, last_page_len=None):
         if silu_scale is None:
-            silu_scale = 1.0 / self.desc.max_seqlen
+            silu_scale = 1.0 / _key_bound(self.desc)
         if stream is None:
             stream = torch.cuda.current_stream(q.device)
         ptr = lambda t: 0 if t is None else t.data_ptr()
+        if _key_side(self.desc):
+            kv = _abi.KV()
+            kv.seq_offsets_k = ptr(seq_offsets_k) or None
+            kv.total_tokens_k = k.shape[0] if seq_offsets_k is not None else q.shape[0]
+            kv.kv_cache = ptr(kv_cache) or None
+            kv.num_pages = 0 if kv_cache is None else kv_cache.shape[0]
+            kv.page_offsets = ptr(page_offsets) or None
+            kv.page_ids = ptr(page_ids) or None
+            kv.last_page_len = ptr(last_page_len) or None
+            extra = mask if self.desc.mask_type == _abi.HSTU_MASK_CUSTOM else rab
+            _abi.check(self._keep.hstu_fwd_run_kv(
+                self._h, q.data_ptr(), ptr(k) or None, ptr(v) or None, ptr(seq_offsets) or None,
+                ctypes.byref(kv), ptr(extra) or None, ptr(num_context) or None,
+                ptr(num_targets) or None, q.shape[0], float(alpha), float(silu_scale),
+                out.data_ptr(), stream.cuda_stream or None), "hstu_fwd_run_kv")
+            return out
         if self.desc.mask_type == _abi.HSTU_MASK_CUSTOM:
             _abi.check(self._keep.hstu_fwd_run_masked(
                 self._h, q.data_ptr(), k.data_ptr(), v.data_ptr(), ptr(seq_offsets) or None,
@@ -143,7 +175,9 @@ def _rab_heads(rab, B, Nq, S):
 
 def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_context=None,
              num_targets=None, causal=True, target_group_size=0, alpha=1.0, silu_scale=None,
-             out=None, watchdog_ms=0, layout="jagged", mask=None):
+             out=None, watchdog_ms=0, layout="jagged", mask=None, seq_offsets_k=None,
+             max_seqlen_k=None, kv_cache=None, page_offsets=None, page_ids=None,
+             last_page_len=None):
     """HSTU forward.
 
     layout "jagged" (default): q [T, Nq, D], k/v [T, Nk, D], seq_offsets [B+1] int32/int64,
@@ -155,6 +189,15 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     selects mask_type 3 (custom mask: P is multiplied by it after the SiLU; no rab, context
     or target counts with it). silu_scale defaults to 1/max_seqlen. Returns out with q's
     shape; rows that belong to no sequence are left as allocated.
+
+    Key side (jagged layout; Inputs and Outputs table, seq_offsets_k / kv_cache rows):
+    seq_offsets_k [B+1] gives the new k/v rows of each sequence (k, v [Tk, Nk, D]; without
+    it they are the query rows). kv_cache [num_pages, 2, page_size, Nk, D] (q's dtype; plane
+    0 K, plane 1 V; page_size 32, 128 or 256) with page_offsets [B+1], page_ids and
+    last_page_len [B] holds a history that precedes the new rows. The Lq queries of a
+    sequence are the last Lq of its Lk keys; max_seqlen bounds Lq, max_seqlen_k (default
+    max_seqlen) bounds Lk and is the S of rab and mask; silu_scale then defaults to
+    1/max_seqlen_k.
     """
     dev = q.device
     if dev.type != "cuda":
@@ -193,8 +236,10 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
             raise ValueError("the jagged layout needs seq_offsets and max_seqlen")
         _check_tensor(seq_offsets, "seq_offsets", None, dev, 1)
         idx_dtype = seq_offsets.dtype
-        if k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
-            raise ValueError("k and v must be [T, Nk, D] with q's T and D")
+        rows_k = k.shape[0] if seq_offsets_k is not None else q.shape[0]
+        if k.shape != v.shape or k.shape[0] != rows_k or k.shape[2] != q.shape[2]:
+            raise ValueError("k and v must be [T, Nk, D] with q's T and D (or [Tk, Nk, D] "
+                             "with seq_offsets_k)")
         B = seq_offsets.shape[0] - 1
         if out is None:
             out = torch.empty_like(q)
@@ -207,25 +252,43 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
         raise ValueError(f"layout must be 'jagged' or 'normal', got {layout!r}")
     if idx_dtype not in (torch.int32, torch.int64):
         raise TypeError("index tensors must be int32 or int64")
-    for name, t in (("num_context", num_context), ("num_targets", num_targets)):
+    for name, t in (("num_context", num_context), ("num_targets", num_targets),
+                    ("seq_offsets_k", seq_offsets_k), ("page_offsets", page_offsets),
+                    ("page_ids", page_ids), ("last_page_len", last_page_len)):
         if t is not None:
             _check_tensor(t, name, idx_dtype, dev, 1)
     T, Nq, D = q3.shape
+    page_size = 0
+    if kv_cache is not None:
+        _check_tensor(kv_cache, "kv_cache", q.dtype, dev, 5)
+        if kv_cache.shape[1] != 2 or tuple(kv_cache.shape[3:]) != (k3.shape[1], D):
+            raise ValueError("kv_cache must be [num_pages, 2, page_size, Nk, D]")
+        if page_offsets is None or page_ids is None or last_page_len is None:
+            raise ValueError("kv_cache needs page_offsets, page_ids and last_page_len")
+        page_size = kv_cache.shape[2]
+    elif page_offsets is not None or page_ids is not None or last_page_len is not None:
+        raise ValueError("a page table needs kv_cache")
+    key_side = seq_offsets_k is not None or kv_cache is not None
+    if key_side and layout != "jagged":
+        raise ValueError("seq_offsets_k and kv_cache need the jagged layout")
+    if max_seqlen_k is not None and not key_side:
+        raise ValueError("max_seqlen_k goes with seq_offsets_k or kv_cache")
+    Sk = int(max_seqlen_k) if max_seqlen_k is not None else int(max_seqlen)
     if rab is not None:
         _check_tensor(rab, "rab", q.dtype, dev, 4)
-    rab_heads = _rab_heads(rab, B, Nq, int(max_seqlen))
+    rab_heads = _rab_heads(rab, B, Nq, Sk)
     custom = mask is not None
     if custom:
         if rab is not None or num_context is not None or num_targets is not None:
             raise ValueError("a custom mask takes no rab, num_context or num_targets")
         _check_tensor(mask, "mask", q.dtype, dev, 4)
-        if tuple(mask.shape) != (B, Nq, int(max_seqlen), int(max_seqlen)):
+        if tuple(mask.shape) != (B, Nq, Sk, Sk):
             raise ValueError(f"mask must be [B, Nq, S, S], got {list(mask.shape)}")
     stream = torch.cuda.current_stream(dev)
     key = (dev.index, stream.cuda_stream, q.dtype, B, Nq, k3.shape[1], D, int(max_seqlen),
            idx_dtype, bool(causal), int(target_group_size), rab is not None,
            num_context is not None, num_targets is not None, int(watchdog_ms), layout, rab_heads,
-           custom)
+           custom, seq_offsets_k is not None, page_size, Sk if key_side else 0)
     plan = _plans.get(key)
     if plan is None:
         with torch.cuda.device(dev):
@@ -235,12 +298,15 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
                                target_group_size=target_group_size, has_rab=rab is not None,
                                has_num_context=num_context is not None,
                                has_num_targets=num_targets is not None, watchdog_ms=watchdog_ms,
-                               layout=layout, rab_heads=rab_heads, custom_mask=custom)
+                               layout=layout, rab_heads=rab_heads, custom_mask=custom,
+                               is_delta_qk=seq_offsets_k is not None,
+                               max_seqlen_k=Sk if key_side else 0, page_size=page_size)
         _plans[key] = plan
     with torch.cuda.device(dev):
         plan.run(q3, k3, v3, seq_offsets, out3, rab=rab, num_context=num_context,
                  num_targets=num_targets, alpha=alpha, silu_scale=silu_scale, stream=stream,
-                 mask=mask)
+                 mask=mask, seq_offsets_k=seq_offsets_k, kv_cache=kv_cache,
+                 page_offsets=page_offsets, page_ids=page_ids, last_page_len=last_page_len)
     return res
 
 
@@ -296,6 +362,29 @@ def count_pairs(seq_offsets, num_heads_q, *, max_seqlen, num_context=None, num_t
     ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     _abi.check(_abi.lib().hstu_fwd_count_pairs(ctypes.byref(d), ptr(so), ptr(nc), ptr(nt),
                                                ctypes.byref(out)), "hstu_fwd_count_pairs")
+    return int(out.value)
+
+
+def count_pairs_kv(seq_offsets, num_heads_q, *, max_seqlen, seq_offsets_k=None,
+                   page_offsets=None, last_page_len=None, page_size=0, max_seqlen_k=None,
+                   num_context=None, num_targets=None, causal=True, target_group_size=0) -> int:
+    """count_pairs for calls whose queries are the last tokens of longer key sequences
+    (seq_offsets_k and / or a KV cache page table), from CPU integer data."""
+    t64 = lambda x: None if x is None else torch.as_tensor(x, dtype=torch.int64).contiguous().cpu()
+    so, sok, po, last = t64(seq_offsets), t64(seq_offsets_k), t64(page_offsets), t64(last_page_len)
+    nc, nt = t64(num_context), t64(num_targets)
+    key_side = sok is not None or po is not None
+    d = _desc(dtype=_abi.HSTU_BF16, batch=so.numel() - 1, num_heads_q=num_heads_q,
+              num_heads_kv=1, head_dim=64, max_seqlen=max_seqlen, index_is_int64=True,
+              causal=causal, target_group_size=target_group_size, has_rab=False,
+              has_num_context=nc is not None, has_num_targets=nt is not None,
+              is_delta_qk=sok is not None,
+              max_seqlen_k=(max_seqlen_k or 0) if key_side else 0, page_size=page_size)
+    out = ctypes.c_longlong(0)
+    ptr = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    _abi.check(_abi.lib().hstu_fwd_count_pairs_kv(ctypes.byref(d), ptr(so), ptr(sok), ptr(po),
+                                                  ptr(last), ptr(nc), ptr(nt),
+                                                  ctypes.byref(out)), "hstu_fwd_count_pairs_kv")
     return int(out.value)
 
 

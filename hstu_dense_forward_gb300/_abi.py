@@ -36,7 +36,23 @@ class Desc(ctypes.Structure):
         ("watchdog_ms", ctypes.c_int),
         ("layout", ctypes.c_int),
         ("rab_heads", ctypes.c_int),
+        ("is_delta_qk", ctypes.c_int),
+        ("max_seqlen_k", ctypes.c_int),
+        ("page_size", ctypes.c_int),
         ("reserved", ctypes.c_int),
+    ]
+
+
+class KV(ctypes.Structure):
+    """hstu_fwd_kv: the key side of hstu_fwd_run_kv (device pointers)."""
+    _fields_ = [
+        ("seq_offsets_k", ctypes.c_void_p),
+        ("total_tokens_k", ctypes.c_longlong),
+        ("kv_cache", ctypes.c_void_p),
+        ("num_pages", ctypes.c_longlong),
+        ("page_offsets", ctypes.c_void_p),
+        ("page_ids", ctypes.c_void_p),
+        ("last_page_len", ctypes.c_void_p),
     ]
 
 
@@ -83,6 +99,12 @@ def lib():
                                            ctypes.POINTER(ctypes.c_longlong)]
         L.hstu_fwd_run_masked.restype = ctypes.c_int
         L.hstu_fwd_run_masked.argtypes = [vp, vp, vp, vp, vp, vp, ll, f, f, vp, vp]
+        L.hstu_fwd_run_kv.restype = ctypes.c_int
+        L.hstu_fwd_run_kv.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(KV), vp, vp, vp, ll, f, f,
+                                      vp, vp]
+        L.hstu_fwd_count_pairs_kv.restype = ctypes.c_int
+        L.hstu_fwd_count_pairs_kv.argtypes = [ctypes.POINTER(Desc), vp, vp, vp, vp, vp, vp,
+                                              ctypes.POINTER(ctypes.c_longlong)]
         L.hstu_fwd_run_noalloc.restype = ctypes.c_int
         L.hstu_fwd_run_noalloc.argtypes = [ctypes.POINTER(Desc), vp, vp, vp, vp, vp, vp, vp, ll, f,
                                            f, vp, vp]

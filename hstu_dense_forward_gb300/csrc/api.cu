@@ -55,10 +55,10 @@ struct hstu_fwd_plan {
   int* d_err;          // device error word (d_count[1])
   int parity;          // work list of the next run
   long long timeout_ns;
-  // tensor maps of the last run, re-encoded when a pointer or T changes
+  // tensor maps of the last run, re-encoded when a pointer or a row count changes
   TcMaps maps;
-  const void* map_ptrs[5];
-  long long map_T;
+  const void* map_ptrs[6];
+  long long map_T, map_Tk, map_pages;
   bool maps_valid;
 };
 
@@ -85,9 +85,24 @@ static bool layout_args_ok(const hstu_fwd_desc& d, const void* seq_offsets,
   return seq_offsets != nullptr;
 }
 
+// The key side differs from the queries (own offsets or a KV cache).
+static bool key_side(const hstu_fwd_desc& d) { return d.is_delta_qk || d.page_size; }
+
+// Bound on the keys of a sequence, and the S of rab and of a custom mask.
+static int key_bound(const hstu_fwd_desc& d) {
+  return key_side(d) && d.max_seqlen_k > 0 ? d.max_seqlen_k : d.max_seqlen;
+}
+
 static hstu_status validate_desc(const hstu_fwd_desc* d) {
   if (!d) return HSTU_ERR_INVALID_ARG;
   if (d->reserved) return HSTU_ERR_INVALID_ARG;
+  if (d->is_delta_qk != 0 && d->is_delta_qk != 1) return HSTU_ERR_INVALID_ARG;
+  if (d->page_size != 0 && d->page_size != 32 && d->page_size != 128 && d->page_size != 256)
+    return HSTU_ERR_INVALID_ARG;  // Inputs and Outputs table: page_size in {32, 128, 256}
+  if (d->max_seqlen_k < 0 || d->max_seqlen_k > hstu::kMaxMTiles * hstu::kTileM ||
+      (!key_side(*d) && d->max_seqlen_k != 0))
+    return HSTU_ERR_INVALID_ARG;
+  if (key_side(*d) && d->layout != HSTU_LAYOUT_JAGGED) return HSTU_ERR_UNSUPPORTED;
   if (d->layout != HSTU_LAYOUT_JAGGED && d->layout != HSTU_LAYOUT_NORMAL)
     return HSTU_ERR_INVALID_ARG;
   if (d->rab_heads != 0 && d->rab_heads != 1 && d->rab_heads != d->num_heads_q)
@@ -110,13 +125,13 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
     // the rab path, so rab and a custom mask together are not built
     if (d->has_num_context || d->has_num_targets || d->rab_heads) return HSTU_ERR_INVALID_ARG;
     if (d->has_rab) return HSTU_ERR_UNSUPPORTED;
-    if (d->dtype != HSTU_F32 && d->max_seqlen % 8 != 0) return HSTU_ERR_UNSUPPORTED;
+    if (d->dtype != HSTU_F32 && key_bound(*d) % 8 != 0) return HSTU_ERR_UNSUPPORTED;
   }
   if (d->dtype == HSTU_F32) {
     if (d->head_dim > 256) return HSTU_ERR_UNSUPPORTED;
   } else {
     if (!hstu::tc_supported_dim(d->head_dim)) return HSTU_ERR_UNSUPPORTED;
-    if (d->has_rab && d->max_seqlen % 8 != 0) return HSTU_ERR_UNSUPPORTED;
+    if (d->has_rab && key_bound(*d) % 8 != 0) return HSTU_ERR_UNSUPPORTED;
   }
   return HSTU_OK;
 }
@@ -184,10 +199,27 @@ static bool encode3d(CUtensorMap* m, CUtensorMapDataType ty, const void* base, u
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+static bool encode4d(CUtensorMap* m, CUtensorMapDataType ty, const void* base,
+                     const uint64_t (&dims)[4], const uint64_t (&strides)[3],
+                     const uint32_t (&box)[4], CUtensorMapSwizzle swz) {
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+  const cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return encode_fn()(m, ty, 4, const_cast<void*>(base), d, st, b, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps: q and out over T rows, k and v over Tk rows (at least one row is mapped: a
+// call without new k/v rows never loads them), rab [planes, Sk, Sk], and the KV cache
+// [num_pages, 2, page_size, Nk, D] as 4-D (D, Nk, page_size, 2 * num_pages).
 static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
-                             const void* rab, const void* out, long long T) {
-  const void* ptrs[5] = {q, k, v, rab, out};
-  if (P->maps_valid && P->map_T == T && memcmp(ptrs, P->map_ptrs, sizeof(ptrs)) == 0)
+                             const void* rab, const void* out, long long T, long long Tk,
+                             const void* cache, long long num_pages) {
+  const void* ptrs[6] = {q, k, v, rab, out, cache};
+  if (P->maps_valid && P->map_T == T && P->map_Tk == Tk && P->map_pages == num_pages &&
+      memcmp(ptrs, P->map_ptrs, sizeof(ptrs)) == 0)
     return HSTU_OK;
   const hstu_fwd_desc& d = P->desc;
   const CUtensorMapDataType ty =
@@ -202,22 +234,31 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
                  Nk = (uint64_t)d.num_heads_kv;
   bool ok = encode3d(&P->maps.q, ty, q, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, epc, 1,
                      hstu::kTileM, swz) &&
-            encode3d(&P->maps.k, ty, k, D, Nk, (uint64_t)T, D * 2, Nk * D * 2, epc, 1,
-                     hstu::kTileN, swz) &&
-            encode3d(&P->maps.v, ty, v, D, Nk, (uint64_t)T, D * 2, Nk * D * 2, epc, 1,
-                     hstu::kTileN, swz) &&
+            encode3d(&P->maps.k, ty, k ? k : (cache ? cache : q), D, Nk, (uint64_t)(Tk > 0 ? Tk : 1), D * 2,
+                     Nk * D * 2, epc, 1, hstu::kTileN, swz) &&
+            encode3d(&P->maps.v, ty, v ? v : (cache ? cache : q), D, Nk, (uint64_t)(Tk > 0 ? Tk : 1), D * 2,
+                     Nk * D * 2, epc, 1, hstu::kTileN, swz) &&
             encode3d(&P->maps.out, ty, out, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, oc, 1, 32,
                      oc * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                      : oc * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                      : oc * 2 == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
                                     : CU_TENSOR_MAP_SWIZZLE_NONE);
   if (ok && rab) {
-    const uint64_t S = (uint64_t)d.max_seqlen;
+    const uint64_t S = (uint64_t)key_bound(d);
     ok = encode3d(&P->maps.rab, ty, rab, S, S, (uint64_t)d.batch * (d.rab_heads == 1 ? 1 : Nq),
                   S * 2, S * S * 2, 64,
                   hstu::kTileM, 1, CU_TENSOR_MAP_SWIZZLE_128B);
   } else if (ok) {
     P->maps.rab = P->maps.q;  // unused by the kernel
+  }
+  if (ok && cache) {
+    const uint64_t ps = (uint64_t)d.page_size;
+    const uint64_t dims[4] = {D, Nk, ps, 2 * (uint64_t)num_pages};
+    const uint64_t strides[3] = {D * 2, Nk * D * 2, ps * Nk * D * 2};
+    const uint32_t box[4] = {epc, 1, (uint32_t)(ps < 128 ? ps : 128), 1};
+    ok = encode4d(&P->maps.cache, ty, cache, dims, strides, box, swz);
+  } else if (ok) {
+    P->maps.cache = P->maps.q;  // unused by the kernel
   }
   if (!ok) {
     P->maps_valid = false;
@@ -225,21 +266,50 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
   }
   memcpy(P->map_ptrs, ptrs, sizeof(ptrs));
   P->map_T = T;
+  P->map_Tk = Tk;
+  P->map_pages = num_pages;
   P->maps_valid = true;
   return HSTU_OK;
 }
 
+// The key-side arguments a plan needs: none (kv NULL) for a plain plan; seq_offsets_k with
+// is_delta_qk; the cache and its page table with page_size.
+static bool kv_args_ok(const hstu_fwd_desc& d, const hstu_fwd_kv* kv, long long total_tokens) {
+  if (!key_side(d)) return kv == nullptr;
+  if (!kv) return false;
+  if (d.is_delta_qk) {
+    if (!kv->seq_offsets_k || kv->total_tokens_k < 0 || kv->total_tokens_k > 0x7fffffffll)
+      return false;
+  } else if (kv->seq_offsets_k) {
+    return false;
+  }
+  if (d.page_size) {
+    if (!kv->kv_cache || !kv->page_offsets || !kv->page_ids || !kv->last_page_len ||
+        kv->num_pages < 1 || kv->num_pages > (1ll << 30) || !aligned16(kv->kv_cache))
+      return false;
+  } else if (kv->kv_cache || kv->page_offsets || kv->page_ids || kv->last_page_len) {
+    return false;
+  }
+  (void)total_tokens;
+  return true;
+}
+
 // One forward. `rab` carries the relative attention bias, or the custom mask when
-// is_mask (plans of mask_type CUSTOM, through hstu_fwd_run_masked).
+// is_mask (plans of mask_type CUSTOM). `kv` describes the key side (NULL: the keys are the
+// query rows of k and v).
 static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
-                            const void* seq_offsets, const void* rab, bool is_mask,
-                            const void* num_context, const void* num_targets,
+                            const void* seq_offsets, const hstu_fwd_kv* kv, const void* rab,
+                            bool is_mask, const void* num_context, const void* num_targets,
                             long long total_tokens, float alpha, float silu_scale, void* out,
                             void* stream) {
   const hstu_fwd_desc& d = P->desc;
   if (total_tokens < 0 || total_tokens > 0x7fffffffll) return HSTU_ERR_INVALID_ARG;
+  if (!kv_args_ok(d, kv, total_tokens)) return HSTU_ERR_INVALID_ARG;
   if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
-  if (!q || !k || !v || !out || !layout_args_ok(d, seq_offsets, total_tokens))
+  const long long Tk = d.is_delta_qk ? kv->total_tokens_k : total_tokens;
+  const bool kv_rows = Tk > 0;  // k and v are read only when there are new rows
+  if (!q || !out || !layout_args_ok(d, seq_offsets, total_tokens) ||
+      (kv_rows && (!k || !v)))
     return HSTU_ERR_INVALID_ARG;
   if ((rab != nullptr) != (is_mask || d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
   if ((num_context != nullptr) != (d.has_num_context != 0)) return HSTU_ERR_INVALID_ARG;
@@ -249,6 +319,7 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
     return HSTU_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != P->device) return HSTU_ERR_INVALID_ARG;
+  const void* cache = d.page_size ? kv->kv_cache : nullptr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   FwdParams p = {};
@@ -273,7 +344,18 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   p.Nq = d.num_heads_q;
   p.Nk = d.num_heads_kv;
   p.D = d.head_dim;
-  p.S = d.max_seqlen;
+  p.S = key_bound(d);
+  p.Sq = d.max_seqlen;
+  p.total_tokens_k = Tk;
+  if (d.is_delta_qk) p.seq_offsets_k = kv->seq_offsets_k;
+  if (d.page_size) {
+    p.kv_cache = kv->kv_cache;
+    p.page_offsets = kv->page_offsets;
+    p.page_ids = kv->page_ids;
+    p.last_page_len = kv->last_page_len;
+    p.num_pages = kv->num_pages;
+    p.page_size = d.page_size;
+  }
   p.mask_type = is_mask ? hstu::kMaskNone : d.mask_type;  // a custom mask: every key a candidate
   p.g = d.mask_type == HSTU_MASK_CAUSAL ? d.target_group_size : 0;
   p.dense = d.layout == HSTU_LAYOUT_NORMAL ? 1 : 0;
@@ -283,7 +365,8 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   p.silu_scale = silu_scale;
 
   if (P->tensor_cores) {
-    hstu_status ms = make_maps(P, q, k, v, rab, out, total_tokens);
+    hstu_status ms = make_maps(P, q, k, v, rab, out, total_tokens, Tk, cache,
+                               d.page_size ? kv->num_pages : 0);
     if (ms != HSTU_OK) return ms;
   }
   if (hstu::launch_build_worklist(p, P->d_work + b * P->work_cap, P->d_count + 4 * b,
@@ -300,8 +383,22 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
                          const void* num_targets, long long total_tokens, float alpha,
                          float silu_scale, void* out, void* stream) {
   if (!P || P->desc.mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_INVALID_ARG;
-  return run_impl(P, q, k, v, seq_offsets, rab, false, num_context, num_targets, total_tokens,
-                  alpha, silu_scale, out, stream);
+  return run_impl(P, q, k, v, seq_offsets, nullptr, rab, false, num_context, num_targets,
+                  total_tokens, alpha, silu_scale, out, stream);
+}
+
+hstu_status hstu_fwd_run_kv(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
+                            const void* seq_offsets, const hstu_fwd_kv* kv,
+                            const void* rab_or_mask, const void* num_context,
+                            const void* num_targets, long long total_tokens, float alpha,
+                            float silu_scale, void* out, void* stream) {
+  if (!P) return HSTU_ERR_INVALID_ARG;
+  const bool custom = P->desc.mask_type == HSTU_MASK_CUSTOM;
+  if (custom && (num_context || num_targets)) return HSTU_ERR_INVALID_ARG;
+  if (custom && !rab_or_mask && P->desc.batch > 0 && P->desc.num_heads_q > 0 && total_tokens > 0)
+    return HSTU_ERR_INVALID_ARG;
+  return run_impl(P, q, k, v, seq_offsets, kv, rab_or_mask, custom, num_context, num_targets,
+                  total_tokens, alpha, silu_scale, out, stream);
 }
 
 hstu_status hstu_fwd_run_masked(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
@@ -311,8 +408,8 @@ hstu_status hstu_fwd_run_masked(hstu_fwd_plan* P, const void* q, const void* k, 
   if (!P || P->desc.mask_type != HSTU_MASK_CUSTOM) return HSTU_ERR_INVALID_ARG;
   if (!mask && P->desc.batch > 0 && P->desc.num_heads_q > 0 && total_tokens > 0)
     return HSTU_ERR_INVALID_ARG;
-  return run_impl(P, q, k, v, seq_offsets, mask, true, nullptr, nullptr, total_tokens, alpha,
-                  silu_scale, out, stream);
+  return run_impl(P, q, k, v, seq_offsets, nullptr, mask, true, nullptr, nullptr, total_tokens,
+                  alpha, silu_scale, out, stream);
 }
 
 hstu_status hstu_fwd_destroy(hstu_fwd_plan* P) {
@@ -369,6 +466,57 @@ hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* d, const void* seq_offsets
     const hstu::SeqGeom s = hstu::make_geom((int)L, nc, nt, g, mt);
     long long c = 0;
     for (int i = 0; i < (int)L; ++i) {
+      const hstu::RowRange r = hstu::row_range(s, i, mt);
+      c += r.hist_end;
+      if (r.grp_hi >= r.grp_lo) c += r.grp_hi - r.grp_lo + 1;
+    }
+    total += c * d->num_heads_q;
+  }
+  *pairs = total;
+  return HSTU_OK;
+}
+
+hstu_status hstu_fwd_count_pairs_kv(const hstu_fwd_desc* d, const void* seq_offsets_host,
+                                    const void* seq_offsets_k_host,
+                                    const void* page_offsets_host,
+                                    const void* last_page_len_host,
+                                    const void* num_context_host, const void* num_targets_host,
+                                    long long* pairs) {
+  if (!d || !pairs) return HSTU_ERR_INVALID_ARG;
+  if (d->batch > 0 && !seq_offsets_host) return HSTU_ERR_INVALID_ARG;
+  if (d->layout != HSTU_LAYOUT_JAGGED) return HSTU_ERR_UNSUPPORTED;
+  if ((page_offsets_host != nullptr) != (last_page_len_host != nullptr)) return HSTU_ERR_INVALID_ARG;
+  if (page_offsets_host && d->page_size <= 0) return HSTU_ERR_INVALID_ARG;
+  if (d->mask_type != HSTU_MASK_CAUSAL && d->mask_type != HSTU_MASK_NONE &&
+      d->mask_type != HSTU_MASK_CUSTOM)
+    return HSTU_ERR_UNSUPPORTED;
+  const int is64 = d->index_is_int64 ? 1 : 0;
+  const int g = d->mask_type == HSTU_MASK_CAUSAL ? d->target_group_size : 0;
+  const int mt = d->mask_type == HSTU_MASK_CUSTOM ? HSTU_MASK_NONE : d->mask_type;
+  const long long Sk = key_bound(*d);
+  long long total = 0;
+  for (int b = 0; b < d->batch; ++b) {
+    const long long Lq = hstu::load_index(seq_offsets_host, b + 1, is64) -
+                         hstu::load_index(seq_offsets_host, b, is64);
+    long long Lk = seq_offsets_k_host ? hstu::load_index(seq_offsets_k_host, b + 1, is64) -
+                                            hstu::load_index(seq_offsets_k_host, b, is64)
+                                      : Lq;
+    if (page_offsets_host) {
+      const long long pages = hstu::load_index(page_offsets_host, b + 1, is64) -
+                              hstu::load_index(page_offsets_host, b, is64);
+      if (pages < 0) return HSTU_ERR_INVALID_ARG;
+      if (pages > 0) {
+        const long long last = hstu::load_index(last_page_len_host, b, is64);
+        if (last < 1 || last > d->page_size || pages > Sk) return HSTU_ERR_INVALID_ARG;
+        Lk += (pages - 1) * d->page_size + last;
+      }
+    }
+    if (Lq < 0 || Lq > d->max_seqlen || Lk < Lq || Lk > Sk) return HSTU_ERR_INVALID_ARG;
+    const long long nc = num_context_host ? hstu::load_index(num_context_host, b, is64) : 0;
+    const long long nt = num_targets_host ? hstu::load_index(num_targets_host, b, is64) : 0;
+    const hstu::SeqGeom s = hstu::make_geom((int)Lk, nc, nt, g, mt);
+    long long c = 0;
+    for (int i = (int)(Lk - Lq); i < (int)Lk; ++i) {
       const hstu::RowRange r = hstu::row_range(s, i, mt);
       c += r.hist_end;
       if (r.grp_hi >= r.grp_lo) c += r.grp_hi - r.grp_lo + 1;
@@ -437,6 +585,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   if ((long long)d.batch * hstu::ceil_div(d.max_seqlen, hstu::kTileM) > HSTU_NOALLOC_MAX_ENTRIES)
     return HSTU_ERR_UNSUPPORTED;  // work list larger than the static scratch array
   if (d.mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_UNSUPPORTED;  // hstu_fwd_run_masked only
+  if (key_side(d)) return HSTU_ERR_UNSUPPORTED;                       // hstu_fwd_run_kv only
   if (!q || !k || !v || !out || !layout_args_ok(d, seq_offsets, total_tokens))
     return HSTU_ERR_INVALID_ARG;
   if ((rab != nullptr) != (d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
@@ -481,6 +630,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   p.Nk = d.num_heads_kv;
   p.D = d.head_dim;
   p.S = d.max_seqlen;
+  p.Sq = d.max_seqlen;
   p.mask_type = d.mask_type;
   p.g = d.mask_type == HSTU_MASK_CAUSAL ? d.target_group_size : 0;
   p.dense = d.layout == HSTU_LAYOUT_NORMAL ? 1 : 0;
@@ -516,6 +666,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
     } else if (ok) {
       maps.rab = maps.q;  // unused by the kernel
     }
+    maps.cache = maps.q;  // no KV cache on this entry point
     if (!ok) return HSTU_ERR_INVALID_ARG;
   }
   // the error word keeps the previous call's value: clear it (the count is rewritten)

@@ -111,6 +111,37 @@ HSTU_HD bool tile_all_valid(const SeqGeom& s, int m0, int rows, int n0, int cols
 
 HSTU_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Key tiles of one work item when the keys are a cached history of `hist` positions
+// followed by new rows. Key tile x covers positions [128x, 128x + 128). A tile in which
+// the history ends and new rows begin is visited twice, first with its cached rows
+// (columns [0, hist % 128)), then with its new rows (columns [hist % 128, 128)), so that
+// every visit loads one run of rows of one tensor. split_tile is that tile, or -1.
+HSTU_HD int split_tile(int hist, int Lk) {
+  return (hist % kTileN != 0 && hist < Lk) ? hist / kTileN : -1;
+}
+
+// Visits of an item whose keys end (for its rows) at kv_end.
+HSTU_HD int key_visits(int kv_end, int split) {
+  const int n = ceil_div(kv_end, kTileN);
+  return n + ((split >= 0 && split < n) ? 1 : 0);
+}
+
+struct KeyTile {
+  int x;         // key tile: positions [128x, 128x + 128)
+  int clo, chi;  // columns of the tile this visit covers
+  bool cached;   // rows come from the cache (else from k / v)
+};
+
+HSTU_HD KeyTile key_tile(int j, int split, int hist) {
+  KeyTile t;
+  const bool second = split >= 0 && j == split + 1;  // new-row part of the split tile
+  t.x = (split >= 0 && j > split) ? j - 1 : j;
+  t.clo = second ? hist % kTileN : 0;
+  t.chi = j == split ? hist % kTileN : kTileN;
+  t.cached = !second && t.x * kTileN < hist;
+  return t;
+}
+
 HSTU_HD uint32_t pack_item(int b, int mt) { return ((uint32_t)b << 10) | (uint32_t)mt; }
 HSTU_HD int item_b(uint32_t e) { return (int)(e >> 10); }
 HSTU_HD int item_mt(uint32_t e) { return (int)(e & 1023u); }

@@ -52,20 +52,23 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams 
     const int h = (int)(it % p.Nq);
     const uint32_t e = p.work[it / p.Nq];
     const int b = item_b(e);
-    const long long t0 = seq_start(p, b);
-    const int L = (int)(seq_start(p, b + 1) - t0);
+    const SeqKV kv = seq_kv(p, b);
+    const long long t0 = kv.tq;
+    const int Lq = (int)kv.Lq, L = (int)kv.Lk, hist = (int)kv.hist;
+    const int off = L - Lq;  // key position of query row 0
     const int m0 = item_mt(e) * kTileM + half * BM;
-    if (m0 >= L) continue;
+    if (m0 >= Lq) continue;
     const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
     const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
     const SeqGeom s = make_geom(L, nc, nt, p.g, p.mask_type);
-    const int kv_end = kv_end_for_rows(s, m0, BM, p.mask_type);
+    const int kv_end = kv_end_for_rows(s, off + m0, BM, p.mask_type);
     const int hk = h / G;
+    const float* cache = static_cast<const float*>(p.kv_cache);
 
     __syncthreads();  // previous item finished with the shared tiles
     for (int x = threadIdx.x; x < BM * D; x += kThreads) {
       const int r = x / D, d = x - r * D;
-      Qs[x] = (m0 + r < L) ? q[((t0 + m0 + r) * p.Nq + h) * D + d] : 0.f;
+      Qs[x] = (m0 + r < Lq) ? q[((t0 + m0 + r) * p.Nq + h) * D + d] : 0.f;
     }
     float acc[4][kMaxU];
 #pragma unroll
@@ -77,10 +80,22 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams 
       __syncthreads();  // previous step finished with Ks/Vs/Ps
       for (int x = threadIdx.x; x < BN * D; x += kThreads) {
         const int r = x / D, d = x - r * D;
-        const bool in = n0 + r < L;
-        const long long g = ((t0 + n0 + r) * p.Nk + hk) * D + d;
-        Ks[r * ldk + d] = in ? k[g] : 0.f;
-        Vs[x] = in ? v[g] : 0.f;
+        const int pos = n0 + r;  // key position
+        float kx = 0.f, vx = 0.f;
+        if (pos < hist) {  // cached history: page row pos % page_size
+          const long long page =
+              load_index(p.page_ids, kv.po + pos / p.page_size, p.index64);
+          const long long g =
+              ((page * 2 * p.page_size + pos % p.page_size) * p.Nk + hk) * D + d;
+          kx = cache[g];
+          vx = cache[g + (long long)p.page_size * p.Nk * D];
+        } else if (pos < L) {  // new rows
+          const long long g = ((kv.tk + pos - hist) * p.Nk + hk) * D + d;
+          kx = k[g];
+          vx = v[g];
+        }
+        Ks[r * ldk + d] = kx;
+        Vs[x] = vx;
       }
       __syncthreads();
       // S for rows ty + 16a, columns tx + 16c
@@ -103,13 +118,13 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams 
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         const int r = ty + 16 * a;
-        const int i = m0 + r;
+        const int i = off + m0 + r;  // key position of the query row
         const RowRange rr = row_range(s, i, p.mask_type);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int j = n0 + tx + 16 * c;
           float x = p.alpha * sc[a][c];
-          const bool ok = (i < L) && (j < L) && valid_in_range(rr, j);
+          const bool ok = (m0 + r < Lq) && (j < L) && valid_in_range(rr, j);
           const float t = (rab != nullptr && ok) ? rab[(rab_plane(p, b, h) * p.S + i) * p.S + j]
                                                  : 0.f;
           if (!p.rab_is_mask) x += t;  // relative attention bias before the SiLU
@@ -138,7 +153,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams 
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const int i = m0 + ty + 16 * a;
-      if (i >= L) continue;
+      if (i >= Lq) continue;
 #pragma unroll
       for (int u = 0; u < kMaxU; ++u) {
         const int d = tx + 16 * u;

@@ -113,9 +113,13 @@ struct Cfg {
 
 // One work item, decoded once (by the Q producer) and read by every role.
 struct Item {
-  int b, h, hk, L, m0, n_kv;
-  long long t0;
-  SeqGeom geom;
+  int b, h, hk, m0, n_kv;
+  int tq, Lq;      // first query row of the sequence, query rows
+  int tk, hist;    // first new k/v row, cached keys (key positions [0, hist))
+  int off;         // key position of query row 0 (Lk - Lq)
+  int split;       // key tile visited twice (cached part, new part), or -1
+  int po;          // first page_ids entry of the sequence
+  SeqGeom geom;    // over the Lk keys
 };
 
 constexpr int kInfoDepth = 8;                   // decoded items kept in shared memory
@@ -143,12 +147,18 @@ __device__ __forceinline__ bool decode_item(const FwdParams& p, long long idx, I
   it.hk = it.h / (p.Nq / p.Nk);
   it.b = item_b(e);
   it.m0 = item_mt(e) * kTileM;
-  it.t0 = seq_start(p, it.b);
-  it.L = (int)(seq_start(p, it.b + 1) - it.t0);
+  const SeqKV kv = seq_kv(p, it.b);
+  it.tq = (int)kv.tq;
+  it.Lq = (int)kv.Lq;
+  it.tk = (int)kv.tk;
+  it.hist = (int)kv.hist;
+  it.po = (int)kv.po;
+  it.off = (int)(kv.Lk - kv.Lq);
   const long long nc = p.num_context ? load_index(p.num_context, it.b, p.index64) : 0;
   const long long nt = p.num_targets ? load_index(p.num_targets, it.b, p.index64) : 0;
-  it.geom = make_geom(it.L, nc, nt, p.g, p.mask_type);
-  it.n_kv = ceil_div(kv_end_for_rows(it.geom, it.m0, kTileM, p.mask_type), kTileN);
+  it.geom = make_geom((int)kv.Lk, nc, nt, p.g, p.mask_type);
+  it.split = split_tile(it.hist, (int)kv.Lk);
+  it.n_kv = key_visits(kv_end_for_rows(it.geom, it.off + it.m0, kTileM, p.mask_type), it.split);
   return true;
 }
 
@@ -207,6 +217,10 @@ __device__ __forceinline__ uint32_t chunk_mask(const RowRange& r, int base) {
   const uint32_t hist = low_bits(r.hist_end - base);
   const uint32_t grp = low_bits(r.grp_hi - base + 1) & ~low_bits(r.grp_lo - base);
   return r.grp_lo <= r.grp_hi ? (hist | grp) : hist;
+}
+// Bits e set where tile column cc + e lies in the visit's column range [clo, chi).
+__device__ __forceinline__ uint32_t cols_mask(const KeyTile& kt, int cc) {
+  return low_bits(kt.chi - cc) & ~low_bits(kt.clo - cc);
 }
 
 template <bool BF16>
@@ -269,7 +283,7 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
         decode_item(p, nidx, nx);
 #pragma unroll
         for (int cb = 0; cb < C::NCB; ++cb)
-          ptx::tma_prefetch_3d(tq, cb * C::EPC, nx.h, (int)(nx.t0 + nx.m0));
+          ptx::tma_prefetch_3d(tq, cb * C::EPC, nx.h, nx.tq + nx.m0);
       }
     }
     const int s = q_it % C::NQ;
@@ -279,15 +293,69 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
     const uint32_t dst = sbase + C::OFF_Q + s * C::TILE_BYTES;
 #pragma unroll
     for (int cb = 0; cb < C::NCB; ++cb)
-      ptx::tma_load_3d(dst + cb * C::CB_BYTES, tq, full, cb * C::EPC, it.h, (int)(it.t0 + it.m0));
+      ptx::tma_load_3d(dst + cb * C::CB_BYTES, tq, full, cb * C::EPC, it.h, it.tq + it.m0);
     ++q_it;
     idx = C::NQ == 1 ? nidx : claim();
   }
 }
 
+// Pages of the KV cache behind one cached key tile (x, positions [128x, 128x + 128), with
+// 128x < hist): one page of >= 128 rows, or four pages of 32 rows. Slots past the sequence's
+// last page repeat the last page: their rows lie beyond the history, where P is 0.
+struct TilePages {
+  int id[4];
+};
+
+__device__ __forceinline__ TilePages tile_pages(const FwdParams& p, const Item& it, int x) {
+  TilePages t;
+  const int npages = ceil_div(it.hist, p.page_size);
+  if (p.page_size >= kTileN) {
+    t.id[0] = (int)load_index(p.page_ids, it.po + (x * kTileN) / p.page_size, p.index64);
+  } else {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int slot = min(x * 4 + m, npages - 1);
+      t.id[m] = (int)load_index(p.page_ids, it.po + slot, p.index64);
+    }
+  }
+  return t;
+}
+
+// One K or V tile (plane 0 or 1) of key visit j into shared memory at dst: from the
+// cache pages when the visit's rows are cached, else rows tk + 128x - hist .. of k / v
+// (rows before the sequence's first new row belong to the cached part of a split tile
+// and meet P = 0 there).
+template <int D, bool RAB>
+__device__ __forceinline__ void load_kv_tile(const FwdParams& p, const Item& it, int j,
+                                             const TilePages& pg, const CUtensorMap* tnew,
+                                             const CUtensorMap* tcache, int plane, uint32_t dst,
+                                             uint32_t full) {
+  using C = Cfg<D, RAB>;
+  const KeyTile kt = key_tile(j, it.split, it.hist);
+  if (!kt.cached) {
+    const int row = it.tk + kt.x * kTileN - it.hist;
+#pragma unroll
+    for (int cb = 0; cb < C::NCB; ++cb)
+      ptx::tma_load_3d(dst + cb * C::CB_BYTES, tnew, full, cb * C::EPC, it.hk, row);
+  } else if (p.page_size >= kTileN) {
+    const int r0 = (kt.x * kTileN) % p.page_size;
+#pragma unroll
+    for (int cb = 0; cb < C::NCB; ++cb)
+      ptx::tma_load_4d(dst + cb * C::CB_BYTES, tcache, full, cb * C::EPC, it.hk, r0,
+                       2 * pg.id[0] + plane);
+  } else {  // four pages of 32 rows
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int cb = 0; cb < C::NCB; ++cb)
+        ptx::tma_load_4d(dst + cb * C::CB_BYTES + m * 32 * C::SWB, tcache, full, cb * C::EPC,
+                         it.hk, 0, 2 * pg.id[m] + plane);
+  }
+}
+
 template <int D, bool RAB>
 __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tk,
-                           long long total) {
+                           const CUtensorMap* tc, long long total) {
   using C = Cfg<D, RAB>;
   uint32_t k_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -296,14 +364,14 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
     if (!get_item(bars, k, it, p) || it.n_kv < 0) return;
     for (int j = 0; j < it.n_kv; ++j) {
       const int s = k_it % C::NK;
-      const int row = (int)(it.t0 + j * kTileN);
+      // page ids are read before the wait for the slot, which hides their latency
+      TilePages pg = {};
+      const KeyTile kt = key_tile(j, it.split, it.hist);
+      if (kt.cached) pg = tile_pages(p, it, kt.x);
       if (!wait_bar(bars, &bars->k_empty[s], ((k_it / C::NK) & 1) ^ 1, p)) return;
       const uint32_t full = ptx::smem_u32(&bars->k_full[s]);
       ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
-      const uint32_t dst = sbase + C::OFF_K + s * C::TILE_BYTES;
-#pragma unroll
-      for (int cb = 0; cb < C::NCB; ++cb)
-        ptx::tma_load_3d(dst + cb * C::CB_BYTES, tk, full, cb * C::EPC, it.hk, row);
+      load_kv_tile<D, RAB>(p, it, j, pg, tk, tc, 0, sbase + C::OFF_K + s * C::TILE_BYTES, full);
       ++k_it;
     }
   }
@@ -327,8 +395,10 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       const uint32_t full = ptx::smem_u32(&bars->r_full[rs]);
       ptx::mbar_arrive_expect_tx(full, C::RAB_BYTES);
       const uint32_t dst = sbase + C::OFF_R + rs * C::RAB_BYTES;
-      ptx::tma_load_3d(dst, tr, full, j * kTileN, it.m0, plane);
-      ptx::tma_load_3d(dst + C::RAB_BYTES / 2, tr, full, j * kTileN + 64, it.m0, plane);
+      // rows: the key positions of the item's queries; columns: the visit's key tile
+      const int n0 = key_tile(j, it.split, it.hist).x * kTileN;
+      ptx::tma_load_3d(dst, tr, full, n0, it.off + it.m0, plane);
+      ptx::tma_load_3d(dst + C::RAB_BYTES / 2, tr, full, n0 + 64, it.off + it.m0, plane);
       ++r_it;
     }
   }
@@ -336,7 +406,7 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 
 template <int D, bool RAB>
 __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tv,
-                           long long total) {
+                           const CUtensorMap* tc, long long total) {
   using C = Cfg<D, RAB>;
   uint32_t v_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -345,14 +415,13 @@ __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const 
     if (!get_item(bars, k, it, p) || it.n_kv < 0) return;
     for (int j = 0; j < it.n_kv; ++j) {
       const int s = v_it % C::NV;
+      TilePages pg = {};
+      const KeyTile kt = key_tile(j, it.split, it.hist);
+      if (kt.cached) pg = tile_pages(p, it, kt.x);
       if (!wait_bar(bars, &bars->v_empty[s], ((v_it / C::NV) & 1) ^ 1, p)) return;
       const uint32_t full = ptx::smem_u32(&bars->v_full[s]);
       ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
-      const uint32_t dst = sbase + C::OFF_V + s * C::TILE_BYTES;
-#pragma unroll
-      for (int cb = 0; cb < C::NCB; ++cb)
-        ptx::tma_load_3d(dst + cb * C::CB_BYTES, tv, full, cb * C::EPC, it.hk,
-                         (int)(it.t0 + j * kTileN));
+      load_kv_tile<D, RAB>(p, it, j, pg, tv, tc, 1, sbase + C::OFF_V + s * C::TILE_BYTES, full);
       ++v_it;
     }
   }
@@ -615,7 +684,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   // last accumulation completes. The item stays in its ring slot until this returns.
   auto drain = [&](int slot) -> bool {
     const Item& pit = bars->info[slot];
-    const int pi = pit.m0 + r;
+    const int pi = pit.m0 + r;  // query row within the sequence
     if (!warp_wait(bars, &bars->o_full, u & 1, p)) return false;
     ptx::tc_fence_after();
     uint8_t* stage = smem + C::OFF_O + warp * C::WARP_STAGE;
@@ -623,7 +692,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       if (lane == 0) ptx::bulk_wait_read0();  // this warp's previous store has read it
       __syncwarp();
     }
-    T16* orow = out + ((pit.t0 + pi) * p.Nq + pit.h) * (long long)D + wg * OC;
+    T16* orow = out + (((long long)pit.tq + pi) * p.Nq + pit.h) * (long long)D + wg * OC;
 #pragma unroll
     for (int c0 = 0; c0 < OC; c0 += OCH) {
       uint32_t part[OCH];
@@ -640,7 +709,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           // chunks, conflict-free for one row per lane
           *reinterpret_cast<uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + c0 * 2 + v4 * 16)) =
               make_uint4(w[0], w[1], w[2], w[3]);
-        } else if (pi < pit.L) {
+        } else if (pi < pit.Lq) {
           reinterpret_cast<uint4*>(orow + c0)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
@@ -652,14 +721,14 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       // one TMA store when all 32 rows of the block lie inside the sequence; a block that
       // crosses the end of the sequence is stored row by row
       const int row0 = pit.m0 + quarter * 32;
-      if (row0 + 32 <= pit.L) {
+      if (row0 + 32 <= pit.Lq) {
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::tma_store_3d(tm_o, ptx::smem_u32(stage), wg * OC, pit.h, (int)(pit.t0 + row0));
+          ptx::tma_store_3d(tm_o, ptx::smem_u32(stage), wg * OC, pit.h, pit.tq + row0);
           ptx::bulk_commit();
         }
-      } else if (pi < pit.L) {
+      } else if (pi < pit.Lq) {
 #pragma unroll
         for (int v4 = 0; v4 < OC / 8; ++v4)
           reinterpret_cast<uint4*>(orow)[v4] =
@@ -677,7 +746,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     if (!warp_wait(bars, &bars->info_full[slot], (k / kInfoDepth) & 1, p)) return;
     const Item it = bars->info[slot];
     if (it.n_kv < 0) break;  // end marker
-    const int i = it.m0 + r;
+    const int i = it.off + it.m0 + r;  // key position of this thread's query row
     const RowRange rr = row_range(it.geom, i, p.mask_type);
     int gtile = 0;  // tiles of this item processed by this group
     for (int j = 0; j < it.n_kv; ++j, ++t) {
@@ -685,8 +754,10 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       const uint32_t sb = t % C::NSB;                 // == group
       if (!warp_wait(bars, &bars->s_full[sb], (t / C::NSB) & 1, p)) return;
       ptx::tc_fence_after();
-      const int n0 = j * kTileN;
-      const bool full = tile_all_valid(it.geom, it.m0, kTileM, n0, kTileN, p.mask_type);
+      const KeyTile kt = key_tile(j, it.split, it.hist);
+      const int n0 = kt.x * kTileN;
+      const bool full = kt.clo == 0 && kt.chi == kTileN &&
+                        tile_all_valid(it.geom, it.off + it.m0, kTileM, n0, kTileN, p.mask_type);
       const uint8_t* rab_row = nullptr;
       int rs = 0;
       if constexpr (RAB) {
@@ -710,7 +781,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           // form (one fused multiply-add per pair); a masked pair half becomes 0. When the
           // stream carries a custom mask instead, P is multiplied by it after the SiLU.
           const uint8_t* box = rab_row + (cc >> 6) * (C::RAB_BYTES / 2);
-          const uint32_t m = full ? 0xffffffffu : chunk_mask(rr, n0 + cc);
+          const uint32_t m = full ? 0xffffffffu : chunk_mask(rr, n0 + cc) & cols_mask(kt, cc);
           const uint32_t half2 = BF16 ? 0x3f003f00u : 0x38003800u;  // (0.5, 0.5)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -743,7 +814,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           if (!full) {
             // valid columns of this row form [0, hist_end) U [grp_lo, grp_hi]: as a bit
             // mask over the 32 columns of the chunk
-            const uint32_t m = chunk_mask(rr, n0 + cc);
+            const uint32_t m = chunk_mask(rr, n0 + cc) & cols_mask(kt, cc);
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               if (!(m & (1u << e))) x[e] = 0.f;
@@ -793,7 +864,8 @@ template <int D, bool BF16, bool RAB, bool MASK = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
-                  const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_o,
+                  const __grid_constant__ CUtensorMap tm_c, const FwdParams p) {
   using C = Cfg<D, RAB>;
   static_assert(C::NQ <= (int)(sizeof(Bars::q_full) / sizeof(uint64_t)) &&
                     C::NK <= (int)(sizeof(Bars::k_full) / sizeof(uint64_t)) &&
@@ -842,6 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tm_v);
     if (RAB) ptx::prefetch_tmap(&tm_r);
     if (C::STAGE) ptx::prefetch_tmap(&tm_o);
+    if (p.page_offsets) ptx::prefetch_tmap(&tm_c);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
@@ -862,11 +935,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kEpiWarps) {
     epilogue<D, BF16, RAB, MASK>(p, bars, smem, tmem, &tm_o, total, warp, lane);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_k<D, RAB>(p, bars, smem, &tm_k, total);
+    if (lane == 0) producer_k<D, RAB>(p, bars, smem, &tm_k, &tm_c, total);
   } else if (warp == kQProducerWarp) {
     if (lane == 0) producer_q<D, RAB>(p, bars, smem, &tm_q, total);
   } else if (warp == kVProducerWarp) {
-    if (lane == 0) producer_v<D, RAB>(p, bars, smem, &tm_v, total);
+    if (lane == 0) producer_v<D, RAB>(p, bars, smem, &tm_v, &tm_c, total);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       if constexpr (C::SERIAL)

@@ -26,7 +26,7 @@ cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, BF16, RAB, MASK>, m.q, m.k, m.v, m.rab, m.out,
-                            p);
+                            m.cache, p);
 }
 
 // Custom-mask variants (fwd_tc_mask.cu): prepare (shared-memory opt-in) or launch.

@@ -31,6 +31,19 @@ struct FwdParams {
                             // multiplied by it after the SiLU instead of rab being added
                             // before (mask_type is then NONE for the tile geometry)
   float alpha, silu_scale;
+  // Key side. The keys of sequence b are its cached history (page_offsets != nullptr)
+  // followed by its new k/v rows: rows [seq_offsets_k[b], seq_offsets_k[b + 1]) of k and v,
+  // or, with seq_offsets_k == nullptr, the rows of its queries. The Lq queries are the last
+  // Lq of the Lk key positions. S bounds Lk (and is the row length of rab), Sq bounds Lq.
+  const void* seq_offsets_k;  // [B+1] or nullptr
+  const void* page_offsets;   // [B+1] or nullptr (no cache)
+  const void* page_ids;       // [page_offsets[B]]
+  const void* last_page_len;  // [B]
+  const void* kv_cache;       // [num_pages, 2, page_size, Nk, D]
+  long long total_tokens_k;   // rows of k and v
+  long long num_pages;
+  int page_size;
+  int Sq;
 };
 
 __host__ __device__ inline long long load_index(const void* p, long long i, int is64) {
@@ -40,6 +53,38 @@ __host__ __device__ inline long long load_index(const void* p, long long i, int 
 // First token of sequence b: from seq_offsets (jagged layout) or b * S (normal layout).
 __host__ __device__ inline long long seq_start(const FwdParams& p, long long b) {
   return p.dense ? b * p.S : load_index(p.seq_offsets, b, p.index64);
+}
+
+// Query and key geometry of sequence b (after the work-list builder has validated it).
+struct SeqKV {
+  long long tq;    // first query row
+  long long tk;    // first new k/v row
+  long long po;    // first page_ids entry of the sequence
+  long long Lq;    // query rows
+  long long hist;  // cached keys: positions [0, hist)
+  long long Lk;    // keys: hist + new rows; query row i sits at position Lk - Lq + i
+};
+
+__host__ __device__ inline SeqKV seq_kv(const FwdParams& p, long long b) {
+  SeqKV s;
+  s.tq = seq_start(p, b);
+  s.Lq = seq_start(p, b + 1) - s.tq;
+  long long nk = s.Lq;
+  s.tk = s.tq;
+  if (p.seq_offsets_k) {
+    s.tk = load_index(p.seq_offsets_k, b, p.index64);
+    nk = load_index(p.seq_offsets_k, b + 1, p.index64) - s.tk;
+  }
+  s.po = 0;
+  s.hist = 0;
+  if (p.page_offsets) {
+    s.po = load_index(p.page_offsets, b, p.index64);
+    const long long pages = load_index(p.page_offsets, b + 1, p.index64) - s.po;
+    if (pages > 0)
+      s.hist = (pages - 1) * p.page_size + load_index(p.last_page_len, b, p.index64);
+  }
+  s.Lk = s.hist + nk;
+  return s;
 }
 
 // rab plane of (sequence b, query head h): [B, Nq, S, S], or [B, 1, S, S] broadcast.
@@ -59,7 +104,7 @@ cudaError_t launch_fwd_simt(const FwdParams& p, int grid, cudaStream_t stream, b
 
 // bf16 / fp16 tensor-core path (tcgen05, TMA, TMEM).
 struct TcMaps {
-  CUtensorMap q, k, v, rab, out;
+  CUtensorMap q, k, v, rab, out, cache;
 };
 bool tc_supported_dim(int D);
 int tc_swizzle_bytes(int D);  // row width of one TMA box / UMMA swizzle atom

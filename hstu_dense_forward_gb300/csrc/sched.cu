@@ -16,8 +16,9 @@
 // previous call has finished.
 //
 // The builder also checks the caller's seq_offsets ("increasing from 0; the user
-// must ensure validity", Inputs and Outputs table) and, if they are unusable,
-// records HSTU_DEVERR_OFFSETS and publishes an empty list so that no kernel
+// must ensure validity", Inputs and Outputs table), and the key side (seq_offsets_k,
+// the page table of the KV cache, at most as many queries as keys) and, if they are
+// unusable, records HSTU_DEVERR_OFFSETS and publishes an empty list so that no kernel
 // reads or writes outside the tensors.
 #include "../../include/hstu_fwd.h"
 #include "common.cuh"
@@ -47,7 +48,35 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
     long long a = seq_start(p, b);
     long long e = seq_start(p, b + 1);
-    if (a < 0 || e < a || e > T || e - a > p.S) bad = 1;
+    if (a < 0 || e < a || e > T || e - a > p.Sq) bad = 1;
+    if (p.seq_offsets_k) {
+      a = load_index(p.seq_offsets_k, b, p.index64);
+      e = load_index(p.seq_offsets_k, b + 1, p.index64);
+      if (a < 0 || e < a || e > p.total_tokens_k) bad = 1;
+    }
+    if (p.page_offsets) {
+      a = load_index(p.page_offsets, b, p.index64);
+      e = load_index(p.page_offsets, b + 1, p.index64);
+      if (a < 0 || e < a || e > 0x7fffffffll) {
+        bad = 1;
+      } else if (e > a) {
+        const long long last = load_index(p.last_page_len, b, p.index64);
+        if (last < 1 || last > p.page_size || e - a > (long long)p.S) bad = 1;
+        for (long long x = a; x < e; ++x) {
+          const long long id = load_index(p.page_ids, x, p.index64);
+          if (id < 0 || id >= p.num_pages) bad = 1;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const bool offsets_ok = !bad;
+  __syncthreads();  // every thread has read the flag before it can be set again
+  if (offsets_ok) {  // lengths, with every offset known to be in range
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+      const SeqKV s = seq_kv(p, b);
+      if (s.Lk > p.S || s.Lq > s.Lk) bad = 1;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) *p.next_item = 0;  // the forward kernel claims items from 0
@@ -60,19 +89,21 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
     return;
   }
 
-  const int tile_n = kTileN;
-  // pass 1: histogram of key-tile counts
+  // key visits of a (sequence, m-tile): key tiles up to the last key its rows may see, plus
+  // one when the cached history ends inside a visited tile that also holds new rows
+  auto visits = [&](const SeqKV& kv, const SeqGeom& s, int mt) {
+    const int off = (int)(kv.Lk - kv.Lq);  // position of query row 0
+    const int kv_end = kv_end_for_rows(s, off + mt * tile_m, tile_m, p.mask_type);
+    return key_visits(kv_end, split_tile((int)kv.hist, (int)kv.Lk));
+  };
+  // pass 1: histogram of key-visit counts
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const long long t0 = seq_start(p, b);
-    const int L = (int)(seq_start(p, b + 1) - t0);
+    const SeqKV kv = seq_kv(p, b);
     const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
     const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
-    const SeqGeom s = make_geom(L, nc, nt, p.g, p.mask_type);
-    const int mtiles = ceil_div(L, tile_m);
-    for (int mt = 0; mt < mtiles; ++mt) {
-      const int nkv = ceil_div(kv_end_for_rows(s, mt * tile_m, tile_m, p.mask_type), tile_n);
-      atomicAdd(&hist[nkv], 1);
-    }
+    const SeqGeom s = make_geom((int)kv.Lk, nc, nt, p.g, p.mask_type);
+    const int mtiles = ceil_div((int)kv.Lq, tile_m);
+    for (int mt = 0; mt < mtiles; ++mt) atomicAdd(&hist[visits(kv, s, mt)], 1);
   }
   __syncthreads();
   // exclusive scan, largest key-tile count first
@@ -87,15 +118,13 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
   __syncthreads();
   // pass 2: scatter
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const long long t0 = seq_start(p, b);
-    const int L = (int)(seq_start(p, b + 1) - t0);
+    const SeqKV kv = seq_kv(p, b);
     const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
     const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
-    const SeqGeom s = make_geom(L, nc, nt, p.g, p.mask_type);
-    const int mtiles = ceil_div(L, tile_m);
+    const SeqGeom s = make_geom((int)kv.Lk, nc, nt, p.g, p.mask_type);
+    const int mtiles = ceil_div((int)kv.Lq, tile_m);
     for (int mt = 0; mt < mtiles; ++mt) {
-      const int nkv = ceil_div(kv_end_for_rows(s, mt * tile_m, tile_m, p.mask_type), tile_n);
-      const int pos = atomicAdd(&cursor[nkv], 1);
+      const int pos = atomicAdd(&cursor[visits(kv, s, mt)], 1);
       work[pos] = pack_item(b, mt);
     }
   }
@@ -107,7 +136,7 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
 
 cudaError_t launch_build_worklist(const FwdParams& p, uint32_t* work, int* work_count,
                                   int tile_m, cudaStream_t stream, bool pdl) {
-  const int nbins = ceil_div(p.S, kTileN) + 1;
+  const int nbins = ceil_div(p.S, kTileN) + 2;  // visits: key tiles + one split tile
   const size_t smem = sizeof(int) * 2 * (size_t)nbins;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(build_worklist_kernel,

@@ -148,3 +148,126 @@ def generate(w: Workload) -> dict:
 def to_device(inputs: dict, device) -> dict:
     """Copy the tensor entries of generate()'s result to a device."""
     return {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
+
+
+# --------------------------------------------------------------------------- key side
+@dataclass(frozen=True)
+class KVWorkload:
+    """Queries that are the newest tokens of longer sequences whose history sits in a paged
+    KV cache (Inputs and Outputs table: seq_offsets_q / seq_offsets_k, kv_cache,
+    page_offsets, page_ids, last_page_len; feature table, "Page")."""
+    name: str
+    dtype: str
+    batch: int
+    num_heads_q: int
+    num_heads_kv: int
+    head_dim: int
+    hist_range: tuple             # cached history rows ~ U[lo, hi]
+    new_range: tuple              # new k/v rows ~ U[lo, hi]
+    page_size: int = 128          # 0: no cache (the history rows are passed as new rows)
+    query_range: Optional[tuple] = None  # None: the queries are the new rows; else
+                                         # Lq ~ U[lo, hi], clipped to the keys
+    spare_pages: int = 8          # cache pages no sequence uses
+    causal: bool = True
+    context_range: Optional[tuple] = None
+    targets_are_queries: bool = False    # num_targets = Lq (the new tokens are the targets)
+    target_group_size: int = 0
+    sigma: float = 1.0
+    rab: bool = False
+    rab_sigma: float = 0.1
+    seed: int = 0
+    alpha: Optional[float] = None        # default 1/sqrt(head_dim)
+    index_dtype: torch.dtype = torch.int64
+
+    @property
+    def max_seqlen(self) -> int:    # bound on query rows
+        hi = self.query_range[1] if self.query_range else self.new_range[1]
+        return max(8, -(-hi // 8) * 8)
+
+    @property
+    def max_seqlen_k(self) -> int:  # bound on keys (a multiple of 8: the rab row stride)
+        return -(-(self.hist_range[1] + self.new_range[1]) // 8) * 8
+
+    @property
+    def alpha_value(self) -> float:
+        return self.alpha if self.alpha is not None else 1.0 / math.sqrt(self.head_dim)
+
+    @property
+    def silu_scale_value(self) -> float:
+        return 1.0 / self.max_seqlen_k
+
+
+KV_WORKLOADS = {
+    # ranking with a cached user history: the new tokens are the candidates (targets of
+    # group size 1: each sees the history and itself)
+    "bf16_paged_b128_hist1k_4k_h4_d128": KVWorkload(
+        name="bf16_paged_b128_hist1k_4k_h4_d128", dtype="bf16", batch=128, num_heads_q=4,
+        num_heads_kv=4, head_dim=128, hist_range=(1024, 4096), new_range=(32, 256),
+        page_size=128, targets_are_queries=True, target_group_size=1, sigma=0.5, seed=5),
+}
+
+
+def generate_kv(w: KVWorkload) -> dict:
+    """CPU tensors of one key-side workload: q [Tq, Nq, D], k / v [Tk, Nk, D] (new rows),
+    seq_offsets (queries), seq_offsets_k, kv_cache [num_pages, 2, page_size, Nk, D] with
+    page_offsets, page_ids (a random permutation of the pages), last_page_len, plus
+    num_context / num_targets / rab and the scalars. Every cache row, used or not, holds
+    finite values. With page_size 0 the history rows are prepended to the new rows instead
+    (the same keys passed contiguously)."""
+    g = torch.Generator().manual_seed(w.seed)
+    B = w.batch
+    hist = torch.randint(w.hist_range[0], w.hist_range[1] + 1, (B,), generator=g)
+    lnew = torch.randint(w.new_range[0], w.new_range[1] + 1, (B,), generator=g)
+    lk = hist + lnew
+    if w.query_range is None:
+        lq = lnew.clone()
+    else:
+        lq = torch.minimum(torch.randint(w.query_range[0], w.query_range[1] + 1, (B,),
+                                         generator=g), lk)
+    num_context = None
+    if w.context_range is not None:
+        num_context = torch.randint(w.context_range[0], w.context_range[1] + 1, (B,),
+                                    generator=g)
+    num_targets = lq.clone() if w.targets_are_queries else None
+    dt = DTYPES[w.dtype]
+
+    def draw(*shape):
+        return (torch.randn(*shape, generator=g, dtype=torch.float32) * w.sigma).to(dt)
+
+    def offsets(lengths):
+        o = torch.zeros(B + 1, dtype=torch.int64)
+        o[1:] = torch.cumsum(lengths, 0)
+        return o
+
+    Nq, Nk, D = w.num_heads_q, w.num_heads_kv, w.head_dim
+    q = draw(int(lq.sum()), Nq, D)
+    out = dict(q=q, seq_offsets=offsets(lq), num_context=num_context, num_targets=num_targets,
+               causal=w.causal, target_group_size=w.target_group_size, alpha=w.alpha_value,
+               silu_scale=w.silu_scale_value, max_seqlen=w.max_seqlen,
+               max_seqlen_k=w.max_seqlen_k)
+    if w.page_size:
+        ps = w.page_size
+        npages = (hist + ps - 1) // ps
+        num_pages = int(npages.sum()) + w.spare_pages
+        cache = draw(num_pages, 2, ps, Nk, D)
+        ids = torch.randperm(num_pages, generator=g)[:int(npages.sum())]
+        last = torch.where(npages > 0, hist - (npages - 1) * ps, torch.ones_like(hist))
+        out.update(k=draw(int(lnew.sum()), Nk, D), v=draw(int(lnew.sum()), Nk, D),
+                   seq_offsets_k=offsets(lnew), kv_cache=cache, page_offsets=offsets(npages),
+                   page_ids=ids, last_page_len=last)
+    else:
+        out.update(k=draw(int(lk.sum()), Nk, D), v=draw(int(lk.sum()), Nk, D),
+                   seq_offsets_k=offsets(lk), kv_cache=None, page_offsets=None, page_ids=None,
+                   last_page_len=None)
+    rab = None
+    if w.rab:
+        S = w.max_seqlen_k
+        rab = (torch.randn(B, Nq, S, S, generator=g, dtype=torch.float32) * w.rab_sigma).to(dt)
+    out["rab"] = rab
+    idx = w.index_dtype
+    for key in ("seq_offsets", "seq_offsets_k", "page_offsets", "page_ids", "last_page_len",
+                "num_context", "num_targets"):
+        if out.get(key) is not None:
+            out[key] = out[key].to(idx)
+    out["history"] = hist  # cached rows per sequence (for checks; not an operator input)
+    return out

@@ -11,7 +11,10 @@
  *     optional relative attention bias rab [b, n, s, s]; no mask or a causal mask
  *     built from num_context, num_targets and target_group_size.
  *   - Inputs and Outputs table: argument layouts, mask_type codes, the silu_scale
- *     default 1/max_seq_len, alpha, and "empty input: the operator does not run".
+ *     default 1/max_seq_len, alpha, and "empty input: the operator does not run";
+ *     seq_offsets_q / seq_offsets_k / max_seq_len_k / is_delta_qk (query and key
+ *     lengths may differ) and kv_cache / page_offsets / page_ids / last_page_len (the
+ *     paged KV cache of the feature table's "Page" row): see hstu_fwd_run_kv.
  *
  * For every sequence b (L = seq_offsets[b+1] - seq_offsets[b], t0 = seq_offsets[b]),
  * query head h (kv head hk = h / (Nq / Nk)), row i < L and column d < D:
@@ -108,8 +111,39 @@ typedef struct {
   int rab_heads;         /* bias planes per sequence: 0 or Nq for rab [B, Nq, S, S]; 1 for
                             rab [B, 1, S, S], one plane added for every query head (feature
                             table, "Support for rab broadcasting") */
+  int is_delta_qk;       /* 1: the new k/v rows have offsets of their own (seq_offsets_k of
+                            hstu_fwd_kv); jagged layout only */
+  int max_seqlen_k;      /* Sk, bound on the keys of a sequence (history + new rows) and the
+                            S of rab / mask when is_delta_qk or page_size is set (0 = use
+                            max_seqlen); must be 0 otherwise. max_seqlen then bounds the
+                            query rows of a sequence */
+  int page_size;         /* 0, or the rows of one KV-cache page: 32, 128 or 256 (Inputs and
+                            Outputs table, kv_cache); jagged layout only */
   int reserved;          /* must be 0 */
 } hstu_fwd_desc;
+
+/*
+ * Key side of hstu_fwd_run_kv (Inputs and Outputs table: seq_offsets_k, kv_cache,
+ * page_offsets, page_ids, last_page_len). Index arrays are int32 or int64 per
+ * desc.index_is_int64; all pointers are DEVICE pointers.
+ */
+typedef struct {
+  const void* seq_offsets_k;  /* [B+1] new k/v rows of each sequence (desc.is_delta_qk = 1),
+                                 increasing, seq_offsets_k[B] <= total_tokens_k; NULL when
+                                 is_delta_qk = 0: the new k/v rows are the query rows */
+  long long total_tokens_k;   /* rows of k and v (is_delta_qk = 1; ignored otherwise, when k
+                                 and v have total_tokens rows). With 0, k and v may be NULL */
+  const void* kv_cache;       /* [num_pages, 2, page_size, Nk, D] of the plan's dtype, 16-byte
+                                 aligned: plane 0 of a page holds K rows, plane 1 V rows.
+                                 NULL iff desc.page_size = 0. Rows past a sequence's last
+                                 valid row must hold finite values (they are multiplied by 0) */
+  long long num_pages;
+  const void* page_offsets;   /* [B+1] the pages of sequence b are page_ids[page_offsets[b]
+                                 .. page_offsets[b+1]), in order */
+  const void* page_ids;       /* [page_offsets[B]] values in [0, num_pages) */
+  const void* last_page_len;  /* [B] rows of the last page, in [1, page_size] (unused for a
+                                 sequence without pages) */
+} hstu_fwd_kv;
 
 typedef struct hstu_fwd_plan hstu_fwd_plan; /* opaque */
 
@@ -151,6 +185,28 @@ HSTU_API hstu_status hstu_fwd_run_masked(hstu_fwd_plan* plan, const void* q, con
                                          const void* mask, long long total_tokens, float alpha,
                                          float silu_scale, void* out, void* stream);
 
+/*
+ * Enqueue one forward whose queries and keys may differ (plans with is_delta_qk or
+ * page_size set; any plan accepts kv = NULL, which is hstu_fwd_run / hstu_fwd_run_masked).
+ * For sequence b: Lq = seq_offsets[b+1] - seq_offsets[b] query rows (q and out rows
+ * from seq_offsets[b]); the keys are the cached history, hist = (pages - 1) * page_size +
+ * last_page_len[b] rows from the pages (0 without pages or cache), followed by the new
+ * k/v rows; Lk = hist + new rows, Lq <= Lk <= Sk, Lq <= max_seqlen. Query row i sits at
+ * key position p = Lk - Lq + i (the queries are the last Lq tokens): the mask is
+ * valid(p, j) over L = Lk and the rab / custom-mask row is p. rab_or_mask is rab
+ * [B, Nq or 1, Sk, Sk] for plans with has_rab, the mask [B, Nq, Sk, Sk] for CUSTOM plans,
+ * else NULL. Other arguments as for hstu_fwd_run. Invalid offsets or page tables (a
+ * page id outside the cache, last_page_len outside [1, page_size], Lq > Lk, a length
+ * above its bound) are reported through the error word (HSTU_DEVERR_OFFSETS) and leave
+ * out unwritten.
+ */
+HSTU_API hstu_status hstu_fwd_run_kv(hstu_fwd_plan* plan, const void* q, const void* k,
+                                     const void* v, const void* seq_offsets,
+                                     const hstu_fwd_kv* kv, const void* rab_or_mask,
+                                     const void* num_context, const void* num_targets,
+                                     long long total_tokens, float alpha, float silu_scale,
+                                     void* out, void* stream);
+
 /* Free the workspace. NULL is accepted. Synchronises the device first. */
 HSTU_API hstu_status hstu_fwd_destroy(hstu_fwd_plan* plan);
 
@@ -171,6 +227,18 @@ HSTU_API hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* desc, const void*
                                  const void* num_context_host, const void* num_targets_host,
                                  long long* pairs);
 
+/* hstu_fwd_count_pairs for hstu_fwd_run_kv calls, from HOST arrays: seq_offsets [B+1]
+ * (queries), seq_offsets_k [B+1] or NULL (new k/v rows = query rows), page_offsets [B+1]
+ * and last_page_len [B] or NULL (no cache); pairs = sum over sequences of
+ * Nq * #{(i, j): i < Lq, j < Lk, valid(Lk - Lq + i, j)}. */
+HSTU_API hstu_status hstu_fwd_count_pairs_kv(const hstu_fwd_desc* desc,
+                                             const void* seq_offsets_host,
+                                             const void* seq_offsets_k_host,
+                                             const void* page_offsets_host,
+                                             const void* last_page_len_host,
+                                             const void* num_context_host,
+                                             const void* num_targets_host, long long* pairs);
+
 /*
  * Same forward as hstu_fwd_run, without a plan and without allocating anything.
  * The source pages have no counterpart to this entry point: it exists for callers
@@ -183,7 +251,8 @@ HSTU_API hstu_status hstu_fwd_count_pairs(const hstu_fwd_desc* desc, const void*
  *     for batch * ceil(max_seqlen / 128) <= 16384 entries; larger descriptors return
  *     HSTU_ERR_UNSUPPORTED without launching anything.
  *   - Arguments, layouts and ownership are those of hstu_fwd_run; desc is validated
- *     like hstu_fwd_create validates it, on every call.
+ *     like hstu_fwd_create validates it, on every call. Descriptors with is_delta_qk or
+ *     page_size set, or mask_type CUSTOM, return HSTU_ERR_UNSUPPORTED.
  *   - The first call on a device (with that device current) looks up the array's
  *     device address and configures the kernels for that device; make that first
  *     call before any stream capture.

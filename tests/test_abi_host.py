@@ -51,6 +51,13 @@ def _desc(**kw):
     (dict(layout=2), _abi.HSTU_ERR_INVALID_ARG),
     (dict(has_rab=1, rab_heads=2), _abi.HSTU_ERR_INVALID_ARG),          # neither 1 nor Nq
     (dict(reserved=1), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(is_delta_qk=2), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(page_size=64), _abi.HSTU_ERR_INVALID_ARG),                    # not in {32, 128, 256}
+    (dict(max_seqlen_k=512), _abi.HSTU_ERR_INVALID_ARG),                # without a key side
+    (dict(is_delta_qk=1, max_seqlen_k=-1), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(is_delta_qk=1, layout=1), _abi.HSTU_ERR_UNSUPPORTED),         # jagged only
+    (dict(page_size=128, layout=1), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(is_delta_qk=1, max_seqlen_k=1001, has_rab=1), _abi.HSTU_ERR_UNSUPPORTED),  # Sk % 8
 ])
 def test_create_rejects_bad_descriptors(built_lib, kw, status):
     lib = _abi.lib()
@@ -140,3 +147,60 @@ def test_count_pairs_custom_mask_counts_every_pair(built_lib):
     assert lib.hstu_fwd_count_pairs(ctypes.byref(d), so, None, None,
                                     ctypes.byref(out)) == _abi.HSTU_OK
     assert out.value == 4 * (100 ** 2 + 150 ** 2)
+
+
+def _kv_case(rng, B, page_size):
+    """Random query lengths, new k/v rows and a page table (histories of 0 to 5 pages)."""
+    lnew = rng.integers(0, 300, B)
+    lq = np.minimum(rng.integers(0, 300, B), lnew)
+    pages = rng.integers(0, 6, B)
+    last = rng.integers(1, page_size + 1, B)
+    hist = np.where(pages > 0, (pages - 1) * page_size + last, 0)
+    lq = np.minimum(lq + rng.integers(0, 50, B), hist + lnew)  # queries may reach into history
+    so_q = np.concatenate([[0], np.cumsum(lq)])
+    so_k = np.concatenate([[0], np.cumsum(lnew)])
+    po = np.concatenate([[0], np.cumsum(pages)])
+    return lq, lnew, hist, so_q, so_k, po, last
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_count_pairs_kv_matches_oracle(built_lib, seed):
+    """Pairs of calls whose queries are the last tokens of longer key sequences (own k/v
+    offsets and a paged history), against the oracle's brute-force count."""
+    from hstu_dense_forward_gb300 import count_pairs_kv
+    rng = np.random.default_rng(seed)
+    B, ps = 5, [32, 128, 256, 32][seed]
+    lq, lnew, hist, so_q, so_k, po, last = _kv_case(rng, B, ps)
+    lk = hist + lnew
+    nc = rng.integers(0, 40, B)
+    nt = rng.integers(0, 60, B)
+    for causal, g in ((True, 0), (True, 2), (False, 0)):
+        kw = dict(num_context=nc, num_targets=nt, target_group_size=g) if causal else {}
+        got = count_pairs_kv(so_q, 3, max_seqlen=512, seq_offsets_k=so_k, page_offsets=po,
+                             last_page_len=last, page_size=ps, max_seqlen_k=int(lk.max()) + 1,
+                             causal=causal, **kw)
+        ref = oracle.count_valid_kv(lq, lk, 3, mask_type=oracle.MASK_CAUSAL if causal
+                                    else oracle.MASK_NONE, **kw)
+        assert got == ref
+
+
+def test_count_pairs_kv_without_key_side_matches_count_pairs(built_lib):
+    from hstu_dense_forward_gb300 import count_pairs_kv
+    so = [0, 100, 350, 351]
+    kw = dict(num_context=[3, 0, 1], num_targets=[10, 20, 0], target_group_size=3)
+    assert count_pairs_kv(so, 2, max_seqlen=256, **kw) == count_pairs(so, 2, max_seqlen=256, **kw)
+
+
+def test_key_side_entry_points_validate_before_the_device(built_lib):
+    """hstu_fwd_run_kv without a plan, and the allocation-free entry point with a key-side
+    descriptor, fail before any CUDA call (the key-side plan checks run in the GPU tests)."""
+    lib = _abi.lib()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the calls fail validation first
+    kv = _abi.KV()
+    assert lib.hstu_fwd_run_kv(None, fake, fake, fake, fake, ctypes.byref(kv), None, None, None,
+                               10, 1.0, 1.0, fake, None) == _abi.HSTU_ERR_INVALID_ARG
+    for kw in (dict(is_delta_qk=1), dict(page_size=128), dict(is_delta_qk=1, page_size=32)):
+        d = _desc(**kw)
+        assert lib.hstu_fwd_run_noalloc(ctypes.byref(d), fake, fake, fake, fake, None, None,
+                                        None, 10, 1.0, 1.0, fake, None) == \
+            _abi.HSTU_ERR_UNSUPPORTED
