@@ -158,7 +158,49 @@ class ClockSampler:
 
 def _workload(name):
     from hstu_dense_forward_gb300 import workloads as W
-    return W.WORKLOADS[name]
+    return W.WORKLOADS[name] if name in W.WORKLOADS else W.KV_WORKLOADS[name]
+
+
+def _is_kv(w):
+    from hstu_dense_forward_gb300 import workloads as W
+    return isinstance(w, W.KVWorkload)
+
+
+KV_KEYS = ("seq_offsets_k", "kv_cache", "page_offsets", "page_ids", "last_page_len")
+
+
+def _generate(w):
+    from hstu_dense_forward_gb300 import workloads as W
+    return W.generate_kv(w) if _is_kv(w) else W.generate(w)
+
+
+def _pairs(w, inp):
+    from hstu_dense_forward_gb300 import count_pairs, count_pairs_kv
+    if _is_kv(w):
+        return count_pairs_kv(inp["seq_offsets"], w.num_heads_q, max_seqlen=w.max_seqlen,
+                              seq_offsets_k=inp["seq_offsets_k"],
+                              page_offsets=inp["page_offsets"],
+                              last_page_len=inp["last_page_len"], page_size=w.page_size,
+                              max_seqlen_k=w.max_seqlen_k, num_context=inp["num_context"],
+                              num_targets=inp["num_targets"], causal=w.causal,
+                              target_group_size=w.target_group_size)
+    return count_pairs(inp["seq_offsets"], w.num_heads_q, max_seqlen=w.max_seqlen,
+                       num_context=inp["num_context"], num_targets=inp["num_targets"],
+                       causal=w.causal, target_group_size=w.target_group_size)
+
+
+def _kv_sample(inp, nb):
+    """The first nb sequences of a key-side workload as oracle arguments, with a cache
+    holding only their pages (renumbered in order)."""
+    so, so_k = inp["seq_offsets"].to(torch.int64), inp["seq_offsets_k"].to(torch.int64)
+    args = dict(seq_offsets_k=so_k[:nb + 1])
+    if inp["kv_cache"] is not None:
+        po = inp["page_offsets"].to(torch.int64)
+        used = inp["page_ids"][:int(po[nb])].to(torch.int64)
+        args.update(kv_cache=inp["kv_cache"][used], page_offsets=po[:nb + 1],
+                    page_ids=torch.arange(used.numel()), last_page_len=inp["last_page_len"][:nb])
+    return (inp["q"][:int(so[nb])], inp["k"][:int(so_k[nb])], inp["v"][:int(so_k[nb])],
+            so[:nb + 1], args)
 
 
 def _algorithmic_bytes(w, inp, pairs_per_head):
@@ -189,13 +231,13 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     w = _workload(args.workload)
-    inp = W.generate(w)
-    pairs = count_pairs(inp["seq_offsets"], w.num_heads_q, max_seqlen=w.max_seqlen,
-                        num_context=inp["num_context"], num_targets=inp["num_targets"],
-                        causal=w.causal, target_group_size=w.target_group_size)
+    kv_side = _is_kv(w)
+    inp = _generate(w)
+    pairs = _pairs(w, inp)
     flops = useful_flops(pairs, w.head_dim)
     set_bytes = sum(t.numel() * t.element_size() for t in
-                    (inp["q"], inp["k"], inp["v"], inp["rab"]) if t is not None) * 2  # + out
+                    (inp["q"], inp["k"], inp["v"], inp["rab"], inp.get("kv_cache"))
+                    if t is not None) + inp["q"].numel() * inp["q"].element_size()  # + out
     nsets = max(3, -(-3 * L2_BYTES // max(set_bytes, 1)))
     nsets = min(nsets, 8)
     sets = []
@@ -206,10 +248,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step(d):
+        kv = {k: d[k] for k in KV_KEYS} if kv_side else {}
+        if kv_side:
+            kv["max_seqlen_k"] = d["max_seqlen_k"]
         hstu_fwd(d["q"], d["k"], d["v"], d["seq_offsets"], max_seqlen=d["max_seqlen"],
                  rab=d["rab"], num_context=d["num_context"], num_targets=d["num_targets"],
                  causal=d["causal"], target_group_size=d["target_group_size"], alpha=d["alpha"],
-                 silu_scale=d["silu_scale"], out=d["out"])
+                 silu_scale=d["silu_scale"], out=d["out"], **kv)
 
     for i in range(args.warmup):
         step(sets[i % nsets])
@@ -235,7 +280,7 @@ def run_ours(args):
     # copy of step i+1 and the D2H copy of step i-1 overlap the forward of step i.
     host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     in_keys = [k for k in ("q", "k", "v", "seq_offsets", "num_context", "num_targets", "rab")
-               if host[k] is not None]
+               + (KV_KEYS if kv_side else ()) if host[k] is not None]
     bufs = []
     for _ in range(2):
         dq = W.to_device(inp, dev)
@@ -291,7 +336,7 @@ def run_ours(args):
                 "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 4),
                 "traffic": traffic, "peak_source": peaks["source"],
                 "timed": "CUDA events around each call: work-list build + forward kernel"}
-    if w.rab:
+    if w.rab and not kv_side:
         gbs = _algorithmic_bytes(w, inp, pairs // w.num_heads_q * w.num_heads_q) / (
             ms_per_step * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
@@ -313,6 +358,10 @@ def run_ours(args):
                        "heads_q": w.num_heads_q, "heads_kv": w.num_heads_kv,
                        "head_dim": w.head_dim, "mask": "causal" if w.causal else "none",
                        "rab": w.rab, "tokens": int(inp["seq_offsets"][-1]),
+                       **({"keys": int((inp["seq_offsets_k"][1:] - inp["seq_offsets_k"][:-1]).sum()
+                                       + inp["history"].sum()),
+                           "cached_keys": int(inp["history"].sum()), "page_size": w.page_size,
+                           "max_seqlen_k": w.max_seqlen_k} if kv_side else {}),
                        "valid_pairs": pairs, "useful_gflop_per_step": round(flops / 1e9, 3),
                        "l2": f"rotating {nsets} input sets of {set_bytes / 2**20:.0f} MiB (> L2)",
                        "parallelism": f"replicas x{ws}"},
@@ -346,14 +395,28 @@ def cpu_baseline(w, inp, seconds):
                     num_targets=None if inp["num_targets"] is None else inp["num_targets"][:nb],
                     mask_type=oracle.MASK_CAUSAL if w.causal else oracle.MASK_NONE,
                     target_group_size=w.target_group_size, alpha=w.alpha_value,
-                    silu_scale=w.silu_scale_value, max_seqlen=w.max_seqlen)
+                    silu_scale=w.silu_scale_value,
+                    max_seqlen=w.max_seqlen_k if _is_kv(w) else w.max_seqlen)
         q, k, v = inp["q"][:T], inp["k"][:T], inp["v"][:T]
+        kv = {}
+        if _is_kv(w):
+            q, k, v, sub, kv = _kv_sample(inp, nb)
         t0 = time.perf_counter()
-        oracle.hstu_fwd(q, k, v, sub, nthreads=nthreads, **args)
+        oracle.hstu_fwd(q, k, v, sub, nthreads=nthreads, **args, **kv)
         dt = time.perf_counter() - t0
-        pairs = oracle.count_valid(sub, w.num_heads_q, num_context=args["num_context"],
-                                   num_targets=args["num_targets"], mask_type=args["mask_type"],
-                                   target_group_size=w.target_group_size)
+        if _is_kv(w):
+            hist = inp["history"][:nb]
+            lk = (kv["seq_offsets_k"][1:] - kv["seq_offsets_k"][:-1]) + hist
+            pairs = oracle.count_valid_kv(sub[1:] - sub[:-1], lk, w.num_heads_q,
+                                          num_context=args["num_context"],
+                                          num_targets=args["num_targets"],
+                                          mask_type=args["mask_type"],
+                                          target_group_size=w.target_group_size)
+        else:
+            pairs = oracle.count_valid(sub, w.num_heads_q, num_context=args["num_context"],
+                                       num_targets=args["num_targets"],
+                                       mask_type=args["mask_type"],
+                                       target_group_size=w.target_group_size)
         best = (nb, dt, pairs)
         if dt >= seconds / 4 or nb >= w.batch:
             break
@@ -375,7 +438,7 @@ def run_reference(args):
         return
     oracle.build()
     w = _workload(args.workload)
-    inp = W.generate(w)
+    inp = _generate(w)
     nthreads = os.cpu_count() or 1
     so = inp["seq_offsets"].to(torch.int64)
     nb = 1  # one sequence, all heads, whole rows: a bounded sample per step
@@ -386,11 +449,21 @@ def run_reference(args):
               num_targets=None if inp["num_targets"] is None else inp["num_targets"][:nb],
               mask_type=oracle.MASK_CAUSAL if w.causal else oracle.MASK_NONE,
               target_group_size=w.target_group_size, alpha=w.alpha_value,
-              silu_scale=w.silu_scale_value, max_seqlen=w.max_seqlen)
+              silu_scale=w.silu_scale_value,
+              max_seqlen=w.max_seqlen_k if _is_kv(w) else w.max_seqlen)
     q, k, v = inp["q"][:T], inp["k"][:T], inp["v"][:T]
-    pairs = oracle.count_valid(sub, w.num_heads_q, num_context=kw["num_context"],
-                               num_targets=kw["num_targets"], mask_type=kw["mask_type"],
-                               target_group_size=w.target_group_size)
+    if _is_kv(w):
+        q, k, v, sub, kv = _kv_sample(inp, nb)
+        kw.update(kv)
+        lk = (kv["seq_offsets_k"][1:] - kv["seq_offsets_k"][:-1]) + inp["history"][:nb]
+        pairs = oracle.count_valid_kv(sub[1:] - sub[:-1], lk, w.num_heads_q,
+                                      num_context=kw["num_context"],
+                                      num_targets=kw["num_targets"], mask_type=kw["mask_type"],
+                                      target_group_size=w.target_group_size)
+    else:
+        pairs = oracle.count_valid(sub, w.num_heads_q, num_context=kw["num_context"],
+                                   num_targets=kw["num_targets"], mask_type=kw["mask_type"],
+                                   target_group_size=w.target_group_size)
     for _ in range(args.warmup):
         oracle.hstu_fwd(q, k, v, sub, nthreads=nthreads, **kw)
     t0 = time.perf_counter()

@@ -160,7 +160,8 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
       }
       // kernel variant: 0 no rab, 1 rab, 2 custom mask (streamed like rab)
       e = hstu::tc_prepare(desc->head_dim, desc->dtype == HSTU_BF16,
-                           desc->mask_type == HSTU_MASK_CUSTOM ? 2 : (desc->has_rab ? 1 : 0));
+                           desc->mask_type == HSTU_MASK_CUSTOM ? 2 : (desc->has_rab ? 1 : 0),
+                           key_side(*desc) ? 1 : 0);
       P->grid = P->num_sms;
     } else {
       e = hstu::simt_prepare();
@@ -562,7 +563,7 @@ cudaError_t noalloc_setup(int dev, const hstu_fwd_desc& d, uint32_t** scratch, i
   if (!(g_noalloc_prepared[dev] & (1u << bit))) {
     cudaError_t e = d.dtype == HSTU_F32
                         ? hstu::simt_prepare()
-                        : hstu::tc_prepare(d.head_dim, d.dtype == HSTU_BF16, d.has_rab);
+                        : hstu::tc_prepare(d.head_dim, d.dtype == HSTU_BF16, d.has_rab, 0);
     if (e != cudaSuccess) return e;
     g_noalloc_prepared[dev] |= 1u << bit;
   }

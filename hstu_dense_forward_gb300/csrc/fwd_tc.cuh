@@ -141,12 +141,27 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 1024, "barrier block");
 
+// KV: the kernel variant for key sides that differ from the queries (own k/v offsets, a
+// KV cache); without it the keys are the query rows and the decomposition folds away.
+template <bool KV>
 __device__ __forceinline__ bool decode_item(const FwdParams& p, long long idx, Item& it) {
   const uint32_t e = p.work[idx / p.Nq];
   it.h = (int)(idx % p.Nq);
   it.hk = it.h / (p.Nq / p.Nk);
   it.b = item_b(e);
   it.m0 = item_mt(e) * kTileM;
+  if constexpr (!KV) {
+    const long long t0 = seq_start(p, it.b);
+    it.tq = it.tk = (int)t0;
+    it.Lq = (int)(seq_start(p, it.b + 1) - t0);
+    it.hist = it.po = it.off = 0;
+    it.split = -1;
+    const long long nc = p.num_context ? load_index(p.num_context, it.b, p.index64) : 0;
+    const long long nt = p.num_targets ? load_index(p.num_targets, it.b, p.index64) : 0;
+    it.geom = make_geom(it.Lq, nc, nt, p.g, p.mask_type);
+    it.n_kv = ceil_div(kv_end_for_rows(it.geom, it.m0, kTileM, p.mask_type), kTileN);
+    return true;
+  }
   const SeqKV kv = seq_kv(p, it.b);
   it.tq = (int)kv.tq;
   it.Lq = (int)kv.Lq;
@@ -255,7 +270,7 @@ __device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
 // load waits behind the release of another ring's slot. With two Q buffers the Q
 // producer runs up to two work items ahead; with one, it prefetches the next
 // item's Q tile into L2 so that the load after the slot frees hits in L2.
-template <int D, bool RAB>
+template <int D, bool RAB, bool KV>
 __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tq,
                            long long total) {
   using C = Cfg<D, RAB>;
@@ -273,14 +288,14 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       put_item(bars, k, it, p);
       return;
     }
-    decode_item(p, idx, it);
+    decode_item<KV>(p, idx, it);
     if (!put_item(bars, k, it, p)) return;
     long long nidx = -1;
     if (C::NQ == 1) {
       nidx = claim();
       if (nidx < total) {
         Item nx;
-        decode_item(p, nidx, nx);
+        decode_item<KV>(p, nidx, nx);
 #pragma unroll
         for (int cb = 0; cb < C::NCB; ++cb)
           ptx::tma_prefetch_3d(tq, cb * C::EPC, nx.h, nx.tq + nx.m0);
@@ -353,7 +368,7 @@ __device__ __forceinline__ void load_kv_tile(const FwdParams& p, const Item& it,
   }
 }
 
-template <int D, bool RAB>
+template <int D, bool RAB, bool KV>
 __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tk,
                            const CUtensorMap* tc, long long total) {
   using C = Cfg<D, RAB>;
@@ -366,12 +381,22 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       const int s = k_it % C::NK;
       // page ids are read before the wait for the slot, which hides their latency
       TilePages pg = {};
-      const KeyTile kt = key_tile(j, it.split, it.hist);
-      if (kt.cached) pg = tile_pages(p, it, kt.x);
+      if constexpr (KV) {
+        const KeyTile kt = key_tile(j, it.split, it.hist);
+        if (kt.cached) pg = tile_pages(p, it, kt.x);
+      }
       if (!wait_bar(bars, &bars->k_empty[s], ((k_it / C::NK) & 1) ^ 1, p)) return;
       const uint32_t full = ptx::smem_u32(&bars->k_full[s]);
       ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
-      load_kv_tile<D, RAB>(p, it, j, pg, tk, tc, 0, sbase + C::OFF_K + s * C::TILE_BYTES, full);
+      const uint32_t dst = sbase + C::OFF_K + s * C::TILE_BYTES;
+      if constexpr (KV) {
+        load_kv_tile<D, RAB>(p, it, j, pg, tk, tc, 0, dst, full);
+      } else {
+#pragma unroll
+        for (int cb = 0; cb < C::NCB; ++cb)
+          ptx::tma_load_3d(dst + cb * C::CB_BYTES, tk, full, cb * C::EPC, it.hk,
+                           it.tq + j * kTileN);
+      }
       ++k_it;
     }
   }
@@ -379,7 +404,7 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 
 // rab tiles of every S tile, in tile order, on their own thread: the rab ring is released
 // by the epilogue (late in a tile), and waiting for it must not hold back the K loads.
-template <int D, bool RAB>
+template <int D, bool RAB, bool KV>
 __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tr,
                            long long total) {
   using C = Cfg<D, RAB>;
@@ -396,15 +421,16 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       ptx::mbar_arrive_expect_tx(full, C::RAB_BYTES);
       const uint32_t dst = sbase + C::OFF_R + rs * C::RAB_BYTES;
       // rows: the key positions of the item's queries; columns: the visit's key tile
-      const int n0 = key_tile(j, it.split, it.hist).x * kTileN;
-      ptx::tma_load_3d(dst, tr, full, n0, it.off + it.m0, plane);
-      ptx::tma_load_3d(dst + C::RAB_BYTES / 2, tr, full, n0 + 64, it.off + it.m0, plane);
+      const int n0 = (KV ? key_tile(j, it.split, it.hist).x : j) * kTileN;
+      const int row = (KV ? it.off : 0) + it.m0;
+      ptx::tma_load_3d(dst, tr, full, n0, row, plane);
+      ptx::tma_load_3d(dst + C::RAB_BYTES / 2, tr, full, n0 + 64, row, plane);
       ++r_it;
     }
   }
 }
 
-template <int D, bool RAB>
+template <int D, bool RAB, bool KV>
 __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tv,
                            const CUtensorMap* tc, long long total) {
   using C = Cfg<D, RAB>;
@@ -416,12 +442,22 @@ __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const 
     for (int j = 0; j < it.n_kv; ++j) {
       const int s = v_it % C::NV;
       TilePages pg = {};
-      const KeyTile kt = key_tile(j, it.split, it.hist);
-      if (kt.cached) pg = tile_pages(p, it, kt.x);
+      if constexpr (KV) {
+        const KeyTile kt = key_tile(j, it.split, it.hist);
+        if (kt.cached) pg = tile_pages(p, it, kt.x);
+      }
       if (!wait_bar(bars, &bars->v_empty[s], ((v_it / C::NV) & 1) ^ 1, p)) return;
       const uint32_t full = ptx::smem_u32(&bars->v_full[s]);
       ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
-      load_kv_tile<D, RAB>(p, it, j, pg, tv, tc, 1, sbase + C::OFF_V + s * C::TILE_BYTES, full);
+      const uint32_t dst = sbase + C::OFF_V + s * C::TILE_BYTES;
+      if constexpr (KV) {
+        load_kv_tile<D, RAB>(p, it, j, pg, tv, tc, 1, dst, full);
+      } else {
+#pragma unroll
+        for (int cb = 0; cb < C::NCB; ++cb)
+          ptx::tma_load_3d(dst + cb * C::CB_BYTES, tv, full, cb * C::EPC, it.hk,
+                           it.tq + j * kTileN);
+      }
       ++v_it;
     }
   }
@@ -660,7 +696,7 @@ __device__ __forceinline__ bool epi_barrier(Bars* bars, uint32_t& phase, const F
   return ok;
 }
 
-template <int D, bool BF16, bool RAB, bool MASK>
+template <int D, bool BF16, bool RAB, bool MASK, bool KV>
 __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                          const CUtensorMap* tm_o, long long total, int warp, int lane) {
   using C = Cfg<D, RAB>;
@@ -746,7 +782,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     if (!warp_wait(bars, &bars->info_full[slot], (k / kInfoDepth) & 1, p)) return;
     const Item it = bars->info[slot];
     if (it.n_kv < 0) break;  // end marker
-    const int i = it.off + it.m0 + r;  // key position of this thread's query row
+    const int m0p = (KV ? it.off : 0) + it.m0;  // key position of the item's first query row
+    const int i = m0p + r;                      // and of this thread's row
     const RowRange rr = row_range(it.geom, i, p.mask_type);
     int gtile = 0;  // tiles of this item processed by this group
     for (int j = 0; j < it.n_kv; ++j, ++t) {
@@ -754,10 +791,18 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       const uint32_t sb = t % C::NSB;                 // == group
       if (!warp_wait(bars, &bars->s_full[sb], (t / C::NSB) & 1, p)) return;
       ptx::tc_fence_after();
-      const KeyTile kt = key_tile(j, it.split, it.hist);
+      KeyTile kt;
+      if constexpr (KV) {
+        kt = key_tile(j, it.split, it.hist);
+      } else {
+        kt.x = j;
+        kt.clo = 0;
+        kt.chi = kTileN;
+        kt.cached = false;
+      }
       const int n0 = kt.x * kTileN;
-      const bool full = kt.clo == 0 && kt.chi == kTileN &&
-                        tile_all_valid(it.geom, it.off + it.m0, kTileM, n0, kTileN, p.mask_type);
+      const bool full = (!KV || (kt.clo == 0 && kt.chi == kTileN)) &&
+                        tile_all_valid(it.geom, m0p, kTileM, n0, kTileN, p.mask_type);
       const uint8_t* rab_row = nullptr;
       int rs = 0;
       if constexpr (RAB) {
@@ -781,7 +826,11 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           // form (one fused multiply-add per pair); a masked pair half becomes 0. When the
           // stream carries a custom mask instead, P is multiplied by it after the SiLU.
           const uint8_t* box = rab_row + (cc >> 6) * (C::RAB_BYTES / 2);
-          const uint32_t m = full ? 0xffffffffu : chunk_mask(rr, n0 + cc) & cols_mask(kt, cc);
+          uint32_t m = 0xffffffffu;
+          if (!full) {
+            m = chunk_mask(rr, n0 + cc);
+            if constexpr (KV) m &= cols_mask(kt, cc);
+          }
           const uint32_t half2 = BF16 ? 0x3f003f00u : 0x38003800u;  // (0.5, 0.5)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -814,7 +863,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           if (!full) {
             // valid columns of this row form [0, hist_end) U [grp_lo, grp_hi]: as a bit
             // mask over the 32 columns of the chunk
-            const uint32_t m = chunk_mask(rr, n0 + cc) & cols_mask(kt, cc);
+            uint32_t m = chunk_mask(rr, n0 + cc);
+            if constexpr (KV) m &= cols_mask(kt, cc);
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               if (!(m & (1u << e))) x[e] = 0.f;
@@ -860,7 +910,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 
 // ------------------------------------------------------------------ kernel
 // MASK: the rab stream carries a custom mask (multiplied into P after the SiLU).
-template <int D, bool BF16, bool RAB, bool MASK = false>
+template <int D, bool BF16, bool RAB, bool MASK = false, bool KV = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
@@ -914,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tm_v);
     if (RAB) ptx::prefetch_tmap(&tm_r);
     if (C::STAGE) ptx::prefetch_tmap(&tm_o);
-    if (p.page_offsets) ptx::prefetch_tmap(&tm_c);
+    if (KV && p.page_offsets) ptx::prefetch_tmap(&tm_c);
   }
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
@@ -933,13 +983,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long total = (long long)(*p.work_count) * p.Nq;
 
   if (warp < kEpiWarps) {
-    epilogue<D, BF16, RAB, MASK>(p, bars, smem, tmem, &tm_o, total, warp, lane);
+    epilogue<D, BF16, RAB, MASK, KV>(p, bars, smem, tmem, &tm_o, total, warp, lane);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_k<D, RAB>(p, bars, smem, &tm_k, &tm_c, total);
+    if (lane == 0) producer_k<D, RAB, KV>(p, bars, smem, &tm_k, &tm_c, total);
   } else if (warp == kQProducerWarp) {
-    if (lane == 0) producer_q<D, RAB>(p, bars, smem, &tm_q, total);
+    if (lane == 0) producer_q<D, RAB, KV>(p, bars, smem, &tm_q, total);
   } else if (warp == kVProducerWarp) {
-    if (lane == 0) producer_v<D, RAB>(p, bars, smem, &tm_v, &tm_c, total);
+    if (lane == 0) producer_v<D, RAB, KV>(p, bars, smem, &tm_v, &tm_c, total);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       if constexpr (C::SERIAL)
@@ -948,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_s_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
     }
   } else if (warp == kRabWarp) {
-    if (RAB && lane == 0) producer_r<D, RAB>(p, bars, smem, &tm_r, total);
+    if (RAB && lane == 0) producer_r<D, RAB, KV>(p, bars, smem, &tm_r, total);
   } else if (warp == kPvWarp) {
     if (lane == 0 && !C::SERIAL) mma_pv_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
   }

@@ -1,18 +1,19 @@
 // Launch helpers of the tensor-core forward kernel, shared by the translation units that
-// instantiate its variants (fwd_tc.cu: no rab / rab; fwd_tc_mask.cu: custom mask).
+// instantiate its variants (fwd_tc.cu: no rab / rab; fwd_tc_mask.cu: custom mask;
+// fwd_tc_kv.cu and fwd_tc_kv_mask.cu: the same with a key side of its own).
 #pragma once
 #include "fwd_tc.cuh"
 
 namespace hstu {
 namespace tc {
 
-template <int D, bool BF16, bool RAB, bool MASK>
+template <int D, bool BF16, bool RAB, bool MASK, bool KV>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(fwd_tc_kernel<D, BF16, RAB, MASK>,
+  return cudaFuncSetAttribute(fwd_tc_kernel<D, BF16, RAB, MASK, KV>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, RAB>::SMEM_BYTES);
 }
 
-template <int D, bool BF16, bool RAB, bool MASK>
+template <int D, bool BF16, bool RAB, bool MASK, bool KV>
 cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t stream,
                        bool pdl) {
   cudaLaunchConfig_t cfg = {};
@@ -25,13 +26,39 @@ cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, BF16, RAB, MASK>, m.q, m.k, m.v, m.rab, m.out,
+  return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, BF16, RAB, MASK, KV>, m.q, m.k, m.v, m.rab, m.out,
                             m.cache, p);
+}
+
+// Prepare (shared-memory opt-in) or launch one variant, chosen by head dim and type.
+template <bool BF16, bool RAB, bool MASK, bool KV>
+cudaError_t dispatch_dim(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
+                         bool pdl, bool prepare) {
+  switch (p.D) {
+    case 32: return prepare ? prepare_one<32, BF16, RAB, MASK, KV>() : launch_one<32, BF16, RAB, MASK, KV>(p, m, grid, st, pdl);
+    case 64: return prepare ? prepare_one<64, BF16, RAB, MASK, KV>() : launch_one<64, BF16, RAB, MASK, KV>(p, m, grid, st, pdl);
+    case 128: return prepare ? prepare_one<128, BF16, RAB, MASK, KV>() : launch_one<128, BF16, RAB, MASK, KV>(p, m, grid, st, pdl);
+    case 256: return prepare ? prepare_one<256, BF16, RAB, MASK, KV>() : launch_one<256, BF16, RAB, MASK, KV>(p, m, grid, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <bool RAB, bool MASK, bool KV>
+cudaError_t dispatch_type(const FwdParams& p, const TcMaps& m, int bf16, int grid,
+                          cudaStream_t st, bool pdl, bool prepare) {
+  return bf16 ? dispatch_dim<true, RAB, MASK, KV>(p, m, grid, st, pdl, prepare)
+              : dispatch_dim<false, RAB, MASK, KV>(p, m, grid, st, pdl, prepare);
 }
 
 // Custom-mask variants (fwd_tc_mask.cu): prepare (shared-memory opt-in) or launch.
 cudaError_t dispatch_mask(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                           cudaStream_t st, bool pdl, bool prepare);
+
+// Key-side variants (fwd_tc_kv.cu, fwd_tc_kv_mask.cu): own k/v offsets and / or a KV cache.
+cudaError_t dispatch_kv(const FwdParams& p, const TcMaps& m, int bf16, int grid,
+                        cudaStream_t st, bool pdl, bool prepare);
+cudaError_t dispatch_kv_mask(const FwdParams& p, const TcMaps& m, int bf16, int grid,
+                             cudaStream_t st, bool pdl, bool prepare);
 
 }  // namespace tc
 }  // namespace hstu

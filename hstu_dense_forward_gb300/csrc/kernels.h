@@ -109,7 +109,8 @@ struct TcMaps {
 bool tc_supported_dim(int D);
 int tc_swizzle_bytes(int D);  // row width of one TMA box / UMMA swizzle atom
 int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
-cudaError_t tc_prepare(int D, int bf16, int rab);  // rab: 0 none, 1 rab, 2 custom mask
+// rab: 0 none, 1 rab, 2 custom mask; kv: the key-side variant (own k/v offsets, KV cache)
+cudaError_t tc_prepare(int D, int bf16, int rab, int kv);
 cudaError_t launch_fwd_tc(const FwdParams& p, const TcMaps& maps, int bf16, int grid,
                           cudaStream_t stream, bool pdl);
 

@@ -70,15 +70,17 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
     }
   }
   __syncthreads();
-  const bool offsets_ok = !bad;
-  __syncthreads();  // every thread has read the flag before it can be set again
-  if (offsets_ok) {  // lengths, with every offset known to be in range
-    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-      const SeqKV s = seq_kv(p, b);
-      if (s.Lk > p.S || s.Lq > s.Lk) bad = 1;
+  if (p.seq_offsets_k || p.page_offsets) {  // key side: lengths, once every offset is in range
+    const bool offsets_ok = !bad;
+    __syncthreads();  // every thread has read the flag before it can be set again
+    if (offsets_ok) {
+      for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+        const SeqKV s = seq_kv(p, b);
+        if (s.Lk > p.S || s.Lq > s.Lk) bad = 1;
+      }
     }
+    __syncthreads();
   }
-  __syncthreads();
   if (threadIdx.x == 0) *p.next_item = 0;  // the forward kernel claims items from 0
   if (bad) {
     if (threadIdx.x == 0) {
