@@ -26,7 +26,12 @@ __all__ = ["hstu_fwd", "hstu_fwd_noalloc", "HstuFwdPlan", "HstuError", "count_pa
            "count_pairs_kv", "useful_flops"]
 
 _DTYPES = {torch.float32: _abi.HSTU_F32, torch.float16: _abi.HSTU_F16,
-           torch.bfloat16: _abi.HSTU_BF16}
+           torch.bfloat16: _abi.HSTU_BF16, torch.float8_e4m3fn: _abi.HSTU_FP8_E4M3}
+
+
+def out_dtype(dtype: torch.dtype) -> torch.dtype:
+    """Element type of out: the input type, bf16 for FP8 E4M3 inputs."""
+    return torch.bfloat16 if dtype == torch.float8_e4m3fn else dtype
 
 
 def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, index_is_int64,
@@ -177,7 +182,7 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
              num_targets=None, causal=True, target_group_size=0, alpha=1.0, silu_scale=None,
              out=None, watchdog_ms=0, layout="jagged", mask=None, seq_offsets_k=None,
              max_seqlen_k=None, kv_cache=None, page_offsets=None, page_ids=None,
-             last_page_len=None):
+             last_page_len=None, q_descale=1.0, k_descale=1.0, v_descale=1.0):
     """HSTU forward.
 
     layout "jagged" (default): q [T, Nq, D], k/v [T, Nk, D], seq_offsets [B+1] int32/int64,
@@ -198,6 +203,11 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     sequence are the last Lq of its Lk keys; max_seqlen bounds Lq, max_seqlen_k (default
     max_seqlen) bounds Lk and is the S of rab and mask; silu_scale then defaults to
     1/max_seqlen_k.
+
+    FP8 (feature table, "FP8 quantization types: cast"): q, k, v (and kv_cache) of dtype
+    torch.float8_e4m3fn, out bf16; q_descale, k_descale, v_descale are per-tensor factors
+    (the values are q_descale * q etc.), folded into alpha and silu_scale. Head dims 32,
+    64, 128; no rab or custom mask.
     """
     dev = q.device
     if dev.type != "cuda":
@@ -221,9 +231,9 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
         idx_dtype = idx[0].dtype if idx else torch.int64
         res = out
         if res is None:
-            res = torch.empty_like(q)
+            res = torch.empty(q.shape, dtype=out_dtype(q.dtype), device=dev)
         else:
-            _check_tensor(res, "out", q.dtype, dev, 4)
+            _check_tensor(res, "out", out_dtype(q.dtype), dev, 4)
             if res.shape != q.shape:
                 raise ValueError("out must have q's shape")
         q3, k3, v3 = q.view(B * S, *q.shape[2:]), k.view(B * S, *k.shape[2:]), v.view(B * S, *v.shape[2:])
@@ -242,9 +252,9 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
                              "with seq_offsets_k)")
         B = seq_offsets.shape[0] - 1
         if out is None:
-            out = torch.empty_like(q)
+            out = torch.empty(q.shape, dtype=out_dtype(q.dtype), device=dev)
         else:
-            _check_tensor(out, "out", q.dtype, dev, 3)
+            _check_tensor(out, "out", out_dtype(q.dtype), dev, 3)
             if out.shape != q.shape:
                 raise ValueError("out must have q's shape")
         q3, k3, v3, out3, res = q, k, v, out, out
@@ -302,6 +312,13 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
                                is_delta_qk=seq_offsets_k is not None,
                                max_seqlen_k=Sk if key_side else 0, page_size=page_size)
         _plans[key] = plan
+    if q.dtype == torch.float8_e4m3fn:  # per-tensor descale factors: x = alpha*qd*kd*(q.k)
+        if silu_scale is None:
+            silu_scale = 1.0 / (Sk if key_side else int(max_seqlen))
+        alpha = float(alpha) * float(q_descale) * float(k_descale)
+        silu_scale = float(silu_scale) * float(v_descale)
+    elif (q_descale, k_descale, v_descale) != (1.0, 1.0, 1.0):
+        raise ValueError("descale factors go with FP8 E4M3 inputs")
     with torch.cuda.device(dev):
         plan.run(q3, k3, v3, seq_offsets, out3, rab=rab, num_context=num_context,
                  num_targets=num_targets, alpha=alpha, silu_scale=silu_scale, stream=stream,

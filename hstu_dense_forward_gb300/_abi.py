@@ -13,7 +13,7 @@ HEADER = os.path.join(os.path.dirname(PKG), "include", "hstu_fwd.h")
 
 HSTU_OK, HSTU_ERR_INVALID_ARG, HSTU_ERR_UNSUPPORTED, HSTU_ERR_CUDA, HSTU_ERR_TIMEOUT, \
     HSTU_ERR_DEVICE_CHECK = range(6)
-HSTU_F32, HSTU_F16, HSTU_BF16 = 0, 1, 2
+HSTU_F32, HSTU_F16, HSTU_BF16, HSTU_FP8_E4M3 = 0, 1, 2, 3
 HSTU_MASK_CAUSAL, HSTU_MASK_UPPER, HSTU_MASK_NONE, HSTU_MASK_CUSTOM = 0, 1, 2, 3
 HSTU_DEVERR_NONE, HSTU_DEVERR_OFFSETS, HSTU_DEVERR_TIMEOUT = 0, 1, 2
 HSTU_LAYOUT_JAGGED, HSTU_LAYOUT_NORMAL = 0, 1

@@ -107,7 +107,8 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
     return HSTU_ERR_INVALID_ARG;
   if (d->rab_heads != 0 && d->rab_heads != 1 && d->rab_heads != d->num_heads_q)
     return HSTU_ERR_INVALID_ARG;
-  if (d->dtype != HSTU_F32 && d->dtype != HSTU_F16 && d->dtype != HSTU_BF16)
+  if (d->dtype != HSTU_F32 && d->dtype != HSTU_F16 && d->dtype != HSTU_BF16 &&
+      d->dtype != HSTU_FP8_E4M3)
     return HSTU_ERR_INVALID_ARG;
   if (d->batch < 0 || d->batch > (1 << 20)) return HSTU_ERR_INVALID_ARG;
   if (d->num_heads_q < 0 || d->num_heads_kv < 1) return HSTU_ERR_INVALID_ARG;
@@ -127,7 +128,12 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
     if (d->has_rab) return HSTU_ERR_UNSUPPORTED;
     if (d->dtype != HSTU_F32 && key_bound(*d) % 8 != 0) return HSTU_ERR_UNSUPPORTED;
   }
-  if (d->dtype == HSTU_F32) {
+  if (d->dtype == HSTU_FP8_E4M3) {
+    // FP8 E4M3 inputs: head dims 32, 64, 128; no rab and no custom mask (their tiles are
+    // 16-bit and share no path with the 8-bit products here)
+    if (d->head_dim != 32 && d->head_dim != 64 && d->head_dim != 128) return HSTU_ERR_UNSUPPORTED;
+    if (d->has_rab || d->mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_UNSUPPORTED;
+  } else if (d->dtype == HSTU_F32) {
     if (d->head_dim > 256) return HSTU_ERR_UNSUPPORTED;
   } else {
     if (!hstu::tc_supported_dim(d->head_dim)) return HSTU_ERR_UNSUPPORTED;
@@ -159,7 +165,8 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
         return HSTU_ERR_UNSUPPORTED;
       }
       // kernel variant: 0 no rab, 1 rab, 2 custom mask (streamed like rab)
-      e = hstu::tc_prepare(desc->head_dim, desc->dtype == HSTU_BF16,
+      e = hstu::tc_prepare(desc->head_dim,
+                           desc->dtype == HSTU_FP8_E4M3 ? 2 : (desc->dtype == HSTU_BF16 ? 1 : 0),
                            desc->mask_type == HSTU_MASK_CUSTOM ? 2 : (desc->has_rab ? 1 : 0),
                            key_side(*desc) ? 1 : 0);
       P->grid = P->num_sms;
@@ -223,23 +230,29 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
       memcmp(ptrs, P->map_ptrs, sizeof(ptrs)) == 0)
     return HSTU_OK;
   const hstu_fwd_desc& d = P->desc;
-  const CUtensorMapDataType ty =
-      d.dtype == HSTU_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const int swb = hstu::tc_swizzle_bytes(d.head_dim);
+  const bool fp8 = d.dtype == HSTU_FP8_E4M3;
+  // q, k, v and the cache: E4M3 bytes (FP8 plans) or 16-bit; out is 16-bit (bf16 for FP8)
+  const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : d.dtype == HSTU_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapDataType oty = d.dtype == HSTU_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t eb = fp8 ? 1 : 2;
+  const int swb = hstu::tc_swizzle_bytes(d.head_dim, (int)eb);
   const CUtensorMapSwizzle swz = swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                  : swb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                              : CU_TENSOR_MAP_SWIZZLE_32B;
-  const uint32_t epc = (uint32_t)(swb / 2);
+  const uint32_t epc = (uint32_t)(swb / eb);
   const uint32_t oc = (uint32_t)hstu::tc_out_box_cols(d.head_dim);
   const uint64_t D = (uint64_t)d.head_dim, Nq = (uint64_t)d.num_heads_q,
                  Nk = (uint64_t)d.num_heads_kv;
-  bool ok = encode3d(&P->maps.q, ty, q, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, epc, 1,
+  bool ok = encode3d(&P->maps.q, ty, q, D, Nq, (uint64_t)T, D * eb, Nq * D * eb, epc, 1,
                      hstu::kTileM, swz) &&
-            encode3d(&P->maps.k, ty, k ? k : (cache ? cache : q), D, Nk, (uint64_t)(Tk > 0 ? Tk : 1), D * 2,
-                     Nk * D * 2, epc, 1, hstu::kTileN, swz) &&
-            encode3d(&P->maps.v, ty, v ? v : (cache ? cache : q), D, Nk, (uint64_t)(Tk > 0 ? Tk : 1), D * 2,
-                     Nk * D * 2, epc, 1, hstu::kTileN, swz) &&
-            encode3d(&P->maps.out, ty, out, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, oc, 1, 32,
+            encode3d(&P->maps.k, ty, k ? k : (cache ? cache : q), D, Nk, (uint64_t)(Tk > 0 ? Tk : 1),
+                     D * eb, Nk * D * eb, epc, 1, hstu::kTileN, swz) &&
+            encode3d(&P->maps.v, ty, v ? v : (cache ? cache : q), D, Nk, (uint64_t)(Tk > 0 ? Tk : 1),
+                     D * eb, Nk * D * eb, epc, 1, hstu::kTileN, swz) &&
+            encode3d(&P->maps.out, oty, out, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, oc, 1, 32,
                      oc * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                      : oc * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                      : oc * 2 == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
@@ -255,7 +268,7 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
   if (ok && cache) {
     const uint64_t ps = (uint64_t)d.page_size;
     const uint64_t dims[4] = {D, Nk, ps, 2 * (uint64_t)num_pages};
-    const uint64_t strides[3] = {D * 2, Nk * D * 2, ps * Nk * D * 2};
+    const uint64_t strides[3] = {D * eb, Nk * D * eb, ps * Nk * D * eb};
     const uint32_t box[4] = {epc, 1, (uint32_t)(ps < 128 ? ps : 128), 1};
     ok = encode4d(&P->maps.cache, ty, cache, dims, strides, box, swz);
   } else if (ok) {
@@ -364,6 +377,8 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   p.rab_is_mask = is_mask ? 1 : 0;
   p.alpha = alpha;
   p.silu_scale = silu_scale;
+  p.fp8 = d.dtype == HSTU_FP8_E4M3 ? 1 : 0;
+  if (p.fp8) p.silu_scale = silu_scale / hstu::kP8Scale;  // the kernel's P carries kP8Scale
 
   if (P->tensor_cores) {
     hstu_status ms = make_maps(P, q, k, v, rab, out, total_tokens, Tk, cache,
@@ -586,6 +601,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   if ((long long)d.batch * hstu::ceil_div(d.max_seqlen, hstu::kTileM) > HSTU_NOALLOC_MAX_ENTRIES)
     return HSTU_ERR_UNSUPPORTED;  // work list larger than the static scratch array
   if (d.mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_UNSUPPORTED;  // hstu_fwd_run_masked only
+  if (d.dtype == HSTU_FP8_E4M3) return HSTU_ERR_UNSUPPORTED;          // plans only
   if (key_side(d)) return HSTU_ERR_UNSUPPORTED;                       // hstu_fwd_run_kv only
   if (!q || !k || !v || !out || !layout_args_ok(d, seq_offsets, total_tokens))
     return HSTU_ERR_INVALID_ARG;
@@ -643,7 +659,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   if (tc) {
     const CUtensorMapDataType ty =
         d.dtype == HSTU_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const int swb = hstu::tc_swizzle_bytes(d.head_dim);
+    const int swb = hstu::tc_swizzle_bytes(d.head_dim, 2);
     const CUtensorMapSwizzle swz = swb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                    : swb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                : CU_TENSOR_MAP_SWIZZLE_32B;

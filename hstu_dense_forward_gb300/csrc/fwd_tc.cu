@@ -1,6 +1,7 @@
 // Instantiations and launch of the tensor-core forward kernel: the plain variants here;
-// the custom-mask variants (fwd_tc_mask.cu) and the key-side variants (fwd_tc_kv.cu,
-// fwd_tc_kv_mask.cu) are instantiated in translation units of their own.
+// the custom-mask variants (fwd_tc_mask.cu), the key-side variants (fwd_tc_kv.cu,
+// fwd_tc_kv_mask.cu) and the FP8 variants (fwd_tc_f8.cu) are instantiated in translation
+// units of their own.
 #include "fwd_tc_launch.cuh"
 
 namespace hstu {
@@ -12,6 +13,7 @@ bool key_side(const FwdParams& p) { return p.seq_offsets_k != nullptr || p.page_
 
 cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cudaStream_t st,
                      bool pdl, bool prepare) {
+  if (p.fp8) return tc::dispatch_f8(p, m, grid, st, pdl, prepare);
   if (key_side(p))
     return p.rab_is_mask ? tc::dispatch_kv_mask(p, m, bf16, grid, st, pdl, prepare)
                          : tc::dispatch_kv(p, m, bf16, grid, st, pdl, prepare);
@@ -24,13 +26,17 @@ cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cu
 
 bool tc_supported_dim(int D) { return D == 32 || D == 64 || D == 128 || D == 256; }
 
-int tc_swizzle_bytes(int D) { return D * 2 >= 128 ? 128 : D * 2; }
+int tc_swizzle_bytes(int D, int elem_bytes) {
+  return D * elem_bytes >= 128 ? 128 : D * elem_bytes;
+}
 
 int tc_out_box_cols(int D) { return D / tc::kEpiWG; }
 
-cudaError_t tc_prepare(int D, int bf16, int rab, int kv) {
+cudaError_t tc_prepare(int D, int elem, int rab, int kv) {
   FwdParams p = {};
   p.D = D;
+  p.fp8 = elem == 2 ? 1 : 0;
+  const int bf16 = elem == 1 ? 1 : 0;
   p.rab = rab ? reinterpret_cast<const void*>(1) : nullptr;
   p.rab_is_mask = rab == 2 ? 1 : 0;
   p.seq_offsets_k = kv ? reinterpret_cast<const void*>(1) : nullptr;  // selects the variant only

@@ -57,16 +57,26 @@ constexpr int kRabWarp = kEpiWarps + 5;        // rab loads
 constexpr int kThreads = (kEpiWarps + 6) * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
+// FP8 kernels round kP8Scale * P to E4M3 (the host divides silu_scale by kP8Scale):
+// 16 keeps P values down to 2^-10 in the normal range and saturates only above P = 28.
+constexpr uint32_t kP8ScaleF16x2 = 0x4C004C00u;  // (16.0, 16.0) as f16x2
 
-template <int D, bool RAB>
+// F8: q, k, v are FP8 E4M3 (one byte each); the products run as tcgen05 kind::f8f6f4 with
+// P rounded to E4M3; O is written as bf16.
+template <int D, bool RAB, bool F8 = false>
 struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head_dim");
-  static constexpr int SWB = (D * 2 >= 128) ? 128 : D * 2;  // bytes per swizzled row
+  static_assert(!F8 || (D <= 128 && !RAB), "fp8: head_dim <= 128, no rab");
+  static constexpr int EB = F8 ? 1 : 2;                     // bytes per q / k / v element
+  static constexpr int SWB = (D * EB >= 128) ? 128 : D * EB;  // bytes per swizzled row
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : (SWB == 64 ? 4u : 6u);
-  static constexpr int EPC = SWB / 2;          // elements per column block
+  static constexpr int EPC = SWB / EB;         // elements per column block
   static constexpr int NCB = D / EPC;          // column blocks per tile row
   static constexpr int CB_BYTES = 128 * SWB;   // one column block of a 128-row tile
-  static constexpr int TILE_BYTES = 128 * D * 2;
+  static constexpr int TILE_BYTES = 128 * D * EB;
+  static constexpr int O_TILE_BYTES = 128 * D * 2;  // O is 16-bit
+  static constexpr int KS = F8 ? 32 : 16;      // K elements of one MMA (32 bytes)
+  static constexpr int PW = F8 ? 32 : 64;      // TMEM columns of one P buffer (128 keys)
   static constexpr int RAB_BYTES = 128 * 128 * 2;
   static constexpr int NQ = (D <= 64) ? 2 : ((D == 128 && !RAB) ? 2 : 1);
   static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 2 : 4) : (D == 128 ? 2 : 1));
@@ -95,20 +105,20 @@ struct Cfg {
   static constexpr bool SERIAL = !P_SEP;
   // TMEM columns
   static constexpr uint32_t S_COL0 = 0, O_COL = NSB * 128;
-  static constexpr uint32_t P_COL0 = O_COL + D;  // P buffers (P_SEP only)
+  static constexpr uint32_t P_COL0 = O_COL + D;  // P buffers of PW columns (P_SEP only)
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
   static constexpr int OFF_R = OFF_V + NV * TILE_BYTES;
   static constexpr int OFF_O = OFF_R + NR * RAB_BYTES;
-  static constexpr int OFF_BAR = OFF_O + (STAGE ? TILE_BYTES : 0);
+  static constexpr int OFF_BAR = OFF_O + (STAGE ? O_TILE_BYTES : 0);
   static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES;
   // keep one CTA per SM (TMEM is allocated whole)
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 < 120 * 1024) ? 120 * 1024 : SMEM_USED + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(O_COL + D + (P_SEP ? 128 : 0) <= kTmemCols, "TMEM map");
+  static_assert(O_COL + D + (P_SEP ? 2 * PW : 0) <= kTmemCols, "TMEM map");
 };
 
 // One work item, decoded once (by the Q producer) and read by every role.
@@ -270,10 +280,10 @@ __device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
 // load waits behind the release of another ring's slot. With two Q buffers the Q
 // producer runs up to two work items ahead; with one, it prefetches the next
 // item's Q tile into L2 so that the load after the slot frees hits in L2.
-template <int D, bool RAB, bool KV>
+template <int D, bool RAB, bool KV, bool F8>
 __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tq,
                            long long total) {
-  using C = Cfg<D, RAB>;
+  using C = Cfg<D, RAB, F8>;
   uint32_t q_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   // Items are claimed dynamically from the heaviest-first list: CTA i starts with item i,
@@ -340,12 +350,12 @@ __device__ __forceinline__ TilePages tile_pages(const FwdParams& p, const Item& 
 // cache pages when the visit's rows are cached, else rows tk + 128x - hist .. of k / v
 // (rows before the sequence's first new row belong to the cached part of a split tile
 // and meet P = 0 there).
-template <int D, bool RAB>
+template <int D, bool RAB, bool F8>
 __device__ __forceinline__ void load_kv_tile(const FwdParams& p, const Item& it, int j,
                                              const TilePages& pg, const CUtensorMap* tnew,
                                              const CUtensorMap* tcache, int plane, uint32_t dst,
                                              uint32_t full) {
-  using C = Cfg<D, RAB>;
+  using C = Cfg<D, RAB, F8>;
   const KeyTile kt = key_tile(j, it.split, it.hist);
   if (!kt.cached) {
     const int row = it.tk + kt.x * kTileN - it.hist;
@@ -368,10 +378,10 @@ __device__ __forceinline__ void load_kv_tile(const FwdParams& p, const Item& it,
   }
 }
 
-template <int D, bool RAB, bool KV>
+template <int D, bool RAB, bool KV, bool F8>
 __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tk,
                            const CUtensorMap* tc, long long total) {
-  using C = Cfg<D, RAB>;
+  using C = Cfg<D, RAB, F8>;
   uint32_t k_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   for (int k = 0;; ++k) {
@@ -390,7 +400,7 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
       const uint32_t dst = sbase + C::OFF_K + s * C::TILE_BYTES;
       if constexpr (KV) {
-        load_kv_tile<D, RAB>(p, it, j, pg, tk, tc, 0, dst, full);
+        load_kv_tile<D, RAB, F8>(p, it, j, pg, tk, tc, 0, dst, full);
       } else {
 #pragma unroll
         for (int cb = 0; cb < C::NCB; ++cb)
@@ -404,10 +414,10 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 
 // rab tiles of every S tile, in tile order, on their own thread: the rab ring is released
 // by the epilogue (late in a tile), and waiting for it must not hold back the K loads.
-template <int D, bool RAB, bool KV>
+template <int D, bool RAB, bool KV, bool F8>
 __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tr,
                            long long total) {
-  using C = Cfg<D, RAB>;
+  using C = Cfg<D, RAB, F8>;
   uint32_t r_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   for (int k = 0;; ++k) {
@@ -430,10 +440,10 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   }
 }
 
-template <int D, bool RAB, bool KV>
+template <int D, bool RAB, bool KV, bool F8>
 __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tv,
                            const CUtensorMap* tc, long long total) {
-  using C = Cfg<D, RAB>;
+  using C = Cfg<D, RAB, F8>;
   uint32_t v_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   for (int k = 0;; ++k) {
@@ -451,7 +461,7 @@ __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
       const uint32_t dst = sbase + C::OFF_V + s * C::TILE_BYTES;
       if constexpr (KV) {
-        load_kv_tile<D, RAB>(p, it, j, pg, tv, tc, 1, dst, full);
+        load_kv_tile<D, RAB, F8>(p, it, j, pg, tv, tc, 1, dst, full);
       } else {
 #pragma unroll
         for (int cb = 0; cb < C::NCB; ++cb)
@@ -486,10 +496,10 @@ __device__ __forceinline__ void mma_drain(Bars* bars, const FwdParams& p) {
 // Single issuer, used when P is written over its S buffer (D = 256): there S(t+2)
 // can only start after PV(t) has read P(t), so the two products form one chain and
 // are issued in that order: S(t0), S(t0+1), then per tile PV(t), S(t+2).
-template <int D, bool BF16, bool RAB>
+template <int D, bool BF16, bool RAB, bool F8>
 __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                                   long long total) {
-  using C = Cfg<D, RAB>;
+  using C = Cfg<D, RAB, F8>;
   constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16 ? 1u : 0u, 128, kTileN, 0);
   constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16 ? 1u : 0u, 128, D, 1);
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -559,11 +569,12 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
   mma_drain(bars, p);
 }
 
-template <int D, bool BF16, bool RAB>
+template <int D, bool BF16, bool RAB, bool F8>
 __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                              long long total) {
-  using C = Cfg<D, RAB>;
-  constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16 ? 1u : 0u, 128, kTileN, 0);
+  using C = Cfg<D, RAB, F8>;
+  // kind::f16: A/B format 0 = f16, 1 = bf16; kind::f8f6f4: format 0 = E4M3
+  constexpr uint32_t IDESC_S = ptx::idesc_f16((BF16 && !F8) ? 1u : 0u, 128, kTileN, 0);
   const uint32_t sbase = ptx::smem_u32(smem);
   uint32_t q_it = 0, k_it = 0, t = 0;
   for (int k = 0;; ++k) {
@@ -591,11 +602,15 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
       ptx::tc_fence_after();
       const uint32_t ka = sbase + C::OFF_K + ks * C::TILE_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk * 16 / C::EPC) * C::CB_BYTES + ((kk * 16) % C::EPC) * 2;
+      for (int kk = 0; kk < D / C::KS; ++kk) {  // K steps of 32 bytes
+        const int e = kk * C::KS;
+        const uint32_t off = (e / C::EPC) * C::CB_BYTES + (e % C::EPC) * C::EB;
         const uint64_t ad = ptx::smem_desc(qa + off, 16, 8 * C::SWB, C::SWZ);
         const uint64_t bd = ptx::smem_desc(ka + off, 16, 8 * C::SWB, C::SWZ);
-        ptx::mma_ss(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        if constexpr (F8)
+          ptx::mma_ss_f8(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        else
+          ptx::mma_ss(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
       }
       ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
       ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
@@ -608,11 +623,11 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
   mma_drain(bars, p);
 }
 
-template <int D, bool BF16, bool RAB>
+template <int D, bool BF16, bool RAB, bool F8>
 __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                               long long total) {
-  using C = Cfg<D, RAB>;
-  constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16 ? 1u : 0u, 128, D, 1);
+  using C = Cfg<D, RAB, F8>;
+  constexpr uint32_t IDESC_O = ptx::idesc_f16((BF16 && !F8) ? 1u : 0u, 128, D, 1);
   const uint32_t sbase = ptx::smem_u32(smem);
   uint32_t v_it = 0, t = 0, u = 0;
   for (int k = 0;; ++k) {
@@ -633,11 +648,15 @@ __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uin
       ptx::tc_fence_after();
       const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < kTileN / 16; ++kk) {
-        // keys [16kk, 16kk + 16) are packed in P columns [8kk, 8kk + 8)
-        const uint32_t pcol = C::P_COL0 + sb * 64 + kk * 8;
-        const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
-        ptx::mma_ts(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < kTileN / C::KS; ++kk) {
+        // keys [KS*kk, KS*kk + KS) are packed in P columns [8kk, 8kk + 8) (2 or 4 per column)
+        const uint32_t pcol = C::P_COL0 + sb * C::PW + kk * 8;
+        const uint64_t bd =
+            ptx::smem_desc(va + kk * C::KS * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
+        if constexpr (F8)
+          ptx::mma_ts_f8(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+        else
+          ptx::mma_ts(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
       }
       ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
       ptx::mma_commit(ptx::smem_u32(&bars->pv_done[sb]));
@@ -696,11 +715,12 @@ __device__ __forceinline__ bool epi_barrier(Bars* bars, uint32_t& phase, const F
   return ok;
 }
 
-template <int D, bool BF16, bool RAB, bool MASK, bool KV>
+template <int D, bool BF16, bool RAB, bool MASK, bool KV, bool F8>
 __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                          const CUtensorMap* tm_o, long long total, int warp, int lane) {
-  using C = Cfg<D, RAB>;
-  using T16 = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  using C = Cfg<D, RAB, F8>;
+  constexpr bool OUT_BF16 = BF16 || F8;  // O type (FP8 inputs give bf16 out)
+  using T16 = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
   constexpr int OC = D / kEpiWG;             // O columns per warpgroup
   constexpr int OCH = OC < 32 ? OC : 32;     // O columns per TMEM load
   const int wg = warp >> 2;
@@ -738,8 +758,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          w[e] = pack2<BF16>(__uint_as_float(part[v4 * 8 + 2 * e]) * p.silu_scale,
-                             __uint_as_float(part[v4 * 8 + 2 * e + 1]) * p.silu_scale);
+          w[e] = pack2<OUT_BF16>(__uint_as_float(part[v4 * 8 + 2 * e]) * p.silu_scale,
+                                 __uint_as_float(part[v4 * 8 + 2 * e + 1]) * p.silu_scale);
         if constexpr (C::STAGE) {
           // this warp's 32-row x (D/4)-column block in the TMA box layout: swizzled 16-byte
           // chunks, conflict-free for one row per lane
@@ -872,7 +892,14 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const uint32_t h2 = pack2<BF16>(x[2 * e], x[2 * e + 1]);
-            pk[e] = fma2<BF16>(h2, tanh2<BF16>(h2), h2);
+            if constexpr (F8) {
+              // kP8Scale * P = (kP8Scale * h) * tanh(h) + kP8Scale * h: P scaled by a power
+              // of two (exact) so that typical values stay in E4M3's normal range
+              const uint32_t hs = fma2<false>(h2, kP8ScaleF16x2, 0x80008000u);
+              pk[e] = fma2<false>(hs, tanh2<false>(h2), hs);
+            } else {
+              pk[e] = fma2<BF16>(h2, tanh2<BF16>(h2), h2);
+            }
           }
         }
         uint32_t pcol;
@@ -881,11 +908,21 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           if (c == 0 && t >= C::NSB &&
               !warp_wait(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p))
             return;
-          pcol = C::P_COL0 + sb * 64 + cc / 2;
+          pcol = C::P_COL0 + sb * C::PW + cc / (C::PW == 64 ? 2 : 4);
         } else {
           pcol = C::S_COL0 + sb * 128 + col + c * 16;  // over S columns already read
         }
-        ptx::tmem_st16(tmem + lane_off + pcol, pk);
+        if constexpr (F8) {
+          // P rounded to E4M3 (saturating), four keys per TMEM column, lowest key in the
+          // low byte: the A operand of the kind::f8f6f4 product
+          uint32_t p8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            p8[e] = ptx::cvt_e4m3x2_f16x2(pk[2 * e]) | (ptx::cvt_e4m3x2_f16x2(pk[2 * e + 1]) << 16);
+          ptx::tmem_st8(tmem + lane_off + pcol, p8);
+        } else {
+          ptx::tmem_st16(tmem + lane_off + pcol, pk);
+        }
       }
       if constexpr (RAB) warp_arrive(&bars->r_empty[rs], lane);
       ptx::tmem_st_wait();
@@ -910,13 +947,13 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 
 // ------------------------------------------------------------------ kernel
 // MASK: the rab stream carries a custom mask (multiplied into P after the SiLU).
-template <int D, bool BF16, bool RAB, bool MASK = false, bool KV = false>
+template <int D, bool BF16, bool RAB, bool MASK = false, bool KV = false, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                   const __grid_constant__ CUtensorMap tm_o,
                   const __grid_constant__ CUtensorMap tm_c, const FwdParams p) {
-  using C = Cfg<D, RAB>;
+  using C = Cfg<D, RAB, F8>;
   static_assert(C::NQ <= (int)(sizeof(Bars::q_full) / sizeof(uint64_t)) &&
                     C::NK <= (int)(sizeof(Bars::k_full) / sizeof(uint64_t)) &&
                     C::NV <= (int)(sizeof(Bars::v_full) / sizeof(uint64_t)) &&
@@ -983,24 +1020,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long total = (long long)(*p.work_count) * p.Nq;
 
   if (warp < kEpiWarps) {
-    epilogue<D, BF16, RAB, MASK, KV>(p, bars, smem, tmem, &tm_o, total, warp, lane);
+    epilogue<D, BF16 && !F8, RAB, MASK, KV, F8>(p, bars, smem, tmem, &tm_o, total, warp, lane);
   } else if (warp == kProducerWarp) {
-    if (lane == 0) producer_k<D, RAB, KV>(p, bars, smem, &tm_k, &tm_c, total);
+    if (lane == 0) producer_k<D, RAB, KV, F8>(p, bars, smem, &tm_k, &tm_c, total);
   } else if (warp == kQProducerWarp) {
-    if (lane == 0) producer_q<D, RAB, KV>(p, bars, smem, &tm_q, total);
+    if (lane == 0) producer_q<D, RAB, KV, F8>(p, bars, smem, &tm_q, total);
   } else if (warp == kVProducerWarp) {
-    if (lane == 0) producer_v<D, RAB, KV>(p, bars, smem, &tm_v, &tm_c, total);
+    if (lane == 0) producer_v<D, RAB, KV, F8>(p, bars, smem, &tm_v, &tm_c, total);
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       if constexpr (C::SERIAL)
-        mma_serial_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+        mma_serial_issuer<D, BF16, RAB, F8>(p, bars, smem, tmem, total);
       else
-        mma_s_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+        mma_s_issuer<D, BF16, RAB, F8>(p, bars, smem, tmem, total);
     }
   } else if (warp == kRabWarp) {
-    if (RAB && lane == 0) producer_r<D, RAB, KV>(p, bars, smem, &tm_r, total);
+    if constexpr (RAB) {
+      if (lane == 0) producer_r<D, RAB, KV, F8>(p, bars, smem, &tm_r, total);
+    }
   } else if (warp == kPvWarp) {
-    if (lane == 0 && !C::SERIAL) mma_pv_issuer<D, BF16, RAB>(p, bars, smem, tmem, total);
+    if (lane == 0 && !C::SERIAL) mma_pv_issuer<D, BF16, RAB, F8>(p, bars, smem, tmem, total);
   }
   __syncwarp();
   ptx::tc_fence_before();

@@ -7,26 +7,26 @@
 namespace hstu {
 namespace tc {
 
-template <int D, bool BF16, bool RAB, bool MASK, bool KV>
+template <int D, bool BF16, bool RAB, bool MASK, bool KV, bool F8 = false>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(fwd_tc_kernel<D, BF16, RAB, MASK, KV>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, RAB>::SMEM_BYTES);
+  return cudaFuncSetAttribute(fwd_tc_kernel<D, BF16, RAB, MASK, KV, F8>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, RAB, F8>::SMEM_BYTES);
 }
 
-template <int D, bool BF16, bool RAB, bool MASK, bool KV>
+template <int D, bool BF16, bool RAB, bool MASK, bool KV, bool F8 = false>
 cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t stream,
                        bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Cfg<D, RAB>::SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<D, RAB, F8>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, BF16, RAB, MASK, KV>, m.q, m.k, m.v, m.rab, m.out,
+  return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, BF16, RAB, MASK, KV, F8>, m.q, m.k, m.v, m.rab, m.out,
                             m.cache, p);
 }
 
@@ -53,6 +53,11 @@ cudaError_t dispatch_type(const FwdParams& p, const TcMaps& m, int bf16, int gri
 // Custom-mask variants (fwd_tc_mask.cu): prepare (shared-memory opt-in) or launch.
 cudaError_t dispatch_mask(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                           cudaStream_t st, bool pdl, bool prepare);
+
+// FP8 E4M3 variants (fwd_tc_f8.cu): head dims 32, 64, 128, no rab or custom mask, with or
+// without a key side.
+cudaError_t dispatch_f8(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st, bool pdl,
+                        bool prepare);
 
 // Key-side variants (fwd_tc_kv.cu, fwd_tc_kv_mask.cu): own k/v offsets and / or a KV cache.
 cudaError_t dispatch_kv(const FwdParams& p, const TcMaps& m, int bf16, int grid,

@@ -44,7 +44,11 @@ struct FwdParams {
   long long num_pages;
   int page_size;
   int Sq;
+  int fp8;                    // q, k, v (and the cache) are FP8 E4M3; out is bf16
 };
+
+// FP8 kernels hold kP8Scale * P (E4M3) for the second product; silu_scale is divided by it.
+constexpr float kP8Scale = 16.0f;
 
 __host__ __device__ inline long long load_index(const void* p, long long i, int is64) {
   return is64 ? static_cast<const long long*>(p)[i] : static_cast<const int*>(p)[i];
@@ -107,10 +111,11 @@ struct TcMaps {
   CUtensorMap q, k, v, rab, out, cache;
 };
 bool tc_supported_dim(int D);
-int tc_swizzle_bytes(int D);  // row width of one TMA box / UMMA swizzle atom
+int tc_swizzle_bytes(int D, int elem_bytes);  // row width of one TMA box / UMMA swizzle atom
 int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
-// rab: 0 none, 1 rab, 2 custom mask; kv: the key-side variant (own k/v offsets, KV cache)
-cudaError_t tc_prepare(int D, int bf16, int rab, int kv);
+// elem: 0 f16, 1 bf16, 2 FP8 E4M3; rab: 0 none, 1 rab, 2 custom mask; kv: the key-side
+// variant (own k/v offsets, KV cache)
+cudaError_t tc_prepare(int D, int elem, int rab, int kv);
 cudaError_t launch_fwd_tc(const FwdParams& p, const TcMaps& maps, int bf16, int grid,
                           cudaStream_t stream, bool pdl);
 

@@ -240,6 +240,28 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// The same two products with 8-bit operands (kind::f8f6f4; A/B format 0 = E4M3 in the
+// instruction descriptor): 32 K elements per instruction.
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 async op issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
@@ -315,6 +337,14 @@ __device__ __forceinline__ uint32_t tanh_bf16x2(uint32_t x) {
   asm("tanh.approx.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
+// Two f16 values (a packed f16x2) rounded to E4M3, saturating to +-448; the low half of x
+// becomes the low byte. Returns the 16-bit pair in the low half of the result.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(x));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t tanh_f16x2(uint32_t x) {
   uint32_t y;
   asm("tanh.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));

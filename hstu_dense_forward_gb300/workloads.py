@@ -17,7 +17,8 @@ from typing import Optional
 
 import torch
 
-DTYPES = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}
+DTYPES = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16,
+          "fp8": torch.float8_e4m3fn}
 
 
 @dataclass(frozen=True)
@@ -77,6 +78,11 @@ WORKLOADS = {
         name="fp16_gqa8x2_targets_b8_s4096_d128", dtype="fp16", batch=8, num_heads_q=8,
         num_heads_kv=2, head_dim=128, max_seqlen=4096, len_lo=1024, len_hi=4096, causal=True,
         context_range=(0, 32), target_range=(16, 256), target_group_size=16, sigma=0.3, seed=3),
+    # the causal workload with FP8 E4M3 inputs (feature table, "FP8 quantization: cast")
+    "fp8_causal_b32_s2048_h4_d128": Workload(
+        name="fp8_causal_b32_s2048_h4_d128", dtype="fp8", batch=32, num_heads_q=4,
+        num_heads_kv=4, head_dim=128, max_seqlen=2048, len_lo=256, len_hi=2048, causal=True,
+        sigma=0.5, seed=1),
     "bf16_long_b4_s8192_h4_d256": Workload(
         name="bf16_long_b4_s8192_h4_d256", dtype="bf16", batch=4, num_heads_q=4, num_heads_kv=4,
         head_dim=256, max_seqlen=8192, len_lo=8192, len_hi=8192, causal=False,

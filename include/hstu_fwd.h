@@ -65,8 +65,13 @@ typedef enum {
 } hstu_status;
 
 /* Element type of q, k, v, rab and out (Inputs and Outputs table: "the type must
- * match q"; the output "same as q"). */
-typedef enum { HSTU_F32 = 0, HSTU_F16 = 1, HSTU_BF16 = 2 } hstu_dtype;
+ * match q"; the output "same as q"). HSTU_FP8_E4M3 (feature table, "FP8 quantization
+ * types: cast"): q, k, v and the KV cache hold FP8 E4M3 bytes (the caller's cast, with
+ * per-tensor descale factors folded into alpha for q and k and into silu_scale for v);
+ * both products run on 8-bit tensor cores with fp32 accumulation, P is rounded to E4M3
+ * (saturating) for the second one, and out is bf16. Head dims 32, 64, 128; no rab or
+ * custom mask (HSTU_ERR_UNSUPPORTED); not on the allocation-free entry point. */
+typedef enum { HSTU_F32 = 0, HSTU_F16 = 1, HSTU_BF16 = 2, HSTU_FP8_E4M3 = 3 } hstu_dtype;
 
 /* Tensor layout (Inputs and Outputs table, layout): "jagged" q [T, Nq, D] with
  * seq_offsets, or "normal" q [B, S, Nq, D] where every sequence has S = max_seqlen

@@ -1,0 +1,171 @@
+"""FP8 E4M3 inputs (feature table, "FP8 quantization types: cast"): q, k, v cast to E4M3
+with per-tensor descale factors, both products on the 8-bit tensor cores, P rounded to
+E4M3 (after scaling by 16) for the second one, out bf16. Checked against the fp64 oracle
+run on the dequantized inputs (the exact values the kernel receives).
+
+Tolerance, derived from the arithmetic: per output row i the kernel's error is at most
+  silu_scale * sum_j valid (2^-4 |P_ij| + 2^-14) |V_j|   (E4M3 rounding of 16 P: relative
+                                                           2^-4, absolute 2^-10 / 16 for
+                                                           subnormals)
+  + 2^-8 silu_scale * sum_j |P_ij| |V_j|                 (P computed in f16)
+  + 2^-8 |O_i|                                            (bf16 output)
+which the tests compute in fp64 from the dequantized inputs (plain causal or no mask)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hstu_dense_forward_gb300 import hstu_fwd
+from hstu_dense_forward_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+E4M3 = torch.float8_e4m3fn
+BASE = W.WORKLOADS["bf16_causal_b32_s2048_h4_d128"]
+
+
+def _quant(x, amax_to=224.0):
+    """Per-tensor cast: x ~ descale * e4m3(x / descale), descale = max|x| / amax_to."""
+    descale = float(x.float().abs().max()) / amax_to
+    return (x.float() / descale).to(E4M3), descale
+
+
+def _case(d, heads, B=3, S=300, causal=True, seed=71, sigma=0.5):
+    w = W.scaled(BASE, batch=B, max_seqlen=S, len_lo=1, len_hi=S, dtype="bf16", head_dim=d,
+                 num_heads_q=heads[0], num_heads_kv=heads[1], causal=causal, seed=seed,
+                 sigma=sigma)
+    return w, W.generate(w)
+
+
+def _bound(qd, kd, vd, so, alpha, silu_scale, causal, nq, nk):
+    """Per-row error bound of the module docstring, [T, Nq] (fp64, dense per sequence)."""
+    G = nq // nk
+    T = qd.shape[0]
+    out = np.zeros((T, nq))
+    ref_abs = np.zeros((T, nq))
+    for b in range(len(so) - 1):
+        a, e = int(so[b]), int(so[b + 1])
+        L = e - a
+        if L == 0:
+            continue
+        m = np.tril(np.ones((L, L))) if causal else np.ones((L, L))
+        for h in range(nq):
+            q = qd[a:e, h]
+            k = kd[a:e, h // G]
+            v = np.abs(vd[a:e, h // G])
+            x = alpha * (q @ k.T)
+            p = np.abs(x / (1.0 + np.exp(-x))) * m
+            pv = (p @ v).max(axis=1)
+            out[a:e, h] = silu_scale * ((2.0 ** -4 + 2.0 ** -8) * pv +
+                                        2.0 ** -14 * (m @ v).max(axis=1))
+    return out
+
+
+@pytest.mark.parametrize("d,heads,causal", [(128, (4, 4), True), (64, (8, 2), True),
+                                            (32, (2, 2), False), (128, (2, 1), False),
+                                            (64, (4, 4), False)])
+def test_fp8_matches_oracle_within_derived_bound(cuda_device, d, heads, causal):
+    w, inp = _case(d, heads, causal=causal)
+    q8, sq = _quant(inp["q"])
+    k8, sk = _quant(inp["k"])
+    v8, sv = _quant(inp["v"])
+    dev = cuda_device
+    out = hstu_fwd(q8.to(dev), k8.to(dev), v8.to(dev), inp["seq_offsets"].to(dev),
+                   max_seqlen=w.max_seqlen, causal=causal, alpha=w.alpha_value,
+                   silu_scale=w.silu_scale_value, q_descale=sq, k_descale=sk, v_descale=sv)
+    torch.cuda.synchronize()
+    assert out.dtype == torch.bfloat16
+    qd, kd, vd = (t.double().numpy() * s for t, s in ((q8, sq), (k8, sk), (v8, sv)))
+    ref = oracle.hstu_fwd(qd, kd, vd, inp["seq_offsets"],
+                          mask_type=oracle.MASK_CAUSAL if causal else oracle.MASK_NONE,
+                          alpha=w.alpha_value, silu_scale=w.silu_scale_value,
+                          max_seqlen=w.max_seqlen, nthreads=8)
+    got = out.double().cpu().numpy()
+    T = int(inp["seq_offsets"][-1])
+    err = np.abs(got[:T] - ref[:T]).max(axis=2)  # [T, Nq]
+    bound = _bound(qd, kd, vd, inp["seq_offsets"].numpy(), w.alpha_value, w.silu_scale_value,
+                   causal, heads[0], heads[1])[:T] + 2.0 ** -8 * np.abs(ref[:T]).max(axis=2)
+    assert np.all(err <= bound), float((err / bound).max())
+    assert np.abs(got[:T] - ref[:T]).max() / np.abs(ref[:T]).max() <= 2.0 ** -4
+
+
+def test_fp8_targets_gqa_against_oracle(cuda_device):
+    """Context and targets with GQA: the global check (error <= 2^-4 of max|O|)."""
+    w = W.scaled(W.WORKLOADS["fp16_gqa8x2_targets_b8_s4096_d128"], batch=3, max_seqlen=400,
+                 len_lo=50, len_hi=400, dtype="bf16", seed=72)
+    inp = W.generate(w)
+    q8, k8, v8 = (inp[n].float().to(E4M3) for n in ("q", "k", "v"))
+    dev = cuda_device
+    out = hstu_fwd(q8.to(dev), k8.to(dev), v8.to(dev), inp["seq_offsets"].to(dev),
+                   max_seqlen=w.max_seqlen, num_context=inp["num_context"].to(dev),
+                   num_targets=inp["num_targets"].to(dev), target_group_size=w.target_group_size,
+                   alpha=w.alpha_value, silu_scale=w.silu_scale_value)
+    torch.cuda.synchronize()
+    ref = oracle.hstu_fwd(q8, k8, v8, inp["seq_offsets"], num_context=inp["num_context"],
+                          num_targets=inp["num_targets"], mask_type=oracle.MASK_CAUSAL,
+                          target_group_size=w.target_group_size, alpha=w.alpha_value,
+                          silu_scale=w.silu_scale_value, max_seqlen=w.max_seqlen, nthreads=8)
+    T = int(inp["seq_offsets"][-1])
+    got = out.double().cpu().numpy()
+    assert np.abs(got[:T] - ref[:T]).max() / np.abs(ref[:T]).max() <= 2.0 ** -4
+
+
+def test_fp8_paged_cache_against_oracle(cuda_device):
+    """E4M3 KV cache pages and new rows, queries at the end of the keys."""
+    from dataclasses import replace
+    kw = replace(W.KV_WORKLOADS["bf16_paged_b128_hist1k_4k_h4_d128"], batch=4,
+                 hist_range=(100, 600), new_range=(10, 200), page_size=32, seed=73)
+    inp = W.generate_kv(kw)
+    for n in ("q", "k", "v", "kv_cache"):
+        inp[n] = inp[n].float().to(E4M3)
+    dev = cuda_device
+    dv = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = hstu_fwd(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], max_seqlen=dv["max_seqlen"],
+                   max_seqlen_k=dv["max_seqlen_k"], num_targets=dv["num_targets"],
+                   target_group_size=1, alpha=dv["alpha"], silu_scale=dv["silu_scale"],
+                   seq_offsets_k=dv["seq_offsets_k"], kv_cache=dv["kv_cache"],
+                   page_offsets=dv["page_offsets"], page_ids=dv["page_ids"],
+                   last_page_len=dv["last_page_len"])
+    torch.cuda.synchronize()
+    ref = oracle.hstu_fwd(inp["q"], inp["k"], inp["v"], inp["seq_offsets"],
+                          seq_offsets_k=inp["seq_offsets_k"], kv_cache=inp["kv_cache"],
+                          page_offsets=inp["page_offsets"], page_ids=inp["page_ids"],
+                          last_page_len=inp["last_page_len"], num_targets=inp["num_targets"],
+                          mask_type=oracle.MASK_CAUSAL, target_group_size=1, alpha=inp["alpha"],
+                          silu_scale=inp["silu_scale"], max_seqlen=inp["max_seqlen_k"],
+                          nthreads=8)
+    got = out.double().cpu().numpy()
+    assert np.abs(got - ref).max() / np.abs(ref).max() <= 2.0 ** -4
+
+
+def test_fp8_full_size_sampled_rows(cuda_device):
+    """The FP8 causal workload at full size (B = 32, L ~ U[256, 2048]), sampled rows."""
+    w = W.WORKLOADS["fp8_causal_b32_s2048_h4_d128"]
+    inp = W.generate(w)
+    d = W.to_device(inp, cuda_device)
+    out = hstu_fwd(d["q"], d["k"], d["v"], d["seq_offsets"], max_seqlen=w.max_seqlen,
+                   alpha=w.alpha_value, silu_scale=w.silu_scale_value)
+    torch.cuda.synchronize()
+    so = inp["seq_offsets"]
+    g = torch.Generator().manual_seed(5)
+    rows = []
+    for _ in range(64):
+        b = int(torch.randint(0, w.batch, (1,), generator=g))
+        i = int(torch.randint(0, int(so[b + 1] - so[b]), (1,), generator=g))
+        rows.append((b, int(torch.randint(0, w.num_heads_q, (1,), generator=g)), i))
+    ref = oracle.hstu_fwd_rows(inp["q"], inp["k"], inp["v"], so, np.array(rows),
+                               mask_type=oracle.MASK_CAUSAL, alpha=w.alpha_value,
+                               silu_scale=w.silu_scale_value, max_seqlen=w.max_seqlen,
+                               nthreads=16)
+    sel = torch.stack([out[int(so[b]) + i, h] for b, h, i in rows]).double().cpu().numpy()
+    assert np.abs(sel - ref).max() / np.abs(ref).max() <= 2.0 ** -4
+
+
+def test_fp8_rejects_rab_and_custom_mask(cuda_device):
+    from hstu_dense_forward_gb300 import HstuError
+    w, inp = _case(64, (2, 2), B=2, S=64)
+    q8 = inp["q"].float().to(E4M3).to(cuda_device)
+    so = inp["seq_offsets"].to(cuda_device)
+    rab = torch.zeros(2, 2, 64, 64, dtype=E4M3, device=cuda_device)
+    with pytest.raises(HstuError):
+        hstu_fwd(q8, q8, q8, so, max_seqlen=64, rab=rab)
