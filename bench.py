@@ -207,9 +207,10 @@ def _algorithmic_bytes_kv(w, inp):
     """Key-side workload: Q read and O written once; per key/value head, every key of a
     sequence (cached history rows and new rows) read once as K and once as V."""
     el = torch.finfo(W_dtype(w)).bits // 8
+    out_el = 2 if w.dtype == "fp8" else el  # FP8 inputs give bf16 out
     tq = int(inp["seq_offsets"][-1])
     keys = int((inp["seq_offsets_k"][1:] - inp["seq_offsets_k"][:-1]).sum() + inp["history"].sum())
-    return (2 * tq * w.num_heads_q + 2 * keys * w.num_heads_kv) * w.head_dim * el
+    return (tq * w.num_heads_q * (el + out_el) + 2 * keys * w.num_heads_kv * el) * w.head_dim
 
 
 def W_dtype(w):

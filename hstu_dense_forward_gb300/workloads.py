@@ -210,6 +210,11 @@ KV_WORKLOADS = {
         name="bf16_paged_b128_hist1k_4k_h4_d128", dtype="bf16", batch=128, num_heads_q=4,
         num_heads_kv=4, head_dim=128, hist_range=(1024, 4096), new_range=(32, 256),
         page_size=128, targets_are_queries=True, target_group_size=1, sigma=0.5, seed=5),
+    # the same with an FP8 E4M3 cache and inputs (half the bytes per key)
+    "fp8_paged_b128_hist1k_4k_h4_d128": KVWorkload(
+        name="fp8_paged_b128_hist1k_4k_h4_d128", dtype="fp8", batch=128, num_heads_q=4,
+        num_heads_kv=4, head_dim=128, hist_range=(1024, 4096), new_range=(32, 256),
+        page_size=128, targets_are_queries=True, target_group_size=1, sigma=0.5, seed=5),
 }
 
 

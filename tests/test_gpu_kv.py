@@ -16,7 +16,8 @@ from hstu_dense_forward_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-TOL = {"fp32": 1e-5, "bf16": 2e-2, "fp16": 1e-2}
+TOL = {"fp32": 1e-5, "bf16": 2e-2, "fp16": 1e-2,
+       "fp8": 2.0 ** -4}  # E4M3 rounding of P (derivation in test_gpu_fp8.py)
 BASE = W.KV_WORKLOADS["bf16_paged_b128_hist1k_4k_h4_d128"]
 KEYS = ("q", "k", "v", "seq_offsets", "seq_offsets_k", "kv_cache", "page_offsets", "page_ids",
         "last_page_len", "num_context", "num_targets", "rab")
@@ -265,11 +266,13 @@ def test_key_side_arguments_checked(cuda_device):
                      dv["q"].shape[0], 1.0, 1.0, out.data_ptr(), 0)
 
 
-def test_full_size_paged_workload_sampled_rows(cuda_device):
-    """The paged ranking workload at its full size (128 sequences, cached histories of 1k-4k
-    keys in 128-row pages, 32-256 new tokens as targets of group size 1): sampled output
-    rows against the oracle, in the launch configuration the benchmark times."""
-    w = BASE
+@pytest.mark.parametrize("name", list(W.KV_WORKLOADS))
+def test_full_size_paged_workload_sampled_rows(cuda_device, name):
+    """The paged ranking workloads at their full size (128 sequences, cached histories of
+    1k-4k keys in 128-row pages, 32-256 new tokens as targets of group size 1; bf16 and
+    FP8 E4M3): sampled output rows against the oracle, in the launch configuration the
+    benchmark times."""
+    w = W.KV_WORKLOADS[name]
     inp = W.generate_kv(w)
     got = _gpu(inp, cuda_device)
     torch.cuda.synchronize()
@@ -286,4 +289,4 @@ def test_full_size_paged_workload_sampled_rows(cuda_device):
     ref = _oracle(inp, rows=np.array(rows))
     sel = torch.stack([got[int(so[b]) + i, h] for b, h, i in rows]).double().cpu().numpy()
     err = np.max(np.abs(sel - ref)) / np.max(np.abs(ref))
-    assert err <= TOL["bf16"]
+    assert err <= TOL[w.dtype]
