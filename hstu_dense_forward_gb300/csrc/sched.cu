@@ -98,6 +98,11 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
     const int kv_end = kv_end_for_rows(s, off + mt * tile_m, tile_m, p.mask_type);
     return key_visits(kv_end, split_tile((int)kv.hist, (int)kv.Lk));
   };
+  // With a key side of its own (a few queries against long, often cached, key sequences)
+  // the query tiles of one sequence read the same keys: they are kept next to each other
+  // in the list, binned by the sequence's heaviest tile, so that they run at the same time
+  // and the later reads of the keys hit L2. Otherwise each tile is binned by its own count.
+  const bool group = p.seq_offsets_k != nullptr || p.page_offsets != nullptr;
   // pass 1: histogram of key-visit counts
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
     const SeqKV kv = seq_kv(p, b);
@@ -105,7 +110,13 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
     const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
     const SeqGeom s = make_geom((int)kv.Lk, nc, nt, p.g, p.mask_type);
     const int mtiles = ceil_div((int)kv.Lq, tile_m);
-    for (int mt = 0; mt < mtiles; ++mt) atomicAdd(&hist[visits(kv, s, mt)], 1);
+    if (group) {
+      int most = 0;
+      for (int mt = 0; mt < mtiles; ++mt) most = max(most, visits(kv, s, mt));
+      if (mtiles > 0) atomicAdd(&hist[most], mtiles);
+    } else {
+      for (int mt = 0; mt < mtiles; ++mt) atomicAdd(&hist[visits(kv, s, mt)], 1);
+    }
   }
   __syncthreads();
   // exclusive scan, largest key-tile count first
@@ -125,9 +136,18 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
     const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
     const SeqGeom s = make_geom((int)kv.Lk, nc, nt, p.g, p.mask_type);
     const int mtiles = ceil_div((int)kv.Lq, tile_m);
-    for (int mt = 0; mt < mtiles; ++mt) {
-      const int pos = atomicAdd(&cursor[visits(kv, s, mt)], 1);
-      work[pos] = pack_item(b, mt);
+    if (group) {
+      int most = 0;
+      for (int mt = 0; mt < mtiles; ++mt) most = max(most, visits(kv, s, mt));
+      if (mtiles > 0) {
+        const int pos = atomicAdd(&cursor[most], mtiles);
+        for (int mt = 0; mt < mtiles; ++mt) work[pos + mt] = pack_item(b, mt);
+      }
+    } else {
+      for (int mt = 0; mt < mtiles; ++mt) {
+        const int pos = atomicAdd(&cursor[visits(kv, s, mt)], 1);
+        work[pos] = pack_item(b, mt);
+      }
     }
   }
   // complete only after the kernel before this one in the stream
