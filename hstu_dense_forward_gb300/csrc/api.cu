@@ -288,7 +288,7 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
 
 // The key-side arguments a plan needs: none (kv NULL) for a plain plan; seq_offsets_k with
 // is_delta_qk; the cache and its page table with page_size.
-static bool kv_args_ok(const hstu_fwd_desc& d, const hstu_fwd_kv* kv, long long total_tokens) {
+static bool kv_args_ok(const hstu_fwd_desc& d, const hstu_fwd_kv* kv) {
   if (!key_side(d)) return kv == nullptr;
   if (!kv) return false;
   if (d.is_delta_qk) {
@@ -304,7 +304,6 @@ static bool kv_args_ok(const hstu_fwd_desc& d, const hstu_fwd_kv* kv, long long 
   } else if (kv->kv_cache || kv->page_offsets || kv->page_ids || kv->last_page_len) {
     return false;
   }
-  (void)total_tokens;
   return true;
 }
 
@@ -318,7 +317,7 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
                             void* stream) {
   const hstu_fwd_desc& d = P->desc;
   if (total_tokens < 0 || total_tokens > 0x7fffffffll) return HSTU_ERR_INVALID_ARG;
-  if (!kv_args_ok(d, kv, total_tokens)) return HSTU_ERR_INVALID_ARG;
+  if (!kv_args_ok(d, kv)) return HSTU_ERR_INVALID_ARG;
   if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
   const long long Tk = d.is_delta_qk ? kv->total_tokens_k : total_tokens;
   const bool kv_rows = Tk > 0;  // k and v are read only when there are new rows
