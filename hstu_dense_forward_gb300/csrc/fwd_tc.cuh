@@ -827,6 +827,15 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       int rs = 0;
       if constexpr (RAB) {
         rs = t % C::NR;  // one rab tile per S tile, in tile order
+        // With two epilogue groups and a one-tile rab ring (D = 256) the rab slot alternates
+        // between the groups, so a group reaching tile t may find r_full two phases behind,
+        // where a parity wait cannot tell phase t from phase t - 2: it first waits until
+        // the other group has released tile t - 1 (r_full is then at phase t at most).
+        if constexpr (C::NR < C::EPI_GROUPS) {
+          if (t >= 1 &&
+              !warp_wait(bars, &bars->r_empty[(t - 1) % C::NR], ((t - 1) / C::NR) & 1, p))
+            return;
+        }
         if (!warp_wait(bars, &bars->r_full[rs], (t / C::NR) & 1, p)) return;
         rab_row = smem + C::OFF_R + rs * C::RAB_BYTES + r * 128;
       }

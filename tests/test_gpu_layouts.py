@@ -164,3 +164,22 @@ def test_custom_causal_mask_matches_builtin(cuda_device):
     T = int(inp["seq_offsets"][-1])
     g, r = got[:T].float(), ref[:T].float()
     assert float((g - r).abs().max()) <= 1e-3 * float(r.abs().max())
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_d256_rab_runs_are_identical_and_match_oracle(cuda_device, dtype):
+    """D = 256 with rab: two epilogue groups share a one-tile rab ring; every run must
+    read each tile's own rab (a stale tile would change some rows from run to run)."""
+    w = W.scaled(BASE, batch=3, max_seqlen=640, len_lo=300, len_hi=640, dtype=dtype,
+                 head_dim=256, num_heads_q=2, num_heads_kv=2, rab=True, rab_sigma=1.0, seed=81)
+    inp = W.generate(w)
+    dv = W.to_device(inp, cuda_device)
+    outs = [_jagged_call(dv, rab=dv["rab"]).clone() for _ in range(6)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    ref = oracle.hstu_fwd(inp["q"], inp["k"], inp["v"], inp["seq_offsets"], rab=inp["rab"],
+                          mask_type=oracle.MASK_CAUSAL, alpha=inp["alpha"],
+                          silu_scale=inp["silu_scale"], max_seqlen=640, nthreads=8)
+    T = int(inp["seq_offsets"][-1])
+    assert _rel_err(outs[0][:T], ref[:T]) <= TOL[dtype]
