@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -54,6 +55,7 @@ struct hstu_fwd_plan {
   int* d_count;
   int* d_err;          // device error word (d_count[1])
   int parity;          // work list of the next run
+  int test_stall;      // HSTU_TEST_STALL=k at create: the watchdog test mode
   long long timeout_ns;
   // tensor maps of the last run, re-encoded when a pointer or a row count changes
   TcMaps maps;
@@ -151,6 +153,10 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
   memset(P, 0, sizeof(*P));
   P->desc = *desc;
   P->timeout_ns = (long long)(desc->watchdog_ms > 0 ? desc->watchdog_ms : 1000) * 1000000ll;
+  // Watchdog test mode (tensor-core plans): the kernel's K producer signals nothing, so a
+  // pipeline wait runs out after watchdog_ms and the run reports HSTU_ERR_TIMEOUT.
+  const char* stall = getenv("HSTU_TEST_STALL");
+  P->test_stall = stall && stall[0] == 'k' && stall[1] == 0 ? 1 : 0;
   P->tensor_cores = desc->dtype != HSTU_F32;
   cudaError_t e = cudaGetDevice(&P->device);
   if (e == cudaSuccess)
@@ -377,6 +383,7 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   p.alpha = alpha;
   p.silu_scale = silu_scale;
   p.fp8 = d.dtype == HSTU_FP8_E4M3 ? 1 : 0;
+  p.test_stall = P->test_stall;
   if (p.fp8) p.silu_scale = silu_scale / hstu::kP8Scale;  // the kernel's P carries kP8Scale
 
   if (P->tensor_cores) {

@@ -384,6 +384,7 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   using C = Cfg<D, RAB, F8>;
   uint32_t k_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
+  if (p.test_stall) return;  // watchdog test: no K tile is ever signalled
   for (int k = 0;; ++k) {
     Item it;
     if (!get_item(bars, k, it, p) || it.n_kv < 0) return;

@@ -45,6 +45,9 @@ struct FwdParams {
   int page_size;
   int Sq;
   int fp8;                    // q, k, v (and the cache) are FP8 E4M3; out is bf16
+  int test_stall;             // watchdog test (plans created with HSTU_TEST_STALL=k): the K
+                              // producer signals nothing, so the first score product's wait
+                              // runs out and the kernel takes its timeout path
 };
 
 // FP8 kernels hold kP8Scale * P (E4M3) for the second product; silu_scale is divided by it.
