@@ -111,7 +111,10 @@ typedef struct {
   int has_rab;           /* 1: rab is passed to every run */
   int has_num_context;   /* 1: num_context [B] is passed to every run */
   int has_num_targets;   /* 1: num_targets [B] is passed to every run */
-  int watchdog_ms;       /* limit of one device pipeline wait; 0 = 1000 ms */
+  int watchdog_ms;       /* limit of one device pipeline wait; 0 = 1000 ms. Test aid: a
+                            bf16/fp16/FP8 plan created while the environment holds
+                            HSTU_TEST_STALL=k never signals its K tiles, so every run
+                            ends through this limit with HSTU_DEVERR_TIMEOUT */
   int layout;            /* hstu_layout; 0 = jagged */
   int rab_heads;         /* bias planes per sequence: 0 or Nq for rab [B, Nq, S, S]; 1 for
                             rab [B, 1, S, S], one plane added for every query head (feature
