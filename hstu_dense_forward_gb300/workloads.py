@@ -59,7 +59,7 @@ class Workload:
         return self.silu_scale if self.silu_scale is not None else 1.0 / self.max_seqlen
 
 
-# The five workloads of the benchmark spec, in order: a tiny fp32 case, the bf16 causal jagged
+# The five configurations, in order: a tiny fp32 case, the bf16 causal jagged
 # throughput case, the rab (HBM) case, the fp16 GQA context/target case and the
 # long-sequence d=256 case.
 WORKLOADS = {
