@@ -498,3 +498,32 @@ def test_rejects_bad_head_ratio():
     q, k, v, so = _jagged(rng, [3], 3, 2, 2)
     with pytest.raises(ValueError):
         oracle.hstu_fwd(q, k, v, so)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_key_side_identities_random_geometries(seed):
+    """Random key-side geometries (page sizes, histories on and off page boundaries, empty
+    histories and new rows, queries reaching into the history, GQA, targets and context):
+    the paged call equals the contiguous-key call and the last rows of the all-queries call,
+    bit for bit."""
+    rng = _rng(100 + seed)
+    B = int(rng.integers(1, 5))
+    nk = int(rng.choice([1, 2]))
+    nq = nk * int(rng.choice([1, 2, 3]))
+    d = int(rng.integers(1, 5))
+    ps = int(rng.choice([1, 2, 3, 4, 8]))
+    lk = rng.integers(1, 14, B)
+    hist = np.array([int(rng.integers(0, L + 1)) for L in lk])
+    lq = np.array([int(rng.integers(0, L + 1)) for L in lk])
+    q_full, k, v, so_k, so_q, rows = _delta_case(rng, list(lk), list(lq), nq, nk, d)
+    nk_, nv_, so_new, cache, po, ids, last = _paged(rng, k, v, so_k, list(hist), ps)
+    S = int(lk.max()) + ps
+    kw = dict(mask_type=oracle.MASK_CAUSAL, num_context=rng.integers(0, 4, B),
+              num_targets=rng.integers(0, 5, B), target_group_size=int(rng.integers(0, 3)),
+              rab=rng.standard_normal((B, nq, S, S)), alpha=0.9, silu_scale=0.3, max_seqlen=S)
+    full = oracle.hstu_fwd(q_full, k, v, so_k, **kw)
+    delta = oracle.hstu_fwd(q_full[rows], k, v, so_q, seq_offsets_k=so_k, **kw)
+    paged = oracle.hstu_fwd(q_full[rows], nk_, nv_, so_q, seq_offsets_k=so_new, kv_cache=cache,
+                            page_offsets=po, page_ids=ids, last_page_len=last, **kw)
+    np.testing.assert_array_equal(delta, full[rows])
+    np.testing.assert_array_equal(paged, delta)
