@@ -166,6 +166,10 @@ def _is_kv(w):
     return isinstance(w, W.KVWorkload)
 
 
+# The headline metric: mask-aware useful TFLOP/s (4 * D per valid pair) and its share of the
+# bf16 peak, or HBM GB/s for the bandwidth-bound workloads; the time of one call.
+METRIC = "HSTU fwd mask-aware TFLOPS & % of GB300 BF16 peak (rab: HBM GB/s); ms/call"
+
 KV_KEYS = ("seq_offsets_k", "kv_cache", "page_offsets", "page_ids", "last_page_len")
 
 
@@ -377,7 +381,7 @@ def run_ours(args):
         cpu = cpu_baseline(w, inp, args.cpu_seconds)
     if rank == 0:
         line = {
-            "metric": "HSTU fwd mask-aware useful TFLOP/s (bf16, causal jagged); ms/call",
+            "metric": METRIC,
             "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -501,7 +505,7 @@ def run_reference(args):
     value = 4 * w.head_dim * pairs / dt / 1e12
     sample = f"sequence 0 of {w.batch} (L={T}, all {w.num_heads_q} heads, whole rows), fp64"
     line = {"impl": "reference",
-            "metric": "HSTU fwd mask-aware useful TFLOP/s (bf16, causal jagged); ms/call",
+            "metric": METRIC,
             "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64",
