@@ -327,32 +327,74 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     return res
 
 
-def hstu_fwd_noalloc(q, k, v, seq_offsets, out, *, max_seqlen, rab=None, num_context=None,
-                     num_targets=None, causal=True, target_group_size=0, alpha=1.0,
-                     silu_scale=None):
+def hstu_fwd_noalloc(q, k, v, seq_offsets, out, *, max_seqlen=None, rab=None,
+                     num_context=None, num_targets=None, causal=True, target_group_size=0,
+                     alpha=1.0, silu_scale=None, layout="jagged"):
     """hstu_fwd through the library's allocation-free entry point (hstu_fwd_run_noalloc):
     no plan, the work list lives in a fixed device array of the library. `out` must be
     given (this call allocates nothing, torch included). Calls that may overlap on the GPU
-    share that array and must be serialised by the caller."""
+    share that array and must be serialised by the caller. Arguments as for hstu_fwd
+    (jagged or normal layout; fp32, fp16 or bf16; no custom mask, key side or FP8)."""
     dev = q.device
-    for name, t in (("k", k), ("v", v), ("out", out)):
-        _check_tensor(t, name, q.dtype, dev, 3)
-    _check_tensor(q, "q", None, dev, 3)
-    B = seq_offsets.shape[0] - 1
-    d = _desc(dtype=q.dtype, batch=B, num_heads_q=q.shape[1],
-              num_heads_kv=k.shape[1], head_dim=q.shape[2], max_seqlen=max_seqlen,
-              index_is_int64=seq_offsets.dtype == torch.int64, causal=causal,
+    if dev.type != "cuda":
+        raise ValueError("hstu_fwd_noalloc runs on CUDA tensors only")
+    if q.dtype not in (torch.float32, torch.float16, torch.bfloat16):
+        raise TypeError(f"hstu_fwd_noalloc takes fp32, fp16 or bf16 inputs, got {q.dtype}")
+    if layout == "normal":
+        for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+            _check_tensor(t, name, q.dtype, dev, 4)
+        if seq_offsets is not None:
+            raise ValueError("the normal layout takes no seq_offsets")
+        B, S = q.shape[0], q.shape[1]
+        if max_seqlen is None:
+            max_seqlen = S
+        elif int(max_seqlen) != S:
+            raise ValueError(f"the normal layout needs max_seqlen == S = {S}")
+        if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+            raise ValueError("k and v must be [B, S, Nk, D] with q's B, S and D")
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+        idx = [t for t in (num_context, num_targets) if t is not None]
+        idx_dtype = idx[0].dtype if idx else torch.int64
+        Nq, Nk, D, T = q.shape[2], k.shape[2], q.shape[3], B * S
+    elif layout == "jagged":
+        for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+            _check_tensor(t, name, q.dtype, dev, 3)
+        if seq_offsets is None or max_seqlen is None:
+            raise ValueError("the jagged layout needs seq_offsets and max_seqlen")
+        _check_tensor(seq_offsets, "seq_offsets", None, dev, 1)
+        if k.shape != v.shape or k.shape[0] != q.shape[0] or k.shape[2] != q.shape[2]:
+            raise ValueError("k and v must be [T, Nk, D] with q's T and D")
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+        idx_dtype = seq_offsets.dtype
+        B = seq_offsets.shape[0] - 1
+        T, Nq, D = q.shape
+        Nk = k.shape[1]
+    else:
+        raise ValueError(f"layout must be 'jagged' or 'normal', got {layout!r}")
+    if idx_dtype not in (torch.int32, torch.int64):
+        raise TypeError("index tensors must be int32 or int64")
+    for name, t in (("num_context", num_context), ("num_targets", num_targets)):
+        if t is not None:
+            _check_tensor(t, name, idx_dtype, dev, 1)
+            if t.shape[0] != B:
+                raise ValueError(f"{name} must have B = {B} entries")
+    if rab is not None:
+        _check_tensor(rab, "rab", q.dtype, dev, 4)
+    d = _desc(dtype=q.dtype, batch=B, num_heads_q=Nq, num_heads_kv=Nk, head_dim=D,
+              max_seqlen=max_seqlen, index_is_int64=idx_dtype == torch.int64, causal=causal,
               target_group_size=target_group_size, has_rab=rab is not None,
               has_num_context=num_context is not None, has_num_targets=num_targets is not None,
-              rab_heads=_rab_heads(rab, B, q.shape[1], int(max_seqlen)))
+              layout=layout, rab_heads=_rab_heads(rab, B, Nq, int(max_seqlen)))
     if silu_scale is None:
         silu_scale = 1.0 / max_seqlen
     ptr = lambda t: None if t is None else t.data_ptr()
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev)
         _abi.check(_abi.lib().hstu_fwd_run_noalloc(
-            ctypes.byref(d), q.data_ptr(), k.data_ptr(), v.data_ptr(), seq_offsets.data_ptr(),
-            ptr(rab), ptr(num_context), ptr(num_targets), q.shape[0], float(alpha),
+            ctypes.byref(d), q.data_ptr(), k.data_ptr(), v.data_ptr(), ptr(seq_offsets),
+            ptr(rab), ptr(num_context), ptr(num_targets), T, float(alpha),
             float(silu_scale), out.data_ptr(), stream.cuda_stream), "hstu_fwd_run_noalloc")
     return out
 

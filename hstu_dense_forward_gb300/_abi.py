@@ -8,7 +8,10 @@ import re
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libhstu_fwd.so")
+# HSTU_FWD_TRACE=1 loads the tracing build of the library (build.build(trace=True));
+# HSTU_FWD_LIB=<path> loads another build of it (for comparing builds)
+LIB_PATH = os.environ.get("HSTU_FWD_LIB") or os.path.join(
+    PKG, "libhstu_fwd_trace.so" if os.environ.get("HSTU_FWD_TRACE") == "1" else "libhstu_fwd.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "hstu_fwd.h")
 
 HSTU_OK, HSTU_ERR_INVALID_ARG, HSTU_ERR_UNSUPPORTED, HSTU_ERR_CUDA, HSTU_ERR_TIMEOUT, \
@@ -108,6 +111,8 @@ def lib():
         L.hstu_fwd_run_noalloc.restype = ctypes.c_int
         L.hstu_fwd_run_noalloc.argtypes = [ctypes.POINTER(Desc), vp, vp, vp, vp, vp, vp, vp, ll, f,
                                            f, vp, vp]
+        L.hstu_fwd_trace_read.restype = ctypes.c_int
+        L.hstu_fwd_trace_read.argtypes = [vp, vp, ll]
         L.hstu_status_string.restype = ctypes.c_char_p
         L.hstu_status_string.argtypes = [ctypes.c_int]
         _lib = L

@@ -18,6 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhstu_fwd.so")
+# the tracing build (-DHSTU_TRACE=1): pipeline events recorded per CTA, read back with
+# hstu_fwd_trace_read; loaded instead of LIB when HSTU_FWD_TRACE=1
+OBJ_TRACE = os.path.join(PKG, "_build_trace")
+LIB_TRACE = os.path.join(PKG, "libhstu_fwd_trace.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
@@ -36,11 +40,12 @@ def _headers_mtime() -> float:
     return max([os.path.getmtime(h) for h in hs] + [os.path.getmtime(__file__)])
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(OBJ, os.path.basename(src) + ".o")
+def _compile(src: str, verbose_ptxas: bool, trace: bool = False) -> str:
+    obj = os.path.join(OBJ_TRACE if trace else OBJ, os.path.basename(src) + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime()):
         return obj
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj + ".tmp"]
+    cmd = [nvcc(), *ARCH, *FLAGS, *(["-DHSTU_TRACE=1"] if trace else []), "-c", src,
+           "-o", obj + ".tmp"]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -52,22 +57,24 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False) -> str:
-    """Compile csrc/*.cu for sm_103a and link libhstu_fwd.so; returns its path."""
-    os.makedirs(OBJ, exist_ok=True)
+def build(verbose_ptxas: bool = False, trace: bool = False) -> str:
+    """Compile csrc/*.cu for sm_103a and link libhstu_fwd.so (or, with trace=True, the
+    tracing build libhstu_fwd_trace.so); returns its path."""
+    obj_dir, lib = (OBJ_TRACE, LIB_TRACE) if trace else (OBJ, LIB)
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, trace), srcs))
+    if not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lpthread",
                "-lrt"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose_ptxas="-v" in sys.argv))
+    print(build(verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv))

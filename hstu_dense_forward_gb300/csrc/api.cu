@@ -7,11 +7,13 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <initializer_list>
 #include <mutex>
 
 #include "../../include/hstu_fwd.h"
 #include "common.cuh"
 #include "kernels.h"
+#include "trace.cuh"
 
 using hstu::FwdParams;
 using hstu::TcMaps;
@@ -62,6 +64,12 @@ struct hstu_fwd_plan {
   const void* map_ptrs[6];
   long long map_T, map_Tk, map_pages;
   bool maps_valid;
+  unsigned long long* d_trace;  // pipeline trace buffer (builds with HSTU_TRACE=1 only)
+  long long runs;               // runs enqueued (selects the trace slot)
+  // Completion of the plan's last run (recorded on the run's stream) and a private
+  // non-blocking stream: get_error and destroy wait for the plan's own work only.
+  cudaEvent_t done;
+  cudaStream_t aux;
 };
 
 extern "C" {
@@ -98,7 +106,10 @@ static int key_bound(const hstu_fwd_desc& d) {
 static hstu_status validate_desc(const hstu_fwd_desc* d) {
   if (!d) return HSTU_ERR_INVALID_ARG;
   if (d->reserved) return HSTU_ERR_INVALID_ARG;
-  if (d->is_delta_qk != 0 && d->is_delta_qk != 1) return HSTU_ERR_INVALID_ARG;
+  // flags are 0 or 1
+  for (int f : {d->is_delta_qk, d->index_is_int64, d->has_rab, d->has_num_context,
+                d->has_num_targets})
+    if (f != 0 && f != 1) return HSTU_ERR_INVALID_ARG;
   if (d->page_size != 0 && d->page_size != 32 && d->page_size != 128 && d->page_size != 256)
     return HSTU_ERR_INVALID_ARG;  // Inputs and Outputs table: page_size in {32, 128, 256}
   if (d->max_seqlen_k < 0 || d->max_seqlen_k > hstu::kMaxMTiles * hstu::kTileM ||
@@ -184,16 +195,30 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
   const size_t mtiles = (size_t)hstu::ceil_div(desc->max_seqlen, hstu::kTileM);
   const size_t entries = (size_t)(desc->batch > 0 ? desc->batch : 1) * mtiles;
   P->work_cap = entries;
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&P->done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&P->aux, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaMalloc(&P->d_work, 2 * entries * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMalloc(&P->d_count, 8 * sizeof(int));
   if (e == cudaSuccess) {
     P->d_err = P->d_count + 1;
-    e = cudaMemset(P->d_count, 0, 8 * sizeof(int));
+    e = cudaMemsetAsync(P->d_count, 0, 8 * sizeof(int), P->aux);
   }
-  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+#if HSTU_TRACE
+  if (e == cudaSuccess && P->tensor_cores)
+    e = cudaMalloc(&P->d_trace, hstu::trace::kBufferWords * sizeof(unsigned long long));
+  if (e == cudaSuccess && P->d_trace)
+    e = cudaMemsetAsync(P->d_trace, 0, hstu::trace::kBufferWords * sizeof(unsigned long long),
+                        P->aux);
+#endif
+  // the workspace is zeroed before any run can be enqueued on another stream
+  if (e == cudaSuccess) e = cudaStreamSynchronize(P->aux);
+  if (e == cudaSuccess) e = cudaEventRecord(P->done, P->aux);  // "no run yet" is complete
   if (e != cudaSuccess) {
     cudaFree(P->d_work);
     cudaFree(P->d_count);
+    cudaFree(P->d_trace);
+    if (P->done) cudaEventDestroy(P->done);
+    if (P->aux) cudaStreamDestroy(P->aux);
     delete P;
     return HSTU_ERR_CUDA;
   }
@@ -384,6 +409,11 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   p.silu_scale = silu_scale;
   p.fp8 = d.dtype == HSTU_FP8_E4M3 ? 1 : 0;
   p.test_stall = P->test_stall;
+#if HSTU_TRACE
+  // run r of the plan records into launch slot r % kSlots
+  if (P->d_trace) p.trace = P->d_trace + (size_t)(P->runs % hstu::trace::kSlots) * hstu::trace::kSlotWords;
+  ++P->runs;
+#endif
   if (p.fp8) p.silu_scale = silu_scale / hstu::kP8Scale;  // the kernel's P carries kP8Scale
 
   if (P->tensor_cores) {
@@ -397,6 +427,7 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   cudaError_t e = P->tensor_cores
                       ? hstu::launch_fwd_tc(p, P->maps, d.dtype == HSTU_BF16, P->grid, st, true)
                       : hstu::launch_fwd_simt(p, P->grid, st, true);
+  if (e == cudaSuccess) e = cudaEventRecord(P->done, st);
   return e == cudaSuccess ? HSTU_OK : HSTU_ERR_CUDA;
 }
 
@@ -436,20 +467,44 @@ hstu_status hstu_fwd_run_masked(hstu_fwd_plan* P, const void* q, const void* k, 
 
 hstu_status hstu_fwd_destroy(hstu_fwd_plan* P) {
   if (!P) return HSTU_OK;
-  cudaDeviceSynchronize();
+  // the plan's last run (and with it every earlier one: runs of a plan never overlap)
+  // has finished with the workspace
+  cudaEventSynchronize(P->done);
+  cudaStreamSynchronize(P->aux);
   cudaFree(P->d_work);
   cudaFree(P->d_count);
+  cudaFree(P->d_trace);
+  cudaEventDestroy(P->done);
+  cudaStreamDestroy(P->aux);
   delete P;
+  return HSTU_OK;
+}
+
+hstu_status hstu_fwd_trace_read(hstu_fwd_plan* P, void* host, long long bytes) {
+  if (!P || !host || bytes < 0) return HSTU_ERR_INVALID_ARG;
+  if (!P->d_trace) return HSTU_ERR_UNSUPPORTED;  // not a tracing build, or an fp32 plan
+#if HSTU_TRACE
+  const size_t all = hstu::trace::kBufferWords * sizeof(unsigned long long);
+  const size_t n = (size_t)bytes < all ? (size_t)bytes : all;
+  if (cudaEventSynchronize(P->done) != cudaSuccess ||
+      cudaMemcpyAsync(host, P->d_trace, n, cudaMemcpyDeviceToHost, P->aux) != cudaSuccess ||
+      cudaMemsetAsync(P->d_trace, 0, all, P->aux) != cudaSuccess ||
+      cudaStreamSynchronize(P->aux) != cudaSuccess)
+    return HSTU_ERR_CUDA;
+#endif
   return HSTU_OK;
 }
 
 hstu_status hstu_fwd_get_error(hstu_fwd_plan* P, int* device_error) {
   if (!P || !device_error) return HSTU_ERR_INVALID_ARG;
-  if (cudaDeviceSynchronize() != cudaSuccess) return HSTU_ERR_CUDA;
+  // wait for the plan's last run only (not the whole device), then read and clear the
+  // word on the plan's private stream
+  if (cudaEventSynchronize(P->done) != cudaSuccess) return HSTU_ERR_CUDA;
   int w = 0;
-  if (cudaMemcpy(&w, P->d_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpyAsync(&w, P->d_err, sizeof(int), cudaMemcpyDeviceToHost, P->aux) != cudaSuccess ||
+      cudaMemsetAsync(P->d_err, 0, sizeof(int), P->aux) != cudaSuccess ||
+      cudaStreamSynchronize(P->aux) != cudaSuccess)
     return HSTU_ERR_CUDA;
-  if (cudaMemset(P->d_err, 0, sizeof(int)) != cudaSuccess) return HSTU_ERR_CUDA;
   *device_error = w;
   if (w == HSTU_DEVERR_TIMEOUT) return HSTU_ERR_TIMEOUT;
   if (w != HSTU_DEVERR_NONE) return HSTU_ERR_DEVICE_CHECK;
@@ -584,7 +639,7 @@ cudaError_t noalloc_setup(int dev, const hstu_fwd_desc& d, uint32_t** scratch, i
   if (!(g_noalloc_prepared[dev] & (1u << bit))) {
     cudaError_t e = d.dtype == HSTU_F32
                         ? hstu::simt_prepare()
-                        : hstu::tc_prepare(d.head_dim, d.dtype == HSTU_BF16, d.has_rab, 0);
+                        : hstu::tc_prepare(d.head_dim, d.dtype == HSTU_BF16, d.has_rab ? 1 : 0, 0);
     if (e != cudaSuccess) return e;
     g_noalloc_prepared[dev] |= 1u << bit;
   }

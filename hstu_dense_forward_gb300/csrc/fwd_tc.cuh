@@ -42,6 +42,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace hstu {
 namespace tc {
@@ -59,7 +60,6 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
 // FP8 kernels round kP8Scale * P to E4M3 (the host divides silu_scale by kP8Scale):
 // 16 keeps P values down to 2^-10 in the normal range and saturates only above P = 28.
-constexpr uint32_t kP8ScaleF16x2 = 0x4C004C00u;  // (16.0, 16.0) as f16x2
 
 // F8: q, k, v are FP8 E4M3 (one byte each); the products run as tcgen05 kind::f8f6f4 with
 // P rounded to E4M3; O is written as bf16.
@@ -259,12 +259,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// A packed 16-bit pair as two fp32 values (exact).
 template <bool BF16>
-__device__ __forceinline__ uint32_t tanh2(uint32_t x) {
-  if constexpr (BF16)
-    return ptx::tanh_bf16x2(x);
-  else
-    return ptx::tanh_f16x2(x);
+__device__ __forceinline__ void unpack2(uint32_t w, float& lo, float& hi) {
+  if constexpr (BF16) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  } else {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    lo = f.x;
+    hi = f.y;
+  }
 }
 
 template <bool BF16>
@@ -299,6 +304,7 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       return;
     }
     decode_item<KV>(p, idx, it);
+    HSTU_TRACE_EV(p, trace::kRoleQ, trace::kItem, idx);
     if (!put_item(bars, k, it, p)) return;
     long long nidx = -1;
     if (C::NQ == 1) {
@@ -319,6 +325,7 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 #pragma unroll
     for (int cb = 0; cb < C::NCB; ++cb)
       ptx::tma_load_3d(dst + cb * C::CB_BYTES, tq, full, cb * C::EPC, it.h, it.tq + it.m0);
+    HSTU_TRACE_EV(p, trace::kRoleQ, trace::kLoad, k);
     ++q_it;
     idx = C::NQ == 1 ? nidx : claim();
   }
@@ -397,6 +404,7 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
         if (kt.cached) pg = tile_pages(p, it, kt.x);
       }
       if (!wait_bar(bars, &bars->k_empty[s], ((k_it / C::NK) & 1) ^ 1, p)) return;
+      HSTU_TRACE_EV(p, trace::kRoleK, trace::kLoad, k_it);
       const uint32_t full = ptx::smem_u32(&bars->k_full[s]);
       ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
       const uint32_t dst = sbase + C::OFF_K + s * C::TILE_BYTES;
@@ -458,6 +466,7 @@ __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const 
         if (kt.cached) pg = tile_pages(p, it, kt.x);
       }
       if (!wait_bar(bars, &bars->v_empty[s], ((v_it / C::NV) & 1) ^ 1, p)) return;
+      HSTU_TRACE_EV(p, trace::kRoleV, trace::kLoad, v_it);
       const uint32_t full = ptx::smem_u32(&bars->v_full[s]);
       ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
       const uint32_t dst = sbase + C::OFF_V + s * C::TILE_BYTES;
@@ -600,6 +609,7 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
         break;
       }
       if (!(ready & 2u) && !wait_bar(bars, kfull, kf_par, p)) { ok = false; break; }
+      HSTU_TRACE_EV(p, trace::kRoleS, trace::kIssue, t);
       ptx::tc_fence_after();
       const uint32_t ka = sbase + C::OFF_K + ks * C::TILE_BYTES;
 #pragma unroll
@@ -646,6 +656,7 @@ __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uin
       if (!(ready & 1u) && !wait_bar(bars, pfull, pf_par, p)) { ok = false; break; }
       if (!(ready & 2u) && !wait_bar(bars, vfull, vf_par, p)) { ok = false; break; }
       if (j == 0 && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) { ok = false; break; }
+      HSTU_TRACE_EV(p, trace::kRolePV, trace::kIssue, t);
       ptx::tc_fence_after();
       const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
 #pragma unroll
@@ -740,6 +751,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   // item's first tile has been written, so that the epilogue is not idle while the item's
   // last accumulation completes. The item stays in its ring slot until this returns.
   auto drain = [&](int slot) -> bool {
+    if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+      HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kDrainBeg, slot);
     const Item& pit = bars->info[slot];
     const int pi = pit.m0 + r;  // query row within the sequence
     if (!warp_wait(bars, &bars->o_full, u & 1, p)) return false;
@@ -794,6 +807,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->info_empty[slot]));
+    if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+      HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kDrainEnd, slot);
     return true;
   };
 
@@ -803,6 +818,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     if (!warp_wait(bars, &bars->info_full[slot], (k / kInfoDepth) & 1, p)) return;
     const Item it = bars->info[slot];
     if (it.n_kv < 0) break;  // end marker
+    if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+      HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kItem, k);
     const int m0p = (KV ? it.off : 0) + it.m0;  // key position of the item's first query row
     const int i = m0p + r;                      // and of this thread's row
     const RowRange rr = row_range(it.geom, i, p.mask_type);
@@ -811,6 +828,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       if ((int)(t % C::EPI_GROUPS) != group) continue;  // the other group's tile
       const uint32_t sb = t % C::NSB;                 // == group
       if (!warp_wait(bars, &bars->s_full[sb], (t / C::NSB) & 1, p)) return;
+      if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+        HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kSReady, t);
       ptx::tc_fence_after();
       KeyTile kt;
       if constexpr (KV) {
@@ -849,19 +868,20 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           ptx::tc_fence_before();
           warp_arrive(&bars->s_free[sb], lane);
         }
-        uint32_t pk[16];
+        // h = alpha*s/2 (+ rab/2) in fp32, and silu(2h) = 2h*sigmoid(2h) = h + h*tanh(h): one
+        // special-function op per element (tanh.approx.f32), products and sums on packed
+        // fp32 pairs, P rounded once to the 16-bit type (or to E4M3). A masked entry gets
+        // h = 0, so its P is silu(0) = 0.
+        float h[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          ptx::mul_f32x2(h[e], h[e + 1], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
+                         half_alpha, half_alpha);
+        uint32_t mw[16];  // custom-mask pairs (MASK)
         if constexpr (RAB) {
-          // rab tile: two 64-column TMA boxes of 128 rows x 128 bytes, 128-byte swizzle.
-          // h = alpha*s/2 is rounded to the 16-bit type and rab/2 is added in packed
-          // form (one fused multiply-add per pair); a masked pair half becomes 0. When the
-          // stream carries a custom mask instead, P is multiplied by it after the SiLU.
+          // rab / custom-mask tile: two 64-column TMA boxes of 128 rows x 128 bytes with
+          // 128-byte swizzle, read conflict-free (one row per lane)
           const uint8_t* box = rab_row + (cc >> 6) * (C::RAB_BYTES / 2);
-          uint32_t m = 0xffffffffu;
-          if (!full) {
-            m = chunk_mask(rr, n0 + cc);
-            if constexpr (KV) m &= cols_mask(kt, cc);
-          }
-          const uint32_t half2 = BF16 ? 0x3f003f00u : 0x38003800u;  // (0.5, 0.5)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             const int chunk = (((cc & 63) >> 3) + q4) ^ (r & 7);
@@ -870,46 +890,47 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int c2 = q4 * 4 + e;  // pair index: columns 2*c2, 2*c2 + 1
-              uint32_t h2 = pack2<BF16>(__uint_as_float(sv[2 * c2]) * half_alpha,
-                                        __uint_as_float(sv[2 * c2 + 1]) * half_alpha);
-              if constexpr (!MASK) h2 = fma2<BF16>(ww[e], half2, h2);
-              if (!full) {
-                const uint32_t lo = (m >> (2 * c2)) & 1u, hi = (m >> (2 * c2 + 1)) & 1u;
-                h2 &= (lo * 0x0000ffffu) | (hi * 0xffff0000u);
+              if constexpr (MASK) {
+                mw[c2] = ww[e];
+              } else {
+                float r0, r1;
+                unpack2<BF16>(ww[e], r0, r1);
+                ptx::fma_f32x2(h[2 * c2], h[2 * c2 + 1], r0, r1, 0.5f, 0.5f, h[2 * c2],
+                               h[2 * c2 + 1]);
               }
-              pk[c2] = fma2<BF16>(h2, tanh2<BF16>(h2), h2);
-              // custom mask: P times the mask pair (adding -0 keeps the product exact)
-              if constexpr (MASK) pk[c2] = fma2<BF16>(pk[c2], ww[e], 0x80008000u);
             }
           }
-        } else {
-          float x[32];
+        }
+        if (!full) {
+          // valid columns of this row form [0, hist_end) U [grp_lo, grp_hi]: as a bit mask
+          // over the 32 columns of the chunk
+          uint32_t m = chunk_mask(rr, n0 + cc);
+          if constexpr (KV) m &= cols_mask(kt, cc);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(sv[e]) * half_alpha;
-          // x holds h = alpha*s/2. silu(2h) = 2h*sigmoid(2h) = h*(1 + tanh(h)): a masked
-          // entry gets h = 0, so its P is silu(0) = 0. h is rounded to the 16-bit type,
-          // tanh runs on packed pairs and p = h*t + h is one packed fused multiply-add
-          // that yields P directly.
-          if (!full) {
-            // valid columns of this row form [0, hist_end) U [grp_lo, grp_hi]: as a bit
-            // mask over the 32 columns of the chunk
-            uint32_t m = chunk_mask(rr, n0 + cc);
-            if constexpr (KV) m &= cols_mask(kt, cc);
+          for (int e = 0; e < 32; ++e)
+            if (!(m & (1u << e))) h[e] = 0.f;
+        }
+        uint32_t pk[16];  // 16-bit P pairs, or (F8) E4M3 P quads in pk[0..7]
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (!(m & (1u << e))) x[e] = 0.f;
-          }
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const uint32_t h2 = pack2<BF16>(x[2 * e], x[2 * e + 1]);
-            if constexpr (F8) {
-              // kP8Scale * P = (kP8Scale * h) * tanh(h) + kP8Scale * h: P scaled by a power
-              // of two (exact) so that typical values stay in E4M3's normal range
-              const uint32_t hs = fma2<false>(h2, kP8ScaleF16x2, 0x80008000u);
-              pk[e] = fma2<false>(hs, tanh2<false>(h2), hs);
-            } else {
-              pk[e] = fma2<BF16>(h2, tanh2<BF16>(h2), h2);
-            }
+        for (int e = 0; e < 16; ++e) {
+          const float t0 = ptx::tanh_approx(h[2 * e]), t1 = ptx::tanh_approx(h[2 * e + 1]);
+          float p0, p1;
+          if constexpr (F8) {
+            // kP8Scale * P = (kP8Scale * h) * tanh(h) + kP8Scale * h: P scaled by a power of
+            // two (exact) so that typical values stay in E4M3's normal range
+            float s0, s1;
+            ptx::mul_f32x2(s0, s1, h[2 * e], h[2 * e + 1], kP8Scale, kP8Scale);
+            ptx::fma_f32x2(p0, p1, s0, s1, t0, t1, s0, s1);
+            const uint32_t q = ptx::cvt_e4m3x2_f32(p0, p1);  // keys 2e, 2e + 1
+            if (e & 1)
+              pk[e >> 1] |= q << 16;
+            else
+              pk[e >> 1] = q;
+          } else {
+            ptx::fma_f32x2(p0, p1, h[2 * e], h[2 * e + 1], t0, t1, h[2 * e], h[2 * e + 1]);
+            pk[e] = pack2<BF16>(p0, p1);
+            // custom mask: P times the mask pair (adding -0 keeps the product exact)
+            if constexpr (MASK) pk[e] = fma2<BF16>(pk[e], mw[e], 0x80008000u);
           }
         }
         uint32_t pcol;
@@ -927,8 +948,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           // low byte: the A operand of the kind::f8f6f4 product
           uint32_t p8[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            p8[e] = ptx::cvt_e4m3x2_f16x2(pk[2 * e]) | (ptx::cvt_e4m3x2_f16x2(pk[2 * e + 1]) << 16);
+          for (int e = 0; e < 8; ++e) p8[e] = pk[e];
           ptx::tmem_st8(tmem + lane_off + pcol, p8);
         } else {
           ptx::tmem_st16(tmem + lane_off + pcol, pk);
@@ -938,6 +958,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       warp_arrive(&bars->p_full[sb], lane);
+      if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+        HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kPDone, t);
       // this group's part of the previous item's O, once the item's last P is queued and,
       // with one group, one more P tile behind it (by then the item's last accumulation
       // has finished), or at this group's last tile of the item
@@ -995,6 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     HSTU_INIT_ALL(v_full, 1)
     HSTU_INIT_ALL(v_empty, 1)
 #undef HSTU_INIT_ALL
+    HSTU_TRACE_INIT();
     ptx::mbar_init(ptx::smem_u32(&bars->o_full), 1);
     ptx::mbar_init(ptx::smem_u32(&bars->o_empty), kEpiWarps);
     ptx::mbar_init(ptx::smem_u32(&bars->epi_sync), kEpiWarps);
@@ -1021,6 +1044,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  if (threadIdx.x == 0) {
+    HSTU_TRACE_EV(p, trace::kRoleCta, trace::kStart, 0);
+    HSTU_TRACE_RAW(p, trace::kRoleCta, ptx::globaltimer_ns());
+  }
 
   // The work list is written by the launch before this one. Dependents (the next call's
   // work-list build) are released only after this wait: by then the call before this one,
@@ -1028,6 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::grid_dependency_wait();
   ptx::grid_dependents_launch();
   const long long total = (long long)(*p.work_count) * p.Nq;
+  if (threadIdx.x == 0) HSTU_TRACE_EV(p, trace::kRoleCta, trace::kDepDone, 0);
 
   if (warp < kEpiWarps) {
     epilogue<D, BF16 && !F8, RAB, MASK, KV, F8>(p, bars, smem, tmem, &tm_o, total, warp, lane);
@@ -1054,6 +1082,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) {
+    HSTU_TRACE_EV(p, trace::kRoleCta, trace::kEnd, 0);
+    HSTU_TRACE_RAW(p, trace::kRoleCta, ptx::globaltimer_ns());
+    HSTU_TRACE_FINISH(p);
+  }
   if (bars->abort) {
     // Let TMA copies that were issued but never consumed land before the CTA exits.
     const uint64_t start = ptx::globaltimer_ns();

@@ -48,6 +48,7 @@ struct FwdParams {
   int test_stall;             // watchdog test (plans created with HSTU_TEST_STALL=k): the K
                               // producer signals nothing, so the first score product's wait
                               // runs out and the kernel takes its timeout path
+  unsigned long long* trace;  // pipeline trace buffer (builds with HSTU_TRACE=1), or nullptr
 };
 
 // FP8 kernels hold kP8Scale * P (E4M3) for the second product; silu_scale is divided by it.

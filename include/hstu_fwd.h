@@ -215,12 +215,14 @@ HSTU_API hstu_status hstu_fwd_run_kv(hstu_fwd_plan* plan, const void* q, const v
                                      long long total_tokens, float alpha, float silu_scale,
                                      void* out, void* stream);
 
-/* Free the workspace. NULL is accepted. Synchronises the device first. */
+/* Free the workspace. NULL is accepted. Waits for the plan's last run to complete first
+ * (an event recorded on that run's stream; other streams and plans are not waited for). */
 HSTU_API hstu_status hstu_fwd_destroy(hstu_fwd_plan* plan);
 
-/* Synchronise the device, read the plan's device error word into *device_error
- * (HSTU_DEVERR_*), and clear it. Returns HSTU_ERR_DEVICE_CHECK or
- * HSTU_ERR_TIMEOUT when the word was set, else HSTU_OK. */
+/* Wait for the plan's last run to complete (an event recorded on that run's stream, not a
+ * device-wide synchronisation), read the plan's device error word into *device_error
+ * (HSTU_DEVERR_*), and clear it. Returns HSTU_ERR_DEVICE_CHECK or HSTU_ERR_TIMEOUT when
+ * the word was set, else HSTU_OK. */
 HSTU_API hstu_status hstu_fwd_get_error(hstu_fwd_plan* plan, int* device_error);
 
 /* Kernel launches one hstu_fwd_run enqueues for this plan (for launch accounting). */
@@ -267,14 +269,27 @@ HSTU_API hstu_status hstu_fwd_count_pairs_kv(const hstu_fwd_desc* desc,
  *   - All calls share the one array: calls whose kernels may overlap on the GPU
  *     (different streams without ordering, several host threads) race and produce
  *     wrong results. Serialise them.
- *   - Device-detected input errors (invalid seq_offsets) leave out unwritten but are
- *     not reported back; use a plan and hstu_fwd_get_error when they must be.
+ *   - Nothing detected on the device is reported back: invalid seq_offsets leave out
+ *     unwritten, and a pipeline wait that runs past its limit (HSTU_DEVERR_TIMEOUT on a
+ *     plan) leaves out partly written, while the call still returns HSTU_OK. Use a plan
+ *     and hstu_fwd_get_error when such errors must be seen.
  */
 HSTU_API hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const void* k,
                                           const void* v, const void* seq_offsets, const void* rab,
                                           const void* num_context, const void* num_targets,
                                           long long total_tokens, float alpha, float silu_scale,
                                           void* out, void* stream);
+
+/*
+ * Pipeline trace of the plan's forward kernels (tooling; the source pages have no
+ * counterpart). Only a library built with -DHSTU_TRACE=1 records one: there every
+ * bf16/fp16/FP8 plan owns a 40 MB device buffer of four launch slots (run r of the plan
+ * records into slot r % 4) into which selected threads of each CTA stamp pipeline events
+ * (event kind, tile or item counter, SM clock). This call waits for the plan's last run,
+ * copies min(bytes, 40 MB) of the buffer to the HOST memory at `host`, and clears it. Returns HSTU_ERR_UNSUPPORTED from ordinary builds and
+ * for fp32 plans; HSTU_ERR_INVALID_ARG for a NULL plan or host pointer.
+ */
+HSTU_API hstu_status hstu_fwd_trace_read(hstu_fwd_plan* plan, void* host, long long bytes);
 
 /* Static description of a status code. */
 HSTU_API const char* hstu_status_string(hstu_status status);
