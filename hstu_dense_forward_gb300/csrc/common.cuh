@@ -109,6 +109,19 @@ HSTU_HD bool tile_all_valid(const SeqGeom& s, int m0, int rows, int n0, int cols
   return false;
 }
 
+// Number of leading key tiles of cols columns (from key 0) for which tile_all_valid holds
+// for the rows [m0, m0 + rows): those tiles form a prefix. Tile n is all valid when its last
+// key n*cols + cols - 1 lies below L and, with a causal mask, below H and at or below m0
+// (or, for context rows only, below H): that is n*cols + cols <= E for the E below.
+HSTU_HD int full_tiles(const SeqGeom& s, int m0, int rows, int cols, int mask_type) {
+  int e = s.L;
+  if (mask_type != kMaskNone) {
+    if (s.H < e) e = s.H;
+    if (!(m0 + rows - 1 < s.nc) && m0 + 1 < e) e = m0 + 1;
+  }
+  return e > 0 ? e / cols : 0;
+}
+
 HSTU_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Key tiles of one work item when the keys are a cached history of `hist` positions

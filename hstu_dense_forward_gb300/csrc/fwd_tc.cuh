@@ -95,17 +95,21 @@ struct Cfg {
   static constexpr int EPI_GROUPS = D == 256 ? 2 : 1;
   static constexpr int GROUP_WARPS = kEpiWarps / EPI_GROUPS;
   static constexpr int COLS_PER_WG = kTileN / (kEpiWG / EPI_GROUPS);  // S columns per tile
-  // S buffers in TMEM; P is written over the S buffer it was computed from. D = 256
-  // leaves room for two (O takes 256 columns) and uses one MMA issuer; smaller D use three.
-  // Two S buffers. For D <= 128, P has its own two 64-column buffers after O and an S
-  // buffer is released as soon as the epilogue has loaded it; for D = 256 (O takes 256
+  // TMEM (512 columns). For D <= 128, P has two buffers of its own, O one accumulator and
+  // S two buffers; an S buffer is released as soon as the epilogue has loaded it, so the
+  // next score products overlap the epilogue. (Two O accumulators with one S buffer let an
+  // item's first PV product skip the wait for the previous item's drain, but measured
+  // slower: the single S buffer holds the score products back.) For D = 256 (O takes 256
   // columns) P is written over the S buffer it came from and one thread issues all MMAs.
-  static constexpr int NSB = 2;
   static constexpr bool P_SEP = (D <= 128);
   static constexpr bool SERIAL = !P_SEP;
+  static constexpr int NO = 1;              // O accumulators
+  static constexpr int NPB = 2;             // P buffers (P_SEP), P over S otherwise
+  static constexpr int NSB_FIT = (int)(kTmemCols - NO * D - (P_SEP ? NPB * PW : 0)) / 128;
+  static constexpr int NSB = NSB_FIT < 2 ? NSB_FIT : 2;  // S buffers
   // TMEM columns
-  static constexpr uint32_t S_COL0 = 0, O_COL = NSB * 128;
-  static constexpr uint32_t P_COL0 = O_COL + D;  // P buffers of PW columns (P_SEP only)
+  static constexpr uint32_t S_COL0 = 0, O_COL0 = NSB * 128;
+  static constexpr uint32_t P_COL0 = O_COL0 + NO * D;  // P buffers of PW columns (P_SEP only)
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
@@ -118,7 +122,8 @@ struct Cfg {
   // keep one CTA per SM (TMEM is allocated whole)
   static constexpr int SMEM_BYTES = (SMEM_USED + 1024 < 120 * 1024) ? 120 * 1024 : SMEM_USED + 1024;
   static_assert(SMEM_BYTES <= 232448, "shared memory");
-  static_assert(O_COL + D + (P_SEP ? 2 * PW : 0) <= kTmemCols, "TMEM map");
+  static_assert(NSB >= 1 && P_COL0 + (P_SEP ? NPB * PW : 0) <= kTmemCols, "TMEM map");
+  static_assert(SERIAL ? NSB == NPB : true, "P over S: P buffer = S buffer");
 };
 
 // One work item, decoded once (by the Q producer) and read by every role.
@@ -143,7 +148,7 @@ struct Bars {
   uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
   uint64_t r_full[4], r_empty[4];
   uint64_t s_full[3], p_full[3], pv_done[3], s_free[2];
-  uint64_t o_full, o_empty, drain, epi_sync;
+  uint64_t o_full[2], o_empty[2], drain;
   uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
   Item info[kInfoDepth];
   uint32_t tmem_base;
@@ -188,20 +193,30 @@ __device__ __forceinline__ bool decode_item(const FwdParams& p, long long idx, I
 }
 
 
+// Pause between two tries of a wait, per role (a pausing thread issues no instructions).
+// Measured: pauses of 128 ns for the producers and 32 ns for the MMA issuers cost more
+// (later products) than the issue slots they free, so none is taken.
+constexpr uint32_t kNapProducer = 0, kNapIssuer = 0, kNapNone = 0;  // nanoseconds
+
 // Bounded wait. Returns false when this CTA is aborting (own timeout or another role's).
+// try_wait suspends the thread in hardware until the phase completes or a short system
+// limit passes; the abort flag and the clock are checked every 16 tries only.
+template <uint32_t NAP = kNapProducer>
 __device__ __forceinline__ bool wait_bar(Bars* bars, uint64_t* bar, uint32_t parity,
                                          const FwdParams& p) {
   const uint32_t a = ptx::smem_u32(bar);
   if (ptx::mbar_try_wait(a, parity)) return true;
   const uint64_t start = ptx::globaltimer_ns();
-  for (;;) {
-    // sleep until the phase flips (or 20 us pass), then check the abort flag and clock
-    if (ptx::mbar_try_wait_sleep(a, parity, 20000u)) return true;
-    if (bars->abort) return false;
-    if ((long long)(ptx::globaltimer_ns() - start) > p.timeout_ns) {
-      bars->abort = 1;
-      atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_TIMEOUT);
-      return false;
+  for (uint32_t i = 1;; ++i) {
+    if constexpr (NAP > 0) __nanosleep(NAP);
+    if (ptx::mbar_try_wait(a, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (bars->abort) return false;
+      if ((long long)(ptx::globaltimer_ns() - start) > p.timeout_ns) {
+        bars->abort = 1;
+        atomicCAS(p.err, HSTU_DEVERR_NONE, HSTU_DEVERR_TIMEOUT);
+        return false;
+      }
     }
   }
 }
@@ -210,7 +225,7 @@ __device__ __forceinline__ bool wait_bar(Bars* bars, uint64_t* bar, uint32_t par
 // together, so the .sync.aligned tcgen05 loads/stores that follow stay converged.
 __device__ __forceinline__ bool warp_wait(Bars* bars, uint64_t* bar, uint32_t parity,
                                           const FwdParams& p) {
-  const bool ok = wait_bar(bars, bar, parity, p);
+  const bool ok = wait_bar<kNapNone>(bars, bar, parity, p);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -226,9 +241,10 @@ __device__ __forceinline__ bool put_item(Bars* bars, int k, const Item& it, cons
 }
 
 // Single-thread reader.
+template <uint32_t NAP = kNapProducer>
 __device__ __forceinline__ bool get_item(Bars* bars, int k, Item& it, const FwdParams& p) {
   const int s = k % kInfoDepth;
-  if (!wait_bar(bars, &bars->info_full[s], (k / kInfoDepth) & 1, p)) return false;
+  if (!wait_bar<NAP>(bars, &bars->info_full[s], (k / kInfoDepth) & 1, p)) return false;
   it = bars->info[s];
   ptx::mbar_arrive(ptx::smem_u32(&bars->info_empty[s]));
   return true;
@@ -516,10 +532,10 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
   uint32_t q_it = 0, k_it = 0, v_it = 0, u = 0, t_base = 0;
   auto issue_s = [&](uint32_t t, int qs) -> bool {
     const uint32_t sb = t % C::NSB;
-    if (t >= C::NSB && !wait_bar(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p))
+    if (t >= C::NSB && !wait_bar<kNapIssuer>(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p))
       return false;
     const int ks = k_it % C::NK;
-    if (!wait_bar(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) return false;
+    if (!wait_bar<kNapIssuer>(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) return false;
     ptx::tc_fence_after();
     const uint32_t qa = sbase + C::OFF_Q + qs * C::TILE_BYTES;
     const uint32_t ka = sbase + C::OFF_K + ks * C::TILE_BYTES;
@@ -538,8 +554,8 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
   auto issue_pv = [&](uint32_t t, bool first) -> bool {
     const uint32_t sb = t % C::NSB;
     const int vs = v_it % C::NV;
-    if (!wait_bar(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) return false;
-    if (first && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) return false;
+    if (!wait_bar<kNapIssuer>(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) return false;
+    if (first && !wait_bar<kNapIssuer>(bars, &bars->o_empty[0], (u & 1) ^ 1, p)) return false;
     ptx::tc_fence_after();
     const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
 #pragma unroll
@@ -547,7 +563,7 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
       const uint32_t pcol = C::S_COL0 + sb * 128 + (16 * kk / C::COLS_PER_WG) * C::COLS_PER_WG +
                             ((16 * kk) % C::COLS_PER_WG) / 2;
       const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
-      ptx::mma_ts(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (!first || kk > 0) ? 1u : 0u);
+      ptx::mma_ts(tmem + C::O_COL0, tmem + pcol, bd, IDESC_O, (!first || kk > 0) ? 1u : 0u);
     }
     ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
     ptx::mma_commit(ptx::smem_u32(&bars->pv_done[sb]));
@@ -556,15 +572,15 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
   };
   for (int k = 0;; ++k) {
     Item it;
-    if (!get_item(bars, k, it, p) || it.n_kv < 0) break;
+    if (!get_item<kNapIssuer>(bars, k, it, p) || it.n_kv < 0) break;
     const int qs = q_it % C::NQ;
-    if (!wait_bar(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) break;
+    if (!wait_bar<kNapIssuer>(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) break;
     const int n = it.n_kv;
     bool ok = issue_s(t_base, qs) && (n < 2 || issue_s(t_base + 1, qs));
     if (ok && n <= 2) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
     for (int j = 0; j < n && ok; ++j) {
       const uint32_t t = t_base + j;
-      ok = wait_bar(bars, &bars->p_full[t % C::NSB], (t / C::NSB) & 1, p) && issue_pv(t, j == 0);
+      ok = wait_bar<kNapIssuer>(bars, &bars->p_full[t % C::NSB], (t / C::NSB) & 1, p) && issue_pv(t, j == 0);
       if (ok && j + 2 < n) {
         ok = issue_s(t + 2, qs);
         if (ok && j + 3 == n) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
@@ -572,7 +588,7 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
     }
     if (!ok) break;
     t_base += n;
-    ptx::mma_commit(ptx::smem_u32(&bars->o_full));
+    ptx::mma_commit(ptx::smem_u32(&bars->o_full[0]));
     ++q_it;
     ++u;
   }
@@ -589,10 +605,11 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
   uint32_t q_it = 0, k_it = 0, t = 0;
   for (int k = 0;; ++k) {
     Item it;
-    if (!get_item(bars, k, it, p) || it.n_kv < 0) break;
+    if (!get_item<kNapIssuer>(bars, k, it, p) || it.n_kv < 0) break;
     const int qs = q_it % C::NQ;
-    if (!wait_bar(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) break;
-    const uint32_t qa = sbase + C::OFF_Q + qs * C::TILE_BYTES;
+    if (!wait_bar<kNapIssuer>(bars, &bars->q_full[qs], (q_it / C::NQ) & 1, p)) break;
+    const uint64_t ad0 =
+        ptx::smem_desc(sbase + C::OFF_Q + qs * C::TILE_BYTES, 16, 8 * C::SWB, C::SWZ);
     bool ok = true;
     for (int j = 0; j < it.n_kv && ok; ++j, ++t) {
       const uint32_t sb = t % C::NSB;
@@ -604,20 +621,21 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
       const uint32_t sf_par = ((t / C::NSB) & 1) ^ 1, kf_par = (k_it / C::NK) & 1;
       const uint32_t ready = ptx::mbar_test2(ptx::smem_u32(sfree), sf_par, ptx::smem_u32(kfull),
                                              kf_par);
-      if (!(ready & 1u) && t >= C::NSB && !wait_bar(bars, sfree, sf_par, p)) {
+      if (!(ready & 1u) && t >= C::NSB && !wait_bar<kNapIssuer>(bars, sfree, sf_par, p)) {
         ok = false;
         break;
       }
-      if (!(ready & 2u) && !wait_bar(bars, kfull, kf_par, p)) { ok = false; break; }
+      if (!(ready & 2u) && !wait_bar<kNapIssuer>(bars, kfull, kf_par, p)) { ok = false; break; }
       HSTU_TRACE_EV(p, trace::kRoleS, trace::kIssue, t);
       ptx::tc_fence_after();
-      const uint32_t ka = sbase + C::OFF_K + ks * C::TILE_BYTES;
+      const uint64_t bd0 =
+          ptx::smem_desc(sbase + C::OFF_K + ks * C::TILE_BYTES, 16, 8 * C::SWB, C::SWZ);
 #pragma unroll
       for (int kk = 0; kk < D / C::KS; ++kk) {  // K steps of 32 bytes
         const int e = kk * C::KS;
         const uint32_t off = (e / C::EPC) * C::CB_BYTES + (e % C::EPC) * C::EB;
-        const uint64_t ad = ptx::smem_desc(qa + off, 16, 8 * C::SWB, C::SWZ);
-        const uint64_t bd = ptx::smem_desc(ka + off, 16, 8 * C::SWB, C::SWZ);
+        const uint64_t ad = ptx::desc_add(ad0, off);
+        const uint64_t bd = ptx::desc_add(bd0, off);
         if constexpr (F8)
           ptx::mma_ss_f8(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
         else
@@ -643,39 +661,45 @@ __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uin
   uint32_t v_it = 0, t = 0, u = 0;
   for (int k = 0;; ++k) {
     Item it;
-    if (!get_item(bars, k, it, p) || it.n_kv < 0) break;
+    if (!get_item<kNapIssuer>(bars, k, it, p) || it.n_kv < 0) break;
     bool ok = true;
     for (int j = 0; j < it.n_kv; ++j, ++t) {
-      const uint32_t sb = t % C::NSB;
+      const uint32_t pb = t % C::NPB;  // P buffer
+      const uint32_t ob = u % C::NO;   // O accumulator of this item
       const int vs = v_it % C::NV;
-      uint64_t* pfull = &bars->p_full[sb];
+      uint64_t* pfull = &bars->p_full[pb];
       uint64_t* vfull = &bars->v_full[vs];
-      const uint32_t pf_par = (t / C::NSB) & 1, vf_par = (v_it / C::NV) & 1;
+      const uint32_t pf_par = (t / C::NPB) & 1, vf_par = (v_it / C::NV) & 1;
       const uint32_t ready = ptx::mbar_test2(ptx::smem_u32(pfull), pf_par, ptx::smem_u32(vfull),
                                              vf_par);
-      if (!(ready & 1u) && !wait_bar(bars, pfull, pf_par, p)) { ok = false; break; }
-      if (!(ready & 2u) && !wait_bar(bars, vfull, vf_par, p)) { ok = false; break; }
-      if (j == 0 && !wait_bar(bars, &bars->o_empty, (u & 1) ^ 1, p)) { ok = false; break; }
+      if (!(ready & 1u) && !wait_bar<kNapIssuer>(bars, pfull, pf_par, p)) { ok = false; break; }
+      if (!(ready & 2u) && !wait_bar<kNapIssuer>(bars, vfull, vf_par, p)) { ok = false; break; }
+      if (j == 0 && !wait_bar<kNapIssuer>(bars, &bars->o_empty[ob], ((u / C::NO) & 1) ^ 1, p)) {
+        ok = false;
+        break;
+      }
       HSTU_TRACE_EV(p, trace::kRolePV, trace::kIssue, t);
       ptx::tc_fence_after();
-      const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
+      const uint64_t bd0 = ptx::smem_desc(sbase + C::OFF_V + vs * C::TILE_BYTES, C::CB_BYTES,
+                                          8 * C::SWB, C::SWZ);
 #pragma unroll
       for (int kk = 0; kk < kTileN / C::KS; ++kk) {
         // keys [KS*kk, KS*kk + KS) are packed in P columns [8kk, 8kk + 8) (2 or 4 per column)
-        const uint32_t pcol = C::P_COL0 + sb * C::PW + kk * 8;
-        const uint64_t bd =
-            ptx::smem_desc(va + kk * C::KS * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
+        const uint32_t pcol = C::P_COL0 + pb * C::PW + kk * 8;
+        const uint64_t bd = ptx::desc_add(bd0, kk * C::KS * C::SWB);
         if constexpr (F8)
-          ptx::mma_ts_f8(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_ts_f8(tmem + C::O_COL0 + ob * D, tmem + pcol, bd, IDESC_O,
+                         (j > 0 || kk > 0) ? 1u : 0u);
         else
-          ptx::mma_ts(tmem + C::O_COL, tmem + pcol, bd, IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_ts(tmem + C::O_COL0 + ob * D, tmem + pcol, bd, IDESC_O,
+                      (j > 0 || kk > 0) ? 1u : 0u);
       }
       ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
-      ptx::mma_commit(ptx::smem_u32(&bars->pv_done[sb]));
+      ptx::mma_commit(ptx::smem_u32(&bars->pv_done[pb]));
       ++v_it;
     }
     if (!ok) break;
-    ptx::mma_commit(ptx::smem_u32(&bars->o_full));
+    ptx::mma_commit(ptx::smem_u32(&bars->o_full[u % C::NO]));
     ++u;
   }
   mma_drain(bars, p);
@@ -700,10 +724,11 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
   ptx::tmem_ld32(taddr, r);
 }
 
-// Per-warp arrive: every lane has finished its part (and fenced its tcgen05 ops).
+// Every lane of the warp arrives once, after its own part (and its tcgen05 fence): one
+// warp instruction and no divergent branch; the barrier counts 32 arrivals per warp.
 __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
-  __syncwarp();
-  if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
+  (void)lane;
+  ptx::mbar_arrive(ptx::smem_u32(bar));
 }
 
 // Byte offset of a 16-byte chunk inside a TMA box written with SWB-byte swizzling
@@ -716,15 +741,6 @@ __device__ __forceinline__ uint32_t swizzle(uint32_t o) {
     constexpr uint32_t mask = SWB == 128 ? 0x70u : (SWB == 64 ? 0x30u : 0x10u);
     return o ^ ((o >> 3) & mask);
   }
-}
-
-// Barrier among the epilogue warps (bounded: an mbarrier rather than bar.sync).
-__device__ __forceinline__ bool epi_barrier(Bars* bars, uint32_t& phase, const FwdParams& p,
-                                            int lane) {
-  warp_arrive(&bars->epi_sync, lane);
-  const bool ok = warp_wait(bars, &bars->epi_sync, phase & 1, p);
-  ++phase;
-  return ok;
 }
 
 template <int D, bool BF16, bool RAB, bool MASK, bool KV, bool F8>
@@ -755,7 +771,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kDrainBeg, slot);
     const Item& pit = bars->info[slot];
     const int pi = pit.m0 + r;  // query row within the sequence
-    if (!warp_wait(bars, &bars->o_full, u & 1, p)) return false;
+    const uint32_t ob = u % C::NO;  // the item's O accumulator
+    if (!warp_wait(bars, &bars->o_full[ob], (u / C::NO) & 1, p)) return false;
     ptx::tc_fence_after();
     uint8_t* stage = smem + C::OFF_O + warp * C::WARP_STAGE;
     if constexpr (C::STAGE) {
@@ -766,14 +783,22 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 #pragma unroll
     for (int c0 = 0; c0 < OC; c0 += OCH) {
       uint32_t part[OCH];
-      tmem_ld<OCH>(tmem + lane_off + C::O_COL + wg * OC + c0, part);
+      tmem_ld<OCH>(tmem + lane_off + C::O_COL0 + ob * D + wg * OC + c0, part);
+      if constexpr (OC == OCH) {
+        // the whole O slice is in registers: hand the accumulator back before converting
+        ptx::tc_fence_before();
+        warp_arrive(&bars->o_empty[ob], lane);
+      }
 #pragma unroll
       for (int v4 = 0; v4 < OCH / 8; ++v4) {
         uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          w[e] = pack2<OUT_BF16>(__uint_as_float(part[v4 * 8 + 2 * e]) * p.silu_scale,
-                                 __uint_as_float(part[v4 * 8 + 2 * e + 1]) * p.silu_scale);
+        for (int e = 0; e < 4; ++e) {
+          float o0, o1;
+          ptx::mul_f32x2(o0, o1, __uint_as_float(part[v4 * 8 + 2 * e]),
+                         __uint_as_float(part[v4 * 8 + 2 * e + 1]), p.silu_scale, p.silu_scale);
+          w[e] = pack2<OUT_BF16>(o0, o1);
+        }
         if constexpr (C::STAGE) {
           // this warp's 32-row x (D/4)-column block in the TMA box layout: swizzled 16-byte
           // chunks, conflict-free for one row per lane
@@ -784,8 +809,10 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         }
       }
     }
-    ptx::tc_fence_before();
-    warp_arrive(&bars->o_empty, lane);
+    if constexpr (OC != OCH) {
+      ptx::tc_fence_before();
+      warp_arrive(&bars->o_empty[ob], lane);
+    }
     ++u;
     if constexpr (C::STAGE) {
       // one TMA store when all 32 rows of the block lie inside the sequence; a block that
@@ -823,10 +850,12 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     const int m0p = (KV ? it.off : 0) + it.m0;  // key position of the item's first query row
     const int i = m0p + r;                      // and of this thread's row
     const RowRange rr = row_range(it.geom, i, p.mask_type);
+    // without a key side, the key tiles that need no mask are a prefix of the item's tiles
+    const int n_full = KV ? 0 : full_tiles(it.geom, m0p, kTileM, kTileN, p.mask_type);
     int gtile = 0;  // tiles of this item processed by this group
     for (int j = 0; j < it.n_kv; ++j, ++t) {
       if ((int)(t % C::EPI_GROUPS) != group) continue;  // the other group's tile
-      const uint32_t sb = t % C::NSB;                 // == group
+      const uint32_t sb = t % C::NSB;  // S buffer (== group with two epilogue groups)
       if (!warp_wait(bars, &bars->s_full[sb], (t / C::NSB) & 1, p)) return;
       if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
         HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kSReady, t);
@@ -841,8 +870,12 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         kt.cached = false;
       }
       const int n0 = kt.x * kTileN;
-      const bool full = (!KV || (kt.clo == 0 && kt.chi == kTileN)) &&
-                        tile_all_valid(it.geom, m0p, kTileM, n0, kTileN, p.mask_type);
+      bool full;
+      if constexpr (KV)
+        full = kt.clo == 0 && kt.chi == kTileN &&
+               tile_all_valid(it.geom, m0p, kTileM, n0, kTileN, p.mask_type);
+      else
+        full = j < n_full;
       const uint8_t* rab_row = nullptr;
       int rs = 0;
       if constexpr (RAB) {
@@ -935,11 +968,12 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         }
         uint32_t pcol;
         if constexpr (C::P_SEP) {
-          // P buffer sb is free once PV(t - NSB) has read it
-          if (c == 0 && t >= C::NSB &&
-              !warp_wait(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p))
+          // P buffer t % NPB is free once PV(t - NPB) has read it
+          const uint32_t pb = t % C::NPB;
+          if (c == 0 && t >= C::NPB &&
+              !warp_wait(bars, &bars->pv_done[pb], ((t / C::NPB) & 1) ^ 1, p))
             return;
-          pcol = C::P_COL0 + sb * C::PW + cc / (C::PW == 64 ? 2 : 4);
+          pcol = C::P_COL0 + pb * C::PW + cc / (C::PW == 64 ? 2 : 4);
         } else {
           pcol = C::S_COL0 + sb * 128 + col + c * 16;  // over S columns already read
         }
@@ -957,14 +991,14 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       if constexpr (RAB) warp_arrive(&bars->r_empty[rs], lane);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
-      warp_arrive(&bars->p_full[sb], lane);
+      warp_arrive(&bars->p_full[t % C::NPB], lane);
       if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
         HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kPDone, t);
-      // this group's part of the previous item's O, once the item's last P is queued and,
-      // with one group, one more P tile behind it (by then the item's last accumulation
-      // has finished), or at this group's last tile of the item
+      // this group's part of the previous item's O, after the group's first tile of this
+      // item (P of a whole tile behind the item's last accumulation, which has finished
+      // by then), or at the group's last tile of the item
       ++gtile;
-      if (prev_slot >= 0 && (gtile == (C::EPI_GROUPS == 1 ? 2 : 1) || j + C::EPI_GROUPS >= it.n_kv)) {
+      if (prev_slot >= 0 && (gtile == 1 || j + C::EPI_GROUPS >= it.n_kv)) {
         if (!drain(prev_slot)) return;
         prev_slot = -1;
       }
@@ -1002,25 +1036,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #define HSTU_INIT_ALL(arr, count)                                       \
   for (int s = 0; s < (int)(sizeof(bars->arr) / sizeof(uint64_t)); ++s) \
     ptx::mbar_init(ptx::smem_u32(&bars->arr[s]), (count));
-    // the warps of the epilogue group that owns an S / P buffer arrive on s_free, p_full
-    // and r_empty
-    HSTU_INIT_ALL(s_free, C::GROUP_WARPS)
+    // every lane of the epilogue group that owns an S / P buffer arrives on s_free, p_full
+    // and r_empty (and every epilogue lane on o_empty)
+    HSTU_INIT_ALL(s_free, C::GROUP_WARPS * 32)
     HSTU_INIT_ALL(s_full, 1)
-    HSTU_INIT_ALL(p_full, C::GROUP_WARPS)
+    HSTU_INIT_ALL(p_full, C::GROUP_WARPS * 32)
     HSTU_INIT_ALL(pv_done, 1)
     HSTU_INIT_ALL(q_full, 1)
     HSTU_INIT_ALL(q_empty, 1)
     HSTU_INIT_ALL(r_full, 1)
-    HSTU_INIT_ALL(r_empty, C::GROUP_WARPS)
+    HSTU_INIT_ALL(r_empty, C::GROUP_WARPS * 32)
     HSTU_INIT_ALL(k_full, 1)
     HSTU_INIT_ALL(k_empty, 1)
     HSTU_INIT_ALL(v_full, 1)
     HSTU_INIT_ALL(v_empty, 1)
+    HSTU_INIT_ALL(o_full, 1)
+    HSTU_INIT_ALL(o_empty, kEpiWarps * 32)
 #undef HSTU_INIT_ALL
     HSTU_TRACE_INIT();
-    ptx::mbar_init(ptx::smem_u32(&bars->o_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&bars->o_empty), kEpiWarps);
-    ptx::mbar_init(ptx::smem_u32(&bars->epi_sync), kEpiWarps);
     ptx::mbar_init(ptx::smem_u32(&bars->drain), C::SERIAL ? 1 : 2);  // one commit per issuer
     for (int s = 0; s < kInfoDepth; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->info_full[s]), 1);
