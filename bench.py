@@ -232,11 +232,159 @@ def _algorithmic_bytes(w, inp, pairs_per_head):
     return qo + kv + rab
 
 
+def time_windows(step, sets, steps, min_windows=10, min_seconds=1.0, stream=None):
+    """Per-step milliseconds of repeated timed windows: each window is `steps` calls (inputs
+    rotating over `sets`) between CUDA events on the launching stream, with a synchronize
+    on both sides; windows repeat until at least `min_windows` ran and `min_seconds` of
+    calls were timed."""
+    out = []
+    total = 0.0
+    i = 0
+    while len(out) < min_windows or total < min_seconds:
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step(sets[i % len(sets)])
+            i += 1
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        out.append(ms / steps)
+        total += ms * 1e-3
+    return out
+
+
+def _input_sets(w, inp, dev, W, out_dtype):
+    set_bytes = sum(t.numel() * t.element_size() for t in
+                    (inp["q"], inp["k"], inp["v"], inp["rab"], inp.get("kv_cache"))
+                    if t is not None) + inp["q"].numel() * inp["q"].element_size()  # + out
+    nsets = max(3, -(-3 * L2_BYTES // max(set_bytes, 1)))
+    nsets = min(nsets, 8)
+    sets = []
+    for _ in range(nsets):
+        d = W.to_device(inp, dev)
+        d["out"] = torch.empty(d["q"].shape, dtype=out_dtype(d["q"].dtype), device=dev)
+        sets.append(d)
+    return sets, set_bytes
+
+
+def _step_fn(kv_side):
+    from hstu_dense_forward_gb300 import hstu_fwd
+
+    def step(d):
+        kv = {k: d[k] for k in KV_KEYS} if kv_side else {}
+        if kv_side:
+            kv["max_seqlen_k"] = d["max_seqlen_k"]
+        hstu_fwd(d["q"], d["k"], d["v"], d["seq_offsets"], max_seqlen=d["max_seqlen"],
+                 rab=d["rab"], num_context=d["num_context"], num_targets=d["num_targets"],
+                 causal=d["causal"], target_group_size=d["target_group_size"], alpha=d["alpha"],
+                 silu_scale=d["silu_scale"], out=d["out"], **kv)
+    return step
+
+
+def _roofline(w, inp, pairs, flops, ms_per_step, peaks, traffic):
+    """The dominant bound of a workload: tensor (TFLOP/s) for the contractions, HBM
+    (algorithmic GB/s) for rab and for key sides read from a paged cache."""
+    achieved = flops / (ms_per_step * 1e-3) / 1e12
+    timed = "CUDA events around each call: work-list build + forward kernel"
+    if w.dtype == "fp32":
+        # the CUDA-core path (FFMA): reported against the bf16 tensor peak for scale only
+        return {"bound": "latency", "achieved": round(achieved, 4), "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16"], 6),
+                "traffic": traffic, "peak_source": peaks["source"], "timed": timed,
+                "note": "fp32 CUDA-core path on a 40-token input: launch-latency bound"}
+    if _is_kv(w):
+        gbs = _algorithmic_bytes_kv(w, inp) / (ms_per_step * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm"], 4), "traffic": traffic,
+                "algorithmic_bytes": _algorithmic_bytes_kv(w, inp),
+                "peak_source": peaks["source"], "tensor_tflops": round(achieved, 2),
+                "timed": timed}
+    if w.rab:
+        ab = _algorithmic_bytes(w, inp, pairs)
+        gbs = ab / (ms_per_step * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(gbs / peaks["hbm"], 4), "frac_of_8tbs": round(gbs / 8000.0, 4),
+                "traffic": traffic, "algorithmic_bytes": ab, "peak_source": peaks["source"],
+                "tensor_tflops": round(achieved, 2), "timed": timed}
+    # an FP8 contraction: the bf16 peak times the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
+    tpeak = peaks["bf16"] * (2.0 if w.dtype == "fp8" else 1.0)
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": tpeak, "unit": "TFLOP/s",
+            "frac": round(achieved / tpeak, 4),
+            "frac_of_sustained": round(achieved / (peaks["bf16_sustained"] *
+                                                   (2.0 if w.dtype == "fp8" else 1.0)), 4),
+            "traffic": traffic,
+            "peak_source": peaks["source"] + (" x 2 (fp8 / bf16 nominal)" if w.dtype == "fp8"
+                                              else ""),
+            "timed": timed}
+
+
+def measure(w, args, dev, ws, peaks, clocks=False):
+    """Time one workload on this rank (inputs resident in HBM, rotating sets larger than
+    L2): returns the per-step times of every window and the derived numbers."""
+    from hstu_dense_forward_gb300 import out_dtype, useful_flops
+    from hstu_dense_forward_gb300 import workloads as W
+
+    kv_side = _is_kv(w)
+    inp = _generate(w)
+    pairs = _pairs(w, inp)
+    flops = useful_flops(pairs, w.head_dim)
+    sets, set_bytes = _input_sets(w, inp, dev, W, out_dtype)
+    step = _step_fn(kv_side)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(args.warmup):
+        step(sets[i % len(sets)])
+    torch.cuda.synchronize()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    clk = ClockSampler(dev.index if dev.index is not None else 0) if clocks else None
+    if clk:
+        clk.__enter__()
+    try:
+        win = time_windows(step, sets, args.steps, args.windows, args.min_seconds, stream)
+    finally:
+        if clk:
+            clk.__exit__(None, None, None)
+    med = reduce_over_ranks(statistics.median(win), ws, dev)
+    mn = reduce_over_ranks(min(win), ws, dev)
+    traffic = args.traffic if (args.traffic is not None and w.name == args.workload) else \
+        stored_traffic(w.name)
+    return dict(w=w, inp=inp, pairs=pairs, flops=flops, sets=sets, set_bytes=set_bytes,
+                step=step, windows=win, ms_median=med, ms_min=mn,
+                value=flops * ws / (med * 1e-3) / 1e12,
+                roofline=_roofline(w, inp, pairs, flops, med, peaks, traffic),
+                clocks=clk.summary() if clk else None)
+
+
+def _config(w, inp, m, ws):
+    kv_side = _is_kv(w)
+    return {"workload": w.name, "batch": w.batch, "max_seqlen": w.max_seqlen,
+            "heads_q": w.num_heads_q, "heads_kv": w.num_heads_kv, "head_dim": w.head_dim,
+            "mask": "causal" if w.causal else "none", "rab": w.rab,
+            "tokens": int(inp["seq_offsets"][-1]),
+            **({"keys": int((inp["seq_offsets_k"][1:] - inp["seq_offsets_k"][:-1]).sum()
+                            + inp["history"].sum()),
+                "cached_keys": int(inp["history"].sum()), "page_size": w.page_size,
+                "max_seqlen_k": w.max_seqlen_k} if kv_side else {}),
+            "valid_pairs": m["pairs"], "useful_gflop_per_step": round(m["flops"] / 1e9, 6),
+            "l2": f"rotating {len(m['sets'])} input sets of {m['set_bytes'] / 2**20:.0f} MiB "
+                  "(> L2)",
+            "parallelism": f"replicas x{ws}"}
+
+
+# Configurations timed in the same run next to the headline one (the other four
+# configurations of the workload list): parity-test cases that also get a line of numbers.
+EXTRA_WORKLOADS = ("fp32_tiny", "bf16_rab_b16_s1024_h8_d64", "fp16_gqa8x2_targets_b8_s4096_d128",
+                   "bf16_long_b4_s8192_h4_d256")
+
+
 def run_ours(args):
     import numpy as np  # noqa: F401
 
     from hstu_dense_forward_gb300 import build as B
-    from hstu_dense_forward_gb300 import hstu_fwd, out_dtype, useful_flops
+    from hstu_dense_forward_gb300 import out_dtype
     from hstu_dense_forward_gb300 import workloads as W
 
     ws, rank, local = _dist()
@@ -249,50 +397,14 @@ def run_ours(args):
         B.build()
     if ws > 1:
         dist.barrier()
+    peaks = _peaks()
     w = _workload(args.workload)
     kv_side = _is_kv(w)
-    inp = _generate(w)
-    pairs = _pairs(w, inp)
-    flops = useful_flops(pairs, w.head_dim)
-    set_bytes = sum(t.numel() * t.element_size() for t in
-                    (inp["q"], inp["k"], inp["v"], inp["rab"], inp.get("kv_cache"))
-                    if t is not None) + inp["q"].numel() * inp["q"].element_size()  # + out
-    nsets = max(3, -(-3 * L2_BYTES // max(set_bytes, 1)))
-    nsets = min(nsets, 8)
-    sets = []
-    for s in range(nsets):
-        d = W.to_device(inp, dev)
-        d["out"] = torch.empty(d["q"].shape, dtype=out_dtype(d["q"].dtype), device=dev)
-        sets.append(d)
+    m = measure(w, args, dev, ws, peaks, clocks=True)
+    inp, flops, step = m["inp"], m["flops"], m["step"]
+    ms_per_step = m["ms_median"]
+    value = m["value"]
     stream = torch.cuda.current_stream(dev)
-
-    def step(d):
-        kv = {k: d[k] for k in KV_KEYS} if kv_side else {}
-        if kv_side:
-            kv["max_seqlen_k"] = d["max_seqlen_k"]
-        hstu_fwd(d["q"], d["k"], d["v"], d["seq_offsets"], max_seqlen=d["max_seqlen"],
-                 rab=d["rab"], num_context=d["num_context"], num_targets=d["num_targets"],
-                 causal=d["causal"], target_group_size=d["target_group_size"], alpha=d["alpha"],
-                 silu_scale=d["silu_scale"], out=d["out"], **kv)
-
-    for i in range(args.warmup):
-        step(sets[i % nsets])
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for i in range(args.steps):
-            step(sets[i % nsets])
-        ev1.record(stream)
-        torch.cuda.synchronize()
-    ms = reduce_over_ranks(ev0.elapsed_time(ev1), ws, dev)
-    if ws > 1:
-        dist.barrier()
-    ms_per_step = ms / args.steps
-    value = aggregate_value(flops, args.steps, ws, ms)
 
     # end to end through the public API: pinned host inputs -> device -> forward -> host,
     # every step. The copies run on their own streams, double-buffered, so that the H2D
@@ -348,74 +460,80 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_value = flops * ws / (e2e_ms * 1e-3) / 1e12
+    del bufs, outs_h, host
 
-    peaks = _peaks()
-    traffic = args.traffic if args.traffic is not None else stored_traffic(w.name)
-    achieved = flops / (ms_per_step * 1e-3) / 1e12
-    # an FP8 contraction: the bf16 peak times the nominal dense fp8 / bf16 ratio (4.5 / 2.25)
-    tpeak = peaks["bf16"] * (2.0 if w.dtype == "fp8" else 1.0)
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tpeak,
-                "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
-                "traffic": traffic,
-                "peak_source": peaks["source"] + (" x 2 (fp8 / bf16 nominal)" if w.dtype == "fp8"
-                                                  else ""),
-                "timed": "CUDA events around each call: work-list build + forward kernel"}
-    if kv_side:
-        # a few queries against long cached histories: every key is read once per call
-        gbs = _algorithmic_bytes_kv(w, inp) / (ms_per_step * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
-                    "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4), "traffic": traffic,
-                    "algorithmic_bytes": _algorithmic_bytes_kv(w, inp),
-                    "peak_source": peaks["source"], "tensor_tflops": round(achieved, 2),
-                    "timed": "CUDA events around each call: work-list build + forward kernel"}
-    elif w.rab:
-        gbs = _algorithmic_bytes(w, inp, pairs // w.num_heads_q * w.num_heads_q) / (
-            ms_per_step * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
-                    "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4), "traffic": traffic,
-                    "peak_source": peaks["source"],
-                    "timed": "CUDA events around each call: work-list build + forward kernel"}
+    # the other configurations, one GPU only (their CPU baselines are rank 0's anyway)
+    extra = {}
+    if ws == 1 and not args.no_workloads:
+        for name in EXTRA_WORKLOADS:
+            if name == w.name:
+                continue
+            we = _workload(name)
+            me = measure(we, args, dev, ws, peaks, clocks=True)
+            extra[name] = {
+                "value": round(me["value"], 4), "unit": "TFLOP/s",
+                "ms_per_step": round(me["ms_median"], 5), "ms_per_step_min": round(me["ms_min"], 5),
+                "windows": len(me["windows"]), "steps_per_window": args.steps,
+                "dtype": we.dtype, "config": _config(we, me["inp"], me, ws),
+                "roofline": me["roofline"], "clocks": me["clocks"],
+                "cpu_baseline": None if args.no_cpu_baseline else
+                cpu_baselines(we, me["inp"], args.cpu_seconds),
+            }
+            del me
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, inp, args.cpu_seconds)
+        cpu = cpu_baselines(w, inp, args.cpu_seconds)
     if rank == 0:
         line = {
             "metric": METRIC,
             "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "ms_per_step_min": round(m["ms_min"], 5), "windows": len(m["windows"]),
+            "value_statistic": f"median of {len(m['windows'])} timed windows of {args.steps} "
+                               f"steps (min window: {flops * ws / (m['ms_min'] * 1e-3) / 1e12:.1f}"
+                               " TFLOP/s)",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded; shapes and distributions of the workload)",
-            "config": {"workload": w.name, "batch": w.batch, "max_seqlen": w.max_seqlen,
-                       "heads_q": w.num_heads_q, "heads_kv": w.num_heads_kv,
-                       "head_dim": w.head_dim, "mask": "causal" if w.causal else "none",
-                       "rab": w.rab, "tokens": int(inp["seq_offsets"][-1]),
-                       **({"keys": int((inp["seq_offsets_k"][1:] - inp["seq_offsets_k"][:-1]).sum()
-                                       + inp["history"].sum()),
-                           "cached_keys": int(inp["history"].sum()), "page_size": w.page_size,
-                           "max_seqlen_k": w.max_seqlen_k} if kv_side else {}),
-                       "valid_pairs": pairs, "useful_gflop_per_step": round(flops / 1e9, 3),
-                       "l2": f"rotating {nsets} input sets of {set_bytes / 2**20:.0f} MiB (> L2)",
-                       "parallelism": f"replicas x{ws}"},
-            "gpu_launches": 2 * args.steps,
-            "roofline": roofline,
+            "config": _config(w, inp, m, ws),
+            "gpu_launches": 2 * args.steps * len(m["windows"]),
+            "roofline": m["roofline"],
             "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                     "pipeline": "pinned H2D of step i+1 and D2H of step i-1 overlap step i"},
-            "clocks": clk.summary(),
+            "clocks": m["clocks"],
             "cpu_baseline": cpu,
+            "workloads": extra,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
 
 
-def cpu_baseline(w, inp, seconds):
+def cpu_baselines(w, inp, seconds):
+    """The oracle on all host cores (the reported baseline) with its single-thread time
+    beside it, each on a bounded sample of the workload."""
+    allc = cpu_baseline(w, inp, seconds)
+    one = cpu_baseline(w, inp, seconds / 2, nthreads=1)
+    allc["single_thread"] = {"value": one["value"], "cores": 1, "sample": one["sample"]}
+    return allc
+
+
+def cpu_baseline(w, inp, seconds, nthreads=None):
     """The fp64 oracle on the host cores over the first sequences of the workload
-    (all heads, whole rows), grown until it takes about `seconds`."""
+    (all heads, whole rows), grown until it takes about `seconds`; sequences too long for
+    that budget are sampled by rows instead."""
     import oracle
 
-    nthreads = os.cpu_count() or 1
+    nthreads = nthreads or os.cpu_count() or 1
+    so0 = inp["seq_offsets"].to(torch.int64)
+    if not _is_kv(w) and w.batch > 0:
+        # whole-sequence cost of sequence 0 at the oracle's rate (about 3 GFLOP/s per thread,
+        # one thread per (sequence, head) unit)
+        L0 = int(so0[1] - so0[0])
+        est = (L0 * L0 * w.num_heads_q * w.head_dim * 4) / (3e9 * min(nthreads, w.num_heads_q))
+        if est > seconds:
+            return _cpu_rows_baseline(w, inp, seconds, nthreads)
     so = inp["seq_offsets"].to(torch.int64)
     nb = 1
     best = None
@@ -460,6 +578,65 @@ def cpu_baseline(w, inp, seconds):
                       f"rows), fp64, {dt:.2f} s"}
 
 
+def _cpu_rows_baseline(w, inp, seconds, nthreads):
+    """The oracle on output rows of the first sequence (row i with every key it sees, all
+    heads in turn), for sequences too long to run whole within the time budget; the row
+    count grows until the run takes about `seconds` / 4."""
+    import numpy as np
+
+    import oracle
+    so = inp["seq_offsets"].to(torch.int64).numpy()
+    L = int(so[1] - so[0])
+    mt = oracle.MASK_CAUSAL if w.causal else oracle.MASK_NONE
+    nc = 0 if inp["num_context"] is None else int(inp["num_context"][0])
+    nt = 0 if inp["num_targets"] is None else int(inp["num_targets"][0])
+    kw = dict(rab=inp["rab"], num_context=inp["num_context"], num_targets=inp["num_targets"],
+              mask_type=mt, target_group_size=w.target_group_size, alpha=w.alpha_value,
+              silu_scale=w.silu_scale_value, max_seqlen=w.max_seqlen)
+    n = 4
+    while True:
+        idx = np.linspace(0, L - 1, n).astype(np.int64)
+        rows = np.stack([np.zeros(n, np.int64), np.arange(n) % w.num_heads_q, idx], axis=1)
+        t0 = time.perf_counter()
+        oracle.hstu_fwd_rows(inp["q"], inp["k"], inp["v"], so, rows, nthreads=nthreads, **kw)
+        dt = time.perf_counter() - t0
+        if dt >= seconds / 4 or n >= 4096:
+            break
+        n = min(4096, max(n + 1, int(n * min(8.0, (seconds / 4) / max(dt, 1e-3)))))
+    pairs = sum(sum(oracle.valid(int(i), j, L, mt, nc, nt, w.target_group_size)
+                    for j in range(L)) if mt != oracle.MASK_NONE else L for i in idx)
+    return {"value": 4 * w.head_dim * pairs / dt / 1e12, "unit": "TFLOP/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{n} output rows of sequence 0 (L={L}, heads in turn, every key), fp64, "
+                      f"{dt:.2f} s"}
+
+
+def run_full_oracle(args):
+    """The oracle over the whole workload once, on all host cores and (unless
+    --skip-single-thread) on one thread: wall times for the results table."""
+    import oracle
+
+    oracle.build()
+    w = _workload(args.workload)
+    inp = _generate(w)
+    kw = dict(rab=inp["rab"], num_context=inp["num_context"], num_targets=inp["num_targets"],
+              mask_type=oracle.MASK_CAUSAL if w.causal else oracle.MASK_NONE,
+              target_group_size=w.target_group_size, alpha=w.alpha_value,
+              silu_scale=w.silu_scale_value,
+              max_seqlen=w.max_seqlen_k if _is_kv(w) else w.max_seqlen)
+    if _is_kv(w):
+        kw.update({k: inp[k] for k in KV_KEYS})
+    cores = os.cpu_count() or 1
+    res = {"workload": w.name, "cores": cores, "pairs": _pairs(w, inp),
+           "useful_gflop": 4 * w.head_dim * _pairs(w, inp) / 1e9}
+    for n in ([cores] if args.skip_single_thread else [cores, 1]):
+        t0 = time.perf_counter()
+        oracle.hstu_fwd(inp["q"], inp["k"], inp["v"], inp["seq_offsets"], nthreads=n, **kw)
+        res[f"oracle_seconds_{'all_cores' if n == cores else '1_thread'}"] = round(
+            time.perf_counter() - t0, 3)
+    print(json.dumps(res), flush=True)
+
+
 def run_reference(args):
     """The fp64 CPU oracle as the reference arm: each step is one bounded sample."""
     import oracle
@@ -467,6 +644,9 @@ def run_reference(args):
 
     ws, rank, _ = _dist()
     if rank != 0:
+        return
+    if args.full_oracle:
+        run_full_oracle(args)
         return
     oracle.build()
     w = _workload(args.workload)
@@ -527,6 +707,16 @@ def main():
     ap.add_argument("--workload", default="bf16_causal_b32_s2048_h4_d128")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--windows", type=int, default=10,
+                    help="timed windows of --steps calls (at least; see --min-seconds)")
+    ap.add_argument("--min-seconds", type=float, default=0.5,
+                    help="keep timing windows until this many seconds of calls ran")
+    ap.add_argument("--full-oracle", action="store_true",
+                    help="with --impl reference: the oracle over the whole workload, once")
+    ap.add_argument("--skip-single-thread", action="store_true",
+                    help="with --full-oracle: all host cores only")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the headline workload only (no 'workloads' object)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the forward kernel from an ncu capture")
     args = ap.parse_args()

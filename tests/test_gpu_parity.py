@@ -3,9 +3,12 @@ the same seeded inputs, element by element.
 
 Bar: max |O_gpu - O_oracle| / max |O_oracle| <= 1e-5 (fp32), 2e-2 (bf16), 1e-2 (fp16),
 over every row that belongs to a sequence. Small cases run the whole oracle; the
-full-size workloads are checked on sampled rows (oracle row by row), in the
-launch configuration the benchmark times.
+full-size workloads are compared whole (every output row) where the oracle finishes in
+seconds on the host cores, else on sampled rows (oracle row by row), in the launch
+configuration the benchmark times.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -182,6 +185,23 @@ def _sample_rows(so, nq, n, rng):
         i = int(rng.choice([0, L - 1, int(rng.integers(0, L))]))
         rows.append((b, int(rng.integers(0, nq)), i))
     return np.array(rows, dtype=np.int64)
+
+
+# full-size configurations whose whole output the oracle computes in seconds on the host
+# cores; the D = 256 one (about 1.1e12 fp64 multiply-adds) is checked on sampled rows
+WHOLE = ("bf16_causal_b32_s2048_h4_d128", "bf16_rab_b16_s1024_h8_d64",
+         "fp16_gqa8x2_targets_b8_s4096_d128")
+
+
+@pytest.mark.parametrize("name", WHOLE)
+def test_full_size_whole_output(cuda_device, name):
+    """Every output row of the full-size configuration against the oracle."""
+    w = W.WORKLOADS[name]
+    inp = W.generate(w)
+    got = _gpu(inp, cuda_device)
+    ref = _oracle_full(inp, nthreads=os.cpu_count() or 8)
+    err = _rel_err(got, ref, inp["seq_offsets"].numpy())
+    assert np.isfinite(err) and err <= TOL[w.dtype], f"{name}: rel err {err:.3e}"
 
 
 @pytest.mark.parametrize("name", [n for n in W.WORKLOADS if n != "fp32_tiny"])

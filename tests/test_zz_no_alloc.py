@@ -19,25 +19,36 @@ pytestmark = pytest.mark.gpu
 TOL = {"bf16": 2e-2, "fp16": 1e-2, "fp32": 1e-5}
 
 
-def _run_both(w, dev):
+def _run_both(w, dev, layout="jagged", rab_bcast=False):
+    """The plan-based call and the allocation-free call on the same inputs; returns the
+    largest difference relative to max |plan output|."""
     inp = W.to_device(W.generate(w), dev)
-    kw = dict(max_seqlen=w.max_seqlen, rab=inp["rab"], num_context=inp["num_context"],
+    q, k, v, so, rab = inp["q"], inp["k"], inp["v"], inp["seq_offsets"], inp["rab"]
+    if rab_bcast:
+        rab = rab[:, :1].contiguous()  # [B, 1, S, S]: one bias plane for every head
+    if layout == "normal":  # every sequence has max_seqlen tokens: [B, S, N, D]
+        B, S = w.batch, w.max_seqlen
+        q, k, v = (t.view(B, S, *t.shape[1:]) for t in (q, k, v))
+        so = None
+    kw = dict(max_seqlen=w.max_seqlen, rab=rab, num_context=inp["num_context"],
               num_targets=inp["num_targets"], causal=w.causal,
               target_group_size=w.target_group_size, alpha=w.alpha_value,
-              silu_scale=w.silu_scale_value)
-    ref = hstu_fwd(inp["q"], inp["k"], inp["v"], inp["seq_offsets"], **kw)
-    out = torch.full_like(inp["q"], float("nan"))
-    hstu_fwd_noalloc(inp["q"], inp["k"], inp["v"], inp["seq_offsets"], out, **kw)
+              silu_scale=w.silu_scale_value, layout=layout)
+    ref = hstu_fwd(q, k, v, so, **kw)
+    out = torch.full_like(q, float("nan"))
+    hstu_fwd_noalloc(q, k, v, so, out, **kw)
     torch.cuda.synchronize()
     T = int(inp["seq_offsets"][-1])
-    r = ref[:T].double().cpu().numpy()
-    g = out[:T].double().cpu().numpy()
+    r = ref.reshape(-1, *ref.shape[-2:])[:T].double().cpu().numpy()
+    g = out.reshape(-1, *out.shape[-2:])[:T].double().cpu().numpy()
     return float(np.max(np.abs(g - r)) / np.max(np.abs(r)))
 
 
 def test_noalloc_matches_plan_entry_point_on_two_calls_in_a_row(cuda_device):
-    """Two calls in a row (different workloads, so the second overwrites the first's
-    work list in the shared array) both match the plan-based entry point."""
+    """Calls in a row (different workloads, so each one overwrites the previous one's work
+    list in the shared array) all match the plan-based entry point: bf16 with context and
+    targets, fp16 with rab, the fp32 CUDA-core path, and the normal layout with a rab
+    plane broadcast to every head."""
     first = W.Workload(name="na1", dtype="bf16", batch=4, num_heads_q=4, num_heads_kv=2,
                        head_dim=128, max_seqlen=512, len_lo=100, len_hi=512, causal=True,
                        context_range=(0, 10), target_range=(0, 40), target_group_size=4,
@@ -45,9 +56,14 @@ def test_noalloc_matches_plan_entry_point_on_two_calls_in_a_row(cuda_device):
     second = W.Workload(name="na2", dtype="fp16", batch=3, num_heads_q=2, num_heads_kv=2,
                         head_dim=64, max_seqlen=264, len_lo=60, len_hi=264, causal=True,
                         rab=True, rab_sigma=0.3, seed=82)
-    for w in (first, second):
-        err = _run_both(w, cuda_device)
-        assert np.isfinite(err) and err <= TOL[w.dtype], f"{w.name}: {err:.3e}"
+    third = W.WORKLOADS["fp32_tiny"]
+    fourth = W.Workload(name="na4", dtype="bf16", batch=3, num_heads_q=4, num_heads_kv=4,
+                        head_dim=64, max_seqlen=200, len_lo=200, len_hi=200, causal=True,
+                        rab=True, rab_sigma=0.3, sigma=0.5, seed=84)
+    for w, layout, bcast in ((first, "jagged", False), (second, "jagged", False),
+                             (third, "jagged", False), (fourth, "normal", True)):
+        err = _run_both(w, cuda_device, layout=layout, rab_bcast=bcast)
+        assert np.isfinite(err) and err <= TOL[w.dtype], f"{w.name} ({layout}): {err:.3e}"
 
 
 def test_noalloc_rejects_work_lists_beyond_the_static_array(cuda_device):
