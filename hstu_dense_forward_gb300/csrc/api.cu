@@ -292,7 +292,7 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
     const uint64_t S = (uint64_t)key_bound(d);
     ok = encode3d(&P->maps.rab, ty, rab, S, S, (uint64_t)d.batch * (d.rab_heads == 1 ? 1 : Nq),
                   S * 2, S * S * 2, 64,
-                  hstu::kTileM, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+                  hstu::tc_rab_box_rows(), 1, CU_TENSOR_MAP_SWIZZLE_128B);
   } else if (ok) {
     P->maps.rab = P->maps.q;  // unused by the kernel
   }
@@ -740,7 +740,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
       const uint64_t S = (uint64_t)d.max_seqlen;
       ok = encode3d(&maps.rab, ty, rab, S, S, (uint64_t)d.batch * (d.rab_heads == 1 ? 1 : Nq),
                     S * 2, S * S * 2, 64,
-                    hstu::kTileM, 1, CU_TENSOR_MAP_SWIZZLE_128B);
+                    hstu::tc_rab_box_rows(), 1, CU_TENSOR_MAP_SWIZZLE_128B);
     } else if (ok) {
       maps.rab = maps.q;  // unused by the kernel
     }

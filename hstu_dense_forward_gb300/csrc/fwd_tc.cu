@@ -32,6 +32,8 @@ int tc_swizzle_bytes(int D, int elem_bytes) {
 
 int tc_out_box_cols(int D) { return D / tc::kEpiWG; }
 
+int tc_rab_box_rows() { return tc::kRabBoxRows; }
+
 cudaError_t tc_prepare(int D, int elem, int rab, int kv) {
   FwdParams p = {};
   p.D = D;

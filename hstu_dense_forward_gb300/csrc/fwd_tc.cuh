@@ -58,6 +58,9 @@ constexpr int kRabWarp = kEpiWarps + 5;        // rab loads
 constexpr int kThreads = (kEpiWarps + 6) * 32;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr uint32_t kTmemCols = 512;
+// A rab / custom-mask tile (128 rows x 128 keys, 16-bit) arrives as boxes of 32 rows x 64
+// keys; boxes whose keys every one of their rows has masked are not loaded (rab only).
+constexpr int kRabBoxRows = 32;
 // FP8 kernels round kP8Scale * P to E4M3 (the host divides silu_scale by kP8Scale):
 // 16 keeps P values down to 2^-10 in the normal range and saturates only above P = 28.
 
@@ -95,16 +98,18 @@ struct Cfg {
   static constexpr int EPI_GROUPS = D == 256 ? 2 : 1;
   static constexpr int GROUP_WARPS = kEpiWarps / EPI_GROUPS;
   static constexpr int COLS_PER_WG = kTileN / (kEpiWG / EPI_GROUPS);  // S columns per tile
-  // TMEM (512 columns). For D <= 128, P has two buffers of its own, O one accumulator and
-  // S two buffers; an S buffer is released as soon as the epilogue has loaded it, so the
-  // next score products overlap the epilogue. (Two O accumulators with one S buffer let an
-  // item's first PV product skip the wait for the previous item's drain, but measured
-  // slower: the single S buffer holds the score products back.) For D = 256 (O takes 256
-  // columns) P is written over the S buffer it came from and one thread issues all MMAs.
+  // TMEM (512 columns). For D <= 128, P has two buffers of its own and S two buffers; an
+  // S buffer is released as soon as the epilogue has loaded it, so the next score products
+  // overlap the epilogue. O has two accumulators where they fit beside them (D <= 64), one
+  // for D = 128 (two there would leave one S buffer, which measured slower: it holds the
+  // score products back). For D = 256 (O takes 256 columns) P is written over the S buffer
+  // it came from and one thread issues all MMAs.
   static constexpr bool P_SEP = (D <= 128);
   static constexpr bool SERIAL = !P_SEP;
-  static constexpr int NO = 1;              // O accumulators
   static constexpr int NPB = 2;             // P buffers (P_SEP), P over S otherwise
+  // O accumulators: two where TMEM has room for them next to two S buffers (D <= 64), so
+  // that an item's first PV product does not wait for the previous item's O to be drained
+  static constexpr int NO = (P_SEP && 2 * 128 + 2 * D + NPB * PW <= (int)kTmemCols) ? 2 : 1;
   static constexpr int NSB_FIT = (int)(kTmemCols - NO * D - (P_SEP ? NPB * PW : 0)) / 128;
   static constexpr int NSB = NSB_FIT < 2 ? NSB_FIT : 2;  // S buffers
   // TMEM columns
@@ -439,27 +444,57 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 
 // rab tiles of every S tile, in tile order, on their own thread: the rab ring is released
 // by the epilogue (late in a tile), and waiting for it must not hold back the K loads.
-template <int D, bool RAB, bool KV, bool F8>
+// A tile is loaded as up to eight boxes of 32 rows x 64 keys (a 128-byte swizzled column
+// block of 128 rows takes four); with rab (not a custom mask, which is multiplied into P)
+// a box is skipped when its rows lie beyond the item's queries or every key of it is at or
+// beyond the end of what its rows may see (diagonal and ragged tiles): its entries are all
+// masked, and the epilogue sets a masked entry's h to 0 after adding rab.
+template <int D, bool RAB, bool MASK, bool KV, bool F8>
 __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tr,
                            long long total) {
   using C = Cfg<D, RAB, F8>;
+  constexpr int STRIPS = kTileM / kRabBoxRows;
+  constexpr uint32_t BOX_BYTES = kRabBoxRows * 128;
   uint32_t r_it = 0;
   const uint32_t sbase = ptx::smem_u32(smem);
   for (int k = 0;; ++k) {
     Item it;
     if (!get_item(bars, k, it, p) || it.n_kv < 0) return;
     const int plane = (int)rab_plane(p, it.b, it.h);
+    const int row = (KV ? it.off : 0) + it.m0;  // key position of the item's first query row
+    // key end of each row strip (keys at or beyond it are masked for all of its rows)
+    int strip_end[STRIPS];
+#pragma unroll
+    for (int st = 0; st < STRIPS; ++st)
+      strip_end[st] = it.m0 + st * kRabBoxRows >= it.Lq
+                          ? 0
+                          : kv_end_for_rows(it.geom, row + st * kRabBoxRows, kRabBoxRows,
+                                            p.mask_type);
     for (int j = 0; j < it.n_kv; ++j) {
       const int rs = r_it % C::NR;
       if (!wait_bar(bars, &bars->r_empty[rs], ((r_it / C::NR) & 1) ^ 1, p)) return;
       const uint32_t full = ptx::smem_u32(&bars->r_full[rs]);
-      ptx::mbar_arrive_expect_tx(full, C::RAB_BYTES);
       const uint32_t dst = sbase + C::OFF_R + rs * C::RAB_BYTES;
       // rows: the key positions of the item's queries; columns: the visit's key tile
-      const int n0 = (KV ? key_tile(j, it.split, it.hist).x : j) * kTileN;
-      const int row = (KV ? it.off : 0) + it.m0;
-      ptx::tma_load_3d(dst, tr, full, n0, row, plane);
-      ptx::tma_load_3d(dst + C::RAB_BYTES / 2, tr, full, n0 + 64, row, plane);
+      const KeyTile kt = KV ? key_tile(j, it.split, it.hist) : KeyTile{j, 0, kTileN, false};
+      const int n0 = kt.x * kTileN;
+      uint32_t need = 0;  // bit st * 2 + cb: box of row strip st, column block cb
+#pragma unroll
+      for (int st = 0; st < STRIPS; ++st)
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+          const bool used = MASK || (strip_end[st] > n0 + 64 * cb && kt.clo < 64 * cb + 64 &&
+                                     kt.chi > 64 * cb);
+          need |= (used ? 1u : 0u) << (st * 2 + cb);
+        }
+      ptx::mbar_arrive_expect_tx(full, __popc(need) * BOX_BYTES);
+#pragma unroll
+      for (int st = 0; st < STRIPS; ++st)
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb)
+          if (need & (1u << (st * 2 + cb)))
+            ptx::tma_load_3d(dst + cb * (C::RAB_BYTES / 2) + st * BOX_BYTES, tr, full,
+                             n0 + 64 * cb, row + st * kRabBoxRows, plane);
       ++r_it;
     }
   }
@@ -1107,7 +1142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kRabWarp) {
     if constexpr (RAB) {
-      if (lane == 0) producer_r<D, RAB, KV, F8>(p, bars, smem, &tm_r, total);
+      if (lane == 0) producer_r<D, RAB, MASK, KV, F8>(p, bars, smem, &tm_r, total);
     }
   } else if (warp == kPvWarp) {
     if (lane == 0 && !C::SERIAL) mma_pv_issuer<D, BF16, RAB, F8>(p, bars, smem, tmem, total);

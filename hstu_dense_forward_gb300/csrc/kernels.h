@@ -117,6 +117,7 @@ struct TcMaps {
 bool tc_supported_dim(int D);
 int tc_swizzle_bytes(int D, int elem_bytes);  // row width of one TMA box / UMMA swizzle atom
 int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
+int tc_rab_box_rows();        // rows of one rab / custom-mask load box (64 columns each)
 // elem: 0 f16, 1 bf16, 2 FP8 E4M3; rab: 0 none, 1 rab, 2 custom mask; kv: the key-side
 // variant (own k/v offsets, KV cache)
 cudaError_t tc_prepare(int D, int elem, int rab, int kv);

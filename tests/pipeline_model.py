@@ -67,7 +67,8 @@ def kernel_cfg(D: int, rab: bool) -> Cfg:
     NK = {32: 4, 64: 2 if rab else 4, 128: 2, 256: 1}[D]
     NR = ({32: 4, 64: 3, 128: 2, 256: 1}[D]) if rab else 0
     serial = D == 256
-    return Cfg(D=D, NQ=NQ, NK=NK, NV=NK, NR=NR, NSB=2, NPB=2, NO=1,
+    # two O accumulators where TMEM has room beside two S buffers and two P buffers
+    return Cfg(D=D, NQ=NQ, NK=NK, NV=NK, NR=NR, NSB=2, NPB=2, NO=2 if D <= 64 else 1,
                EPI_GROUPS=2 if serial else 1, SERIAL=serial)
 
 
