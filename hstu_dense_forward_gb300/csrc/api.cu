@@ -2,11 +2,14 @@
 // TMA tensor maps, kernel selection and launch. See include/hstu_fwd.h for the
 // contract of every entry point.
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
+#include <cmath>
 #include <initializer_list>
 #include <mutex>
 
@@ -97,6 +100,36 @@ static bool layout_args_ok(const hstu_fwd_desc& d, const void* seq_offsets,
 
 // The key side differs from the queries (own offsets or a KV cache).
 static bool key_side(const hstu_fwd_desc& d) { return d.is_delta_qk || d.page_size; }
+
+// rab goes through the tensor core (S accumulates the rab tile times a diagonal operand of
+// c = 1/alpha) when that kernel variant exists for the call and c is a finite, normal value
+// of the input type; its 16-bit pattern is the diagonal. Otherwise the epilogue adds rab.
+static void set_rab_mode(FwdParams& p, const hstu_fwd_desc& d, bool is_mask) {
+  p.rab_mma = 0;
+  p.rab_ident = 0;
+  const int elem = d.dtype == HSTU_FP8_E4M3 ? 2 : (d.dtype == HSTU_BF16 ? 1 : 0);
+  if (!p.rab || d.dtype == HSTU_F32 ||
+      !hstu::rab_mma_dim(d.head_dim, elem, is_mask ? 2 : 1, key_side(d) ? 1 : 0))
+    return;
+  if (!(p.alpha != 0.0f) || !std::isfinite(p.alpha)) return;
+  const float c = 1.0f / p.alpha;
+  float back;
+  uint16_t bits;
+  if (d.dtype == HSTU_BF16) {
+    const __nv_bfloat16 b = __float2bfloat16_rn(c);
+    back = __bfloat162float(b);
+    memcpy(&bits, &b, 2);
+  } else {
+    const __half h = __float2half_rn(c);
+    back = __half2float(h);
+    memcpy(&bits, &h, 2);
+  }
+  if (!std::isfinite(back) || std::fabs(back) < (d.dtype == HSTU_BF16 ? 1.17549435e-38f
+                                                                      : 6.103515625e-05f))
+    return;
+  p.rab_mma = 1;
+  p.rab_ident = bits;
+}
 
 // Bound on the keys of a sequence, and the S of rab and of a custom mask.
 static int key_bound(const hstu_fwd_desc& d) {
@@ -409,6 +442,7 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   p.silu_scale = silu_scale;
   p.fp8 = d.dtype == HSTU_FP8_E4M3 ? 1 : 0;
   p.test_stall = P->test_stall;
+  set_rab_mode(p, d, is_mask);
 #if HSTU_TRACE
   // run r of the plan records into launch slot r % kSlots
   if (P->d_trace) p.trace = P->d_trace + (size_t)(P->runs % hstu::trace::kSlots) * hstu::trace::kSlotWords;
@@ -715,6 +749,7 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
   p.rab_bcast = d.rab_heads == 1 ? 1 : 0;
   p.alpha = alpha;
   p.silu_scale = silu_scale;
+  set_rab_mode(p, d, false);
 
   TcMaps maps;
   if (tc) {

@@ -18,8 +18,9 @@ cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cu
     return p.rab_is_mask ? tc::dispatch_kv_mask(p, m, bf16, grid, st, pdl, prepare)
                          : tc::dispatch_kv(p, m, bf16, grid, st, pdl, prepare);
   if (p.rab_is_mask) return tc::dispatch_mask(p, m, bf16, grid, st, pdl, prepare);
-  return p.rab ? tc::dispatch_type<true, false, false>(p, m, bf16, grid, st, pdl, prepare)
-               : tc::dispatch_type<false, false, false>(p, m, bf16, grid, st, pdl, prepare);
+  if (p.rab && p.rab_mma) return tc::dispatch_rab_mma(p, m, bf16, grid, st, pdl, prepare);
+  return p.rab ? tc::dispatch_type<1, false, false>(p, m, bf16, grid, st, pdl, prepare)
+               : tc::dispatch_type<0, false, false>(p, m, bf16, grid, st, pdl, prepare);
 }
 
 }  // namespace
@@ -43,7 +44,16 @@ cudaError_t tc_prepare(int D, int elem, int rab, int kv) {
   p.rab_is_mask = rab == 2 ? 1 : 0;
   p.seq_offsets_k = kv ? reinterpret_cast<const void*>(1) : nullptr;  // selects the variant only
   TcMaps m = {};
-  return dispatch(p, m, bf16, 0, nullptr, false, true);
+  cudaError_t e = dispatch(p, m, bf16, 0, nullptr, false, true);
+  if (e == cudaSuccess && rab_mma_dim(D, elem, rab, kv)) {
+    p.rab_mma = 1;  // runs whose 1/alpha is finite in the input type take this variant
+    e = dispatch(p, m, bf16, 0, nullptr, false, true);
+  }
+  return e;
+}
+
+bool rab_mma_dim(int D, int elem, int rab, int kv) {
+  return rab == 1 && !kv && elem != 2 && (D == 32 || D == 64);
 }
 
 cudaError_t launch_fwd_tc(const FwdParams& p, const TcMaps& maps, int bf16, int grid,

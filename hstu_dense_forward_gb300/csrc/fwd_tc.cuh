@@ -66,10 +66,18 @@ constexpr int kRabBoxRows = 32;
 
 // F8: q, k, v are FP8 E4M3 (one byte each); the products run as tcgen05 kind::f8f6f4 with
 // P rounded to E4M3; O is written as bf16.
-template <int D, bool RAB, bool F8 = false>
+// RAB: 0 no rab; 1 rab (or a custom mask) read from shared memory by the epilogue; 2 rab
+// added to S by the tensor core: for each 16-key step k of the tile, S[:, 16k:16k+16] +=
+// R[:, 16k:16k+16] (c I16) with the rab tile R as the A operand and a 16 x 16 diagonal B of
+// c = 1/alpha, so that alpha*S = alpha Q K^T + rab and the epilogue is that of the plain
+// kernel (head dims up to 64; eight M128 N16 K16 products per tile).
+template <int D, int RAB, bool F8 = false>
 struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head_dim");
   static_assert(!F8 || (D <= 128 && !RAB), "fp8: head_dim <= 128, no rab");
+  static constexpr bool RM = RAB == 2;        // rab by the tensor core
+  static constexpr bool EPI_RAB = RAB == 1;   // rab / mask tiles read by the epilogue
+  static_assert(!RM || D <= 64, "rab by the tensor core: head_dim <= 64");
   static constexpr int EB = F8 ? 1 : 2;                     // bytes per q / k / v element
   static constexpr int SWB = (D * EB >= 128) ? 128 : D * EB;  // bytes per swizzled row
   static constexpr uint32_t SWZ = (SWB == 128) ? 2u : (SWB == 64 ? 4u : 6u);
@@ -86,6 +94,8 @@ struct Cfg {
   static constexpr int NV = NK;                                  // K and V ring depths
   // rab tiles stream from HBM once each: the deeper the ring, the more bytes in flight
   static constexpr int NR = RAB ? (D == 32 ? 4 : (D == 64 ? 3 : (D == 128 ? 2 : 1))) : 0;
+  // RM: the 16 x 16 diagonal B operand, K-major rows of 64 bytes (64-byte swizzle)
+  static constexpr int IDENT_BYTES = RM ? 16 * 64 : 0;
   // O is staged in shared memory and written by TMA when there is room for a tile
   static constexpr bool STAGE = D <= 64 || (D == 128 && !RAB);
   static constexpr int OC = D / kEpiWG;              // O columns per epilogue warpgroup
@@ -120,7 +130,8 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
   static constexpr int OFF_R = OFF_V + NV * TILE_BYTES;
-  static constexpr int OFF_O = OFF_R + NR * RAB_BYTES;
+  static constexpr int OFF_I = OFF_R + NR * RAB_BYTES;  // diagonal B operand (RM)
+  static constexpr int OFF_O = OFF_I + (RM ? 1024 : 0);   // (a 1024-byte swizzle atom)
   static constexpr int OFF_BAR = OFF_O + (STAGE ? O_TILE_BYTES : 0);
   static constexpr int BAR_BYTES = 1024;
   static constexpr int SMEM_USED = OFF_BAR + BAR_BYTES;
@@ -144,7 +155,7 @@ struct Item {
 
 constexpr int kInfoDepth = 8;                   // decoded items kept in shared memory
 // item readers: epilogue warps, the MMA issuer(s), K and V producers, the rab producer
-template <bool SERIAL, bool RAB>
+template <bool SERIAL, int RAB>
 constexpr int info_readers() { return kEpiWarps + (SERIAL ? 3 : 4) + (RAB ? 1 : 0); }
 
 // Barrier block layout.
@@ -306,7 +317,7 @@ __device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
 // load waits behind the release of another ring's slot. With two Q buffers the Q
 // producer runs up to two work items ahead; with one, it prefetches the next
 // item's Q tile into L2 so that the load after the slot frees hits in L2.
-template <int D, bool RAB, bool KV, bool F8>
+template <int D, int RAB, bool KV, bool F8>
 __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tq,
                            long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -378,7 +389,7 @@ __device__ __forceinline__ TilePages tile_pages(const FwdParams& p, const Item& 
 // cache pages when the visit's rows are cached, else rows tk + 128x - hist .. of k / v
 // (rows before the sequence's first new row belong to the cached part of a split tile
 // and meet P = 0 there).
-template <int D, bool RAB, bool F8>
+template <int D, int RAB, bool F8>
 __device__ __forceinline__ void load_kv_tile(const FwdParams& p, const Item& it, int j,
                                              const TilePages& pg, const CUtensorMap* tnew,
                                              const CUtensorMap* tcache, int plane, uint32_t dst,
@@ -406,7 +417,7 @@ __device__ __forceinline__ void load_kv_tile(const FwdParams& p, const Item& it,
   }
 }
 
-template <int D, bool RAB, bool KV, bool F8>
+template <int D, int RAB, bool KV, bool F8>
 __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tk,
                            const CUtensorMap* tc, long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -449,7 +460,7 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 // a box is skipped when its rows lie beyond the item's queries or every key of it is at or
 // beyond the end of what its rows may see (diagonal and ragged tiles): its entries are all
 // masked, and the epilogue sets a masked entry's h to 0 after adding rab.
-template <int D, bool RAB, bool MASK, bool KV, bool F8>
+template <int D, int RAB, bool MASK, bool KV, bool F8>
 __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tr,
                            long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -500,7 +511,7 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   }
 }
 
-template <int D, bool RAB, bool KV, bool F8>
+template <int D, int RAB, bool KV, bool F8>
 __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tv,
                            const CUtensorMap* tc, long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -557,7 +568,7 @@ __device__ __forceinline__ void mma_drain(Bars* bars, const FwdParams& p) {
 // Single issuer, used when P is written over its S buffer (D = 256): there S(t+2)
 // can only start after PV(t) has read P(t), so the two products form one chain and
 // are issued in that order: S(t0), S(t0+1), then per tile PV(t), S(t+2).
-template <int D, bool BF16, bool RAB, bool F8>
+template <int D, bool BF16, int RAB, bool F8>
 __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                                   long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -630,7 +641,7 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
   mma_drain(bars, p);
 }
 
-template <int D, bool BF16, bool RAB, bool F8>
+template <int D, bool BF16, int RAB, bool F8>
 __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                              long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -638,6 +649,10 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
   constexpr uint32_t IDESC_S = ptx::idesc_f16((BF16 && !F8) ? 1u : 0u, 128, kTileN, 0);
   const uint32_t sbase = ptx::smem_u32(smem);
   uint32_t q_it = 0, k_it = 0, t = 0;
+  // RM: the rab tile of S(t) (A, K-major, 128-byte swizzle) against the 16 x 16 diagonal
+  // operand (K-major, 64-byte swizzle), one M128 N16 K16 product per 16 keys
+  const uint64_t id0 = C::RM ? ptx::smem_desc(sbase + C::OFF_I, 16, 8 * 64, 4) : 0;
+  constexpr uint32_t IDESC_R = ptx::idesc_f16((BF16 && !F8) ? 1u : 0u, 128, 16, 0);
   for (int k = 0;; ++k) {
     Item it;
     if (!get_item<kNapIssuer>(bars, k, it, p) || it.n_kv < 0) break;
@@ -676,6 +691,23 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
         else
           ptx::mma_ss(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, kk > 0 ? 1u : 0u);
       }
+      if constexpr (C::RM) {
+        // S[:, 16k:16k+16] += R[:, 16k:16k+16] (c I16) for the eight 16-key steps k
+        const int rs = t % C::NR;
+        if (!wait_bar<kNapIssuer>(bars, &bars->r_full[rs], (t / C::NR) & 1, p)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint64_t rd0 = ptx::smem_desc(sbase + C::OFF_R + rs * C::RAB_BYTES, 16, 1024, 2);
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          const uint32_t off = (kk / 4) * (C::RAB_BYTES / 2) + (kk % 4) * 32;
+          ptx::mma_ss(tmem + C::S_COL0 + sb * 128 + 16 * kk, ptx::desc_add(rd0, off), id0,
+                      IDESC_R, 1u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->r_empty[rs]));
+      }
       ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
       ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
       if (j + 1 == it.n_kv) ptx::mma_commit(ptx::smem_u32(&bars->q_empty[qs]));
@@ -687,7 +719,7 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
   mma_drain(bars, p);
 }
 
-template <int D, bool BF16, bool RAB, bool F8>
+template <int D, bool BF16, int RAB, bool F8>
 __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                               long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -778,7 +810,7 @@ __device__ __forceinline__ uint32_t swizzle(uint32_t o) {
   }
 }
 
-template <int D, bool BF16, bool RAB, bool MASK, bool KV, bool F8>
+template <int D, bool BF16, int RAB, bool MASK, bool KV, bool F8>
 __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                          const CUtensorMap* tm_o, long long total, int warp, int lane) {
   using C = Cfg<D, RAB, F8>;
@@ -913,7 +945,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         full = j < n_full;
       const uint8_t* rab_row = nullptr;
       int rs = 0;
-      if constexpr (RAB) {
+      if constexpr (C::EPI_RAB) {
         rs = t % C::NR;  // one rab tile per S tile, in tile order
         // With two epilogue groups and a one-tile rab ring (D = 256) the rab slot alternates
         // between the groups, so a group reaching tile t may find r_full two phases behind,
@@ -946,7 +978,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           ptx::mul_f32x2(h[e], h[e + 1], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
                          half_alpha, half_alpha);
         uint32_t mw[16];  // custom-mask pairs (MASK)
-        if constexpr (RAB) {
+        if constexpr (C::EPI_RAB) {
           // rab / custom-mask tile: two 64-column TMA boxes of 128 rows x 128 bytes with
           // 128-byte swizzle, read conflict-free (one row per lane)
           const uint8_t* box = rab_row + (cc >> 6) * (C::RAB_BYTES / 2);
@@ -1023,7 +1055,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           ptx::tmem_st16(tmem + lane_off + pcol, pk);
         }
       }
-      if constexpr (RAB) warp_arrive(&bars->r_empty[rs], lane);
+      if constexpr (C::EPI_RAB) warp_arrive(&bars->r_empty[rs], lane);
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       warp_arrive(&bars->p_full[t % C::NPB], lane);
@@ -1048,7 +1080,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 
 // ------------------------------------------------------------------ kernel
 // MASK: the rab stream carries a custom mask (multiplied into P after the SiLU).
-template <int D, bool BF16, bool RAB, bool MASK = false, bool KV = false, bool F8 = false>
+template <int D, bool BF16, int RAB, bool MASK = false, bool KV = false, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
@@ -1080,7 +1112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     HSTU_INIT_ALL(q_full, 1)
     HSTU_INIT_ALL(q_empty, 1)
     HSTU_INIT_ALL(r_full, 1)
-    HSTU_INIT_ALL(r_empty, C::GROUP_WARPS * 32)
+    // rab slots are released by the epilogue lanes, or (RM) by the score issuer's commit
+    HSTU_INIT_ALL(r_empty, C::RM ? 1 : C::GROUP_WARPS * 32)
     HSTU_INIT_ALL(k_full, 1)
     HSTU_INIT_ALL(k_empty, 1)
     HSTU_INIT_ALL(v_full, 1)
@@ -1107,6 +1140,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
+  }
+  if constexpr (C::RM) {
+    // The diagonal B operand (16 keys x 16, K-major, rows of 64 bytes with the 64-byte
+    // swizzle, the first 32 bytes used) holds c = 1/alpha on its diagonal, and the rab ring
+    // starts zeroed: a rab box that is never loaded (all of its entries masked) then holds
+    // finite values, so its products with the zeros of the diagonal stay finite (and 0 in
+    // the entries that are not masked).
+    uint4* z = reinterpret_cast<uint4*>(smem + C::OFF_R);
+    const int n16 = (C::NR * C::RAB_BYTES + C::IDENT_BYTES) / 16;
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (threadIdx.x < 16) {
+      const uint32_t j = threadIdx.x;  // key row j, contraction column j
+      const uint32_t off = swizzle<64>(j * 64 + (j >> 3) * 16) + (j & 7) * 2;
+      *reinterpret_cast<uint16_t*>(smem + C::OFF_I + off) = (uint16_t)p.rab_ident;
+    }
+    ptx::fence_proxy_async_smem();  // the tensor core (async proxy) reads both
   }
   ptx::tc_fence_before();
   __syncthreads();

@@ -7,13 +7,13 @@
 namespace hstu {
 namespace tc {
 
-template <int D, bool BF16, bool RAB, bool MASK, bool KV, bool F8 = false>
+template <int D, bool BF16, int RAB, bool MASK, bool KV, bool F8 = false>
 cudaError_t prepare_one() {
   return cudaFuncSetAttribute(fwd_tc_kernel<D, BF16, RAB, MASK, KV, F8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, RAB, F8>::SMEM_BYTES);
 }
 
-template <int D, bool BF16, bool RAB, bool MASK, bool KV, bool F8 = false>
+template <int D, bool BF16, int RAB, bool MASK, bool KV, bool F8 = false>
 cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t stream,
                        bool pdl) {
   cudaLaunchConfig_t cfg = {};
@@ -31,7 +31,7 @@ cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream
 }
 
 // Prepare (shared-memory opt-in) or launch one variant, chosen by head dim and type.
-template <bool BF16, bool RAB, bool MASK, bool KV>
+template <bool BF16, int RAB, bool MASK, bool KV>
 cudaError_t dispatch_dim(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
                          bool pdl, bool prepare) {
   switch (p.D) {
@@ -43,12 +43,16 @@ cudaError_t dispatch_dim(const FwdParams& p, const TcMaps& m, int grid, cudaStre
   }
 }
 
-template <bool RAB, bool MASK, bool KV>
+template <int RAB, bool MASK, bool KV>
 cudaError_t dispatch_type(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                           cudaStream_t st, bool pdl, bool prepare) {
   return bf16 ? dispatch_dim<true, RAB, MASK, KV>(p, m, grid, st, pdl, prepare)
               : dispatch_dim<false, RAB, MASK, KV>(p, m, grid, st, pdl, prepare);
 }
+
+// rab added by the tensor core (fwd_tc_rab_mma.cu): head dims 32 and 64, no key side.
+cudaError_t dispatch_rab_mma(const FwdParams& p, const TcMaps& m, int bf16, int grid,
+                             cudaStream_t st, bool pdl, bool prepare);
 
 // Custom-mask variants (fwd_tc_mask.cu): prepare (shared-memory opt-in) or launch.
 cudaError_t dispatch_mask(const FwdParams& p, const TcMaps& m, int bf16, int grid,

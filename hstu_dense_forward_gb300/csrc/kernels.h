@@ -49,6 +49,11 @@ struct FwdParams {
                               // producer signals nothing, so the first score product's wait
                               // runs out and the kernel takes its timeout path
   unsigned long long* trace;  // pipeline trace buffer (builds with HSTU_TRACE=1), or nullptr
+  // rab added by the tensor core (head dims up to 64, bf16/fp16, no key side): the kernel
+  // variant that multiplies the rab tile by a diagonal operand holding rab_ident, the 16-bit
+  // pattern of 1/alpha in the input type (set by the host when 1/alpha is finite there)
+  int rab_mma;
+  unsigned rab_ident;
 };
 
 // FP8 kernels hold kP8Scale * P (E4M3) for the second product; silu_scale is divided by it.
@@ -121,6 +126,9 @@ int tc_rab_box_rows();        // rows of one rab / custom-mask load box (64 colu
 // elem: 0 f16, 1 bf16, 2 FP8 E4M3; rab: 0 none, 1 rab, 2 custom mask; kv: the key-side
 // variant (own k/v offsets, KV cache)
 cudaError_t tc_prepare(int D, int elem, int rab, int kv);
+// The variant that adds rab with the tensor core exists for these (rab = 1: rab, not a
+// custom mask; no key side; bf16 / fp16; head dim 32 or 64).
+bool rab_mma_dim(int D, int elem, int rab, int kv);
 cudaError_t launch_fwd_tc(const FwdParams& p, const TcMaps& maps, int bf16, int grid,
                           cudaStream_t stream, bool pdl);
 

@@ -129,6 +129,20 @@ def test_rab_variants(cuda_device, dtype):
     _check(w, cuda_device)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("alpha", [0.3, 0.125, 0.0, 1e-6])
+def test_rab_paths_small_head_dims(cuda_device, dtype, d, alpha):
+    """Head dims up to 64 add rab with the tensor core when 1/alpha is a finite normal
+    value of the input type (0.3: 1/alpha rounded once; 0.125: exact), else in the
+    epilogue (alpha = 0; 1e-6, whose reciprocal overflows fp16); both match the oracle."""
+    w = W.Workload(name="rabpath", dtype=dtype, batch=3, num_heads_q=4, num_heads_kv=4,
+                   head_dim=d, max_seqlen=264, len_lo=40, len_hi=264, causal=True,
+                   context_range=(0, 12), target_range=(0, 30), target_group_size=3, rab=True,
+                   rab_sigma=0.5, sigma=0.7, alpha=alpha, seed=43)
+    _check(w, cuda_device)
+
+
 def test_int32_offsets(cuda_device):
     w = W.Workload(name="i32", dtype="bf16", batch=3, num_heads_q=2, num_heads_kv=2, head_dim=128,
                    max_seqlen=300, len_lo=50, len_hi=300, causal=True, context_range=(0, 9),
