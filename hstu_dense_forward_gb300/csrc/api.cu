@@ -667,7 +667,8 @@ cudaError_t noalloc_setup(int dev, const hstu_fwd_desc& d, uint32_t** scratch, i
   // shared-memory opt-in of the kernel variant this descriptor uses
   int bit = 0;
   if (d.dtype != HSTU_F32) {
-    const int di = d.head_dim == 32 ? 0 : d.head_dim == 64 ? 1 : d.head_dim == 128 ? 2 : 3;
+    const int kd = hstu::tc_kernel_dim(d.head_dim);
+    const int di = kd == 32 ? 0 : kd == 64 ? 1 : kd == 128 ? 2 : 3;
     bit = 1 + di * 4 + (d.dtype == HSTU_BF16 ? 2 : 0) + (d.has_rab ? 1 : 0);
   }
   if (!(g_noalloc_prepared[dev] & (1u << bit))) {

@@ -25,13 +25,20 @@ cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cu
 
 }  // namespace
 
-bool tc_supported_dim(int D) { return D == 32 || D == 64 || D == 128 || D == 256; }
+// Every multiple of 16 up to 256 runs on the kernel built for the next of 32, 64, 128, 256:
+// the tensor maps keep the true head dim (rows of D elements) with boxes of the kernel's,
+// so TMA loads fill the extra columns of q, k and v with zeros (Q K^T is unchanged, the
+// extra O columns are 0) and TMA stores clip them; direct stores skip them.
+bool tc_supported_dim(int D) { return D % 16 == 0 && D >= 16 && D <= 256; }
+
+int tc_kernel_dim(int D) { return D <= 32 ? 32 : (D <= 64 ? 64 : (D <= 128 ? 128 : 256)); }
 
 int tc_swizzle_bytes(int D, int elem_bytes) {
-  return D * elem_bytes >= 128 ? 128 : D * elem_bytes;
+  const int k = tc_kernel_dim(D);
+  return k * elem_bytes >= 128 ? 128 : k * elem_bytes;
 }
 
-int tc_out_box_cols(int D) { return D / tc::kEpiWG; }
+int tc_out_box_cols(int D) { return tc_kernel_dim(D) / tc::kEpiWG; }
 
 int tc_rab_box_rows() { return tc::kRabBoxRows; }
 
@@ -53,7 +60,7 @@ cudaError_t tc_prepare(int D, int elem, int rab, int kv) {
 }
 
 bool rab_mma_dim(int D, int elem, int rab, int kv) {
-  return rab == 1 && !kv && elem != 2 && (D == 32 || D == 64);
+  return rab == 1 && !kv && elem != 2 && tc_kernel_dim(D) <= 64;
 }
 
 cudaError_t launch_fwd_tc(const FwdParams& p, const TcMaps& maps, int bf16, int grid,

@@ -846,7 +846,9 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       if (lane == 0) ptx::bulk_wait_read0();  // this warp's previous store has read it
       __syncwarp();
     }
-    T16* orow = out + (((long long)pit.tq + pi) * p.Nq + pit.h) * (long long)D + wg * OC;
+    // rows of out hold p.D elements (the kernel's D for a padded head dim is larger; its
+    // extra columns are not stored)
+    T16* orow = out + (((long long)pit.tq + pi) * p.Nq + pit.h) * (long long)p.D + wg * OC;
 #pragma unroll
     for (int c0 = 0; c0 < OC; c0 += OCH) {
       uint32_t part[OCH];
@@ -871,7 +873,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           // chunks, conflict-free for one row per lane
           *reinterpret_cast<uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + c0 * 2 + v4 * 16)) =
               make_uint4(w[0], w[1], w[2], w[3]);
-        } else if (pi < pit.Lq) {
+        } else if (pi < pit.Lq && wg * OC + c0 + v4 * 8 < p.D) {
           reinterpret_cast<uint4*>(orow + c0)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
@@ -888,15 +890,16 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       if (row0 + 32 <= pit.Lq) {
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && wg * OC < p.D) {  // (a slice wholly beyond a padded head dim: none)
           ptx::tma_store_3d(tm_o, ptx::smem_u32(stage), wg * OC, pit.h, pit.tq + row0);
           ptx::bulk_commit();
         }
       } else if (pi < pit.Lq) {
 #pragma unroll
         for (int v4 = 0; v4 < OC / 8; ++v4)
-          reinterpret_cast<uint4*>(orow)[v4] =
-              *reinterpret_cast<const uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + v4 * 16));
+          if (wg * OC + v4 * 8 < p.D)
+            reinterpret_cast<uint4*>(orow)[v4] = *reinterpret_cast<const uint4*>(
+                stage + swizzle<C::OSWB>(lane * OC * 2 + v4 * 16));
       }
     }
     __syncwarp();

@@ -11,7 +11,7 @@ namespace {
 template <bool KV>
 cudaError_t dispatch_f8_dim(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
                             bool pdl, bool prepare) {
-  switch (p.D) {
+  switch (tc_kernel_dim(p.D)) {
     case 32: return prepare ? prepare_one<32, false, false, false, KV, true>() : launch_one<32, false, false, false, KV, true>(p, m, grid, st, pdl);
     case 64: return prepare ? prepare_one<64, false, false, false, KV, true>() : launch_one<64, false, false, false, KV, true>(p, m, grid, st, pdl);
     case 128: return prepare ? prepare_one<128, false, false, false, KV, true>() : launch_one<128, false, false, false, KV, true>(p, m, grid, st, pdl);

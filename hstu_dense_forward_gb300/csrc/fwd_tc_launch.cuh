@@ -34,7 +34,7 @@ cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream
 template <bool BF16, int RAB, bool MASK, bool KV>
 cudaError_t dispatch_dim(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
                          bool pdl, bool prepare) {
-  switch (p.D) {
+  switch (tc_kernel_dim(p.D)) {
     case 32: return prepare ? prepare_one<32, BF16, RAB, MASK, KV>() : launch_one<32, BF16, RAB, MASK, KV>(p, m, grid, st, pdl);
     case 64: return prepare ? prepare_one<64, BF16, RAB, MASK, KV>() : launch_one<64, BF16, RAB, MASK, KV>(p, m, grid, st, pdl);
     case 128: return prepare ? prepare_one<128, BF16, RAB, MASK, KV>() : launch_one<128, BF16, RAB, MASK, KV>(p, m, grid, st, pdl);

@@ -10,7 +10,7 @@ namespace {
 template <bool BF16>
 cudaError_t one_type(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st, bool pdl,
                      bool prepare) {
-  switch (p.D) {
+  switch (tc_kernel_dim(p.D)) {
     case 32: return prepare ? prepare_one<32, BF16, 2, false, false>() : launch_one<32, BF16, 2, false, false>(p, m, grid, st, pdl);
     case 64: return prepare ? prepare_one<64, BF16, 2, false, false>() : launch_one<64, BF16, 2, false, false>(p, m, grid, st, pdl);
     default: return cudaErrorInvalidValue;

@@ -120,6 +120,7 @@ struct TcMaps {
   CUtensorMap q, k, v, rab, out, cache;
 };
 bool tc_supported_dim(int D);
+int tc_kernel_dim(int D);     // head dim of the kernel variant that runs D (32/64/128/256)
 int tc_swizzle_bytes(int D, int elem_bytes);  // row width of one TMA box / UMMA swizzle atom
 int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
 int tc_rab_box_rows();        // rows of one rab / custom-mask load box (64 columns each)

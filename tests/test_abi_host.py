@@ -39,7 +39,9 @@ def _desc(**kw):
     (dict(mask_type=_abi.HSTU_MASK_CUSTOM, rab_heads=1), _abi.HSTU_ERR_INVALID_ARG),
     (dict(mask_type=_abi.HSTU_MASK_CUSTOM, max_seqlen=100), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(mask_type=7), _abi.HSTU_ERR_INVALID_ARG),
-    (dict(head_dim=48), _abi.HSTU_ERR_UNSUPPORTED),                      # no tensor-core tile
+    (dict(head_dim=40), _abi.HSTU_ERR_UNSUPPORTED),                      # not a multiple of 16
+    (dict(head_dim=272), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(dtype=_abi.HSTU_FP8_E4M3, head_dim=48), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(dtype=_abi.HSTU_F32, head_dim=300), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(head_dim=0), _abi.HSTU_ERR_INVALID_ARG),
     (dict(max_seqlen=0), _abi.HSTU_ERR_INVALID_ARG),

@@ -82,13 +82,36 @@ def test_small_workloads(cuda_device, w):
     _check(w, cuda_device)
 
 
+HEAD_DIMS = [16, 32, 48, 64, 80, 96, 112, 128, 144, 160, 176, 192, 208, 224, 240, 256]
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
-@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("d", HEAD_DIMS)
 @pytest.mark.parametrize("causal", [True, False])
 def test_head_dims(cuda_device, dtype, d, causal):
+    """Every multiple of 16 up to 256: the tensor-core kernels built for 32, 64, 128 and 256
+    run the others with zero-filled extra columns, whose output columns are never stored
+    (the output buffer is filled with NaN first, so a stray store would show)."""
     w = W.Workload(name=f"{dtype}_d{d}", dtype=dtype, batch=3, num_heads_q=2, num_heads_kv=1,
                    head_dim=d, max_seqlen=300, len_lo=1, len_hi=300, causal=causal, seed=7 + d)
     _check(w, cuda_device)
+
+
+@pytest.mark.parametrize("d", [16, 48, 80, 208])
+def test_padded_head_dims_store_nothing_past_the_output(cuda_device, d):
+    """A padded head dim writes exactly its D columns per row: the output is the front of a
+    larger buffer whose tail must keep its sentinel (the last rows' extra columns would
+    land there)."""
+    w = W.Workload(name=f"pad{d}", dtype="bf16", batch=2, num_heads_q=2, num_heads_kv=2,
+                   head_dim=d, max_seqlen=260, len_lo=100, len_hi=260, causal=True, seed=90 + d)
+    inp = W.generate(w)
+    T = int(inp["seq_offsets"][-1])
+    n = T * 2 * d
+    flat = torch.full((n + 4096,), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    got = _gpu(inp, cuda_device, out=flat[:n].view(T, 2, d))
+    assert torch.all(flat[n:] == 7.0)
+    err = _rel_err(got, _oracle_full(inp), inp["seq_offsets"].numpy())
+    assert err <= TOL["bf16"], f"d={d}: rel err {err:.3e}"
 
 
 @pytest.mark.parametrize("lengths", [(1,), (5, 1, 15), (128,), (129, 127), (256, 255, 257),
