@@ -37,7 +37,7 @@ def out_dtype(dtype: torch.dtype) -> torch.dtype:
 def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, index_is_int64,
           causal, target_group_size, has_rab, has_num_context, has_num_targets, watchdog_ms=0,
           layout="jagged", rab_heads=0, custom_mask=False, is_delta_qk=False, max_seqlen_k=0,
-          page_size=0):
+          page_size=0, descale=0):
     d = _abi.Desc()
     d.dtype = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     d.batch = int(batch)
@@ -60,6 +60,7 @@ def _desc(*, dtype, batch, num_heads_q, num_heads_kv, head_dim, max_seqlen, inde
     d.is_delta_qk = int(bool(is_delta_qk))
     d.max_seqlen_k = int(max_seqlen_k)
     d.page_size = int(page_size)
+    d.descale = int(descale)
     return d
 
 
@@ -94,12 +95,15 @@ class HstuFwdPlan:
 
     def run(self, q, k, v, seq_offsets, out, *, rab=None, num_context=None, num_targets=None,
             alpha=1.0, silu_scale=None, stream=None, mask=None, seq_offsets_k=None,
-            kv_cache=None, page_offsets=None, page_ids=None, last_page_len=None):
+            kv_cache=None, page_offsets=None, page_ids=None, last_page_len=None, descale=None):
+        """descale: (q, k, v) fp32 device tensors of the plan's descale granularity (FP8
+        plans whose granularity is not the plain cast)."""
         if silu_scale is None:
             silu_scale = 1.0 / _key_bound(self.desc)
         if stream is None:
             stream = torch.cuda.current_stream(q.device)
         ptr = lambda t: 0 if t is None else t.data_ptr()
+        kv = None
         if _key_side(self.desc):
             kv = _abi.KV()
             kv.seq_offsets_k = ptr(seq_offsets_k) or None
@@ -109,6 +113,17 @@ class HstuFwdPlan:
             kv.page_offsets = ptr(page_offsets) or None
             kv.page_ids = ptr(page_ids) or None
             kv.last_page_len = ptr(last_page_len) or None
+        if self.desc.descale != _abi.HSTU_DESCALE_CAST:
+            ds = _abi.Descale()
+            ds.q, ds.k, ds.v = (t.data_ptr() for t in descale)
+            _abi.check(self._keep.hstu_fwd_run_fp8(
+                self._h, q.data_ptr(), ptr(k) or None, ptr(v) or None, ptr(seq_offsets) or None,
+                None if kv is None else ctypes.byref(kv), ptr(rab) or None,
+                ptr(num_context) or None, ptr(num_targets) or None, ctypes.byref(ds),
+                q.shape[0], float(alpha), float(silu_scale), out.data_ptr(),
+                stream.cuda_stream or None), "hstu_fwd_run_fp8")
+            return out
+        if kv is not None:
             extra = mask if self.desc.mask_type == _abi.HSTU_MASK_CUSTOM else rab
             _abi.check(self._keep.hstu_fwd_run_kv(
                 self._h, q.data_ptr(), ptr(k) or None, ptr(v) or None, ptr(seq_offsets) or None,
@@ -178,11 +193,45 @@ def _rab_heads(rab, B, Nq, S):
     return 1 if rab.shape[1] == 1 and Nq > 1 else 0
 
 
+def _descales(q_descale, k_descale, v_descale, *, dev, B, Nq, Nk, Sq, Sk):
+    """FP8 descale factors as the C ABI takes them: (granularity, (q, k, v) fp32 device
+    tensors), from Python floats or one-element tensors (per tensor), [B] (per sequence),
+    q [B, Nq] and k, v [B, Nk] (per sequence and head), or q [B, ceil(Sq / 128), Nq] and
+    k, v [B, ceil(Sk / 128), Nk] (per block of 128 query rows / key positions). All
+    three None: the plain cast."""
+    given = [x is not None for x in (q_descale, k_descale, v_descale)]
+    if not any(given):
+        return _abi.HSTU_DESCALE_CAST, None
+    if not all(given):
+        raise ValueError("q_descale, k_descale and v_descale go together")
+    ts = []
+    for name, x in (("q_descale", q_descale), ("k_descale", k_descale), ("v_descale", v_descale)):
+        if isinstance(x, torch.Tensor):
+            _check_tensor(x, name, torch.float32, dev)
+            ts.append(x)
+        else:
+            ts.append(torch.tensor([float(x)], dtype=torch.float32, device=dev))
+    qd, kd, vd = ts
+    if kd.shape != vd.shape:
+        raise ValueError("k_descale and v_descale must have one shape")
+    cdiv = lambda a, b: -(-a // b)
+    if qd.numel() == 1 and qd.dim() <= 1 and kd.numel() == 1 and kd.dim() <= 1:
+        return _abi.HSTU_DESCALE_TENSOR, ts
+    shapes = {1: ((B,), (B,), _abi.HSTU_DESCALE_BATCH),
+              2: ((B, Nq), (B, Nk), _abi.HSTU_DESCALE_HEAD),
+              3: ((B, cdiv(Sq, 128), Nq), (B, cdiv(Sk, 128), Nk), _abi.HSTU_DESCALE_BLOCK)}
+    want = shapes.get(qd.dim())
+    if want is None or tuple(qd.shape) != want[0] or tuple(kd.shape) != want[1]:
+        raise ValueError(f"descale shapes q {list(qd.shape)}, k/v {list(kd.shape)} match no "
+                         "granularity (one factor, [B], [B, N] or [B, ceil(S/128), N])")
+    return want[2], ts
+
+
 def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_context=None,
              num_targets=None, causal=True, target_group_size=0, alpha=1.0, silu_scale=None,
              out=None, watchdog_ms=0, layout="jagged", mask=None, seq_offsets_k=None,
              max_seqlen_k=None, kv_cache=None, page_offsets=None, page_ids=None,
-             last_page_len=None, q_descale=1.0, k_descale=1.0, v_descale=1.0):
+             last_page_len=None, q_descale=None, k_descale=None, v_descale=None):
     """HSTU forward.
 
     layout "jagged" (default): q [T, Nq, D], k/v [T, Nk, D], seq_offsets [B+1] int32/int64,
@@ -204,10 +253,13 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     max_seqlen) bounds Lk and is the S of rab and mask; silu_scale then defaults to
     1/max_seqlen_k.
 
-    FP8 (feature table, "FP8 quantization types: cast"): q, k, v (and kv_cache) of dtype
-    torch.float8_e4m3fn, out bf16; q_descale, k_descale, v_descale are per-tensor factors
-    (the values are q_descale * q etc.), folded into alpha and silu_scale. Head dims 32,
-    64, 128; no rab or custom mask.
+    FP8 (feature table, "FP8 quantization types"): q, k, v (and kv_cache) of dtype
+    torch.float8_e4m3fn, out bf16; rab (no key side) bf16. q_descale, k_descale, v_descale
+    (all or none; none is the plain cast) give the values as factor * stored value: floats
+    or one-element fp32 tensors (per tensor), [B] (per sequence), q [B, Nq] and k, v
+    [B, Nk] (per sequence and head), q [B, ceil(max_seqlen / 128), Nq] and k, v
+    [B, ceil(Sk / 128), Nk] (per block of 128 query rows / key positions). Head dims up to
+    128; no custom mask.
     """
     dev = q.device
     if dev.type != "cuda":
@@ -285,8 +337,15 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
         raise ValueError("max_seqlen_k goes with seq_offsets_k or kv_cache")
     Sk = int(max_seqlen_k) if max_seqlen_k is not None else int(max_seqlen)
     if rab is not None:
-        _check_tensor(rab, "rab", q.dtype, dev, 4)
+        _check_tensor(rab, "rab", out_dtype(q.dtype), dev, 4)  # (bf16 for FP8 inputs)
     rab_heads = _rab_heads(rab, B, Nq, Sk)
+    if q.dtype == torch.float8_e4m3fn:
+        descale, ds = _descales(q_descale, k_descale, v_descale, dev=dev, B=B, Nq=Nq,
+                                Nk=k3.shape[1], Sq=int(max_seqlen), Sk=Sk)
+    elif (q_descale, k_descale, v_descale) != (None, None, None):
+        raise ValueError("descale factors go with FP8 E4M3 inputs")
+    else:
+        descale, ds = _abi.HSTU_DESCALE_CAST, None
     custom = mask is not None
     if custom:
         if rab is not None or num_context is not None or num_targets is not None:
@@ -298,7 +357,7 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     key = (dev.index, stream.cuda_stream, q.dtype, B, Nq, k3.shape[1], D, int(max_seqlen),
            idx_dtype, bool(causal), int(target_group_size), rab is not None,
            num_context is not None, num_targets is not None, int(watchdog_ms), layout, rab_heads,
-           custom, seq_offsets_k is not None, page_size, Sk if key_side else 0)
+           custom, seq_offsets_k is not None, page_size, Sk if key_side else 0, descale)
     plan = _plans.get(key)
     if plan is None:
         with torch.cuda.device(dev):
@@ -310,20 +369,15 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
                                has_num_targets=num_targets is not None, watchdog_ms=watchdog_ms,
                                layout=layout, rab_heads=rab_heads, custom_mask=custom,
                                is_delta_qk=seq_offsets_k is not None,
-                               max_seqlen_k=Sk if key_side else 0, page_size=page_size)
+                               max_seqlen_k=Sk if key_side else 0, page_size=page_size,
+                               descale=descale)
         _plans[key] = plan
-    if q.dtype == torch.float8_e4m3fn:  # per-tensor descale factors: x = alpha*qd*kd*(q.k)
-        if silu_scale is None:
-            silu_scale = 1.0 / (Sk if key_side else int(max_seqlen))
-        alpha = float(alpha) * float(q_descale) * float(k_descale)
-        silu_scale = float(silu_scale) * float(v_descale)
-    elif (q_descale, k_descale, v_descale) != (1.0, 1.0, 1.0):
-        raise ValueError("descale factors go with FP8 E4M3 inputs")
     with torch.cuda.device(dev):
         plan.run(q3, k3, v3, seq_offsets, out3, rab=rab, num_context=num_context,
                  num_targets=num_targets, alpha=alpha, silu_scale=silu_scale, stream=stream,
                  mask=mask, seq_offsets_k=seq_offsets_k, kv_cache=kv_cache,
-                 page_offsets=page_offsets, page_ids=page_ids, last_page_len=last_page_len)
+                 page_offsets=page_offsets, page_ids=page_ids, last_page_len=last_page_len,
+                 descale=ds)
     return res
 
 

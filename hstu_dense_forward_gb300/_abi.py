@@ -20,6 +20,8 @@ HSTU_F32, HSTU_F16, HSTU_BF16, HSTU_FP8_E4M3 = 0, 1, 2, 3
 HSTU_MASK_CAUSAL, HSTU_MASK_UPPER, HSTU_MASK_NONE, HSTU_MASK_CUSTOM = 0, 1, 2, 3
 HSTU_DEVERR_NONE, HSTU_DEVERR_OFFSETS, HSTU_DEVERR_TIMEOUT = 0, 1, 2
 HSTU_LAYOUT_JAGGED, HSTU_LAYOUT_NORMAL = 0, 1
+(HSTU_DESCALE_CAST, HSTU_DESCALE_TENSOR, HSTU_DESCALE_BATCH, HSTU_DESCALE_HEAD,
+ HSTU_DESCALE_BLOCK) = 0, 1, 2, 3, 4
 
 
 class Desc(ctypes.Structure):
@@ -42,6 +44,7 @@ class Desc(ctypes.Structure):
         ("is_delta_qk", ctypes.c_int),
         ("max_seqlen_k", ctypes.c_int),
         ("page_size", ctypes.c_int),
+        ("descale", ctypes.c_int),
         ("reserved", ctypes.c_int),
     ]
 
@@ -57,6 +60,11 @@ class KV(ctypes.Structure):
         ("page_ids", ctypes.c_void_p),
         ("last_page_len", ctypes.c_void_p),
     ]
+
+
+class Descale(ctypes.Structure):
+    """hstu_fwd_descale: FP8 descale factor arrays (device fp32 pointers)."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p)]
 
 
 class HstuError(RuntimeError):
@@ -111,6 +119,9 @@ def lib():
         L.hstu_fwd_run_noalloc.restype = ctypes.c_int
         L.hstu_fwd_run_noalloc.argtypes = [ctypes.POINTER(Desc), vp, vp, vp, vp, vp, vp, vp, ll, f,
                                            f, vp, vp]
+        L.hstu_fwd_run_fp8.restype = ctypes.c_int
+        L.hstu_fwd_run_fp8.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(KV), vp, vp, vp,
+                                       ctypes.POINTER(Descale), ll, f, f, vp, vp]
         L.hstu_fwd_trace_read.restype = ctypes.c_int
         L.hstu_fwd_trace_read.argtypes = [vp, vp, ll]
         L.hstu_status_string.restype = ctypes.c_char_p

@@ -139,6 +139,9 @@ static int key_bound(const hstu_fwd_desc& d) {
 static hstu_status validate_desc(const hstu_fwd_desc* d) {
   if (!d) return HSTU_ERR_INVALID_ARG;
   if (d->reserved) return HSTU_ERR_INVALID_ARG;
+  if (d->descale < HSTU_DESCALE_CAST || d->descale > HSTU_DESCALE_BLOCK ||
+      (d->descale != HSTU_DESCALE_CAST && d->dtype != HSTU_FP8_E4M3))
+    return HSTU_ERR_INVALID_ARG;
   // flags are 0 or 1
   for (int f : {d->is_delta_qk, d->index_is_int64, d->has_rab, d->has_num_context,
                 d->has_num_targets})
@@ -175,10 +178,11 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
     if (d->dtype != HSTU_F32 && key_bound(*d) % 8 != 0) return HSTU_ERR_UNSUPPORTED;
   }
   if (d->dtype == HSTU_FP8_E4M3) {
-    // FP8 E4M3 inputs: head dims 32, 64, 128; no rab and no custom mask (their tiles are
-    // 16-bit and share no path with the 8-bit products here)
-    if (d->head_dim != 32 && d->head_dim != 64 && d->head_dim != 128) return HSTU_ERR_UNSUPPORTED;
-    if (d->has_rab || d->mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_UNSUPPORTED;
+    // FP8 E4M3 inputs: head dims up to 128; bf16 rab without a key side; no custom mask
+    // (it multiplies 16-bit P, which the 8-bit products do not have)
+    if (!hstu::tc_supported_dim(d->head_dim) || d->head_dim > 128) return HSTU_ERR_UNSUPPORTED;
+    if (d->mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_UNSUPPORTED;
+    if (d->has_rab && (key_side(*d) || key_bound(*d) % 8 != 0)) return HSTU_ERR_UNSUPPORTED;
   } else if (d->dtype == HSTU_F32) {
     if (d->head_dim > 256) return HSTU_ERR_UNSUPPORTED;
   } else {
@@ -323,7 +327,8 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
                                     : CU_TENSOR_MAP_SWIZZLE_NONE);
   if (ok && rab) {
     const uint64_t S = (uint64_t)key_bound(d);
-    ok = encode3d(&P->maps.rab, ty, rab, S, S, (uint64_t)d.batch * (d.rab_heads == 1 ? 1 : Nq),
+    // rab of FP8 plans is bf16
+    ok = encode3d(&P->maps.rab, fp8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : ty, rab, S, S, (uint64_t)d.batch * (d.rab_heads == 1 ? 1 : Nq),
                   S * 2, S * S * 2, 64,
                   hstu::tc_rab_box_rows(), 1, CU_TENSOR_MAP_SWIZZLE_128B);
   } else if (ok) {
@@ -378,8 +383,13 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
                             const void* seq_offsets, const hstu_fwd_kv* kv, const void* rab,
                             bool is_mask, const void* num_context, const void* num_targets,
                             long long total_tokens, float alpha, float silu_scale, void* out,
-                            void* stream) {
+                            void* stream, const hstu_fwd_descale* ds = nullptr) {
   const hstu_fwd_desc& d = P->desc;
+  if (d.descale != HSTU_DESCALE_CAST) {  // factor arrays: present, fp32-aligned
+    if (!ds || !ds->q || !ds->k || !ds->v) return HSTU_ERR_INVALID_ARG;
+    for (const float* f : {ds->q, ds->k, ds->v})
+      if (reinterpret_cast<uintptr_t>(f) % 4 != 0) return HSTU_ERR_INVALID_ARG;
+  }
   if (total_tokens < 0 || total_tokens > 0x7fffffffll) return HSTU_ERR_INVALID_ARG;
   if (!kv_args_ok(d, kv)) return HSTU_ERR_INVALID_ARG;
   if (d.batch == 0 || d.num_heads_q == 0 || total_tokens == 0) return HSTU_OK;  // empty input
@@ -442,6 +452,14 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   p.silu_scale = silu_scale;
   p.fp8 = d.dtype == HSTU_FP8_E4M3 ? 1 : 0;
   p.test_stall = P->test_stall;
+  if (d.descale != HSTU_DESCALE_CAST) {
+    p.q_ds = ds->q;
+    p.k_ds = ds->k;
+    p.v_ds = ds->v;
+    p.ds_mode = d.descale;
+    p.ds_qb = hstu::ceil_div(d.max_seqlen, hstu::kTileM);
+    p.ds_kb = hstu::ceil_div(key_bound(d), hstu::kTileN);
+  }
   set_rab_mode(p, d, is_mask);
 #if HSTU_TRACE
   // run r of the plan records into launch slot r % kSlots
@@ -469,9 +487,20 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
                          const void* seq_offsets, const void* rab, const void* num_context,
                          const void* num_targets, long long total_tokens, float alpha,
                          float silu_scale, void* out, void* stream) {
-  if (!P || P->desc.mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_INVALID_ARG;
+  if (!P || P->desc.mask_type == HSTU_MASK_CUSTOM || P->desc.descale != HSTU_DESCALE_CAST)
+    return HSTU_ERR_INVALID_ARG;
   return run_impl(P, q, k, v, seq_offsets, nullptr, rab, false, num_context, num_targets,
                   total_tokens, alpha, silu_scale, out, stream);
+}
+
+hstu_status hstu_fwd_run_fp8(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
+                             const void* seq_offsets, const hstu_fwd_kv* kv, const void* rab,
+                             const void* num_context, const void* num_targets,
+                             const hstu_fwd_descale* descale, long long total_tokens,
+                             float alpha, float silu_scale, void* out, void* stream) {
+  if (!P || P->desc.dtype != HSTU_FP8_E4M3) return HSTU_ERR_INVALID_ARG;
+  return run_impl(P, q, k, v, seq_offsets, kv, rab, false, num_context, num_targets,
+                  total_tokens, alpha, silu_scale, out, stream, descale);
 }
 
 hstu_status hstu_fwd_run_kv(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
@@ -479,7 +508,7 @@ hstu_status hstu_fwd_run_kv(hstu_fwd_plan* P, const void* q, const void* k, cons
                             const void* rab_or_mask, const void* num_context,
                             const void* num_targets, long long total_tokens, float alpha,
                             float silu_scale, void* out, void* stream) {
-  if (!P) return HSTU_ERR_INVALID_ARG;
+  if (!P || P->desc.descale != HSTU_DESCALE_CAST) return HSTU_ERR_INVALID_ARG;
   const bool custom = P->desc.mask_type == HSTU_MASK_CUSTOM;
   if (custom && (num_context || num_targets)) return HSTU_ERR_INVALID_ARG;
   if (custom && !rab_or_mask && P->desc.batch > 0 && P->desc.num_heads_q > 0 && total_tokens > 0)

@@ -74,7 +74,7 @@ constexpr int kRabBoxRows = 32;
 template <int D, int RAB, bool F8 = false>
 struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head_dim");
-  static_assert(!F8 || (D <= 128 && !RAB), "fp8: head_dim <= 128, no rab");
+  static_assert(!F8 || (D <= 128 && RAB != 2), "fp8: head_dim <= 128, rab in the epilogue");
   static constexpr bool RM = RAB == 2;        // rab by the tensor core
   static constexpr bool EPI_RAB = RAB == 1;   // rab / mask tiles read by the epilogue
   static_assert(!RM || D <= 64, "rab by the tensor core: head_dim <= 64");
@@ -810,6 +810,29 @@ __device__ __forceinline__ uint32_t swizzle(uint32_t o) {
   }
 }
 
+// FP8 descale factor of (sequence b, block blk, head h) for the granularity p.ds_mode (one
+// factor; one per sequence; per sequence and head; per sequence, 128-row block and head,
+// with nb blocks per sequence and n heads).
+__device__ __forceinline__ long long ds_index(const FwdParams& p, int b, int blk, int h, int nb,
+                                              int n) {
+  if (p.ds_mode == 1) return 0;
+  if (p.ds_mode == 2) return b;
+  if (p.ds_mode == 3) return (long long)b * n + h;
+  return ((long long)b * nb + blk) * n + h;
+}
+
+// The v factor of an item's output: its v descale (one per item below block granularity),
+// or the largest |v descale| over the sequence's key blocks, relative to which the
+// epilogue scales P for each key tile (block granularity). 1 for the plain cast.
+__device__ __forceinline__ float item_v_scale(const FwdParams& p, const Item& it) {
+  if (p.ds_mode == 0) return 1.f;
+  if (p.ds_mode < 4) return __ldg(p.v_ds + ds_index(p, it.b, 0, it.hk, p.ds_kb, p.Nk));
+  float m = 0.f;
+  for (int x = 0; x * kTileN < it.geom.L; ++x)
+    m = fmaxf(m, fabsf(__ldg(p.v_ds + ds_index(p, it.b, x, it.hk, p.ds_kb, p.Nk))));
+  return m;
+}
+
 template <int D, bool BF16, int RAB, bool MASK, bool KV, bool F8>
 __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                          const CUtensorMap* tm_o, long long total, int warp, int lane) {
@@ -838,6 +861,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kDrainBeg, slot);
     const Item& pit = bars->info[slot];
     const int pi = pit.m0 + r;  // query row within the sequence
+    float osc = p.silu_scale;   // (FP8: times the item's v factor)
+    if constexpr (F8) osc *= item_v_scale(p, pit);
     const uint32_t ob = u % C::NO;  // the item's O accumulator
     if (!warp_wait(bars, &bars->o_full[ob], (u / C::NO) & 1, p)) return false;
     ptx::tc_fence_after();
@@ -865,7 +890,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         for (int e = 0; e < 4; ++e) {
           float o0, o1;
           ptx::mul_f32x2(o0, o1, __uint_as_float(part[v4 * 8 + 2 * e]),
-                         __uint_as_float(part[v4 * 8 + 2 * e + 1]), p.silu_scale, p.silu_scale);
+                         __uint_as_float(part[v4 * 8 + 2 * e + 1]), osc, osc);
           w[e] = pack2<OUT_BF16>(o0, o1);
         }
         if constexpr (C::STAGE) {
@@ -922,6 +947,20 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     const RowRange rr = row_range(it.geom, i, p.mask_type);
     // without a key side, the key tiles that need no mask are a prefix of the item's tiles
     const int n_full = KV ? 0 : full_tiles(it.geom, m0p, kTileM, kTileN, p.mask_type);
+    // FP8 descales: alpha * qd * kd folds into the SiLU argument's factor, vd into P (block
+    // granularity: per key tile, relative to the item's v factor) or the output scale
+    float ha_item = half_alpha, qds = 1.f, p8_per_v = kP8Scale;
+    if constexpr (F8) {
+      if (p.ds_mode != 0) {
+        qds = __ldg(p.q_ds + ds_index(p, it.b, it.m0 / kTileM, it.h, p.ds_qb, p.Nq));
+        if (p.ds_mode < 4) {
+          ha_item = half_alpha * qds * __ldg(p.k_ds + ds_index(p, it.b, 0, it.hk, p.ds_kb, p.Nk));
+        } else {
+          const float vm = item_v_scale(p, it);
+          p8_per_v = vm > 0.f ? kP8Scale / vm : 0.f;
+        }
+      }
+    }
     int gtile = 0;  // tiles of this item processed by this group
     for (int j = 0; j < it.n_kv; ++j, ++t) {
       if ((int)(t % C::EPI_GROUPS) != group) continue;  // the other group's tile
@@ -940,6 +979,14 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
         kt.cached = false;
       }
       const int n0 = kt.x * kTileN;
+      float ha = ha_item, p8 = kP8Scale;
+      if constexpr (F8) {
+        if (p.ds_mode == 4) {
+          const long long ki = ds_index(p, it.b, kt.x, it.hk, p.ds_kb, p.Nk);
+          ha = half_alpha * qds * __ldg(p.k_ds + ki);
+          p8 = p8_per_v * __ldg(p.v_ds + ki);
+        }
+      }
       bool full;
       if constexpr (KV)
         full = kt.clo == 0 && kt.chi == kTileN &&
@@ -979,7 +1026,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 #pragma unroll
         for (int e = 0; e < 32; e += 2)
           ptx::mul_f32x2(h[e], h[e + 1], __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
-                         half_alpha, half_alpha);
+                         ha, ha);
         uint32_t mw[16];  // custom-mask pairs (MASK)
         if constexpr (C::EPI_RAB) {
           // rab / custom-mask tile: two 64-column TMA boxes of 128 rows x 128 bytes with
@@ -1019,10 +1066,11 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           const float t0 = ptx::tanh_approx(h[2 * e]), t1 = ptx::tanh_approx(h[2 * e + 1]);
           float p0, p1;
           if constexpr (F8) {
-            // kP8Scale * P = (kP8Scale * h) * tanh(h) + kP8Scale * h: P scaled by a power of
-            // two (exact) so that typical values stay in E4M3's normal range
+            // p8 * P = (p8 * h) * tanh(h) + p8 * h with p8 = kP8Scale (a power of two, so
+            // that typical values stay in E4M3's normal range), times vd / max vd for block
+            // descales
             float s0, s1;
-            ptx::mul_f32x2(s0, s1, h[2 * e], h[2 * e + 1], kP8Scale, kP8Scale);
+            ptx::mul_f32x2(s0, s1, h[2 * e], h[2 * e + 1], p8, p8);
             ptx::fma_f32x2(p0, p1, s0, s1, t0, t1, s0, s1);
             const uint32_t q = ptx::cvt_e4m3x2_f32(p0, p1);  // keys 2e, 2e + 1
             if (e & 1)
@@ -1179,7 +1227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) HSTU_TRACE_EV(p, trace::kRoleCta, trace::kDepDone, 0);
 
   if (warp < kEpiWarps) {
-    epilogue<D, BF16 && !F8, RAB, MASK, KV, F8>(p, bars, smem, tmem, &tm_o, total, warp, lane);
+    epilogue<D, BF16, RAB, MASK, KV, F8>(p, bars, smem, tmem, &tm_o, total, warp, lane);
   } else if (warp == kProducerWarp) {
     if (lane == 0) producer_k<D, RAB, KV, F8>(p, bars, smem, &tm_k, &tm_c, total);
   } else if (warp == kQProducerWarp) {

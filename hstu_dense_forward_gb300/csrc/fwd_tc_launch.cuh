@@ -58,10 +58,12 @@ cudaError_t dispatch_rab_mma(const FwdParams& p, const TcMaps& m, int bf16, int 
 cudaError_t dispatch_mask(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                           cudaStream_t st, bool pdl, bool prepare);
 
-// FP8 E4M3 variants (fwd_tc_f8.cu): head dims 32, 64, 128, no rab or custom mask, with or
-// without a key side.
+// FP8 E4M3 variants (fwd_tc_f8.cu): head dims up to 128, no custom mask, with or without a
+// key side; with rab (fwd_tc_f8_rab.cu) without a key side.
 cudaError_t dispatch_f8(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st, bool pdl,
                         bool prepare);
+cudaError_t dispatch_f8_rab(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
+                            bool pdl, bool prepare);
 
 // Key-side variants (fwd_tc_kv.cu, fwd_tc_kv_mask.cu): own k/v offsets and / or a KV cache.
 cudaError_t dispatch_kv(const FwdParams& p, const TcMaps& m, int bf16, int grid,

@@ -54,6 +54,14 @@ struct FwdParams {
   // pattern of 1/alpha in the input type (set by the host when 1/alpha is finite there)
   int rab_mma;
   unsigned rab_ident;
+  // FP8 descale factors (an element's value is its factor times the stored E4M3 value):
+  // device fp32 arrays indexed by ds_index; ds_mode 0 is the plain cast (no arrays)
+  const float* q_ds;
+  const float* k_ds;
+  const float* v_ds;
+  int ds_mode;  // 0 cast, 1 per tensor, 2 per sequence, 3 per sequence and head, 4 per block
+  int ds_qb;    // 128-row query blocks per sequence (ceil(Sq / 128)), mode 4
+  int ds_kb;    // 128-position key blocks per sequence (ceil(S / 128)), mode 4
 };
 
 // FP8 kernels hold kP8Scale * P (E4M3) for the second product; silu_scale is divided by it.

@@ -66,12 +66,35 @@ typedef enum {
 
 /* Element type of q, k, v, rab and out (Inputs and Outputs table: "the type must
  * match q"; the output "same as q"). HSTU_FP8_E4M3 (feature table, "FP8 quantization
- * types: cast"): q, k, v and the KV cache hold FP8 E4M3 bytes (the caller's cast, with
- * per-tensor descale factors folded into alpha for q and k and into silu_scale for v);
- * both products run on 8-bit tensor cores with fp32 accumulation, P is rounded to E4M3
- * (saturating) for the second one, and out is bf16. Head dims 32, 64, 128; no rab or
- * custom mask (HSTU_ERR_UNSUPPORTED); not on the allocation-free entry point. */
+ * types"): q, k, v and the KV cache hold FP8 E4M3 bytes, either a plain cast or scaled
+ * copies with descale factors (desc.descale, hstu_fwd_run_fp8); both products run on
+ * 8-bit tensor cores with fp32 accumulation, P is rounded to E4M3 (saturating) for the
+ * second one, and out is bf16. rab (has_rab, no key side) is bf16 [B, Nq or 1, S, S] and
+ * is added in fp32. Head dims 16 to 128 in steps of 16; no custom mask
+ * (HSTU_ERR_UNSUPPORTED); not on the allocation-free entry point. */
 typedef enum { HSTU_F32 = 0, HSTU_F16 = 1, HSTU_BF16 = 2, HSTU_FP8_E4M3 = 3 } hstu_dtype;
+
+/* Granularity of the FP8 descale factors (feature table, "FP8 quantization types": cast,
+ * per-tensor, per-batch, per-head, per-block). The value of an element is its descale
+ * factor times the stored E4M3 value. Factor arrays are fp32 (hstu_fwd_descale):
+ *   CAST    no factors (every factor 1)
+ *   TENSOR  q [1], k [1], v [1]
+ *   BATCH   q [B], k [B], v [B]: one factor per sequence
+ *   HEAD    q [B, Nq], k [B, Nk], v [B, Nk]: per sequence and head
+ *   BLOCK   q [B, ceil(max_seqlen / 128), Nq], k and v [B, ceil(Sk / 128), Nk]: per
+ *           sequence, head and block of 128 query rows (q) or 128 key positions (k, v),
+ *           counted from the sequence's first query row / first key (cached history
+ *           included); Sk is the key bound (max_seqlen_k, else max_seqlen).
+ * BLOCK factors of v scale P before its E4M3 rounding relative to the largest |factor| of
+ * the sequence's v blocks, so blocks whose factors are far below that largest one lose
+ * precision to E4M3's subnormal range. */
+typedef enum {
+  HSTU_DESCALE_CAST = 0,
+  HSTU_DESCALE_TENSOR = 1,
+  HSTU_DESCALE_BATCH = 2,
+  HSTU_DESCALE_HEAD = 3,
+  HSTU_DESCALE_BLOCK = 4
+} hstu_descale_granularity;
 
 /* Tensor layout (Inputs and Outputs table, layout): "jagged" q [T, Nq, D] with
  * seq_offsets, or "normal" q [B, S, Nq, D] where every sequence has S = max_seqlen
@@ -102,7 +125,8 @@ typedef struct {
   int batch;             /* B in [0, 2^20]; 0 = empty input, run does nothing */
   int num_heads_q;       /* Nq >= 0; 0 = empty input */
   int num_heads_kv;      /* Nk >= 1, Nq % Nk == 0 (Inputs and Outputs table, k) */
-  int head_dim;          /* D: f16/bf16 need D in {32, 64, 128, 256}; f32 needs 1 <= D <= 256 */
+  int head_dim;          /* D: f16/bf16 need a multiple of 16 in [16, 256], FP8 one in
+                            [16, 128]; f32 needs 1 <= D <= 256 */
   int max_seqlen;        /* S in [1, 131072]: bound on every L; rab is [B, Nq, S, S];
                             for rab with f16/bf16, S must be a multiple of 8 */
   int index_is_int64;    /* 1: seq_offsets/num_context/num_targets are int64, 0: int32 */
@@ -127,6 +151,8 @@ typedef struct {
                             query rows of a sequence */
   int page_size;         /* 0, or the rows of one KV-cache page: 32, 128 or 256 (Inputs and
                             Outputs table, kv_cache); jagged layout only */
+  int descale;           /* hstu_descale_granularity; FP8 plans only (0 otherwise). Plans
+                            with a value other than CAST run through hstu_fwd_run_fp8 */
   int reserved;          /* must be 0 */
 } hstu_fwd_desc;
 
@@ -214,6 +240,30 @@ HSTU_API hstu_status hstu_fwd_run_kv(hstu_fwd_plan* plan, const void* q, const v
                                      const void* num_context, const void* num_targets,
                                      long long total_tokens, float alpha, float silu_scale,
                                      void* out, void* stream);
+
+/* Descale factor arrays of hstu_fwd_run_fp8: DEVICE pointers to fp32, 4-byte aligned, of
+ * the lengths that desc.descale gives (hstu_descale_granularity). */
+typedef struct {
+  const float* q;
+  const float* k;
+  const float* v;
+} hstu_fwd_descale;
+
+/*
+ * Enqueue one forward of an FP8 E4M3 plan with descale factors (feature table, "FP8
+ * quantization types"): x_ij = alpha * (qd q_i) . (kd k_j) (+ rab), and v_j is vd v_j,
+ * with qd, kd, vd the factors of desc.descale's granularity for row i and key j.
+ * kv as for hstu_fwd_run_kv (NULL for a plan without a key side), rab as for hstu_fwd_run
+ * (bf16; not with a key side), other arguments as for hstu_fwd_run. descale may be NULL
+ * only for a CAST plan. Returns HSTU_ERR_INVALID_ARG for a plan that is not FP8, and
+ * hstu_fwd_run / hstu_fwd_run_kv do for an FP8 plan whose granularity is not CAST.
+ */
+HSTU_API hstu_status hstu_fwd_run_fp8(hstu_fwd_plan* plan, const void* q, const void* k,
+                                      const void* v, const void* seq_offsets,
+                                      const hstu_fwd_kv* kv, const void* rab,
+                                      const void* num_context, const void* num_targets,
+                                      const hstu_fwd_descale* descale, long long total_tokens,
+                                      float alpha, float silu_scale, void* out, void* stream);
 
 /* Free the workspace. NULL is accepted. Waits for the plan's last run to complete first
  * (an event recorded on that run's stream; other streams and plans are not waited for). */

@@ -243,6 +243,38 @@ def hstu_fwd_rows(q, k, v, seq_offsets, rows, *, rab=None, num_context=None, num
     return out
 
 
+DESCALE_GRANULARITIES = ("tensor", "batch", "head", "block")
+
+
+def dequantize(x, descale, granularity, seq_offsets, *, block=128):
+    """Values of FP8 inputs with descale factors (feature table, "FP8 quantization types":
+    per-tensor, per-batch, per-head, per-block): element (t, n, d) of the jagged tensor x
+    [T, N, D] is factor * x[t, n, d], with the factor of its sequence b (seq_offsets[b] <=
+    t < seq_offsets[b + 1]), head n and block (t - seq_offsets[b]) // block:
+      "tensor" descale [1]; "batch" [B]; "head" [B, N]; "block" [B, nblocks, N].
+    Rows outside every sequence become 0. Plain loops, fp64."""
+    x = _f64(x)
+    so = _i64(seq_offsets)
+    f = np.asarray(descale, dtype=np.float64)
+    if granularity not in DESCALE_GRANULARITIES:
+        raise ValueError(f"granularity must be one of {DESCALE_GRANULARITIES}")
+    out = np.zeros_like(x)
+    for b in range(so.shape[0] - 1):
+        for t in range(int(so[b]), int(so[b + 1])):
+            i = t - int(so[b])  # position within the sequence
+            for n in range(x.shape[1]):
+                if granularity == "tensor":
+                    c = f.reshape(-1)[0]
+                elif granularity == "batch":
+                    c = f[b]
+                elif granularity == "head":
+                    c = f[b, n]
+                else:
+                    c = f[b, i // block, n]
+                out[t, n] = c * x[t, n]
+    return out
+
+
 def valid(i, j, L, mask_type=MASK_CAUSAL, num_context=0, num_targets=0, target_group_size=0):
     """The oracle's mask predicate for one pair (0 or 1)."""
     return _load().hstu_oracle_valid(i, j, L, mask_type, num_context, num_targets,

@@ -41,7 +41,12 @@ def _desc(**kw):
     (dict(mask_type=7), _abi.HSTU_ERR_INVALID_ARG),
     (dict(head_dim=40), _abi.HSTU_ERR_UNSUPPORTED),                      # not a multiple of 16
     (dict(head_dim=272), _abi.HSTU_ERR_UNSUPPORTED),
-    (dict(dtype=_abi.HSTU_FP8_E4M3, head_dim=48), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(dtype=_abi.HSTU_FP8_E4M3, head_dim=144), _abi.HSTU_ERR_UNSUPPORTED),  # FP8: <= 128
+    (dict(dtype=_abi.HSTU_FP8_E4M3, mask_type=_abi.HSTU_MASK_CUSTOM), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(dtype=_abi.HSTU_FP8_E4M3, has_rab=1, is_delta_qk=1), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(descale=_abi.HSTU_DESCALE_HEAD), _abi.HSTU_ERR_INVALID_ARG),  # descales: FP8 only
+    (dict(dtype=_abi.HSTU_FP8_E4M3, descale=5), _abi.HSTU_ERR_INVALID_ARG),
+    (dict(dtype=_abi.HSTU_FP8_E4M3, descale=-1), _abi.HSTU_ERR_INVALID_ARG),
     (dict(dtype=_abi.HSTU_F32, head_dim=300), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(head_dim=0), _abi.HSTU_ERR_INVALID_ARG),
     (dict(max_seqlen=0), _abi.HSTU_ERR_INVALID_ARG),

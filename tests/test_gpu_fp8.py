@@ -1,15 +1,17 @@
-"""FP8 E4M3 inputs (feature table, "FP8 quantization types: cast"): q, k, v cast to E4M3
-with per-tensor descale factors, both products on the 8-bit tensor cores, P rounded to
-E4M3 (after scaling by 16) for the second one, out bf16. Checked against the fp64 oracle
-run on the dequantized inputs (the exact values the kernel receives).
+"""FP8 E4M3 inputs (feature table, "FP8 quantization types": cast, per-tensor, per-batch,
+per-head, per-block): q, k, v as E4M3 with descale factors of each granularity, optional
+bf16 rab, both products on the 8-bit tensor cores, P rounded to E4M3 (after scaling by 16)
+for the second one, out bf16. Checked against the fp64 oracle run on the dequantized
+inputs (the exact values the kernel receives: oracle.dequantize).
 
 Tolerance, derived from the arithmetic: per output row i the kernel's error is at most
-  silu_scale * sum_j valid (2^-4 |P_ij| + 2^-14) |V_j|   (E4M3 rounding of 16 P: relative
-                                                           2^-4, absolute 2^-10 / 16 for
-                                                           subnormals)
-  + 2^-8 silu_scale * sum_j |P_ij| |V_j|                 (P computed in f16)
-  + 2^-8 |O_i|                                            (bf16 output)
-which the tests compute in fp64 from the dequantized inputs (plain causal or no mask)."""
+  silu_scale * sum_j valid 2^-4 |P_ij| |V_j|     (E4M3 rounding of 16 P: relative 2^-4)
+  + silu_scale * sum_j valid 2^-14 c_j |v_j|     (E4M3 subnormals: absolute 2^-10 / 16 in
+                                                  units of c_j, the v factor of key j, or
+                                                  with block factors the sequence's largest)
+  + 2^-8 silu_scale * sum_j |P_ij| |V_j|         (fp32 SiLU with tanh.approx, fp32 sums)
+  + 2^-8 |O_i|                                    (bf16 output)
+with V_j = c_j v_j the dequantized values, which the tests compute in fp64."""
 import numpy as np
 import pytest
 import torch
@@ -161,11 +163,129 @@ def test_fp8_full_size_sampled_rows(cuda_device):
     assert np.abs(sel - ref).max() / np.abs(ref).max() <= 2.0 ** -4
 
 
-def test_fp8_rejects_rab_and_custom_mask(cuda_device):
+def test_fp8_rejects_custom_mask_and_key_side_rab(cuda_device):
     from hstu_dense_forward_gb300 import HstuError
     w, inp = _case(64, (2, 2), B=2, S=64)
     q8 = inp["q"].float().to(E4M3).to(cuda_device)
     so = inp["seq_offsets"].to(cuda_device)
-    rab = torch.zeros(2, 2, 64, 64, dtype=E4M3, device=cuda_device)
+    mask = torch.ones(2, 2, 64, 64, dtype=E4M3, device=cuda_device)
+    with pytest.raises((HstuError, TypeError)):
+        hstu_fwd(q8, q8, q8, so, max_seqlen=64, mask=mask)
+    rab = torch.zeros(2, 2, 64, 64, dtype=torch.bfloat16, device=cuda_device)
     with pytest.raises(HstuError):
-        hstu_fwd(q8, q8, q8, so, max_seqlen=64, rab=rab)
+        hstu_fwd(q8, q8, q8, so, max_seqlen=64, rab=rab, seq_offsets_k=so)
+
+
+# ------------------------------------------------ descale granularities, rab, head dims
+def _e4m3(shape, g, spread=64.0):
+    """Random E4M3 values (normal, sigma = spread) as stored by a scaled cast."""
+    return (torch.randn(*shape, generator=g) * spread).clamp(-440, 440).to(E4M3)
+
+
+def _factors(gran, B, N, nblk, g, lo=-9.0, hi=-5.0):
+    """Random descale factors 2^U[lo, hi] of a granularity's shape (fp32, CPU)."""
+    shape = {"tensor": (1,), "batch": (B,), "head": (B, N), "block": (B, nblk, N)}[gran]
+    return torch.exp2(torch.rand(*shape, generator=g) * (hi - lo) + lo)
+
+
+def _bound_rows(qd, kd, vd, vsub, so, alpha, silu_scale, causal, nq, nk, rab=None):
+    """Per-row error bound of the module docstring [T, Nq] (fp64): vsub [T, Nk, D] is what
+    the subnormal term scales (|vd v| per element, or the sequence's largest v factor
+    times |v| with block factors, where P carries vd / that factor)."""
+    G = nq // nk
+    out = np.zeros((qd.shape[0], nq))
+    for b in range(len(so) - 1):
+        a, e = int(so[b]), int(so[b + 1])
+        L = e - a
+        if L == 0:
+            continue
+        m = np.tril(np.ones((L, L))) if causal else np.ones((L, L))
+        for h in range(nq):
+            x = alpha * (qd[a:e, h] @ kd[a:e, h // G].T)
+            if rab is not None:
+                x = x + rab[b, h if rab.shape[1] > 1 else 0, :L, :L]
+            p = np.abs(x / (1.0 + np.exp(-x))) * m
+            out[a:e, h] = silu_scale * ((2.0 ** -4 + 2.0 ** -8) *
+                                        (p @ np.abs(vd[a:e, h // G])).max(axis=1) +
+                                        2.0 ** -14 * (m @ vsub[a:e, h // G]).max(axis=1))
+    return out
+
+
+def _run_descaled(dev, gran, d, heads, causal, seed, rab_mode=None, S=300, B=3):
+    g = torch.Generator().manual_seed(seed)
+    w, inp = _case(d, heads, B=B, S=S, causal=causal, seed=seed)
+    so = inp["seq_offsets"]
+    T = int(so[-1])
+    nq, nk = heads
+    nblk = -(-S // 128)
+    q8, k8, v8 = _e4m3((T, nq, d), g), _e4m3((T, nk, d), g), _e4m3((T, nk, d), g)
+    fq = _factors(gran, B, nq, nblk, g)
+    fk = _factors(gran, B, nk, nblk, g)
+    fv = _factors(gran, B, nk, nblk, g, lo=-10.0, hi=-5.0)  # (block: up to 32x apart)
+    qd, kd, vd = (oracle.dequantize(x.double().numpy(), f.double().numpy(), gran, so)
+                  for x, f in ((q8, fq), (k8, fk), (v8, fv)))
+    rab = None
+    if rab_mode is not None:
+        rab = (torch.randn(B, 1 if rab_mode == "bcast" else nq, S, S, generator=g) * 0.5
+               ).to(torch.bfloat16)
+    out = hstu_fwd(q8.to(dev), k8.to(dev), v8.to(dev), so.to(dev), max_seqlen=S,
+                   causal=causal, alpha=w.alpha_value, silu_scale=w.silu_scale_value,
+                   rab=None if rab is None else rab.to(dev),
+                   q_descale=fq.to(dev), k_descale=fk.to(dev), v_descale=fv.to(dev))
+    torch.cuda.synchronize()
+    assert out.dtype == torch.bfloat16
+    rab64 = None if rab is None else rab.double().numpy()
+    ref = oracle.hstu_fwd(qd, kd, vd, so, rab=rab64,
+                          mask_type=oracle.MASK_CAUSAL if causal else oracle.MASK_NONE,
+                          alpha=w.alpha_value, silu_scale=w.silu_scale_value, max_seqlen=S,
+                          nthreads=8)
+    if gran == "block":  # P carries vd / (the sequence-head's largest v factor)
+        vmax = fv.abs().amax(dim=1).double().numpy()  # [B, Nk]
+        vsub = np.abs(v8.double().numpy())
+        for b in range(B):
+            vsub[int(so[b]):int(so[b + 1])] *= vmax[b][None, :, None]
+    else:
+        vsub = np.abs(vd)
+    got = out.double().cpu().numpy()[:T]
+    err = np.abs(got - ref[:T]).max(axis=2)
+    bound = _bound_rows(qd, kd, vd, vsub, so.numpy(), w.alpha_value, w.silu_scale_value,
+                        causal, nq, nk, rab64)[:T] + 2.0 ** -8 * np.abs(ref[:T]).max(axis=2)
+    assert np.all(err <= bound), float((err / bound).max())
+    assert np.abs(got - ref[:T]).max() / np.abs(ref[:T]).max() <= 2.0 ** -4
+
+
+@pytest.mark.parametrize("gran", oracle.DESCALE_GRANULARITIES)
+@pytest.mark.parametrize("d,heads,causal", [(128, (4, 2), True), (64, (2, 2), False)])
+def test_fp8_descale_granularities(cuda_device, gran, d, heads, causal):
+    """Descale factors per tensor, sequence, sequence and head, and 128-row block, spread
+    over 2^-9 .. 2^-5 (v: 2^-10 .. 2^-5), against the oracle on the dequantized values."""
+    _run_descaled(cuda_device, gran, d, heads, causal, seed=200 + d + len(gran))
+
+
+@pytest.mark.parametrize("gran,d,rab_mode", [("tensor", 128, "full"), ("block", 64, "full"),
+                                             ("head", 32, "bcast"), ("batch", 96, "full")])
+def test_fp8_with_rab(cuda_device, gran, d, rab_mode):
+    """FP8 inputs with a bf16 rab (per head, or one plane broadcast to every head), added
+    in fp32 to the SiLU argument: x = alpha (qd q).(kd k) + rab."""
+    _run_descaled(cuda_device, gran, d, (4, 2), True, seed=300 + d, rab_mode=rab_mode, S=264)
+
+
+@pytest.mark.parametrize("d", [16, 48, 80, 112])
+def test_fp8_padded_head_dims(cuda_device, d):
+    """Head dims between the built 32, 64, 128 (zero-filled extra columns)."""
+    _run_descaled(cuda_device, "head", d, (2, 1), True, seed=400 + d)
+
+
+def test_fp8_descale_shapes_are_checked(cuda_device):
+    w, inp = _case(64, (2, 2), B=2, S=64)
+    q8 = inp["q"].float().to(E4M3).to(cuda_device)
+    so = inp["seq_offsets"].to(cuda_device)
+    one = torch.ones(2, 2, dtype=torch.float32, device=cuda_device)
+    with pytest.raises(ValueError):  # [B, N] for q, [B] for k and v
+        hstu_fwd(q8, q8, q8, so, max_seqlen=64, q_descale=one, k_descale=one[:, 0].contiguous(),
+                 v_descale=one[:, 0].contiguous())
+    with pytest.raises(ValueError):  # all three or none
+        hstu_fwd(q8, q8, q8, so, max_seqlen=64, q_descale=1.0)
+    bf = inp["q"].to(cuda_device)
+    with pytest.raises(ValueError):  # descales go with FP8 inputs
+        hstu_fwd(bf, bf, bf, so, max_seqlen=64, q_descale=1.0, k_descale=1.0, v_descale=1.0)

@@ -527,3 +527,43 @@ def test_key_side_identities_random_geometries(seed):
                             page_offsets=po, page_ids=ids, last_page_len=last, **kw)
     np.testing.assert_array_equal(delta, full[rows])
     np.testing.assert_array_equal(paged, delta)
+
+
+# ------------------------------------------------------------ FP8 descale granularities
+def test_dequantize_granularities_by_hand():
+    """The factor each element gets, written out for a tiny jagged tensor: sequences of
+    3 and 5 rows, 2 heads, blocks of 2 rows (so the second sequence spans 3 blocks)."""
+    so = np.array([0, 3, 8])
+    x = np.arange(8 * 2 * 1, dtype=np.float64).reshape(8, 2, 1) + 1.0
+    # per tensor: one factor
+    assert np.array_equal(oracle.dequantize(x, [0.5], "tensor", so), 0.5 * x)
+    # per batch: rows 0-2 by 2, rows 3-7 by 3
+    want = x.copy()
+    want[:3] *= 2.0
+    want[3:] *= 3.0
+    assert np.array_equal(oracle.dequantize(x, [2.0, 3.0], "batch", so), want)
+    # per head: [B, N]
+    f = np.array([[1.0, 10.0], [100.0, 1000.0]])
+    got = oracle.dequantize(x, f, "head", so)
+    assert got[1, 0, 0] == 1.0 * x[1, 0, 0] and got[1, 1, 0] == 10.0 * x[1, 1, 0]
+    assert got[7, 0, 0] == 100.0 * x[7, 0, 0] and got[4, 1, 0] == 1000.0 * x[4, 1, 0]
+    # per block: [B, nblocks, N], block = position in the sequence // 2
+    fb = np.arange(2 * 3 * 2, dtype=np.float64).reshape(2, 3, 2) + 1.0
+    got = oracle.dequantize(x, fb, "block", so, block=2)
+    for t, b, i in [(0, 0, 0), (1, 0, 1), (2, 0, 2), (3, 1, 0), (4, 1, 1), (5, 1, 2),
+                    (6, 1, 3), (7, 1, 4)]:
+        for n in range(2):
+            assert got[t, n, 0] == fb[b, i // 2, n] * x[t, n, 0], (t, n)
+
+
+def test_dequantize_reduces_to_per_tensor():
+    """Every granularity with all factors equal is the per-tensor case, and rows outside
+    every sequence are zero."""
+    rng = np.random.default_rng(3)
+    so = np.array([0, 100, 100, 300])
+    x = rng.normal(size=(310, 3, 4))
+    ref = oracle.dequantize(x, [0.25], "tensor", so)
+    assert np.all(ref[300:] == 0)
+    assert np.array_equal(oracle.dequantize(x, np.full(3, 0.25), "batch", so), ref)
+    assert np.array_equal(oracle.dequantize(x, np.full((3, 3), 0.25), "head", so), ref)
+    assert np.array_equal(oracle.dequantize(x, np.full((3, 2, 3), 0.25), "block", so), ref)
