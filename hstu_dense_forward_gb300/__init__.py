@@ -113,6 +113,18 @@ class HstuFwdPlan:
             kv.page_offsets = ptr(page_offsets) or None
             kv.page_ids = ptr(page_ids) or None
             kv.last_page_len = ptr(last_page_len) or None
+        if self.desc.mask_type == _abi.HSTU_MASK_CUSTOM and self.desc.has_rab:
+            a = _abi.Args()  # a custom mask with rab: the general entry point
+            a.q, a.k, a.v, a.out = q.data_ptr(), ptr(k) or None, ptr(v) or None, out.data_ptr()
+            a.seq_offsets = ptr(seq_offsets) or None
+            if kv is not None:
+                a.kv = ctypes.pointer(kv)
+            a.rab, a.mask = ptr(rab) or None, ptr(mask) or None
+            a.total_tokens, a.alpha, a.silu_scale = q.shape[0], float(alpha), float(silu_scale)
+            _abi.check(self._keep.hstu_fwd_run_args(self._h, ctypes.byref(a),
+                                                    stream.cuda_stream or None),
+                       "hstu_fwd_run_args")
+            return out
         if self.desc.descale != _abi.HSTU_DESCALE_CAST:
             ds = _abi.Descale()
             ds.q, ds.k, ds.v = (t.data_ptr() for t in descale)
@@ -240,8 +252,8 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     Same dtype for q, k, v: fp32, fp16 or bf16. num_context / num_targets [B] of the index
     dtype (int32/int64). rab [B, Nq, S, S] or [B, 1, S, S] (one plane for all heads) of q's
     dtype, or None. causal=False is mask_type 2 (no mask). mask [B, Nq, S, S] of q's dtype
-    selects mask_type 3 (custom mask: P is multiplied by it after the SiLU; no rab, context
-    or target counts with it). silu_scale defaults to 1/max_seqlen. Returns out with q's
+    selects mask_type 3 (custom mask: P is multiplied by it after the SiLU; no context or
+    target counts with it; rab, added before the SiLU, may come with it). silu_scale defaults to 1/max_seqlen. Returns out with q's
     shape; rows that belong to no sequence are left as allocated.
 
     Key side (jagged layout; Inputs and Outputs table, seq_offsets_k / kv_cache rows):
@@ -348,8 +360,8 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
         descale, ds = _abi.HSTU_DESCALE_CAST, None
     custom = mask is not None
     if custom:
-        if rab is not None or num_context is not None or num_targets is not None:
-            raise ValueError("a custom mask takes no rab, num_context or num_targets")
+        if num_context is not None or num_targets is not None:
+            raise ValueError("a custom mask takes no num_context or num_targets")
         _check_tensor(mask, "mask", q.dtype, dev, 4)
         if tuple(mask.shape) != (B, Nq, Sk, Sk):
             raise ValueError(f"mask must be [B, Nq, S, S], got {list(mask.shape)}")

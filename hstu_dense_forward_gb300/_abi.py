@@ -67,6 +67,18 @@ class Descale(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p)]
 
 
+class Args(ctypes.Structure):
+    """hstu_fwd_args: every input of one forward (hstu_fwd_run_args)."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("seq_offsets", ctypes.c_void_p),
+        ("kv", ctypes.POINTER(KV)), ("rab", ctypes.c_void_p), ("mask", ctypes.c_void_p),
+        ("num_context", ctypes.c_void_p), ("num_targets", ctypes.c_void_p),
+        ("descale", ctypes.POINTER(Descale)), ("total_tokens", ctypes.c_longlong),
+        ("alpha", ctypes.c_float), ("silu_scale", ctypes.c_float),
+    ]
+
+
 class HstuError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -122,6 +134,8 @@ def lib():
         L.hstu_fwd_run_fp8.restype = ctypes.c_int
         L.hstu_fwd_run_fp8.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(KV), vp, vp, vp,
                                        ctypes.POINTER(Descale), ll, f, f, vp, vp]
+        L.hstu_fwd_run_args.restype = ctypes.c_int
+        L.hstu_fwd_run_args.argtypes = [vp, ctypes.POINTER(Args), vp]
         L.hstu_fwd_trace_read.restype = ctypes.c_int
         L.hstu_fwd_trace_read.argtypes = [vp, vp, ll]
         L.hstu_status_string.restype = ctypes.c_char_p

@@ -64,7 +64,7 @@ struct hstu_fwd_plan {
   long long timeout_ns;
   // tensor maps of the last run, re-encoded when a pointer or a row count changes
   TcMaps maps;
-  const void* map_ptrs[6];
+  const void* map_ptrs[7];
   long long map_T, map_Tk, map_pages;
   bool maps_valid;
   unsigned long long* d_trace;  // pipeline trace buffer (builds with HSTU_TRACE=1 only)
@@ -173,8 +173,12 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
   if (d->mask_type == HSTU_MASK_CUSTOM) {
     // the mask replaces the built-in one (no context / target counts); it streams through
     // the rab path, so rab and a custom mask together are not built
-    if (d->has_num_context || d->has_num_targets || d->rab_heads) return HSTU_ERR_INVALID_ARG;
-    if (d->has_rab) return HSTU_ERR_UNSUPPORTED;
+    if (d->has_num_context || d->has_num_targets || (d->rab_heads && !d->has_rab))
+      return HSTU_ERR_INVALID_ARG;
+    // with rab: one ring slot holds a rab and a mask tile (head dims up to 128, no key side)
+    if (d->has_rab && d->dtype != HSTU_F32 &&
+        (key_side(*d) || !hstu::tc_supported_dim(d->head_dim) || d->head_dim > 128))
+      return HSTU_ERR_UNSUPPORTED;
     if (d->dtype != HSTU_F32 && key_bound(*d) % 8 != 0) return HSTU_ERR_UNSUPPORTED;
   }
   if (d->dtype == HSTU_FP8_E4M3) {
@@ -221,7 +225,8 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
       // kernel variant: 0 no rab, 1 rab, 2 custom mask (streamed like rab)
       e = hstu::tc_prepare(desc->head_dim,
                            desc->dtype == HSTU_FP8_E4M3 ? 2 : (desc->dtype == HSTU_BF16 ? 1 : 0),
-                           desc->mask_type == HSTU_MASK_CUSTOM ? 2 : (desc->has_rab ? 1 : 0),
+                           desc->mask_type == HSTU_MASK_CUSTOM ? (desc->has_rab ? 3 : 2)
+                                                                : (desc->has_rab ? 1 : 0),
                            key_side(*desc) ? 1 : 0);
       P->grid = P->num_sms;
     } else {
@@ -292,8 +297,8 @@ static bool encode4d(CUtensorMap* m, CUtensorMapDataType ty, const void* base,
 // [num_pages, 2, page_size, Nk, D] as 4-D (D, Nk, page_size, 2 * num_pages).
 static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, const void* v,
                              const void* rab, const void* out, long long T, long long Tk,
-                             const void* cache, long long num_pages) {
-  const void* ptrs[6] = {q, k, v, rab, out, cache};
+                             const void* cache, long long num_pages, const void* mask) {
+  const void* ptrs[7] = {q, k, v, rab, out, cache, mask};
   if (P->maps_valid && P->map_T == T && P->map_Tk == Tk && P->map_pages == num_pages &&
       memcmp(ptrs, P->map_ptrs, sizeof(ptrs)) == 0)
     return HSTU_OK;
@@ -333,6 +338,13 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
                   hstu::tc_rab_box_rows(), 1, CU_TENSOR_MAP_SWIZZLE_128B);
   } else if (ok) {
     P->maps.rab = P->maps.q;  // unused by the kernel
+  }
+  if (ok && mask) {  // a custom mask beside rab: [B * Nq, S, S] like a rab of Nq planes
+    const uint64_t S = (uint64_t)key_bound(d);
+    ok = encode3d(&P->maps.mask, ty, mask, S, S, (uint64_t)d.batch * Nq, S * 2, S * S * 2, 64,
+                  hstu::tc_rab_box_rows(), 1, CU_TENSOR_MAP_SWIZZLE_128B);
+  } else if (ok) {
+    P->maps.mask = P->maps.q;  // unused by the kernel
   }
   if (ok && cache) {
     const uint64_t ps = (uint64_t)d.page_size;
@@ -383,8 +395,15 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
                             const void* seq_offsets, const hstu_fwd_kv* kv, const void* rab,
                             bool is_mask, const void* num_context, const void* num_targets,
                             long long total_tokens, float alpha, float silu_scale, void* out,
-                            void* stream, const hstu_fwd_descale* ds = nullptr) {
+                            void* stream, const hstu_fwd_descale* ds = nullptr,
+                            const void* mask_with_rab = nullptr) {
   const hstu_fwd_desc& d = P->desc;
+  // a CUSTOM plan with has_rab takes both (rab in `rab`, the mask in mask_with_rab)
+  const bool both = d.mask_type == HSTU_MASK_CUSTOM && d.has_rab;
+  if (both && is_mask) return HSTU_ERR_INVALID_ARG;
+  if (!both && mask_with_rab) return HSTU_ERR_INVALID_ARG;
+  if (both && !mask_with_rab && d.batch > 0 && d.num_heads_q > 0 && total_tokens > 0)
+    return HSTU_ERR_INVALID_ARG;
   if (d.descale != HSTU_DESCALE_CAST) {  // factor arrays: present, fp32-aligned
     if (!ds || !ds->q || !ds->k || !ds->v) return HSTU_ERR_INVALID_ARG;
     for (const float* f : {ds->q, ds->k, ds->v})
@@ -399,6 +418,7 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
       (kv_rows && (!k || !v)))
     return HSTU_ERR_INVALID_ARG;
   if ((rab != nullptr) != (is_mask || d.has_rab != 0)) return HSTU_ERR_INVALID_ARG;
+  if (mask_with_rab && !aligned16(mask_with_rab)) return HSTU_ERR_INVALID_ARG;
   if ((num_context != nullptr) != (d.has_num_context != 0)) return HSTU_ERR_INVALID_ARG;
   if ((num_targets != nullptr) != (d.has_num_targets != 0)) return HSTU_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
@@ -448,6 +468,8 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
   p.dense = d.layout == HSTU_LAYOUT_NORMAL ? 1 : 0;
   p.rab_bcast = d.rab_heads == 1 ? 1 : 0;
   p.rab_is_mask = is_mask ? 1 : 0;
+  p.mask = mask_with_rab;
+  if (both) p.mask_type = hstu::kMaskNone;  // the mask decides: every key a candidate
   p.alpha = alpha;
   p.silu_scale = silu_scale;
   p.fp8 = d.dtype == HSTU_FP8_E4M3 ? 1 : 0;
@@ -470,7 +492,7 @@ static hstu_status run_impl(hstu_fwd_plan* P, const void* q, const void* k, cons
 
   if (P->tensor_cores) {
     hstu_status ms = make_maps(P, q, k, v, rab, out, total_tokens, Tk, cache,
-                               d.page_size ? kv->num_pages : 0);
+                               d.page_size ? kv->num_pages : 0, mask_with_rab);
     if (ms != HSTU_OK) return ms;
   }
   if (hstu::launch_build_worklist(p, P->d_work + b * P->work_cap, P->d_count + 4 * b,
@@ -491,6 +513,25 @@ hstu_status hstu_fwd_run(hstu_fwd_plan* P, const void* q, const void* k, const v
     return HSTU_ERR_INVALID_ARG;
   return run_impl(P, q, k, v, seq_offsets, nullptr, rab, false, num_context, num_targets,
                   total_tokens, alpha, silu_scale, out, stream);
+}
+
+hstu_status hstu_fwd_run_args(hstu_fwd_plan* P, const hstu_fwd_args* a, void* stream) {
+  if (!P || !a) return HSTU_ERR_INVALID_ARG;
+  const hstu_fwd_desc& d = P->desc;
+  const bool custom = d.mask_type == HSTU_MASK_CUSTOM;
+  if (!custom && a->mask) return HSTU_ERR_INVALID_ARG;
+  if (custom && (a->num_context || a->num_targets)) return HSTU_ERR_INVALID_ARG;
+  if (d.descale == HSTU_DESCALE_CAST && a->descale) return HSTU_ERR_INVALID_ARG;
+  if (custom && !d.has_rab) {  // the mask streams where rab would
+    if (a->rab) return HSTU_ERR_INVALID_ARG;
+    if (!a->mask && d.batch > 0 && d.num_heads_q > 0 && a->total_tokens > 0)
+      return HSTU_ERR_INVALID_ARG;
+    return run_impl(P, a->q, a->k, a->v, a->seq_offsets, a->kv, a->mask, true, nullptr, nullptr,
+                    a->total_tokens, a->alpha, a->silu_scale, a->out, stream, a->descale);
+  }
+  return run_impl(P, a->q, a->k, a->v, a->seq_offsets, a->kv, a->rab, false, a->num_context,
+                  a->num_targets, a->total_tokens, a->alpha, a->silu_scale, a->out, stream,
+                  a->descale, custom ? a->mask : nullptr);
 }
 
 hstu_status hstu_fwd_run_fp8(hstu_fwd_plan* P, const void* q, const void* k, const void* v,

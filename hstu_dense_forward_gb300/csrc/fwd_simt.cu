@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_f32_kernel(const FwdParams 
           if (!p.rab_is_mask) x += t;  // relative attention bias before the SiLU
           float pv = x / (1.0f + expf(-x));
           if (p.rab_is_mask) pv *= t;  // custom mask after it
+          if (p.mask != nullptr && ok)  // (a custom mask given together with rab)
+            pv *= static_cast<const float*>(p.mask)[(((long long)b * p.Nq + h) * p.S + i) * p.S + j];
           Ps[r * (BN + 1) + tx + 16 * c] = ok ? pv : 0.f;
         }
       }

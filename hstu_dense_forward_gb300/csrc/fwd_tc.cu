@@ -18,6 +18,7 @@ cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cu
     return p.rab_is_mask ? tc::dispatch_kv_mask(p, m, bf16, grid, st, pdl, prepare)
                          : tc::dispatch_kv(p, m, bf16, grid, st, pdl, prepare);
   if (p.rab_is_mask) return tc::dispatch_mask(p, m, bf16, grid, st, pdl, prepare);
+  if (p.mask) return tc::dispatch_mask_rab(p, m, bf16, grid, st, pdl, prepare);
   if (p.rab && p.rab_mma) return tc::dispatch_rab_mma(p, m, bf16, grid, st, pdl, prepare);
   return p.rab ? tc::dispatch_type<1, false, false>(p, m, bf16, grid, st, pdl, prepare)
                : tc::dispatch_type<0, false, false>(p, m, bf16, grid, st, pdl, prepare);
@@ -49,6 +50,7 @@ cudaError_t tc_prepare(int D, int elem, int rab, int kv) {
   const int bf16 = elem == 1 ? 1 : 0;
   p.rab = rab ? reinterpret_cast<const void*>(1) : nullptr;
   p.rab_is_mask = rab == 2 ? 1 : 0;
+  p.mask = rab == 3 ? reinterpret_cast<const void*>(1) : nullptr;
   p.seq_offsets_k = kv ? reinterpret_cast<const void*>(1) : nullptr;  // selects the variant only
   TcMaps m = {};
   cudaError_t e = dispatch(p, m, bf16, 0, nullptr, false, true);

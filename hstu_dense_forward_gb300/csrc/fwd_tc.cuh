@@ -66,7 +66,8 @@ constexpr int kRabBoxRows = 32;
 
 // F8: q, k, v are FP8 E4M3 (one byte each); the products run as tcgen05 kind::f8f6f4 with
 // P rounded to E4M3; O is written as bf16.
-// RAB: 0 no rab; 1 rab (or a custom mask) read from shared memory by the epilogue; 2 rab
+// RAB: 0 no rab; 1 rab (or a custom mask) read from shared memory by the epilogue; 3 rab
+// and a custom mask, one tile of each per ring slot, both read by the epilogue; 2 rab
 // added to S by the tensor core: for each 16-key step k of the tile, S[:, 16k:16k+16] +=
 // R[:, 16k:16k+16] (c I16) with the rab tile R as the A operand and a 16 x 16 diagonal B of
 // c = 1/alpha, so that alpha*S = alpha Q K^T + rab and the epilogue is that of the plain
@@ -74,9 +75,11 @@ constexpr int kRabBoxRows = 32;
 template <int D, int RAB, bool F8 = false>
 struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head_dim");
-  static_assert(!F8 || (D <= 128 && RAB != 2), "fp8: head_dim <= 128, rab in the epilogue");
+  static_assert(!F8 || (D <= 128 && RAB <= 1), "fp8: head_dim <= 128, rab in the epilogue");
   static constexpr bool RM = RAB == 2;        // rab by the tensor core
-  static constexpr bool EPI_RAB = RAB == 1;   // rab / mask tiles read by the epilogue
+  static constexpr bool TWO = RAB == 3;       // rab and custom-mask tiles
+  static constexpr bool EPI_RAB = RAB == 1 || TWO;  // rab / mask tiles read by the epilogue
+  static_assert(!TWO || D <= 128, "rab with a custom mask: head_dim <= 128");
   static_assert(!RM || D <= 64, "rab by the tensor core: head_dim <= 64");
   static constexpr int EB = F8 ? 1 : 2;                     // bytes per q / k / v element
   static constexpr int SWB = (D * EB >= 128) ? 128 : D * EB;  // bytes per swizzled row
@@ -93,7 +96,10 @@ struct Cfg {
   static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 2 : 4) : (D == 128 ? 2 : 1));
   static constexpr int NV = NK;                                  // K and V ring depths
   // rab tiles stream from HBM once each: the deeper the ring, the more bytes in flight
-  static constexpr int NR = RAB ? (D == 32 ? 4 : (D == 64 ? 3 : (D == 128 ? 2 : 1))) : 0;
+  // (with a custom mask beside rab a slot holds both tiles and the ring is shallower)
+  static constexpr int NR = TWO ? (D == 32 ? 2 : 1)
+                                : RAB ? (D == 32 ? 4 : (D == 64 ? 3 : (D == 128 ? 2 : 1))) : 0;
+  static constexpr int RSLOT = (TWO ? 2 : 1) * RAB_BYTES;  // one ring slot
   // RM: the 16 x 16 diagonal B operand, K-major rows of 64 bytes (64-byte swizzle)
   static constexpr int IDENT_BYTES = RM ? 16 * 64 : 0;
   // O is staged in shared memory and written by TMA when there is room for a tile
@@ -130,7 +136,7 @@ struct Cfg {
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
   static constexpr int OFF_R = OFF_V + NV * TILE_BYTES;
-  static constexpr int OFF_I = OFF_R + NR * RAB_BYTES;  // diagonal B operand (RM)
+  static constexpr int OFF_I = OFF_R + NR * RSLOT;  // diagonal B operand (RM)
   static constexpr int OFF_O = OFF_I + (RM ? 1024 : 0);   // (a 1024-byte swizzle atom)
   static constexpr int OFF_BAR = OFF_O + (STAGE ? O_TILE_BYTES : 0);
   static constexpr int BAR_BYTES = 1024;
@@ -462,7 +468,7 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 // masked, and the epilogue sets a masked entry's h to 0 after adding rab.
 template <int D, int RAB, bool MASK, bool KV, bool F8>
 __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tr,
-                           long long total) {
+                           const CUtensorMap* tm, long long total) {
   using C = Cfg<D, RAB, F8>;
   constexpr int STRIPS = kTileM / kRabBoxRows;
   constexpr uint32_t BOX_BYTES = kRabBoxRows * 128;
@@ -485,7 +491,7 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       const int rs = r_it % C::NR;
       if (!wait_bar(bars, &bars->r_empty[rs], ((r_it / C::NR) & 1) ^ 1, p)) return;
       const uint32_t full = ptx::smem_u32(&bars->r_full[rs]);
-      const uint32_t dst = sbase + C::OFF_R + rs * C::RAB_BYTES;
+      const uint32_t dst = sbase + C::OFF_R + rs * C::RSLOT;
       // rows: the key positions of the item's queries; columns: the visit's key tile
       const KeyTile kt = KV ? key_tile(j, it.split, it.hist) : KeyTile{j, 0, kTileN, false};
       const int n0 = kt.x * kTileN;
@@ -498,7 +504,7 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
                                      kt.chi > 64 * cb);
           need |= (used ? 1u : 0u) << (st * 2 + cb);
         }
-      ptx::mbar_arrive_expect_tx(full, __popc(need) * BOX_BYTES);
+      ptx::mbar_arrive_expect_tx(full, (__popc(need) + (C::TWO ? 2 * STRIPS : 0)) * BOX_BYTES);
 #pragma unroll
       for (int st = 0; st < STRIPS; ++st)
 #pragma unroll
@@ -506,6 +512,15 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
           if (need & (1u << (st * 2 + cb)))
             ptx::tma_load_3d(dst + cb * (C::RAB_BYTES / 2) + st * BOX_BYTES, tr, full,
                              n0 + 64 * cb, row + st * kRabBoxRows, plane);
+      if constexpr (C::TWO) {  // the custom-mask tile behind the rab tile (every box)
+        const int mplane = it.b * p.Nq + it.h;
+#pragma unroll
+        for (int st = 0; st < STRIPS; ++st)
+#pragma unroll
+          for (int cb = 0; cb < 2; ++cb)
+            ptx::tma_load_3d(dst + C::RAB_BYTES + cb * (C::RAB_BYTES / 2) + st * BOX_BYTES, tm,
+                             full, n0 + 64 * cb, row + st * kRabBoxRows, mplane);
+      }
       ++r_it;
     }
   }
@@ -1007,7 +1022,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
             return;
         }
         if (!warp_wait(bars, &bars->r_full[rs], (t / C::NR) & 1, p)) return;
-        rab_row = smem + C::OFF_R + rs * C::RAB_BYTES + r * 128;
+        rab_row = smem + C::OFF_R + rs * C::RSLOT + r * 128;
       }
 #pragma unroll 1
       for (int c = 0; c < C::COLS_PER_WG / 32; ++c) {  // 32-column chunks, one after the other
@@ -1040,7 +1055,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const int c2 = q4 * 4 + e;  // pair index: columns 2*c2, 2*c2 + 1
-              if constexpr (MASK) {
+              if constexpr (MASK && !C::TWO) {
                 mw[c2] = ww[e];
               } else {
                 float r0, r1;
@@ -1048,6 +1063,17 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
                 ptx::fma_f32x2(h[2 * c2], h[2 * c2 + 1], r0, r1, 0.5f, 0.5f, h[2 * c2],
                                h[2 * c2 + 1]);
               }
+            }
+          }
+          if constexpr (C::TWO) {  // the custom-mask tile, behind the rab tile in the slot
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int chunk = (((cc & 63) >> 3) + q4) ^ (r & 7);
+              const uint4 w = *reinterpret_cast<const uint4*>(box + C::RAB_BYTES + chunk * 16);
+              mw[q4 * 4 + 0] = w.x;
+              mw[q4 * 4 + 1] = w.y;
+              mw[q4 * 4 + 2] = w.z;
+              mw[q4 * 4 + 3] = w.w;
             }
           }
         }
@@ -1136,7 +1162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                   const __grid_constant__ CUtensorMap tm_o,
-                  const __grid_constant__ CUtensorMap tm_c, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_m,
+                  const FwdParams p) {
   using C = Cfg<D, RAB, F8>;
   static_assert(C::NQ <= (int)(sizeof(Bars::q_full) / sizeof(uint64_t)) &&
                     C::NK <= (int)(sizeof(Bars::k_full) / sizeof(uint64_t)) &&
@@ -1185,6 +1212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
     if (RAB) ptx::prefetch_tmap(&tm_r);
+    if (C::TWO) ptx::prefetch_tmap(&tm_m);
     if (C::STAGE) ptx::prefetch_tmap(&tm_o);
     if (KV && p.page_offsets) ptx::prefetch_tmap(&tm_c);
   }
@@ -1243,7 +1271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kRabWarp) {
     if constexpr (RAB) {
-      if (lane == 0) producer_r<D, RAB, MASK, KV, F8>(p, bars, smem, &tm_r, total);
+      if (lane == 0) producer_r<D, RAB, MASK, KV, F8>(p, bars, smem, &tm_r, &tm_m, total);
     }
   } else if (warp == kPvWarp) {
     if (lane == 0 && !C::SERIAL) mma_pv_issuer<D, BF16, RAB, F8>(p, bars, smem, tmem, total);

@@ -27,7 +27,7 @@ cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, BF16, RAB, MASK, KV, F8>, m.q, m.k, m.v, m.rab, m.out,
-                            m.cache, p);
+                            m.cache, m.mask, p);
 }
 
 // Prepare (shared-memory opt-in) or launch one variant, chosen by head dim and type.
@@ -57,6 +57,9 @@ cudaError_t dispatch_rab_mma(const FwdParams& p, const TcMaps& m, int bf16, int 
 // Custom-mask variants (fwd_tc_mask.cu): prepare (shared-memory opt-in) or launch.
 cudaError_t dispatch_mask(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                           cudaStream_t st, bool pdl, bool prepare);
+// A custom mask together with rab (fwd_tc_mask_rab.cu): head dims up to 128, no key side.
+cudaError_t dispatch_mask_rab(const FwdParams& p, const TcMaps& m, int bf16, int grid,
+                              cudaStream_t st, bool pdl, bool prepare);
 
 // FP8 E4M3 variants (fwd_tc_f8.cu): head dims up to 128, no custom mask, with or without a
 // key side; with rab (fwd_tc_f8_rab.cu) without a key side.

@@ -30,6 +30,8 @@ struct FwdParams {
   int rab_is_mask;          // the rab stream carries a custom mask [B, Nq, S, S]: P is
                             // multiplied by it after the SiLU instead of rab being added
                             // before (mask_type is then NONE for the tile geometry)
+  const void* mask;         // a custom mask [B, Nq, S, S] given together with rab (rab in
+                            // `rab`, rab_is_mask 0, mask_type NONE), or nullptr
   float alpha, silu_scale;
   // Key side. The keys of sequence b are its cached history (page_offsets != nullptr)
   // followed by its new k/v rows: rows [seq_offsets_k[b], seq_offsets_k[b + 1]) of k and v,
@@ -125,15 +127,15 @@ cudaError_t launch_fwd_simt(const FwdParams& p, int grid, cudaStream_t stream, b
 
 // bf16 / fp16 tensor-core path (tcgen05, TMA, TMEM).
 struct TcMaps {
-  CUtensorMap q, k, v, rab, out, cache;
+  CUtensorMap q, k, v, rab, out, cache, mask;  // (mask: a custom mask beside rab)
 };
 bool tc_supported_dim(int D);
 int tc_kernel_dim(int D);     // head dim of the kernel variant that runs D (32/64/128/256)
 int tc_swizzle_bytes(int D, int elem_bytes);  // row width of one TMA box / UMMA swizzle atom
 int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
 int tc_rab_box_rows();        // rows of one rab / custom-mask load box (64 columns each)
-// elem: 0 f16, 1 bf16, 2 FP8 E4M3; rab: 0 none, 1 rab, 2 custom mask; kv: the key-side
-// variant (own k/v offsets, KV cache)
+// elem: 0 f16, 1 bf16, 2 FP8 E4M3; rab: 0 none, 1 rab, 2 custom mask, 3 custom mask and
+// rab; kv: the key-side variant (own k/v offsets, KV cache)
 cudaError_t tc_prepare(int D, int elem, int rab, int kv);
 // The variant that adds rab with the tensor core exists for these (rab = 1: rab, not a
 // custom mask; no key side; bf16 / fp16; head dim 32 or 64).

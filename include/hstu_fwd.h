@@ -107,9 +107,11 @@ typedef enum {
   HSTU_MASK_CAUSAL = 0, /* built-in lower-triangular mask with context/targets */
   HSTU_MASK_UPPER = 1,
   HSTU_MASK_NONE = 2,   /* bidirectional: no mask */
-  HSTU_MASK_CUSTOM = 3  /* mask [B, Nq, S, S] passed to hstu_fwd_run_masked: P is multiplied
-                           by mask[b, h, i, j] after the SiLU and the scaling; no context or
-                           target counts, no rab with it (HSTU_ERR_UNSUPPORTED) */
+  HSTU_MASK_CUSTOM = 3  /* mask [B, Nq, S, S] passed to hstu_fwd_run_masked (or, together
+                           with rab, to hstu_fwd_run_args): P is multiplied by mask[b, h, i, j]
+                           after the SiLU and the scaling; no context or target counts. With
+                           rab (has_rab): head dims up to 128 and no key side on the 16-bit
+                           path (HSTU_ERR_UNSUPPORTED otherwise) */
 } hstu_mask_type;
 
 /* Device error word values (hstu_fwd_get_error). */
@@ -211,8 +213,9 @@ HSTU_API hstu_status hstu_fwd_run(hstu_fwd_plan* plan, const void* q, const void
  *   mask [B, Nq, S, S] of the plan's dtype, 16-byte aligned; every other argument as
  *   for hstu_fwd_run (no rab, num_context or num_targets). Every key j < L of a
  *   sequence is a candidate and P(i, j) is multiplied by mask[b, h, i, j]; a 0/1 mask
- *   selects. Returns HSTU_ERR_INVALID_ARG for a plan of another mask type (and
- *   hstu_fwd_run does for a CUSTOM plan).
+ *   selects. Returns HSTU_ERR_INVALID_ARG for a plan of another mask type or one with
+ *   has_rab (which runs through hstu_fwd_run_args), and hstu_fwd_run does for a CUSTOM
+ *   plan.
  */
 HSTU_API hstu_status hstu_fwd_run_masked(hstu_fwd_plan* plan, const void* q, const void* k,
                                          const void* v, const void* seq_offsets,
@@ -241,13 +244,43 @@ HSTU_API hstu_status hstu_fwd_run_kv(hstu_fwd_plan* plan, const void* q, const v
                                      long long total_tokens, float alpha, float silu_scale,
                                      void* out, void* stream);
 
-/* Descale factor arrays of hstu_fwd_run_fp8: DEVICE pointers to fp32, 4-byte aligned, of
- * the lengths that desc.descale gives (hstu_descale_granularity). */
+/*
+ * Every input of one forward, for hstu_fwd_run_args: the general entry point, the only one
+ * that takes a custom mask together with rab. Pointers as for hstu_fwd_run / _kv / _fp8;
+ * NULL for what the plan does not use.
+ */
+typedef struct hstu_fwd_descale hstu_fwd_descale;
 typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  const void* seq_offsets;
+  const hstu_fwd_kv* kv;            /* key side (plans with is_delta_qk or page_size) */
+  const void* rab;                  /* plans with has_rab */
+  const void* mask;                 /* plans with mask_type CUSTOM */
+  const void* num_context;
+  const void* num_targets;
+  const hstu_fwd_descale* descale;  /* FP8 plans whose descale is not CAST */
+  long long total_tokens;
+  float alpha;
+  float silu_scale;
+} hstu_fwd_args;
+
+/* Enqueue one forward with every input in `args` (see hstu_fwd_args). A CUSTOM plan with
+ * has_rab adds rab[b, h, i, j] before the SiLU and multiplies P by mask[b, h, i, j] after
+ * it. Returns HSTU_ERR_INVALID_ARG when an input the plan needs is missing or one it does
+ * not take is given. */
+HSTU_API hstu_status hstu_fwd_run_args(hstu_fwd_plan* plan, const hstu_fwd_args* args,
+                                       void* stream);
+
+/* Descale factor arrays of hstu_fwd_run_fp8 / hstu_fwd_run_args: DEVICE pointers to fp32, 4-byte aligned, of
+ * the lengths that desc.descale gives (hstu_descale_granularity). */
+struct hstu_fwd_descale {
   const float* q;
   const float* k;
   const float* v;
-} hstu_fwd_descale;
+};
 
 /*
  * Enqueue one forward of an FP8 E4M3 plan with descale factors (feature table, "FP8

@@ -148,6 +148,45 @@ def test_custom_mask_against_oracle(cuda_device, dtype, d, heads, binary):
     assert _rel_err(got[:T], ref[:T]) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("dtype,d,heads,binary,bcast", [("bf16", 128, (4, 2), False, False),
+                                                        ("fp16", 64, (4, 4), True, True),
+                                                        ("bf16", 32, (2, 1), False, False),
+                                                        ("fp16", 96, (2, 2), False, False),
+                                                        ("fp32", 64, (2, 1), False, True)])
+def test_custom_mask_with_rab_against_oracle(cuda_device, dtype, d, heads, binary, bcast):
+    """A custom mask together with rab (general entry point): x = alpha q.k + rab before the
+    SiLU, P times mask[b, h, i, j] after it; rab per head or one plane for every head."""
+    inp, m = _mask_case(dtype, d, heads, binary=binary, seed=33 + d)
+    g = torch.Generator().manual_seed(44 + d)
+    rab = (torch.randn(3, 1 if bcast else heads[0], 264, 264, generator=g) * 0.5).to(
+        W.DTYPES[dtype])
+    dv = W.to_device(inp, cuda_device)
+    got = hstu_fwd(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], max_seqlen=264,
+                   alpha=inp["alpha"], silu_scale=inp["silu_scale"], mask=m.to(cuda_device),
+                   rab=rab.to(cuda_device))
+    torch.cuda.synchronize()
+    ref = oracle.hstu_fwd(inp["q"], inp["k"], inp["v"], inp["seq_offsets"], mask=m, rab=rab,
+                          mask_type=oracle.MASK_CUSTOM, alpha=inp["alpha"],
+                          silu_scale=inp["silu_scale"], max_seqlen=264, nthreads=8)
+    T = int(inp["seq_offsets"][-1])
+    assert _rel_err(got[:T], ref[:T]) <= TOL[dtype]
+
+
+def test_custom_mask_with_zero_rab_equals_mask_alone(cuda_device):
+    """rab = 0 beside a custom mask gives the mask-only kernel's output bit for bit (the
+    same SiLU arithmetic, with rab / 2 = 0 added)."""
+    inp, m = _mask_case("bf16", 128, (4, 4), seed=35)
+    dv = W.to_device(inp, cuda_device)
+    md = m.to(cuda_device)
+    zero = torch.zeros(3, 4, 264, 264, dtype=torch.bfloat16, device=cuda_device)
+    kw = dict(max_seqlen=264, alpha=inp["alpha"], silu_scale=inp["silu_scale"], mask=md)
+    a = hstu_fwd(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], **kw)
+    b = hstu_fwd(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], rab=zero, **kw)
+    torch.cuda.synchronize()
+    T = int(inp["seq_offsets"][-1])
+    assert torch.equal(a[:T], b[:T])
+
+
 def test_custom_causal_mask_matches_builtin(cuda_device):
     """The built-in causal mask written out as a 0/1 custom mask gives the same output
     (the custom path computes the tiles above the diagonal and multiplies them by 0)."""
