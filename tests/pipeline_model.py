@@ -58,18 +58,28 @@ class Cfg:
     # the D = 256 rab-ring guard (a group first waits for the other group's release of
     # tile t - 1 when the rab ring is shallower than the number of groups)
     rab_guard: bool = True
+    # rab added by the tensor core: the score issuer consumes the rab ring (its product
+    # accumulates the rab tile into S) and releases each slot with a commit
+    RM: bool = False
 
 
 # The kernel's configurations (four warps per group are modelled as fewer: the barrier
 # counts scale with them, the protocol does not depend on the number).
-def kernel_cfg(D: int, rab: bool) -> Cfg:
+def kernel_cfg(D: int, rab: bool, rab_mode: str = "epi") -> Cfg:
+    """rab_mode: "epi" (rab or a custom mask read by the epilogue), "mma" (rab added by the
+    tensor core, D <= 64), "two" (rab and a custom mask in one slot, D <= 128)."""
     NQ = 2 if (D <= 64 or (D == 128 and not rab)) else 1
     NK = {32: 4, 64: 2 if rab else 4, 128: 2, 256: 1}[D]
-    NR = ({32: 4, 64: 3, 128: 2, 256: 1}[D]) if rab else 0
+    if not rab:
+        NR = 0
+    elif rab_mode == "two":
+        NR = 2 if D == 32 else 1
+    else:
+        NR = {32: 4, 64: 3, 128: 2, 256: 1}[D]
     serial = D == 256
     # two O accumulators where TMEM has room beside two S buffers and two P buffers
     return Cfg(D=D, NQ=NQ, NK=NK, NV=NK, NR=NR, NSB=2, NPB=2, NO=2 if D <= 64 else 1,
-               EPI_GROUPS=2 if serial else 1, SERIAL=serial)
+               EPI_GROUPS=2 if serial else 1, SERIAL=serial, RM=rab and rab_mode == "mma")
 
 
 @dataclass
@@ -129,7 +139,7 @@ def make_world(cfg: Cfg, items, seed: int) -> World:
     add("v_full", cfg.NV, 1)
     add("v_empty", cfg.NV, 1)
     add("r_full", max(cfg.NR, 1), 1)
-    add("r_empty", max(cfg.NR, 1), gw)
+    add("r_empty", max(cfg.NR, 1), 1 if cfg.RM else gw)
     add("s_full", cfg.NSB, 1)
     add("s_free", cfg.NSB, gw)
     add("p_full", cfg.NPB, gw)
@@ -228,6 +238,11 @@ def s_issuer(w: World):
                 yield ("wait", ("s_free", sb), t // c.NSB - 1)
             yield ("wait", ("k_full", ks), k_it // c.NK)
             yield ("mma", [("Q", qs, k), ("K", ks, t)], ("S", sb, ("S", t)))
+            if c.RM:  # S += R (c I16): the rab tile of t, released by the commit
+                rs = t % c.NR
+                yield ("wait", ("r_full", rs), t // c.NR)
+                yield ("mma", [("R", rs, t), ("S", sb, ("S", t))], ("S", sb, ("S", t)))
+                yield ("commit", ("r_empty", rs))
             yield ("commit", ("s_full", sb))
             yield ("commit", ("k_empty", ks))
             if j + 1 == n:
@@ -318,7 +333,7 @@ def epilogue_warp(w: World, group: int, wid: int):
     c = w.cfg
     t = u = 0
     prev = None  # item whose O is still to be drained
-    rab = c.NR > 0
+    rab = c.NR > 0 and not c.RM  # (RM: the score issuer reads rab)
 
     def drain(item):
         nonlocal u

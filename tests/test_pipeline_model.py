@@ -7,7 +7,8 @@ import pytest
 
 import pipeline_model as M
 
-CONFIGS = [(d, rab) for d in (32, 64, 128, 256) for rab in (False, True)]
+CONFIGS = ([(d, rab, "epi") for d in (32, 64, 128, 256) for rab in (False, True)] +
+           [(d, True, "mma") for d in (32, 64)] + [(d, True, "two") for d in (32, 64, 128)])
 
 
 def _items(seed):
@@ -15,11 +16,13 @@ def _items(seed):
     return [rng.randint(1, 6) for _ in range(rng.randint(1, 12))]
 
 
-@pytest.mark.parametrize("d,rab", CONFIGS)
-def test_protocol_has_no_stale_phase_overrun_or_hang(d, rab):
+@pytest.mark.parametrize("d,rab,mode", CONFIGS)
+def test_protocol_has_no_stale_phase_overrun_or_hang(d, rab, mode):
     """Every wait passes on exactly its phase, every buffer read finds its tile and every
-    role finishes, over 400 schedules (half of them with slow loads and products)."""
-    cfg = M.kernel_cfg(d, rab)
+    role finishes, over 400 schedules (half of them with slow loads and products), for
+    every kernel variant: rab read by the epilogue, added by the tensor core, or sharing
+    its ring slots with a custom mask."""
+    cfg = M.kernel_cfg(d, rab, mode)
     for seed in range(200):
         for p_async in (0.5, 0.1):
             M.run(cfg, _items(seed), seed, p_async=p_async)
@@ -56,6 +59,31 @@ def test_model_finds_a_missing_free_wait():
     try:
         with pytest.raises(M.Violation):
             for seed in range(200):
+                M.run(cfg, _items(seed), seed, p_async=0.1)
+    finally:
+        M.s_issuer = orig
+
+
+def test_model_finds_a_tensor_core_rab_slot_released_too_early():
+    """With rab added by the tensor core, a score issuer that releases the rab slot before
+    its product has read it (an arrive instead of a commit behind the product) lets the
+    producer overwrite the tile: the model must report the stale read."""
+    cfg = M.kernel_cfg(64, True, "mma")
+    orig = M.s_issuer
+
+    def early(w):
+        for a in orig(w):
+            if a[0] == "commit" and a[1][0] == "r_empty":
+                continue
+            if a[0] == "wait" and a[1][0] == "r_full":
+                yield a
+                yield ("arrive", ("r_empty", a[1][1]))
+                continue
+            yield a
+    M.s_issuer = early
+    try:
+        with pytest.raises(M.Violation):
+            for seed in range(300):
                 M.run(cfg, _items(seed), seed, p_async=0.1)
     finally:
         M.s_issuer = orig
