@@ -192,6 +192,9 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
   } else {
     if (!hstu::tc_supported_dim(d->head_dim)) return HSTU_ERR_UNSUPPORTED;
     if (d->has_rab && key_bound(*d) % 8 != 0) return HSTU_ERR_UNSUPPORTED;
+    // head dims above 256 (the 512 kernel): built-in masks only, no rab or key side
+    if (d->head_dim > 256 && (d->has_rab || d->mask_type == HSTU_MASK_CUSTOM || key_side(*d)))
+      return HSTU_ERR_UNSUPPORTED;
   }
   return HSTU_OK;
 }
@@ -738,7 +741,7 @@ cudaError_t noalloc_setup(int dev, const hstu_fwd_desc& d, uint32_t** scratch, i
   int bit = 0;
   if (d.dtype != HSTU_F32) {
     const int kd = hstu::tc_kernel_dim(d.head_dim);
-    const int di = kd == 32 ? 0 : kd == 64 ? 1 : kd == 128 ? 2 : 3;
+    const int di = kd == 32 ? 0 : kd == 64 ? 1 : kd == 128 ? 2 : kd == 256 ? 3 : 4;
     bit = 1 + di * 4 + (d.dtype == HSTU_BF16 ? 2 : 0) + (d.has_rab ? 1 : 0);
   }
   if (!(g_noalloc_prepared[dev] & (1u << bit))) {

@@ -14,6 +14,7 @@ bool key_side(const FwdParams& p) { return p.seq_offsets_k != nullptr || p.page_
 cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cudaStream_t st,
                      bool pdl, bool prepare) {
   if (p.fp8) return tc::dispatch_f8(p, m, grid, st, pdl, prepare);
+  if (tc_kernel_dim(p.D) == 512) return tc::dispatch_wide(p, m, bf16, grid, st, pdl, prepare);
   if (key_side(p))
     return p.rab_is_mask ? tc::dispatch_kv_mask(p, m, bf16, grid, st, pdl, prepare)
                          : tc::dispatch_kv(p, m, bf16, grid, st, pdl, prepare);
@@ -26,20 +27,25 @@ cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cu
 
 }  // namespace
 
-// Every multiple of 16 up to 256 runs on the kernel built for the next of 32, 64, 128, 256:
-// the tensor maps keep the true head dim (rows of D elements) with boxes of the kernel's,
-// so TMA loads fill the extra columns of q, k and v with zeros (Q K^T is unchanged, the
-// extra O columns are 0) and TMA stores clip them; direct stores skip them.
-bool tc_supported_dim(int D) { return D % 16 == 0 && D >= 16 && D <= 256; }
+// Every multiple of 16 up to 512 runs on the kernel built for the next of 32, 64, 128, 256,
+// 512: the tensor maps keep the true head dim (rows of D elements) with boxes of the
+// kernel's, so TMA loads fill the extra columns of q, k and v with zeros (Q K^T is
+// unchanged, the extra O columns are 0) and TMA stores clip them; direct stores skip them.
+bool tc_supported_dim(int D) { return D % 16 == 0 && D >= 16 && D <= 512; }
 
-int tc_kernel_dim(int D) { return D <= 32 ? 32 : (D <= 64 ? 64 : (D <= 128 ? 128 : 256)); }
+int tc_kernel_dim(int D) {
+  return D <= 32 ? 32 : (D <= 64 ? 64 : (D <= 128 ? 128 : (D <= 256 ? 256 : 512)));
+}
 
 int tc_swizzle_bytes(int D, int elem_bytes) {
   const int k = tc_kernel_dim(D);
   return k * elem_bytes >= 128 ? 128 : k * elem_bytes;
 }
 
-int tc_out_box_cols(int D) { return tc_kernel_dim(D) / tc::kEpiWG; }
+int tc_out_box_cols(int D) {  // (an item of the 512 kernel writes 256 columns)
+  const int k = tc_kernel_dim(D);
+  return (k > 256 ? 256 : k) / tc::kEpiWG;
+}
 
 int tc_rab_box_rows() { return tc::kRabBoxRows; }
 

@@ -74,7 +74,14 @@ constexpr int kRabBoxRows = 32;
 // kernel (head dims up to 64; eight M128 N16 K16 products per tile).
 template <int D, int RAB, bool F8 = false>
 struct Cfg {
-  static_assert(D == 32 || D == 64 || D == 128 || D == 256, "head_dim");
+  static_assert(D == 32 || D == 64 || D == 128 || D == 256 || D == 512, "head_dim");
+  // WIDE (D = 512): an item computes S over all 512 columns of q and k but O over one half
+  // (256 columns) of v and out; the two halves of a tile are two items. Q stays resident
+  // (128 KB), K streams as 64-column chunks through a ring of its own, V as one 256-column
+  // tile; P is written over S as for D = 256. No rab, mask tiles, key side or FP8.
+  static constexpr bool WIDE = D == 512;
+  static_assert(!WIDE || (!RAB && !F8), "head_dim 512: no rab or FP8");
+  static constexpr int DV = WIDE ? 256 : D;  // O columns of one item
   static_assert(!F8 || (D <= 128 && RAB <= 1), "fp8: head_dim <= 128, rab in the epilogue");
   static constexpr bool RM = RAB == 2;        // rab by the tensor core
   static constexpr bool TWO = RAB == 3;       // rab and custom-mask tiles
@@ -88,13 +95,16 @@ struct Cfg {
   static constexpr int NCB = D / EPC;          // column blocks per tile row
   static constexpr int CB_BYTES = 128 * SWB;   // one column block of a 128-row tile
   static constexpr int TILE_BYTES = 128 * D * EB;
-  static constexpr int O_TILE_BYTES = 128 * D * 2;  // O is 16-bit
+  static constexpr int O_TILE_BYTES = 128 * DV * 2;  // O is 16-bit
+  static constexpr int K_SLOT = WIDE ? CB_BYTES : TILE_BYTES;  // one K ring slot
+  static constexpr int V_TILE = 128 * DV * EB;                 // one V tile (DV columns)
+  static constexpr int NCBV = DV / EPC;                        // its column blocks
   static constexpr int KS = F8 ? 32 : 16;      // K elements of one MMA (32 bytes)
   static constexpr int PW = F8 ? 32 : 64;      // TMEM columns of one P buffer (128 keys)
   static constexpr int RAB_BYTES = 128 * 128 * 2;
   static constexpr int NQ = (D <= 64) ? 2 : ((D == 128 && !RAB) ? 2 : 1);
-  static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 2 : 4) : (D == 128 ? 2 : 1));
-  static constexpr int NV = NK;                                  // K and V ring depths
+  static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 2 : 4) : (D == 128 ? 2 : (WIDE ? 2 : 1)));
+  static constexpr int NV = WIDE ? 1 : NK;                       // K and V ring depths
   // rab tiles stream from HBM once each: the deeper the ring, the more bytes in flight
   // (with a custom mask beside rab a slot holds both tiles and the ring is shallower)
   static constexpr int NR = TWO ? (D == 32 ? 2 : 1)
@@ -104,14 +114,14 @@ struct Cfg {
   static constexpr int IDENT_BYTES = RM ? 16 * 64 : 0;
   // O is staged in shared memory and written by TMA when there is room for a tile
   static constexpr bool STAGE = D <= 64 || (D == 128 && !RAB);
-  static constexpr int OC = D / kEpiWG;              // O columns per epilogue warpgroup
+  static constexpr int OC = DV / kEpiWG;             // O columns per epilogue warpgroup
   static constexpr int OSWB = OC * 2;                // O staging row bytes (swizzle span)
   static constexpr int WARP_STAGE = 32 * OC * 2;     // one warp's O block in shared memory
   // Epilogue groups. With two, the epilogue warps form two groups of two warpgroups and
   // group g takes the S tiles t with t % 2 == g (S and P buffer g), so that one group
   // computes while the other waits for its next tile; that pays for D = 256, whose longer
   // products leave the epilogue waiting. With one, all four warpgroups work on every tile.
-  static constexpr int EPI_GROUPS = D == 256 ? 2 : 1;
+  static constexpr int EPI_GROUPS = D >= 256 ? 2 : 1;
   static constexpr int GROUP_WARPS = kEpiWarps / EPI_GROUPS;
   static constexpr int COLS_PER_WG = kTileN / (kEpiWG / EPI_GROUPS);  // S columns per tile
   // TMEM (512 columns). For D <= 128, P has two buffers of its own and S two buffers; an
@@ -126,16 +136,16 @@ struct Cfg {
   // O accumulators: two where TMEM has room for them next to two S buffers (D <= 64), so
   // that an item's first PV product does not wait for the previous item's O to be drained
   static constexpr int NO = (P_SEP && 2 * 128 + 2 * D + NPB * PW <= (int)kTmemCols) ? 2 : 1;
-  static constexpr int NSB_FIT = (int)(kTmemCols - NO * D - (P_SEP ? NPB * PW : 0)) / 128;
+  static constexpr int NSB_FIT = (int)(kTmemCols - NO * DV - (P_SEP ? NPB * PW : 0)) / 128;
   static constexpr int NSB = NSB_FIT < 2 ? NSB_FIT : 2;  // S buffers
   // TMEM columns
   static constexpr uint32_t S_COL0 = 0, O_COL0 = NSB * 128;
-  static constexpr uint32_t P_COL0 = O_COL0 + NO * D;  // P buffers of PW columns (P_SEP only)
+  static constexpr uint32_t P_COL0 = O_COL0 + NO * DV;  // P buffers of PW columns (P_SEP only)
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
-  static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
-  static constexpr int OFF_R = OFF_V + NV * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * K_SLOT;
+  static constexpr int OFF_R = OFF_V + NV * V_TILE;
   static constexpr int OFF_I = OFF_R + NR * RSLOT;  // diagonal B operand (RM)
   static constexpr int OFF_O = OFF_I + (RM ? 1024 : 0);   // (a 1024-byte swizzle atom)
   static constexpr int OFF_BAR = OFF_O + (STAGE ? O_TILE_BYTES : 0);
@@ -155,7 +165,10 @@ struct Item {
   int tk, hist;    // first new k/v row, cached keys (key positions [0, hist))
   int off;         // key position of query row 0 (Lk - Lq)
   int split;       // key tile visited twice (cached part, new part), or -1
-  int po;          // first page_ids entry of the sequence
+  union {
+    int po;        // first page_ids entry of the sequence (key side)
+    int half;      // O half of a head dim 512 item (no key side)
+  };
   SeqGeom geom;    // over the Lk keys
 };
 
@@ -180,8 +193,14 @@ static_assert(sizeof(Bars) <= 1024, "barrier block");
 
 // KV: the kernel variant for key sides that differ from the queries (own k/v offsets, a
 // KV cache); without it the keys are the query rows and the decomposition folds away.
-template <bool KV>
+// WIDE: items 2i and 2i + 1 are the two O halves of item i of the plain numbering.
+template <bool KV, bool WIDE = false>
 __device__ __forceinline__ bool decode_item(const FwdParams& p, long long idx, Item& it) {
+  int half = 0;
+  if constexpr (WIDE) {
+    half = (int)(idx & 1);
+    idx >>= 1;
+  }
   const uint32_t e = p.work[idx / p.Nq];
   it.h = (int)(idx % p.Nq);
   it.hk = it.h / (p.Nq / p.Nk);
@@ -191,7 +210,9 @@ __device__ __forceinline__ bool decode_item(const FwdParams& p, long long idx, I
     const long long t0 = seq_start(p, it.b);
     it.tq = it.tk = (int)t0;
     it.Lq = (int)(seq_start(p, it.b + 1) - t0);
-    it.hist = it.po = it.off = 0;
+    it.hist = it.off = 0;
+    it.po = 0;
+    if constexpr (WIDE) it.half = half;
     it.split = -1;
     const long long nc = p.num_context ? load_index(p.num_context, it.b, p.index64) : 0;
     const long long nt = p.num_targets ? load_index(p.num_targets, it.b, p.index64) : 0;
@@ -341,7 +362,7 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       put_item(bars, k, it, p);
       return;
     }
-    decode_item<KV>(p, idx, it);
+    decode_item<KV, C::WIDE>(p, idx, it);
     HSTU_TRACE_EV(p, trace::kRoleQ, trace::kItem, idx);
     if (!put_item(bars, k, it, p)) return;
     long long nidx = -1;
@@ -349,7 +370,7 @@ __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       nidx = claim();
       if (nidx < total) {
         Item nx;
-        decode_item<KV>(p, nidx, nx);
+        decode_item<KV, C::WIDE>(p, nidx, nx);
 #pragma unroll
         for (int cb = 0; cb < C::NCB; ++cb)
           ptx::tma_prefetch_3d(tq, cb * C::EPC, nx.h, nx.tq + nx.m0);
@@ -433,6 +454,19 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   for (int k = 0;; ++k) {
     Item it;
     if (!get_item(bars, k, it, p) || it.n_kv < 0) return;
+    if constexpr (C::WIDE) {  // 64-column chunks of each K tile, one ring slot each
+      for (int j = 0; j < it.n_kv; ++j)
+        for (int cb = 0; cb < C::NCB; ++cb) {
+          const int s = k_it % C::NK;
+          if (!wait_bar(bars, &bars->k_empty[s], ((k_it / C::NK) & 1) ^ 1, p)) return;
+          const uint32_t full = ptx::smem_u32(&bars->k_full[s]);
+          ptx::mbar_arrive_expect_tx(full, C::K_SLOT);
+          ptx::tma_load_3d(sbase + C::OFF_K + s * C::K_SLOT, tk, full, cb * C::EPC, it.hk,
+                           it.tq + j * kTileN);
+          ++k_it;
+        }
+      continue;
+    }
     for (int j = 0; j < it.n_kv; ++j) {
       const int s = k_it % C::NK;
       // page ids are read before the wait for the slot, which hides their latency
@@ -545,14 +579,15 @@ __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       if (!wait_bar(bars, &bars->v_empty[s], ((v_it / C::NV) & 1) ^ 1, p)) return;
       HSTU_TRACE_EV(p, trace::kRoleV, trace::kLoad, v_it);
       const uint32_t full = ptx::smem_u32(&bars->v_full[s]);
-      ptx::mbar_arrive_expect_tx(full, C::TILE_BYTES);
-      const uint32_t dst = sbase + C::OFF_V + s * C::TILE_BYTES;
+      ptx::mbar_arrive_expect_tx(full, C::V_TILE);
+      const uint32_t dst = sbase + C::OFF_V + s * C::V_TILE;
       if constexpr (KV) {
         load_kv_tile<D, RAB, F8>(p, it, j, pg, tv, tc, 1, dst, full);
       } else {
+        const int x0 = C::WIDE ? it.half * C::DV : 0;  // first v column of the item
 #pragma unroll
-        for (int cb = 0; cb < C::NCB; ++cb)
-          ptx::tma_load_3d(dst + cb * C::CB_BYTES, tv, full, cb * C::EPC, it.hk,
+        for (int cb = 0; cb < C::NCBV; ++cb)
+          ptx::tma_load_3d(dst + cb * C::CB_BYTES, tv, full, x0 + cb * C::EPC, it.hk,
                            it.tq + j * kTileN);
       }
       ++v_it;
@@ -588,13 +623,32 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
                                   long long total) {
   using C = Cfg<D, RAB, F8>;
   constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16 ? 1u : 0u, 128, kTileN, 0);
-  constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16 ? 1u : 0u, 128, D, 1);
+  constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16 ? 1u : 0u, 128, C::DV, 1);
   const uint32_t sbase = ptx::smem_u32(smem);
   uint32_t q_it = 0, k_it = 0, v_it = 0, u = 0, t_base = 0;
   auto issue_s = [&](uint32_t t, int qs) -> bool {
     const uint32_t sb = t % C::NSB;
     if (t >= C::NSB && !wait_bar<kNapIssuer>(bars, &bars->pv_done[sb], ((t / C::NSB) & 1) ^ 1, p))
       return false;
+    if constexpr (C::WIDE) {  // S = sum over the 64-column chunks of Q_c K_c^T
+      const uint32_t qa = sbase + C::OFF_Q + qs * C::TILE_BYTES;
+      for (int cb = 0; cb < C::NCB; ++cb) {
+        const int ks = k_it % C::NK;
+        if (!wait_bar<kNapIssuer>(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) return false;
+        ptx::tc_fence_after();
+        const uint32_t ka = sbase + C::OFF_K + ks * C::K_SLOT;
+#pragma unroll
+        for (int kk = 0; kk < C::EPC / 16; ++kk) {
+          const uint64_t ad = ptx::smem_desc(qa + cb * C::CB_BYTES + kk * 32, 16, 8 * C::SWB, C::SWZ);
+          const uint64_t bd = ptx::smem_desc(ka + kk * 32, 16, 8 * C::SWB, C::SWZ);
+          ptx::mma_ss(tmem + C::S_COL0 + sb * 128, ad, bd, IDESC_S, (cb > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&bars->k_empty[ks]));
+        ++k_it;
+      }
+      ptx::mma_commit(ptx::smem_u32(&bars->s_full[sb]));
+      return true;
+    }
     const int ks = k_it % C::NK;
     if (!wait_bar<kNapIssuer>(bars, &bars->k_full[ks], (k_it / C::NK) & 1, p)) return false;
     ptx::tc_fence_after();
@@ -618,7 +672,7 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
     if (!wait_bar<kNapIssuer>(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) return false;
     if (first && !wait_bar<kNapIssuer>(bars, &bars->o_empty[0], (u & 1) ^ 1, p)) return false;
     ptx::tc_fence_after();
-    const uint32_t va = sbase + C::OFF_V + vs * C::TILE_BYTES;
+    const uint32_t va = sbase + C::OFF_V + vs * C::V_TILE;
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
       const uint32_t pcol = C::S_COL0 + sb * 128 + (16 * kk / C::COLS_PER_WG) * C::COLS_PER_WG +
@@ -854,7 +908,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   using C = Cfg<D, RAB, F8>;
   constexpr bool OUT_BF16 = BF16 || F8;  // O type (FP8 inputs give bf16 out)
   using T16 = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
-  constexpr int OC = D / kEpiWG;             // O columns per warpgroup
+  constexpr int OC = C::DV / kEpiWG;         // O columns per warpgroup
   constexpr int OCH = OC < 32 ? OC : 32;     // O columns per TMEM load
   const int wg = warp >> 2;
   const int quarter = warp & 3;              // TMEM lane quarter
@@ -888,11 +942,12 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     }
     // rows of out hold p.D elements (the kernel's D for a padded head dim is larger; its
     // extra columns are not stored)
-    T16* orow = out + (((long long)pit.tq + pi) * p.Nq + pit.h) * (long long)p.D + wg * OC;
+    const int oc0 = (C::WIDE ? pit.half * C::DV : 0) + wg * OC;  // first out column
+    T16* orow = out + (((long long)pit.tq + pi) * p.Nq + pit.h) * (long long)p.D + oc0;
 #pragma unroll
     for (int c0 = 0; c0 < OC; c0 += OCH) {
       uint32_t part[OCH];
-      tmem_ld<OCH>(tmem + lane_off + C::O_COL0 + ob * D + wg * OC + c0, part);
+      tmem_ld<OCH>(tmem + lane_off + C::O_COL0 + ob * C::DV + wg * OC + c0, part);
       if constexpr (OC == OCH) {
         // the whole O slice is in registers: hand the accumulator back before converting
         ptx::tc_fence_before();
@@ -913,7 +968,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
           // chunks, conflict-free for one row per lane
           *reinterpret_cast<uint4*>(stage + swizzle<C::OSWB>(lane * OC * 2 + c0 * 2 + v4 * 16)) =
               make_uint4(w[0], w[1], w[2], w[3]);
-        } else if (pi < pit.Lq && wg * OC + c0 + v4 * 8 < p.D) {
+        } else if (pi < pit.Lq && oc0 + c0 + v4 * 8 < p.D) {
           reinterpret_cast<uint4*>(orow + c0)[v4] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
@@ -930,14 +985,14 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       if (row0 + 32 <= pit.Lq) {
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && wg * OC < p.D) {  // (a slice wholly beyond a padded head dim: none)
+        if (lane == 0 && oc0 < p.D) {  // (a slice wholly beyond a padded head dim: none)
           ptx::tma_store_3d(tm_o, ptx::smem_u32(stage), wg * OC, pit.h, pit.tq + row0);
           ptx::bulk_commit();
         }
       } else if (pi < pit.Lq) {
 #pragma unroll
         for (int v4 = 0; v4 < OC / 8; ++v4)
-          if (wg * OC + v4 * 8 < p.D)
+          if (oc0 + v4 * 8 < p.D)
             reinterpret_cast<uint4*>(orow)[v4] = *reinterpret_cast<const uint4*>(
                 stage + swizzle<C::OSWB>(lane * OC * 2 + v4 * 16));
       }
@@ -1251,7 +1306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // which used the other work list, has completed.
   ptx::grid_dependency_wait();
   ptx::grid_dependents_launch();
-  const long long total = (long long)(*p.work_count) * p.Nq;
+  const long long total = (long long)(*p.work_count) * p.Nq * (C::WIDE ? 2 : 1);
   if (threadIdx.x == 0) HSTU_TRACE_EV(p, trace::kRoleCta, trace::kDepDone, 0);
 
   if (warp < kEpiWarps) {

@@ -50,6 +50,10 @@ cudaError_t dispatch_type(const FwdParams& p, const TcMaps& m, int bf16, int gri
               : dispatch_dim<false, RAB, MASK, KV>(p, m, grid, st, pdl, prepare);
 }
 
+// Head dims above 256 (fwd_tc_wide.cu): the 512 kernel, no rab, mask tiles or key side.
+cudaError_t dispatch_wide(const FwdParams& p, const TcMaps& m, int bf16, int grid,
+                          cudaStream_t st, bool pdl, bool prepare);
+
 // rab added by the tensor core (fwd_tc_rab_mma.cu): head dims 32 and 64, no key side.
 cudaError_t dispatch_rab_mma(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                              cudaStream_t st, bool pdl, bool prepare);

@@ -127,8 +127,9 @@ typedef struct {
   int batch;             /* B in [0, 2^20]; 0 = empty input, run does nothing */
   int num_heads_q;       /* Nq >= 0; 0 = empty input */
   int num_heads_kv;      /* Nk >= 1, Nq % Nk == 0 (Inputs and Outputs table, k) */
-  int head_dim;          /* D: f16/bf16 need a multiple of 16 in [16, 256], FP8 one in
-                            [16, 128]; f32 needs 1 <= D <= 256 */
+  int head_dim;          /* D: f16/bf16 need a multiple of 16 in [16, 512] (above 256: no
+                            rab, custom mask or key side), FP8 one in [16, 128]; f32 needs
+                            1 <= D <= 256 */
   int max_seqlen;        /* S in [1, 131072]: bound on every L; rab is [B, Nq, S, S];
                             for rab with f16/bf16, S must be a multiple of 8 */
   int index_is_int64;    /* 1: seq_offsets/num_context/num_targets are int64, 0: int32 */

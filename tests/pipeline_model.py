@@ -61,13 +61,19 @@ class Cfg:
     # rab added by the tensor core: the score issuer consumes the rab ring (its product
     # accumulates the rab tile into S) and releases each slot with a commit
     RM: bool = False
+    # K chunks per tile (head dim 512: eight 64-column chunks, each its own ring slot)
+    KCH: int = 1
 
 
 # The kernel's configurations (four warps per group are modelled as fewer: the barrier
 # counts scale with them, the protocol does not depend on the number).
 def kernel_cfg(D: int, rab: bool, rab_mode: str = "epi") -> Cfg:
     """rab_mode: "epi" (rab or a custom mask read by the epilogue), "mma" (rab added by the
-    tensor core, D <= 64), "two" (rab and a custom mask in one slot, D <= 128)."""
+    tensor core, D <= 64), "two" (rab and a custom mask in one slot, D <= 128). D = 512:
+    Q resident, K in 64-column chunks through a two-slot ring, one V tile, P over S."""
+    if D == 512:
+        return Cfg(D=D, NQ=1, NK=2, NV=1, NR=0, NSB=2, NPB=2, NO=1, EPI_GROUPS=2,
+                   SERIAL=True, KCH=8)
     NQ = 2 if (D <= 64 or (D == 128 and not rab)) else 1
     NK = {32: 4, 64: 2 if rab else 4, 128: 2, 256: 1}[D]
     if not rab:
@@ -199,11 +205,13 @@ def kv_producer(w: World, name):  # "K" or "V"
         if n < 0:
             return
         for j in range(n):
-            s = it % depth
-            for a in _prod_wait((empty, s), it, depth):
-                yield a
-            yield ("load", (full, s), name, s, tile)
-            it += 1
+            chunks = c.KCH if name == "K" else 1
+            for ch in range(chunks):
+                s = it % depth
+                for a in _prod_wait((empty, s), it, depth):
+                    yield a
+                yield ("load", (full, s), name, s, (tile, ch) if chunks > 1 else tile)
+                it += 1
             tile += 1
 
 
@@ -283,9 +291,19 @@ def serial_issuer(w: World):
 
     def issue_s(t, qs, item):
         nonlocal k_it
-        sb, ks = t % c.NSB, k_it % c.NK
+        sb = t % c.NSB
         if t >= c.NSB:
             yield ("wait", ("pv_done", sb), t // c.NSB - 1)
+        if c.KCH > 1:  # one product and one slot release per K chunk
+            for ch in range(c.KCH):
+                ks = k_it % c.NK
+                yield ("wait", ("k_full", ks), k_it // c.NK)
+                yield ("mma", [("Q", qs, item), ("K", ks, (t, ch))], ("S", sb, ("S", t)))
+                yield ("commit", ("k_empty", ks))
+                k_it += 1
+            yield ("commit", ("s_full", sb))
+            return
+        ks = k_it % c.NK
         yield ("wait", ("k_full", ks), k_it // c.NK)
         yield ("mma", [("Q", qs, item), ("K", ks, t)], ("S", sb, ("S", t)))
         yield ("commit", ("s_full", sb))

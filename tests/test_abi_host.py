@@ -41,7 +41,10 @@ def _desc(**kw):
     (dict(mask_type=_abi.HSTU_MASK_CUSTOM, max_seqlen=100), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(mask_type=7), _abi.HSTU_ERR_INVALID_ARG),
     (dict(head_dim=40), _abi.HSTU_ERR_UNSUPPORTED),                      # not a multiple of 16
-    (dict(head_dim=272), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(head_dim=528), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(head_dim=512, has_rab=1), _abi.HSTU_ERR_UNSUPPORTED),          # 512: built-in masks
+    (dict(head_dim=384, mask_type=_abi.HSTU_MASK_CUSTOM), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(head_dim=512, is_delta_qk=1), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(dtype=_abi.HSTU_FP8_E4M3, head_dim=144), _abi.HSTU_ERR_UNSUPPORTED),  # FP8: <= 128
     (dict(dtype=_abi.HSTU_FP8_E4M3, mask_type=_abi.HSTU_MASK_CUSTOM), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(dtype=_abi.HSTU_FP8_E4M3, has_rab=1, is_delta_qk=1), _abi.HSTU_ERR_UNSUPPORTED),

@@ -97,7 +97,21 @@ def test_head_dims(cuda_device, dtype, d, causal):
     _check(w, cuda_device)
 
 
-@pytest.mark.parametrize("d", [16, 48, 80, 208])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("d", [272, 320, 384, 448, 512])
+@pytest.mark.parametrize("causal", [True, False])
+def test_wide_head_dims(cuda_device, dtype, d, causal):
+    """Head dims above 256 (v's D up to 512): S over all D columns, O in two halves of
+    256 columns computed by separate work items, with context and target counts."""
+    w = W.Workload(name=f"{dtype}_d{d}", dtype=dtype, batch=3, num_heads_q=4, num_heads_kv=2,
+                   head_dim=d, max_seqlen=400, len_lo=1, len_hi=400, causal=causal,
+                   context_range=(0, 12) if causal else None,
+                   target_range=(0, 60) if causal else None, target_group_size=3 if causal else 0,
+                   seed=11 + d)
+    _check(w, cuda_device)
+
+
+@pytest.mark.parametrize("d", [16, 48, 80, 208, 400])
 def test_padded_head_dims_store_nothing_past_the_output(cuda_device, d):
     """A padded head dim writes exactly its D columns per row: the output is the front of a
     larger buffer whose tail must keep its sentinel (the last rows' extra columns would

@@ -8,7 +8,8 @@ import pytest
 import pipeline_model as M
 
 CONFIGS = ([(d, rab, "epi") for d in (32, 64, 128, 256) for rab in (False, True)] +
-           [(d, True, "mma") for d in (32, 64)] + [(d, True, "two") for d in (32, 64, 128)])
+           [(d, True, "mma") for d in (32, 64)] + [(d, True, "two") for d in (32, 64, 128)] +
+           [(512, False, "epi")])
 
 
 def _items(seed):

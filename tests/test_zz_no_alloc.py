@@ -47,8 +47,8 @@ def _run_both(w, dev, layout="jagged", rab_bcast=False):
 def test_noalloc_matches_plan_entry_point_on_two_calls_in_a_row(cuda_device):
     """Calls in a row (different workloads, so each one overwrites the previous one's work
     list in the shared array) all match the plan-based entry point: bf16 with context and
-    targets, fp16 with rab, the fp32 CUDA-core path, and the normal layout with a rab
-    plane broadcast to every head."""
+    targets, fp16 with rab, the fp32 CUDA-core path, the normal layout with a rab plane
+    broadcast to every head, and head dim 512."""
     first = W.Workload(name="na1", dtype="bf16", batch=4, num_heads_q=4, num_heads_kv=2,
                        head_dim=128, max_seqlen=512, len_lo=100, len_hi=512, causal=True,
                        context_range=(0, 10), target_range=(0, 40), target_group_size=4,
@@ -60,8 +60,12 @@ def test_noalloc_matches_plan_entry_point_on_two_calls_in_a_row(cuda_device):
     fourth = W.Workload(name="na4", dtype="bf16", batch=3, num_heads_q=4, num_heads_kv=4,
                         head_dim=64, max_seqlen=200, len_lo=200, len_hi=200, causal=True,
                         rab=True, rab_sigma=0.3, sigma=0.5, seed=84)
+    fifth = W.Workload(name="na5", dtype="bf16", batch=2, num_heads_q=2, num_heads_kv=1,
+                       head_dim=512, max_seqlen=300, len_lo=100, len_hi=300, causal=True,
+                       seed=85)
     for w, layout, bcast in ((first, "jagged", False), (second, "jagged", False),
-                             (third, "jagged", False), (fourth, "normal", True)):
+                             (third, "jagged", False), (fourth, "normal", True),
+                             (fifth, "jagged", False)):
         err = _run_both(w, cuda_device, layout=layout, rab_bcast=bcast)
         assert np.isfinite(err) and err <= TOL[w.dtype], f"{w.name} ({layout}): {err:.3e}"
 
