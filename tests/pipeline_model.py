@@ -75,7 +75,8 @@ def kernel_cfg(D: int, rab: bool, rab_mode: str = "epi") -> Cfg:
         return Cfg(D=D, NQ=1, NK=2, NV=1, NR=0, NSB=2, NPB=2, NO=1, EPI_GROUPS=2,
                    SERIAL=True, KCH=8)
     NQ = 2 if (D <= 64 or (D == 128 and not rab)) else 1
-    NK = {32: 4, 64: 2 if rab else 4, 128: 2, 256: 1}[D]
+    NK = {32: 4, 64: 3 if rab else 4, 128: 2, 256: 1}[D]
+    NV = 2 if (D == 64 and rab) else NK
     if not rab:
         NR = 0
     elif rab_mode == "two":
@@ -84,7 +85,7 @@ def kernel_cfg(D: int, rab: bool, rab_mode: str = "epi") -> Cfg:
         NR = {32: 4, 64: 3, 128: 2, 256: 1}[D]
     serial = D == 256
     # two O accumulators where TMEM has room beside two S buffers and two P buffers
-    return Cfg(D=D, NQ=NQ, NK=NK, NV=NK, NR=NR, NSB=2, NPB=2, NO=2 if D <= 64 else 1,
+    return Cfg(D=D, NQ=NQ, NK=NK, NV=NV, NR=NR, NSB=2, NPB=2, NO=2 if D <= 64 else 1,
                EPI_GROUPS=2 if serial else 1, SERIAL=serial, RM=rab and rab_mode == "mma")
 
 
