@@ -230,7 +230,7 @@ hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** plan) {
                            desc->dtype == HSTU_FP8_E4M3 ? 2 : (desc->dtype == HSTU_BF16 ? 1 : 0),
                            desc->mask_type == HSTU_MASK_CUSTOM ? (desc->has_rab ? 3 : 2)
                                                                 : (desc->has_rab ? 1 : 0),
-                           key_side(*desc) ? 1 : 0);
+                           key_side(*desc) ? 1 : 0, desc->descale);
       P->grid = P->num_sms;
     } else {
       e = hstu::simt_prepare();

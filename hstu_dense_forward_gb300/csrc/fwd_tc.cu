@@ -49,9 +49,10 @@ int tc_out_box_cols(int D) {  // (an item of the 512 kernel writes 256 columns)
 
 int tc_rab_box_rows() { return tc::kRabBoxRows; }
 
-cudaError_t tc_prepare(int D, int elem, int rab, int kv) {
+cudaError_t tc_prepare(int D, int elem, int rab, int kv, int ds) {
   FwdParams p = {};
   p.D = D;
+  p.ds_mode = ds;  // (FP8: the plain-cast or the descaled kernels)
   p.fp8 = elem == 2 ? 1 : 0;
   const int bf16 = elem == 1 ? 1 : 0;
   p.rab = rab ? reinterpret_cast<const void*>(1) : nullptr;

@@ -65,14 +65,15 @@ constexpr int kRabBoxRows = 32;
 // 16 keeps P values down to 2^-10 in the normal range and saturates only above P = 28.
 
 // F8: q, k, v are FP8 E4M3 (one byte each); the products run as tcgen05 kind::f8f6f4 with
-// P rounded to E4M3; O is written as bf16.
+// P rounded to E4M3; O is written as bf16. F8 = 1: the plain cast (every descale factor 1,
+// nothing read); F8 = 2: descale factors of any granularity (FwdParams::ds_mode).
 // RAB: 0 no rab; 1 rab (or a custom mask) read from shared memory by the epilogue; 3 rab
 // and a custom mask, one tile of each per ring slot, both read by the epilogue; 2 rab
 // added to S by the tensor core: for each 16-key step k of the tile, S[:, 16k:16k+16] +=
 // R[:, 16k:16k+16] (c I16) with the rab tile R as the A operand and a 16 x 16 diagonal B of
 // c = 1/alpha, so that alpha*S = alpha Q K^T + rab and the epilogue is that of the plain
 // kernel (head dims up to 64; eight M128 N16 K16 products per tile).
-template <int D, int RAB, bool F8 = false>
+template <int D, int RAB, int F8 = 0>
 struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128 || D == 256 || D == 512, "head_dim");
   // WIDE (D = 512): an item computes S over all 512 columns of q and k but O over one half
@@ -348,7 +349,7 @@ __device__ __forceinline__ uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
 // load waits behind the release of another ring's slot. With two Q buffers the Q
 // producer runs up to two work items ahead; with one, it prefetches the next
 // item's Q tile into L2 so that the load after the slot frees hits in L2.
-template <int D, int RAB, bool KV, bool F8>
+template <int D, int RAB, bool KV, int F8>
 __device__ void producer_q(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tq,
                            long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -420,7 +421,7 @@ __device__ __forceinline__ TilePages tile_pages(const FwdParams& p, const Item& 
 // cache pages when the visit's rows are cached, else rows tk + 128x - hist .. of k / v
 // (rows before the sequence's first new row belong to the cached part of a split tile
 // and meet P = 0 there).
-template <int D, int RAB, bool F8>
+template <int D, int RAB, int F8>
 __device__ __forceinline__ void load_kv_tile(const FwdParams& p, const Item& it, int j,
                                              const TilePages& pg, const CUtensorMap* tnew,
                                              const CUtensorMap* tcache, int plane, uint32_t dst,
@@ -448,7 +449,7 @@ __device__ __forceinline__ void load_kv_tile(const FwdParams& p, const Item& it,
   }
 }
 
-template <int D, int RAB, bool KV, bool F8>
+template <int D, int RAB, bool KV, int F8>
 __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tk,
                            const CUtensorMap* tc, long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -504,7 +505,7 @@ __device__ void producer_k(const FwdParams& p, Bars* bars, uint8_t* smem, const 
 // a box is skipped when its rows lie beyond the item's queries or every key of it is at or
 // beyond the end of what its rows may see (diagonal and ragged tiles): its entries are all
 // masked, and the epilogue sets a masked entry's h to 0 after adding rab.
-template <int D, int RAB, bool MASK, bool KV, bool F8>
+template <int D, int RAB, bool MASK, bool KV, int F8>
 __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tr,
                            const CUtensorMap* tm, long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -564,7 +565,7 @@ __device__ void producer_r(const FwdParams& p, Bars* bars, uint8_t* smem, const 
   }
 }
 
-template <int D, int RAB, bool KV, bool F8>
+template <int D, int RAB, bool KV, int F8>
 __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const CUtensorMap* tv,
                            const CUtensorMap* tc, long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -622,7 +623,7 @@ __device__ __forceinline__ void mma_drain(Bars* bars, const FwdParams& p) {
 // Single issuer, used when P is written over its S buffer (D = 256): there S(t+2)
 // can only start after PV(t) has read P(t), so the two products form one chain and
 // are issued in that order: S(t0), S(t0+1), then per tile PV(t), S(t+2).
-template <int D, bool BF16, int RAB, bool F8>
+template <int D, bool BF16, int RAB, int F8>
 __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                                   long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -714,7 +715,7 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
   mma_drain(bars, p);
 }
 
-template <int D, bool BF16, int RAB, bool F8>
+template <int D, bool BF16, int RAB, int F8>
 __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                              long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -792,7 +793,7 @@ __device__ void mma_s_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint
   mma_drain(bars, p);
 }
 
-template <int D, bool BF16, int RAB, bool F8>
+template <int D, bool BF16, int RAB, int F8>
 __device__ void mma_pv_issuer(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                               long long total) {
   using C = Cfg<D, RAB, F8>;
@@ -906,7 +907,7 @@ __device__ __forceinline__ float item_v_scale(const FwdParams& p, const Item& it
   return m;
 }
 
-template <int D, bool BF16, int RAB, bool MASK, bool KV, bool F8>
+template <int D, bool BF16, int RAB, bool MASK, bool KV, int F8>
 __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t tmem,
                          const CUtensorMap* tm_o, long long total, int warp, int lane) {
   using C = Cfg<D, RAB, F8>;
@@ -935,7 +936,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     const Item& pit = bars->info[slot];
     const int pi = pit.m0 + r;  // query row within the sequence
     float osc = p.silu_scale;   // (FP8: times the item's v factor)
-    if constexpr (F8) osc *= item_v_scale(p, pit);
+    if constexpr (F8 == 2) osc *= item_v_scale(p, pit);
     const uint32_t ob = u % C::NO;  // the item's O accumulator
     if (!warp_wait(bars, &bars->o_full[ob], (u / C::NO) & 1, p)) return false;
     ptx::tc_fence_after();
@@ -1024,8 +1025,8 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     // FP8 descales: alpha * qd * kd folds into the SiLU argument's factor, vd into P (block
     // granularity: per key tile, relative to the item's v factor) or the output scale
     float ha_item = half_alpha, qds = 1.f, p8_per_v = kP8Scale;
-    if constexpr (F8) {
-      if (p.ds_mode != 0) {
+    if constexpr (F8 == 2) {
+      {
         qds = __ldg(p.q_ds + ds_index(p, it.b, it.m0 / kTileM, it.h, p.ds_qb, p.Nq));
         if (p.ds_mode < 4) {
           ha_item = half_alpha * qds * __ldg(p.k_ds + ds_index(p, it.b, 0, it.hk, p.ds_kb, p.Nk));
@@ -1054,7 +1055,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       }
       const int n0 = kt.x * kTileN;
       float ha = ha_item, p8 = kP8Scale;
-      if constexpr (F8) {
+      if constexpr (F8 == 2) {
         if (p.ds_mode == 4) {
           const long long ki = ds_index(p, it.b, kt.x, it.hk, p.ds_kb, p.Nk);
           ha = half_alpha * qds * __ldg(p.k_ds + ki);
@@ -1216,7 +1217,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 
 // ------------------------------------------------------------------ kernel
 // MASK: the rab stream carries a custom mask (multiplied into P after the SiLU).
-template <int D, bool BF16, int RAB, bool MASK = false, bool KV = false, bool F8 = false>
+template <int D, bool BF16, int RAB, bool MASK = false, bool KV = false, int F8 = 0>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,

@@ -7,13 +7,13 @@
 namespace hstu {
 namespace tc {
 
-template <int D, bool BF16, int RAB, bool MASK, bool KV, bool F8 = false>
+template <int D, bool BF16, int RAB, bool MASK, bool KV, int F8 = 0>
 cudaError_t prepare_one() {
   return cudaFuncSetAttribute(fwd_tc_kernel<D, BF16, RAB, MASK, KV, F8>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D, RAB, F8>::SMEM_BYTES);
 }
 
-template <int D, bool BF16, int RAB, bool MASK, bool KV, bool F8 = false>
+template <int D, bool BF16, int RAB, bool MASK, bool KV, int F8 = 0>
 cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t stream,
                        bool pdl) {
   cudaLaunchConfig_t cfg = {};
@@ -71,6 +71,9 @@ cudaError_t dispatch_f8(const FwdParams& p, const TcMaps& m, int grid, cudaStrea
                         bool prepare);
 cudaError_t dispatch_f8_rab(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
                             bool pdl, bool prepare);
+// FP8 with descale factors (fwd_tc_f8_ds.cu; fwd_tc_f8_rab.cu with rab): F8 = 2 kernels
+cudaError_t dispatch_f8_ds(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
+                           bool pdl, bool prepare);
 
 // Key-side variants (fwd_tc_kv.cu, fwd_tc_kv_mask.cu): own k/v offsets and / or a KV cache.
 cudaError_t dispatch_kv(const FwdParams& p, const TcMaps& m, int bf16, int grid,

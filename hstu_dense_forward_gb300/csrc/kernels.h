@@ -136,7 +136,7 @@ int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
 int tc_rab_box_rows();        // rows of one rab / custom-mask load box (64 columns each)
 // elem: 0 f16, 1 bf16, 2 FP8 E4M3; rab: 0 none, 1 rab, 2 custom mask, 3 custom mask and
 // rab; kv: the key-side variant (own k/v offsets, KV cache)
-cudaError_t tc_prepare(int D, int elem, int rab, int kv);
+cudaError_t tc_prepare(int D, int elem, int rab, int kv, int ds = 0);  // ds: FP8 descale mode
 // The variant that adds rab with the tensor core exists for these (rab = 1: rab, not a
 // custom mask; no key side; bf16 / fp16; head dim 32 or 64).
 bool rab_mma_dim(int D, int elem, int rab, int kv);
