@@ -375,9 +375,11 @@ def _config(w, inp, m, ws):
 
 
 # Configurations timed in the same run next to the headline one (the other four
-# configurations of the workload list): parity-test cases that also get a line of numbers.
+# configurations of the workload list, then the FP8, paged-cache and head-dim-512 ones):
+# parity-test cases that also get a line of numbers.
 EXTRA_WORKLOADS = ("fp32_tiny", "bf16_rab_b16_s1024_h8_d64", "fp16_gqa8x2_targets_b8_s4096_d128",
-                   "bf16_long_b4_s8192_h4_d256")
+                   "bf16_long_b4_s8192_h4_d256", "fp8_causal_b32_s2048_h4_d128",
+                   "bf16_paged_b128_hist1k_4k_h4_d128", "bf16_causal_b8_s2048_h4_d512")
 
 
 def run_ours(args):

@@ -83,6 +83,11 @@ WORKLOADS = {
         name="fp8_causal_b32_s2048_h4_d128", dtype="fp8", batch=32, num_heads_q=4,
         num_heads_kv=4, head_dim=128, max_seqlen=2048, len_lo=256, len_hi=2048, causal=True,
         sigma=0.5, seed=1),
+    # head dim 512 (Inputs and Outputs table: v's D up to 512), causal jagged
+    "bf16_causal_b8_s2048_h4_d512": Workload(
+        name="bf16_causal_b8_s2048_h4_d512", dtype="bf16", batch=8, num_heads_q=4,
+        num_heads_kv=4, head_dim=512, max_seqlen=2048, len_lo=512, len_hi=2048, causal=True,
+        sigma=0.5, seed=6),
     "bf16_long_b4_s8192_h4_d256": Workload(
         name="bf16_long_b4_s8192_h4_d256", dtype="bf16", batch=4, num_heads_q=4, num_heads_kv=4,
         head_dim=256, max_seqlen=8192, len_lo=8192, len_hi=8192, causal=False,
