@@ -327,7 +327,7 @@ static hstu_status make_maps(hstu_fwd_plan* P, const void* q, const void* k, con
             encode3d(&P->maps.k, ty, k ? k : (cache ? cache : q), D, Nk, (uint64_t)(Tk > 0 ? Tk : 1),
                      D * eb, Nk * D * eb, epc, 1, hstu::kTileN, swz) &&
             encode3d(&P->maps.v, ty, v ? v : (cache ? cache : q), D, Nk, (uint64_t)(Tk > 0 ? Tk : 1),
-                     D * eb, Nk * D * eb, epc, 1, hstu::kTileN, swz) &&
+                     D * eb, Nk * D * eb, epc, 1, (uint32_t)hstu::tc_v_box_rows(d.head_dim), swz) &&
             encode3d(&P->maps.out, oty, out, D, Nq, (uint64_t)T, D * 2, Nq * D * 2, oc, 1, 32,
                      oc * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                      : oc * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -839,7 +839,8 @@ hstu_status hstu_fwd_run_noalloc(const hstu_fwd_desc* desc, const void* q, const
                    Nk = (uint64_t)d.num_heads_kv, T = (uint64_t)total_tokens;
     bool ok = encode3d(&maps.q, ty, q, D, Nq, T, D * 2, Nq * D * 2, epc, 1, hstu::kTileM, swz) &&
               encode3d(&maps.k, ty, k, D, Nk, T, D * 2, Nk * D * 2, epc, 1, hstu::kTileN, swz) &&
-              encode3d(&maps.v, ty, v, D, Nk, T, D * 2, Nk * D * 2, epc, 1, hstu::kTileN, swz) &&
+              encode3d(&maps.v, ty, v, D, Nk, T, D * 2, Nk * D * 2, epc, 1,
+                       (uint32_t)hstu::tc_v_box_rows(d.head_dim), swz) &&
               encode3d(&maps.out, ty, out, D, Nq, T, D * 2, Nq * D * 2, oc, 1, 32,
                        oc * 2 == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                        : oc * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B

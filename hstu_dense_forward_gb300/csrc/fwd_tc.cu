@@ -49,6 +49,8 @@ int tc_out_box_cols(int D) {  // (an item of the 512 kernel writes 256 columns)
 
 int tc_rab_box_rows() { return tc::kRabBoxRows; }
 
+int tc_v_box_rows(int D) { return tc_kernel_dim(D) == 512 ? tc::Cfg<512, 0, 0>::VROWS : kTileN; }
+
 cudaError_t tc_prepare(int D, int elem, int rab, int kv, int ds) {
   FwdParams p = {};
   p.D = D;

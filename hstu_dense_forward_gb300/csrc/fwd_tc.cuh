@@ -78,8 +78,9 @@ struct Cfg {
   static_assert(D == 32 || D == 64 || D == 128 || D == 256 || D == 512, "head_dim");
   // WIDE (D = 512): an item computes S over all 512 columns of q and k but O over one half
   // (256 columns) of v and out; the two halves of a tile are two items. Q stays resident
-  // (128 KB), K streams as 64-column chunks through a ring of its own, V as one 256-column
-  // tile; P is written over S as for D = 256. No rab, mask tiles, key side or FP8.
+  // (128 KB), K streams as 64-column chunks through a ring of four, V as two 64-key halves
+  // of 256 columns through a one-slot ring; P is written over S as for D = 256. No rab,
+  // mask tiles, key side or FP8.
   static constexpr bool WIDE = D == 512;
   static_assert(!WIDE || (!RAB && !F8), "head_dim 512: no rab or FP8");
   static constexpr int DV = WIDE ? 256 : D;  // O columns of one item
@@ -98,7 +99,9 @@ struct Cfg {
   static constexpr int TILE_BYTES = 128 * D * EB;
   static constexpr int O_TILE_BYTES = 128 * DV * 2;  // O is 16-bit
   static constexpr int K_SLOT = WIDE ? CB_BYTES : TILE_BYTES;  // one K ring slot
-  static constexpr int V_TILE = 128 * DV * EB;                 // one V tile (DV columns)
+  static constexpr int VROWS = WIDE ? 64 : 128;                // keys of one V ring slot
+  static constexpr int V_TILE = VROWS * DV * EB;               // one V slot (DV columns)
+  static constexpr int V_CB = VROWS * SWB;                     // one of its column blocks
   static constexpr int NCBV = DV / EPC;                        // its column blocks
   static constexpr int KS = F8 ? 32 : 16;      // K elements of one MMA (32 bytes)
   static constexpr int PW = F8 ? 32 : 64;      // TMEM columns of one P buffer (128 keys)
@@ -108,7 +111,7 @@ struct Cfg {
   // requested when the product two tiles back completes, which is too late under the rab
   // stream's HBM load (measured 1.2% faster than two K and two V slots, and than two K,
   // two V and four rab slots)
-  static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 3 : 4) : (D == 128 ? 2 : (WIDE ? 2 : 1)));
+  static constexpr int NK = D == 32 ? 4 : (D == 64 ? (RAB ? 3 : 4) : (D == 128 ? 2 : (WIDE ? 4 : 1)));
   static constexpr int NV = WIDE ? 1 : ((D == 64 && RAB) ? 2 : NK);
   // rab tiles stream from HBM once each: the deeper the ring, the more bytes in flight
   // (with a custom mask beside rab a slot holds both tiles and the ring is shallower)
@@ -588,11 +591,26 @@ __device__ void producer_v(const FwdParams& p, Bars* bars, uint8_t* smem, const 
       const uint32_t dst = sbase + C::OFF_V + s * C::V_TILE;
       if constexpr (KV) {
         load_kv_tile<D, RAB, F8>(p, it, j, pg, tv, tc, 1, dst, full);
-      } else {
-        const int x0 = C::WIDE ? it.half * C::DV : 0;  // first v column of the item
+      } else if constexpr (C::WIDE) {
+        // the first 64 keys of the tile (the map's box is 64 rows); the second half below
 #pragma unroll
         for (int cb = 0; cb < C::NCBV; ++cb)
-          ptx::tma_load_3d(dst + cb * C::CB_BYTES, tv, full, x0 + cb * C::EPC, it.hk,
+          ptx::tma_load_3d(dst + cb * C::V_CB, tv, full, it.half * C::DV + cb * C::EPC, it.hk,
+                           it.tq + j * kTileN);
+        ++v_it;
+        const int s2 = v_it % C::NV;
+        if (!wait_bar(bars, &bars->v_empty[s2], ((v_it / C::NV) & 1) ^ 1, p)) return;
+        const uint32_t full2 = ptx::smem_u32(&bars->v_full[s2]);
+        ptx::mbar_arrive_expect_tx(full2, C::V_TILE);
+        const uint32_t dst2 = sbase + C::OFF_V + s2 * C::V_TILE;
+#pragma unroll
+        for (int cb = 0; cb < C::NCBV; ++cb)
+          ptx::tma_load_3d(dst2 + cb * C::V_CB, tv, full2, it.half * C::DV + cb * C::EPC, it.hk,
+                           it.tq + j * kTileN + C::VROWS);
+      } else {
+#pragma unroll
+        for (int cb = 0; cb < C::NCBV; ++cb)
+          ptx::tma_load_3d(dst + cb * C::CB_BYTES, tv, full, cb * C::EPC, it.hk,
                            it.tq + j * kTileN);
       }
       ++v_it;
@@ -673,21 +691,25 @@ __device__ void mma_serial_issuer(const FwdParams& p, Bars* bars, uint8_t* smem,
   };
   auto issue_pv = [&](uint32_t t, bool first) -> bool {
     const uint32_t sb = t % C::NSB;
-    const int vs = v_it % C::NV;
-    if (!wait_bar<kNapIssuer>(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) return false;
     if (first && !wait_bar<kNapIssuer>(bars, &bars->o_empty[0], (u & 1) ^ 1, p)) return false;
-    ptx::tc_fence_after();
-    const uint32_t va = sbase + C::OFF_V + vs * C::V_TILE;
+    // one V slot holds VROWS keys: the tile's 128 keys in one slot, or (WIDE) two halves
+    for (int k0 = 0; k0 < kTileN; k0 += C::VROWS) {
+      const int vs = v_it % C::NV;
+      if (!wait_bar<kNapIssuer>(bars, &bars->v_full[vs], (v_it / C::NV) & 1, p)) return false;
+      ptx::tc_fence_after();
+      const uint32_t va = sbase + C::OFF_V + vs * C::V_TILE;
 #pragma unroll
-    for (int kk = 0; kk < kTileN / 16; ++kk) {
-      const uint32_t pcol = C::S_COL0 + sb * 128 + (16 * kk / C::COLS_PER_WG) * C::COLS_PER_WG +
-                            ((16 * kk) % C::COLS_PER_WG) / 2;
-      const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::CB_BYTES, 8 * C::SWB, C::SWZ);
-      ptx::mma_ts(tmem + C::O_COL0, tmem + pcol, bd, IDESC_O, (!first || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < C::VROWS / 16; ++kk) {
+        const int key = k0 + 16 * kk;  // first key of this K = 16 step
+        const uint32_t pcol = C::S_COL0 + sb * 128 + (key / C::COLS_PER_WG) * C::COLS_PER_WG +
+                              (key % C::COLS_PER_WG) / 2;
+        const uint64_t bd = ptx::smem_desc(va + kk * 16 * C::SWB, C::V_CB, 8 * C::SWB, C::SWZ);
+        ptx::mma_ts(tmem + C::O_COL0, tmem + pcol, bd, IDESC_O, (!first || key > 0) ? 1u : 0u);
+      }
+      ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
+      ++v_it;
     }
-    ptx::mma_commit(ptx::smem_u32(&bars->v_empty[vs]));
     ptx::mma_commit(ptx::smem_u32(&bars->pv_done[sb]));
-    ++v_it;
     return true;
   };
   for (int k = 0;; ++k) {

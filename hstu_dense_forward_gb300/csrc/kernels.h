@@ -134,6 +134,7 @@ int tc_kernel_dim(int D);     // head dim of the kernel variant that runs D (32/
 int tc_swizzle_bytes(int D, int elem_bytes);  // row width of one TMA box / UMMA swizzle atom
 int tc_out_box_cols(int D);   // columns of one output store box (32 rows each)
 int tc_rab_box_rows();        // rows of one rab / custom-mask load box (64 columns each)
+int tc_v_box_rows(int D);     // rows of one V load box (64 for the 512 kernel, else 128)
 // elem: 0 f16, 1 bf16, 2 FP8 E4M3; rab: 0 none, 1 rab, 2 custom mask, 3 custom mask and
 // rab; kv: the key-side variant (own k/v offsets, KV cache)
 cudaError_t tc_prepare(int D, int elem, int rab, int kv, int ds = 0);  // ds: FP8 descale mode

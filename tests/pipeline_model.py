@@ -61,8 +61,10 @@ class Cfg:
     # rab added by the tensor core: the score issuer consumes the rab ring (its product
     # accumulates the rab tile into S) and releases each slot with a commit
     RM: bool = False
-    # K chunks per tile (head dim 512: eight 64-column chunks, each its own ring slot)
+    # K chunks per tile (head dim 512: eight 64-column chunks, each its own ring slot) and
+    # V slots per tile (head dim 512: two 64-key halves)
     KCH: int = 1
+    VCH: int = 1
 
 
 # The kernel's configurations (four warps per group are modelled as fewer: the barrier
@@ -72,8 +74,8 @@ def kernel_cfg(D: int, rab: bool, rab_mode: str = "epi") -> Cfg:
     tensor core, D <= 64), "two" (rab and a custom mask in one slot, D <= 128). D = 512:
     Q resident, K in 64-column chunks through a two-slot ring, one V tile, P over S."""
     if D == 512:
-        return Cfg(D=D, NQ=1, NK=2, NV=1, NR=0, NSB=2, NPB=2, NO=1, EPI_GROUPS=2,
-                   SERIAL=True, KCH=8)
+        return Cfg(D=D, NQ=1, NK=4, NV=1, NR=0, NSB=2, NPB=2, NO=1, EPI_GROUPS=2,
+                   SERIAL=True, KCH=8, VCH=2)
     NQ = 2 if (D <= 64 or (D == 128 and not rab)) else 1
     NK = {32: 4, 64: 3 if rab else 4, 128: 2, 256: 1}[D]
     NV = 2 if (D == 64 and rab) else NK
@@ -206,7 +208,7 @@ def kv_producer(w: World, name):  # "K" or "V"
         if n < 0:
             return
         for j in range(n):
-            chunks = c.KCH if name == "K" else 1
+            chunks = c.KCH if name == "K" else c.VCH
             for ch in range(chunks):
                 s = it % depth
                 for a in _prod_wait((empty, s), it, depth):
@@ -313,14 +315,17 @@ def serial_issuer(w: World):
 
     def issue_pv(t, first, item):
         nonlocal v_it
-        sb, vs = t % c.NSB, v_it % c.NV
-        yield ("wait", ("v_full", vs), v_it // c.NV)
+        sb = t % c.NSB
         if first and u >= 1:
             yield ("wait", ("o_empty", 0), u - 1)
-        yield ("mma", [("S", sb, ("P", t)), ("V", vs, t)], ("O", 0, item))
-        yield ("commit", ("v_empty", vs))
+        for ch in range(c.VCH):  # one V slot per chunk of keys
+            vs = v_it % c.NV
+            yield ("wait", ("v_full", vs), v_it // c.NV)
+            yield ("mma", [("S", sb, ("P", t)), ("V", vs, (t, ch) if c.VCH > 1 else t)],
+                   ("O", 0, item))
+            yield ("commit", ("v_empty", vs))
+            v_it += 1
         yield ("commit", ("pv_done", sb))
-        v_it += 1
 
     for k, n in enumerate(w.items + [-1]):
         yield from _get_item(w, k)
