@@ -275,6 +275,53 @@ def dequantize(x, descale, granularity, seq_offsets, *, block=128):
     return out
 
 
+def dequantize_kv(k, v, kv_cache, k_descale, v_descale, granularity, seq_offsets_k,
+                  page_offsets, page_ids, last_page_len, *, block=128):
+    """FP8 descale factors on the key side: the keys of sequence b are its cached history
+    (pages page_ids[page_offsets[b]] .. in order, rows of each page, the last one holding
+    last_page_len[b] rows) followed by its new rows k/v [seq_offsets_k[b] ..). Key position
+    p (0 for the first cached row) takes the factor of (b, p // block, kv head) ("block"),
+    (b, kv head) ("head"), b ("batch") or the one factor ("tensor"). Returns the values
+    (k, v, kv_cache) in fp64; cache rows that belong to no sequence keep their stored
+    values (they are never read as keys). Plain loops."""
+    k, v, cache = _f64(k), _f64(v), _f64(kv_cache)
+    so = _i64(seq_offsets_k)
+    po, ids, last = _i64(page_offsets), _i64(page_ids), _i64(last_page_len)
+    fk = np.asarray(k_descale, dtype=np.float64)
+    fv = np.asarray(v_descale, dtype=np.float64)
+    if granularity not in DESCALE_GRANULARITIES:
+        raise ValueError(f"granularity must be one of {DESCALE_GRANULARITIES}")
+    page_size = cache.shape[2]
+
+    def factor(f, b, pos, h):
+        if granularity == "tensor":
+            return f.reshape(-1)[0]
+        if granularity == "batch":
+            return f[b]
+        if granularity == "head":
+            return f[b, h]
+        return f[b, pos // block, h]
+
+    ko, vo, co = k.copy(), v.copy(), cache.copy()
+    for b in range(so.shape[0] - 1):
+        pages = [int(x) for x in ids[int(po[b]):int(po[b + 1])]]
+        hist = 0
+        for s_, pg in enumerate(pages):
+            rows = page_size if s_ + 1 < len(pages) else int(last[b])
+            for r in range(rows):
+                pos = s_ * page_size + r
+                for h in range(cache.shape[3]):
+                    co[pg, 0, r, h] = factor(fk, b, pos, h) * cache[pg, 0, r, h]
+                    co[pg, 1, r, h] = factor(fv, b, pos, h) * cache[pg, 1, r, h]
+            hist += rows
+        for t in range(int(so[b]), int(so[b + 1])):
+            pos = hist + t - int(so[b])
+            for h in range(k.shape[1]):
+                ko[t, h] = factor(fk, b, pos, h) * k[t, h]
+                vo[t, h] = factor(fv, b, pos, h) * v[t, h]
+    return ko, vo, co
+
+
 def valid(i, j, L, mask_type=MASK_CAUSAL, num_context=0, num_targets=0, target_group_size=0):
     """The oracle's mask predicate for one pair (0 or 1)."""
     return _load().hstu_oracle_valid(i, j, L, mask_type, num_context, num_targets,

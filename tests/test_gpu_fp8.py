@@ -289,3 +289,45 @@ def test_fp8_descale_shapes_are_checked(cuda_device):
     bf = inp["q"].to(cuda_device)
     with pytest.raises(ValueError):  # descales go with FP8 inputs
         hstu_fwd(bf, bf, bf, so, max_seqlen=64, q_descale=1.0, k_descale=1.0, v_descale=1.0)
+
+
+@pytest.mark.parametrize("gran", ["head", "block"])
+def test_fp8_descales_with_paged_cache(cuda_device, gran):
+    """Descale factors on the key side: cached pages and new rows take the factor of their
+    key position (per block: position // 128, cached history first), queries that of their
+    row; against the oracle on the dequantized values (oracle.dequantize_kv)."""
+    from dataclasses import replace
+    kw = replace(W.KV_WORKLOADS["bf16_paged_b128_hist1k_4k_h4_d128"], batch=4,
+                 hist_range=(100, 600), new_range=(10, 200), page_size=32, seed=74)
+    inp = W.generate_kv(kw)
+    g = torch.Generator().manual_seed(75)
+    st = {n: (inp[n].float() * 64).clamp(-440, 440).to(E4M3) for n in ("q", "k", "v", "kv_cache")}
+    B, Nq, Nk = kw.batch, kw.num_heads_q, kw.num_heads_kv
+    Sq, Sk = int(inp["max_seqlen"]), int(inp["max_seqlen_k"])
+    fq = _factors(gran, B, Nq, -(-Sq // 128), g)
+    fk = _factors(gran, B, Nk, -(-Sk // 128), g)
+    fv = _factors(gran, B, Nk, -(-Sk // 128), g, lo=-10.0, hi=-5.0)
+    dev = cuda_device
+    dv = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = hstu_fwd(st["q"].to(dev), st["k"].to(dev), st["v"].to(dev), dv["seq_offsets"],
+                   max_seqlen=Sq, max_seqlen_k=Sk, num_targets=dv["num_targets"],
+                   target_group_size=1, alpha=dv["alpha"], silu_scale=dv["silu_scale"],
+                   seq_offsets_k=dv["seq_offsets_k"], kv_cache=st["kv_cache"].to(dev),
+                   page_offsets=dv["page_offsets"], page_ids=dv["page_ids"],
+                   last_page_len=dv["last_page_len"], q_descale=fq.to(dev), k_descale=fk.to(dev),
+                   v_descale=fv.to(dev))
+    torch.cuda.synchronize()
+    qd = oracle.dequantize(st["q"].double().numpy(), fq.double().numpy(), gran,
+                           inp["seq_offsets"])
+    kd, vd, cd = oracle.dequantize_kv(st["k"].double().numpy(), st["v"].double().numpy(),
+                                      st["kv_cache"].double().numpy(), fk.double().numpy(),
+                                      fv.double().numpy(), gran, inp["seq_offsets_k"],
+                                      inp["page_offsets"], inp["page_ids"], inp["last_page_len"])
+    ref = oracle.hstu_fwd(qd, kd, vd, inp["seq_offsets"], seq_offsets_k=inp["seq_offsets_k"],
+                          kv_cache=cd, page_offsets=inp["page_offsets"], page_ids=inp["page_ids"],
+                          last_page_len=inp["last_page_len"], num_targets=inp["num_targets"],
+                          mask_type=oracle.MASK_CAUSAL, target_group_size=1, alpha=inp["alpha"],
+                          silu_scale=inp["silu_scale"], max_seqlen=Sk, nthreads=8)
+    T = int(inp["seq_offsets"][-1])
+    got = out.double().cpu().numpy()[:T]
+    assert np.abs(got - ref[:T]).max() / np.abs(ref[:T]).max() <= 2.0 ** -4

@@ -567,3 +567,34 @@ def test_dequantize_reduces_to_per_tensor():
     assert np.array_equal(oracle.dequantize(x, np.full(3, 0.25), "batch", so), ref)
     assert np.array_equal(oracle.dequantize(x, np.full((3, 3), 0.25), "head", so), ref)
     assert np.array_equal(oracle.dequantize(x, np.full((3, 2, 3), 0.25), "block", so), ref)
+
+
+def test_dequantize_kv_positions_by_hand():
+    """Key positions on the key side: sequence 0 has cached pages [3, 1] (page_size 2, last
+    page 1 row) then two new rows; sequence 1 no pages and one new row. With per-block
+    factors of block 2 the positions 0..4 of sequence 0 fall in blocks 0, 0, 1, 1, 2."""
+    cache = np.arange(4 * 2 * 2 * 1 * 1, dtype=np.float64).reshape(4, 2, 2, 1, 1) + 1.0
+    k = np.array([[[10.0]], [[20.0]], [[30.0]]])
+    v = -k
+    so_k = np.array([0, 2, 3])
+    po = np.array([0, 2, 2])
+    ids = np.array([3, 1])
+    last = np.array([1, 1])
+    fk = np.array([[[2.0], [3.0], [5.0]], [[7.0], [11.0], [13.0]]])  # [B, 3 blocks, 1 head]
+    fv = fk * 10
+    ko, vo, co = oracle.dequantize_kv(k, v, cache, fk, fv, "block", so_k, po, ids, last,
+                                      block=2)
+    # cached: page 3 rows 0, 1 = positions 0, 1 (block 0); page 1 row 0 = position 2 (block 1)
+    assert co[3, 0, 0, 0, 0] == 2.0 * cache[3, 0, 0, 0, 0]
+    assert co[3, 0, 1, 0, 0] == 2.0 * cache[3, 0, 1, 0, 0]
+    assert co[1, 0, 0, 0, 0] == 3.0 * cache[1, 0, 0, 0, 0]
+    assert co[1, 1, 0, 0, 0] == 30.0 * cache[1, 1, 0, 0, 0]
+    assert co[1, 0, 1, 0, 0] == cache[1, 0, 1, 0, 0]  # past the last page's rows: untouched
+    assert co[0, 0, 0, 0, 0] == cache[0, 0, 0, 0, 0]  # a page of no sequence
+    # new rows of sequence 0: positions 3 (block 1) and 4 (block 2); sequence 1: position 0
+    assert ko[0, 0, 0] == 3.0 * 10.0 and ko[1, 0, 0] == 5.0 * 20.0
+    assert ko[2, 0, 0] == 7.0 * 30.0 and vo[2, 0, 0] == 70.0 * -30.0
+    # per head: one factor per (sequence, kv head) everywhere
+    fh = np.array([[0.5], [4.0]])
+    ko, vo, co = oracle.dequantize_kv(k, v, cache, fh, fh, "head", so_k, po, ids, last)
+    assert co[1, 1, 0, 0, 0] == 0.5 * cache[1, 1, 0, 0, 0] and ko[2, 0, 0] == 4.0 * 30.0
