@@ -88,6 +88,11 @@ def test_null_arguments(built_lib):
                             None, None) == _abi.HSTU_ERR_INVALID_ARG
     n = ctypes.c_int()
     assert lib.hstu_fwd_get_error(None, ctypes.byref(n)) == _abi.HSTU_ERR_INVALID_ARG
+    a = _abi.Args()
+    assert lib.hstu_fwd_run_args(None, ctypes.byref(a), None) == _abi.HSTU_ERR_INVALID_ARG
+    assert lib.hstu_fwd_run_fp8(None, None, None, None, None, None, None, None, None, None, 0,
+                                1.0, 1.0, None, None) == _abi.HSTU_ERR_INVALID_ARG
+    assert lib.hstu_fwd_trace_read(None, None, 0) == _abi.HSTU_ERR_INVALID_ARG
     for s in range(6):
         assert lib.hstu_status_string(s)
 

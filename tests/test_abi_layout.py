@@ -1,4 +1,5 @@
-"""The ctypes mirrors of the C ABI structs (hstu_fwd_desc, hstu_fwd_kv) must match
+"""The ctypes mirrors of the C ABI structs (hstu_fwd_desc, hstu_fwd_kv, hstu_fwd_descale,
+hstu_fwd_args) must match
 include/hstu_fwd.h field by field: a small C program built with gcc prints every field's
 offset and each struct's size, compared with the ctypes layout. CPU only."""
 import ctypes
@@ -26,7 +27,9 @@ def _c_layout(tmp_path, struct, fields):
     return {k: int(v) for k, v in (line.split() for line in out if line)}
 
 
-@pytest.mark.parametrize("struct,cls", [("hstu_fwd_desc", _abi.Desc), ("hstu_fwd_kv", _abi.KV)])
+@pytest.mark.parametrize("struct,cls", [("hstu_fwd_desc", _abi.Desc), ("hstu_fwd_kv", _abi.KV),
+                                        ("hstu_fwd_descale", _abi.Descale),
+                                        ("hstu_fwd_args", _abi.Args)])
 def test_ctypes_mirror_matches_header(tmp_path, struct, cls):
     fields = [f for f, _ in cls._fields_]
     c = _c_layout(tmp_path, struct, fields)
@@ -41,7 +44,9 @@ def test_enum_values_match_header(tmp_path):
              "HSTU_ERR_TIMEOUT", "HSTU_ERR_DEVICE_CHECK", "HSTU_F32", "HSTU_F16", "HSTU_BF16",
              "HSTU_FP8_E4M3", "HSTU_MASK_CAUSAL", "HSTU_MASK_UPPER", "HSTU_MASK_NONE",
              "HSTU_MASK_CUSTOM", "HSTU_DEVERR_NONE", "HSTU_DEVERR_OFFSETS",
-             "HSTU_DEVERR_TIMEOUT", "HSTU_LAYOUT_JAGGED", "HSTU_LAYOUT_NORMAL"]
+             "HSTU_DEVERR_TIMEOUT", "HSTU_LAYOUT_JAGGED", "HSTU_LAYOUT_NORMAL",
+             "HSTU_DESCALE_CAST", "HSTU_DESCALE_TENSOR", "HSTU_DESCALE_BATCH",
+             "HSTU_DESCALE_HEAD", "HSTU_DESCALE_BLOCK"]
     body = "\n".join(f'  printf("{n} %d\\n", (int){n});' for n in names)
     src.write_text('#include <stdio.h>\n#include "hstu_fwd.h"\nint main(void) {\n' + body +
                    "\n  return 0;\n}\n")

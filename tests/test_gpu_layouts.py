@@ -222,3 +222,43 @@ def test_d256_rab_runs_are_identical_and_match_oracle(cuda_device, dtype):
                           silu_scale=inp["silu_scale"], max_seqlen=640, nthreads=8)
     T = int(inp["seq_offsets"][-1])
     assert _rel_err(outs[0][:T], ref[:T]) <= TOL[dtype]
+
+
+def test_general_entry_point_matches_the_specific_ones(cuda_device):
+    """hstu_fwd_run_args with a plain plan (rab, context and targets) gives hstu_fwd_run's
+    output bit for bit, and rejects inputs the plan does not take (a mask, descales)."""
+    import ctypes
+
+    from hstu_dense_forward_gb300 import HstuFwdPlan, _abi
+    w = W.Workload(name="args", dtype="bf16", batch=3, num_heads_q=4, num_heads_kv=2,
+                   head_dim=64, max_seqlen=264, len_lo=60, len_hi=264, causal=True,
+                   context_range=(0, 10), target_range=(0, 30), target_group_size=2, rab=True,
+                   rab_sigma=0.3, seed=61)
+    d = W.to_device(W.generate(w), cuda_device)
+    plan = HstuFwdPlan(dtype=torch.bfloat16, batch=3, num_heads_q=4, num_heads_kv=2, head_dim=64,
+                       max_seqlen=264, index_is_int64=True, causal=True, target_group_size=2,
+                       has_rab=True, has_num_context=True, has_num_targets=True)
+    a_out = torch.full_like(d["q"], float("nan"))
+    b_out = torch.full_like(d["q"], float("nan"))
+    plan.run(d["q"], d["k"], d["v"], d["seq_offsets"], a_out, rab=d["rab"],
+             num_context=d["num_context"], num_targets=d["num_targets"], alpha=d["alpha"],
+             silu_scale=d["silu_scale"])
+    args = _abi.Args()
+    args.q, args.k, args.v, args.out = (d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
+                                        b_out.data_ptr())
+    args.seq_offsets, args.rab = d["seq_offsets"].data_ptr(), d["rab"].data_ptr()
+    args.num_context, args.num_targets = d["num_context"].data_ptr(), d["num_targets"].data_ptr()
+    args.total_tokens, args.alpha, args.silu_scale = d["q"].shape[0], d["alpha"], d["silu_scale"]
+    stream = torch.cuda.current_stream(cuda_device).cuda_stream or None
+    lib = _abi.lib()
+    assert lib.hstu_fwd_run_args(plan._h, ctypes.byref(args), stream) == _abi.HSTU_OK
+    torch.cuda.synchronize()
+    T = int(d["seq_offsets"][-1])
+    assert torch.equal(a_out[:T], b_out[:T])
+    args.mask = d["rab"].data_ptr()  # a plain plan takes no mask
+    assert lib.hstu_fwd_run_args(plan._h, ctypes.byref(args), stream) == _abi.HSTU_ERR_INVALID_ARG
+    args.mask = None
+    ds = _abi.Descale()
+    args.descale = ctypes.pointer(ds)  # nor descale factors
+    assert lib.hstu_fwd_run_args(plan._h, ctypes.byref(args), stream) == _abi.HSTU_ERR_INVALID_ARG
+    plan.close()
