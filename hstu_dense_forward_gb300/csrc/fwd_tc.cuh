@@ -1,33 +1,37 @@
-// bf16 / fp16 HSTU forward on the 5th-generation tensor cores (sm_103a).
+// bf16 / fp16 / FP8 E4M3 HSTU forward on the 5th-generation tensor cores (sm_103a).
 //
 // Operation ("RecOps Running Case Documentation", feature table and Inputs and
 // Outputs table): per sequence, query head and 128-row query tile,
-//   S = Q K^T, x = alpha*S (+ rab), P = silu(x) masked, O = P V, out = silu_scale*O.
+//   S = Q K^T, x = alpha*S (+ rab), P = silu(x) masked (x custom mask), O = P V,
+//   out = silu_scale*O.
 // HSTU has no softmax, so there is no running max or rescaling: O is a plain sum
 // over key tiles and key tiles the mask removes entirely are never visited.
 //
 // CTA layout (persistent, one CTA per SM, 704 threads):
 //   warps 0-15 epilogue: four warpgroups; each thread owns one query row (TMEM lane)
-//              and a quarter of the 128 key columns of every S tile (for D = 256: two
+//              and a quarter of the 128 key columns of every S tile (for D >= 256: two
 //              groups of two warpgroups take alternate tiles, half the columns each). It
-//              reads S from TMEM, applies alpha, rab, SiLU (as h + h*tanh(h), h = x/2,
-//              one MUFU op per element) and the mask, and writes P (bf16/fp16) back to
-//              TMEM. An item's O is read, scaled, converted and stored by TMA after P of
-//              the next item's second tile.
+//              reads S from TMEM, applies alpha, rab, SiLU (as h + h*tanh(h), h = x/2, in
+//              fp32, one MUFU op per element), the mask and a custom mask, and writes P
+//              (16-bit, or E4M3) back to TMEM. An item's O is read, scaled, converted and
+//              stored (TMA from a staging block, or row stores) after P of the next item's
+//              first tile.
 //   warps 16, 18, 19, 21  producers: TMA loads of the K ring, the V ring, the Q tiles
-//              and the rab ring, one thread each; the Q producer also claims and decodes
-//              the work items (heaviest first; CTA i starts with item i).
+//              and the rab (and custom-mask) ring, one thread each; the Q producer also
+//              claims and decodes the work items (heaviest first; CTA i starts with item i).
 //   warp 17    TMEM owner; one thread issues S(t) = Q K(t)^T (tcgen05.mma, A = Q and
-//              B = K from smem, K-major) as soon as its S buffer is free.
+//              B = K from smem, K-major) as soon as its S buffer is free, followed by the
+//              rab products when the tensor core adds rab (RAB = 2).
 //   warp 20    one thread issues O += P(t) V(t) (tcgen05.mma, A = P from TMEM, B = V
 //              from smem, MN-major) as soon as P(t) is written. Two issuers keep a
 //              thread stalled on tensor-pipe back-pressure from delaying the other
-//              product. D = 256 uses one issuer (see mma_serial_issuer).
-// TMEM (512 columns): two S buffers of 128 columns from column 0, O after them (D columns)
-// and, for D <= 128, two P buffers of 64 columns after O. An S buffer is handed back as
-// soon as the epilogue has loaded it, so S(t + 2) is computed while the epilogue works on
-// tile t. For D = 256 P(t) is written over the columns of S(t) already read, and
-// S(t + 2) waits for PV(t) to have read P(t).
+//              product. D >= 256 uses one issuer (see mma_serial_issuer).
+// TMEM (512 columns): two S buffers of 128 columns from column 0, O after them (D columns,
+// 256 for the head-dim-512 kernel, which computes one half of O per item) and, for
+// D <= 128, two P buffers of 64 columns after O. An S buffer is handed back as soon as
+// the epilogue has loaded it, so S(t + 2) is computed while the epilogue works on tile t.
+// For D >= 256 P(t) is written over the columns of S(t) already read, and S(t + 2) waits
+// for PV(t) to have read P(t).
 //
 // Every mbarrier wait is bounded (FwdParams::timeout_ns): on expiry the CTA
 // records HSTU_DEVERR_TIMEOUT, all roles leave their loops, the MMA queue is
@@ -127,7 +131,7 @@ struct Cfg {
   static constexpr int WARP_STAGE = 32 * OC * 2;     // one warp's O block in shared memory
   // Epilogue groups. With two, the epilogue warps form two groups of two warpgroups and
   // group g takes the S tiles t with t % 2 == g (S and P buffer g), so that one group
-  // computes while the other waits for its next tile; that pays for D = 256, whose longer
+  // computes while the other waits for its next tile; that pays for D >= 256, whose longer
   // products leave the epilogue waiting. With one, all four warpgroups work on every tile.
   static constexpr int EPI_GROUPS = D >= 256 ? 2 : 1;
   static constexpr int GROUP_WARPS = kEpiWarps / EPI_GROUPS;
@@ -136,8 +140,8 @@ struct Cfg {
   // S buffer is released as soon as the epilogue has loaded it, so the next score products
   // overlap the epilogue. O has two accumulators where they fit beside them (D <= 64), one
   // for D = 128 (two there would leave one S buffer, which measured slower: it holds the
-  // score products back). For D = 256 (O takes 256 columns) P is written over the S buffer
-  // it came from and one thread issues all MMAs.
+  // score products back). For D >= 256 (O takes 256 columns) P is written over the S
+  // buffer it came from and one thread issues all MMAs.
   static constexpr bool P_SEP = (D <= 128);
   static constexpr bool SERIAL = !P_SEP;
   static constexpr int NPB = 2;             // P buffers (P_SEP), P over S otherwise
