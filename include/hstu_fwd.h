@@ -346,7 +346,8 @@ HSTU_API hstu_status hstu_fwd_count_pairs_kv(const hstu_fwd_desc* desc,
  *     HSTU_ERR_UNSUPPORTED without launching anything.
  *   - Arguments, layouts and ownership are those of hstu_fwd_run; desc is validated
  *     like hstu_fwd_create validates it, on every call. Descriptors with is_delta_qk or
- *     page_size set, or mask_type CUSTOM, return HSTU_ERR_UNSUPPORTED.
+ *     page_size set, mask_type CUSTOM or dtype HSTU_FP8_E4M3 return
+ *     HSTU_ERR_UNSUPPORTED.
  *   - The first call on a device (with that device current) looks up the array's
  *     device address and configures the kernels for that device; make that first
  *     call before any stream capture.
