@@ -63,3 +63,24 @@ def test_largest_batch_of_short_sequences(cuda_device, dtype):
         if L:
             rows.append((int(b), int(g.integers(0, 4)), int(g.integers(0, L))))
     assert _sampled(inp, got, w, rows) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("head_dim,heads", [(512, (16, 4)), (48, (16, 16))])
+def test_longest_sequence_other_head_dims(cuda_device, head_dim, heads):
+    """The longest sequence with 16 query heads at head dim 512 (two O halves per tile) and
+    at a padded head dim (48 on the 64 kernel), context and targets at their limits."""
+    w = W.Workload(name="max_d", dtype="bf16", batch=1, num_heads_q=heads[0],
+                   num_heads_kv=heads[1], head_dim=head_dim, max_seqlen=20480,
+                   fixed_offsets=(0, 20480), causal=True, context_range=(256, 256),
+                   target_range=(512, 512), target_group_size=3, sigma=0.5, seed=93)
+    inp = W.generate(w)
+    d = W.to_device(inp, cuda_device)
+    got = hstu_fwd(d["q"], d["k"], d["v"], d["seq_offsets"], max_seqlen=w.max_seqlen,
+                   num_context=d["num_context"], num_targets=d["num_targets"],
+                   target_group_size=3, alpha=w.alpha_value, silu_scale=w.silu_scale_value)
+    torch.cuda.synchronize()
+    g = np.random.default_rng(3)
+    rows = [(0, int(g.integers(0, heads[0])), int(i))
+            for i in np.concatenate([[0, 255, 256, 19967, 19968, 20479], g.integers(0, 20480, 20)])]
+    assert _sampled(inp, got, w, rows) <= TOL["bf16"]
+    assert torch.isfinite(got.float()).all()
