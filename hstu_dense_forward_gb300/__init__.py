@@ -113,14 +113,20 @@ class HstuFwdPlan:
             kv.page_offsets = ptr(page_offsets) or None
             kv.page_ids = ptr(page_ids) or None
             kv.last_page_len = ptr(last_page_len) or None
-        if self.desc.mask_type == _abi.HSTU_MASK_CUSTOM and self.desc.has_rab:
-            a = _abi.Args()  # a custom mask with rab: the general entry point
+        custom = self.desc.mask_type == _abi.HSTU_MASK_CUSTOM
+        if (custom and self.desc.has_rab) or (custom and
+                                              self.desc.descale != _abi.HSTU_DESCALE_CAST):
+            a = _abi.Args()  # a custom mask with rab or descales: the general entry point
             a.q, a.k, a.v, a.out = q.data_ptr(), ptr(k) or None, ptr(v) or None, out.data_ptr()
             a.seq_offsets = ptr(seq_offsets) or None
             if kv is not None:
                 a.kv = ctypes.pointer(kv)
             a.rab, a.mask = ptr(rab) or None, ptr(mask) or None
             a.total_tokens, a.alpha, a.silu_scale = q.shape[0], float(alpha), float(silu_scale)
+            if self.desc.descale != _abi.HSTU_DESCALE_CAST:
+                ds = _abi.Descale()
+                ds.q, ds.k, ds.v = (t.data_ptr() for t in descale)
+                a.descale = ctypes.pointer(ds)
             _abi.check(self._keep.hstu_fwd_run_args(self._h, ctypes.byref(a),
                                                     stream.cuda_stream or None),
                        "hstu_fwd_run_args")
@@ -362,7 +368,7 @@ def hstu_fwd(q, k, v, seq_offsets=None, *, max_seqlen=None, rab=None, num_contex
     if custom:
         if num_context is not None or num_targets is not None:
             raise ValueError("a custom mask takes no num_context or num_targets")
-        _check_tensor(mask, "mask", q.dtype, dev, 4)
+        _check_tensor(mask, "mask", out_dtype(q.dtype), dev, 4)  # (bf16 for FP8 inputs)
         if tuple(mask.shape) != (B, Nq, Sk, Sk):
             raise ValueError(f"mask must be [B, Nq, S, S], got {list(mask.shape)}")
     stream = torch.cuda.current_stream(dev)

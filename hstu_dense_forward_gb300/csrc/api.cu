@@ -182,10 +182,11 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
     if (d->dtype != HSTU_F32 && key_bound(*d) % 8 != 0) return HSTU_ERR_UNSUPPORTED;
   }
   if (d->dtype == HSTU_FP8_E4M3) {
-    // FP8 E4M3 inputs: head dims up to 128; bf16 rab without a key side; no custom mask
-    // (it multiplies 16-bit P, which the 8-bit products do not have)
+    // FP8 E4M3 inputs: head dims up to 128; bf16 rab or a bf16 custom mask (one of them)
+    // without a key side
     if (!hstu::tc_supported_dim(d->head_dim) || d->head_dim > 128) return HSTU_ERR_UNSUPPORTED;
-    if (d->mask_type == HSTU_MASK_CUSTOM) return HSTU_ERR_UNSUPPORTED;
+    if (d->mask_type == HSTU_MASK_CUSTOM && (d->has_rab || key_side(*d)))
+      return HSTU_ERR_UNSUPPORTED;
     if (d->has_rab && (key_side(*d) || key_bound(*d) % 8 != 0)) return HSTU_ERR_UNSUPPORTED;
   } else if (d->dtype == HSTU_F32) {
     if (d->head_dim > 256) return HSTU_ERR_UNSUPPORTED;
@@ -542,7 +543,9 @@ hstu_status hstu_fwd_run_fp8(hstu_fwd_plan* P, const void* q, const void* k, con
                              const void* num_context, const void* num_targets,
                              const hstu_fwd_descale* descale, long long total_tokens,
                              float alpha, float silu_scale, void* out, void* stream) {
-  if (!P || P->desc.dtype != HSTU_FP8_E4M3) return HSTU_ERR_INVALID_ARG;
+  // (a CUSTOM plan takes its mask through hstu_fwd_run_masked or hstu_fwd_run_args)
+  if (!P || P->desc.dtype != HSTU_FP8_E4M3 || P->desc.mask_type == HSTU_MASK_CUSTOM)
+    return HSTU_ERR_INVALID_ARG;
   return run_impl(P, q, k, v, seq_offsets, kv, rab, false, num_context, num_targets,
                   total_tokens, alpha, silu_scale, out, stream, descale);
 }

@@ -1184,6 +1184,11 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
             float s0, s1;
             ptx::mul_f32x2(s0, s1, h[2 * e], h[2 * e + 1], p8, p8);
             ptx::fma_f32x2(p0, p1, s0, s1, t0, t1, s0, s1);
+            if constexpr (MASK) {  // custom mask (bf16) applied before the E4M3 rounding
+              float m0, m1;
+              unpack2<true>(mw[e], m0, m1);
+              ptx::mul_f32x2(p0, p1, p0, p1, m0, m1);
+            }
             const uint32_t q = ptx::cvt_e4m3x2_f32(p0, p1);  // keys 2e, 2e + 1
             if (e & 1)
               pk[e >> 1] |= q << 16;

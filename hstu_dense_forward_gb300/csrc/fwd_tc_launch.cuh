@@ -65,12 +65,15 @@ cudaError_t dispatch_mask(const FwdParams& p, const TcMaps& m, int bf16, int gri
 cudaError_t dispatch_mask_rab(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                               cudaStream_t st, bool pdl, bool prepare);
 
-// FP8 E4M3 variants (fwd_tc_f8.cu): head dims up to 128, no custom mask, with or without a
-// key side; with rab (fwd_tc_f8_rab.cu) without a key side.
+// FP8 E4M3 variants (fwd_tc_f8.cu): head dims up to 128, with or without a key side; with
+// rab (fwd_tc_f8_rab.cu) or a custom mask (fwd_tc_f8_mask.cu) without a key side.
 cudaError_t dispatch_f8(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st, bool pdl,
                         bool prepare);
 cudaError_t dispatch_f8_rab(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
                             bool pdl, bool prepare);
+// FP8 with a custom mask (fwd_tc_f8_mask.cu): no key side, no rab
+cudaError_t dispatch_f8_mask(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
+                             bool pdl, bool prepare);
 // FP8 with descale factors (fwd_tc_f8_ds.cu; fwd_tc_f8_rab.cu with rab): F8 = 2 kernels
 cudaError_t dispatch_f8_ds(const FwdParams& p, const TcMaps& m, int grid, cudaStream_t st,
                            bool pdl, bool prepare);

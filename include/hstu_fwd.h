@@ -70,8 +70,9 @@ typedef enum {
  * copies with descale factors (desc.descale, hstu_fwd_run_fp8); both products run on
  * 8-bit tensor cores with fp32 accumulation, P is rounded to E4M3 (saturating) for the
  * second one, and out is bf16. rab (has_rab, no key side) is bf16 [B, Nq or 1, S, S] and
- * is added in fp32. Head dims 16 to 128 in steps of 16; no custom mask
- * (HSTU_ERR_UNSUPPORTED); not on the allocation-free entry point. */
+ * is added in fp32; a custom mask (no key side, not together with rab) is bf16 and
+ * multiplies P in fp32 before its E4M3 rounding. Head dims 16 to 128 in steps of 16; not
+ * on the allocation-free entry point. */
 typedef enum { HSTU_F32 = 0, HSTU_F16 = 1, HSTU_BF16 = 2, HSTU_FP8_E4M3 = 3 } hstu_dtype;
 
 /* Granularity of the FP8 descale factors (feature table, "FP8 quantization types": cast,
@@ -289,8 +290,9 @@ struct hstu_fwd_descale {
  * with qd, kd, vd the factors of desc.descale's granularity for row i and key j.
  * kv as for hstu_fwd_run_kv (NULL for a plan without a key side), rab as for hstu_fwd_run
  * (bf16; not with a key side), other arguments as for hstu_fwd_run. descale may be NULL
- * only for a CAST plan. Returns HSTU_ERR_INVALID_ARG for a plan that is not FP8, and
- * hstu_fwd_run / hstu_fwd_run_kv do for an FP8 plan whose granularity is not CAST.
+ * only for a CAST plan. Returns HSTU_ERR_INVALID_ARG for a plan that is not FP8 or has
+ * mask_type CUSTOM (hstu_fwd_run_args takes a mask with descales), and hstu_fwd_run /
+ * hstu_fwd_run_kv do for an FP8 plan whose granularity is not CAST.
  */
 HSTU_API hstu_status hstu_fwd_run_fp8(hstu_fwd_plan* plan, const void* q, const void* k,
                                       const void* v, const void* seq_offsets,

@@ -46,7 +46,10 @@ def _desc(**kw):
     (dict(head_dim=384, mask_type=_abi.HSTU_MASK_CUSTOM), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(head_dim=512, is_delta_qk=1), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(dtype=_abi.HSTU_FP8_E4M3, head_dim=144), _abi.HSTU_ERR_UNSUPPORTED),  # FP8: <= 128
-    (dict(dtype=_abi.HSTU_FP8_E4M3, mask_type=_abi.HSTU_MASK_CUSTOM), _abi.HSTU_ERR_UNSUPPORTED),
+    (dict(dtype=_abi.HSTU_FP8_E4M3, mask_type=_abi.HSTU_MASK_CUSTOM, has_rab=1),
+     _abi.HSTU_ERR_UNSUPPORTED),                                         # FP8: mask or rab
+    (dict(dtype=_abi.HSTU_FP8_E4M3, mask_type=_abi.HSTU_MASK_CUSTOM, is_delta_qk=1),
+     _abi.HSTU_ERR_UNSUPPORTED),
     (dict(dtype=_abi.HSTU_FP8_E4M3, has_rab=1, is_delta_qk=1), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(descale=_abi.HSTU_DESCALE_HEAD), _abi.HSTU_ERR_INVALID_ARG),  # descales: FP8 only
     (dict(dtype=_abi.HSTU_FP8_E4M3, descale=5), _abi.HSTU_ERR_INVALID_ARG),

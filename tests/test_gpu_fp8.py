@@ -163,17 +163,46 @@ def test_fp8_full_size_sampled_rows(cuda_device):
     assert np.abs(sel - ref).max() / np.abs(ref).max() <= 2.0 ** -4
 
 
-def test_fp8_rejects_custom_mask_and_key_side_rab(cuda_device):
+def test_fp8_rejects_key_side_rab_and_mask_with_rab(cuda_device):
     from hstu_dense_forward_gb300 import HstuError
     w, inp = _case(64, (2, 2), B=2, S=64)
     q8 = inp["q"].float().to(E4M3).to(cuda_device)
     so = inp["seq_offsets"].to(cuda_device)
-    mask = torch.ones(2, 2, 64, 64, dtype=E4M3, device=cuda_device)
-    with pytest.raises((HstuError, TypeError)):
-        hstu_fwd(q8, q8, q8, so, max_seqlen=64, mask=mask)
     rab = torch.zeros(2, 2, 64, 64, dtype=torch.bfloat16, device=cuda_device)
     with pytest.raises(HstuError):
         hstu_fwd(q8, q8, q8, so, max_seqlen=64, rab=rab, seq_offsets_k=so)
+    with pytest.raises(HstuError):
+        hstu_fwd(q8, q8, q8, so, max_seqlen=64, rab=rab, mask=torch.ones_like(rab))
+
+
+@pytest.mark.parametrize("gran", ["cast", "head"])
+def test_fp8_custom_mask(cuda_device, gran):
+    """A bf16 custom mask (weights in [-1, 2)) with FP8 inputs: P times the mask in fp32,
+    then rounded to E4M3; against the oracle on the dequantized values (global bound)."""
+    g = torch.Generator().manual_seed(501)
+    w, inp = _case(64, (4, 2), B=3, S=264, causal=False, seed=502)
+    so = inp["seq_offsets"]
+    T = int(so[-1])
+    spread = 1.0 if gran == "cast" else 64.0  # (cast: the values themselves are N(0, 1))
+    q8, k8, v8 = (_e4m3((T, n, 64), g, spread) for n in (4, 2, 2))
+    m = (torch.rand(3, 4, 264, 264, generator=g) * 3.0 - 1.0).to(torch.bfloat16)
+    dev = cuda_device
+    kw = {}
+    if gran == "cast":
+        qd, kd, vd = (x.double().numpy() for x in (q8, k8, v8))
+    else:
+        fq, fk, fv = (_factors("head", 3, n, 3, g) for n in (4, 2, 2))
+        kw = dict(q_descale=fq.to(dev), k_descale=fk.to(dev), v_descale=fv.to(dev))
+        qd, kd, vd = (oracle.dequantize(x.double().numpy(), f.double().numpy(), "head", so)
+                      for x, f in ((q8, fq), (k8, fk), (v8, fv)))
+    alpha = w.alpha_value
+    out = hstu_fwd(q8.to(dev), k8.to(dev), v8.to(dev), so.to(dev), max_seqlen=264,
+                   alpha=alpha, silu_scale=w.silu_scale_value, mask=m.to(dev), **kw)
+    torch.cuda.synchronize()
+    ref = oracle.hstu_fwd(qd, kd, vd, so, mask=m.double().numpy(), mask_type=oracle.MASK_CUSTOM,
+                          alpha=alpha, silu_scale=w.silu_scale_value, max_seqlen=264, nthreads=8)
+    got = out.double().cpu().numpy()[:T]
+    assert np.abs(got - ref[:T]).max() / np.abs(ref[:T]).max() <= 2.0 ** -4
 
 
 # ------------------------------------------------ descale granularities, rab, head dims
