@@ -175,9 +175,9 @@ static hstu_status validate_desc(const hstu_fwd_desc* d) {
     // the rab path, so rab and a custom mask together are not built
     if (d->has_num_context || d->has_num_targets || (d->rab_heads && !d->has_rab))
       return HSTU_ERR_INVALID_ARG;
-    // with rab: one ring slot holds a rab and a mask tile (head dims up to 128, no key side)
+    // with rab: one ring slot holds a rab and a mask tile (head dims up to 128)
     if (d->has_rab && d->dtype != HSTU_F32 &&
-        (key_side(*d) || !hstu::tc_supported_dim(d->head_dim) || d->head_dim > 128))
+        (!hstu::tc_supported_dim(d->head_dim) || d->head_dim > 128))
       return HSTU_ERR_UNSUPPORTED;
     if (d->dtype != HSTU_F32 && key_bound(*d) % 8 != 0) return HSTU_ERR_UNSUPPORTED;
   }

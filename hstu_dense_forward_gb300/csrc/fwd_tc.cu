@@ -16,8 +16,9 @@ cudaError_t dispatch(const FwdParams& p, const TcMaps& m, int bf16, int grid, cu
   if (p.fp8) return tc::dispatch_f8(p, m, grid, st, pdl, prepare);
   if (tc_kernel_dim(p.D) == 512) return tc::dispatch_wide(p, m, bf16, grid, st, pdl, prepare);
   if (key_side(p))
-    return p.rab_is_mask ? tc::dispatch_kv_mask(p, m, bf16, grid, st, pdl, prepare)
-                         : tc::dispatch_kv(p, m, bf16, grid, st, pdl, prepare);
+    return p.mask ? tc::dispatch_kv_mask_rab(p, m, bf16, grid, st, pdl, prepare)
+           : p.rab_is_mask ? tc::dispatch_kv_mask(p, m, bf16, grid, st, pdl, prepare)
+                           : tc::dispatch_kv(p, m, bf16, grid, st, pdl, prepare);
   if (p.rab_is_mask) return tc::dispatch_mask(p, m, bf16, grid, st, pdl, prepare);
   if (p.mask) return tc::dispatch_mask_rab(p, m, bf16, grid, st, pdl, prepare);
   if (p.rab && p.rab_mma) return tc::dispatch_rab_mma(p, m, bf16, grid, st, pdl, prepare);

@@ -61,9 +61,12 @@ cudaError_t dispatch_rab_mma(const FwdParams& p, const TcMaps& m, int bf16, int 
 // Custom-mask variants (fwd_tc_mask.cu): prepare (shared-memory opt-in) or launch.
 cudaError_t dispatch_mask(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                           cudaStream_t st, bool pdl, bool prepare);
-// A custom mask together with rab (fwd_tc_mask_rab.cu): head dims up to 128, no key side.
+// A custom mask together with rab (fwd_tc_mask_rab.cu; with a key side fwd_tc_kv_mask_rab.cu):
+// head dims up to 128.
 cudaError_t dispatch_mask_rab(const FwdParams& p, const TcMaps& m, int bf16, int grid,
                               cudaStream_t st, bool pdl, bool prepare);
+cudaError_t dispatch_kv_mask_rab(const FwdParams& p, const TcMaps& m, int bf16, int grid,
+                                 cudaStream_t st, bool pdl, bool prepare);
 
 // FP8 E4M3 variants (fwd_tc_f8.cu): head dims up to 128, with or without a key side; with
 // rab (fwd_tc_f8_rab.cu) or a custom mask (fwd_tc_f8_mask.cu) without a key side.

@@ -111,8 +111,8 @@ typedef enum {
   HSTU_MASK_CUSTOM = 3  /* mask [B, Nq, S, S] passed to hstu_fwd_run_masked (or, together
                            with rab, to hstu_fwd_run_args): P is multiplied by mask[b, h, i, j]
                            after the SiLU and the scaling; no context or target counts. With
-                           rab (has_rab): head dims up to 128 and no key side on the 16-bit
-                           path (HSTU_ERR_UNSUPPORTED otherwise) */
+                           rab (has_rab): head dims up to 128 on the 16-bit path
+                           (HSTU_ERR_UNSUPPORTED otherwise) */
 } hstu_mask_type;
 
 /* Device error word values (hstu_fwd_get_error). */

@@ -35,7 +35,6 @@ def _desc(**kw):
     (dict(num_heads_q=3, num_heads_kv=2), _abi.HSTU_ERR_INVALID_ARG),   # Nq % Nk != 0
     (dict(mask_type=_abi.HSTU_MASK_UPPER), _abi.HSTU_ERR_UNSUPPORTED),  # "currently not supported"
     (dict(mask_type=_abi.HSTU_MASK_CUSTOM, has_rab=1, head_dim=256), _abi.HSTU_ERR_UNSUPPORTED),
-    (dict(mask_type=_abi.HSTU_MASK_CUSTOM, has_rab=1, is_delta_qk=1), _abi.HSTU_ERR_UNSUPPORTED),
     (dict(mask_type=_abi.HSTU_MASK_CUSTOM, has_num_targets=1), _abi.HSTU_ERR_INVALID_ARG),
     (dict(mask_type=_abi.HSTU_MASK_CUSTOM, rab_heads=1), _abi.HSTU_ERR_INVALID_ARG),
     (dict(mask_type=_abi.HSTU_MASK_CUSTOM, max_seqlen=100), _abi.HSTU_ERR_UNSUPPORTED),

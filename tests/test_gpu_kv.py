@@ -191,6 +191,24 @@ def test_paged_custom_mask_matches_oracle(cuda_device):
     assert _rel_err(got, _oracle(inp, mask=m)) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("dtype,d,ps", [("bf16", 64, 32), ("fp16", 128, 128), ("bf16", 96, 0),
+                                         ("fp32", 64, 32)])
+def test_key_side_custom_mask_with_rab(cuda_device, dtype, d, ps):
+    """A custom mask together with rab on the key side (a paged history, or own k/v offsets
+    without a cache): both read at the query positions, rab added before the SiLU and the
+    mask multiplied after it."""
+    w, inp = _case(dtype, d, (2, 2), batch=3, hist_range=(50, 300), new_range=(10, 200),
+                   page_size=ps, causal=False, targets_are_queries=False, rab=True,
+                   rab_sigma=0.4, seed=66 + d)
+    inp["num_targets"] = None
+    Sk = inp["max_seqlen_k"]
+    g = torch.Generator().manual_seed(4)
+    m = (torch.rand(3, 2, Sk, Sk, generator=g) * 3.0 - 1.0).to(inp["q"].dtype)
+    got = _gpu(inp, cuda_device, mask=m.to(cuda_device), causal=True)
+    torch.cuda.synchronize()
+    assert _rel_err(got, _oracle(inp, mask=m)) <= TOL[dtype]
+
+
 def _plan_and_inputs(dev, ps=32, max_seqlen=None, max_seqlen_k=None):
     w, inp = _case("bf16", 64, (2, 2), batch=3, hist_range=(40, 200), new_range=(5, 60),
                    page_size=ps, seed=65)
