@@ -101,8 +101,12 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
   // With a key side of its own (a few queries against long, often cached, key sequences)
   // the query tiles of one sequence read the same keys: they are kept next to each other
   // in the list, binned by the sequence's heaviest tile, so that they run at the same time
-  // and the later reads of the keys hit L2. Otherwise each tile is binned by its own count.
-  const bool group = p.seq_offsets_k != nullptr || p.page_offsets != nullptr;
+  // and the later reads of the keys hit L2. Without a mask every tile of a sequence visits
+  // all of its keys, and its tiles are kept together the same way: interleaved with other
+  // sequences' tiles, a sequence's keys are read again from HBM once the keys of all
+  // sequences exceed L2. With a causal mask each tile is binned by its own count.
+  const bool group = p.seq_offsets_k != nullptr || p.page_offsets != nullptr ||
+                     p.mask_type == kMaskNone;
   // pass 1: histogram of key-visit counts
   for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
     const SeqKV kv = seq_kv(p, b);
