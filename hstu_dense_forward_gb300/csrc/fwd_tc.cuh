@@ -124,8 +124,11 @@ struct Cfg {
   static constexpr int RSLOT = (TWO ? 2 : 1) * RAB_BYTES;  // one ring slot
   // RM: the 16 x 16 diagonal B operand, K-major rows of 64 bytes (64-byte swizzle)
   static constexpr int IDENT_BYTES = RM ? 16 * 64 : 0;
-  // O is staged in shared memory and written by TMA when there is room for a tile
-  static constexpr bool STAGE = D <= 64 || (D == 128 && !RAB);
+  // O is staged in shared memory and written by TMA in the kernels without a rab / mask
+  // stream (head dims up to 128). With one, each thread writes its row directly: the rab
+  // workload's short items make the staging's proxy fence and store issue a larger share
+  // of every item (measured 1.7 % faster at D = 64 with rab).
+  static constexpr bool STAGE = !RAB && D <= 128;
   static constexpr int OC = DV / kEpiWG;             // O columns per epilogue warpgroup
   static constexpr int OSWB = OC * 2;                // O staging row bytes (swizzle span)
   static constexpr int WARP_STAGE = 32 * OC * 2;     // one warp's O block in shared memory
