@@ -131,11 +131,27 @@ def test_padded_head_dims_store_nothing_past_the_output(cuda_device, d):
 @pytest.mark.parametrize("lengths", [(1,), (5, 1, 15), (128,), (129, 127), (256, 255, 257),
                                      (0, 70, 0)])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-def test_ragged_edges(cuda_device, lengths, dtype):
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_edges(cuda_device, lengths, dtype, causal):
     so = tuple(int(x) for x in np.concatenate([[0], np.cumsum(lengths)]))
     w = W.Workload(name="edges", dtype=dtype, batch=len(lengths), num_heads_q=2, num_heads_kv=2,
-                   head_dim=64, max_seqlen=max(max(lengths), 8), fixed_offsets=so, causal=True,
+                   head_dim=64, max_seqlen=max(max(lengths), 8), fixed_offsets=so, causal=causal,
                    seed=11)
+    _check(w, cuda_device)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_bidirectional_many_sequences(cuda_device, dtype):
+    """Without a mask the work list keeps each sequence's query tiles together (one run of
+    positions per sequence, binned by its key-tile count): many sequences of lengths from 1
+    to 700 fill most bins with runs of different lengths, next to empty sequences."""
+    g = np.random.default_rng(41)
+    lengths = g.integers(1, 701, size=46)
+    lengths[[3, 17, 30]] = 0
+    so = tuple(int(x) for x in np.concatenate([[0], np.cumsum(lengths)]))
+    w = W.Workload(name="bidir_many", dtype=dtype, batch=len(lengths), num_heads_q=4,
+                   num_heads_kv=2, head_dim=64, max_seqlen=704, fixed_offsets=so, causal=False,
+                   seed=42)
     _check(w, cuda_device)
 
 
