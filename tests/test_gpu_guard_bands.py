@@ -29,3 +29,22 @@ def test_no_write_outside_out(cuda_device, dtype, d):
     assert bool((big[:BAND] == 1234.0).all())
     assert bool((big[BAND + T:] == 1234.0).all())
     assert bool(torch.isfinite(out.float()).all())
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 64), ("fp16", 32), ("bf16", 128)])
+def test_no_write_outside_out_with_rab(cuda_device, dtype, d):
+    """The rab kernels write O by row stores from registers (no staging), with ragged last
+    tiles: still nothing outside [0, T) of out."""
+    w = W.scaled(W.WORKLOADS["bf16_rab_b16_s1024_h8_d64"], batch=3, max_seqlen=304, len_lo=1,
+                 len_hi=300, dtype=dtype, head_dim=d, num_heads_q=2, num_heads_kv=2, seed=98)
+    inp = W.generate(w)
+    dv = W.to_device(inp, cuda_device)
+    T = dv["q"].shape[0]
+    big = torch.full((T + 2 * BAND, 2, d), 1234.0, dtype=dv["q"].dtype, device=cuda_device)
+    out = big[BAND:BAND + T]
+    hstu_fwd(dv["q"], dv["k"], dv["v"], dv["seq_offsets"], max_seqlen=304, rab=dv["rab"],
+             causal=True, alpha=w.alpha_value, silu_scale=w.silu_scale_value, out=out)
+    torch.cuda.synchronize()
+    assert bool((big[:BAND] == 1234.0).all())
+    assert bool((big[BAND + T:] == 1234.0).all())
+    assert bool(torch.isfinite(out.float()).all())
