@@ -203,6 +203,18 @@ HSTU_API hstu_status hstu_fwd_create(const hstu_fwd_desc* desc, hstu_fwd_plan** 
  * Asynchronous: no allocation, no synchronisation. One plan must not be used by
  * two runs that may execute at the same time (it holds one work list).
  * Returns HSTU_OK with nothing enqueued when B, Nq or T is 0.
+ *
+ * Stream order (every entry point that takes a plan): the run's first kernel, the
+ * work-list build, is launched with programmatic dependent launch. It reads the index
+ * arrays (seq_offsets, num_context, num_targets and the key side's seq_offsets_k,
+ * page_offsets, page_ids, last_page_len) while the kernel before it on the stream may
+ * still run, and it completes only after that kernel; every other input is read after
+ * that. A kernel that does not trigger its dependents early (no
+ * cudaTriggerProgrammaticLaunchCompletion / griddepcontrol.launch_dependents): every
+ * PyTorch kernel, and this library's forward kernel, which writes no index array, has
+ * completed before the build starts. A kernel that does trigger early and writes those
+ * arrays after its trigger must not directly precede a run: put another stream operation
+ * between them.
  */
 HSTU_API hstu_status hstu_fwd_run(hstu_fwd_plan* plan, const void* q, const void* k, const void* v,
                          const void* seq_offsets, const void* rab, const void* num_context,
