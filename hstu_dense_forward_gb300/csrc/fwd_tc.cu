@@ -43,9 +43,10 @@ int tc_swizzle_bytes(int D, int elem_bytes) {
   return k * elem_bytes >= 128 ? 128 : k * elem_bytes;
 }
 
-int tc_out_box_cols(int D) {  // (an item of the 512 kernel writes 256 columns)
+int tc_out_box_cols(int D) {  // a warpgroup's O staging box (head dims up to 128; the larger
+                              // ones store O rows directly and never read this map)
   const int k = tc_kernel_dim(D);
-  return (k > 256 ? 256 : k) / tc::kEpiWG;
+  return k == 32 ? tc::Cfg<32, 0>::OC : k == 64 ? tc::Cfg<64, 0>::OC : k == 128 ? tc::Cfg<128, 0>::OC : 64;
 }
 
 int tc_rab_box_rows() { return tc::kRabBoxRows; }

@@ -51,16 +51,17 @@
 namespace hstu {
 namespace tc {
 
-constexpr int kEpiWG = 4;                   // epilogue warpgroups
-constexpr int kEpiWarps = 4 * kEpiWG;
-constexpr int kProducerWarp = kEpiWarps;      // K and rab loads
-constexpr int kMmaWarp = kEpiWarps + 1;
-constexpr int kVProducerWarp = kEpiWarps + 2;  // V loads
-constexpr int kQProducerWarp = kEpiWarps + 3;  // Q loads
-constexpr int kPvWarp = kEpiWarps + 4;         // issues O += P V
-constexpr int kRabWarp = kEpiWarps + 5;        // rab loads
-constexpr int kThreads = (kEpiWarps + 6) * 32;
-constexpr int kEpiThreads = kEpiWarps * 32;
+// Warp roles: the epilogue warpgroups come first (their count is set per head dim by Cfg),
+// then six warps of one working thread each, in this order after them.
+enum : int {
+  kRoleProducerK = 0,  // K and rab loads
+  kRoleMma = 1,        // score products (and, with P over S, every product)
+  kRoleProducerV = 2,  // V loads
+  kRoleProducerQ = 3,  // Q loads, item claims
+  kRolePv = 4,         // issues O += P V
+  kRoleRab = 5,        // rab loads
+  kRoleWarps = 6
+};
 constexpr uint32_t kTmemCols = 512;
 // A rab / custom-mask tile (128 rows x 128 keys, 16-bit) arrives as boxes of 32 rows x 64
 // keys; boxes whose keys every one of their rows has masked are not loaded (rab only).
@@ -129,7 +130,21 @@ struct Cfg {
   // workload's short items make the staging's proxy fence and store issue a larger share
   // of every item (measured 1.7 % faster at D = 64 with rab).
   static constexpr bool STAGE = !RAB && D <= 128;
-  static constexpr int OC = DV / kEpiWG;             // O columns per epilogue warpgroup
+  // Epilogue warpgroups. Four for D <= 128: a thread then takes one 32-column chunk of each
+  // tile, and more warps hide more of the chain's latency (two warpgroups measured 10-28 %
+  // slower there). Two for D >= 256, whose two epilogue groups are then one warpgroup each
+  // with four chunks a thread: 1.8 % faster at D = 256 and 0.7 % at D = 512, and a 448-thread
+  // CTA leaves up to 144 registers a thread.
+  static constexpr int EPI_WG = D >= 256 ? 2 : 4;
+  static constexpr int EPI_WARPS = 4 * EPI_WG;
+  static constexpr int THREADS = (EPI_WARPS + kRoleWarps) * 32;
+  static constexpr int PRODUCER_WARP = EPI_WARPS + kRoleProducerK;
+  static constexpr int MMA_WARP = EPI_WARPS + kRoleMma;
+  static constexpr int V_PRODUCER_WARP = EPI_WARPS + kRoleProducerV;
+  static constexpr int Q_PRODUCER_WARP = EPI_WARPS + kRoleProducerQ;
+  static constexpr int PV_WARP = EPI_WARPS + kRolePv;
+  static constexpr int RAB_WARP = EPI_WARPS + kRoleRab;
+  static constexpr int OC = DV / EPI_WG;             // O columns per epilogue warpgroup
   static constexpr int OSWB = OC * 2;                // O staging row bytes (swizzle span)
   static constexpr int WARP_STAGE = 32 * OC * 2;     // one warp's O block in shared memory
   // Epilogue groups. With two, the epilogue warps form two groups of two warpgroups and
@@ -137,8 +152,8 @@ struct Cfg {
   // computes while the other waits for its next tile; that pays for D >= 256, whose longer
   // products leave the epilogue waiting. With one, all four warpgroups work on every tile.
   static constexpr int EPI_GROUPS = D >= 256 ? 2 : 1;
-  static constexpr int GROUP_WARPS = kEpiWarps / EPI_GROUPS;
-  static constexpr int COLS_PER_WG = kTileN / (kEpiWG / EPI_GROUPS);  // S columns per tile
+  static constexpr int GROUP_WARPS = EPI_WARPS / EPI_GROUPS;
+  static constexpr int COLS_PER_WG = kTileN / (EPI_WG / EPI_GROUPS);  // S columns per tile
   // TMEM (512 columns). For D <= 128, P has two buffers of its own and S two buffers; an
   // S buffer is released as soon as the epilogue has loaded it, so the next score products
   // overlap the epilogue. O has two accumulators where they fit beside them (D <= 64), one
@@ -189,8 +204,8 @@ struct Item {
 
 constexpr int kInfoDepth = 8;                   // decoded items kept in shared memory
 // item readers: epilogue warps, the MMA issuer(s), K and V producers, the rab producer
-template <bool SERIAL, int RAB>
-constexpr int info_readers() { return kEpiWarps + (SERIAL ? 3 : 4) + (RAB ? 1 : 0); }
+template <bool SERIAL, int RAB, int EPI_WARPS>
+constexpr int info_readers() { return EPI_WARPS + (SERIAL ? 3 : 4) + (RAB ? 1 : 0); }
 
 // Barrier block layout.
 struct Bars {
@@ -942,13 +957,13 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   using C = Cfg<D, RAB, F8>;
   constexpr bool OUT_BF16 = BF16 || F8;  // O type (FP8 inputs give bf16 out)
   using T16 = typename std::conditional<OUT_BF16, __nv_bfloat16, __half>::type;
-  constexpr int OC = C::DV / kEpiWG;         // O columns per warpgroup
+  constexpr int OC = C::OC;                  // O columns per warpgroup
   constexpr int OCH = OC < 32 ? OC : 32;     // O columns per TMEM load
   const int wg = warp >> 2;
   const int quarter = warp & 3;              // TMEM lane quarter
   const int r = quarter * 32 + lane;         // query row within the tile
   const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-  constexpr int WG_PER_GROUP = kEpiWG / C::EPI_GROUPS;
+  constexpr int WG_PER_GROUP = C::EPI_WG / C::EPI_GROUPS;
   const int group = wg / WG_PER_GROUP;  // takes the S tiles t with t % EPI_GROUPS == group
   const int col = (wg % WG_PER_GROUP) * C::COLS_PER_WG;  // first S column of this warpgroup
   const float half_alpha = 0.5f * p.alpha;
@@ -960,7 +975,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
   // item's first tile has been written, so that the epilogue is not idle while the item's
   // last accumulation completes. The item stays in its ring slot until this returns.
   auto drain = [&](int slot) -> bool {
-    if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+    if (lane == 0 && (warp == 0 || warp == C::EPI_WARPS - 1))
       HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kDrainBeg, slot);
     const Item& pit = bars->info[slot];
     const int pi = pit.m0 + r;  // query row within the sequence
@@ -1033,7 +1048,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->info_empty[slot]));
-    if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+    if (lane == 0 && (warp == 0 || warp == C::EPI_WARPS - 1))
       HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kDrainEnd, slot);
     return true;
   };
@@ -1044,7 +1059,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
     if (!warp_wait(bars, &bars->info_full[slot], (k / kInfoDepth) & 1, p)) return;
     const Item it = bars->info[slot];
     if (it.n_kv < 0) break;  // end marker
-    if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+    if (lane == 0 && (warp == 0 || warp == C::EPI_WARPS - 1))
       HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kItem, k);
     const int m0p = (KV ? it.off : 0) + it.m0;  // key position of the item's first query row
     const int i = m0p + r;                      // and of this thread's row
@@ -1070,7 +1085,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       if ((int)(t % C::EPI_GROUPS) != group) continue;  // the other group's tile
       const uint32_t sb = t % C::NSB;  // S buffer (== group with two epilogue groups)
       if (!warp_wait(bars, &bars->s_full[sb], (t / C::NSB) & 1, p)) return;
-      if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+      if (lane == 0 && (warp == 0 || warp == C::EPI_WARPS - 1))
         HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kSReady, t);
       ptx::tc_fence_after();
       KeyTile kt;
@@ -1230,7 +1245,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
       ptx::tmem_st_wait();
       ptx::tc_fence_before();
       warp_arrive(&bars->p_full[t % C::NPB], lane);
-      if (lane == 0 && (warp == 0 || warp == kEpiWarps - 1))
+      if (lane == 0 && (warp == 0 || warp == C::EPI_WARPS - 1))
         HSTU_TRACE_EV(p, warp == 0 ? trace::kRoleEpi : trace::kRoleEpiB, trace::kPDone, t);
       // this group's part of the previous item's O, after the group's first tile of this
       // item (P of a whole tile behind the item's last accumulation, which has finished
@@ -1252,7 +1267,7 @@ __device__ void epilogue(const FwdParams& p, Bars* bars, uint8_t* smem, uint32_t
 // ------------------------------------------------------------------ kernel
 // MASK: the rab stream carries a custom mask (multiplied into P after the SiLU).
 template <int D, bool BF16, int RAB, bool MASK = false, bool KV = false, int F8 = 0>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D, RAB, F8>::THREADS, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                   const __grid_constant__ CUtensorMap tm_o,
@@ -1271,7 +1286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + C::OFF_BAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  if (warp == kProducerWarp && lane == 0) {
+  if (warp == C::PRODUCER_WARP && lane == 0) {
 #define HSTU_INIT_ALL(arr, count)                                       \
   for (int s = 0; s < (int)(sizeof(bars->arr) / sizeof(uint64_t)); ++s) \
     ptx::mbar_init(ptx::smem_u32(&bars->arr[s]), (count));
@@ -1291,13 +1306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     HSTU_INIT_ALL(v_full, 1)
     HSTU_INIT_ALL(v_empty, 1)
     HSTU_INIT_ALL(o_full, 1)
-    HSTU_INIT_ALL(o_empty, kEpiWarps * 32)
+    HSTU_INIT_ALL(o_empty, C::EPI_WARPS * 32)
 #undef HSTU_INIT_ALL
     HSTU_TRACE_INIT();
     ptx::mbar_init(ptx::smem_u32(&bars->drain), C::SERIAL ? 1 : 2);  // one commit per issuer
     for (int s = 0; s < kInfoDepth; ++s) {
       ptx::mbar_init(ptx::smem_u32(&bars->info_full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), info_readers<C::SERIAL, RAB>());
+      ptx::mbar_init(ptx::smem_u32(&bars->info_empty[s]), info_readers<C::SERIAL, RAB, C::EPI_WARPS>());
     }
     bars->abort = 0;
     ptx::fence_barrier_init();
@@ -1310,7 +1325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (C::STAGE) ptx::prefetch_tmap(&tm_o);
     if (KV && p.page_offsets) ptx::prefetch_tmap(&tm_c);
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::MMA_WARP) {
     ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -1348,26 +1363,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const long long total = (long long)(*p.work_count) * p.Nq * (C::WIDE ? 2 : 1);
   if (threadIdx.x == 0) HSTU_TRACE_EV(p, trace::kRoleCta, trace::kDepDone, 0);
 
-  if (warp < kEpiWarps) {
+  if (warp < C::EPI_WARPS) {
     epilogue<D, BF16, RAB, MASK, KV, F8>(p, bars, smem, tmem, &tm_o, total, warp, lane);
-  } else if (warp == kProducerWarp) {
+  } else if (warp == C::PRODUCER_WARP) {
     if (lane == 0) producer_k<D, RAB, KV, F8>(p, bars, smem, &tm_k, &tm_c, total);
-  } else if (warp == kQProducerWarp) {
+  } else if (warp == C::Q_PRODUCER_WARP) {
     if (lane == 0) producer_q<D, RAB, KV, F8>(p, bars, smem, &tm_q, total);
-  } else if (warp == kVProducerWarp) {
+  } else if (warp == C::V_PRODUCER_WARP) {
     if (lane == 0) producer_v<D, RAB, KV, F8>(p, bars, smem, &tm_v, &tm_c, total);
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::MMA_WARP) {
     if (lane == 0) {
       if constexpr (C::SERIAL)
         mma_serial_issuer<D, BF16, RAB, F8>(p, bars, smem, tmem, total);
       else
         mma_s_issuer<D, BF16, RAB, F8>(p, bars, smem, tmem, total);
     }
-  } else if (warp == kRabWarp) {
+  } else if (warp == C::RAB_WARP) {
     if constexpr (RAB) {
       if (lane == 0) producer_r<D, RAB, MASK, KV, F8>(p, bars, smem, &tm_r, &tm_m, total);
     }
-  } else if (warp == kPvWarp) {
+  } else if (warp == C::PV_WARP) {
     if (lane == 0 && !C::SERIAL) mma_pv_issuer<D, BF16, RAB, F8>(p, bars, smem, tmem, total);
   }
   __syncwarp();
@@ -1385,7 +1400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   ptx::tc_fence_after();
-  if (warp == kMmaWarp) {
+  if (warp == C::MMA_WARP) {
     __syncwarp();
     ptx::tmem_dealloc(tmem, kTmemCols);
   }

@@ -18,7 +18,7 @@ cudaError_t launch_one(const FwdParams& p, const TcMaps& m, int grid, cudaStream
                        bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Cfg<D, RAB, F8>::THREADS);
   cfg.dynamicSmemBytes = Cfg<D, RAB, F8>::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -29,7 +29,7 @@ constexpr size_t kBufferWords = kSlots * kSlotWords;
 enum Role : int {
   kRoleCta = 0,   // thread 0: start / end (global timer)
   kRoleEpi = 1,   // epilogue warp 0, lane 0
-  kRoleEpiB = 2,  // epilogue warp 15, lane 0 (the last warpgroup)
+  kRoleEpiB = 2,  // the last epilogue warp, lane 0 (the last warpgroup)
   kRoleS = 3,     // score-product issuer
   kRolePV = 4,    // O += P V issuer
   kRoleQ = 5,     // Q producer / item claimer
