@@ -107,51 +107,61 @@ __global__ void __launch_bounds__(kThreads) build_worklist_kernel(FwdParams p, u
   // sequences exceed L2. With a causal mask each tile is binned by its own count.
   const bool group = p.seq_offsets_k != nullptr || p.page_offsets != nullptr ||
                      p.mask_type == kMaskNone;
-  // pass 1: histogram of key-visit counts
-  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const SeqKV kv = seq_kv(p, b);
-    const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
-    const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
-    const SeqGeom s = make_geom((int)kv.Lk, nc, nt, p.g, p.mask_type);
-    const int mtiles = ceil_div((int)kv.Lq, tile_m);
-    if (group) {
-      int most = 0;
-      for (int mt = 0; mt < mtiles; ++mt) most = max(most, visits(kv, s, mt));
-      if (mtiles > 0) atomicAdd(&hist[most], mtiles);
-    } else {
-      for (int mt = 0; mt < mtiles; ++mt) atomicAdd(&hist[visits(kv, s, mt)], 1);
-    }
-  }
-  __syncthreads();
-  // exclusive scan, largest key-tile count first
-  if (threadIdx.x == 0) {
-    int run = 0;
-    for (int n = nbins - 1; n >= 0; --n) {
-      cursor[n] = run;
-      run += hist[n];
-    }
-    *work_count = run;
-  }
-  __syncthreads();
-  // pass 2: scatter
-  for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-    const SeqKV kv = seq_kv(p, b);
-    const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
-    const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
-    const SeqGeom s = make_geom((int)kv.Lk, nc, nt, p.g, p.mask_type);
-    const int mtiles = ceil_div((int)kv.Lq, tile_m);
-    if (group) {
-      int most = 0;
-      for (int mt = 0; mt < mtiles; ++mt) most = max(most, visits(kv, s, mt));
-      if (mtiles > 0) {
-        const int pos = atomicAdd(&cursor[most], mtiles);
-        for (int mt = 0; mt < mtiles; ++mt) work[pos + mt] = pack_item(b, mt);
+  // Per-tile bins: the tiles of a sequence are spread over `share` threads (tiles
+  // mt = j, j + share, ...), so that a batch of few sequences keeps every warp busy.
+  // Per-sequence bins: one thread per sequence.
+  const int share = (!group && p.B < (int)blockDim.x) ? (int)blockDim.x / p.B : 1;
+  // pass 1: histogram of key-visit counts; pass 2: scatter
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int w = threadIdx.x; w < p.B * share; w += blockDim.x) {
+      const int b = w % p.B, j = w / p.B;
+      const SeqKV kv = seq_kv(p, b);
+      const long long nc = p.num_context ? load_index(p.num_context, b, p.index64) : 0;
+      const long long nt = p.num_targets ? load_index(p.num_targets, b, p.index64) : 0;
+      const SeqGeom s = make_geom((int)kv.Lk, nc, nt, p.g, p.mask_type);
+      const int mtiles = ceil_div((int)kv.Lq, tile_m);
+      if (group) {
+        int most = 0;
+        for (int mt = 0; mt < mtiles; ++mt) most = max(most, visits(kv, s, mt));
+        if (mtiles == 0) continue;
+        if (pass == 0) {
+          atomicAdd(&hist[most], mtiles);
+        } else {
+          const int pos = atomicAdd(&cursor[most], mtiles);
+          for (int mt = 0; mt < mtiles; ++mt) work[pos + mt] = pack_item(b, mt);
+        }
+      } else {
+        for (int mt = j; mt < mtiles; mt += share) {
+          const int n = visits(kv, s, mt);
+          if (pass == 0)
+            atomicAdd(&hist[n], 1);
+          else
+            work[atomicAdd(&cursor[n], 1)] = pack_item(b, mt);
+        }
       }
-    } else {
-      for (int mt = 0; mt < mtiles; ++mt) {
-        const int pos = atomicAdd(&cursor[visits(kv, s, mt)], 1);
-        work[pos] = pack_item(b, mt);
+    }
+    __syncthreads();
+    if (pass == 0) {
+      // exclusive scan, largest key-tile count first (cursor[n] = hist[n + 1] + ... +
+      // hist[nbins - 1]): warp 0, 32 bins at a time with shuffles
+      if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry = 0;
+        for (int base = 0; base < nbins; base += 32) {
+          const int r = base + lane;  // the r-th bin from the top
+          const int v = r < nbins ? hist[nbins - 1 - r] : 0;
+          int x = v;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, d);
+            if (lane >= d) x += y;
+          }
+          if (r < nbins) cursor[nbins - 1 - r] = carry + x - v;
+          carry += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) *work_count = carry;
       }
+      __syncthreads();
     }
   }
   // complete only after the kernel before this one in the stream
