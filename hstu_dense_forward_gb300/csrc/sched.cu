@@ -13,7 +13,10 @@
 // of the plan's two work lists, has completed). It reads only the call's inputs and writes
 // this call's work list, then waits for the previous kernel before it completes: the forward
 // kernel behind it, which waits for the builder, therefore starts its work only after the
-// previous call has finished.
+// previous call has finished. The index arrays are read before that wait, so the kernel
+// before the builder must not write them after triggering its dependents early (the stream
+// order note of hstu_fwd_run in the public header); a kernel that does not trigger early has
+// completed before the builder starts.
 //
 // The builder also checks the caller's seq_offsets ("increasing from 0; the user
 // must ensure validity", Inputs and Outputs table), and the key side (seq_offsets_k,
